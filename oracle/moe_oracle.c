@@ -1,0 +1,294 @@
+/*
+ * moe_oracle.c -- TEST INFRASTRUCTURE, not product code.
+ *
+ * A plain, slow, obviously correct CPU statement of the forward pass of one top-k routed
+ * mixture-of-experts FFN layer, in double precision. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it; the CUDA library never links, calls or includes it,
+ * and it shares no code, header or table with the CUDA library.
+ *
+ * Sources (web pages on mixture of experts), cited by page and section:
+ *   [CURIO]   llm.curionode.com "Mixture of Experts." (Plate 4), opening text and "Workshop":
+ *             the layer replaces the MLP with E MLPs plus a router, a linear layer and a softmax;
+ *             the top K experts run and their outputs are added, weighted by the normalised scores.
+ *   [LENSA-1] lensaml.com "Mixture of Experts", Step 1 of 6 "Bigger Model, Same Compute".
+ *   [LENSA-2] same page, Step 2 of 6 "The Router": logits = h . W_r, then a softmax over experts.
+ *   [LENSA-3] same page, Step 3 of 6 "Top-k Routing": the gates are a softmax over the chosen
+ *             logits (Mixtral: y = sum softmax(TopK(h . W_g))_i E_i(h)); Switch top-1 scales the
+ *             output by the raw router probability p_i instead; y = sum g . E(h).
+ *   [LENSA-4] same page, Step 4 of 6 "Load Balancing": the auxiliary term N . sum_i f_i P_i,
+ *             f_i the fraction of tokens sent to expert i, P_i its mean router probability;
+ *             it equals 1 under uniform routing.
+ *   [LENSA-5] same page, Step 5 of 6 "Capacity & Dropped Tokens" (dropless grouping, MegaBlocks).
+ *   [LENSA-6] same page, Step 6 of 6 "MoE in Practice" (Mixtral expert = 3 x 4096 x 14336).
+ *   [JAGGI]   arjunjaggi.com "Mixture of Experts in LLMs: How Sparse Models Scale", sections
+ *             "The Router" (Switch k = 1) and "Switch Transformers" (router kept in float32).
+ *
+ * Readings where the pages leave a step open (each is also listed with the design notes):
+ *   - f_i = count_i / (T k), so that sum_i f_i = 1 and the auxiliary term is exactly 1 under
+ *     uniform routing for any k; P_i is the mean of the FULL softmax (before top-k).
+ *   - The auxiliary value returned is E . sum f P; the weight alpha is the caller's.
+ *   - Top-k order: logits descending, equal logits broken toward the lower expert index.
+ *   - Renormalised gates are the softmax over the chosen logits (equal to p_j / sum_S p).
+ *   - Activation "GELU" is the tanh form 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))).
+ *   - SwiGLU expert: W2 (SiLU(W1 x) * (W3 x)), no biases; SiLU(x) = x / (1 + e^-x).
+ *   - Grouping order: a stable counting sort of the flattened slots s = t k + j by expert,
+ *     i.e. (expert ascending, token ascending); nothing is dropped.
+ *
+ * Precision: inputs are read exactly as stored (f32, or bf16 widened bit-exactly) and every sum,
+ * product and transcendental is taken in double, in index order, with no intermediate rounding.
+ *
+ * Every function below is pinned by tests/test_oracle_pins.py against the pages' printed values,
+ * closed forms, brute force or an independent library computation.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_F32 0
+#define OR_BF16 1
+#define OR_GELU_TANH 0
+#define OR_SWIGLU 1
+#define OR_RENORM 0
+#define OR_RAW_PROB 1
+
+/* Read element i of a tensor stored as f32 or as raw bf16 bits, widened exactly to double. */
+static double widen(const void *p, int dtype, int64_t i)
+{
+    if (dtype == OR_F32) return (double)((const float *)p)[i];
+    uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float v;
+    memcpy(&v, &bits, sizeof v);
+    return (double)v;
+}
+
+/* [LENSA-2], [CURIO], [JAGGI]: logits z[t,e] = sum_i h[t,i] W_r[i,e] (+ b_r[e]); p = softmax_e(z),
+ * evaluated with the maximum subtracted (an identity of the softmax). W_r is [d, E] row-major. */
+void oracle_router(int64_t T, int32_t d, int32_t E, const void *h, int32_t h_dtype,
+                   const float *W_r, const float *b_r, double *z, double *p)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double zmax = -INFINITY;
+        for (int32_t e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                acc += widen(h, h_dtype, t * d + i) * (double)W_r[(int64_t)i * E + e];
+            if (b_r) acc += (double)b_r[e];
+            z[t * E + e] = acc;
+            if (acc > zmax) zmax = acc;
+        }
+        double s = 0.0;
+        for (int32_t e = 0; e < E; ++e) s += exp(z[t * E + e] - zmax);
+        for (int32_t e = 0; e < E; ++e) p[t * E + e] = exp(z[t * E + e] - zmax) / s;
+    }
+}
+
+/* [LENSA-3], [CURIO] "Top-K routing": the k experts with the largest logits, listed in descending
+ * order, equal logits toward the lower index. Also records, per token, the gap between the k-th
+ * and (k+1)-th logit (boundary; +inf when k == E) and the smallest gap between consecutive chosen
+ * logits (inset; +inf when k == 1): where those are tiny, another precision may choose otherwise. */
+void oracle_topk(int64_t T, int32_t E, int32_t k, const double *z, int32_t *idx,
+                 double *boundary_margin, double *inset_margin)
+{
+#pragma omp parallel
+    {
+        unsigned char *chosen = (unsigned char *)malloc((size_t)E);
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            const double *zt = z + t * E;
+            memset(chosen, 0, (size_t)E);
+            double inset = INFINITY, prev = 0.0;
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t best = -1;
+                for (int32_t e = 0; e < E; ++e)
+                    if (!chosen[e] && (best < 0 || zt[e] > zt[best])) best = e;
+                chosen[best] = 1;
+                idx[t * k + j] = best;
+                if (j > 0 && prev - zt[best] < inset) inset = prev - zt[best];
+                prev = zt[best];
+            }
+            double boundary = INFINITY;
+            if (k < E) {
+                int32_t nxt = -1;
+                for (int32_t e = 0; e < E; ++e)
+                    if (!chosen[e] && (nxt < 0 || zt[e] > zt[nxt])) nxt = e;
+                boundary = prev - zt[nxt];
+            }
+            if (boundary_margin) boundary_margin[t] = boundary;
+            if (inset_margin) inset_margin[t] = inset;
+        }
+        free(chosen);
+    }
+}
+
+/* [LENSA-3]: gate weights of the chosen experts.
+ *   mode RENORM   : g_j = softmax over the chosen logits = exp(z_j - z_1) / sum_{i in S} exp(z_i - z_1)
+ *                   (the Mixtral form softmax(TopK(h . W_g)); it sums to 1 over the chosen set)
+ *   mode RAW_PROB : g_j = p_j, the full-softmax probability (the Switch top-1 form) */
+void oracle_gates(int64_t T, int32_t E, int32_t k, int32_t mode, const double *z, const double *p,
+                  const int32_t *idx, double *g)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        const int32_t *it = idx + t * k;
+        if (mode == OR_RAW_PROB) {
+            for (int32_t j = 0; j < k; ++j) g[t * k + j] = p[t * E + it[j]];
+        } else {
+            double zmax = z[t * E + it[0]];
+            double s = 0.0;
+            for (int32_t j = 0; j < k; ++j) s += exp(z[t * E + it[j]] - zmax);
+            for (int32_t j = 0; j < k; ++j) g[t * k + j] = exp(z[t * E + it[j]] - zmax) / s;
+        }
+    }
+}
+
+/* [LENSA-4] histogram of routing slots per expert, [LENSA-5] dropless grouping: a stable counting
+ * sort of the flattened slots s = t*k + j by expert idx[s].
+ *   counts[e]        slots routed to e
+ *   offsets[0..E]    exclusive prefix sum of counts (offsets[E] = T k)
+ *   sorted_token[r]  token of the r-th slot in (expert, token) order
+ *   slot_of[s]       sorted position of slot s (the inverse map) */
+void oracle_dispatch(int64_t T, int32_t E, int32_t k, const int32_t *idx, int32_t *counts,
+                     int32_t *offsets, int32_t *sorted_token, int32_t *slot_of)
+{
+    const int64_t P = T * k;
+    int64_t *cursor = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E > 0 ? E : 1));
+    for (int32_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t s = 0; s < P; ++s) counts[idx[s]] += 1;
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    for (int32_t e = 0; e < E; ++e) cursor[e] = offsets[e];
+    for (int64_t s = 0; s < P; ++s) {
+        int64_t pos = cursor[idx[s]]++;
+        sorted_token[pos] = (int32_t)(s / k);
+        slot_of[s] = (int32_t)pos;
+    }
+    free(cursor);
+}
+
+/* GELU in its tanh form and SiLU, in double. */
+static double gelu_tanh(double x)
+{
+    const double c = sqrt(2.0 / M_PI);
+    return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+static double silu(double x) { return x / (1.0 + exp(-x)); }
+
+double oracle_gelu_tanh(double x) { return gelu_tanh(x); }
+double oracle_silu(double x) { return silu(x); }
+
+/* [CURIO] "Workshop" (experts are MLPs of width f), [LENSA-1]/[LENSA-6] (a full expert is three
+ * d x f matrices): expert e applied to one input row x of length d.
+ *   GELU form   : y = W2_e GELU(W1_e x + b1_e) + b2_e
+ *   SwiGLU form : y = W2_e (SiLU(W1_e x) * (W3_e x))
+ * W1, W3 are [E, f, d] and W2 is [E, d, f], row-major (output index, then input index). */
+static void expert_mlp(int32_t d, int32_t f, int32_t act, const double *x, int32_t e,
+                       const void *W1, const void *W3, const void *W2, int32_t w_dtype,
+                       const float *b1, const float *b2, double *hid, double *y)
+{
+    const int64_t base1 = (int64_t)e * f * d;
+    const int64_t base2 = (int64_t)e * d * f;
+    for (int32_t j = 0; j < f; ++j) {
+        double a = 0.0;
+        for (int32_t i = 0; i < d; ++i) a += widen(W1, w_dtype, base1 + (int64_t)j * d + i) * x[i];
+        if (act == OR_SWIGLU) {
+            double c = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                c += widen(W3, w_dtype, base1 + (int64_t)j * d + i) * x[i];
+            hid[j] = silu(a) * c;
+        } else {
+            if (b1) a += (double)b1[(int64_t)e * f + j];
+            hid[j] = gelu_tanh(a);
+        }
+    }
+    for (int32_t o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int32_t j = 0; j < f; ++j) acc += widen(W2, w_dtype, base2 + (int64_t)o * f + j) * hid[j];
+        if (act != OR_SWIGLU && b2) acc += (double)b2[(int64_t)e * d + o];
+        y[o] = acc;
+    }
+}
+
+/* Expert MLPs on n independent rows: y[r] = FFN_{expert[r]}(x[r]); x and y are [n, d] double. */
+void oracle_expert_ffn(int64_t n, int32_t d, int32_t f, int32_t act, const double *x,
+                       const int32_t *expert, const void *W1, const void *W3, const void *W2,
+                       int32_t w_dtype, const float *b1, const float *b2, double *y)
+{
+#pragma omp parallel
+    {
+        double *hid = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n; ++r)
+            expert_mlp(d, f, act, x + r * d, expert[r], W1, W3, W2, w_dtype, b1, b2, hid, y + r * d);
+        free(hid);
+    }
+}
+
+/* [LENSA-3] "y = sum g . E(h)", [CURIO]: the chosen experts' outputs added, weighted by the gates,
+ * in slot order j = 0..k-1. yslot is [n, k, d] (expert output of slot j of token t), g is [n, k]. */
+void oracle_combine(int64_t n, int32_t k, int32_t d, const double *g, const double *yslot,
+                    double *y)
+{
+    for (int64_t t = 0; t < n; ++t)
+        for (int32_t o = 0; o < d; ++o) {
+            double acc = 0.0;
+            for (int32_t j = 0; j < k; ++j) acc += g[t * k + j] * yslot[(t * k + j) * d + o];
+            y[t * d + o] = acc;
+        }
+}
+
+/* The layer output of the listed tokens: y[r] = sum_j g[t,j] FFN_{idx[t,j]}(h[t]) with t = tokens[r].
+ * Each output row depends only on its own token, so any subset of tokens can be evaluated. */
+void oracle_forward_rows(int64_t n, const int64_t *tokens, int32_t d, int32_t f, int32_t k,
+                         int32_t act, const void *h, int32_t h_dtype, const int32_t *idx,
+                         const double *g, const void *W1, const void *W3, const void *W2,
+                         int32_t w_dtype, const float *b1, const float *b2, double *y)
+{
+    const int64_t nk = n * k;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(nk * d + 1));
+    double *ys = (double *)malloc(sizeof(double) * (size_t)(nk * d + 1));
+    double *gs = (double *)malloc(sizeof(double) * (size_t)(nk + 1));
+    int32_t *ex = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nk + 1));
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = tokens[r];
+        for (int32_t j = 0; j < k; ++j) {
+            for (int32_t i = 0; i < d; ++i) x[(r * k + j) * d + i] = widen(h, h_dtype, t * d + i);
+            ex[r * k + j] = idx[t * k + j];
+            gs[r * k + j] = g[t * k + j];
+        }
+    }
+    oracle_expert_ffn(nk, d, f, act, x, ex, W1, W3, W2, w_dtype, b1, b2, ys);
+    oracle_combine(n, k, d, gs, ys, y);
+    free(x); free(ys); free(gs); free(ex);
+}
+
+/* [LENSA-4]: E . sum_e f_e P_e with f_e = counts[e] / (T k) and P_e = (1/T) sum_t p[t,e]
+ * (the full softmax). The weight alpha is not applied. */
+double oracle_aux_loss(int64_t T, int32_t E, int32_t k, const int32_t *counts, const double *p)
+{
+    double acc = 0.0;
+    for (int32_t e = 0; e < E; ++e) {
+        double Pe = 0.0;
+        for (int64_t t = 0; t < T; ++t) Pe += p[t * E + e];
+        Pe /= (double)T;
+        const double fe = (double)counts[e] / ((double)T * (double)k);
+        acc += fe * Pe;
+    }
+    return (double)E * acc;
+}
+
+/* [CURIO] "Parameters you hold, parameters you use", [LENSA-1], [LENSA-6]: total and active
+ * parameter counts of a model whose FFN blocks are replaced by E experts of mats x d x f weights
+ * each, k of them active per token. Everything else (attention, norms, embeddings) is shared:
+ * shared_per_layer is counted once per layer, shared_global once per model. The router (d x E per
+ * layer) is counted as shared when with_router is set. */
+void oracle_param_count(int32_t n_layers, int64_t d, int64_t f, int32_t E, int32_t k,
+                        int32_t mats, int64_t shared_per_layer, int64_t shared_global,
+                        int32_t with_router, int64_t *total, int64_t *active)
+{
+    const int64_t expert = (int64_t)mats * d * f;
+    const int64_t router = with_router ? d * E : 0;
+    *total = (int64_t)n_layers * (shared_per_layer + router + (int64_t)E * expert) + shared_global;
+    *active = (int64_t)n_layers * (shared_per_layer + router + (int64_t)k * expert) + shared_global;
+}

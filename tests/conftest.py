@@ -1,0 +1,31 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
+
+
+def read_golden(name: str) -> dict:
+    """Parse a tests/golden fixture: `key = v1 v2 ...` lines, `#` comments."""
+    out = {}
+    with open(os.path.join(ROOT, "tests", "golden", name)) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, val = (s.strip() for s in line.split("=", 1))
+            vals = [float(v) for v in val.split()]
+            out[key] = vals if len(vals) > 1 else vals[0]
+    return out
+
+
+@pytest.fixture(scope="session")
+def golden():
+    return read_golden
