@@ -1,0 +1,346 @@
+"""Benchmark of the MoE layer forward on B300: tokens/s and the grouped expert GEMM's roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral] [--impl ours|reference]
+
+One step = one pass of the whole layer (router + top-k, dispatch + permute, grouped expert FFN,
+combine, auxiliary value) over one batch of the workload's seeded synthetic inputs, with weights
+and inputs resident in HBM. Each rank (one process per GPU, launched by torchrun for N > 1) runs
+an independent replica of the layer on its own batch: there is no exchange on this path, so the
+scaling is weak and `value` is the tokens of all ranks over the slowest rank's time.
+
+The JSON line also carries:
+  e2e          the same metric through moe_forward with host buffers: pinned h copied in and y
+               (plus aux) copied out inside the timed region, every step;
+  roofline     the dominant kernel (grouped_gemm_tc_kernel, launched twice per step: GEMM1 and
+               GEMM2) against the measured bf16 tensor peak: algorithmic flops of the two launches
+               over their summed CUDA-event duration on the launching stream;
+  cpu_baseline the double-precision oracle on this machine's host cores, on a bounded token
+               sample of the same workload (rank 0, N = 1 only);
+  clocks       nvidia-smi samples taken during the timed region.
+--impl reference times the oracle itself (the method's plain statement) as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mixture_experts_70_b300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE layer tokens/s at 1 B300; % of bf16 TC peak (GEMM) or HBM BW (decode)"
+GEMM_KERNEL = "grouped_gemm_tc_kernel"
+
+
+def _peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return dict(bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
+                    hbm=p["hbm_gbs"], source="measured")
+    return dict(bf16=1800.0, bf16_sustained=1400.0, hbm=6400.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+            os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def _cpu_baseline(w, budget_s: float = 12.0) -> dict:
+    """The oracle (double, OpenMP over rows) on a bounded prefix of the workload's tokens."""
+    import oracle
+    threads = oracle.max_threads()
+    inputs = wl.generate(w)
+
+    def run(n):
+        sub = w.with_(T=n)
+        part = dict(inputs)
+        part["h"] = inputs["h"][:n].contiguous()
+        t0 = time.perf_counter()
+        oracle.reference(sub, part)
+        return time.perf_counter() - t0
+
+    n = 1
+    t = run(n)
+    while t < budget_s / 8 and n < w.T:
+        n = min(w.T, n * 4)
+        t = run(n)
+    if t < budget_s / 2 and n < w.T:
+        n = min(w.T, max(n + 1, int(n * (budget_s / 2) / max(t, 1e-3))))
+        t = run(n)
+    return {"value": n / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {w.T} tokens of the {w.name} workload, full layer "
+                      f"(router, top-k, gates, dispatch, expert MLPs, combine, aux) in double, "
+                      f"{t:.1f} s"}
+
+
+def run_reference(args, w) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cb = _cpu_baseline(w, budget_s=max(2.0, 60.0 / max(args.steps + args.warmup, 1)))
+    n_tok = int(cb["sample"].split()[1])
+    sub = w.with_(T=n_tok)
+    inputs = wl.generate(w)
+    part = dict(inputs)
+    part["h"] = inputs["h"][:n_tok].contiguous()
+    for _ in range(args.warmup):
+        oracle.reference(sub, part)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.reference(sub, part)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, N(0,1/fan_in))",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "k": w.k,
+                       "act": w.act, "gate": w.gate, "sample_tokens": n_tok},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mixtral", choices=list(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = wl.WORKLOADS[args.workload]
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    from sparse_mixture_experts_70_b300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    peaks = _peaks()
+    cfg = B.config_for(w)
+    inputs = wl.generate(w)
+    dev = {k: (v.cuda().contiguous() if v is not None else None) for k, v in inputs.items()}
+    ws = B.workspace(cfg)
+    T, k, E, d = w.T, w.k, w.E, w.d
+    rows = B.moe_router_partials(cfg)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    psum = torch.empty((rows, E), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sorted_token = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    slot_of = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((T * k, d), dtype=w.torch_dtype, device="cuda")
+    y_perm = torch.empty((T * k, d), dtype=w.torch_dtype, device="cuda")
+    y = torch.empty((T, d), dtype=w.torch_dtype, device="cuda")
+    aux = torch.empty(1, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    h = dev["h"]
+
+    def step(ev=None):
+        # the five step calls (the same kernels moe_forward launches), with events around them
+        if ev is not None:
+            ev[0].record(stream)
+        B.moe_router_topk(cfg, h, dev["W_r"], dev["b_r"], idx, gates, psum, stream)
+        B.moe_build_dispatch(cfg, idx, h, counts, offsets, sorted_token, slot_of, x_perm, ws,
+                             stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.moe_expert_ffn(cfg, x_perm, offsets, dev["W1"], dev["b1"], dev["W3"], dev["W2"],
+                         dev["b2"], y_perm, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        B.moe_combine(cfg, y_perm, slot_of, gates, y, stream)
+        B.moe_aux_loss(cfg, counts, psum, aux, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = B.moe_device_status(ws)
+    if st != B.MOE_OK:
+        raise SystemExit(f"device status after warm-up: {B.status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    clocks = clk.summary()
+    ms = start.elapsed_time(stop) / args.steps
+    ffn_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    route_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    comb_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    st = B.moe_device_status(ws)
+    if st != B.MOE_OK:
+        raise SystemExit(f"device status after timed region: {B.status_string(st)}")
+
+    # end to end through moe_forward with host buffers (pinned), copies inside the timed region
+    layer = B.Layer(cfg, dev)
+    h_host = inputs["h"].pin_memory()
+    y_host = torch.empty((T, d), dtype=w.torch_dtype).pin_memory()
+    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    h_dev = torch.empty_like(dev["h"])
+
+    def e2e_step():
+        h_dev.copy_(h_host, non_blocking=True)
+        layer.forward(h_dev, stream)
+        y_host.copy_(layer.y, non_blocking=True)
+        aux_host.copy_(layer.aux, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_stop = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e_start.elapsed_time(e_stop) / args.steps
+    if B.moe_device_status(layer.ws) != B.MOE_OK:
+        raise SystemExit("device status after e2e region")
+
+    if dist:
+        t = torch.tensor([ms, e_ms, ffn_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e_ms, ffn_ms = t.tolist()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    tokens = T * world
+    flops = w.expert_flops()
+    tflops = flops / (ffn_ms * 1e-3) / 1e12
+    peak = peaks["bf16_sustained"]
+    # router, dispatch, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine, aux
+    launches_per_step = 7
+    line = {
+        "metric": METRIC,
+        "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded; h ~ N(0,1), weights ~ N(0, 1/fan_in))",
+        "config": {"workload": w.name, "T": T, "d": d, "f": w.f, "E": E, "k": k,
+                   "act": w.act, "gate": w.gate, "per_rank_tokens": T,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({w.weight_bytes() / 1e9:.2f} GB of expert "
+                         "weights read every step)"},
+        "breakdown_ms": {"router_dispatch_permute": route_ms, "expert_ffn": ffn_ms,
+                         "combine_aux": comb_ms},
+        "roofline": {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops,
+                     "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "frac_of_burst": tflops / peaks["bf16"],
+                     "traffic": None},
+        "e2e": {"value": tokens / (e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
+                "d2h_bytes_per_step": T * d * y.element_size() + 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

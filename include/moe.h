@@ -1,0 +1,159 @@
+/*
+ * moe.h -- C ABI of libmoe: the forward pass of one top-k routed mixture-of-experts FFN layer on
+ * one NVIDIA B300 (sm_103a).
+ *
+ * The layer (llm.curionode.com "Mixture of Experts.", Plate 4, opening text; lensaml.com
+ * "Mixture of Experts", Steps 2-4) replaces one FFN with E expert MLPs and a router:
+ *   1. router      z = h . W_r (+ b_r), p = softmax_E(z), in f32
+ *   2. top-k       the k largest logits per token and their gates
+ *   3. dispatch    per-expert histogram, prefix sum, and a permutation grouping token copies by expert
+ *   4. expert FFN  every expert's MLP over its contiguous block of rows
+ *   5. combine     y[t] = sum_j g[t,j] . FFN_{idx[t,j]}(h[t]), plus the auxiliary value E . sum f P
+ *
+ * Conventions for every entry point
+ *   - Pointers to tensors are DEVICE pointers (cudaMalloc'd or PyTorch-owned), caller-owned.
+ *     The library allocates nothing and keeps no state between calls; all scratch lives in the
+ *     caller's workspace `ws` (see moe_workspace_size).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call is
+ *     asynchronous on that stream; results are valid once the stream reaches the call.
+ *   - All tensors are dense row-major. "dtype" below is cfg->dtype: MOE_F32 (float) or MOE_BF16
+ *     (bfloat16, raw 16-bit storage). Router weights, router bias, expert biases and gates are
+ *     always float. Integer tensors are int32.
+ *   - Device pointers must be 16-byte aligned.
+ *   - Errors: argument checks run on the host before anything is launched and return a status
+ *     without touching the device. A failed launch returns MOE_ERR_CUDA. Failures detected on the
+ *     device (a spin-wait that ran out of its time limit, an out-of-range expert index) never trap:
+ *     the kernel records a bit in a status word inside `ws` and returns; moe_device_status() reads
+ *     and clears it. There is no CPU fallback.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status_t;
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, k outside [1, E] */
+    MOE_ERR_UNSUPPORTED = 2,  /* a dtype / activation / gate / bias combination not built */
+    MOE_ERR_WORKSPACE = 3,    /* ws smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+    MOE_ERR_TIMEOUT = 5,      /* (device) a bounded spin-wait gave up; outputs are invalid */
+    MOE_ERR_DEVICE_INDEX = 6  /* (device) an expert index outside [0, E) was read */
+};
+
+enum { MOE_F32 = 0, MOE_BF16 = 1 };
+enum { MOE_ACT_GELU_TANH = 0, MOE_ACT_SWIGLU = 1 };
+enum { MOE_GATE_RENORM = 0, MOE_GATE_RAW_PROB = 1 };
+
+/* Layer shape and variant.
+ *   T tokens (>= 0); d model width; f expert hidden width; E experts; k experts per token.
+ *   Limits: 1 <= E <= 256, 1 <= k <= E, d and f multiples of 64 (>= 64), T * k < 2^31.
+ *   act  MOE_ACT_GELU_TANH : expert(x) = W2 GELU_tanh(W1 x + b1) + b2   (2 matrices)
+ *        MOE_ACT_SWIGLU    : expert(x) = W2 (SiLU(W1 x) * (W3 x))       (3 matrices, no biases)
+ *   gate MOE_GATE_RENORM   : g = softmax over the chosen logits (Mixtral form, sums to 1)
+ *        MOE_GATE_RAW_PROB : g = p, the full-softmax probability (Switch top-1 form)
+ *   has_bias : expert biases b1 [E, f] and b2 [E, d] (float) are present; GELU form only. */
+typedef struct {
+    int64_t T;
+    int32_t d, f, E, k;
+    int32_t dtype;
+    int32_t act;
+    int32_t gate;
+    int32_t has_bias;
+} moe_config_t;
+
+/* Bytes of workspace every call below needs for `cfg` (the largest of their needs, so one
+ * workspace serves them all). The workspace must be zero-filled once after allocation (or passed
+ * through moe_workspace_init); afterwards the library keeps its status word consistent itself.
+ * Returns MOE_ERR_INVALID_ARG for an invalid cfg. */
+moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
+
+/* Zero the workspace header (status word and dispatch flags) on `stream`. */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Number of floats of the router's per-block probability sums, psum_part [rows, E]. */
+moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows);
+
+/* Steps 1-2. Router, softmax and top-k (lensaml.com "Mixture of Experts", Step 2 "The Router"
+ * and Step 3 "Top-k Routing"; arjunjaggi.com "Mixture of Experts in LLMs", "Switch Transformers":
+ * the router is kept in f32).
+ *   h        [T, d] dtype           input activations
+ *   W_r      [d, E] float           router weight;  b_r [E] float or NULL
+ *   topk_idx [T, k] int32  (out)    chosen experts, logits descending, ties to the lower index
+ *   gates    [T, k] float  (out)    gate of each chosen expert (RENORM or RAW_PROB)
+ *   psum_part [moe_router_partials rows, E] float (out) per-block sums of p over tokens, in a
+ *            fixed order (input of moe_aux_loss).
+ * Logits are accumulated in f32 from the stored h; exp is CUDA's expf. */
+moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float *W_r,
+                             const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
+                             void *stream);
+
+/* Step 3. Dispatch (lensaml.com "Mixture of Experts", Step 4 "Load Balancing": the histogram of
+ * routing slots per expert; Step 5 "Capacity & Dropped Tokens": dropless grouping of any number
+ * of tokens per expert). A stable counting sort of the slots s = t*k + j by topk_idx[s]:
+ *   counts       [E]    int32 (out)  slots routed to each expert
+ *   offsets      [E+1]  int32 (out)  exclusive prefix sum of counts; offsets[E] = T k
+ *   sorted_token [T k]  int32 (out)  token of each sorted row, order (expert, token) ascending
+ *   slot_of      [T k]  int32 (out)  sorted row of slot s (the inverse permutation)
+ *   x_perm       [T k, d] dtype (out, may be NULL): x_perm[r] = h[sorted_token[r]]
+ *   h            [T, d] dtype, read only when x_perm is not NULL.
+ * One cooperative kernel (histogram without atomics, decoupled look-back scan over blocks) and,
+ * when x_perm is given, one gather kernel. Bit-exact and deterministic. */
+moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, const void *h,
+                                int32_t *counts, int32_t *offsets, int32_t *sorted_token,
+                                int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/* Step 4. Every expert's MLP over its block of rows of x_perm (llm.curionode.com "Mixture of
+ * Experts.", "Workshop": the experts are MLPs; lensaml.com "Mixture of Experts", Step 1 and
+ * Step 6: a full expert is three d x f matrices).
+ *   x_perm  [T k, d] dtype          rows grouped by expert, as moe_build_dispatch writes them
+ *   offsets [E+1] int32             expert e owns rows [offsets[e], offsets[e+1])
+ *   W1 [E, f, d], W3 [E, f, d] (SwiGLU only, else NULL), W2 [E, d, f]: dtype, out x in
+ *   b1 [E, f], b2 [E, d] float, only when cfg->has_bias (else NULL)
+ *   y_perm  [T k, d] dtype (out)    expert output of every row
+ * The hidden activations H [T k, f] (dtype) live in ws. bf16: tcgen05 tensor cores, f32
+ * accumulation, H rounded to bf16. f32: CUDA-core f32 FMA. */
+moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets,
+                            const void *W1, const float *b1, const void *W3, const void *W2,
+                            const float *b2, void *y_perm, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/* Step 5a. Gate-weighted combine (lensaml.com "Mixture of Experts", Step 3: y = sum g . E(h)):
+ *   y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :], in f32, j ascending, then
+ *   rounded to dtype.  y [T, d] dtype (out). */
+moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int32_t *slot_of,
+                         const float *gates, void *y, void *stream);
+
+/* Step 5b. Auxiliary load-balancing value (lensaml.com "Mixture of Experts", Step 4):
+ *   aux = E . sum_e f_e P_e,  f_e = counts[e] / (T k),  P_e = (1/T) sum_t p[t, e]
+ * (the weight alpha is the caller's). Reduced in a fixed order. aux_out: one float (device).
+ * T = 0 gives 0. */
+moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const float *psum_part,
+                          float *aux_out, void *stream);
+
+/* Steps 1-5 in one call. y [T, d] dtype (out); aux_out one float (out); topk_idx_out [T, k] and
+ * counts_out [E] are optional copies of the routing (NULL to skip). Everything else lives in ws. */
+moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
+                         const float *b_r, const void *W1, const float *b1, const void *W3,
+                         const void *W2, const float *b2, void *y, float *aux_out,
+                         int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/* Synchronise `stream`, read the device status word in ws, clear it, and return MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_INDEX (MOE_ERR_CUDA if the copy itself fails). */
+moe_status_t moe_device_status(void *ws, void *stream);
+
+/* A static string naming a status code. */
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,208 @@
+"""Thin Python binding of libmoe's C ABI (include/moe.h), one function per entry point, same names.
+
+Argument marshalling only: tensors are passed as device pointers (``data_ptr()``), the stream as
+the current torch stream, and a non-OK status raises ``MoEError``. Every step of the layer runs in
+libmoe's CUDA kernels; there is no CPU path. If libmoe.so is missing the import of the library
+fails loudly (build it with ``python -m sparse_mixture_experts_70_b300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INDEX = 4, 5, 6
+MOE_F32, MOE_BF16 = 0, 1
+MOE_ACT_GELU_TANH, MOE_ACT_SWIGLU = 0, 1
+MOE_GATE_RENORM, MOE_GATE_RAW_PROB = 0, 1
+
+
+class moe_config_t(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("f", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("act", ctypes.c_int32), ("gate", ctypes.c_int32), ("has_bias", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lib = None
+_P = ctypes.c_void_p
+_CFG = ctypes.POINTER(moe_config_t)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: run `python -m sparse_mixture_experts_70_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        st = ctypes.c_int32
+        sig = {
+            "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
+            "moe_workspace_init": [_P, ctypes.c_size_t, _P],
+            "moe_router_partials": [_CFG, ctypes.POINTER(ctypes.c_int64)],
+            "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P],
+            "moe_build_dispatch": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+            "moe_expert_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+            "moe_combine": [_CFG, _P, _P, _P, _P, _P],
+            "moe_aux_loss": [_CFG, _P, _P, _P, _P],
+            "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                            ctypes.c_size_t, _P],
+            "moe_device_status": [_P, _P],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = st
+        L.moe_status_string.argtypes = [ctypes.c_int32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions include/moe.h declares."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:moe_status_t|const char\s*\*)\s*(moe_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def config(T: int, d: int, f: int, E: int, k: int, dtype: int = MOE_BF16,
+           act: int = MOE_ACT_SWIGLU, gate: int = MOE_GATE_RENORM, has_bias: bool = False) -> moe_config_t:
+    return moe_config_t(T, d, f, E, k, dtype, act, gate, 1 if has_bias else 0)
+
+
+def config_for(w) -> moe_config_t:
+    """The moe_config_t of a workloads.Workload."""
+    return config(w.T, w.d, w.f, w.E, w.k, MOE_F32 if w.dtype == "f32" else MOE_BF16,
+                  MOE_ACT_SWIGLU if w.act == "swiglu" else MOE_ACT_GELU_TANH,
+                  MOE_GATE_RAW_PROB if w.gate == "raw_prob" else MOE_GATE_RENORM, w.has_bias)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoEError(status, where)
+
+
+def moe_workspace_size(cfg: moe_config_t) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(lib().moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_workspace_init")
+
+
+def moe_router_partials(cfg: moe_config_t) -> int:
+    n = ctypes.c_int64()
+    _check(lib().moe_router_partials(ctypes.byref(cfg), ctypes.byref(n)), "moe_router_partials")
+    return n.value
+
+
+def workspace(cfg: moe_config_t, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of moe_workspace_size(cfg) bytes (PyTorch-owned device memory)."""
+    return torch.zeros(max(moe_workspace_size(cfg), 1024), dtype=torch.uint8, device=device)
+
+
+def moe_router_topk(cfg, h, W_r, b_r, topk_idx, gates, psum_part, stream=None) -> None:
+    _check(lib().moe_router_topk(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(topk_idx),
+                                 _ptr(gates), _ptr(psum_part), _stream(stream)), "moe_router_topk")
+
+
+def moe_build_dispatch(cfg, topk_idx, h, counts, offsets, sorted_token, slot_of, x_perm, ws,
+                       stream=None) -> None:
+    _check(lib().moe_build_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(h), _ptr(counts),
+                                    _ptr(offsets), _ptr(sorted_token), _ptr(slot_of),
+                                    _ptr(x_perm), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream)), "moe_build_dispatch")
+
+
+def moe_expert_ffn(cfg, x_perm, offsets, W1, b1, W3, W2, b2, y_perm, ws, stream=None) -> None:
+    _check(lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(W1),
+                                _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y_perm), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(cfg, y_perm, slot_of, gates, y, stream=None) -> None:
+    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(y_perm), _ptr(slot_of), _ptr(gates), _ptr(y),
+                             _stream(stream)), "moe_combine")
+
+
+def moe_aux_loss(cfg, counts, psum_part, aux_out, stream=None) -> None:
+    _check(lib().moe_aux_loss(ctypes.byref(cfg), _ptr(counts), _ptr(psum_part), _ptr(aux_out),
+                              _stream(stream)), "moe_aux_loss")
+
+
+def moe_forward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out, counts_out, ws,
+                stream=None) -> None:
+    _check(lib().moe_forward(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(W1), _ptr(b1),
+                             _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y), _ptr(aux_out),
+                             _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+
+
+def moe_device_status(ws, stream=None) -> int:
+    """Synchronise, read and clear the device status word; returns the status code."""
+    return int(lib().moe_device_status(_ptr(ws), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------------------------
+# convenience: the whole layer on tensors already on the device
+
+class Layer:
+    """Holds device copies of a layer's weights and a workspace; ``forward(h)`` calls moe_forward."""
+
+    def __init__(self, cfg: moe_config_t, weights: dict, device="cuda"):
+        self.cfg = cfg
+        dev = torch.device(device)
+        self.w = {k: (v.to(dev).contiguous() if v is not None else None) for k, v in weights.items()
+                  if k != "h"}
+        self.ws = workspace(cfg, dev)
+        dt = torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
+        self.y = torch.empty((cfg.T, cfg.d), dtype=dt, device=dev)
+        self.aux = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.topk_idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+        self.counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+
+    def forward(self, h: torch.Tensor, stream=None) -> torch.Tensor:
+        w = self.w
+        moe_forward(self.cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"),
+                    w["W2"], w.get("b2"), self.y, self.aux, self.topk_idx, self.counts, self.ws,
+                    stream)
+        return self.y

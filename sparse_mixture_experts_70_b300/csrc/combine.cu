@@ -1,0 +1,141 @@
+// combine.cu -- step 5 of the MoE layer: gate-weighted combine and the auxiliary value.
+//
+// lensaml.com "Mixture of Experts", Step 3 "Top-k Routing": y = sum g . E(h), the chosen
+// experts' outputs blended by their gates. Step 4 "Load Balancing": the auxiliary term
+// N . sum_i f_i P_i, with f_i the fraction of routing slots sent to expert i and P_i its mean
+// router probability, equal to 1 under uniform routing.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+    uint4 v;
+    __device__ __forceinline__ void load(const void *p, int64_t i) {
+        v = __ldg(reinterpret_cast<const uint4 *>(p) + i);
+    }
+    __device__ __forceinline__ float get(int q) const {
+        const uint32_t w = (&v.x)[q >> 1];
+        const uint16_t b = (q & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xffffu);
+        return __bfloat162float(__ushort_as_bfloat16(b));
+    }
+    static __device__ __forceinline__ void store(void *p, int64_t i, const float *x) {
+        uint4 o;
+        uint32_t *ow = &o.x;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
+            ow[q] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        reinterpret_cast<uint4 *>(p)[i] = o;
+    }
+};
+template <> struct Vec8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void *p, int64_t i) {
+        a = __ldg(reinterpret_cast<const float4 *>(p) + 2 * i);
+        b = __ldg(reinterpret_cast<const float4 *>(p) + 2 * i + 1);
+    }
+    __device__ __forceinline__ float get(int q) const {
+        return q < 4 ? (&a.x)[q] : (&b.x)[q - 4];
+    }
+    static __device__ __forceinline__ void store(void *p, int64_t i, const float *x) {
+        reinterpret_cast<float4 *>(p)[2 * i] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4 *>(p)[2 * i + 1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+};
+
+// y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :]: one warp per token, eight
+// elements per lane per step, f32 FMA in j order, rounded once to the output type.
+template <typename VT>
+__global__ void __launch_bounds__(256) combine_kernel(const void *__restrict__ y_perm,
+                                                      const int32_t *__restrict__ slot_of,
+                                                      const float *__restrict__ gates,
+                                                      void *__restrict__ y, int64_t T, int64_t P,
+                                                      int d, int k, uint32_t *dev_status) {
+    const int lane = threadIdx.x & 31;
+    const int v8 = d / 8;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        // k <= 32: lane j fetches slot j; the warp reads them back by shuffles.
+        int32_t my_row = 0;
+        float my_g = 0.f;
+        if (lane < k) {
+            my_row = __ldg(slot_of + t * k + lane);
+            my_g = __ldg(gates + t * k + lane);
+            if (my_row < 0 || my_row >= P) {
+                report(dev_status, DEV_ERR_INDEX);
+                my_row = 0;
+                my_g = 0.f;
+            }
+        }
+        for (int i0 = 0; i0 < v8; i0 += 32) {
+            const int i = i0 + lane;
+            const bool ok = i < v8;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            for (int j = 0; j < k; ++j) {
+                const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
+                const float gj = __shfl_sync(0xffffffffu, my_g, j);
+                if (ok) {
+                    Vec8<VT> v;
+                    v.load(y_perm, (int64_t)row * v8 + i);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] = fmaf(gj, v.get(q), acc[q]);
+                }
+            }
+            if (ok) Vec8<VT>::store(y, t * v8 + i, acc);
+        }
+    }
+}
+
+// aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T), reduced in a fixed order.
+__global__ void aux_kernel(const int32_t *__restrict__ counts, const float *__restrict__ psum,
+                           int64_t rows, int E, int64_t T, int k, float *aux_out) {
+    __shared__ double term[256];
+    const int e = threadIdx.x;
+    if (e < E) {
+        double s = 0.0;
+        for (int64_t b = 0; b < rows; ++b) s += (double)psum[b * E + e];
+        const double Pe = s / (double)T;
+        const double fe = (double)counts[e] / ((double)T * (double)k);
+        term[e] = fe * Pe;
+    }
+    __syncthreads();
+    if (e == 0) {
+        double acc = 0.0;
+        for (int q = 0; q < E; ++q) acc += term[q];
+        *aux_out = T > 0 ? (float)((double)E * acc) : 0.f;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
+                           const float *gates, void *y, uint32_t *dev_status, cudaStream_t s) {
+    if (c.T == 0) return cudaSuccess;
+    int64_t blocks = (c.T + 7) / 8;
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    const int64_t P = c.T * c.k;
+    if (c.dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+            y_perm, slot_of, gates, y, c.T, P, c.d, c.k, dev_status);
+    else
+        combine_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(y_perm, slot_of, gates, y, c.T, P,
+                                                               c.d, c.k, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
+                       float *aux_out, cudaStream_t s) {
+    if (c.T == 0) return cudaMemsetAsync(aux_out, 0, sizeof(float), s);
+    aux_kernel<<<1, 256, 0, s>>>(counts, psum_part, router_partial_rows(c), c.E, c.T, c.k,
+                                 aux_out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

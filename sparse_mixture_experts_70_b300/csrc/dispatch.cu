@@ -1,0 +1,280 @@
+// dispatch.cu -- step 3 of the MoE layer: group the token copies by expert.
+//
+// lensaml.com "Mixture of Experts", Step 4 "Load Balancing" shows the histogram of routing slots
+// per expert; Step 5 "Capacity & Dropped Tokens" names dropless block-sparse kernels (MegaBlocks)
+// that accept any number of tokens per expert. Here every slot s = t*k + j is kept and the slots
+// are stably sorted by expert, so that each expert's rows are contiguous:
+//   sorted position of slot s (expert e) = offsets[e] + #{slots s' < s routed to e}.
+//
+// One cooperative kernel, 1024 slots per chunk, one chunk per block iteration:
+//   1. Histogram without atomics: __match_any_sync groups the lanes of a warp by expert; the
+//      group's lowest lane writes the group size into a per-warp row of shared memory; thread e
+//      then scans the 32 warp rows of expert e in warp order. This gives the chunk aggregate and,
+//      per slot, its rank inside the chunk (warp base + rank among equal lanes below it).
+//   2. Decoupled look-back over chunks (Merrill & Garland, single-pass prefix scan): thread e
+//      publishes (AGGREGATE, count) for its expert, then walks back over earlier chunks adding
+//      aggregates until it meets an INCLUSIVE prefix, and publishes (INCLUSIVE, prefix). Each
+//      flag/value pair is one 64-bit release store, read with acquire loads.
+//   3. The last chunk knows the totals: it writes counts and offsets (exclusive scan over
+//      experts) and raises a done flag; every block waits for it and scatters sorted_token and
+//      slot_of.
+// The launch is cooperative, so all blocks are co-resident and every wait can be satisfied;
+// each wait is still bounded by %globaltimer and reports DEV_ERR_TIMEOUT instead of hanging.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint64_t FLAG_AGG = 1ull << 32;
+constexpr uint64_t FLAG_INC = 2ull << 32;
+
+struct DispatchArgs {
+    const int32_t *idx;
+    int32_t *counts, *offsets, *sorted_token, *slot_of, *excl;
+    unsigned long long *words;  // [nchunks][E] look-back words
+    uint32_t *done;
+    uint32_t *dev_status;
+    int64_t P;
+    int k, E, nchunks;
+};
+
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Chunk histogram: returns this thread's expert (-1 for no slot) and its rank inside the chunk;
+// thread e < E receives the chunk's count of expert e in *agg.
+__device__ __forceinline__ int chunk_ranks(const DispatchArgs &a, int c, int32_t *cnt, int *lrank,
+                                           int *agg) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = a.E;
+    const int64_t s = (int64_t)c * DISPATCH_THREADS + tid;
+    int e = -1;
+    if (s < a.P) {
+        e = a.idx[s];
+        if (e < 0 || e >= E) {
+            report(a.dev_status, DEV_ERR_INDEX);
+            e = -1;
+        }
+    }
+    for (int q = tid; q < 32 * E; q += DISPATCH_THREADS) cnt[q] = 0;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) cnt[w * E + e] = __popc(peers);
+    __syncthreads();
+    int run = 0;
+    if (tid < E) {
+        for (int ww = 0; ww < 32; ++ww) {
+            const int v = cnt[ww * E + tid];
+            cnt[ww * E + tid] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    *lrank = e >= 0 ? cnt[w * E + e] + rank : 0;
+    *agg = run;
+    __syncthreads();
+    return e;
+}
+
+__global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchArgs a) {
+    __shared__ int32_t cnt[32 * 256];
+    __shared__ int32_t s_tot[257];
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, E = a.E;
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+
+    for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+        int lrank, agg;
+        chunk_ranks(a, c, cnt, &lrank, &agg);
+        if (tid < E) {
+            unsigned long long *mine = a.words + (size_t)c * E + tid;
+            int excl = 0;
+            if (c == 0) {
+                st_release(mine, FLAG_INC | (uint32_t)agg);
+            } else {
+                st_release(mine, FLAG_AGG | (uint32_t)agg);
+                unsigned long long t_start = 0;
+                int q = c - 1;
+                uint32_t spins = 0;
+                while (q >= 0) {
+                    const unsigned long long v = ld_acquire(a.words + (size_t)q * E + tid);
+                    const unsigned long long flag = v & 0xffffffff00000000ull;
+                    if (flag == 0) {
+                        if ((++spins & 255u) == 0) {
+                            const unsigned long long now = globaltimer_ns();
+                            if (t_start == 0) t_start = now;
+                            else if (now - t_start > SPIN_LIMIT_NS) {
+                                report(a.dev_status, DEV_ERR_TIMEOUT);
+                                s_abort = 1;
+                                break;
+                            }
+                        }
+                        continue;
+                    }
+                    excl += (int)(uint32_t)v;
+                    if (flag == FLAG_INC) break;
+                    --q;
+                }
+                st_release(mine, FLAG_INC | (uint32_t)(excl + agg));
+            }
+            a.excl[(size_t)c * E + tid] = excl;
+            if (c == a.nchunks - 1) s_tot[tid] = excl + agg;
+        }
+        if (c == a.nchunks - 1) {
+            __syncthreads();
+            if (tid == 0) {
+                int run = 0;
+                for (int e = 0; e < E; ++e) {
+                    a.counts[e] = s_tot[e];
+                    a.offsets[e] = run;
+                    run += s_tot[e];
+                }
+                a.offsets[E] = run;
+                __threadfence();
+                st_release_u32(a.done, 1u);
+            }
+        }
+    }
+
+    // Wait until the last chunk has published the offsets.
+    __syncthreads();
+    __shared__ int32_t s_off[257];
+    if (tid == 0) {
+        unsigned long long t_start = 0;
+        uint32_t spins = 0;
+        while (ld_acquire_u32(a.done) == 0u) {
+            if ((++spins & 255u) == 0) {
+                const unsigned long long now = globaltimer_ns();
+                if (t_start == 0) t_start = now;
+                else if (now - t_start > SPIN_LIMIT_NS) {
+                    report(a.dev_status, DEV_ERR_TIMEOUT);
+                    s_abort = 1;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (s_abort) return;
+    for (int e = tid; e <= E; e += DISPATCH_THREADS) s_off[e] = __ldcg(a.offsets + e);
+    __syncthreads();
+
+    for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+        int lrank, agg;
+        const int e = chunk_ranks(a, c, cnt, &lrank, &agg);
+        if (e >= 0) {
+            const int64_t s = (int64_t)c * DISPATCH_THREADS + tid;
+            const int64_t pos = (int64_t)s_off[e] + a.excl[(size_t)c * E + e] + lrank;
+            if (pos >= 0 && pos < a.P) {
+                a.sorted_token[pos] = (int32_t)(s / a.k);
+                a.slot_of[s] = (int32_t)pos;
+            } else {
+                report(a.dev_status, DEV_ERR_INDEX);
+            }
+        }
+    }
+}
+
+// x_perm[r, :] = h[sorted_token[r], :] -- one warp per destination row, 16-byte vectors.
+__global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ h,
+                                                      const int32_t *__restrict__ sorted_token,
+                                                      uint4 *__restrict__ x_perm, int64_t P,
+                                                      int64_t T, int vecs, uint32_t *dev_status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P;
+         r += warps) {
+        const int t = __ldg(sorted_token + r);
+        if (t < 0 || t >= T) {
+            if (lane == 0) report(dev_status, DEV_ERR_INDEX);
+            continue;
+        }
+        const uint4 *src = h + (int64_t)t * vecs;
+        uint4 *dst = x_perm + r * vecs;
+        int i = lane;
+        for (; i + 96 < vecs; i += 128) {
+            const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 32);
+            const uint4 v2 = __ldg(src + i + 64), v3 = __ldg(src + i + 96);
+            dst[i] = v0; dst[i + 32] = v1; dst[i + 64] = v2; dst[i + 96] = v3;
+        }
+        for (; i < vecs; i += 32) dst[i] = __ldg(src + i);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
+                            cudaStream_t s) {
+    const int64_t P = c.T * c.k;
+    if (P == 0) {
+        cudaError_t err = cudaMemsetAsync(b.counts, 0, sizeof(int32_t) * c.E, s);
+        if (err != cudaSuccess) return err;
+        return cudaMemsetAsync(b.offsets, 0, sizeof(int32_t) * (c.E + 1), s);
+    }
+    cudaError_t err = cudaMemsetAsync(b.flags, 0, b.flags_bytes, s);
+    if (err != cudaSuccess) return err;
+    DispatchArgs a;
+    a.idx = topk_idx;
+    a.counts = b.counts;
+    a.offsets = b.offsets;
+    a.sorted_token = b.sorted_token;
+    a.slot_of = b.slot_of;
+    a.excl = b.excl;
+    a.done = reinterpret_cast<uint32_t *>(b.flags);
+    a.words = reinterpret_cast<unsigned long long *>(static_cast<char *>(b.flags) + 256);
+    a.dev_status = b.dev_status;
+    a.P = P;
+    a.k = c.k;
+    a.E = c.E;
+    a.nchunks = (int)dispatch_chunks(c);
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel,
+                                                        DISPATCH_THREADS, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    int64_t grid = (int64_t)per_sm * num_sms();
+    if (grid > a.nchunks) grid = a.nchunks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(DISPATCH_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dispatch_kernel, a);
+}
+
+cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
+                           void *x_perm, uint32_t *dev_status, cudaStream_t s) {
+    const int64_t P = c.T * c.k;
+    if (P == 0) return cudaSuccess;
+    const int es = c.dtype == MOE_BF16 ? 2 : 4;
+    const int vecs = c.d * es / 16;
+    int64_t blocks = (P + 7) / 8;
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    permute_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(h), sorted_token,
+                                                    static_cast<uint4 *>(x_perm), P, c.T, vecs,
+                                                    dev_status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

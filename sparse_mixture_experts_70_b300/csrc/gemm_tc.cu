@@ -1,0 +1,529 @@
+// gemm_tc.cu -- step 4 of the MoE layer on the 5th-generation tensor cores (bf16 workloads).
+//
+// Every expert e is an MLP over its contiguous block of permuted rows [offsets[e], offsets[e+1])
+// (llm.curionode.com "Mixture of Experts.", "Workshop"; lensaml.com "Mixture of Experts", Step 1
+// and Step 6: a full expert is three d x f matrices; Step 5: dropless grouping of any number of
+// tokens per expert):
+//   GEMM1  SwiGLU : H[r, n] = SiLU(x_r . W1_e[n]) * (x_r . W3_e[n])      (bf16 out)
+//          GELU   : H[r, n] = GELU_tanh(x_r . W1_e[n] + b1_e[n])          (bf16 out)
+//   GEMM2         : y_perm[r, o] = H_r . W2_e[o] (+ b2_e[o])              (bf16 out)
+// Both are "A times B-transposed" with A and B K-contiguous, which is exactly the K-major operand
+// form of tcgen05.mma.
+//
+// Kernel design (one persistent CTA per SM, 192 threads, static round-robin tile schedule):
+//   warp 0      TMA producer: 2-D tiled bulk copies (128-byte swizzle) of a 128 x 64 A tile and
+//               a 256 x 64 B tile (SwiGLU: 128 rows of W1 stacked on 128 rows of W3) into a
+//               4-stage shared-memory ring, signalling mbarriers with transaction counts.
+//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M = 128, N = 256,
+//               K = 16, f32 accumulation in tensor memory; tcgen05.commit releases a ring stage
+//               when its MMAs have read it, and hands a finished accumulator to the epilogue.
+//               Warp 1 also owns the 512-column TMEM allocation (two 128 x 256 f32 accumulators,
+//               so the epilogue of tile i overlaps the MMAs of tile i + 1).
+//   warps 2-5   epilogue: tcgen05.ld of the thread's accumulator row (TMEM lane = row),
+//               bias / GELU / SwiGLU in f32, round to bf16, masked 16-byte stores.
+// Tile order: expert-major, then N tile, then M tile, so the CTAs in flight at any moment share a
+// few weight tiles (read once from HBM, then from L2) and one expert's activations.
+// Rows of an expert's last M tile that belong to the next expert (or lie past the end, which TMA
+// fills with zeros) are computed and masked at the store.
+// Every mbarrier wait is bounded by %globaltimer: on expiry the CTA records DEV_ERR_TIMEOUT,
+// stops issuing, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = GEMM_BM, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KiB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KiB
+constexpr int TC_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int CTL_BYTES = 4096;
+constexpr size_t TC_SMEM = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + CTL_BYTES;
+
+enum { EPI_STORE = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
+
+struct TcArgs {
+    const int32_t *offsets;  // [E+1]
+    const float *bias;       // [E, N] or null
+    __nv_bfloat16 *out;      // [P, N]
+    uint32_t *dev_status;
+    int64_t P;
+    int E, K, N, n_tiles, epi;
+};
+
+// ---------------------------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of `parity` to complete; false on abort (set by another role) or on
+// running out of time (then this call sets the abort flag and the device status bit).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            uint32_t *dev_status) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (abort && *abort) return false;
+            if (globaltimer_ns() - t0 > SPIN_LIMIT_NS) {
+                if (abort) *abort = 1;
+                report(dev_status, DEV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint32_t *dev_status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, dev_status);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, f32 accumulator.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored the way a 128-byte-swizzled TMA box
+// writes it: rows of 128 bytes (64 bf16 along K), groups of 8 rows 1024 bytes apart.
+//   bits  0-13  start address >> 4        bits 16-29  leading byte offset >> 4 (unused here: 1)
+//   bits 32-45  stride byte offset >> 4   bits 46-47  descriptor version (1 on sm_100 family)
+//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
+// The K = 16 slices of a 64-wide stage start 32 bytes apart; the swizzle is applied by the
+// hardware on absolute addresses, so the stage base must be 1024-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor of kind::f16: f32 accumulator (bits 4-5 = 1), A and B bf16 (bits 7-9,
+// 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Load 32 consecutive f32 columns of this thread's TMEM lane, and wait for the load.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two such loads (columns at taddr0 and taddr1) with a single wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, float (&v0)[32],
+                                            float (&v1)[32]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr0), "r"(taddr1)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v0[i] = __uint_as_float(r[i]);
+        v1[i] = __uint_as_float(r[32 + i]);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+__device__ __forceinline__ float gelu_tanh(float x) {
+    return 0.5f * x * (1.f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));
+}
+__device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
+
+struct Tile {
+    int e, n, row0, rows;
+};
+// Tile t of the schedule: s_cum[e] is the first tile of expert e (E+1 entries); within an
+// expert, tiles run N-major, M-minor. eh is a cursor that only moves forward.
+__device__ __forceinline__ Tile decode_tile(int t, int &eh, const int32_t *s_cum,
+                                            const int32_t *s_off, int n_tiles) {
+    while (s_cum[eh + 1] <= t) ++eh;
+    const int e = eh;
+    const int local = t - s_cum[e];
+    const int mt = (s_cum[e + 1] - s_cum[e]) / n_tiles;
+    const int n = local / mt;
+    const int m = local - n * mt;
+    Tile ti;
+    ti.e = e;
+    ti.n = n;
+    ti.row0 = s_off[e] + m * BM;
+    ti.rows = min(BM, s_off[e + 1] - ti.row0);
+    return ti;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmB3, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + STAGES * A_STAGE;
+    uint8_t *ctl = gbase + STAGES * (A_STAGE + B_STAGE);
+    const uint32_t bar0 = smem_u32(ctl);
+    // barriers: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+    const uint32_t bar_full = bar0, bar_empty = bar0 + 8 * STAGES;
+    const uint32_t bar_tfull = bar0 + 16 * STAGES, bar_tempty = bar_tfull + 16;
+    const uint32_t bar_drain = bar_tempty + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl + 256);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(ctl + 260);
+    int32_t *s_cum = reinterpret_cast<int32_t *>(ctl + 512);   // [E+1]
+    int32_t *s_off = s_cum + 260;                             // [E+1]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(bar_tfull + 8 * q, 1);
+            mbar_init(bar_tempty + 8 * q, 128);
+        }
+        mbar_init(bar_drain, 1);
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 2 && lane == 0) {
+        int cum = 0;
+        bool bad = false;
+        for (int e = 0; e < E; ++e) {
+            const int lo = a.offsets[e], hi = a.offsets[e + 1];
+            if (lo < 0 || hi < lo || (int64_t)hi > a.P) bad = true;
+            s_off[e] = lo;
+            s_cum[e] = cum;
+            if (!bad) cum += ((hi - lo + BM - 1) / BM) * a.n_tiles;
+        }
+        s_off[E] = a.offsets[E];
+        s_cum[E] = cum;
+        if (bad) {
+            report(a.dev_status, DEV_ERR_INDEX);
+            for (int e = 0; e <= E; ++e) s_cum[e] = 0;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = s_cum[E];
+    const int nk = a.K / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0, eh = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, last_phase = 0;  // per-stage bits
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile ti = decode_tile(t, eh, s_cum, s_off, a.n_tiles);
+                const int brow = ti.e * a.N + ti.n * (a.epi == EPI_SWIGLU ? BN / 2 : BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full + 8 * stage;
+                    mbar_expect_tx(fb, A_STAGE + B_STAGE);
+                    tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
+                    if (a.epi == EPI_SWIGLU) {
+                        tma_load_2d(sB + stage * B_STAGE, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(sB + stage * B_STAGE + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
+                    } else {
+                        tma_load_2d(sB + stage * B_STAGE, &tmB, fb, kb * BK, brow);
+                    }
+                    issued |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Our own copies must have landed before the CTA may exit.
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    mbar_wait(bar_full + 8 * s, (last_phase >> s) & 1u, nullptr, a.dev_status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, s_abort, a.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_k_sw128(sA + stage * A_STAGE);
+                    const uint64_t bd = sdesc_k_sw128(sB + stage * B_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit(bar_empty + 8 * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(bar_tfull + 8 * acc);
+                acc ^= 1;
+                if (acc == 0) aphase ^= 1u;
+            }
+            // Every MMA this thread issued has completed once the drain barrier fires.
+            umma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, nullptr, a.dev_status);
+        }
+    } else {
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;
+        int acc = 0, eh = 0;
+        uint32_t aphase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile ti = decode_tile(t, eh, s_cum, s_off, a.n_tiles);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            const bool valid = r < ti.rows;
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
+            if (a.epi == EPI_SWIGLU) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    float x1[32], x3[32];
+                    tmem_ld32x2(trow + c, trow + BN / 2 + c, x1, x3);
+                    const int col = ti.n * (BN / 2) + c;
+                    if (valid && col < a.N) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16(silu(x1[2 * i]) * x3[2 * i],
+                                              silu(x1[2 * i + 1]) * x3[2 * i + 1]);
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    const int col = ti.n * BN + c;
+                    if (col >= a.N) break;  // warp-uniform
+                    float v[32];
+                    tmem_ld32(trow + c, v);
+                    if (a.bias) {
+                        const float *bp = a.bias + (int64_t)ti.e * a.N + col;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += __ldg(bp + i);
+                    }
+                    if (a.epi == EPI_GELU) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                    }
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]),
+                                                pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                                                pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                                                pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_tempty + 8 * acc);
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of box_rows x 64 with the
+// 128-byte swizzle; out-of-range rows read as zeros.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P, int E, int K,
+                        int N, int epi, const int32_t *offsets, const float *bias, void *out,
+                        uint32_t *dev_status, cudaStream_t s) {
+    const int b_rows = epi == EPI_SWIGLU ? BN / 2 : BN;
+    CUtensorMap mA, mB, mB3;
+    if (!make_map(&mA, A, P, K, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mB, B, (int64_t)E * N, K, b_rows)) return cudaErrorInvalidValue;
+    if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, b_rows))
+        return cudaErrorInvalidValue;
+    TcArgs a;
+    a.offsets = offsets;
+    a.bias = bias;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.dev_status = dev_status;
+    a.P = P;
+    a.E = E;
+    a.K = K;
+    a.N = N;
+    a.n_tiles = (N + b_rows - 1) / b_rows;
+    a.epi = epi;
+    const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
+    int64_t grid = num_sms();
+    if (grid > upper) grid = upper;
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)TC_SMEM);
+    if (err != cudaSuccess) return err;
+    grouped_gemm_tc_kernel<<<(unsigned)grid, TC_THREADS, TC_SMEM, s>>>(mA, mB, mB3, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s) {
+    const int64_t P = c.T * c.k;
+    if (P == 0) return cudaSuccess;
+    const bool swiglu = c.act == MOE_ACT_SWIGLU;
+    cudaError_t err = launch_gemm(b.x_perm, b.W1, b.W3, P, c.E, c.d, c.f,
+                                  swiglu ? EPI_SWIGLU : EPI_GELU, b.offsets,
+                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, s);
+    if (err != cudaSuccess) return err;
+    return launch_gemm(b.H, b.W2, nullptr, P, c.E, c.f, c.d, EPI_STORE, b.offsets,
+                       c.has_bias ? b.b2 : nullptr, b.y_perm, b.dev_status, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,98 @@
+// internal.cuh -- declarations shared by libmoe's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------
+// device status word (first 4 bytes of every workspace)
+enum : uint32_t {
+    DEV_ERR_TIMEOUT = 1u,  // a bounded spin-wait gave up
+    DEV_ERR_INDEX = 2u,    // an expert / token / row index outside its range was read
+};
+
+// Every spin-wait in libmoe gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long SPIN_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void report(uint32_t *dev_status, uint32_t bits) {
+    if (dev_status) atomicOr(dev_status, bits);
+}
+
+// ------------------------------------------------------------------------------------------
+// shapes and the workspace layout
+constexpr int DISPATCH_THREADS = 1024;  // slots per dispatch chunk
+constexpr int GEMM_BM = 128;            // rows per tensor-core tile
+
+struct WsLayout {
+    size_t status;        // u32 device status word
+    size_t disp_flags;    // u32 done flag + pad, then nchunks*E u64 look-back words
+    size_t disp_flags_bytes;
+    size_t disp_excl;     // nchunks*E int32 (per-chunk exclusive counts)
+    size_t psum;          // router partial sums [rows, E] f32
+    size_t topk_idx, gates, counts, offsets, sorted_token, slot_of, aux;
+    size_t x_perm, H, y_perm;
+    size_t total;
+};
+
+inline int64_t dispatch_chunks(const moe_config_t &c) {
+    const int64_t P = c.T * c.k;
+    return (P + DISPATCH_THREADS - 1) / DISPATCH_THREADS;
+}
+
+int router_block_tokens(int E);  // tokens per router block (rows of psum_part per block)
+
+inline int64_t router_partial_rows(const moe_config_t &c) {
+    const int bt = router_block_tokens(c.E);
+    return (c.T + bt - 1) / bt;
+}
+
+WsLayout ws_layout(const moe_config_t &c);
+
+int num_sms();
+
+// ------------------------------------------------------------------------------------------
+// launchers (each returns the launch's cudaError_t)
+cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
+                               const float *b_r, int32_t *topk_idx, float *gates,
+                               float *psum_part, cudaStream_t s);
+
+struct DispatchBufs {
+    int32_t *counts, *offsets, *sorted_token, *slot_of;
+    void *flags;        // workspace look-back region (zeroed by the launcher)
+    size_t flags_bytes;
+    int32_t *excl;
+    uint32_t *dev_status;
+};
+cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
+                            cudaStream_t s);
+cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
+                           void *x_perm, uint32_t *dev_status, cudaStream_t s);
+cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
+                           const float *gates, void *y, uint32_t *dev_status, cudaStream_t s);
+cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
+                       float *aux_out, cudaStream_t s);
+
+struct FfnBufs {
+    const void *x_perm;
+    const int32_t *offsets;
+    const void *W1, *W3, *W2;
+    const float *b1, *b2;
+    void *H;       // [P, f] workspace
+    void *y_perm;  // [P, d]
+    uint32_t *dev_status;
+};
+cudaError_t launch_ffn_f32(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
+cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
+
+}  // namespace moe

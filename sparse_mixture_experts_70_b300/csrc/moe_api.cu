@@ -1,0 +1,264 @@
+// moe_api.cu -- the extern "C" entry points declared in include/moe.h: argument checks, the
+// workspace layout, and the launch sequence of the layer forward. No allocation, no global state
+// beyond a per-device cache of the SM count.
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.cuh"
+
+namespace moe {
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+static size_t align_up(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+WsLayout ws_layout(const moe_config_t &c) {
+    WsLayout L;
+    const size_t P = (size_t)(c.T * c.k);
+    const size_t es = c.dtype == MOE_BF16 ? 2 : 4;
+    const size_t E = (size_t)c.E;
+    const size_t nch = (size_t)dispatch_chunks(c);
+    size_t off = 0;
+    L.status = off;                       off = align_up(off + 256);
+    L.disp_flags = off;
+    L.disp_flags_bytes = 256 + nch * E * 8;
+    off = align_up(off + L.disp_flags_bytes);
+    L.disp_excl = off;                    off = align_up(off + nch * E * 4);
+    L.psum = off;                         off = align_up(off + (size_t)router_partial_rows(c) * E * 4);
+    L.topk_idx = off;                     off = align_up(off + P * 4);
+    L.gates = off;                        off = align_up(off + P * 4);
+    L.counts = off;                       off = align_up(off + E * 4);
+    L.offsets = off;                      off = align_up(off + (E + 1) * 4);
+    L.sorted_token = off;                 off = align_up(off + P * 4);
+    L.slot_of = off;                      off = align_up(off + P * 4);
+    L.aux = off;                          off = align_up(off + 4);
+    L.x_perm = off;                       off = align_up(off + P * (size_t)c.d * es);
+    L.H = off;                            off = align_up(off + P * (size_t)c.f * es);
+    L.y_perm = off;                       off = align_up(off + P * (size_t)c.d * es);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status_t check_cfg(const moe_config_t *c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->E < 1 || c->E > 256 || c->k < 1 || c->k > c->E) return MOE_ERR_INVALID_ARG;
+    if (c->d < 64 || c->f < 64 || c->d % 64 != 0 || c->f % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (c->T * (int64_t)c->k >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)c->E * c->d >= ((int64_t)1 << 31) || (int64_t)c->E * c->f >= ((int64_t)1 << 31))
+        return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->act != MOE_ACT_GELU_TANH && c->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    if (c->gate != MOE_GATE_RENORM && c->gate != MOE_GATE_RAW_PROB) return MOE_ERR_UNSUPPORTED;
+    if (c->k > 32) return MOE_ERR_UNSUPPORTED;
+    if (c->has_bias && c->act == MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return p && ((uintptr_t)p & 3u) == 0; }
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes) {
+    const moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    if (!aligned16(ws) || ws_bytes < 1024) return MOE_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(ws, 0, 1024, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows) {
+    const moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!rows) return MOE_ERR_INVALID_ARG;
+    *rows = router_partial_rows(*cfg);
+    return MOE_OK;
+}
+
+moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float *W_r,
+                             const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
+                             void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) || !aligned4(topk_idx) ||
+        !aligned4(gates) || !aligned4(psum_part))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_router_topk(*cfg, h, W_r, b_r, topk_idx, gates, psum_part,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, const void *h,
+                                int32_t *counts, int32_t *offsets, int32_t *sorted_token,
+                                int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes,
+                                void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!aligned4(counts) || !aligned4(offsets) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cfg->T > 0) {
+        if (!aligned4(topk_idx) || !aligned4(sorted_token) || !aligned4(slot_of))
+            return MOE_ERR_INVALID_ARG;
+        if (x_perm && (!aligned16(x_perm) || !aligned16(h))) return MOE_ERR_INVALID_ARG;
+    }
+    char *w = static_cast<char *>(ws);
+    DispatchBufs b{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
+                   reinterpret_cast<int32_t *>(w + L.disp_excl),
+                   reinterpret_cast<uint32_t *>(w + L.status)};
+    st = from_cuda(launch_dispatch(*cfg, topk_idx, b, s));
+    if (st != MOE_OK || !x_perm || cfg->T == 0) return st;
+    return from_cuda(launch_permute(*cfg, h, sorted_token, x_perm, b.dev_status, s));
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets,
+                            const void *W1, const float *b1, const void *W3, const void *W2,
+                            const float *b2, void *y_perm, void *ws, size_t ws_bytes,
+                            void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (cfg->T == 0) return MOE_OK;
+    if (!aligned16(x_perm) || !aligned4(offsets) || !aligned16(W1) || !aligned16(W2) ||
+        !aligned16(y_perm))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->act == MOE_ACT_SWIGLU && !aligned16(W3)) return MOE_ERR_INVALID_ARG;
+    if (cfg->has_bias && (!aligned4(b1) || !aligned4(b2))) return MOE_ERR_INVALID_ARG;
+    char *w = static_cast<char *>(ws);
+    FfnBufs b{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm,
+              reinterpret_cast<uint32_t *>(w + L.status)};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(cfg->dtype == MOE_BF16 ? launch_ffn_tc(*cfg, b, s) : launch_ffn_f32(*cfg, b, s));
+}
+
+moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int32_t *slot_of,
+                         const float *gates, void *y, void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    if (!aligned16(y_perm) || !aligned4(slot_of) || !aligned4(gates) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_combine(*cfg, y_perm, slot_of, gates, y, nullptr,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const float *psum_part,
+                          float *aux_out, void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!aligned4(aux_out)) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!aligned4(counts) || !aligned4(psum_part))) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_aux(*cfg, counts, psum_part, aux_out, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
+                         const float *b_r, const void *W1, const float *b1, const void *W3,
+                         const void *W2, const float *b2, void *y, float *aux_out,
+                         int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
+                         void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config_t &c = *cfg;
+    if (!aligned16(ws) || !aligned4(aux_out)) return MOE_ERR_INVALID_ARG;
+    if (c.T > 0) {
+        if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) || !aligned16(W1) ||
+            !aligned16(W2) || !aligned16(y))
+            return MOE_ERR_INVALID_ARG;
+        if (c.act == MOE_ACT_SWIGLU && !aligned16(W3)) return MOE_ERR_INVALID_ARG;
+        if (c.has_bias && (!aligned4(b1) || !aligned4(b2))) return MOE_ERR_INVALID_ARG;
+        if ((topk_idx_out && !aligned4(topk_idx_out)) || (counts_out && !aligned4(counts_out)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const WsLayout L = ws_layout(c);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *w = static_cast<char *>(ws);
+    uint32_t *dev_status = reinterpret_cast<uint32_t *>(w + L.status);
+    int32_t *topk = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t *>(w + L.topk_idx);
+    int32_t *counts = counts_out ? counts_out : reinterpret_cast<int32_t *>(w + L.counts);
+    float *gates = reinterpret_cast<float *>(w + L.gates);
+    float *psum = reinterpret_cast<float *>(w + L.psum);
+    int32_t *offsets = reinterpret_cast<int32_t *>(w + L.offsets);
+    int32_t *sorted_token = reinterpret_cast<int32_t *>(w + L.sorted_token);
+    int32_t *slot_of = reinterpret_cast<int32_t *>(w + L.slot_of);
+    void *x_perm = w + L.x_perm;
+    void *y_perm = w + L.y_perm;
+
+    if (c.T == 0) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(aux_out, 0, sizeof(float), s);
+        return from_cuda(e);
+    }
+    cudaError_t e = launch_router_topk(c, h, W_r, b_r, topk, gates, psum, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
+                    reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
+    if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_permute(c, h, sorted_token, x_perm, dev_status, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
+    e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if ((e = launch_aux(c, counts, psum, aux_out, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status_t moe_device_status(void *ws, void *stream) {
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(ws, 0, sizeof(word), s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (word & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (word & DEV_ERR_INDEX) return MOE_ERR_DEVICE_INDEX;
+    return MOE_OK;
+}
+
+const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

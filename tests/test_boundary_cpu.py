@@ -1,0 +1,104 @@
+"""The C-ABI library on the host: it loads, exports every function include/moe.h declares, and its
+argument checks return the documented status codes before touching any device. CPU only."""
+import ctypes
+import subprocess
+
+import pytest
+
+from sparse_mixture_experts_70_b300 import binding as B
+from sparse_mixture_experts_70_b300 import workloads as wl
+
+
+def test_library_exports_every_declared_symbol():
+    declared = B.header_symbols()
+    assert len(declared) >= 11
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [s for s in declared if s not in exported]
+    assert not missing, missing
+    L = B.lib()
+    for s in declared:
+        assert getattr(L, s) is not None
+
+
+def test_status_strings():
+    for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (2, "MOE_ERR_UNSUPPORTED"),
+                       (3, "MOE_ERR_WORKSPACE"), (4, "MOE_ERR_CUDA"), (5, "MOE_ERR_TIMEOUT"),
+                       (6, "MOE_ERR_DEVICE_INDEX")]:
+        assert B.status_string(code) == name
+
+
+def _ws_size(cfg):
+    n = ctypes.c_size_t()
+    return B.lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), n.value
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_workspace_sizes_of_the_workloads(name):
+    w = wl.WORKLOADS[name]
+    st, n = _ws_size(B.config_for(w))
+    assert st == B.MOE_OK
+    es = 4 if w.dtype == "f32" else 2
+    # at least x_perm, H and y_perm
+    assert n >= w.P * (2 * w.d + w.f) * es
+    assert n < w.P * (2 * w.d + w.f) * es + 64 * 2**20
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(k=0), B.MOE_ERR_INVALID_ARG),
+    (dict(k=9), B.MOE_ERR_INVALID_ARG),           # k > E
+    (dict(E=0), B.MOE_ERR_INVALID_ARG),
+    (dict(E=257, k=2), B.MOE_ERR_INVALID_ARG),
+    (dict(d=100), B.MOE_ERR_INVALID_ARG),          # not a multiple of 64
+    (dict(f=32), B.MOE_ERR_INVALID_ARG),
+    (dict(T=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(T=2**30, k=2), B.MOE_ERR_INVALID_ARG),   # T k >= 2^31
+    (dict(dtype=7), B.MOE_ERR_UNSUPPORTED),
+    (dict(act=5), B.MOE_ERR_UNSUPPORTED),
+    (dict(gate=3), B.MOE_ERR_UNSUPPORTED),
+    (dict(E=64, k=33), B.MOE_ERR_UNSUPPORTED),     # k > 32 not built
+    (dict(has_bias=True), B.MOE_ERR_UNSUPPORTED),  # SwiGLU has no biases
+])
+def test_invalid_configs_are_rejected(kw, expect):
+    base = dict(T=64, d=128, f=256, E=8, k=2, dtype=B.MOE_BF16, act=B.MOE_ACT_SWIGLU,
+                gate=B.MOE_GATE_RENORM, has_bias=False)
+    base.update(kw)
+    cfg = B.config(**base)
+    st, _ = _ws_size(cfg)
+    assert st == expect
+    L = B.lib()
+    assert L.moe_forward(ctypes.byref(cfg), *([None] * 13), 0, None) == expect
+
+
+def test_null_and_misaligned_pointers_are_rejected_on_the_host():
+    cfg = B.config(T=64, d=128, f=256, E=8, k=2)
+    L = B.lib()
+    st, n = _ws_size(cfg)
+    assert st == 0
+    fake = 1 << 40          # never dereferenced: the checks run before any launch
+    # missing h
+    assert L.moe_forward(ctypes.byref(cfg), None, fake, None, fake, None, fake, fake, None, fake,
+                         fake, None, None, fake, n, None) == B.MOE_ERR_INVALID_ARG
+    # misaligned W1
+    assert L.moe_forward(ctypes.byref(cfg), fake, fake, None, fake + 2, None, fake, fake, None,
+                         fake, fake, None, None, fake, n, None) == B.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert L.moe_forward(ctypes.byref(cfg), fake, fake, None, fake, None, fake, fake, None, fake,
+                         fake, None, None, fake, n - 1, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_expert_ffn(ctypes.byref(cfg), fake, fake, fake, None, fake, fake, None, fake,
+                            fake, n - 1, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_build_dispatch(ctypes.byref(cfg), fake, None, None, fake, fake, fake, None,
+                                fake, n, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(cfg), fake, fake, fake, fake + 8, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_topk(ctypes.byref(cfg), fake, None, None, fake, fake, fake, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert L.moe_aux_loss(ctypes.byref(cfg), fake, fake, None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_device_status(None, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_router_partial_rows():
+    for name, w in wl.WORKLOADS.items():
+        rows = B.moe_router_partials(B.config_for(w))
+        assert 1 <= rows <= w.T

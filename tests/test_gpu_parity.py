@@ -1,0 +1,168 @@
+"""GPU parity: libmoe (through its C ABI) against the double-precision oracle, on the same seeded
+inputs. Indices, counts and the permutation are compared bit for bit (outside near ties); the
+layer output within max-abs 1e-4 (f32) or relative L2 1e-2 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mixture_experts_70_b300 import binding as B
+from sparse_mixture_experts_70_b300 import workloads as wl
+
+from parity import (AUX_REL, GATE_ABS, check_dispatch_valid, check_layer_output, rel_l2,
+                    routing_agreement, run_forward, run_steps, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+G, S = wl.ACT_GELU_TANH, wl.ACT_SWIGLU
+
+SMALL = [
+    wl.small("single_expert", T=1, d=64, f=64, E=1, k=1),
+    wl.small("k_equals_E", T=37, d=64, f=128, E=4, k=4),
+    wl.small("ragged_swiglu", T=300, d=192, f=320, E=6, k=2),
+    wl.small("ragged_gelu_bias_f32", T=133, d=128, f=192, E=5, k=2, act=G, dtype="f32",
+             has_bias=True),
+    wl.small("f32_swiglu", T=200, d=128, f=256, E=8, k=2, dtype="f32"),
+    wl.small("gelu_bias_raw_prob", T=517, d=256, f=512, E=16, k=1, act=G,
+             gate=wl.GATE_RAW_PROB, has_bias=True),
+    wl.small("skewed_idle", T=1000, d=128, f=256, E=32, k=4, router_bias_var=8.0),
+    wl.small("many_chunks", T=5000, d=64, f=64, E=64, k=4),
+    wl.small("wide_E", T=700, d=128, f=128, E=256, k=8),
+    wl.small("several_tiles", T=1100, d=512, f=768, E=3, k=2),
+]
+
+
+def _inputs(w):
+    inp = wl.generate(w)
+    if w.has_bias:
+        inp = wl.random_biases(w, inp, seed=w.seed + 100)
+    return inp
+
+
+def _check_steps(w, inputs, ref, got):
+    assert got["status"] == B.MOE_OK, B.status_string(got["status"])
+    idx = got["idx"].numpy()
+    diff = routing_agreement(ref, idx)
+    keep = np.setdiff1d(np.arange(w.T), diff)
+    np.testing.assert_allclose(got["gates"].numpy()[keep], ref["g"][keep], rtol=0, atol=GATE_ABS)
+    counts, offsets = got["counts"].numpy(), got["offsets"].numpy()
+    st, so = got["sorted_token"].numpy(), got["slot_of"].numpy()
+    if len(diff) == 0:
+        np.testing.assert_array_equal(counts, ref["counts"])
+        np.testing.assert_array_equal(offsets, ref["offsets"])
+        np.testing.assert_array_equal(st, ref["sorted_token"])
+        np.testing.assert_array_equal(so, ref["slot_of"])
+    else:
+        check_dispatch_valid(idx, w.E, counts, offsets, st, so)
+    # the permute is a copy: bit-exact
+    assert torch.equal(got["x_perm"], inputs["h"][torch.from_numpy(st).long()])
+    assert got["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
+    return diff
+
+
+def _check_expert_rows(w, inputs, got, rows):
+    """y_perm rows against the oracle's expert MLP applied to the same (exact) x_perm rows."""
+    offsets = got["offsets"].numpy()
+    expert_of_row = np.searchsorted(offsets, rows, side="right") - 1
+    x = got["x_perm"][torch.from_numpy(rows).long()].double().numpy()
+    yr = oracle.expert_ffn(x, expert_of_row.astype(np.int32), inputs["W1"], inputs.get("W3"),
+                           inputs["W2"], inputs.get("b1"), inputs.get("b2"), oracle.act_code(w))
+    yg = got["y_perm"][torch.from_numpy(rows).long()].double().numpy()
+    if w.dtype == "f32":
+        assert np.abs(yg - yr).max() <= 1e-4
+    else:
+        assert rel_l2(yg, yr) <= 1e-2
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_cases_step_by_step(w):
+    inputs = _inputs(w)
+    ref = oracle.reference(w, inputs)
+    dev = to_dev(inputs)
+    got = run_steps(w, inputs, dev)
+    diff = _check_steps(w, inputs, ref, got)
+    rows = np.arange(w.P) if w.P <= 4096 else np.unique(np.linspace(0, w.P - 1, 2048).astype(int))
+    _check_expert_rows(w, inputs, got, rows)
+    check_layer_output(w, ref, got["y"], skip_tokens=diff)
+    # the fused call runs the same kernels: identical bits
+    fw = run_forward(w, dev)
+    assert fw["status"] == B.MOE_OK
+    assert torch.equal(fw["y"], got["y"])
+    assert torch.equal(fw["idx"], got["idx"]) and torch.equal(fw["counts"], got["counts"])
+    assert fw["aux"].item() == got["aux"].item()
+
+
+def _token_sample(w):
+    if w.T <= 256:
+        return np.arange(w.T)
+    n = {"mixtral": 24, "many_small": 128, "switch": 256}.get(w.name, 128)
+    edge = max(n // 4, 4)
+    mid = np.linspace(edge, w.T - edge - 1, n - 2 * edge).astype(np.int64)
+    return np.unique(np.concatenate([np.arange(edge), mid, np.arange(w.T - edge, w.T)]))
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_full_size_workloads(name):
+    """The five workloads at full size, through moe_forward (the call the benchmark times) and
+    through the five step calls: routing, counts and permutation over all tokens, the layer
+    output on a deterministic token sample (every token for micro and decode)."""
+    w = wl.WORKLOADS[name]
+    inputs = _inputs(w)
+    tokens = _token_sample(w)
+    ref = oracle.reference(w, inputs, tokens=tokens)
+    dev = to_dev(inputs)
+    fw = run_forward(w, dev)
+    assert fw["status"] == B.MOE_OK
+    diff = routing_agreement(ref, fw["idx"].numpy())
+    if len(diff) == 0:
+        np.testing.assert_array_equal(fw["counts"].numpy(), ref["counts"])
+    assert fw["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
+    stats = check_layer_output(w, ref, fw["y"], skip_tokens=diff)
+    print(f"{name}: near-tie tokens {len(diff)}, {stats}")
+    got = run_steps(w, inputs, dev)
+    _check_steps(w, inputs, ref, got)
+    assert torch.equal(got["y"], fw["y"])
+    if name == "decode":
+        assert (got["counts"] > 0).all()
+
+
+def test_empty_batch():
+    w = wl.small("empty", T=0, d=64, f=64, E=4, k=2)
+    cfg = B.config_for(w)
+    ws = B.workspace(cfg)
+    counts = torch.full((4,), 9, dtype=torch.int32, device="cuda")
+    aux = torch.full((1,), 9.0, device="cuda")
+    z = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    B.moe_forward(cfg, z, torch.zeros(64, 4, device="cuda"), None, z, None, z, z, None, z, aux,
+                  None, counts, ws)
+    assert B.moe_device_status(ws) == B.MOE_OK
+    assert counts.cpu().tolist() == [0, 0, 0, 0] and aux.item() == 0.0
+
+
+def test_outputs_stay_inside_their_buffers_and_runs_are_deterministic():
+    w = wl.small("canary", T=333, d=128, f=192, E=12, k=3, router_bias_var=1.0)
+    inputs = _inputs(w)
+    dev = to_dev(inputs)
+    cfg = B.config_for(w)
+    ws = B.workspace(cfg)
+    guard = 64
+    ybuf = torch.full((w.T + 2 * guard, w.d), 7.0, dtype=torch.bfloat16, device="cuda")
+    ibuf = torch.full((w.T * w.k + 2 * guard,), -5, dtype=torch.int32, device="cuda")
+    cbuf = torch.full((w.E + 2 * guard,), -5, dtype=torch.int32, device="cuda")
+    y = ybuf[guard:guard + w.T]
+    idx = ibuf[guard:guard + w.T * w.k]
+    cnt = cbuf[guard:guard + w.E]
+    aux = torch.zeros(1, device="cuda")
+    outs = []
+    for _ in range(3):
+        B.moe_forward(cfg, dev["h"], dev["W_r"], dev["b_r"], dev["W1"], None, dev["W3"],
+                      dev["W2"], None, y, aux, idx, cnt, ws)
+        assert B.moe_device_status(ws) == B.MOE_OK
+        outs.append((y.clone(), idx.clone(), cnt.clone(), aux.clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    for a, b in zip(outs[0], outs[2]):
+        assert torch.equal(a, b)
+    assert (ybuf[:guard] == 7.0).all() and (ybuf[guard + w.T:] == 7.0).all()
+    assert (ibuf[:guard] == -5).all() and (ibuf[guard + w.T * w.k:] == -5).all()
+    assert (cbuf[:guard] == -5).all() and (cbuf[guard + w.E:] == -5).all()
