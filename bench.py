@@ -171,8 +171,13 @@ def main() -> None:
     ap.add_argument("--workload", default="mixtral", choices=list(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="reshape the workload for profiling, e.g. T=2048,E=2,k=1 (not a bench line)")
     args = ap.parse_args()
     w = wl.WORKLOADS[args.workload]
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        w = w.with_(name=w.name + "_override", **{k_: int(v) for k_, v in kv.items()})
     if args.warmup < 3:
         args.warmup = 3
 
