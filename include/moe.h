@@ -13,7 +13,8 @@
  * Conventions for every entry point
  *   - Pointers to tensors are DEVICE pointers (cudaMalloc'd or PyTorch-owned), caller-owned.
  *     The library allocates nothing and keeps no state between calls; all scratch lives in the
- *     caller's workspace `ws` (see moe_workspace_size).
+ *     caller's workspace `ws` (see moe_workspace_size) -- except for moe_build_dispatch_static,
+ *     whose scratch is a static device array inside the library.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call is
  *     asynchronous on that stream; results are valid once the stream reaches the call.
  *   - All tensors are dense row-major. "dtype" below is cfg->dtype: MOE_F32 (float) or MOE_BF16
@@ -109,6 +110,28 @@ moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx
                                 int32_t *counts, int32_t *offsets, int32_t *sorted_token,
                                 int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes,
                                 void *stream);
+
+/* Step 3 for callers that cannot allocate device memory -- for instance a custom operator inside
+ * a host runtime that owns every device buffer and hands the operator only its inputs and
+ * outputs, or a latency-critical loop that must never call cudaMalloc (which can synchronise the
+ * device). The pages have no counterpart of this call; it exists only for such callers.
+ * Same arguments, outputs and results as moe_build_dispatch, but no workspace: the dispatch
+ * scratch (look-back words, per-chunk counts, the done flag) is a file-scope device array inside
+ * libmoe of STATIC_SCRATCH = 256 + 12 * 65536 bytes (768.25 KiB), which every GPU that loads the
+ * library holds until the process exits. It serves at most 65536 look-back cells:
+ *   ceil(T k / 1024) * E <= 65536   (e.g. T k <= 1M slots for E = 64, 256K slots for E = 256);
+ * larger shapes are rejected with MOE_ERR_WORKSPACE before anything is launched.
+ *   status  (device, may be NULL) one uint32 the caller zeroes; device-side failures are OR-ed
+ *           into it (1 = a spin-wait ran out of time, 2 = an index out of range). With NULL they
+ *           are not reported.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture. No call allocates or frees memory.
+ * All calls share the one array: each call clears the parts that must start at zero, and calls
+ * whose kernels overlap on the GPU (different streams without ordering) race on it. */
+moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *topk_idx,
+                                       const void *h, int32_t *counts, int32_t *offsets,
+                                       int32_t *sorted_token, int32_t *slot_of, void *x_perm,
+                                       uint32_t *status, void *stream);
 
 /* Step 4. Every expert's MLP over its block of rows of x_perm (llm.curionode.com "Mixture of
  * Experts.", "Workshop": the experts are MLPs; lensaml.com "Mixture of Experts", Step 1 and

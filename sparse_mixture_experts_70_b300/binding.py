@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
             "moe_router_partials": [_CFG, ctypes.POINTER(ctypes.c_int64)],
             "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P],
             "moe_build_dispatch": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+            "moe_build_dispatch_static": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
             "moe_expert_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_combine": [_CFG, _P, _P, _P, _P, _P],
             "moe_aux_loss": [_CFG, _P, _P, _P, _P],
@@ -151,6 +152,15 @@ def moe_build_dispatch(cfg, topk_idx, h, counts, offsets, sorted_token, slot_of,
                                     _ptr(offsets), _ptr(sorted_token), _ptr(slot_of),
                                     _ptr(x_perm), _ptr(ws), ws.numel() * ws.element_size(),
                                     _stream(stream)), "moe_build_dispatch")
+
+
+def moe_build_dispatch_static(cfg, topk_idx, h, counts, offsets, sorted_token, slot_of, x_perm,
+                              status=None, stream=None) -> None:
+    """moe_build_dispatch without a workspace (its scratch is a static array inside libmoe)."""
+    _check(lib().moe_build_dispatch_static(ctypes.byref(cfg), _ptr(topk_idx), _ptr(h),
+                                           _ptr(counts), _ptr(offsets), _ptr(sorted_token),
+                                           _ptr(slot_of), _ptr(x_perm), _ptr(status),
+                                           _stream(stream)), "moe_build_dispatch_static")
 
 
 def moe_expert_ffn(cfg, x_perm, offsets, W1, b1, W3, W2, b2, y_perm, ws, stream=None) -> None:

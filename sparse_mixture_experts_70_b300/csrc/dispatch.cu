@@ -262,6 +262,53 @@ cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, cons
     return cudaLaunchKernelEx(&cfg, dispatch_kernel, a);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Dispatch without a caller workspace. Its scratch is this file-scope device array: the look-back
+// header (done flag), up to STATIC_LOOKBACK_CELLS look-back words and as many per-chunk counts.
+// Every GPU that loads the library holds it until the process exits; all calls share it.
+constexpr size_t STATIC_HDR = 256;
+constexpr size_t STATIC_SCRATCH_BYTES =
+    STATIC_HDR + (size_t)STATIC_LOOKBACK_CELLS * 8 + (size_t)STATIC_LOOKBACK_CELLS * 4;
+static __device__ __align__(256) unsigned char g_dispatch_scratch[STATIC_SCRATCH_BYTES];
+
+// Device address of g_dispatch_scratch on the current device, looked up once per device (host
+// code only sees a stand-in symbol; it must not hand that to a kernel).
+static cudaError_t static_scratch(unsigned char **out) {
+    static unsigned char *cache[64] = {nullptr};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (err != cudaSuccess) return err;
+        cache[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_idx,
+                                   int32_t *counts, int32_t *offsets, int32_t *sorted_token,
+                                   int32_t *slot_of, uint32_t *status, cudaStream_t s) {
+    unsigned char *scratch = nullptr;
+    cudaError_t err = static_scratch(&scratch);
+    if (err != cudaSuccess) return err;
+    const size_t cells = (size_t)dispatch_chunks(c) * (size_t)c.E;
+    DispatchBufs b;
+    b.counts = counts;
+    b.offsets = offsets;
+    b.sorted_token = sorted_token;
+    b.slot_of = slot_of;
+    b.flags = scratch;                                   // done flag + look-back words, zeroed
+    b.flags_bytes = STATIC_HDR + cells * 8;              // by launch_dispatch on every call
+    b.excl = reinterpret_cast<int32_t *>(scratch + STATIC_HDR + (size_t)STATIC_LOOKBACK_CELLS * 8);
+    // Without a caller status word, device-side failures land in the (cleared) header.
+    b.dev_status = status ? status : reinterpret_cast<uint32_t *>(scratch + 64);
+    return launch_dispatch(c, topk_idx, b, s);
+}
+
 cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
                            void *x_perm, uint32_t *dev_status, cudaStream_t s) {
     const int64_t P = c.T * c.k;

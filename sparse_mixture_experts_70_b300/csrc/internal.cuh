@@ -76,6 +76,12 @@ struct DispatchBufs {
 };
 cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
                             cudaStream_t s);
+// Dispatch whose scratch is a file-scope device array (no workspace); nchunks * E must not
+// exceed STATIC_LOOKBACK_CELLS.
+constexpr int64_t STATIC_LOOKBACK_CELLS = 65536;
+cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_idx,
+                                   int32_t *counts, int32_t *offsets, int32_t *sorted_token,
+                                   int32_t *slot_of, uint32_t *status, cudaStream_t s);
 cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
                            void *x_perm, uint32_t *dev_status, cudaStream_t s);
 cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,

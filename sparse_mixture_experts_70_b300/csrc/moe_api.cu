@@ -136,6 +136,27 @@ moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx
     return from_cuda(launch_permute(*cfg, h, sorted_token, x_perm, b.dev_status, s));
 }
 
+moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *topk_idx,
+                                       const void *h, int32_t *counts, int32_t *offsets,
+                                       int32_t *sorted_token, int32_t *slot_of, void *x_perm,
+                                       uint32_t *status, void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (dispatch_chunks(*cfg) * (int64_t)cfg->E > STATIC_LOOKBACK_CELLS) return MOE_ERR_WORKSPACE;
+    if (!aligned4(counts) || !aligned4(offsets) || (status && !aligned4(status)))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0) {
+        if (!aligned4(topk_idx) || !aligned4(sorted_token) || !aligned4(slot_of))
+            return MOE_ERR_INVALID_ARG;
+        if (x_perm && (!aligned16(x_perm) || !aligned16(h))) return MOE_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = from_cuda(launch_dispatch_static(*cfg, topk_idx, counts, offsets, sorted_token, slot_of,
+                                          status, s));
+    if (st != MOE_OK || !x_perm || cfg->T == 0) return st;
+    return from_cuda(launch_permute(*cfg, h, sorted_token, x_perm, status, s));
+}
+
 moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets,
                             const void *W1, const float *b1, const void *W3, const void *W2,
                             const float *b2, void *y_perm, void *ws, size_t ws_bytes,
