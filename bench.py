@@ -166,8 +166,8 @@ def run_reference(args, w) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="mixtral", choices=list(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -221,7 +221,7 @@ def main() -> None:
         # the five step calls (the same kernels moe_forward launches), with events around them
         if ev is not None:
             ev[0].record(stream)
-        B.moe_router_topk(cfg, h, dev["W_r"], dev["b_r"], idx, gates, psum, stream)
+        B.moe_router_topk(cfg, h, dev["W_r"], dev["b_r"], idx, gates, psum, ws, stream)
         B.moe_build_dispatch(cfg, idx, h, counts, offsets, sorted_token, slot_of, x_perm, ws,
                              stream)
         if ev is not None:

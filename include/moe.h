@@ -90,10 +90,12 @@ moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows);
  *   gates    [T, k] float  (out)    gate of each chosen expert (RENORM or RAW_PROB)
  *   psum_part [moe_router_partials rows, E] float (out) per-block sums of p over tokens, in a
  *            fixed order (input of moe_aux_loss).
- * Logits are accumulated in f32 from the stored h; exp is CUDA's expf. */
+ *   ws       workspace (moe_workspace_size bytes): for bf16 h and 32 < E <= 128 the router runs
+ *            on the tensor cores with W_r split exactly into three bf16 pieces stored in ws.
+ * Logits are accumulated in f32 from the stored h (every product exact); exp is CUDA's expf. */
 moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float *W_r,
                              const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
-                             void *stream);
+                             void *ws, size_t ws_bytes, void *stream);
 
 /* Step 3. Dispatch (lensaml.com "Mixture of Experts", Step 4 "Load Balancing": the histogram of
  * routing slots per expert; Step 5 "Capacity & Dropped Tokens": dropless grouping of any number

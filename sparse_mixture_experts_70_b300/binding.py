@@ -53,7 +53,7 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
             "moe_workspace_init": [_P, ctypes.c_size_t, _P],
             "moe_router_partials": [_CFG, ctypes.POINTER(ctypes.c_int64)],
-            "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P],
+            "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_build_dispatch": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_build_dispatch_static": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
             "moe_expert_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -141,9 +141,11 @@ def workspace(cfg: moe_config_t, device="cuda") -> torch.Tensor:
     return torch.zeros(max(moe_workspace_size(cfg), 1024), dtype=torch.uint8, device=device)
 
 
-def moe_router_topk(cfg, h, W_r, b_r, topk_idx, gates, psum_part, stream=None) -> None:
+def moe_router_topk(cfg, h, W_r, b_r, topk_idx, gates, psum_part, ws, stream=None) -> None:
     _check(lib().moe_router_topk(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(topk_idx),
-                                 _ptr(gates), _ptr(psum_part), _stream(stream)), "moe_router_topk")
+                                 _ptr(gates), _ptr(psum_part), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_router_topk")
 
 
 def moe_build_dispatch(cfg, topk_idx, h, counts, offsets, sorted_token, slot_of, x_perm, ws,

@@ -40,6 +40,7 @@ struct WsLayout {
     size_t disp_flags_bytes;
     size_t disp_excl;     // nchunks*E int32 (per-chunk exclusive counts)
     size_t psum;          // router partial sums [rows, E] f32
+    size_t router;        // router scratch (split weights of the tensor-core router)
     size_t topk_idx, gates, counts, offsets, sorted_token, slot_of, aux;
     size_t x_perm, H, y_perm;
     size_t total;
@@ -50,12 +51,13 @@ inline int64_t dispatch_chunks(const moe_config_t &c) {
     return (P + DISPATCH_THREADS - 1) / DISPATCH_THREADS;
 }
 
-int router_block_tokens(int E);  // tokens per router block (rows of psum_part per block)
-
-inline int64_t router_partial_rows(const moe_config_t &c) {
-    const int bt = router_block_tokens(c.E);
-    return (c.T + bt - 1) / bt;
-}
+// Rows of psum_part the router writes (one per router block; depends only on the shape).
+int64_t router_partial_rows(const moe_config_t &c);
+// Workspace bytes the router needs (the split router weights of the tensor-core path).
+size_t router_scratch_bytes(const moe_config_t &c);
+constexpr int ROUTER_TC_MAX_E = 128;   // tensor-core router: bf16 h, 32 < E <= 128
+constexpr int ROUTER_TC_TOKENS = 128;  // tokens per tensor-core router CTA
+size_t router_tc_scratch_bytes(const moe_config_t &c);
 
 WsLayout ws_layout(const moe_config_t &c);
 
@@ -65,7 +67,11 @@ int num_sms();
 // launchers (each returns the launch's cudaError_t)
 cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
                                const float *b_r, int32_t *topk_idx, float *gates,
-                               float *psum_part, cudaStream_t s);
+                               float *psum_part, void *scratch, uint32_t *dev_status,
+                               cudaStream_t s);
+cudaError_t launch_router_tc(const moe_config_t &c, const void *h, const float *W_r,
+                             const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
+                             void *scratch, uint32_t *dev_status, cudaStream_t s);
 
 struct DispatchBufs {
     int32_t *counts, *offsets, *sorted_token, *slot_of;

@@ -34,6 +34,7 @@ WsLayout ws_layout(const moe_config_t &c) {
     off = align_up(off + L.disp_flags_bytes);
     L.disp_excl = off;                    off = align_up(off + nch * E * 4);
     L.psum = off;                         off = align_up(off + (size_t)router_partial_rows(c) * E * 4);
+    L.router = off;                       off = align_up(off + router_scratch_bytes(c));
     L.topk_idx = off;                     off = align_up(off + P * 4);
     L.gates = off;                        off = align_up(off + P * 4);
     L.counts = off;                       off = align_up(off + E * 4);
@@ -101,14 +102,19 @@ moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows) {
 
 moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float *W_r,
                              const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
-                             void *stream) {
+                             void *ws, size_t ws_bytes, void *stream) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     if (cfg->T == 0) return MOE_OK;
     if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) || !aligned4(topk_idx) ||
         !aligned4(gates) || !aligned4(psum_part))
         return MOE_ERR_INVALID_ARG;
+    char *w = static_cast<char *>(ws);
     return from_cuda(launch_router_topk(*cfg, h, W_r, b_r, topk_idx, gates, psum_part,
+                                        w + L.router, reinterpret_cast<uint32_t *>(w + L.status),
                                         static_cast<cudaStream_t>(stream)));
 }
 
@@ -237,7 +243,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_
         if (e == cudaSuccess) e = cudaMemsetAsync(aux_out, 0, sizeof(float), s);
         return from_cuda(e);
     }
-    cudaError_t e = launch_router_topk(c, h, W_r, b_r, topk, gates, psum, s);
+    cudaError_t e = launch_router_topk(c, h, W_r, b_r, topk, gates, psum, w + L.router, dev_status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};

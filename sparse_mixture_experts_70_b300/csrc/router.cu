@@ -6,20 +6,26 @@
 // (Switch top-1). arjunjaggi.com "Mixture of Experts in LLMs", "Switch Transformers": the router
 // is kept in float32 while the rest runs in bfloat16.
 //
-// One block owns BT tokens and all E experts. Phase 1 is a register-blocked f32 contraction of
-// the [BT, d] activation tile with W_r [d, E] (both staged through shared memory in K-steps of
-// 32; every logit is a sequential FMA chain over i = 0..d-1). Phase 2 gives each warp one token:
-// max, sum of exponentials and k rounds of a warp arg-max (larger logit first, lower index on
-// equal logits), all by butterfly shuffles, so the result is deterministic. The block then sums
-// its tokens' probabilities per expert in token order into one row of psum_part, the input of
-// the auxiliary value.
+// Three kernels share the work by shape (the choice is a pure function of the shape, so
+// moe_router_partials can tell the caller how many partial-sum rows there will be):
+//   router_small_kernel  E <= 32 and W_r fits in shared memory: one warp per token, lanes across
+//                        d with 16-byte loads of h, W_r resident in shared memory in a
+//                        lane-interleaved layout (conflict-free 16-byte reads); the E partial sums
+//                        are folded across lanes by a butterfly then a reduce-scatter, leaving
+//                        lane e with logit e. Bandwidth-bound on h.
+//   router_tc_kernel     bf16 h and 32 < E <= 128: tensor cores (router_tc.cu).
+//   router_tile_kernel   everything else: a block owns BT tokens x all E experts and runs a
+//                        register-blocked f32 FMA contraction staged through shared memory.
+// All three end with the same per-token step: max, sum of exponentials and k rounds of arg-max
+// (larger logit first, lower index on equal logits), and per-block sums of p in token order
+// (one row of psum_part per block), the input of the auxiliary value.
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int RT_THREADS = 256;
-constexpr int DK = 32;  // K-step of the contraction
+constexpr int DK = 32;  // K-step of the tiled contraction
 
 template <typename Tin> __device__ __forceinline__ float to_f32(Tin v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
@@ -33,8 +39,175 @@ struct RouterArgs {
     int32_t *idx;
     float *gates, *psum;
     int64_t T;
-    int d, E, k, gate_mode;
+    int d, E, k, gate_mode, tokens_per_block;
 };
+
+// Per-token step shared by the CUDA-core kernels. Lane l holds the logits of experts
+// l + 32 m (m < MAXM, -inf where absent). Writes the k chosen experts and their gates and returns
+// zmax and the softmax denominator in every lane.
+template <int MAXM>
+__device__ __forceinline__ void route_token(const float (&v)[MAXM], int E, int k, int gate_mode,
+                                            int64_t tok, int32_t *idx, float *gates, float &zmax,
+                                            float &ssum) {
+    const int lane = threadIdx.x & 31;
+    zmax = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) zmax = fmaxf(zmax, v[m]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+    ssum = 0.f;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m)
+        if (lane + 32 * m < E) ssum += expf(v[m] - zmax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+
+    // k rounds of arg-max; lane j keeps the j-th winner.
+    uint32_t chosen = 0;
+    int sel_e = -1;
+    float sel_v = 0.f;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) {
+            const int e = lane + 32 * m;
+            if (e < E && !((chosen >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < be))) {
+                bv = v[m];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+        if (lane == j) { sel_e = be; sel_v = bv; }
+    }
+    float g;
+    if (gate_mode == MOE_GATE_RAW_PROB) {
+        g = expf(sel_v - zmax) / ssum;
+    } else {
+        const float ex = lane < k ? expf(sel_v - zmax) : 0.f;
+        float gs = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+        g = ex / gs;
+    }
+    if (lane < k) {
+        idx[tok * k + lane] = sel_e;
+        gates[tok * k + lane] = g;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// small E: warp per token, W_r resident in shared memory
+
+constexpr int SMALL_WARPS = 8;
+constexpr size_t SMALL_SMEM_MAX = 192 * 1024;
+
+__host__ __device__ inline int small_emax(int E) { return E <= 8 ? 8 : (E <= 16 ? 16 : 32); }
+
+// Eight consecutive inputs of one token, widened to f32 (one 16-byte load for bf16, two for f32).
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        x[2 * q] = __uint_as_float(w[q] << 16);
+        x[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Lane l of a warp covers inputs i = 256 j + 8 l + q (q < 8). W_r[i, e] (padded to EMAX experts)
+// sits at float4 index ((j * 8 + q) * EMAX/4 + e/4) * 32 + l, so the 32 lanes of a warp read 32
+// consecutive 16-byte words for every (j, q, e/4).
+template <typename Tin, int EMAX>
+__global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) {
+    extern __shared__ float4 w4[];
+    __shared__ float red[SMALL_WARPS][32];
+    constexpr int V = EMAX / 4;
+    const int E = a.E, d = a.d, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *wf = reinterpret_cast<float *>(w4);
+    for (int q = tid; q < d * EMAX; q += RT_THREADS) {
+        const int i = q / EMAX, e = q % EMAX;
+        const int j = i >> 8, l = (i >> 3) & 31, qq = i & 7;
+        wf[((((j * 8 + qq) * V + (e >> 2)) * 32 + l) << 2) + (e & 3)] =
+            e < E ? a.W_r[(int64_t)i * E + e] : 0.f;
+    }
+    __syncthreads();
+    const Tin *h = reinterpret_cast<const Tin *>(a.h);
+    const int nj = (d + 255) / 256;
+    const int64_t t_begin = (int64_t)blockIdx.x * a.tokens_per_block;
+    const int64_t t_end = min(a.T, t_begin + (int64_t)a.tokens_per_block);
+    const int my_e = lane & (EMAX - 1);
+    const float bias = (a.b_r && my_e < E) ? a.b_r[my_e] : 0.f;
+    float psum_lane = 0.f;
+    for (int64_t t = t_begin + warp; t < t_end; t += SMALL_WARPS) {
+        float acc[EMAX];
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+        const Tin *hrow = h + t * d;
+        for (int j = 0; j < nj; ++j) {
+            const int i0 = 256 * j + 8 * lane;
+            if (i0 < d) {
+                float x[8];
+                load8(hrow + i0, x);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const float4 w = w4[((j * 8 + q) * V + v) * 32 + lane];
+                        acc[4 * v + 0] = fmaf(x[q], w.x, acc[4 * v + 0]);
+                        acc[4 * v + 1] = fmaf(x[q], w.y, acc[4 * v + 1]);
+                        acc[4 * v + 2] = fmaf(x[q], w.z, acc[4 * v + 2]);
+                        acc[4 * v + 3] = fmaf(x[q], w.w, acc[4 * v + 3]);
+                    }
+                }
+            }
+        }
+        // Fold the lanes: butterfly over the lane bits >= EMAX, then a reduce-scatter over the
+        // lower bits; afterwards lane l holds logit (l & (EMAX - 1)).
+#pragma unroll
+        for (int o = 16; o >= EMAX; o >>= 1)
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+#pragma unroll
+        for (int o = EMAX / 2; o >= 1; o >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int m = 0; m < o; ++m) {
+                const float send = up ? acc[m] : acc[m + o];
+                const float keep = up ? acc[m + o] : acc[m];
+                acc[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        float v[1];
+        v[0] = (lane < EMAX && my_e < E) ? acc[0] + bias : -INFINITY;
+        float zmax, ssum;
+        route_token<1>(v, E, a.k, a.gate_mode, t, a.idx, a.gates, zmax, ssum);
+        if (lane < E) psum_lane += expf(v[0] - zmax) / ssum;
+    }
+    red[warp][lane] = psum_lane;
+    __syncthreads();
+    if (tid < E) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < SMALL_WARPS; ++w) s += red[w][tid];
+        a.psum[(int64_t)blockIdx.x * E + tid] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// general shapes: tiled f32 contraction
 
 // Tile geometry for E experts: threads form TR rows x TC columns, each computing RT tokens x RE
 // experts (experts strided by TC so that shared-memory reads of W_r are conflict-free).
@@ -51,7 +224,7 @@ __host__ __device__ inline Geo geometry(int E) {
 }
 
 template <int RT, int RE, typename Tin>
-__global__ void __launch_bounds__(RT_THREADS) router_topk_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
     extern __shared__ float sm[];
     const int E = a.E, d = a.d;
     const int TC = E / RE;
@@ -109,7 +282,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_topk_kernel(RouterArgs a) {
     }
     __syncthreads();
 
-    // Phase 2: one warp per token.
+    // one warp per token
     const int warp = tid >> 5, lane = tid & 31;
     constexpr int NW = RT_THREADS / 32;
     constexpr int MAXM = 8;  // E <= 256 -> at most 8 logits per lane
@@ -121,60 +294,13 @@ __global__ void __launch_bounds__(RT_THREADS) router_topk_kernel(RouterArgs a) {
             continue;
         }
         float v[MAXM];
-        float zmax = -INFINITY;
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             const int e = lane + 32 * m;
             v[m] = e < E ? zr[e] : -INFINITY;
-            zmax = fmaxf(zmax, v[m]);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-        float ssum = 0.f;
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m)
-            if (lane + 32 * m < E) ssum += expf(v[m] - zmax);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-
-        // k rounds of arg-max; lane j keeps the j-th winner.
-        uint32_t chosen = 0;
-        int sel_e = -1;
-        float sel_v = 0.f;
-        for (int j = 0; j < a.k; ++j) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int m = 0; m < MAXM; ++m) {
-                const int e = lane + 32 * m;
-                if (e < E && !((chosen >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < be))) {
-                    bv = v[m];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-            }
-            if ((be & 31) == lane) chosen |= 1u << (be >> 5);
-            if (lane == j) { sel_e = be; sel_v = bv; }
-        }
-        float g;
-        if (a.gate_mode == MOE_GATE_RAW_PROB) {
-            g = expf(sel_v - zmax) / ssum;
-        } else {
-            const float ex = lane < a.k ? expf(sel_v - zmax) : 0.f;
-            float gs = ex;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-            g = ex / gs;
-        }
-        if (lane < a.k) {
-            a.idx[tok * a.k + lane] = sel_e;
-            a.gates[tok * a.k + lane] = g;
-        }
+        float zmax, ssum;
+        route_token<MAXM>(v, E, a.k, a.gate_mode, tok, a.idx, a.gates, zmax, ssum);
         __syncwarp();
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
@@ -190,36 +316,90 @@ __global__ void __launch_bounds__(RT_THREADS) router_topk_kernel(RouterArgs a) {
     }
 }
 
-template <int RT, int RE, typename Tin>
-cudaError_t launch_t(const RouterArgs &a, int blocks, size_t smem, cudaStream_t s) {
-    auto kern = router_topk_kernel<RT, RE, Tin>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-    if (err != cudaSuccess) return err;
-    kern<<<blocks, RT_THREADS, smem, s>>>(a);
+template <typename K>
+cudaError_t launch_k(K kern, const RouterArgs &a, int64_t blocks, size_t smem, cudaStream_t s) {
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    kern<<<(unsigned)blocks, RT_THREADS, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+enum RouterPath { PATH_SMALL, PATH_TC, PATH_TILE };
+
+RouterPath router_path(const moe_config_t &c) {
+    if (c.E <= 32 && (size_t)c.d * small_emax(c.E) * 4 <= SMALL_SMEM_MAX) return PATH_SMALL;
+    if (c.dtype == MOE_BF16 && c.E > 32 && c.E <= ROUTER_TC_MAX_E) return PATH_TC;
+    return PATH_TILE;
+}
+
+// Tokens per block of the small kernel: about one block per SM, at least one token per warp.
+int small_tokens_per_block(int64_t T) {
+    int64_t tpb = (T + 147) / 148;
+    tpb = (tpb + SMALL_WARPS - 1) / SMALL_WARPS * SMALL_WARPS;
+    return (int)(tpb < SMALL_WARPS ? SMALL_WARPS : tpb);
 }
 
 }  // namespace
 
-int router_block_tokens(int E) { return geometry(E).BT; }
+int64_t router_partial_rows(const moe_config_t &c) {
+    switch (router_path(c)) {
+        case PATH_SMALL: {
+            const int tpb = small_tokens_per_block(c.T);
+            return (c.T + tpb - 1) / tpb;
+        }
+        case PATH_TC: return (c.T + ROUTER_TC_TOKENS - 1) / ROUTER_TC_TOKENS;
+        default: {
+            const int bt = geometry(c.E).BT;
+            return (c.T + bt - 1) / bt;
+        }
+    }
+}
+
+size_t router_scratch_bytes(const moe_config_t &c) {
+    return router_path(c) == PATH_TC ? router_tc_scratch_bytes(c) : 0;
+}
 
 cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
                                const float *b_r, int32_t *topk_idx, float *gates,
-                               float *psum_part, cudaStream_t s) {
+                               float *psum_part, void *scratch, uint32_t *dev_status,
+                               cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
+    RouterArgs a{h, W_r, b_r, topk_idx, gates, psum_part, c.T, c.d, c.E, c.k, c.gate, 0};
+    const RouterPath path = router_path(c);
+    if (path == PATH_TC)
+        return launch_router_tc(c, h, W_r, b_r, topk_idx, gates, psum_part, scratch, dev_status, s);
+    const bool bf16 = c.dtype == MOE_BF16;
+    if (path == PATH_SMALL) {
+        a.tokens_per_block = small_tokens_per_block(c.T);
+        const int emax = small_emax(c.E);
+        const size_t smem = (size_t)((c.d + 255) / 256) * 256 * emax * 4;
+        const int64_t blocks = (c.T + a.tokens_per_block - 1) / a.tokens_per_block;
+        switch (emax) {
+            case 8:
+                return bf16 ? launch_k(router_small_kernel<__nv_bfloat16, 8>, a, blocks, smem, s)
+                            : launch_k(router_small_kernel<float, 8>, a, blocks, smem, s);
+            case 16:
+                return bf16 ? launch_k(router_small_kernel<__nv_bfloat16, 16>, a, blocks, smem, s)
+                            : launch_k(router_small_kernel<float, 16>, a, blocks, smem, s);
+            default:
+                return bf16 ? launch_k(router_small_kernel<__nv_bfloat16, 32>, a, blocks, smem, s)
+                            : launch_k(router_small_kernel<float, 32>, a, blocks, smem, s);
+        }
+    }
     const Geo g = geometry(c.E);
     const int64_t blocks = (c.T + g.BT - 1) / g.BT;
     const size_t stage = sizeof(float) * ((size_t)g.BT * (DK + 1) + (size_t)DK * c.E);
     const size_t logits = sizeof(float) * (size_t)g.BT * c.E;
     const size_t smem = stage > logits ? stage : logits;
-    RouterArgs a{h, W_r, b_r, topk_idx, gates, psum_part, c.T, c.d, c.E, c.k, c.gate};
     const bool wide = g.RE == 4;
-    if (c.dtype == MOE_BF16)
-        return wide ? launch_t<8, 4, __nv_bfloat16>(a, (int)blocks, smem, s)
-                    : launch_t<1, 1, __nv_bfloat16>(a, (int)blocks, smem, s);
-    return wide ? launch_t<8, 4, float>(a, (int)blocks, smem, s)
-                : launch_t<1, 1, float>(a, (int)blocks, smem, s);
+    if (bf16)
+        return wide ? launch_k(router_tile_kernel<8, 4, __nv_bfloat16>, a, blocks, smem, s)
+                    : launch_k(router_tile_kernel<1, 1, __nv_bfloat16>, a, blocks, smem, s);
+    return wide ? launch_k(router_tile_kernel<8, 4, float>, a, blocks, smem, s)
+                : launch_k(router_tile_kernel<1, 1, float>, a, blocks, smem, s);
 }
 
 }  // namespace moe

@@ -39,7 +39,7 @@ def run_steps(w, inputs: dict, dev: dict | None = None) -> dict:
     y_perm = torch.empty((max(P, 1), d), dtype=dt, device="cuda")
     y = torch.empty((max(T, 1), d), dtype=dt, device="cuda")
     aux = torch.full((1,), -7.0, dtype=torch.float32, device="cuda")
-    B.moe_router_topk(cfg, dev["h"], dev["W_r"], dev["b_r"], idx, gates, psum)
+    B.moe_router_topk(cfg, dev["h"], dev["W_r"], dev["b_r"], idx, gates, psum, ws)
     B.moe_build_dispatch(cfg, idx, dev["h"], counts, offsets, sorted_token, slot_of, x_perm, ws)
     B.moe_expert_ffn(cfg, x_perm, offsets, dev["W1"], dev["b1"], dev["W3"], dev["W2"], dev["b2"],
                      y_perm, ws)

@@ -92,8 +92,10 @@ def test_null_and_misaligned_pointers_are_rejected_on_the_host():
                                 fake, n, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(cfg), fake, fake, fake, fake + 8, None) == \
         B.MOE_ERR_INVALID_ARG
-    assert L.moe_router_topk(ctypes.byref(cfg), fake, None, None, fake, fake, fake, None) == \
-        B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_topk(ctypes.byref(cfg), fake, None, None, fake, fake, fake, fake, n,
+                             None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_topk(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake, n - 1,
+                             None) == B.MOE_ERR_WORKSPACE
     assert L.moe_aux_loss(ctypes.byref(cfg), fake, fake, None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_device_status(None, None) == B.MOE_ERR_INVALID_ARG
 

@@ -29,6 +29,11 @@ SMALL = [
     wl.small("many_chunks", T=5000, d=64, f=64, E=64, k=4),
     wl.small("wide_E", T=700, d=128, f=128, E=256, k=8),
     wl.small("several_tiles", T=1100, d=512, f=768, E=3, k=2),
+    # router paths: tensor-core router with E padded to 48 and 112, small router with E = 20
+    wl.small("tc_router_E40", T=600, d=256, f=128, E=40, k=3, router_bias_var=1.0),
+    wl.small("tc_router_E100_raw_prob", T=300, d=128, f=128, E=100, k=1, act=G,
+             gate=wl.GATE_RAW_PROB),
+    wl.small("small_router_E20_f32", T=77, d=320, f=64, E=20, k=5, dtype="f32"),
 ]
 
 

@@ -23,7 +23,7 @@ def _dispatch_both(w):
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
     psum = torch.empty((rows, E), dtype=torch.float32, device="cuda")
-    B.moe_router_topk(cfg, h, W_r, b_r, idx, gates, psum)
+    B.moe_router_topk(cfg, h, W_r, b_r, idx, gates, psum, B.workspace(cfg))
     outs = []
     for use_static in (False, True):
         counts = torch.full((E,), -3, dtype=torch.int32, device="cuda")
