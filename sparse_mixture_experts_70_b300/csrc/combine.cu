@@ -46,69 +46,67 @@ template <> struct Vec8<float> {
     }
 };
 
-// y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :]: one warp per token, eight
-// elements per lane per step, f32 FMA in j order, rounded once to the output type.
+// y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :]: one thread per (token,
+// 8-element vector), consecutive threads along the row; f32 FMA in j order, one rounding.
 template <typename VT>
 __global__ void __launch_bounds__(256) combine_kernel(const void *__restrict__ y_perm,
                                                       const int32_t *__restrict__ slot_of,
                                                       const float *__restrict__ gates,
                                                       void *__restrict__ y, int64_t T, int64_t P,
                                                       int d, int k, uint32_t *dev_status) {
-    const int lane = threadIdx.x & 31;
     const int v8 = d / 8;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
-         t += warps) {
-        // k <= 32: lane j fetches slot j; the warp reads them back by shuffles.
-        int32_t my_row = 0;
-        float my_g = 0.f;
-        if (lane < k) {
-            my_row = __ldg(slot_of + t * k + lane);
-            my_g = __ldg(gates + t * k + lane);
-            if (my_row < 0 || my_row >= P) {
+    const int64_t units = T * v8;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = u / v8;
+        const int i = (int)(u - t * v8);
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int32_t row = __ldg(slot_of + t * k + j);
+            const float g = __ldg(gates + t * k + j);
+            if (row < 0 || row >= P) {
                 report(dev_status, DEV_ERR_INDEX);
-                my_row = 0;
-                my_g = 0.f;
+                continue;
             }
-        }
-        for (int i0 = 0; i0 < v8; i0 += 32) {
-            const int i = i0 + lane;
-            const bool ok = i < v8;
-            float acc[8];
+            Vec8<VT> v;
+            v.load(y_perm, (int64_t)row * v8 + i);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-            for (int j = 0; j < k; ++j) {
-                const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
-                const float gj = __shfl_sync(0xffffffffu, my_g, j);
-                if (ok) {
-                    Vec8<VT> v;
-                    v.load(y_perm, (int64_t)row * v8 + i);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[q] = fmaf(gj, v.get(q), acc[q]);
-                }
-            }
-            if (ok) Vec8<VT>::store(y, t * v8 + i, acc);
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, v.get(q), acc[q]);
         }
+        Vec8<VT>::store(y, u, acc);
     }
 }
 
-// aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T), reduced in a fixed order.
-__global__ void aux_kernel(const int32_t *__restrict__ counts, const float *__restrict__ psum,
-                           int64_t rows, int E, int64_t T, int k, float *aux_out) {
-    __shared__ double term[256];
-    const int e = threadIdx.x;
-    if (e < E) {
-        double s = 0.0;
-        for (int64_t b = 0; b < rows; ++b) s += (double)psum[b * E + e];
-        const double Pe = s / (double)T;
-        const double fe = (double)counts[e] / ((double)T * (double)k);
-        term[e] = fe * Pe;
+// aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T), reduced in a fixed order:
+// thread (g, e) of the block sums rows g, g + G, g + 2G, ... (G = 1024 / E groups), then thread e
+// adds the G group sums in g order, then thread 0 adds the E terms in e order.
+__global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ counts,
+                                                   const float *__restrict__ psum, int64_t rows,
+                                                   int E, int64_t T, int k, float *aux_out) {
+    __shared__ float part[1024];
+    __shared__ float term[256];
+    const int G = 1024 / E;
+    const int g = threadIdx.x / E, e = threadIdx.x % E;
+    if (g < G) {
+        float s = 0.f;
+        for (int64_t b = g; b < rows; b += G) s += __ldg(psum + b * E + e);
+        part[g * E + e] = s;
     }
     __syncthreads();
-    if (e == 0) {
-        double acc = 0.0;
+    if (threadIdx.x < E) {
+        float s = 0.f;
+        for (int q = 0; q < G; ++q) s += part[q * E + threadIdx.x];
+        const float Pe = s / (float)T;
+        const float fe = (float)counts[threadIdx.x] / ((float)T * (float)k);
+        term[threadIdx.x] = fe * Pe;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float acc = 0.f;
         for (int q = 0; q < E; ++q) acc += term[q];
-        *aux_out = T > 0 ? (float)((double)E * acc) : 0.f;
+        *aux_out = T > 0 ? (float)E * acc : 0.f;
     }
 }
 
@@ -117,8 +115,8 @@ __global__ void aux_kernel(const int32_t *__restrict__ counts, const float *__re
 cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
                            const float *gates, void *y, uint32_t *dev_status, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
-    int64_t blocks = (c.T + 7) / 8;
-    const int64_t cap = (int64_t)num_sms() * 16;
+    int64_t blocks = (c.T * (c.d / 8) + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     const int64_t P = c.T * c.k;
     if (c.dtype == MOE_BF16)
@@ -133,7 +131,7 @@ cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int3
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
                        float *aux_out, cudaStream_t s) {
     if (c.T == 0) return cudaMemsetAsync(aux_out, 0, sizeof(float), s);
-    aux_kernel<<<1, 256, 0, s>>>(counts, psum_part, router_partial_rows(c), c.E, c.T, c.k,
+    aux_kernel<<<1, 1024, 0, s>>>(counts, psum_part, router_partial_rows(c), c.E, c.T, c.k,
                                  aux_out);
     return cudaGetLastError();
 }

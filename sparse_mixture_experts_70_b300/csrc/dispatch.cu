@@ -90,6 +90,35 @@ __device__ __forceinline__ int chunk_ranks(const DispatchArgs &a, int c, int32_t
     return e;
 }
 
+// All slots fit in one chunk: histogram, scan over experts and scatter in one block, with no
+// look-back, flags or workspace.
+__global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(DispatchArgs a) {
+    __shared__ int32_t cnt[32 * 256];
+    __shared__ int32_t s_off[257];
+    const int tid = threadIdx.x, E = a.E;
+    int lrank, agg;
+    const int e = chunk_ranks(a, 0, cnt, &lrank, &agg);
+    if (tid < E) s_off[tid] = agg;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int q = 0; q < E; ++q) {
+            const int c = s_off[q];
+            a.counts[q] = c;
+            a.offsets[q] = run;
+            s_off[q] = run;
+            run += c;
+        }
+        a.offsets[E] = run;
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int pos = s_off[e] + lrank;
+        a.sorted_token[pos] = tid / a.k;
+        a.slot_of[tid] = pos;
+    }
+}
+
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchArgs a) {
     __shared__ int32_t cnt[32 * 256];
     __shared__ int32_t s_tot[257];
@@ -97,10 +126,14 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
     const int tid = threadIdx.x, E = a.E;
     if (tid == 0) s_abort = 0;
     __syncthreads();
+    // a block that owns exactly one chunk keeps its ranks for the scatter
+    const bool one_chunk = a.nchunks <= (int)gridDim.x;
+    int keep_e = -1, keep_rank = 0;
 
     for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
         int lrank, agg;
-        chunk_ranks(a, c, cnt, &lrank, &agg);
+        keep_e = chunk_ranks(a, c, cnt, &lrank, &agg);
+        keep_rank = lrank;
         if (tid < E) {
             unsigned long long *mine = a.words + (size_t)c * E + tid;
             int excl = 0;
@@ -175,8 +208,8 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
     __syncthreads();
 
     for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
-        int lrank, agg;
-        const int e = chunk_ranks(a, c, cnt, &lrank, &agg);
+        int lrank = keep_rank, agg;
+        const int e = one_chunk ? keep_e : chunk_ranks(a, c, cnt, &lrank, &agg);
         if (e >= 0) {
             const int64_t s = (int64_t)c * DISPATCH_THREADS + tid;
             const int64_t pos = (int64_t)s_off[e] + a.excl[(size_t)c * E + e] + lrank;
@@ -190,33 +223,55 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
     }
 }
 
-// x_perm[r, :] = h[sorted_token[r], :] -- one warp per destination row, 16-byte vectors.
+// x_perm[r, :] = h[sorted_token[r], :] -- one thread per (row, 16-byte vector), consecutive
+// threads along the row, four vectors per thread in flight.
 __global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ h,
                                                       const int32_t *__restrict__ sorted_token,
                                                       uint4 *__restrict__ x_perm, int64_t P,
                                                       int64_t T, int vecs, uint32_t *dev_status) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P;
-         r += warps) {
-        const int t = __ldg(sorted_token + r);
-        if (t < 0 || t >= T) {
-            if (lane == 0) report(dev_status, DEV_ERR_INDEX);
-            continue;
+    const int64_t units = P * vecs;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u0 < units;
+         u0 += 4 * stride) {
+        uint4 v[4];
+        int64_t dst[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t u = u0 + q * stride;
+            dst[q] = -1;
+            if (u < units) {
+                const int64_t r = u / vecs;
+                const int i = (int)(u - r * vecs);
+                const int t = __ldg(sorted_token + r);
+                if (t < 0 || t >= T) {
+                    report(dev_status, DEV_ERR_INDEX);
+                } else {
+                    v[q] = __ldg(h + (int64_t)t * vecs + i);
+                    dst[q] = u;
+                }
+            }
         }
-        const uint4 *src = h + (int64_t)t * vecs;
-        uint4 *dst = x_perm + r * vecs;
-        int i = lane;
-        for (; i + 96 < vecs; i += 128) {
-            const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 32);
-            const uint4 v2 = __ldg(src + i + 64), v3 = __ldg(src + i + 96);
-            dst[i] = v0; dst[i + 32] = v1; dst[i + 64] = v2; dst[i + 96] = v3;
-        }
-        for (; i < vecs; i += 32) dst[i] = __ldg(src + i);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (dst[q] >= 0) x_perm[dst[q]] = v[q];
     }
 }
 
 }  // namespace
+
+int dispatch_blocks_per_sm() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel,
+                                                          DISPATCH_THREADS, 0) != cudaSuccess)
+            return 0;
+        cache[dev] = per_sm;
+    }
+    return cache[dev];
+}
 
 cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
                             cudaStream_t s) {
@@ -226,8 +281,6 @@ cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, cons
         if (err != cudaSuccess) return err;
         return cudaMemsetAsync(b.offsets, 0, sizeof(int32_t) * (c.E + 1), s);
     }
-    cudaError_t err = cudaMemsetAsync(b.flags, 0, b.flags_bytes, s);
-    if (err != cudaSuccess) return err;
     DispatchArgs a;
     a.idx = topk_idx;
     a.counts = b.counts;
@@ -242,10 +295,13 @@ cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, cons
     a.k = c.k;
     a.E = c.E;
     a.nchunks = (int)dispatch_chunks(c);
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel,
-                                                        DISPATCH_THREADS, 0);
+    if (a.nchunks == 1) {
+        dispatch_single_kernel<<<1, DISPATCH_THREADS, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaError_t err = cudaMemsetAsync(b.flags, 0, b.flags_bytes, s);
     if (err != cudaSuccess) return err;
+    const int per_sm = dispatch_blocks_per_sm();
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)per_sm * num_sms();
     if (grid > a.nchunks) grid = a.nchunks;
@@ -315,8 +371,8 @@ cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *
     if (P == 0) return cudaSuccess;
     const int es = c.dtype == MOE_BF16 ? 2 : 4;
     const int vecs = c.d * es / 16;
-    int64_t blocks = (P + 7) / 8;
-    const int64_t cap = (int64_t)num_sms() * 16;
+    int64_t blocks = (P * vecs + 1023) / 1024;
+    const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     permute_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(h), sorted_token,
                                                     static_cast<uint4 *>(x_perm), P, c.T, vecs,

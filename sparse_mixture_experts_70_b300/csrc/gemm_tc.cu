@@ -19,8 +19,10 @@
 //               when its MMAs have read it, and hands a finished accumulator to the epilogue.
 //               Warp 1 also owns the 512-column TMEM allocation (two 128 x 256 f32 accumulators,
 //               so the epilogue of tile i overlaps the MMAs of tile i + 1).
-//   warps 2-5   epilogue: tcgen05.ld of the thread's accumulator row (TMEM lane = row),
-//               bias / GELU / SwiGLU in f32, round to bf16, masked 16-byte stores.
+//   warps 2-9   epilogue, two warps per TMEM lane quarter (each converts half of the tile's
+//               columns): tcgen05.ld of the thread's accumulator row (TMEM lane = row), bias /
+//               GELU / SwiGLU in f32 on the special-function unit, round to bf16, masked 16-byte
+//               stores.
 // Tile order: expert-major, then N tile, then M tile, so the CTAs in flight at any moment share a
 // few weight tiles (read once from HBM, then from L2) and one expert's activations.
 // Rows of an expert's last M tile that belong to the next expert (or lie past the end, which TMA
@@ -37,7 +39,7 @@ using namespace tc;
 constexpr int BM = GEMM_BM, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KiB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KiB
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CTL_BYTES = 4096;
 constexpr size_t TC_SMEM = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + CTL_BYTES;
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         for (int q = 0; q < 2; ++q) {
             mbar_init(bar_tfull + 8 * q, 1);
-            mbar_init(bar_tempty + 8 * q, 128);
+            mbar_init(bar_tempty + 8 * q, 256);
         }
         mbar_init(bar_drain, 1);
         *s_abort = 0;
@@ -212,7 +214,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_wait(bar_drain, 0, nullptr, a.dev_status);
         }
     } else {
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;  // which half of the tile's columns it converts
         const int r = q * 32 + lane;
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
             if (a.epi == EPI_SWIGLU) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
+                for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
                     float x1[32], x3[32];
                     tmem_ld32x2(trow + c, trow + BN / 2 + c, x1, x3);
                     const int col = ti.n * (BN / 2) + c;
@@ -237,8 +240,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16(silu(x1[2 * i]) * x3[2 * i],
-                                              silu(x1[2 * i + 1]) * x3[2 * i + 1]);
+                            pk[i] = pack_bf16(silu_fast(x1[2 * i]) * x3[2 * i],
+                                              silu_fast(x1[2 * i + 1]) * x3[2 * i + 1]);
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
                     const int col = ti.n * BN + c;
                     if (col >= a.N) break;  // warp-uniform
                     float v[32];
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     if (a.epi == EPI_GELU) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_fast(v[i]);
                     }
                     if (valid) {
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
@@ -312,9 +315,7 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
     if (grid > upper) grid = upper;
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)TC_SMEM);
+    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel, TC_SMEM);
     if (err != cudaSuccess) return err;
     grouped_gemm_tc_kernel<<<(unsigned)grid, TC_THREADS, TC_SMEM, s>>>(mA, mB, mB3, a);
     return cudaGetLastError();

@@ -62,6 +62,10 @@ size_t router_tc_scratch_bytes(const moe_config_t &c);
 WsLayout ws_layout(const moe_config_t &c);
 
 int num_sms();
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device, size).
+cudaError_t set_max_dynamic_smem(const void *kernel, size_t bytes);
+// Resident blocks per SM of the dispatch kernel on the current device (queried once).
+int dispatch_blocks_per_sm();
 
 // ------------------------------------------------------------------------------------------
 // launchers (each returns the launch's cudaError_t)

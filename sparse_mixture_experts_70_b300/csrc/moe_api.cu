@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace moe {
@@ -17,6 +19,33 @@ int num_sms() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
     if (dev >= 0 && dev < 64) cache[dev] = n;
     return n;
+}
+
+cudaError_t set_max_dynamic_smem(const void *kernel, size_t bytes) {
+    struct Entry {
+        const void *kernel;
+        int dev;
+        size_t bytes;
+    };
+    static Entry table[64];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (table[i].kernel == kernel && table[i].dev == dev && table[i].bytes >= bytes)
+            return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err != cudaSuccess) return err;
+    for (int i = 0; i < used; ++i)
+        if (table[i].kernel == kernel && table[i].dev == dev) {
+            table[i].bytes = bytes;
+            return cudaSuccess;
+        }
+    if (used < 64) table[used++] = Entry{kernel, dev, bytes};
+    return cudaSuccess;
 }
 
 static size_t align_up(size_t x) { return (x + 1023) & ~(size_t)1023; }

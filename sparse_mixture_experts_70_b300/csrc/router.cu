@@ -6,8 +6,10 @@
 // (Switch top-1). arjunjaggi.com "Mixture of Experts in LLMs", "Switch Transformers": the router
 // is kept in float32 while the rest runs in bfloat16.
 //
-// Three kernels share the work by shape (the choice is a pure function of the shape, so
+// Four kernels share the work by shape (the choice is a pure function of the shape, so
 // moe_router_partials can tell the caller how many partial-sum rows there will be):
+//   router_splitd_kernel E <= 32 and few tokens: one token per block, the warps split d and read
+//                        W_r from L2 (latency-bound shapes such as decode).
 //   router_small_kernel  E <= 32 and W_r fits in shared memory: one warp per token, lanes across
 //                        d with 16-byte loads of h, W_r resident in shared memory in a
 //                        lane-interleaved layout (conflict-free 16-byte reads); the E partial sums
@@ -16,7 +18,7 @@
 //   router_tc_kernel     bf16 h and 32 < E <= 128: tensor cores (router_tc.cu).
 //   router_tile_kernel   everything else: a block owns BT tokens x all E experts and runs a
 //                        register-blocked f32 FMA contraction staged through shared memory.
-// All three end with the same per-token step: max, sum of exponentials and k rounds of arg-max
+// All four end with the same per-token step: max, sum of exponentials and k rounds of arg-max
 // (larger logit first, lower index on equal logits), and per-block sums of p in token order
 // (one row of psum_part per block), the input of the auxiliary value.
 #include "internal.cuh"
@@ -137,11 +139,32 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
     constexpr int V = EMAX / 4;
     const int E = a.E, d = a.d, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *wf = reinterpret_cast<float *>(w4);
-    for (int q = tid; q < d * EMAX; q += RT_THREADS) {
-        const int i = q / EMAX, e = q % EMAX;
-        const int j = i >> 8, l = (i >> 3) & 31, qq = i & 7;
-        wf[((((j * 8 + qq) * V + (e >> 2)) * 32 + l) << 2) + (e & 3)] =
-            e < E ? a.W_r[(int64_t)i * E + e] : 0.f;
+    if (E == EMAX) {
+        // one float4 of W_r (4 experts of one input row) lands in one float4 slot; 8 in flight
+        const int n4 = d * EMAX / 4;
+        const float4 *src = reinterpret_cast<const float4 *>(a.W_r);
+        for (int q0 = tid; q0 < n4; q0 += 8 * RT_THREADS) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (q0 + u * RT_THREADS < n4) v[u] = __ldg(src + q0 + u * RT_THREADS);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = q0 + u * RT_THREADS;
+                if (q < n4) {
+                    const int i = q / V, vv = q % V;
+                    const int j = i >> 8, l = (i >> 3) & 31, qq = i & 7;
+                    w4[((j * 8 + qq) * V + vv) * 32 + l] = v[u];
+                }
+            }
+        }
+    } else {
+        for (int q = tid; q < d * EMAX; q += RT_THREADS) {
+            const int i = q / EMAX, e = q % EMAX;
+            const int j = i >> 8, l = (i >> 3) & 31, qq = i & 7;
+            wf[((((j * 8 + qq) * V + (e >> 2)) * 32 + l) << 2) + (e & 3)] =
+                e < E ? a.W_r[(int64_t)i * E + e] : 0.f;
+        }
     }
     __syncthreads();
     const Tin *h = reinterpret_cast<const Tin *>(a.h);
@@ -156,20 +179,28 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
         const Tin *hrow = h + t * d;
-        for (int j = 0; j < nj; ++j) {
-            const int i0 = 256 * j + 8 * lane;
-            if (i0 < d) {
-                float x[8];
-                load8(hrow + i0, x);
+        for (int j0 = 0; j0 < nj; j0 += 4) {
+            // four 8-element groups of h in flight per lane
+            float x[4][8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+            for (int u = 0; u < 4; ++u) {
+                const int i0 = 256 * (j0 + u) + 8 * lane;
+                if (j0 + u < nj && i0 < d) load8(hrow + i0, x[u]);
+            }
 #pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        const float4 w = w4[((j * 8 + q) * V + v) * 32 + lane];
-                        acc[4 * v + 0] = fmaf(x[q], w.x, acc[4 * v + 0]);
-                        acc[4 * v + 1] = fmaf(x[q], w.y, acc[4 * v + 1]);
-                        acc[4 * v + 2] = fmaf(x[q], w.z, acc[4 * v + 2]);
-                        acc[4 * v + 3] = fmaf(x[q], w.w, acc[4 * v + 3]);
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u;
+                if (j < nj && 256 * j + 8 * lane < d) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            const float4 w = w4[((j * 8 + q) * V + v) * 32 + lane];
+                            acc[4 * v + 0] = fmaf(x[u][q], w.x, acc[4 * v + 0]);
+                            acc[4 * v + 1] = fmaf(x[u][q], w.y, acc[4 * v + 1]);
+                            acc[4 * v + 2] = fmaf(x[u][q], w.z, acc[4 * v + 2]);
+                            acc[4 * v + 3] = fmaf(x[u][q], w.w, acc[4 * v + 3]);
+                        }
                     }
                 }
             }
@@ -203,6 +234,77 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
 #pragma unroll
         for (int w = 0; w < SMALL_WARPS; ++w) s += red[w][tid];
         a.psum[(int64_t)blockIdx.x * E + tid] = s;
+    }
+}
+
+// Few tokens: one token per block, the 8 warps take the 256-wide slices of d in turn and read
+// W_r straight from L2 (it is shared by all blocks), so no block pays for staging W_r; the warps'
+// partial logits meet in shared memory and warp 0 finishes the token. psum_part gets one row per
+// token.
+template <typename Tin, int EMAX>
+__global__ void __launch_bounds__(RT_THREADS) router_splitd_kernel(RouterArgs a) {
+    __shared__ float part[SMALL_WARPS][EMAX];
+    const int E = a.E, d = a.d, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = blockIdx.x;
+    const Tin *hrow = reinterpret_cast<const Tin *>(a.h) + t * d;
+    const int nj = (d + 255) / 256;
+    const bool vec = (E & 3) == 0;
+    float acc[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+    for (int j = warp; j < nj; j += SMALL_WARPS) {
+        const int i0 = 256 * j + 8 * lane;
+        if (i0 >= d) continue;
+        float x[8];
+        load8(hrow + i0, x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float *wrow = a.W_r + (int64_t)(i0 + q) * E;
+            if (vec) {
+#pragma unroll
+                for (int v = 0; v < EMAX / 4; ++v) {
+                    if (4 * v < E) {
+                        const float4 w = __ldg(reinterpret_cast<const float4 *>(wrow) + v);
+                        acc[4 * v + 0] = fmaf(x[q], w.x, acc[4 * v + 0]);
+                        acc[4 * v + 1] = fmaf(x[q], w.y, acc[4 * v + 1]);
+                        acc[4 * v + 2] = fmaf(x[q], w.z, acc[4 * v + 2]);
+                        acc[4 * v + 3] = fmaf(x[q], w.w, acc[4 * v + 3]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e)
+                    if (e < E) acc[e] = fmaf(x[q], __ldg(wrow + e), acc[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= EMAX; o >>= 1)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+#pragma unroll
+    for (int o = EMAX / 2; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int m = 0; m < o; ++m) {
+            const float send = up ? acc[m] : acc[m + o];
+            const float keep = up ? acc[m + o] : acc[m];
+            acc[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    if (lane < EMAX) part[warp][lane] = acc[0];
+    __syncthreads();
+    if (warp == 0) {
+        float z = 0.f;
+        if (lane < EMAX) {
+#pragma unroll
+            for (int w = 0; w < SMALL_WARPS; ++w) z += part[w][lane];
+        }
+        float v[1];
+        v[0] = (lane < EMAX && lane < E) ? z + (a.b_r ? a.b_r[lane] : 0.f) : -INFINITY;
+        float zmax, ssum;
+        route_token<1>(v, E, a.k, a.gate_mode, t, a.idx, a.gates, zmax, ssum);
+        if (lane < E) a.psum[t * E + lane] = expf(v[0] - zmax) / ssum;
     }
 }
 
@@ -319,18 +421,22 @@ __global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
 template <typename K>
 cudaError_t launch_k(K kern, const RouterArgs &a, int64_t blocks, size_t smem, cudaStream_t s) {
     if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+        cudaError_t err = set_max_dynamic_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
     }
     kern<<<(unsigned)blocks, RT_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-enum RouterPath { PATH_SMALL, PATH_TC, PATH_TILE };
+enum RouterPath { PATH_SPLITD, PATH_SMALL, PATH_TC, PATH_TILE };
 
 RouterPath router_path(const moe_config_t &c) {
-    if (c.E <= 32 && (size_t)c.d * small_emax(c.E) * 4 <= SMALL_SMEM_MAX) return PATH_SMALL;
+    // few tokens: every block reads all of W_r from L2; keep that traffic within 64 MiB
+    if (c.E <= 32 && c.T <= 1024 &&
+        (double)c.T * c.d * small_emax(c.E) * 4 <= 64.0 * 1024 * 1024)
+        return PATH_SPLITD;
+    if (c.E <= 32 && (size_t)((c.d + 255) / 256) * 256 * small_emax(c.E) * 4 <= SMALL_SMEM_MAX)
+        return PATH_SMALL;
     if (c.dtype == MOE_BF16 && c.E > 32 && c.E <= ROUTER_TC_MAX_E) return PATH_TC;
     return PATH_TILE;
 }
@@ -346,6 +452,7 @@ int small_tokens_per_block(int64_t T) {
 
 int64_t router_partial_rows(const moe_config_t &c) {
     switch (router_path(c)) {
+        case PATH_SPLITD: return c.T;
         case PATH_SMALL: {
             const int tpb = small_tokens_per_block(c.T);
             return (c.T + tpb - 1) / tpb;
@@ -372,6 +479,19 @@ cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float
     if (path == PATH_TC)
         return launch_router_tc(c, h, W_r, b_r, topk_idx, gates, psum_part, scratch, dev_status, s);
     const bool bf16 = c.dtype == MOE_BF16;
+    if (path == PATH_SPLITD) {
+        switch (small_emax(c.E)) {
+            case 8:
+                return bf16 ? launch_k(router_splitd_kernel<__nv_bfloat16, 8>, a, c.T, 0, s)
+                            : launch_k(router_splitd_kernel<float, 8>, a, c.T, 0, s);
+            case 16:
+                return bf16 ? launch_k(router_splitd_kernel<__nv_bfloat16, 16>, a, c.T, 0, s)
+                            : launch_k(router_splitd_kernel<float, 16>, a, c.T, 0, s);
+            default:
+                return bf16 ? launch_k(router_splitd_kernel<__nv_bfloat16, 32>, a, c.T, 0, s)
+                            : launch_k(router_splitd_kernel<float, 32>, a, c.T, 0, s);
+        }
+    }
     if (path == PATH_SMALL) {
         a.tokens_per_block = small_tokens_per_block(c.T);
         const int emax = small_emax(c.E);

@@ -168,6 +168,20 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 }
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
+// Epilogue forms on the special-function unit: tanh.approx.f32 (max relative error about 2^-11)
+// and ex2.approx through __expf. Both errors sit below the bf16 rounding (2^-9) that the hidden
+// activations H receive right after, and they keep the epilogue shorter than a tile's MMAs.
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_tanh_fast(float x) {
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    return 0.5f * x * (1.f + tanh_approx(u));
+}
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
 
 // ---------------------------------------------------------------------------------------------
 // host side: 2-D bf16 tensor maps
