@@ -49,6 +49,11 @@ def lib() -> ctypes.CDLL:
         L.oracle_combine.argtypes = [I64, I32, I32, P, P, P]
         L.oracle_forward_rows.argtypes = [I64, P, I32, I32, I32, I32, P, I32, P, P, P, P, P, I32,
                                           P, P, P]
+        L.oracle_forward_rows_kept.argtypes = [I64, P, I32, I32, I32, I32, P, I32, P, P, P, P, P,
+                                               I32, P, P, P, P]
+        L.oracle_capacity.argtypes = [D, I64, I32, I32]
+        L.oracle_capacity.restype = I64
+        L.oracle_dispatch_capacity.argtypes = [I64, I32, I32, P, I64, P, P, P, P]
         L.oracle_aux_loss.argtypes = [I64, I32, I32, P, P]
         L.oracle_aux_loss.restype = D
         L.oracle_param_count.argtypes = [I32, I64, I64, I32, I32, I32, I64, I64, I32, P, P]
@@ -159,6 +164,23 @@ def dispatch(idx: np.ndarray, E: int):
     return counts, offsets, sorted_token, slot_of
 
 
+def capacity(factor: float, T: int, k: int, E: int) -> int:
+    return int(lib().oracle_capacity(float(factor), T, k, E))
+
+
+def dispatch_capacity(idx: np.ndarray, E: int, C: int):
+    """Dispatch with a per-expert capacity C (C < 0: no limit); slot_of is -1 for dropped slots."""
+    idx = _np(idx, np.int32)
+    T, k = idx.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    sorted_token = np.full(T * k, -1, np.int32)
+    slot_of = np.empty(T * k, np.int32)
+    lib().oracle_dispatch_capacity(T, E, k, _ptr(idx), int(C), _ptr(counts), _ptr(offsets),
+                                   _ptr(sorted_token), _ptr(slot_of))
+    return counts, offsets, sorted_token, slot_of
+
+
 def _weights(W1, W3, W2):
     w1, wdt = _stored(W1)
     w2, wdt2 = _stored(W2)
@@ -194,7 +216,9 @@ def combine(g: np.ndarray, yslot: np.ndarray) -> np.ndarray:
     return y
 
 
-def forward_rows(tokens, h, idx, g, W1, W3, W2, b1=None, b2=None, act: int = SWIGLU):
+def forward_rows(tokens, h, idx, g, W1, W3, W2, b1=None, b2=None, act: int = SWIGLU,
+                 keep=None):
+    """Layer output rows of `tokens`; keep [T, k] (optional) marks the slots an expert processes."""
     tokens = _np(tokens, np.int64)
     hs, hdt = _stored(h)
     d = hs.shape[1]
@@ -206,8 +230,14 @@ def forward_rows(tokens, h, idx, g, W1, W3, W2, b1=None, b2=None, act: int = SWI
     b1c, b2c = _f32(b1), _f32(b2)
     n = tokens.shape[0]
     y = np.empty((n, d), np.float64)
-    lib().oracle_forward_rows(n, _ptr(tokens), d, f, k, act, _ptr(hs), hdt, _ptr(idx), _ptr(g),
-                              _ptr(w1), _ptr(w3), _ptr(w2), wdt, _ptr(b1c), _ptr(b2c), _ptr(y))
+    if keep is None:
+        lib().oracle_forward_rows(n, _ptr(tokens), d, f, k, act, _ptr(hs), hdt, _ptr(idx), _ptr(g),
+                                  _ptr(w1), _ptr(w3), _ptr(w2), wdt, _ptr(b1c), _ptr(b2c), _ptr(y))
+    else:
+        kp = _np(keep, np.uint8)
+        lib().oracle_forward_rows_kept(n, _ptr(tokens), d, f, k, act, _ptr(hs), hdt, _ptr(idx),
+                                       _ptr(g), _ptr(w1), _ptr(w3), _ptr(w2), wdt, _ptr(b1c),
+                                       _ptr(b2c), _ptr(kp), _ptr(y))
     return y
 
 
@@ -246,14 +276,21 @@ def gate_code(w) -> int:
 
 
 def route(w, inputs) -> dict:
-    """Router, top-k, gates, dispatch and auxiliary value over all T tokens of workload w."""
+    """Router, top-k, gates, dispatch and auxiliary value over all T tokens of workload w
+    (with the workload's capacity limit when it has one)."""
     z, p = router(inputs["h"], inputs["W_r"], inputs.get("b_r"))
     idx, bnd, ins = topk(z, w.k)
     g = gates(z, p, idx, gate_code(w))
-    counts, offsets, sorted_token, slot_of = dispatch(idx, w.E)
+    factor = getattr(w, "capacity_factor", 0.0)
+    if factor > 0:
+        C = capacity(factor, w.T, w.k, w.E)
+        counts, offsets, sorted_token, slot_of = dispatch_capacity(idx, w.E, C)
+    else:
+        C = -1
+        counts, offsets, sorted_token, slot_of = dispatch(idx, w.E)
     aux = aux_loss(counts, p, w.k)
     return dict(z=z, p=p, idx=idx, boundary=bnd, inset=ins, g=g, counts=counts, offsets=offsets,
-                sorted_token=sorted_token, slot_of=slot_of, aux=aux)
+                sorted_token=sorted_token, slot_of=slot_of, aux=aux, capacity=C)
 
 
 def reference(w, inputs, tokens=None) -> dict:
@@ -263,8 +300,9 @@ def reference(w, inputs, tokens=None) -> dict:
         tokens = np.arange(w.T, dtype=np.int64)
     tokens = np.asarray(tokens, dtype=np.int64)
     r["tokens"] = tokens
+    keep = None if r["capacity"] < 0 else (r["slot_of"] >= 0).reshape(w.T, w.k)
     r["y"] = forward_rows(tokens, inputs["h"], r["idx"], r["g"], inputs["W1"], inputs.get("W3"),
-                          inputs["W2"], inputs.get("b1"), inputs.get("b2"), act_code(w))
+                          inputs["W2"], inputs.get("b1"), inputs.get("b2"), act_code(w), keep=keep)
     return r
 
 

@@ -32,7 +32,10 @@
  *   - Activation "GELU" is the tanh form 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))).
  *   - SwiGLU expert: W2 (SiLU(W1 x) * (W3 x)), no biases; SiLU(x) = x / (1 + e^-x).
  *   - Grouping order: a stable counting sort of the flattened slots s = t k + j by expert,
- *     i.e. (expert ascending, token ascending); nothing is dropped.
+ *     i.e. (expert ascending, token ascending); nothing is dropped unless a capacity is given.
+ *   - Capacity ([LENSA-5]): C = floor(factor T k / E); an expert keeps the first C of its slots
+ *     in that order; a dropped slot contributes nothing and the kept gates are not renormalised;
+ *     the auxiliary value uses the routed (pre-drop) counts.
  *
  * Precision: inputs are read exactly as stored (f32, or bf16 widened bit-exactly) and every sum,
  * product and transcendental is taken in double, in index order, with no intermediate rounding.
@@ -166,6 +169,45 @@ void oracle_dispatch(int64_t T, int32_t E, int32_t k, const int32_t *idx, int32_
     free(cursor);
 }
 
+/* [LENSA-5] capacity: every expert gets a buffer of C = factor x T x k / E slots; routing slots
+ * beyond it are skipped by the expert. Reading: C is rounded down, and within an expert the first
+ * C slots in stable token order are kept (the grouping order of oracle_dispatch).
+ *   counts[e]   slots routed to e (the demand, before dropping)
+ *   offsets     exclusive prefix sum of min(counts[e], C); offsets[E] = slots kept
+ *   sorted_token / slot_of as in oracle_dispatch for kept slots; slot_of[s] = -1 when dropped.
+ * C < 0 means no capacity limit (the dropless dispatch). */
+int64_t oracle_capacity(double factor, int64_t T, int32_t k, int32_t E)
+{
+    return (int64_t)floor(factor * (double)T * (double)k / (double)E);
+}
+
+void oracle_dispatch_capacity(int64_t T, int32_t E, int32_t k, const int32_t *idx, int64_t C,
+                              int32_t *counts, int32_t *offsets, int32_t *sorted_token,
+                              int32_t *slot_of)
+{
+    const int64_t P = T * k;
+    int64_t *rank = (int64_t *)calloc((size_t)(E > 0 ? E : 1), sizeof(int64_t));
+    for (int32_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t s = 0; s < P; ++s) counts[idx[s]] += 1;
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        const int64_t kept = (C >= 0 && counts[e] > C) ? C : counts[e];
+        offsets[e + 1] = offsets[e] + (int32_t)kept;
+    }
+    for (int64_t s = 0; s < P; ++s) {
+        const int32_t e = idx[s];
+        const int64_t r = rank[e]++;
+        if (C >= 0 && r >= C) {
+            slot_of[s] = -1;
+        } else {
+            const int64_t pos = offsets[e] + r;
+            sorted_token[pos] = (int32_t)(s / k);
+            slot_of[s] = (int32_t)pos;
+        }
+    }
+    free(rank);
+}
+
 /* GELU in its tanh form and SiLU, in double. */
 static double gelu_tanh(double x)
 {
@@ -239,11 +281,14 @@ void oracle_combine(int64_t n, int32_t k, int32_t d, const double *g, const doub
 }
 
 /* The layer output of the listed tokens: y[r] = sum_j g[t,j] FFN_{idx[t,j]}(h[t]) with t = tokens[r].
- * Each output row depends only on its own token, so any subset of tokens can be evaluated. */
-void oracle_forward_rows(int64_t n, const int64_t *tokens, int32_t d, int32_t f, int32_t k,
-                         int32_t act, const void *h, int32_t h_dtype, const int32_t *idx,
-                         const double *g, const void *W1, const void *W3, const void *W2,
-                         int32_t w_dtype, const float *b1, const float *b2, double *y)
+ * Each output row depends only on its own token, so any subset of tokens can be evaluated.
+ * keep (may be NULL) marks the routing slots t*k+j that an expert processes; a slot that is not
+ * kept (dropped by the capacity limit, [LENSA-5]) contributes nothing. */
+void oracle_forward_rows_kept(int64_t n, const int64_t *tokens, int32_t d, int32_t f, int32_t k,
+                              int32_t act, const void *h, int32_t h_dtype, const int32_t *idx,
+                              const double *g, const void *W1, const void *W3, const void *W2,
+                              int32_t w_dtype, const float *b1, const float *b2,
+                              const unsigned char *keep, double *y)
 {
     const int64_t nk = n * k;
     double *x = (double *)malloc(sizeof(double) * (size_t)(nk * d + 1));
@@ -255,12 +300,21 @@ void oracle_forward_rows(int64_t n, const int64_t *tokens, int32_t d, int32_t f,
         for (int32_t j = 0; j < k; ++j) {
             for (int32_t i = 0; i < d; ++i) x[(r * k + j) * d + i] = widen(h, h_dtype, t * d + i);
             ex[r * k + j] = idx[t * k + j];
-            gs[r * k + j] = g[t * k + j];
+            gs[r * k + j] = (keep && !keep[t * k + j]) ? 0.0 : g[t * k + j];
         }
     }
     oracle_expert_ffn(nk, d, f, act, x, ex, W1, W3, W2, w_dtype, b1, b2, ys);
     oracle_combine(n, k, d, gs, ys, y);
     free(x); free(ys); free(gs); free(ex);
+}
+
+void oracle_forward_rows(int64_t n, const int64_t *tokens, int32_t d, int32_t f, int32_t k,
+                         int32_t act, const void *h, int32_t h_dtype, const int32_t *idx,
+                         const double *g, const void *W1, const void *W3, const void *W2,
+                         int32_t w_dtype, const float *b1, const float *b2, double *y)
+{
+    oracle_forward_rows_kept(n, tokens, d, f, k, act, h, h_dtype, idx, g, W1, W3, W2, w_dtype, b1,
+                             b2, NULL, y);
 }
 
 /* [LENSA-4]: E . sum_e f_e P_e with f_e = counts[e] / (T k) and P_e = (1/T) sum_t p[t,e]

@@ -428,3 +428,82 @@ def test_many_small_routing_is_skewed_with_idle_experts():
     assert r["counts"].sum() == w.P
     assert (r["counts"] == 0).sum() >= 1
     assert r["counts"].max() > 4 * w.P / w.E
+
+
+# ---------------------------------------------------------------------------------------------
+# capacity and dropped slots (lensaml.com explainer, Step 5)
+
+def _routing_with_demand(demand, T):
+    labels = np.repeat(np.arange(len(demand)), demand)
+    assert len(labels) == 2 * T and max(demand) <= T
+    return np.stack([labels[:T], labels[T:]], axis=1).astype(np.int32)
+
+
+def test_capacity_reproduces_printed_step5_example(golden):
+    g = golden("lensa_step5_capacity.txt")
+    T, k, E = int(g["T"]), int(g["k"]), int(g["E"])
+    C = oracle.capacity(g["factor"], T, k, E)
+    assert C == g["capacity"] == 64
+    kept_printed = [int(x) for x in g["kept"]]
+    demand = [kk + int(o) for kk, o in zip(kept_printed, g["overflow"])]
+    assert demand == [104, 104, 78, 55, 50, 46, 50, 25] and sum(demand) == T * k
+    idx = _routing_with_demand(demand, T)
+    counts, offsets, st, so = oracle.dispatch_capacity(idx, E, C)
+    assert counts.tolist() == demand
+    assert np.diff(offsets).tolist() == kept_printed
+    dropped = int((so < 0).sum())
+    assert dropped == g["dropped"] == 94
+    assert round(dropped / (T * k), 3) == g["dropped_share"]
+
+
+@pytest.mark.parametrize("factor", [0.25, 0.5, 1.0, 1.25, 2.0])
+def test_capacity_keeps_the_first_C_slots_in_token_order(factor):
+    rng = np.random.default_rng(int(factor * 100))
+    T, E, k = 300, 6, 2
+    z = rng.standard_normal((T, E)) + np.array([2.0, 1.0, 0.5, 0, 0, -1.0])
+    idx, _, _ = oracle.topk(z, k)
+    C = oracle.capacity(factor, T, k, E)
+    assert C == int(np.floor(factor * T * k / E))
+    counts, offsets, st, so = oracle.dispatch_capacity(idx, E, C)
+    flat = idx.reshape(-1)
+    np.testing.assert_array_equal(counts, np.bincount(flat, minlength=E))
+    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(np.minimum(counts, C))]))
+    for e in range(E):
+        slots = [s for s in range(T * k) if flat[s] == e]      # token order
+        kept, dropped = slots[:C], slots[C:]
+        assert [so[s] for s in kept] == list(range(offsets[e], offsets[e] + len(kept)))
+        assert all(so[s] == -1 for s in dropped)
+        assert st[offsets[e]:offsets[e + 1]].tolist() == [s // k for s in kept]
+
+
+def test_capacity_unlimited_equals_dropless_and_zero_drops_all():
+    rng = np.random.default_rng(21)
+    idx, _, _ = oracle.topk(rng.standard_normal((77, 9)), 3)
+    ref = oracle.dispatch(idx, 9)
+    big = oracle.dispatch_capacity(idx, 9, 77 * 3)
+    none = oracle.dispatch_capacity(idx, 9, -1)
+    for a, b, c in zip(ref, big, none):
+        np.testing.assert_array_equal(a, b)
+        np.testing.assert_array_equal(a, c)
+    counts, offsets, st, so = oracle.dispatch_capacity(idx, 9, 0)
+    np.testing.assert_array_equal(counts, ref[0])
+    assert offsets[-1] == 0 and (so == -1).all()
+
+
+def test_dropped_slots_contribute_nothing():
+    w = wl.small(T=50, d=16, f=32, E=4, k=2, act=wl.ACT_GELU_TANH, dtype="f32", has_bias=True,
+                 router_bias_var=4.0, capacity_factor=0.75)
+    inp = wl.random_biases(w, wl.generate(w), seed=9)
+    ref = oracle.reference(w, inp)
+    keep = (ref["slot_of"] >= 0).reshape(w.T, w.k)
+    assert 0 < keep.sum() < w.P
+    hx = inp["h"].numpy().astype(np.float64)
+    for t in range(w.T):
+        ys = oracle.expert_ffn(np.repeat(hx[t:t + 1], 2, 0), ref["idx"][t], inp["W1"], None,
+                               inp["W2"], inp["b1"], inp["b2"], act=oracle.GELU_TANH)
+        expect = (ref["g"][t] * keep[t]) @ ys
+        np.testing.assert_allclose(ref["y"][t], expect, rtol=1e-13, atol=1e-14)
+        if not keep[t].any():
+            assert (ref["y"][t] == 0).all()
+    # the auxiliary value uses the routed (pre-drop) counts
+    assert ref["counts"].sum() == w.P
