@@ -59,7 +59,13 @@ enum { MOE_GATE_RENORM = 0, MOE_GATE_RAW_PROB = 1 };
  *        MOE_ACT_SWIGLU    : expert(x) = W2 (SiLU(W1 x) * (W3 x))       (3 matrices, no biases)
  *   gate MOE_GATE_RENORM   : g = softmax over the chosen logits (Mixtral form, sums to 1)
  *        MOE_GATE_RAW_PROB : g = p, the full-softmax probability (Switch top-1 form)
- *   has_bias : expert biases b1 [E, f] and b2 [E, d] (float) are present; GELU form only. */
+ *   has_bias : expert biases b1 [E, f] and b2 [E, d] (float) are present; GELU form only.
+ *   capacity_factor : 0 = dropless. > 0: every expert processes at most
+ *            C = floor(capacity_factor * T * k / E) routing slots -- the first C in token order --
+ *            and the other slots are dropped: they contribute nothing to y (a token whose slots
+ *            are all dropped gets y = 0, its residual passing around the layer), the kept gates
+ *            are not renormalised, and the auxiliary value still uses the routed counts
+ *            (lensaml.com "Mixture of Experts", Step 5 "Capacity & Dropped Tokens"). */
 typedef struct {
     int64_t T;
     int32_t d, f, E, k;
@@ -67,6 +73,7 @@ typedef struct {
     int32_t act;
     int32_t gate;
     int32_t has_bias;
+    float capacity_factor;
 } moe_config_t;
 
 /* Bytes of workspace every call below needs for `cfg` (the largest of their needs, so one
@@ -102,9 +109,13 @@ moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float
  * of tokens per expert). A stable counting sort of the slots s = t*k + j by topk_idx[s]:
  *   counts       [E]    int32 (out)  slots routed to each expert
  *   offsets      [E+1]  int32 (out)  exclusive prefix sum of counts; offsets[E] = T k
+ *                                    (with a capacity C: of min(counts, C); offsets[E] = kept)
  *   sorted_token [T k]  int32 (out)  token of each sorted row, order (expert, token) ascending
- *   slot_of      [T k]  int32 (out)  sorted row of slot s (the inverse permutation)
- *   x_perm       [T k, d] dtype (out, may be NULL): x_perm[r] = h[sorted_token[r]]
+ *                                    (rows [0, offsets[E]) are written)
+ *   slot_of      [T k]  int32 (out)  sorted row of slot s (the inverse permutation); -1 for a
+ *                                    slot dropped by the capacity
+ *   x_perm       [T k, d] dtype (out, may be NULL): x_perm[r] = h[sorted_token[r]] for the
+ *                                    offsets[E] kept rows
  *   h            [T, d] dtype, read only when x_perm is not NULL.
  * One cooperative kernel (histogram without atomics, decoupled look-back scan over blocks) and,
  * when x_perm is given, one gather kernel. Bit-exact and deterministic. */
@@ -152,7 +163,7 @@ moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const i
 
 /* Step 5a. Gate-weighted combine (lensaml.com "Mixture of Experts", Step 3: y = sum g . E(h)):
  *   y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :], in f32, j ascending, then
- *   rounded to dtype.  y [T, d] dtype (out). */
+ *   rounded to dtype; slots with slot_of = -1 (dropped) are skipped.  y [T, d] dtype (out). */
 moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int32_t *slot_of,
                          const float *gates, void *y, void *stream);
 

@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const void *__restrict__ y
         for (int j = 0; j < k; ++j) {
             const int32_t row = __ldg(slot_of + t * k + j);
             const float g = __ldg(gates + t * k + j);
+            if (row == -1) continue;  // dropped by the capacity: contributes nothing
             if (row < 0 || row >= P) {
                 report(dev_status, DEV_ERR_INDEX);
                 continue;

@@ -36,6 +36,7 @@ struct DispatchArgs {
     uint32_t *dev_status;
     int64_t P;
     int k, E, nchunks;
+    int64_t cap;  // per-expert capacity, -1 when dropless
 };
 
 __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
@@ -107,15 +108,19 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(Di
             a.counts[q] = c;
             a.offsets[q] = run;
             s_off[q] = run;
-            run += c;
+            run += (a.cap >= 0 && c > a.cap) ? (int)a.cap : c;
         }
         a.offsets[E] = run;
     }
     __syncthreads();
     if (e >= 0) {
-        const int pos = s_off[e] + lrank;
-        a.sorted_token[pos] = tid / a.k;
-        a.slot_of[tid] = pos;
+        if (a.cap >= 0 && lrank >= a.cap) {
+            a.slot_of[tid] = -1;  // over capacity: dropped
+        } else {
+            const int pos = s_off[e] + lrank;
+            a.sorted_token[pos] = tid / a.k;
+            a.slot_of[tid] = pos;
+        }
     }
 }
 
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
                 for (int e = 0; e < E; ++e) {
                     a.counts[e] = s_tot[e];
                     a.offsets[e] = run;
-                    run += s_tot[e];
+                    run += (a.cap >= 0 && s_tot[e] > a.cap) ? (int)a.cap : s_tot[e];
                 }
                 a.offsets[E] = run;
                 __threadfence();
@@ -212,8 +217,11 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
         const int e = one_chunk ? keep_e : chunk_ranks(a, c, cnt, &lrank, &agg);
         if (e >= 0) {
             const int64_t s = (int64_t)c * DISPATCH_THREADS + tid;
-            const int64_t pos = (int64_t)s_off[e] + a.excl[(size_t)c * E + e] + lrank;
-            if (pos >= 0 && pos < a.P) {
+            const int64_t rank = (int64_t)a.excl[(size_t)c * E + e] + lrank;  // within expert e
+            const int64_t pos = (int64_t)s_off[e] + rank;
+            if (a.cap >= 0 && rank >= a.cap) {
+                a.slot_of[s] = -1;  // over capacity: dropped
+            } else if (pos >= 0 && pos < a.P) {
                 a.sorted_token[pos] = (int32_t)(s / a.k);
                 a.slot_of[s] = (int32_t)pos;
             } else {
@@ -227,9 +235,16 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
 // threads along the row, four vectors per thread in flight.
 __global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ h,
                                                       const int32_t *__restrict__ sorted_token,
-                                                      uint4 *__restrict__ x_perm, int64_t P,
-                                                      int64_t T, int vecs, uint32_t *dev_status) {
-    const int64_t units = P * vecs;
+                                                      uint4 *__restrict__ x_perm,
+                                                      const int32_t *__restrict__ rows_kept,
+                                                      int64_t P, int64_t T, int vecs,
+                                                      uint32_t *dev_status) {
+    int64_t rows = __ldg(rows_kept);
+    if (rows < 0 || rows > P) {
+        report(dev_status, DEV_ERR_INDEX);
+        rows = 0;
+    }
+    const int64_t units = rows * vecs;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u0 < units;
          u0 += 4 * stride) {
@@ -295,6 +310,7 @@ cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, cons
     a.k = c.k;
     a.E = c.E;
     a.nchunks = (int)dispatch_chunks(c);
+    a.cap = capacity_of(c);
     if (a.nchunks == 1) {
         dispatch_single_kernel<<<1, DISPATCH_THREADS, 0, s>>>(a);
         return cudaGetLastError();
@@ -366,7 +382,8 @@ cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_id
 }
 
 cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
-                           void *x_perm, uint32_t *dev_status, cudaStream_t s) {
+                           const int32_t *offsets, void *x_perm, uint32_t *dev_status,
+                           cudaStream_t s) {
     const int64_t P = c.T * c.k;
     if (P == 0) return cudaSuccess;
     const int es = c.dtype == MOE_BF16 ? 2 : 4;
@@ -375,8 +392,8 @@ cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     permute_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(h), sorted_token,
-                                                    static_cast<uint4 *>(x_perm), P, c.T, vecs,
-                                                    dev_status);
+                                                    static_cast<uint4 *>(x_perm), offsets + c.E, P,
+                                                    c.T, vecs, dev_status);
     return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "moe.h"
@@ -45,6 +46,13 @@ struct WsLayout {
     size_t x_perm, H, y_perm;
     size_t total;
 };
+
+// Per-expert capacity in routing slots: floor(factor T k / E), or -1 when dropless.
+inline int64_t capacity_of(const moe_config_t &c) {
+    if (!(c.capacity_factor > 0.f)) return -1;
+    const double C = (double)c.capacity_factor * (double)c.T * (double)c.k / (double)c.E;
+    return (int64_t)floor(C);
+}
 
 inline int64_t dispatch_chunks(const moe_config_t &c) {
     const int64_t P = c.T * c.k;
@@ -92,8 +100,10 @@ constexpr int64_t STATIC_LOOKBACK_CELLS = 65536;
 cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_idx,
                                    int32_t *counts, int32_t *offsets, int32_t *sorted_token,
                                    int32_t *slot_of, uint32_t *status, cudaStream_t s);
+// Rows copied: offsets[E] (read on the device; fewer than T k when a capacity drops slots).
 cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
-                           void *x_perm, uint32_t *dev_status, cudaStream_t s);
+                           const int32_t *offsets, void *x_perm, uint32_t *dev_status,
+                           cudaStream_t s);
 cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
                            const float *gates, void *y, uint32_t *dev_status, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,

@@ -1,6 +1,7 @@
 // moe_api.cu -- the extern "C" entry points declared in include/moe.h: argument checks, the
 // workspace layout, and the launch sequence of the layer forward. No allocation, no global state
 // beyond a per-device cache of the SM count.
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -96,6 +97,7 @@ moe_status_t check_cfg(const moe_config_t *c) {
     if (c->gate != MOE_GATE_RENORM && c->gate != MOE_GATE_RAW_PROB) return MOE_ERR_UNSUPPORTED;
     if (c->k > 32) return MOE_ERR_UNSUPPORTED;
     if (c->has_bias && c->act == MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    if (!(c->capacity_factor >= 0.f) || !isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -168,7 +170,7 @@ moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx
                    reinterpret_cast<uint32_t *>(w + L.status)};
     st = from_cuda(launch_dispatch(*cfg, topk_idx, b, s));
     if (st != MOE_OK || !x_perm || cfg->T == 0) return st;
-    return from_cuda(launch_permute(*cfg, h, sorted_token, x_perm, b.dev_status, s));
+    return from_cuda(launch_permute(*cfg, h, sorted_token, offsets, x_perm, b.dev_status, s));
 }
 
 moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *topk_idx,
@@ -189,7 +191,7 @@ moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *t
     st = from_cuda(launch_dispatch_static(*cfg, topk_idx, counts, offsets, sorted_token, slot_of,
                                           status, s));
     if (st != MOE_OK || !x_perm || cfg->T == 0) return st;
-    return from_cuda(launch_permute(*cfg, h, sorted_token, x_perm, status, s));
+    return from_cuda(launch_permute(*cfg, h, sorted_token, offsets, x_perm, status, s));
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets,
@@ -277,7 +279,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
     if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_permute(c, h, sorted_token, x_perm, dev_status, s)) != cudaSuccess)
+    if ((e = launch_permute(c, h, sorted_token, offsets, x_perm, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
     e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);

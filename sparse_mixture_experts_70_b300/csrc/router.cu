@@ -174,58 +174,75 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
     const int my_e = lane & (EMAX - 1);
     const float bias = (a.b_r && my_e < E) ? a.b_r[my_e] : 0.f;
     float psum_lane = 0.f;
-    for (int64_t t = t_begin + warp; t < t_end; t += SMALL_WARPS) {
-        float acc[EMAX];
+    // Each warp takes two tokens at a time: every W_r read from shared memory feeds both.
+    for (int64_t t = t_begin + 2 * warp; t < t_end; t += 2 * SMALL_WARPS) {
+        const bool two = t + 1 < t_end;
+        float acc[2][EMAX];
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
-        const Tin *hrow = h + t * d;
-        for (int j0 = 0; j0 < nj; j0 += 4) {
-            // four 8-element groups of h in flight per lane
-            float x[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i0 = 256 * (j0 + u) + 8 * lane;
-                if (j0 + u < nj && i0 < d) load8(hrow + i0, x[u]);
+        for (int e = 0; e < EMAX; ++e) acc[0][e] = acc[1][e] = 0.f;
+        const Tin *hrow0 = h + t * d;
+        const Tin *hrow1 = two ? hrow0 + d : hrow0;
+        // software pipeline: the loads of slice j + 1 are in flight while slice j is computed
+        // (two register buffers, the loop unrolled by two so that both stay in registers)
+        float xa[2][8], xb[2][8];
+        auto load_slice = [&](int j, float (&xx)[2][8]) {
+            const int i0 = 256 * j + 8 * lane;
+            if (j < nj && i0 < d) {
+                load8(hrow0 + i0, xx[0]);
+                load8(hrow1 + i0, xx[1]);
             }
+        };
+        auto fma_slice = [&](int j, const float (&xx)[2][8]) {
+            if (j < nj && 256 * j + 8 * lane < d) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u;
-                if (j < nj && 256 * j + 8 * lane < d) {
+                for (int q = 0; q < 8; ++q) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int v = 0; v < V; ++v) {
+                        const float4 w = w4[((j * 8 + q) * V + v) * 32 + lane];
 #pragma unroll
-                        for (int v = 0; v < V; ++v) {
-                            const float4 w = w4[((j * 8 + q) * V + v) * 32 + lane];
-                            acc[4 * v + 0] = fmaf(x[u][q], w.x, acc[4 * v + 0]);
-                            acc[4 * v + 1] = fmaf(x[u][q], w.y, acc[4 * v + 1]);
-                            acc[4 * v + 2] = fmaf(x[u][q], w.z, acc[4 * v + 2]);
-                            acc[4 * v + 3] = fmaf(x[u][q], w.w, acc[4 * v + 3]);
+                        for (int tt = 0; tt < 2; ++tt) {
+                            acc[tt][4 * v + 0] = fmaf(xx[tt][q], w.x, acc[tt][4 * v + 0]);
+                            acc[tt][4 * v + 1] = fmaf(xx[tt][q], w.y, acc[tt][4 * v + 1]);
+                            acc[tt][4 * v + 2] = fmaf(xx[tt][q], w.z, acc[tt][4 * v + 2]);
+                            acc[tt][4 * v + 3] = fmaf(xx[tt][q], w.w, acc[tt][4 * v + 3]);
                         }
                     }
                 }
             }
+        };
+        load_slice(0, xa);
+        for (int j = 0; j < nj; j += 2) {
+            load_slice(j + 1, xb);
+            fma_slice(j, xa);
+            load_slice(j + 2, xa);
+            fma_slice(j + 1, xb);
         }
-        // Fold the lanes: butterfly over the lane bits >= EMAX, then a reduce-scatter over the
-        // lower bits; afterwards lane l holds logit (l & (EMAX - 1)).
 #pragma unroll
-        for (int o = 16; o >= EMAX; o >>= 1)
+        for (int tt = 0; tt < 2; ++tt) {
+            if (tt == 1 && !two) break;  // warp-uniform
+            float *av = acc[tt];
+            // Fold the lanes: butterfly over the lane bits >= EMAX, then a reduce-scatter over
+            // the lower bits; afterwards lane l holds logit (l & (EMAX - 1)).
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+            for (int o = 16; o >= EMAX; o >>= 1)
 #pragma unroll
-        for (int o = EMAX / 2; o >= 1; o >>= 1) {
-            const bool up = (lane & o) != 0;
+                for (int e = 0; e < EMAX; ++e) av[e] += __shfl_xor_sync(0xffffffffu, av[e], o);
 #pragma unroll
-            for (int m = 0; m < o; ++m) {
-                const float send = up ? acc[m] : acc[m + o];
-                const float keep = up ? acc[m + o] : acc[m];
-                acc[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            for (int o = EMAX / 2; o >= 1; o >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int m = 0; m < o; ++m) {
+                    const float send = up ? av[m] : av[m + o];
+                    const float keep = up ? av[m + o] : av[m];
+                    av[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
             }
+            float v[1];
+            v[0] = (lane < EMAX && my_e < E) ? av[0] + bias : -INFINITY;
+            float zmax, ssum;
+            route_token<1>(v, E, a.k, a.gate_mode, t + tt, a.idx, a.gates, zmax, ssum);
+            if (lane < E) psum_lane += expf(v[0] - zmax) / ssum;
         }
-        float v[1];
-        v[0] = (lane < EMAX && my_e < E) ? acc[0] + bias : -INFINITY;
-        float zmax, ssum;
-        route_token<1>(v, E, a.k, a.gate_mode, t, a.idx, a.gates, zmax, ssum);
-        if (lane < E) psum_lane += expf(v[0] - zmax) / ssum;
     }
     red[warp][lane] = psum_lane;
     __syncthreads();
@@ -441,11 +458,11 @@ RouterPath router_path(const moe_config_t &c) {
     return PATH_TILE;
 }
 
-// Tokens per block of the small kernel: about one block per SM, at least one token per warp.
+// Tokens per block of the small kernel: about one block per SM, two tokens per warp at least.
 int small_tokens_per_block(int64_t T) {
     int64_t tpb = (T + 147) / 148;
-    tpb = (tpb + SMALL_WARPS - 1) / SMALL_WARPS * SMALL_WARPS;
-    return (int)(tpb < SMALL_WARPS ? SMALL_WARPS : tpb);
+    tpb = (tpb + 2 * SMALL_WARPS - 1) / (2 * SMALL_WARPS) * (2 * SMALL_WARPS);
+    return (int)(tpb < 2 * SMALL_WARPS ? 2 * SMALL_WARPS : tpb);
 }
 
 }  // namespace

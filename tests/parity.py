@@ -75,22 +75,24 @@ def routing_agreement(ref: dict, idx_gpu: np.ndarray) -> np.ndarray:
     return diff
 
 
-def check_dispatch_valid(idx: np.ndarray, E: int, counts, offsets, sorted_token, slot_of) -> None:
-    """The dispatch of routing `idx` is the stable counting sort: checked by its properties."""
+def check_dispatch_valid(idx: np.ndarray, E: int, counts, offsets, sorted_token, slot_of,
+                         C: int = -1) -> None:
+    """The dispatch of routing `idx` (capacity C, -1 for none) is the stable counting sort that
+    keeps the first C slots of every expert: checked by its properties."""
     T, k = idx.shape
     P = T * k
     flat = idx.reshape(-1)
     np.testing.assert_array_equal(counts, np.bincount(flat, minlength=E))
-    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
-    assert np.array_equal(np.sort(slot_of), np.arange(P))
-    np.testing.assert_array_equal(sorted_token[slot_of], np.arange(P) // k)
-    # stable: within an expert, sorted rows follow slot order
-    order = np.argsort(slot_of)
-    e_sorted = flat[order]
-    assert np.all(np.diff(e_sorted) >= 0)
+    kept_counts = counts if C < 0 else np.minimum(counts, C)
+    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(kept_counts)]))
+    kept = slot_of >= 0
+    assert np.array_equal(np.sort(slot_of[kept]), np.arange(offsets[-1]))
+    np.testing.assert_array_equal(sorted_token[slot_of[kept]], np.nonzero(kept)[0] // k)
     for e in range(E):
-        seg = order[offsets[e]:offsets[e + 1]]
-        assert np.all(np.diff(seg) > 0)
+        slots = np.nonzero(flat == e)[0]            # token order
+        lim = len(slots) if C < 0 else min(C, len(slots))
+        np.testing.assert_array_equal(slot_of[slots[:lim]], np.arange(offsets[e], offsets[e] + lim))
+        assert (slot_of[slots[lim:]] == -1).all()
 
 
 def rel_l2(a: np.ndarray, b: np.ndarray) -> float:

@@ -59,6 +59,9 @@ def test_workspace_sizes_of_the_workloads(name):
     (dict(gate=3), B.MOE_ERR_UNSUPPORTED),
     (dict(E=64, k=33), B.MOE_ERR_UNSUPPORTED),     # k > 32 not built
     (dict(has_bias=True), B.MOE_ERR_UNSUPPORTED),  # SwiGLU has no biases
+    (dict(capacity_factor=-1.0), B.MOE_ERR_INVALID_ARG),
+    (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
+    (dict(capacity_factor=float("inf")), B.MOE_ERR_INVALID_ARG),
 ])
 def test_invalid_configs_are_rejected(kw, expect):
     base = dict(T=64, d=128, f=256, E=8, k=2, dtype=B.MOE_BF16, act=B.MOE_ACT_SWIGLU,

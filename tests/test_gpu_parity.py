@@ -34,6 +34,15 @@ SMALL = [
     wl.small("tc_router_E100_raw_prob", T=300, d=128, f=128, E=100, k=1, act=G,
              gate=wl.GATE_RAW_PROB),
     wl.small("small_router_E20_f32", T=77, d=320, f=64, E=20, k=5, dtype="f32"),
+    # capacity factor (drops): single-chunk and multi-chunk dispatch, f32 and bf16, everything
+    # dropped (C = 0)
+    wl.small("capacity_skewed_k2", T=800, d=128, f=256, E=8, k=2, router_bias_var=4.0,
+             capacity_factor=1.0),
+    wl.small("capacity_switch_gelu", T=3000, d=128, f=128, E=16, k=1, act=G,
+             gate=wl.GATE_RAW_PROB, has_bias=True, router_bias_var=2.0, capacity_factor=1.25),
+    wl.small("capacity_f32", T=200, d=64, f=128, E=4, k=2, dtype="f32", router_bias_var=2.0,
+             capacity_factor=0.5),
+    wl.small("capacity_zero", T=100, d=64, f=64, E=8, k=2, capacity_factor=0.02),
 ]
 
 
@@ -52,15 +61,16 @@ def _check_steps(w, inputs, ref, got):
     np.testing.assert_allclose(got["gates"].numpy()[keep], ref["g"][keep], rtol=0, atol=GATE_ABS)
     counts, offsets = got["counts"].numpy(), got["offsets"].numpy()
     st, so = got["sorted_token"].numpy(), got["slot_of"].numpy()
+    kept = int(offsets[-1])
     if len(diff) == 0:
         np.testing.assert_array_equal(counts, ref["counts"])
         np.testing.assert_array_equal(offsets, ref["offsets"])
-        np.testing.assert_array_equal(st, ref["sorted_token"])
+        np.testing.assert_array_equal(st[:kept], ref["sorted_token"][:kept])
         np.testing.assert_array_equal(so, ref["slot_of"])
     else:
-        check_dispatch_valid(idx, w.E, counts, offsets, st, so)
+        check_dispatch_valid(idx, w.E, counts, offsets, st, so, ref["capacity"])
     # the permute is a copy: bit-exact
-    assert torch.equal(got["x_perm"], inputs["h"][torch.from_numpy(st).long()])
+    assert torch.equal(got["x_perm"][:kept], inputs["h"][torch.from_numpy(st[:kept]).long()])
     assert got["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
     return diff
 
@@ -86,8 +96,14 @@ def test_small_cases_step_by_step(w):
     dev = to_dev(inputs)
     got = run_steps(w, inputs, dev)
     diff = _check_steps(w, inputs, ref, got)
-    rows = np.arange(w.P) if w.P <= 4096 else np.unique(np.linspace(0, w.P - 1, 2048).astype(int))
-    _check_expert_rows(w, inputs, got, rows)
+    kept = int(got["offsets"][-1])
+    rows = np.arange(kept) if kept <= 4096 else np.unique(np.linspace(0, kept - 1, 2048).astype(int))
+    if kept:
+        _check_expert_rows(w, inputs, got, rows)
+    if w.capacity_factor > 0:
+        print(f"{w.name}: capacity {ref['capacity']}, kept {kept} of {w.P} slots")
+        if kept == 0:
+            assert (got["y"].float() == 0).all()
     check_layer_output(w, ref, got["y"], skip_tokens=diff)
     # the fused call runs the same kernels: identical bits
     fw = run_forward(w, dev)
