@@ -186,15 +186,12 @@ def main() -> None:
         return
 
     from sparse_mixture_experts_70_b300 import binding as B
+    from sparse_mixture_experts_70_b300 import dist as D
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = D.env()
     torch.cuda.set_device(local)
-    dist = None
     if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        D.init("nccl", torch.device("cuda", local))
 
     peaks = _peaks()
     cfg = B.config_for(w)
@@ -246,16 +243,14 @@ def main() -> None:
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
-        if dist:
-            dist.barrier()
+        D.barrier()
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         stop.record(stream)
         torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+        D.barrier()
     clocks = clk.summary()
     ms = start.elapsed_time(stop) / args.steps
     ffn_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
@@ -283,8 +278,7 @@ def main() -> None:
     torch.cuda.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_stop = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
+    D.barrier()
     e_start.record(stream)
     for _ in range(args.steps):
         e2e_step()
@@ -294,16 +288,11 @@ def main() -> None:
     if B.moe_device_status(layer.ws) != B.MOE_OK:
         raise SystemExit("device status after e2e region")
 
-    if dist:
-        t = torch.tensor([ms, e_ms, ffn_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e_ms, ffn_ms = t.tolist()
+    ms, e_ms, ffn_ms = D.max_over_ranks([ms, e_ms, ffn_ms], device="cuda")
     if rank != 0:
-        if dist:
-            dist.destroy_process_group()
+        D.shutdown()
         return
 
-    tokens = T * world
     flops = w.expert_flops()
     tflops = flops / (ffn_ms * 1e-3) / 1e12
     peak = peaks["bf16_sustained"]
@@ -311,7 +300,7 @@ def main() -> None:
     launches_per_step = 7
     line = {
         "metric": METRIC,
-        "value": tokens / (ms * 1e-3),
+        "value": D.job_tokens_per_s(T, world, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -334,7 +323,7 @@ def main() -> None:
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "frac_of_burst": tflops / peaks["bf16"],
                      "traffic": None},
-        "e2e": {"value": tokens / (e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": D.job_tokens_per_s(T, world, e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
                 "d2h_bytes_per_step": T * d * y.element_size() + 4},
         "gpu_launches": launches_per_step * args.steps,
@@ -343,8 +332,7 @@ def main() -> None:
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(w)
     print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    D.shutdown()
 
 
 if __name__ == "__main__":

@@ -15,7 +15,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
-HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+INCLUDE_DIR = os.path.join(os.path.dirname(_HERE), "include")
+HEADER_PATH = os.path.join(INCLUDE_DIR, "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INDEX = 4, 5, 6
@@ -63,6 +64,10 @@ def lib() -> ctypes.CDLL:
             "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                             ctypes.c_size_t, _P],
             "moe_device_status": [_P, _P],
+            "moe_debug_dispatch_timeout": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                           ctypes.c_uint64, _P],
+            "moe_debug_expert_ffn_timeout": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                             ctypes.c_size_t, ctypes.c_uint64, _P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -75,10 +80,14 @@ def lib() -> ctypes.CDLL:
 
 
 def header_symbols() -> list[str]:
-    """Names of the functions include/moe.h declares."""
-    text = open(HEADER_PATH).read()
-    return sorted(set(re.findall(r"^\s*(?:moe_status_t|const char\s*\*)\s*(moe_\w+)\s*\(", text,
-                                 flags=re.M)))
+    """Names of the functions the headers in include/ declare."""
+    names = set()
+    for fn in sorted(os.listdir(INCLUDE_DIR)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(INCLUDE_DIR, fn)).read()
+            names |= set(re.findall(r"^\s*(?:moe_status_t|const char\s*\*)\s*(moe_\w+)\s*\(",
+                                    text, flags=re.M))
+    return sorted(names)
 
 
 def status_string(status: int) -> str:
@@ -190,6 +199,26 @@ def moe_forward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out, 
                              _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y), _ptr(aux_out),
                              _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+
+
+def moe_debug_dispatch_timeout(cfg, topk_idx, counts, offsets, sorted_token, slot_of, ws,
+                               spin_limit_ns: int, stream=None) -> None:
+    """Test hook (include/moe_debug.h): dispatch whose look-back wait runs out on purpose."""
+    _check(lib().moe_debug_dispatch_timeout(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts),
+                                            _ptr(offsets), _ptr(sorted_token), _ptr(slot_of),
+                                            _ptr(ws), ws.numel() * ws.element_size(),
+                                            int(spin_limit_ns), _stream(stream)),
+           "moe_debug_dispatch_timeout")
+
+
+def moe_debug_expert_ffn_timeout(cfg, x_perm, offsets, W1, b1, W3, W2, b2, y_perm, ws,
+                                 spin_limit_ns: int, stream=None) -> None:
+    """Test hook (include/moe_debug.h): expert GEMM whose first-stage wait runs out on purpose."""
+    _check(lib().moe_debug_expert_ffn_timeout(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets),
+                                              _ptr(W1), _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2),
+                                              _ptr(y_perm), _ptr(ws),
+                                              ws.numel() * ws.element_size(), int(spin_limit_ns),
+                                              _stream(stream)), "moe_debug_expert_ffn_timeout")
 
 
 def moe_device_status(ws, stream=None) -> int:

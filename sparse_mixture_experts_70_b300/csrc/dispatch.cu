@@ -37,6 +37,8 @@ struct DispatchArgs {
     int64_t P;
     int k, E, nchunks;
     int64_t cap;  // per-expert capacity, -1 when dropless
+    unsigned long long spin_limit_ns;
+    int withhold;  // test hook: chunk 0 never publishes its look-back word
 };
 
 __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
             unsigned long long *mine = a.words + (size_t)c * E + tid;
             int excl = 0;
             if (c == 0) {
-                st_release(mine, FLAG_INC | (uint32_t)agg);
+                if (!a.withhold) st_release(mine, FLAG_INC | (uint32_t)agg);
             } else {
                 st_release(mine, FLAG_AGG | (uint32_t)agg);
                 unsigned long long t_start = 0;
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
                         if ((++spins & 255u) == 0) {
                             const unsigned long long now = globaltimer_ns();
                             if (t_start == 0) t_start = now;
-                            else if (now - t_start > SPIN_LIMIT_NS) {
+                            else if (now - t_start > a.spin_limit_ns) {
                                 report(a.dev_status, DEV_ERR_TIMEOUT);
                                 s_abort = 1;
                                 break;
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
             if ((++spins & 255u) == 0) {
                 const unsigned long long now = globaltimer_ns();
                 if (t_start == 0) t_start = now;
-                else if (now - t_start > SPIN_LIMIT_NS) {
+                else if (now - t_start > a.spin_limit_ns) {
                     report(a.dev_status, DEV_ERR_TIMEOUT);
                     s_abort = 1;
                     break;
@@ -289,7 +291,7 @@ int dispatch_blocks_per_sm() {
 }
 
 cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
-                            cudaStream_t s) {
+                            cudaStream_t s, const FaultHook &hook) {
     const int64_t P = c.T * c.k;
     if (P == 0) {
         cudaError_t err = cudaMemsetAsync(b.counts, 0, sizeof(int32_t) * c.E, s);
@@ -311,7 +313,9 @@ cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, cons
     a.E = c.E;
     a.nchunks = (int)dispatch_chunks(c);
     a.cap = capacity_of(c);
-    if (a.nchunks == 1) {
+    a.spin_limit_ns = hook.spin_limit_ns;
+    a.withhold = hook.withhold;
+    if (a.nchunks == 1 && !hook.withhold) {
         dispatch_single_kernel<<<1, DISPATCH_THREADS, 0, s>>>(a);
         return cudaGetLastError();
     }

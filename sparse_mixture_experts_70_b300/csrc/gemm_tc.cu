@@ -53,6 +53,8 @@ struct TcArgs {
     uint32_t *dev_status;
     int64_t P;
     int E, K, N, n_tiles, epi;
+    unsigned long long spin_limit_ns;  // bound of every mbarrier wait
+    int withhold_loads;                // test hook: the producer issues no loads
 };
 
 struct Tile {
@@ -140,18 +142,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int total = s_cum[E];
     const int nk = a.K / BK;
+    const unsigned long long lim = a.spin_limit_ns;
 
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0, eh = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bits
-            bool ok = true;
+            bool ok = !a.withhold_loads;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile ti = decode_tile(t, eh, s_cum, s_off, a.n_tiles);
                 const int brow = ti.e * a.N + ti.n * (a.epi == EPI_SWIGLU ? BN / 2 : BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status)) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
                     }
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // Our own copies must have landed before the CTA may exit.
             for (int s = 0; s < STAGES; ++s)
                 if ((issued >> s) & 1u)
-                    mbar_wait(bar_full + 8 * s, (last_phase >> s) & 1u, nullptr, a.dev_status);
+                    mbar_wait(bar_full + 8 * s, (last_phase >> s) & 1u, nullptr, a.dev_status, lim);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -184,11 +187,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             constexpr uint32_t idesc = idesc_bf16(BM, BN);
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status)) break;
+                if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, s_abort, a.dev_status)) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
                     }
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             // Every MMA this thread issued has completed once the drain barrier fires.
             umma_commit(bar_drain);
-            mbar_wait(bar_drain, 0, nullptr, a.dev_status);
+            mbar_wait(bar_drain, 0, nullptr, a.dev_status, lim);
         }
     } else {
         const int q = warp & 3;           // TMEM lane quarter this warp may access
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = decode_tile(t, eh, s_cum, s_off, a.n_tiles);
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status);
+            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             __syncwarp();
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P, int E, int K,
                         int N, int epi, const int32_t *offsets, const float *bias, void *out,
-                        uint32_t *dev_status, cudaStream_t s) {
+                        uint32_t *dev_status, const FaultHook &hook, cudaStream_t s) {
     const int b_rows = epi == EPI_SWIGLU ? BN / 2 : BN;
     CUtensorMap mA, mB, mB3;
     if (!make_map(&mA, A, P, K, BM)) return cudaErrorInvalidValue;
@@ -312,6 +315,8 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.N = N;
     a.n_tiles = (N + b_rows - 1) / b_rows;
     a.epi = epi;
+    a.spin_limit_ns = hook.spin_limit_ns;
+    a.withhold_loads = hook.withhold;
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
     if (grid > upper) grid = upper;
@@ -323,16 +328,17 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
 
 }  // namespace
 
-cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s) {
+cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,
+                          const FaultHook &hook) {
     const int64_t P = c.T * c.k;
     if (P == 0) return cudaSuccess;
     const bool swiglu = c.act == MOE_ACT_SWIGLU;
     cudaError_t err = launch_gemm(b.x_perm, b.W1, b.W3, P, c.E, c.d, c.f,
                                   swiglu ? EPI_SWIGLU : EPI_GELU, b.offsets,
-                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, s);
+                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, hook, s);
     if (err != cudaSuccess) return err;
     return launch_gemm(b.H, b.W2, nullptr, P, c.E, c.f, c.d, EPI_STORE, b.offsets,
-                       c.has_bias ? b.b2 : nullptr, b.y_perm, b.dev_status, s);
+                       c.has_bias ? b.b2 : nullptr, b.y_perm, b.dev_status, hook, s);
 }
 
 }  // namespace moe

@@ -30,6 +30,13 @@ __device__ __forceinline__ void report(uint32_t *dev_status, uint32_t bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Test hook: a shorter spin limit and one withheld signal, so that a bounded wait runs out
+// (the kernel then records DEV_ERR_TIMEOUT and returns). Normal calls use the defaults.
+struct FaultHook {
+    unsigned long long spin_limit_ns = SPIN_LIMIT_NS;
+    int withhold = 0;  // dispatch: chunk 0 never publishes; GEMM: the producer issues no loads
+};
+
 // ------------------------------------------------------------------------------------------
 // shapes and the workspace layout
 constexpr int DISPATCH_THREADS = 1024;  // slots per dispatch chunk
@@ -93,7 +100,7 @@ struct DispatchBufs {
     uint32_t *dev_status;
 };
 cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
-                            cudaStream_t s);
+                            cudaStream_t s, const FaultHook &hook = FaultHook());
 // Dispatch whose scratch is a file-scope device array (no workspace); nchunks * E must not
 // exceed STATIC_LOOKBACK_CELLS.
 constexpr int64_t STATIC_LOOKBACK_CELLS = 65536;
@@ -119,6 +126,7 @@ struct FfnBufs {
     uint32_t *dev_status;
 };
 cudaError_t launch_ffn_f32(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
-cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
+cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,
+                          const FaultHook &hook = FaultHook());
 
 }  // namespace moe

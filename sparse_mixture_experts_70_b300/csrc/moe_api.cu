@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "moe_debug.h"
 
 namespace moe {
 
@@ -288,6 +289,53 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_
         return MOE_ERR_CUDA;
     if ((e = launch_aux(c, counts, psum, aux_out, s)) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+moe_status_t moe_debug_dispatch_timeout(const moe_config_t *cfg, const int32_t *topk_idx,
+                                        int32_t *counts, int32_t *offsets,
+                                        int32_t *sorted_token, int32_t *slot_of, void *ws,
+                                        size_t ws_bytes, uint64_t spin_limit_ns, void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (spin_limit_ns < 1000000ull || spin_limit_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+    if (dispatch_chunks(*cfg) < 2) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(topk_idx) || !aligned4(counts) || !aligned4(offsets) || !aligned4(sorted_token) ||
+        !aligned4(slot_of) || !aligned16(ws))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char *w = static_cast<char *>(ws);
+    DispatchBufs b{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
+                   reinterpret_cast<int32_t *>(w + L.disp_excl),
+                   reinterpret_cast<uint32_t *>(w + L.status)};
+    FaultHook hook;
+    hook.spin_limit_ns = spin_limit_ns;
+    hook.withhold = 1;
+    return from_cuda(launch_dispatch(*cfg, topk_idx, b, static_cast<cudaStream_t>(stream), hook));
+}
+
+moe_status_t moe_debug_expert_ffn_timeout(const moe_config_t *cfg, const void *x_perm,
+                                          const int32_t *offsets, const void *W1, const float *b1,
+                                          const void *W3, const void *W2, const float *b2,
+                                          void *y_perm, void *ws, size_t ws_bytes,
+                                          uint64_t spin_limit_ns, void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (spin_limit_ns < 1000000ull || spin_limit_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || !aligned16(x_perm) || !aligned4(offsets) || !aligned16(W1) ||
+        !aligned16(W2) || !aligned16(y_perm) || (cfg->act == MOE_ACT_SWIGLU && !aligned16(W3)))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (cfg->T == 0) return MOE_OK;
+    char *w = static_cast<char *>(ws);
+    FfnBufs b{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm,
+              reinterpret_cast<uint32_t *>(w + L.status)};
+    FaultHook hook;
+    hook.spin_limit_ns = spin_limit_ns;
+    hook.withhold = 1;
+    return from_cuda(launch_ffn_tc(*cfg, b, static_cast<cudaStream_t>(stream), hook));
 }
 
 moe_status_t moe_device_status(void *ws, void *stream) {

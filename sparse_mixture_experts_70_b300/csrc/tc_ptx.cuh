@@ -40,13 +40,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `parity` to complete; false on abort (set by another role) or on
 // running out of time (then this call sets the abort flag and the device status bit).
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
-                                            uint32_t *dev_status) {
+                                                   uint32_t *dev_status,
+                                                   unsigned long long limit_ns) {
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 63u) == 0) {
             if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > SPIN_LIMIT_NS) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 if (abort) *abort = 1;
                 report(dev_status, DEV_ERR_TIMEOUT);
                 return false;
@@ -55,9 +56,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *dev_status) {
+                                          uint32_t *dev_status,
+                                          unsigned long long limit_ns = SPIN_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort, dev_status);
+    return mbar_wait_slow(bar, parity, abort, dev_status, limit_ns);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
