@@ -58,18 +58,20 @@ struct TcArgs {
 };
 
 struct Tile {
-    int e, n, row0, rows;
+    int e, n, row0, rows;  // rows <= 0: nothing to compute (the idle half of a CTA pair)
 };
-// Tile t of the schedule: s_cum[e] is the first tile of expert e (E+1 entries); within an
-// expert, tiles run N-major, M-minor. eh is a cursor that only moves forward.
+// Unit t of the schedule. s_cum[e] is the first unit of expert e (E+1 entries); within an
+// expert, units run N-major, M-minor. A unit is one 128-row M tile, or -- for a CTA pair -- two
+// adjacent M tiles, of which CTA `rank` takes the first or the second. eh only moves forward.
+template <bool PAIR>
 __device__ __forceinline__ Tile decode_tile(int t, int &eh, const int32_t *s_cum,
-                                            const int32_t *s_off, int n_tiles) {
+                                            const int32_t *s_off, int n_tiles, int rank) {
     while (s_cum[eh + 1] <= t) ++eh;
     const int e = eh;
     const int local = t - s_cum[e];
-    const int mt = (s_cum[e + 1] - s_cum[e]) / n_tiles;
-    const int n = local / mt;
-    const int m = local - n * mt;
+    const int mu = (s_cum[e + 1] - s_cum[e]) / n_tiles;
+    const int n = local / mu;
+    const int m = PAIR ? 2 * (local - n * mu) + rank : local - n * mu;
     Tile ti;
     ti.e = e;
     ti.n = n;
@@ -78,6 +80,63 @@ __device__ __forceinline__ Tile decode_tile(int t, int &eh, const int32_t *s_cum
     return ti;
 }
 
+// Convert this thread's accumulator row (TMEM lane q*32+lane of accumulator `acc_col`) of tile
+// ti into bf16 outputs: half the tile's columns per thread (`half`), bias / GELU / SwiGLU in f32.
+// Every tcgen05.ld here is executed by the whole warp; only the stores depend on the row.
+__device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, uint32_t tmem_base,
+                                              uint32_t acc_col, int q, int lane, int half) {
+    const int r = q * 32 + lane;
+    const bool valid = r < ti.rows;
+    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
+    __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
+    if (a.epi == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
+            float x1[32], x3[32];
+            tmem_ld32x2(trow + c, trow + BN / 2 + c, x1, x3);
+            const int col = ti.n * (BN / 2) + c;
+            if (valid && col < a.N) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16(silu_fast(x1[2 * i]) * x3[2 * i],
+                                      silu_fast(x1[2 * i + 1]) * x3[2 * i + 1]);
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+            const int col = ti.n * BN + c;
+            if (col >= a.N) break;  // warp-uniform
+            float v[32];
+            tmem_ld32(trow + c, v);
+            if (a.bias) {
+                const float *bp = a.bias + (int64_t)ti.e * a.N + col;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] += __ldg(bp + i);
+            }
+            if (a.epi == EPI_GELU) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_fast(v[i]);
+            }
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]),
+                                        pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                                        pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                                        pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+            }
+        }
+    }
+}
+
+// One CTA per SM; see the file comment.
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -101,6 +160,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E;
+    constexpr bool PAIR = false;
+    const int rank = 0;
+    const int unit0 = (int)blockIdx.x;
+    const int ustep = (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -127,7 +190,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (lo < 0 || hi < lo || (int64_t)hi > a.P) bad = true;
             s_off[e] = lo;
             s_cum[e] = cum;
-            if (!bad) cum += ((hi - lo + BM - 1) / BM) * a.n_tiles;
+            const int mt = (hi - lo + BM - 1) / BM;
+            if (!bad) cum += mt * a.n_tiles;
         }
         s_off[E] = a.offsets[E];
         s_cum[E] = cum;
@@ -150,22 +214,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bits
             bool ok = !a.withhold_loads;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = decode_tile(t, eh, s_cum, s_off, a.n_tiles);
-                const int brow = ti.e * a.N + ti.n * (a.epi == EPI_SWIGLU ? BN / 2 : BN);
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                // B rows of this N tile: SwiGLU stacks 128 rows of W1 over 128 rows of W3
+                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                     : ti.e * a.N + ti.n * BN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = bar_full + 8 * stage;
+                    const uint32_t sb = sB + stage * B_STAGE;
                     mbar_expect_tx(fb, A_STAGE + B_STAGE);
                     tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
                     if (a.epi == EPI_SWIGLU) {
-                        tma_load_2d(sB + stage * B_STAGE, &tmB, fb, kb * BK, brow);
-                        tma_load_2d(sB + stage * B_STAGE + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
+                        tma_load_2d(sb, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
                     } else {
-                        tma_load_2d(sB + stage * B_STAGE, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(sb, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kb * BK, brow + BN / 2);
                     }
                     issued |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -175,18 +243,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
             }
-            // Our own copies must have landed before the CTA may exit.
+            // Every copy into this CTA's ring must have landed before it may exit.
             for (int s = 0; s < STAGES; ++s)
                 if ((issued >> s) & 1u)
                     mbar_wait(bar_full + 8 * s, (last_phase >> s) & 1u, nullptr, a.dev_status, lim);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int stage = 0, acc = 0;
+            int stage = 0, acc = 0, eh = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
             constexpr uint32_t idesc = idesc_bf16(BM, BN);
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                const bool idle = ti.rows <= 0;
                 if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
@@ -196,11 +266,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_k_sw128(sA + stage * A_STAGE);
-                    const uint64_t bd = sdesc_k_sw128(sB + stage * B_STAGE);
+                    if (!idle) {
+                        const uint64_t ad = sdesc_k_sw128(sA + stage * A_STAGE);
+                        const uint64_t bd = sdesc_k_sw128(sB + stage * B_STAGE);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
                     umma_commit(bar_empty + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -219,65 +291,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else {
         const int q = warp & 3;           // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;  // which half of the tile's columns it converts
-        const int r = q * 32 + lane;
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = decode_tile(t, eh, s_cum, s_off, a.n_tiles);
+        for (int t = unit0; t < total; t += ustep) {
+            const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            const bool valid = r < ti.rows;
-            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
-            if (a.epi == EPI_SWIGLU) {
-#pragma unroll 1
-                for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
-                    float x1[32], x3[32];
-                    tmem_ld32x2(trow + c, trow + BN / 2 + c, x1, x3);
-                    const int col = ti.n * (BN / 2) + c;
-                    if (valid && col < a.N) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16(silu_fast(x1[2 * i]) * x3[2 * i],
-                                              silu_fast(x1[2 * i + 1]) * x3[2 * i + 1]);
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
-                    const int col = ti.n * BN + c;
-                    if (col >= a.N) break;  // warp-uniform
-                    float v[32];
-                    tmem_ld32(trow + c, v);
-                    if (a.bias) {
-                        const float *bp = a.bias + (int64_t)ti.e * a.N + col;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += __ldg(bp + i);
-                    }
-                    if (a.epi == EPI_GELU) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_fast(v[i]);
-                    }
-                    if (valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]),
-                                                pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                                                pack_bf16(v[8 * i + 4], v[8 * i + 5]),
-                                                pack_bf16(v[8 * i + 6], v[8 * i + 7]));
-                    }
-                }
-            }
+            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half);
             tc_fence_before();
             mbar_arrive(bar_tempty + 8 * acc);
             acc ^= 1;
@@ -285,6 +309,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     }
 
+    tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -293,16 +318,248 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
+// CTA-pair kernel: a 2-CTA cluster computes 256 x 256 tiles with tcgen05.mma.cta_group::2.
+//
+// One MMA of M = 256 drives both SMs' tensor cores and reads each operand byte from shared
+// memory once: CTA r holds rows 128r..128r+127 of the A tile and rows 128r..128r+127 of the
+// 256-row B tile, at the same shared-memory offsets, and receives D rows 128r..128r+127 in its
+// own tensor memory. Per SM and per 64-wide k-step that is 32 KiB of TMA writes and operand reads
+// instead of 48 KiB for the single-CTA 128 x 256 tile, whose combined shared-memory traffic caps
+// its tensor pipe near two thirds. The ring therefore holds 6 stages.
+//   - Both CTAs' producers load their own halves; the copies complete on the first (leader)
+//     CTA's full barrier, which expects the bytes of both (TMA .cta_group::2 lets the barrier
+//     live in the peer CTA).
+//   - The leader's single MMA thread issues the MMAs; its commits arrive on the empty and
+//     accumulator-full barriers of both CTAs (multicast).
+//   - Both CTAs' epilogues read their own accumulator rows and arrive on the leader's
+//     accumulator-empty barrier (one arrival per warp, 16 in all).
+// The tile table counts units of two adjacent 128-row M tiles; on an expert's odd last tile the
+// second CTA computes rows past the expert's end, which its epilogue masks.
+constexpr int STAGES2 = 6;
+constexpr int A_HALF = BM * BK * 2;          // 16 KiB: this CTA's A rows
+constexpr int B_HALF = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the B tile
+constexpr size_t TC_SMEM_PAIR = 1024 + (size_t)STAGES2 * (A_HALF + B_HALF) + CTL_BYTES;
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmB3, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + STAGES2 * A_HALF;
+    uint8_t *ctl = gbase + STAGES2 * (A_HALF + B_HALF);
+    const uint32_t bar0 = smem_u32(ctl);
+    const uint32_t bar_full = bar0, bar_empty = bar0 + 8 * STAGES2;
+    const uint32_t bar_tfull = bar0 + 16 * STAGES2, bar_tempty = bar_tfull + 16;
+    const uint32_t bar_drain = bar_tempty + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl + 256);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(ctl + 260);
+    int32_t *s_cum = reinterpret_cast<int32_t *>(ctl + 512);   // [E+1]
+    int32_t *s_off = s_cum + 260;                             // [E+1]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E;
+    const int rank = (int)cluster_ctarank();
+    const bool leader = rank == 0;
+    const int unit0 = (int)(blockIdx.x >> 1);
+    const int ustep = (int)(gridDim.x >> 1);
+    constexpr uint16_t BOTH = 0x3;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(bar_tfull + 8 * q, 1);
+            mbar_init(bar_tempty + 8 * q, 16);
+        }
+        mbar_init(bar_drain, 1);
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);  // collective: the same columns in both
+        tmem_relinquish_pair();
+    }
+    if (warp == 2 && lane == 0) {
+        int cum = 0;
+        bool bad = false;
+        for (int e = 0; e < E; ++e) {
+            const int lo = a.offsets[e], hi = a.offsets[e + 1];
+            if (lo < 0 || hi < lo || (int64_t)hi > a.P) bad = true;
+            s_off[e] = lo;
+            s_cum[e] = cum;
+            const int mt = (hi - lo + BM - 1) / BM;
+            if (!bad) cum += (mt + 1) / 2 * a.n_tiles;
+        }
+        s_off[E] = a.offsets[E];
+        s_cum[E] = cum;
+        if (bad) {
+            report(a.dev_status, DEV_ERR_INDEX);
+            for (int e = 0; e <= E; ++e) s_cum[e] = 0;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy completes
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = s_cum[E];
+    const int nk = a.K / BK;
+    const unsigned long long lim = a.spin_limit_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0, eh = 0;
+            uint32_t phase = 0;
+            bool ok = !a.withhold_loads;
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                // this CTA's half of the B tile: SwiGLU W1 (CTA 0) / W3 (CTA 1) rows, else rows
+                // 128 r.. of the 256-row W tile
+                const CUtensorMap *bm = (a.epi == EPI_SWIGLU && rank == 1) ? &tmB3 : &tmB;
+                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                     : ti.e * a.N + ti.n * BN + rank * (BN / 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);  // leader's barrier
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_HALF + B_HALF));
+                    tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
+                    tma_load_2d_pair(sB + stage * B_HALF, bm, fb, kb * BK, brow);
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // A slot is released only after the leader's MMAs consumed it, hence after every copy
+            // into it (this CTA's included) landed: wait for all slots once more before exiting.
+            if (ok) {
+                for (int i = 0; i < STAGES2; ++i) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim))
+                        break;
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
+            for (int t = unit0; t < total && ok; t += ustep) {
+                if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, s_abort, a.dev_status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_k_sw128(sA + stage * A_HALF);
+                    const uint64_t bd = sdesc_k_sw128(sB + stage * B_HALF);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit_pair_multicast(bar_empty + 8 * stage, BOTH);
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_multicast(bar_tfull + 8 * acc, BOTH);
+                acc ^= 1;
+                if (acc == 0) aphase ^= 1u;
+            }
+            umma_commit_pair(bar_drain);
+            mbar_wait(bar_drain, 0, nullptr, a.dev_status, lim);
+        }
+    } else {
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        int acc = 0, eh = 0;
+        uint32_t aphase = 0;
+        for (int t = unit0; t < total; t += ustep) {
+            const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no copy, commit or remote arrive targets either CTA any more
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // host side
+
+// Resident 2-CTA clusters of the pair kernel on this device (0: cannot launch it).
+int pair_clusters() {
+    static int cache[64];
+    static bool done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!done[dev]) {
+        int n = 0;
+        if (set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel, TC_SMEM_PAIR) ==
+            cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * 74);
+            cfg.blockDim = dim3(TC_THREADS);
+            cfg.dynamicSmemBytes = TC_SMEM_PAIR;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel, &cfg) != cudaSuccess)
+                n = 0;
+        }
+        cudaGetLastError();
+        cache[dev] = n;
+        done[dev] = true;
+    }
+    return cache[dev];
+}
 
 cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P, int E, int K,
                         int N, int epi, const int32_t *offsets, const float *bias, void *out,
                         uint32_t *dev_status, const FaultHook &hook, cudaStream_t s) {
-    const int b_rows = epi == EPI_SWIGLU ? BN / 2 : BN;
+    // every B box is 128 rows: one half of the 256-row B tile
     CUtensorMap mA, mB, mB3;
     if (!make_map(&mA, A, P, K, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mB, B, (int64_t)E * N, K, b_rows)) return cudaErrorInvalidValue;
-    if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, b_rows))
+    if (!make_map(&mB, B, (int64_t)E * N, K, BN / 2)) return cudaErrorInvalidValue;
+    if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, BN / 2))
         return cudaErrorInvalidValue;
     TcArgs a;
     a.offsets = offsets;
@@ -313,10 +570,32 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.E = E;
     a.K = K;
     a.N = N;
+    const int b_rows = epi == EPI_SWIGLU ? BN / 2 : BN;  // output columns per N tile
     a.n_tiles = (N + b_rows - 1) / b_rows;
     a.epi = epi;
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold_loads = hook.withhold;
+    // The CTA-pair kernel when experts average at least four M tiles (on an expert's odd last
+    // tile the second CTA computes masked rows, a small loss there).
+    const int clusters = pair_clusters();
+    const bool pair = clusters > 0 && P >= (int64_t)4 * BM * E;
+    if (pair) {
+        const int64_t units = ((P + 2 * BM - 1) / (2 * BM) + E) * (int64_t)a.n_tiles;
+        int64_t ncl = clusters < units ? clusters : units;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * ncl));
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = TC_SMEM_PAIR;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, mA, mB, mB3, a);
+    }
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
     if (grid > upper) grid = upper;

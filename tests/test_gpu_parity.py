@@ -43,6 +43,9 @@ SMALL = [
     wl.small("capacity_f32", T=200, d=64, f=128, E=4, k=2, dtype="f32", router_bias_var=2.0,
              capacity_factor=0.5),
     wl.small("capacity_zero", T=100, d=64, f=64, E=8, k=2, capacity_factor=0.02),
+    # paired-CTA GEMM (experts of >= 4 M tiles): odd tile counts, ragged N tail, skew
+    wl.small("paired_gelu_bias", T=2500, d=256, f=320, E=3, k=2, act=G, has_bias=True),
+    wl.small("paired_swiglu_skewed", T=3000, d=128, f=256, E=4, k=2, router_bias_var=3.0),
 ]
 
 
