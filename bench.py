@@ -2,18 +2,19 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral] [--impl ours|reference]
 
-One step = one pass of the whole layer (router + top-k, dispatch + permute, grouped expert FFN,
-combine, auxiliary value) over one batch of the workload's seeded synthetic inputs, with weights
-and inputs resident in HBM. Each rank (one process per GPU, launched by torchrun for N > 1) runs
+One step = one moe_forward call: the whole layer (router + top-k, dispatch + permute, grouped
+expert FFN, combine, auxiliary value) over one batch of the workload's seeded synthetic inputs,
+with weights and inputs resident in HBM. Each rank (one process per GPU, launched by torchrun for N > 1) runs
 an independent replica of the layer on its own batch: there is no exchange on this path, so the
 scaling is weak and `value` is the tokens of all ranks over the slowest rank's time.
 
 The JSON line also carries:
   e2e          the same metric through moe_forward with host buffers: pinned h copied in and y
                (plus aux) copied out inside the timed region, every step;
-  roofline     the dominant kernel (grouped_gemm_tc_kernel, launched twice per step: GEMM1 and
+  roofline     the dominant kernel (the grouped expert GEMM, launched twice per step: GEMM1 and
                GEMM2) against the measured bf16 tensor peak: algorithmic flops of the two launches
-               over their summed CUDA-event duration on the launching stream;
+               over their CUDA-event duration, recorded by moe_forward_events on the launching
+               stream inside the timed region;
   cpu_baseline the double-precision oracle on this machine's host cores, on a bounded token
                sample of the same workload (rank 0, N = 1 only);
   clocks       nvidia-smi samples taken during the timed region.
@@ -39,7 +40,12 @@ sys.path.insert(0, ROOT)
 from sparse_mixture_experts_70_b300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE layer tokens/s at 1 B300; % of bf16 TC peak (GEMM) or HBM BW (decode)"
-GEMM_KERNEL = "grouped_gemm_tc_kernel"
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu capture summarised in
+# profiles/grouped_gemm_pair_T2048_E2_k1.md (a reduced case: 2 of 8 experts, 2048 of 8192 rows),
+# scaled to the full Mixtral-shape launch by the experts and rows processed (traffic grows in
+# proportion: weights once, activations once). Average of GEMM1 (2.19 GB) and GEMM2 (1.34 GB).
+MEASURED_TRAFFIC = {"mixtral": 1.76e9}
+GEMM_KERNEL = "grouped_gemm_pair_kernel / grouped_gemm_tc_kernel"
 
 
 def _peaks() -> dict:
@@ -197,49 +203,22 @@ def main() -> None:
     cfg = B.config_for(w)
     inputs = wl.generate(w)
     dev = {k: (v.cuda().contiguous() if v is not None else None) for k, v in inputs.items()}
-    ws = B.workspace(cfg)
     T, k, E, d = w.T, w.k, w.E, w.d
-    rows = B.moe_router_partials(cfg)
-    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    psum = torch.empty((rows, E), dtype=torch.float32, device="cuda")
-    counts = torch.empty(E, dtype=torch.int32, device="cuda")
-    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-    sorted_token = torch.empty(T * k, dtype=torch.int32, device="cuda")
-    slot_of = torch.empty(T * k, dtype=torch.int32, device="cuda")
-    x_perm = torch.empty((T * k, d), dtype=w.torch_dtype, device="cuda")
-    y_perm = torch.empty((T * k, d), dtype=w.torch_dtype, device="cuda")
-    y = torch.empty((T, d), dtype=w.torch_dtype, device="cuda")
-    aux = torch.empty(1, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    layer = B.Layer(cfg, dev)          # weights resident, workspace and outputs preallocated
     h = dev["h"]
 
-    def step(ev=None):
-        # the five step calls (the same kernels moe_forward launches), with events around them
-        if ev is not None:
-            ev[0].record(stream)
-        B.moe_router_topk(cfg, h, dev["W_r"], dev["b_r"], idx, gates, psum, ws, stream)
-        B.moe_build_dispatch(cfg, idx, h, counts, offsets, sorted_token, slot_of, x_perm, ws,
-                             stream)
-        if ev is not None:
-            ev[1].record(stream)
-        B.moe_expert_ffn(cfg, x_perm, offsets, dev["W1"], dev["b1"], dev["W3"], dev["W2"],
-                         dev["b2"], y_perm, ws, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        B.moe_combine(cfg, y_perm, slot_of, gates, y, stream)
-        B.moe_aux_loss(cfg, counts, psum, aux, stream)
-        if ev is not None:
-            ev[3].record(stream)
-
     for _ in range(args.warmup):
-        step()
+        layer.forward(h, stream)
     torch.cuda.synchronize()
-    st = B.moe_device_status(ws)
+    st = B.moe_device_status(layer.ws)
     if st != B.MOE_OK:
         raise SystemExit(f"device status after warm-up: {B.status_string(st)}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Timed region: K calls of moe_forward (the call a user makes); each also records two events
+    # on its stream around the expert-FFN launches, the dominant kernel's live duration.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
@@ -247,21 +226,18 @@ def main() -> None:
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            layer.forward(h, stream, ffn_events=evs[i])
         stop.record(stream)
         torch.cuda.synchronize()
         D.barrier()
     clocks = clk.summary()
     ms = start.elapsed_time(stop) / args.steps
-    ffn_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-    route_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    comb_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
-    st = B.moe_device_status(ws)
+    ffn_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
+    st = B.moe_device_status(layer.ws)
     if st != B.MOE_OK:
         raise SystemExit(f"device status after timed region: {B.status_string(st)}")
 
     # end to end through moe_forward with host buffers (pinned), copies inside the timed region
-    layer = B.Layer(cfg, dev)
     h_host = inputs["h"].pin_memory()
     y_host = torch.empty((T, d), dtype=w.torch_dtype).pin_memory()
     aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
@@ -296,8 +272,9 @@ def main() -> None:
     flops = w.expert_flops()
     tflops = flops / (ffn_ms * 1e-3) / 1e12
     peak = peaks["bf16_sustained"]
-    # router, dispatch, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine, aux
-    launches_per_step = 7
+    # router (+ weight split on the tensor-core path), dispatch, permute, GEMM1, GEMM2 (or the
+    # two f32 FFN launches), combine, aux
+    launches_per_step = 8 if (w.dtype == "bf16" and w.E <= 128 and w.T > 1024) else 7
     line = {
         "metric": METRIC,
         "value": D.job_tokens_per_s(T, world, ms),
@@ -316,16 +293,15 @@ def main() -> None:
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({w.weight_bytes() / 1e9:.2f} GB of expert "
                          "weights read every step)"},
-        "breakdown_ms": {"router_dispatch_permute": route_ms, "expert_ffn": ffn_ms,
-                         "combine_aux": comb_ms},
+        "breakdown_ms": {"expert_ffn": ffn_ms, "router_dispatch_combine_aux": ms - ffn_ms},
         "roofline": {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "frac_of_burst": tflops / peaks["bf16"],
-                     "traffic": None},
+                     "traffic": MEASURED_TRAFFIC.get(w.name if not args.override else "")},
         "e2e": {"value": D.job_tokens_per_s(T, world, e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
-                "d2h_bytes_per_step": T * d * y.element_size() + 4},
+                "d2h_bytes_per_step": T * d * layer.y.element_size() + 4},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }

@@ -182,6 +182,16 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_
                          int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
                          void *stream);
 
+/* moe_forward that also records two caller-created CUDA events (cudaEvent_t, passed as void*) on
+ * `stream`: ffn_begin right before the expert-FFN launches and ffn_end right after them, so that
+ * a caller can time the dominant step live inside a longer run. Same results as moe_forward. */
+moe_status_t moe_forward_events(const moe_config_t *cfg, const void *h, const float *W_r,
+                                const float *b_r, const void *W1, const float *b1,
+                                const void *W3, const void *W2, const float *b2, void *y,
+                                float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
+                                void *ws, size_t ws_bytes, void *stream, void *ffn_begin,
+                                void *ffn_end);
+
 /* Synchronise `stream`, read the device status word in ws, clear it, and return MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_INDEX (MOE_ERR_CUDA if the copy itself fails). */
 moe_status_t moe_device_status(void *ws, void *stream);

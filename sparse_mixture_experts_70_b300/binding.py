@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             "moe_aux_loss": [_CFG, _P, _P, _P, _P],
             "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                             ctypes.c_size_t, _P],
+            "moe_forward_events": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   ctypes.c_size_t, _P, _P, _P],
             "moe_device_status": [_P, _P],
             "moe_debug_dispatch_timeout": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                            ctypes.c_uint64, _P],
@@ -221,6 +223,21 @@ def moe_debug_expert_ffn_timeout(cfg, x_perm, offsets, W1, b1, W3, W2, b2, y_per
                                               _stream(stream)), "moe_debug_expert_ffn_timeout")
 
 
+def moe_forward_events(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out,
+                       counts_out, ws, ffn_begin, ffn_end, stream=None) -> None:
+    """moe_forward recording torch.cuda.Event ffn_begin / ffn_end around the expert FFN."""
+    for ev in (ffn_begin, ffn_end):
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record(stream if isinstance(stream, torch.cuda.Stream)
+                      else torch.cuda.current_stream())
+    _check(lib().moe_forward_events(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(W1),
+                                    _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y),
+                                    _ptr(aux_out), _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream),
+                                    ffn_begin.cuda_event, ffn_end.cuda_event),
+           "moe_forward_events")
+
+
 def moe_device_status(ws, stream=None) -> int:
     """Synchronise, read and clear the device status word; returns the status code."""
     return int(lib().moe_device_status(_ptr(ws), _stream(stream)))
@@ -244,9 +261,13 @@ class Layer:
         self.topk_idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
         self.counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
 
-    def forward(self, h: torch.Tensor, stream=None) -> torch.Tensor:
+    def forward(self, h: torch.Tensor, stream=None, ffn_events=None) -> torch.Tensor:
+        """moe_forward on h; ffn_events = (begin, end) torch.cuda.Event to time the expert FFN."""
         w = self.w
-        moe_forward(self.cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"),
-                    w["W2"], w.get("b2"), self.y, self.aux, self.topk_idx, self.counts, self.ws,
-                    stream)
+        args = (self.cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"), w["W2"],
+                w.get("b2"), self.y, self.aux, self.topk_idx, self.counts, self.ws)
+        if ffn_events is None:
+            moe_forward(*args, stream)
+        else:
+            moe_forward_events(*args, ffn_events[0], ffn_events[1], stream)
         return self.y

@@ -237,11 +237,12 @@ moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const 
     return from_cuda(launch_aux(*cfg, counts, psum_part, aux_out, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
-                         const float *b_r, const void *W1, const float *b1, const void *W3,
-                         const void *W2, const float *b2, void *y, float *aux_out,
-                         int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
-                         void *stream) {
+static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const float *W_r,
+                                 const float *b_r, const void *W1, const float *b1,
+                                 const void *W3, const void *W2, const float *b2, void *y,
+                                 float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
+                                 void *ws, size_t ws_bytes, void *stream, cudaEvent_t ev_ffn0,
+                                 cudaEvent_t ev_ffn1) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     const moe_config_t &c = *cfg;
@@ -283,8 +284,10 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_
     if ((e = launch_permute(c, h, sorted_token, offsets, x_perm, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
+    if (ev_ffn0 && cudaEventRecord(ev_ffn0, s) != cudaSuccess) return MOE_ERR_CUDA;
     e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (ev_ffn1 && cudaEventRecord(ev_ffn1, s) != cudaSuccess) return MOE_ERR_CUDA;
     if ((e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     if ((e = launch_aux(c, counts, psum, aux_out, s)) != cudaSuccess) return MOE_ERR_CUDA;
@@ -336,6 +339,31 @@ moe_status_t moe_debug_expert_ffn_timeout(const moe_config_t *cfg, const void *x
     hook.spin_limit_ns = spin_limit_ns;
     hook.withhold = 1;
     return from_cuda(launch_ffn_tc(*cfg, b, static_cast<cudaStream_t>(stream), hook));
+}
+
+}  // extern "C"
+
+extern "C" {
+
+moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
+                         const float *b_r, const void *W1, const float *b1, const void *W3,
+                         const void *W2, const float *b2, void *y, float *aux_out,
+                         int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
+                         void *stream) {
+    return forward_impl(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out,
+                        counts_out, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status_t moe_forward_events(const moe_config_t *cfg, const void *h, const float *W_r,
+                                const float *b_r, const void *W1, const float *b1,
+                                const void *W3, const void *W2, const float *b2, void *y,
+                                float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
+                                void *ws, size_t ws_bytes, void *stream, void *ffn_begin,
+                                void *ffn_end) {
+    if (!ffn_begin || !ffn_end) return MOE_ERR_INVALID_ARG;
+    return forward_impl(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out,
+                        counts_out, ws, ws_bytes, stream, static_cast<cudaEvent_t>(ffn_begin),
+                        static_cast<cudaEvent_t>(ffn_end));
 }
 
 moe_status_t moe_device_status(void *ws, void *stream) {

@@ -10,12 +10,13 @@
 // moe_router_partials can tell the caller how many partial-sum rows there will be):
 //   router_splitd_kernel E <= 32 and few tokens: one token per block, the warps split d and read
 //                        W_r from L2 (latency-bound shapes such as decode).
-//   router_small_kernel  E <= 32 and W_r fits in shared memory: one warp per token, lanes across
+//   router_small_kernel  f32 h, E <= 32, W_r fits in shared memory: one warp per token, lanes across
 //                        d with 16-byte loads of h, W_r resident in shared memory in a
 //                        lane-interleaved layout (conflict-free 16-byte reads); the E partial sums
 //                        are folded across lanes by a butterfly then a reduce-scatter, leaving
 //                        lane e with logit e. Bandwidth-bound on h.
-//   router_tc_kernel     bf16 h and 32 < E <= 128: tensor cores (router_tc.cu).
+//   router_tc_kernel     bf16 h, E <= 128, more tokens than the split-d kernel takes: tensor
+//                        cores (router_tc.cu).
 //   router_tile_kernel   everything else: a block owns BT tokens x all E experts and runs a
 //                        register-blocked f32 FMA contraction staged through shared memory.
 // All four end with the same per-token step: max, sum of exponentials and k rounds of arg-max
@@ -452,9 +453,10 @@ RouterPath router_path(const moe_config_t &c) {
     if (c.E <= 32 && c.T <= 1024 &&
         (double)c.T * c.d * small_emax(c.E) * 4 <= 64.0 * 1024 * 1024)
         return PATH_SPLITD;
+    // bf16 with many tokens: the tensor cores (exact three-piece split of W_r)
+    if (c.dtype == MOE_BF16 && c.E <= ROUTER_TC_MAX_E) return PATH_TC;
     if (c.E <= 32 && (size_t)((c.d + 255) / 256) * 256 * small_emax(c.E) * 4 <= SMALL_SMEM_MAX)
         return PATH_SMALL;
-    if (c.dtype == MOE_BF16 && c.E > 32 && c.E <= ROUTER_TC_MAX_E) return PATH_TC;
     return PATH_TILE;
 }
 

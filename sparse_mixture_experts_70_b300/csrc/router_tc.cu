@@ -1,8 +1,9 @@
-// router_tc.cu -- steps 1-2 of the MoE layer on the tensor cores, for bf16 h and 32 < E <= 128.
+// router_tc.cu -- steps 1-2 of the MoE layer on the tensor cores, for bf16 h and E <= 128.
 //
 // The router logits z = h . W_r (lensaml.com "Mixture of Experts", Step 2) are a dense
 // [T, d] x [d, E] contraction; with E of 64-128 it is far too much f32 arithmetic for the CUDA
-// cores (2 d E flop per token), so it runs as a tcgen05 GEMM. The router stays f32-accurate
+// cores (2 d E flop per token), so it runs as a tcgen05 GEMM; for small E it is a bandwidth-bound
+// stream of h that the TMA ring feeds at full rate. The router stays f32-accurate
 // (arjunjaggi.com "Mixture of Experts in LLMs", "Switch Transformers": router in float32):
 //   W_r (f32) is split exactly into three bf16 pieces, w = w_hi + w_mid + w_lo (each piece keeps
 //   the next 8 significant bits of the remainder; 3 x 8 bits cover f32's 24), and
@@ -344,6 +345,7 @@ cudaError_t launch_router_tc(const moe_config_t &c, const void *h, const float *
     const int64_t tiles = (c.T + RB - 1) / RB;
     const int64_t blocks = tiles < num_sms() ? tiles : num_sms();
     switch (nch) {
+        case 1: return launch_nch<1>(mh, mw, a, blocks, smem, s);
         case 2: return launch_nch<2>(mh, mw, a, blocks, smem, s);
         case 3: return launch_nch<3>(mh, mw, a, blocks, smem, s);
         default: return launch_nch<4>(mh, mw, a, blocks, smem, s);

@@ -34,6 +34,7 @@ SMALL = [
     wl.small("tc_router_E100_raw_prob", T=300, d=128, f=128, E=100, k=1, act=G,
              gate=wl.GATE_RAW_PROB),
     wl.small("small_router_E20_f32", T=77, d=320, f=64, E=20, k=5, dtype="f32"),
+    wl.small("smem_router_f32_many_tokens", T=1500, d=320, f=64, E=8, k=2, dtype="f32"),
     # capacity factor (drops): single-chunk and multi-chunk dispatch, f32 and bf16, everything
     # dropped (C = 0)
     wl.small("capacity_skewed_k2", T=800, d=128, f=256, E=8, k=2, router_bias_var=4.0,
