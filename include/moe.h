@@ -65,7 +65,13 @@ enum { MOE_GATE_RENORM = 0, MOE_GATE_RAW_PROB = 1 };
  *            and the other slots are dropped: they contribute nothing to y (a token whose slots
  *            are all dropped gets y = 0, its residual passing around the layer), the kept gates
  *            are not renormalised, and the auxiliary value still uses the routed counts
- *            (lensaml.com "Mixture of Experts", Step 5 "Capacity & Dropped Tokens"). */
+ *            (lensaml.com "Mixture of Experts", Step 5 "Capacity & Dropped Tokens").
+ *   fuse_gather : 0 or 1 (else MOE_ERR_INVALID_ARG); bf16 only, ignored for f32. 1: moe_forward
+ *            does not build the permuted copy x_perm; the first expert GEMM reads its rows of h
+ *            through sorted_token with 4-row TMA gathers, and the workspace holds no x_perm
+ *            (P d 2 bytes less). Same bits as 0, but slower on the shapes measured here: the
+ *            gather repeats for each of the f/128 column tiles of an expert, where the permute
+ *            kernel gathers every row once. */
 typedef struct {
     int64_t T;
     int32_t d, f, E, k;
@@ -74,6 +80,7 @@ typedef struct {
     int32_t gate;
     int32_t has_bias;
     float capacity_factor;
+    int32_t fuse_gather;
 } moe_config_t;
 
 /* Bytes of workspace every call below needs for `cfg` (the largest of their needs, so one

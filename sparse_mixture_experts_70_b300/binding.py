@@ -29,7 +29,8 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("f", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("gate", ctypes.c_int32), ("has_bias", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_float),
+                ("fuse_gather", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):
@@ -98,8 +99,9 @@ def status_string(status: int) -> str:
 
 def config(T: int, d: int, f: int, E: int, k: int, dtype: int = MOE_BF16,
            act: int = MOE_ACT_SWIGLU, gate: int = MOE_GATE_RENORM, has_bias: bool = False,
-           capacity_factor: float = 0.0) -> moe_config_t:
-    return moe_config_t(T, d, f, E, k, dtype, act, gate, 1 if has_bias else 0, capacity_factor)
+           capacity_factor: float = 0.0, fuse_gather: bool = False) -> moe_config_t:
+    return moe_config_t(T, d, f, E, k, dtype, act, gate, 1 if has_bias else 0, capacity_factor,
+                        1 if fuse_gather else 0)
 
 
 def config_for(w) -> moe_config_t:
@@ -107,7 +109,7 @@ def config_for(w) -> moe_config_t:
     return config(w.T, w.d, w.f, w.E, w.k, MOE_F32 if w.dtype == "f32" else MOE_BF16,
                   MOE_ACT_SWIGLU if w.act == "swiglu" else MOE_ACT_GELU_TANH,
                   MOE_GATE_RAW_PROB if w.gate == "raw_prob" else MOE_GATE_RENORM, w.has_bias,
-                  getattr(w, "capacity_factor", 0.0))
+                  getattr(w, "capacity_factor", 0.0), getattr(w, "fuse_gather", False))
 
 
 def _ptr(t) -> int | None:

@@ -55,7 +55,32 @@ struct TcArgs {
     int E, K, N, n_tiles, epi;
     unsigned long long spin_limit_ns;  // bound of every mbarrier wait
     int withhold_loads;                // test hook: the producer issues no loads
+    // fused gather (GEMM1): A row r is row a_rows[r] of a [a_src_rows, K] tensor, read with
+    // 4-row TMA gathers, instead of row r of a permuted copy
+    const int32_t *a_rows;
+    int64_t a_src_rows;
+    // fused scatter (GEMM2, one expert per token): sorted row r goes to output row
+    // out_token[r], scaled by out_gate[out_token[r]]
+    const int32_t *out_token;
+    const float *out_gate;
 };
+
+// The 4 source rows this lane gathers for tile ti (rows 4 lane .. 4 lane + 3 of the tile);
+// rows past the tile's valid rows read a real row (token 0), computed and never stored.
+__device__ __forceinline__ int4 gather_rows(const TcArgs &a, int row0, int rows, int lane) {
+    int r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = 4 * lane + j;
+        int tok = 0;
+        if (i < rows) {
+            tok = __ldg(a.a_rows + row0 + i);
+            if (tok < 0 || (int64_t)tok >= a.a_src_rows) tok = 0;
+        }
+        r[j] = tok;
+    }
+    return make_int4(r[0], r[1], r[2], r[3]);
+}
 
 struct Tile {
     int e, n, row0, rows;  // rows <= 0: nothing to compute (the idle half of a CTA pair)
@@ -89,6 +114,12 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
     const bool valid = r < ti.rows;
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
     __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
+    float gscale = 1.f;
+    if (a.out_token && valid) {  // fused combine of a top-1 layer: y[token] = g * (H W2^T + b2)
+        const int tok = __ldg(a.out_token + ti.row0 + r);
+        gscale = __ldg(a.out_gate + tok);
+        orow = a.out + (int64_t)tok * a.N;
+    }
     if (a.epi == EPI_SWIGLU) {
 #pragma unroll 1
         for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
@@ -122,6 +153,10 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
             if (a.epi == EPI_GELU) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_fast(v[i]);
+            }
+            if (a.out_token) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= gscale;
             }
             if (valid) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
@@ -209,25 +244,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const unsigned long long lim = a.spin_limit_ns;
 
     if (warp == 0) {
-        if (lane == 0) {
-            int stage = 0, eh = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0, last_phase = 0;  // per-stage bits
-            bool ok = !a.withhold_loads;
-            for (int t = unit0; t < total && ok; t += ustep) {
-                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
-                // B rows of this N tile: SwiGLU stacks 128 rows of W1 over 128 rows of W3
-                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
-                                                     : ti.e * a.N + ti.n * BN;
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar_full + 8 * stage;
-                    const uint32_t sb = sB + stage * B_STAGE;
+        // The whole warp runs the producer loop: lane 0 waits for free slots and issues the B
+        // (and tiled A) copies; with a fused gather every lane copies 4 of the tile's 128 A rows.
+        const bool gather = a.a_rows != nullptr;
+        int stage = 0, eh = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, last_phase = 0;  // per-stage bits
+        bool ok = !a.withhold_loads;
+        for (int t = unit0; t < total && ok; t += ustep) {
+            const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+            const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                 : ti.e * a.N + ti.n * BN;
+            const int4 gr = gather ? gather_rows(a, ti.row0, ti.rows, lane) : make_int4(0, 0, 0, 0);
+            for (int kb = 0; kb < nk; ++kb) {
+                int go = 1;
+                if (lane == 0)
+                    go = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim);
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_full + 8 * stage;
+                const uint32_t sb = sB + stage * B_STAGE;
+                if (lane == 0) {
                     mbar_expect_tx(fb, A_STAGE + B_STAGE);
-                    tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
+                    if (!gather) tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
                     if (a.epi == EPI_SWIGLU) {
                         tma_load_2d(sb, &tmB, fb, kb * BK, brow);
                         tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
@@ -235,19 +277,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         tma_load_2d(sb, &tmB, fb, kb * BK, brow);
                         tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kb * BK, brow + BN / 2);
                     }
-                    issued |= 1u << stage;
-                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                }
+                if (gather) {
+                    __syncwarp();
+                    tma_gather4(sA + stage * A_STAGE + lane * 512, &tmA, fb, kb * BK, gr.x, gr.y,
+                                gr.z, gr.w);
+                }
+                issued |= 1u << stage;
+                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            // Every copy into this CTA's ring must have landed before it may exit.
+        }
+        // Every copy into this CTA's ring must have landed before it may exit.
+        if (lane == 0)
             for (int s = 0; s < STAGES; ++s)
                 if ((issued >> s) & 1u)
                     mbar_wait(bar_full + 8 * s, (last_phase >> s) & 1u, nullptr, a.dev_status, lim);
-        }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             int stage = 0, acc = 0, eh = 0;
@@ -336,6 +385,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // The tile table counts units of two adjacent 128-row M tiles; on an expert's odd last tile the
 // second CTA computes rows past the expert's end, which its epilogue masks.
 constexpr int STAGES2 = 6;
+// The pair kernel runs when experts average at least this many 128-row M tiles.
+#ifndef PAIR_MIN_TILES
+#define PAIR_MIN_TILES 4
+#endif
 constexpr int A_HALF = BM * BK * 2;          // 16 KiB: this CTA's A rows
 constexpr int B_HALF = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the B tile
 constexpr size_t TC_SMEM_PAIR = 1024 + (size_t)STAGES2 * (A_HALF + B_HALF) + CTL_BYTES;
@@ -413,45 +466,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const unsigned long long lim = a.spin_limit_ns;
 
     if (warp == 0) {
-        if (lane == 0) {
-            int stage = 0, eh = 0;
-            uint32_t phase = 0;
-            bool ok = !a.withhold_loads;
-            for (int t = unit0; t < total && ok; t += ustep) {
-                const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
-                // this CTA's half of the B tile: SwiGLU W1 (CTA 0) / W3 (CTA 1) rows, else rows
-                // 128 r.. of the 256-row W tile
-                const CUtensorMap *bm = (a.epi == EPI_SWIGLU && rank == 1) ? &tmB3 : &tmB;
-                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
-                                                     : ti.e * a.N + ti.n * BN + rank * (BN / 2);
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);  // leader's barrier
-                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_HALF + B_HALF));
-                    tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
-                    tma_load_2d_pair(sB + stage * B_HALF, bm, fb, kb * BK, brow);
-                    if (++stage == STAGES2) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        // The whole warp runs the producer loop (see the single-CTA kernel).
+        const bool gather = a.a_rows != nullptr;
+        int stage = 0, eh = 0;
+        uint32_t phase = 0;
+        bool ok = !a.withhold_loads;
+        for (int t = unit0; t < total && ok; t += ustep) {
+            const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
+            // this CTA's half of the B tile: SwiGLU W1 (CTA 0) / W3 (CTA 1) rows, else rows
+            // 128 r.. of the 256-row W tile
+            const CUtensorMap *bm = (a.epi == EPI_SWIGLU && rank == 1) ? &tmB3 : &tmB;
+            const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                 : ti.e * a.N + ti.n * BN + rank * (BN / 2);
+            const int4 gr = gather ? gather_rows(a, ti.row0, ti.rows, lane) : make_int4(0, 0, 0, 0);
+            for (int kb = 0; kb < nk; ++kb) {
+                int go = 1;
+                if (lane == 0)
+                    go = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim);
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
                 }
-            }
-            // A slot is released only after the leader's MMAs consumed it, hence after every copy
-            // into it (this CTA's included) landed: wait for all slots once more before exiting.
-            if (ok) {
-                for (int i = 0; i < STAGES2; ++i) {
-                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim))
-                        break;
-                    if (++stage == STAGES2) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);  // leader's barrier
+                if (lane == 0) {
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_HALF + B_HALF));
+                    if (!gather) tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
+                    tma_load_2d_pair(sB + stage * B_HALF, bm, fb, kb * BK, brow);
+                }
+                if (gather) {
+                    __syncwarp();
+                    tma_gather4_pair(sA + stage * A_HALF + lane * 512, &tmA, fb, kb * BK, gr.x,
+                                     gr.y, gr.z, gr.w);
+                }
+                if (++stage == STAGES2) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
         }
+        // A slot is released only after the leader's MMAs consumed it, hence after every copy
+        // into it (this CTA's included) landed: wait for all slots once more before exiting.
+        if (ok && lane == 0) {
+            for (int i = 0; i < STAGES2; ++i) {
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim))
+                    break;
+                if (++stage == STAGES2) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             int stage = 0, acc = 0;
@@ -552,12 +618,16 @@ int pair_clusters() {
     return cache[dev];
 }
 
+// A_rows / A_src_rows: fused gather of A (see TcArgs); out_token / out_gate: fused scatter.
 cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P, int E, int K,
                         int N, int epi, const int32_t *offsets, const float *bias, void *out,
-                        uint32_t *dev_status, const FaultHook &hook, cudaStream_t s) {
-    // every B box is 128 rows: one half of the 256-row B tile
+                        uint32_t *dev_status, const FaultHook &hook, cudaStream_t s,
+                        const int32_t *A_rows = nullptr, int64_t A_src_rows = 0,
+                        const int32_t *out_token = nullptr, const float *out_gate = nullptr) {
+    // every B box is 128 rows: one half of the 256-row B tile; a gathered A reads one-row boxes
     CUtensorMap mA, mB, mB3;
-    if (!make_map(&mA, A, P, K, BM)) return cudaErrorInvalidValue;
+    if (A_rows ? !make_map(&mA, A, A_src_rows, K, 1) : !make_map(&mA, A, P, K, BM))
+        return cudaErrorInvalidValue;
     if (!make_map(&mB, B, (int64_t)E * N, K, BN / 2)) return cudaErrorInvalidValue;
     if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, BN / 2))
         return cudaErrorInvalidValue;
@@ -575,10 +645,14 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.epi = epi;
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold_loads = hook.withhold;
+    a.a_rows = A_rows;
+    a.a_src_rows = A_src_rows;
+    a.out_token = out_token;
+    a.out_gate = out_gate;
     // The CTA-pair kernel when experts average at least four M tiles (on an expert's odd last
     // tile the second CTA computes masked rows, a small loss there).
     const int clusters = pair_clusters();
-    const bool pair = clusters > 0 && P >= (int64_t)4 * BM * E;
+    const bool pair = clusters > 0 && P >= (int64_t)PAIR_MIN_TILES * BM * E;
     if (pair) {
         const int64_t units = ((P + 2 * BM - 1) / (2 * BM) + E) * (int64_t)a.n_tiles;
         int64_t ncl = clusters < units ? clusters : units;
@@ -612,12 +686,19 @@ cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t 
     const int64_t P = c.T * c.k;
     if (P == 0) return cudaSuccess;
     const bool swiglu = c.act == MOE_ACT_SWIGLU;
-    cudaError_t err = launch_gemm(b.x_perm, b.W1, b.W3, P, c.E, c.d, c.f,
+    const bool gather = b.gather_h != nullptr;
+    const bool scatter = b.scatter_y != nullptr;
+    if ((gather || scatter) && (b.sorted_token == nullptr || (scatter && b.gates == nullptr)))
+        return cudaErrorInvalidValue;
+    cudaError_t err = launch_gemm(gather ? b.gather_h : b.x_perm, b.W1, b.W3, P, c.E, c.d, c.f,
                                   swiglu ? EPI_SWIGLU : EPI_GELU, b.offsets,
-                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, hook, s);
+                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, hook, s,
+                                  gather ? b.sorted_token : nullptr, c.T);
     if (err != cudaSuccess) return err;
     return launch_gemm(b.H, b.W2, nullptr, P, c.E, c.f, c.d, EPI_STORE, b.offsets,
-                       c.has_bias ? b.b2 : nullptr, b.y_perm, b.dev_status, hook, s);
+                       c.has_bias ? b.b2 : nullptr, scatter ? b.scatter_y : b.y_perm,
+                       b.dev_status, hook, s, nullptr, 0, scatter ? b.sorted_token : nullptr,
+                       scatter ? b.gates : nullptr);
 }
 
 }  // namespace moe

@@ -124,6 +124,11 @@ struct FfnBufs {
     void *H;       // [P, f] workspace
     void *y_perm;  // [P, d]
     uint32_t *dev_status;
+    // fused variants (tensor-core path, moe_forward only):
+    const void *gather_h = nullptr;          // GEMM1 reads A rows h[sorted_token[r]] directly
+    const int32_t *sorted_token = nullptr;
+    void *scatter_y = nullptr;               // top-1: GEMM2 writes y[token] = g * expert(h)
+    const float *gates = nullptr;
 };
 cudaError_t launch_ffn_f32(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,

@@ -73,7 +73,8 @@ WsLayout ws_layout(const moe_config_t &c) {
     L.sorted_token = off;                 off = align_up(off + P * 4);
     L.slot_of = off;                      off = align_up(off + P * 4);
     L.aux = off;                          off = align_up(off + 4);
-    L.x_perm = off;                       off = align_up(off + P * (size_t)c.d * es);
+    L.x_perm = off;
+    if (!(c.fuse_gather && c.dtype == MOE_BF16)) off = align_up(off + P * (size_t)c.d * es);
     L.H = off;                            off = align_up(off + P * (size_t)c.f * es);
     L.y_perm = off;                       off = align_up(off + P * (size_t)c.d * es);
     L.total = off;
@@ -99,6 +100,7 @@ moe_status_t check_cfg(const moe_config_t *c) {
     if (c->k > 32) return MOE_ERR_UNSUPPORTED;
     if (c->has_bias && c->act == MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     if (!(c->capacity_factor >= 0.f) || !isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if (c->fuse_gather != 0 && c->fuse_gather != 1) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -281,14 +283,28 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
     if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_permute(c, h, sorted_token, offsets, x_perm, dev_status, s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    // Fused variants on the tensor-core path: with fuse_gather GEMM1 gathers its rows of h itself
+    // (no permuted copy), and a dropless top-1 layer's GEMM2 scatters g * output straight into y
+    // (no combine).
+    const bool tc = c.dtype == MOE_BF16;
+    const bool scatter = tc && c.k == 1 && capacity_of(c) < 0;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
+    fb.sorted_token = sorted_token;
+    if (tc && c.fuse_gather) {
+        fb.gather_h = h;
+    } else if ((e = launch_permute(c, h, sorted_token, offsets, x_perm, dev_status, s)) !=
+               cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
+    if (scatter) {
+        fb.scatter_y = y;
+        fb.gates = gates;
+    }
     if (ev_ffn0 && cudaEventRecord(ev_ffn0, s) != cudaSuccess) return MOE_ERR_CUDA;
     e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (ev_ffn1 && cudaEventRecord(ev_ffn1, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
+    if (!scatter && (e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     if ((e = launch_aux(c, counts, psum, aux_out, s)) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;

@@ -48,6 +48,7 @@ class Workload:
     router_bias_var: float | None
     seed: int
     capacity_factor: float = 0.0  # > 0: each expert keeps at most floor(factor T k / E) slots
+    fuse_gather: bool = False     # the layer call reads expert rows of h without a permuted copy
 
     @property
     def P(self) -> int:
@@ -145,11 +146,11 @@ def generate_router_inputs(w: Workload) -> dict[str, torch.Tensor | None]:
 def small(name: str = "small", *, T: int, d: int, f: int, E: int, k: int, act: str = ACT_SWIGLU,
           gate: str = GATE_RENORM, dtype: str = "bf16", has_bias: bool = False,
           router_bias_var: float | None = None, seed: int = 11,
-          capacity_factor: float = 0.0) -> Workload:
+          capacity_factor: float = 0.0, fuse_gather: bool = False) -> Workload:
     """A custom-shaped workload for parity cases (ragged tails, several tiles, edge cases)."""
     return Workload(name, T=T, d=d, f=f, E=E, k=k, act=act, gate=gate, dtype=dtype,
                     has_bias=has_bias, router_bias_var=router_bias_var, seed=seed,
-                    capacity_factor=capacity_factor)
+                    capacity_factor=capacity_factor, fuse_gather=fuse_gather)
 
 
 def random_biases(w: Workload, inputs: dict, seed: int) -> dict:

@@ -74,6 +74,25 @@ def test_invalid_configs_are_rejected(kw, expect):
     assert L.moe_forward(ctypes.byref(cfg), *([None] * 13), 0, None) == expect
 
 
+def test_fuse_gather_flag():
+    """fuse_gather takes 0 or 1; with bf16 it removes x_perm (P d 2 bytes, page-rounded) from the
+    workspace, with f32 it changes nothing."""
+    for dt in (B.MOE_BF16, B.MOE_F32):
+        base = B.config(T=1000, d=256, f=512, E=8, k=2, dtype=dt)
+        st0, n0 = _ws_size(base)
+        fused = B.config(T=1000, d=256, f=512, E=8, k=2, dtype=dt, fuse_gather=True)
+        st1, n1 = _ws_size(fused)
+        assert st0 == st1 == B.MOE_OK
+        if dt == B.MOE_BF16:
+            assert n0 - n1 == 2000 * 256 * 2
+        else:
+            assert n0 == n1
+    bad = B.config(T=64, d=128, f=256, E=8, k=2)
+    bad.fuse_gather = 2
+    assert _ws_size(bad)[0] == B.MOE_ERR_INVALID_ARG
+    assert B.lib().moe_forward(ctypes.byref(bad), *([None] * 13), 0, None) == B.MOE_ERR_INVALID_ARG
+
+
 def test_null_and_misaligned_pointers_are_rejected_on_the_host():
     cfg = B.config(T=64, d=128, f=256, E=8, k=2)
     L = B.lib()

@@ -47,6 +47,13 @@ SMALL = [
     # paired-CTA GEMM (experts of >= 4 M tiles): odd tile counts, ragged N tail, skew
     wl.small("paired_gelu_bias", T=2500, d=256, f=320, E=3, k=2, act=G, has_bias=True),
     wl.small("paired_swiglu_skewed", T=3000, d=128, f=256, E=4, k=2, router_bias_var=3.0),
+    # moe_forward with GEMM1 gathering its rows of h (single-CTA and paired kernels, ragged row
+    # counts that leave part of a 4-row gather past an expert's end), with and without top-1 scatter
+    wl.small("gather_ragged_k3", T=301, d=192, f=320, E=5, k=3, fuse_gather=True),
+    wl.small("gather_paired_gelu_bias", T=2500, d=256, f=320, E=3, k=2, act=G, has_bias=True,
+             fuse_gather=True),
+    wl.small("gather_top1_scatter", T=999, d=128, f=256, E=6, k=1, act=G, gate=wl.GATE_RAW_PROB,
+             has_bias=True, router_bias_var=1.0, fuse_gather=True),
 ]
 
 
@@ -55,6 +62,10 @@ def _inputs(w):
     if w.has_bias:
         inp = wl.random_biases(w, inp, seed=w.seed + 100)
     return inp
+
+
+def _fused_scatter(w) -> bool:
+    return w.dtype == "bf16" and w.k == 1 and w.capacity_factor == 0
 
 
 def _check_steps(w, inputs, ref, got):
@@ -109,10 +120,15 @@ def test_small_cases_step_by_step(w):
         if kept == 0:
             assert (got["y"].float() == 0).all()
     check_layer_output(w, ref, got["y"], skip_tokens=diff)
-    # the fused call runs the same kernels: identical bits
+    # moe_forward gathers its GEMM1 rows from h directly (same bytes as x_perm): identical bits,
+    # except where a dropless top-1 bf16 layer also fuses the combine into GEMM2 (one bf16
+    # rounding fewer), which is checked against the oracle instead
     fw = run_forward(w, dev)
     assert fw["status"] == B.MOE_OK
-    assert torch.equal(fw["y"], got["y"])
+    if _fused_scatter(w):
+        check_layer_output(w, ref, fw["y"], skip_tokens=diff)
+    else:
+        assert torch.equal(fw["y"], got["y"])
     assert torch.equal(fw["idx"], got["idx"]) and torch.equal(fw["counts"], got["counts"])
     assert fw["aux"].item() == got["aux"].item()
 
@@ -146,7 +162,10 @@ def test_full_size_workloads(name):
     print(f"{name}: near-tie tokens {len(diff)}, {stats}")
     got = run_steps(w, inputs, dev)
     _check_steps(w, inputs, ref, got)
-    assert torch.equal(got["y"], fw["y"])
+    if _fused_scatter(w):
+        check_layer_output(w, ref, got["y"], skip_tokens=diff)
+    else:
+        assert torch.equal(got["y"], fw["y"])
     if name == "decode":
         assert (got["counts"] > 0).all()
 
