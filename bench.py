@@ -272,9 +272,8 @@ def main() -> None:
     flops = w.expert_flops()
     tflops = flops / (ffn_ms * 1e-3) / 1e12
     peak = peaks["bf16_sustained"]
-    # router (+ weight split on the tensor-core path), dispatch, permute, GEMM1, GEMM2 (or the
-    # two f32 FFN launches), combine, aux
-    launches_per_step = 8 if (w.dtype == "bf16" and w.E <= 128 and w.T > 1024) else 7
+    # the library's own count of the kernels one moe_forward launches for this config
+    launches_per_step = B.moe_forward_launch_count(cfg)
     line = {
         "metric": METRIC,
         "value": D.job_tokens_per_s(T, world, ms),

@@ -182,7 +182,10 @@ moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const 
                           float *aux_out, void *stream);
 
 /* Steps 1-5 in one call. y [T, d] dtype (out); aux_out one float (out); topk_idx_out [T, k] and
- * counts_out [E] are optional copies of the routing (NULL to skip). Everything else lives in ws. */
+ * counts_out [E] are optional copies of the routing (NULL to skip). Everything else lives in ws.
+ * Same results as the step calls in sequence, bit for bit, except for a dropless (capacity_factor
+ * 0) top-1 bf16 layer: there the second expert GEMM writes y[t] = g * expert(h[t]) itself, with
+ * one bf16 rounding instead of two (no y_perm, no combine kernel). */
 moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
                          const float *b_r, const void *W1, const float *b1, const void *W3,
                          const void *W2, const float *b2, void *y, float *aux_out,
@@ -198,6 +201,11 @@ moe_status_t moe_forward_events(const moe_config_t *cfg, const void *h, const fl
                                 float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
                                 void *ws, size_t ws_bytes, void *stream, void *ffn_begin,
                                 void *ffn_end);
+
+/* Number of kernels one moe_forward call with `cfg` launches (device memsets not counted; 0 for
+ * T = 0). Host-only: reads no device state. MOE_ERR_INVALID_ARG for an invalid cfg or a NULL
+ * `kernels`. */
+moe_status_t moe_forward_launch_count(const moe_config_t *cfg, int32_t *kernels);
 
 /* Synchronise `stream`, read the device status word in ws, clear it, and return MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_INDEX (MOE_ERR_CUDA if the copy itself fails). */

@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "moe_forward_events": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    ctypes.c_size_t, _P, _P, _P],
             "moe_device_status": [_P, _P],
+            "moe_forward_launch_count": [_CFG, ctypes.POINTER(ctypes.c_int32)],
             "moe_debug_dispatch_timeout": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                            ctypes.c_uint64, _P],
             "moe_debug_expert_ffn_timeout": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -149,6 +150,14 @@ def moe_workspace_init(ws: torch.Tensor, stream=None) -> None:
 def moe_router_partials(cfg: moe_config_t) -> int:
     n = ctypes.c_int64()
     _check(lib().moe_router_partials(ctypes.byref(cfg), ctypes.byref(n)), "moe_router_partials")
+    return n.value
+
+
+def moe_forward_launch_count(cfg: moe_config_t) -> int:
+    """Kernels one moe_forward call with cfg launches (host-only)."""
+    n = ctypes.c_int32()
+    _check(lib().moe_forward_launch_count(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_forward_launch_count")
     return n.value
 
 

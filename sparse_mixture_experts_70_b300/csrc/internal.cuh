@@ -70,6 +70,8 @@ inline int64_t dispatch_chunks(const moe_config_t &c) {
 int64_t router_partial_rows(const moe_config_t &c);
 // Workspace bytes the router needs (the split router weights of the tensor-core path).
 size_t router_scratch_bytes(const moe_config_t &c);
+// Kernels one router call launches for T > 0 (the tensor-core path also splits W_r first).
+int router_launches(const moe_config_t &c);
 constexpr int ROUTER_TC_MAX_E = 128;   // tensor-core router: bf16 h, E <= 128
 constexpr int ROUTER_TC_TOKENS = 128;  // tokens per tensor-core router CTA
 size_t router_tc_scratch_bytes(const moe_config_t &c);

@@ -239,6 +239,18 @@ moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const 
     return from_cuda(launch_aux(*cfg, counts, psum_part, aux_out, static_cast<cudaStream_t>(stream)));
 }
 
+// The fused variants moe_forward takes on the tensor-core path: with fuse_gather GEMM1 gathers
+// its rows of h itself (no permuted copy); a dropless top-1 layer's GEMM2 scatters g * output
+// straight into y (no combine).
+struct ForwardPlan {
+    bool gather, scatter;
+};
+
+static ForwardPlan plan_of(const moe_config_t &c) {
+    const bool tc = c.dtype == MOE_BF16;
+    return {tc && c.fuse_gather != 0, tc && c.k == 1 && capacity_of(c) < 0};
+}
+
 static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const float *W_r,
                                  const float *b_r, const void *W1, const float *b1,
                                  const void *W3, const void *W2, const float *b2, void *y,
@@ -283,14 +295,11 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
     if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
-    // Fused variants on the tensor-core path: with fuse_gather GEMM1 gathers its rows of h itself
-    // (no permuted copy), and a dropless top-1 layer's GEMM2 scatters g * output straight into y
-    // (no combine).
-    const bool tc = c.dtype == MOE_BF16;
-    const bool scatter = tc && c.k == 1 && capacity_of(c) < 0;
+    const ForwardPlan plan = plan_of(c);
+    const bool scatter = plan.scatter;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
     fb.sorted_token = sorted_token;
-    if (tc && c.fuse_gather) {
+    if (plan.gather) {
         fb.gather_h = h;
     } else if ((e = launch_permute(c, h, sorted_token, offsets, x_perm, dev_status, s)) !=
                cudaSuccess) {
@@ -360,6 +369,20 @@ moe_status_t moe_debug_expert_ffn_timeout(const moe_config_t *cfg, const void *x
 }  // extern "C"
 
 extern "C" {
+
+moe_status_t moe_forward_launch_count(const moe_config_t *cfg, int32_t *kernels) {
+    const moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!kernels) return MOE_ERR_INVALID_ARG;
+    if (cfg->T == 0) {
+        *kernels = 0;
+        return MOE_OK;
+    }
+    const ForwardPlan plan = plan_of(*cfg);
+    // router (+ split), dispatch, permute, two FFN launches, combine, aux
+    *kernels = router_launches(*cfg) + 1 + (plan.gather ? 0 : 1) + 2 + (plan.scatter ? 0 : 1) + 1;
+    return MOE_OK;
+}
 
 moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
                          const float *b_r, const void *W1, const float *b1, const void *W3,

@@ -488,6 +488,8 @@ size_t router_scratch_bytes(const moe_config_t &c) {
     return router_path(c) == PATH_TC ? router_tc_scratch_bytes(c) : 0;
 }
 
+int router_launches(const moe_config_t &c) { return router_path(c) == PATH_TC ? 2 : 1; }
+
 cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
                                const float *b_r, int32_t *topk_idx, float *gates,
                                float *psum_part, void *scratch, uint32_t *dev_status,

@@ -93,6 +93,22 @@ def test_fuse_gather_flag():
     assert B.lib().moe_forward(ctypes.byref(bad), *([None] * 13), 0, None) == B.MOE_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("name,kw,expect", [
+    # router, dispatch, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine, aux
+    ("micro", {}, 7),
+    ("decode", {}, 7),
+    ("mixtral", {}, 8),                           # tensor-core router: W_r split + router
+    ("mixtral", {"fuse_gather": True}, 7),        # no permute
+    ("switch", {}, 7),                            # top-1: GEMM2 scatters into y, no combine
+    ("switch", {"capacity_factor": 1.0}, 8),      # drops possible: combine runs
+    ("switch", {"fuse_gather": True}, 6),
+    ("micro", {"T": 0}, 0),
+])
+def test_forward_launch_count(name, kw, expect):
+    w = wl.WORKLOADS[name].with_(**kw)
+    assert B.moe_forward_launch_count(B.config_for(w)) == expect
+
+
 def test_null_and_misaligned_pointers_are_rejected_on_the_host():
     cfg = B.config(T=64, d=128, f=256, E=8, k=2)
     L = B.lib()
