@@ -9,12 +9,14 @@ an independent replica of the layer on its own batch: there is no exchange on th
 scaling is weak and `value` is the tokens of all ranks over the slowest rank's time.
 
 The JSON line also carries:
-  e2e          the same metric through moe_forward with host buffers: pinned h copied in and y
-               (plus aux) copied out inside the timed region, every step;
+  e2e          the same metric through the C-ABI pipeline (moe_pipeline_submit) with host
+               buffers: every step copies its pinned h in and its y (plus aux) out inside the
+               timed region, the copies of neighbouring steps overlapping the layer computation;
   roofline     the dominant kernel (the grouped expert GEMM, launched twice per step: GEMM1 and
-               GEMM2) against the measured bf16 tensor peak: algorithmic flops of the two launches
-               over their CUDA-event duration, recorded by moe_forward_events on the launching
-               stream inside the timed region;
+               GEMM2) over its CUDA-event duration, recorded by moe_forward_events on the
+               launching stream inside the timed region: algorithmic flops against the measured
+               bf16 tensor peak when the FFN's flops per HBM byte exceed the ridge point of the
+               measured peaks, else its algorithmic bytes against the measured HBM bandwidth;
   cpu_baseline the double-precision oracle on this machine's host cores, on a bounded token
                sample of the same workload (rank 0, N = 1 only);
   clocks       nvidia-smi samples taken during the timed region.
@@ -237,41 +239,55 @@ def main() -> None:
     if st != B.MOE_OK:
         raise SystemExit(f"device status after timed region: {B.status_string(st)}")
 
-    # end to end through moe_forward with host buffers (pinned), copies inside the timed region
+    # end to end through the C-ABI pipeline with host buffers (pinned): every step copies its h in
+    # and its y + aux out; the copies of neighbouring steps overlap the layer computation
     h_host = inputs["h"].pin_memory()
     y_host = torch.empty((T, d), dtype=w.torch_dtype).pin_memory()
     aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    h_dev = torch.empty_like(dev["h"])
-
-    def e2e_step():
-        h_dev.copy_(h_host, non_blocking=True)
-        layer.forward(h_dev, stream)
-        y_host.copy_(layer.y, non_blocking=True)
-        aux_host.copy_(layer.aux, non_blocking=True)
-
+    pipe = B.Pipeline(cfg, layer.w, stream=stream)
     for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
+        pipe.submit(h_host, y_host, aux_host)
+    if pipe.device_status() != B.MOE_OK:
+        raise SystemExit("device status after e2e warm-up")
     e_start = torch.cuda.Event(enable_timing=True)
     e_stop = torch.cuda.Event(enable_timing=True)
     D.barrier()
     e_start.record(stream)
     for _ in range(args.steps):
-        e2e_step()
+        pipe.submit(h_host, y_host, aux_host)
+    pipe.join(stream)
     e_stop.record(stream)
     torch.cuda.synchronize()
     e_ms = e_start.elapsed_time(e_stop) / args.steps
-    if B.moe_device_status(layer.ws) != B.MOE_OK:
+    if pipe.device_status() != B.MOE_OK:
         raise SystemExit("device status after e2e region")
+    pipe.close()
 
     ms, e_ms, ffn_ms = D.max_over_ranks([ms, e_ms, ffn_ms], device="cuda")
     if rank != 0:
         D.shutdown()
         return
 
-    flops = w.expert_flops()
+    # The expert FFN's roofline: tensor-bound when its arithmetic intensity (flops per HBM byte
+    # it must move) is above the ridge point of the measured peaks, else HBM-bound (decode).
+    flops, nbytes = w.expert_flops(), w.ffn_bytes()
     tflops = flops / (ffn_ms * 1e-3) / 1e12
-    peak = peaks["bf16_sustained"]
+    gbs = nbytes / (ffn_ms * 1e-3) / 1e9
+    intensity = flops / nbytes
+    ridge = peaks["bf16_sustained"] * 1e12 / (peaks["hbm"] * 1e9)
+    traffic = MEASURED_TRAFFIC.get(w.name if not args.override else "")
+    if intensity >= ridge:
+        roofline = {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops,
+                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                    "frac": tflops / peaks["bf16_sustained"],
+                    "peak_kind": f"bf16 sustained ({peaks['source']})",
+                    "frac_of_burst": tflops / peaks["bf16"], "traffic": traffic,
+                    "flop_per_byte": intensity, "hbm_gbs": gbs}
+    else:
+        roofline = {"bound": "hbm", "kernel": GEMM_KERNEL, "achieved": gbs, "peak": peaks["hbm"],
+                    "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                    "peak_kind": f"HBM copy ({peaks['source']})", "traffic": traffic,
+                    "flop_per_byte": intensity, "tensor_tflops": tflops}
     # the library's own count of the kernels one moe_forward launches for this config
     launches_per_step = B.moe_forward_launch_count(cfg)
     line = {
@@ -293,11 +309,7 @@ def main() -> None:
                    "l2": f"inputs larger than L2 ({w.weight_bytes() / 1e9:.2f} GB of expert "
                          "weights read every step)"},
         "breakdown_ms": {"expert_ffn": ffn_ms, "router_dispatch_combine_aux": ms - ffn_ms},
-        "roofline": {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops,
-                     "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "frac_of_burst": tflops / peaks["bf16"],
-                     "traffic": MEASURED_TRAFFIC.get(w.name if not args.override else "")},
+        "roofline": roofline,
         "e2e": {"value": D.job_tokens_per_s(T, world, e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
                 "d2h_bytes_per_step": T * d * layer.y.element_size() + 4},

@@ -14,7 +14,8 @@
  *   - Pointers to tensors are DEVICE pointers (cudaMalloc'd or PyTorch-owned), caller-owned.
  *     The library allocates nothing and keeps no state between calls; all scratch lives in the
  *     caller's workspace `ws` (see moe_workspace_size) -- except for moe_build_dispatch_static,
- *     whose scratch is a static device array inside the library.
+ *     whose scratch is a static device array inside the library, and the pipeline objects of
+ *     moe_pipeline.h, which own their device buffers and streams.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call is
  *     asynchronous on that stream; results are valid once the stream reaches the call.
  *   - All tensors are dense row-major. "dtype" below is cfg->dtype: MOE_F32 (float) or MOE_BF16

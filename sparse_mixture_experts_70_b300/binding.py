@@ -68,6 +68,12 @@ def lib() -> ctypes.CDLL:
                                    ctypes.c_size_t, _P, _P, _P],
             "moe_device_status": [_P, _P],
             "moe_forward_launch_count": [_CFG, ctypes.POINTER(ctypes.c_int32)],
+            "moe_pipeline_create": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    ctypes.POINTER(ctypes.c_void_p)],
+            "moe_pipeline_submit": [_P, _P, _P, _P],
+            "moe_pipeline_join": [_P, _P],
+            "moe_pipeline_device_status": [_P],
+            "moe_pipeline_destroy": [_P],
             "moe_debug_dispatch_timeout": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                            ctypes.c_uint64, _P],
             "moe_debug_expert_ffn_timeout": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -282,3 +288,67 @@ class Layer:
         else:
             moe_forward_events(*args, ffn_events[0], ffn_events[1], stream)
         return self.y
+
+
+class Pipeline:
+    """moe_pipeline_*: batches of h in host memory through the layer, each batch's copy-in and
+    copy-out overlapped with the neighbouring batches' computation (include/moe_pipeline.h).
+    `weights` are device tensors (as for Layer); the layer runs on `stream` (default: the current
+    stream at construction). Host tensors passed to submit() are kept alive until
+    device_status() or close()."""
+
+    def __init__(self, cfg: moe_config_t, weights: dict, stream=None):
+        self.cfg = cfg
+        self.w = {k: v for k, v in weights.items() if k != "h"}
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        w = self.w
+        handle = ctypes.c_void_p()
+        _check(lib().moe_pipeline_create(ctypes.byref(cfg), _ptr(w["W_r"]), _ptr(w.get("b_r")),
+                                         _ptr(w["W1"]), _ptr(w.get("b1")), _ptr(w.get("W3")),
+                                         _ptr(w["W2"]), _ptr(w.get("b2")), _stream(self.stream),
+                                         ctypes.byref(handle)), "moe_pipeline_create")
+        self._handle = handle
+        self._pending = []
+        self._dtype = torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
+
+    def submit(self, h_host: torch.Tensor, y_host: torch.Tensor, aux_host: torch.Tensor) -> None:
+        """Enqueue one batch: h_host [T, d] -> y_host [T, d], aux_host [1] (host tensors)."""
+        shape = (self.cfg.T, self.cfg.d)
+        for t in (h_host, y_host):
+            if t.device.type != "cpu" or tuple(t.shape) != shape or t.dtype != self._dtype:
+                raise ValueError(f"host tensors of shape {shape} and dtype {self._dtype} expected")
+        if aux_host.device.type != "cpu" or aux_host.dtype != torch.float32 or aux_host.numel() < 1:
+            raise ValueError("aux_host: a float32 host tensor")
+        _check(lib().moe_pipeline_submit(self._handle, _ptr(h_host), _ptr(y_host), _ptr(aux_host)),
+               "moe_pipeline_submit")
+        self._pending.append((h_host, y_host, aux_host))
+
+    def join(self, stream=None) -> None:
+        """Make `stream` (default: the pipeline's stream) wait for every submitted batch."""
+        _check(lib().moe_pipeline_join(self._handle, _stream(stream if stream is not None
+                                                               else self.stream)),
+               "moe_pipeline_join")
+
+    def device_status(self) -> int:
+        """Wait for all submitted batches; read and clear the device status word."""
+        st = int(lib().moe_pipeline_device_status(self._handle))
+        self._pending.clear()
+        return st
+
+    def close(self) -> None:
+        if self._handle is not None and self._handle.value:
+            lib().moe_pipeline_destroy(self._handle)
+        self._handle = None
+        self._pending.clear()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

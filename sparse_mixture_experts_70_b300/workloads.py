@@ -71,6 +71,13 @@ class Workload:
         es = 4 if self.dtype == "f32" else 2
         return self.E * self.n_mats * self.d * self.f * es
 
+    def ffn_bytes(self) -> int:
+        """HBM bytes the grouped expert FFN must move at least (both GEMM launches): every
+        expert's weights once, the P permuted rows read, H [P, f] written and read back, and the
+        P output rows written."""
+        es = 4 if self.dtype == "f32" else 2
+        return self.weight_bytes() + self.P * (2 * self.d + 2 * self.f) * es
+
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 

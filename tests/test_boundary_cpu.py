@@ -109,6 +109,27 @@ def test_forward_launch_count(name, kw, expect):
     assert B.moe_forward_launch_count(B.config_for(w)) == expect
 
 
+def test_pipeline_arguments_are_checked_before_any_cuda_call():
+    L = B.lib()
+    out = ctypes.c_void_p(123)
+    bad = B.config(T=64, d=100, f=256, E=8, k=2)
+    assert L.moe_pipeline_create(ctypes.byref(bad), *([None] * 8), ctypes.byref(out)) == \
+        B.MOE_ERR_INVALID_ARG
+    assert out.value is None  # *out cleared
+    good = B.config(T=64, d=128, f=256, E=8, k=2)
+    # NULL weights, misaligned weights, NULL out
+    assert L.moe_pipeline_create(ctypes.byref(good), *([None] * 8), ctypes.byref(out)) == \
+        B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_create(ctypes.byref(good), 4, None, 18, None, 32, 64, None, None,
+                                 ctypes.byref(out)) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_create(ctypes.byref(good), 16, None, 32, None, 48, 64, None, None,
+                                 None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_submit(None, 16, 16, 16) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_join(None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_device_status(None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_destroy(None) == B.MOE_OK
+
+
 def test_null_and_misaligned_pointers_are_rejected_on_the_host():
     cfg = B.config(T=64, d=128, f=256, E=8, k=2)
     L = B.lib()
