@@ -68,13 +68,19 @@ inline int64_t dispatch_chunks(const moe_config_t &c) {
 
 // Rows of psum_part the router writes (one per router block; depends only on the shape).
 int64_t router_partial_rows(const moe_config_t &c);
-// Workspace bytes the router needs (the split router weights of the tensor-core path).
+// Workspace bytes the router needs (tensor-core path: the split router weights and the partial
+// logits).
 size_t router_scratch_bytes(const moe_config_t &c);
-// Kernels one router call launches for T > 0 (the tensor-core path also splits W_r first).
+// Kernels one router call launches for T > 0 (the tensor-core path: W_r split, logits, select).
 int router_launches(const moe_config_t &c);
 constexpr int ROUTER_TC_MAX_E = 128;   // tensor-core router: bf16 h, E <= 128
-constexpr int ROUTER_TC_TOKENS = 128;  // tokens per tensor-core router CTA
+constexpr int ROUTER_TC_TOKENS = 128;  // tokens per tensor-core logits tile
 size_t router_tc_scratch_bytes(const moe_config_t &c);
+// K chunks of the tensor-core logits (a pure function of the shape), the padded expert count
+// (row stride of the partial logits), and where the partial logits [S][T][Epad] f32 live.
+int router_tc_splits(const moe_config_t &c);
+int router_tc_epad(const moe_config_t &c);
+float *router_tc_logits(void *scratch, const moe_config_t &c);
 
 WsLayout ws_layout(const moe_config_t &c);
 
@@ -90,8 +96,8 @@ cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float
                                const float *b_r, int32_t *topk_idx, float *gates,
                                float *psum_part, void *scratch, uint32_t *dev_status,
                                cudaStream_t s);
+// W_r split and the partial logits on the tensor cores (the selection follows in router.cu).
 cudaError_t launch_router_tc(const moe_config_t &c, const void *h, const float *W_r,
-                             const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
                              void *scratch, uint32_t *dev_status, cudaStream_t s);
 
 struct DispatchBufs {

@@ -6,7 +6,7 @@
 // (Switch top-1). arjunjaggi.com "Mixture of Experts in LLMs", "Switch Transformers": the router
 // is kept in float32 while the rest runs in bfloat16.
 //
-// Four kernels share the work by shape (the choice is a pure function of the shape, so
+// Four paths share the work by shape (the choice is a pure function of the shape, so
 // moe_router_partials can tell the caller how many partial-sum rows there will be):
 //   router_splitd_kernel E <= 32 and few tokens: one token per block, the warps split d and read
 //                        W_r from L2 (latency-bound shapes such as decode).
@@ -15,8 +15,9 @@
 //                        lane-interleaved layout (conflict-free 16-byte reads); the E partial sums
 //                        are folded across lanes by a butterfly then a reduce-scatter, leaving
 //                        lane e with logit e. Bandwidth-bound on h.
-//   router_tc_kernel     bf16 h, E <= 128, more tokens than the split-d kernel takes: tensor
-//                        cores (router_tc.cu).
+//   router_logits_kernel bf16 h, E <= 128, more tokens than the split-d kernel takes: partial
+//                        logits on the tensor cores (router_tc.cu), then router_select_kernel,
+//                        warp per token, for the per-token step below.
 //   router_tile_kernel   everything else: a block owns BT tokens x all E experts and runs a
 //                        register-blocked f32 FMA contraction staged through shared memory.
 // All four end with the same per-token step: max, sum of exponentials and k rounds of arg-max
@@ -446,6 +447,166 @@ cudaError_t launch_k(K kern, const RouterArgs &a, int64_t blocks, size_t smem, c
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------------
+// selection after the tensor-core logits (router_tc.cu): warp per token
+
+constexpr int SEL_WARPS = 16;
+
+// Tokens per selection block: about two blocks per SM of a 148-SM part (a pure function of T,
+// which fixes the rows of psum_part), whole multiples of the warps.
+int select_tokens_per_block(int64_t T) {
+    int64_t tpb = (T + 295) / 296;
+    tpb = (tpb + SEL_WARPS - 1) / SEL_WARPS * SEL_WARPS;
+    return (int)(tpb < SEL_WARPS ? SEL_WARPS : tpb);
+}
+
+// A float's bits as an unsigned key with the same order (-inf lowest; no NaN here).
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The per-token step for the selection kernel: as route_token, but every exponential
+// ex = exp(z - zmax) is taken once and serves the softmax sum, the gates and p (returned in
+// p[m] = ex / sum, for the per-expert sums), and the warp-wide maxima use the redux unit on the
+// order-preserving keys (exact: the largest logit, then the lowest index among equal ones).
+template <int MAXM>
+__device__ __forceinline__ void select_token(const float (&v)[MAXM], int E, int k, int gate_mode,
+                                             int64_t tok, int32_t *idx, float *gates,
+                                             float (&p)[MAXM]) {
+    const int lane = threadIdx.x & 31;
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) lmax = fmaxf(lmax, v[m]);
+    const float zmax = key_float(__reduce_max_sync(0xffffffffu, order_key(lmax)));
+    float ex[MAXM], ssum = 0.f;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        ex[m] = lane + 32 * m < E ? expf(v[m] - zmax) : 0.f;
+        ssum += ex[m];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    const float inv = 1.f / ssum;
+    // k rounds of arg-max (larger logit first, lower index on ties); lane j keeps the j-th.
+    uint32_t chosen = 0;
+    int sel_e = -1;
+    float sel_x = 0.f;
+    for (int j = 0; j < k; ++j) {
+        // this lane's best remaining candidate (its lowest index among equal logits)
+        float bv = -INFINITY, bx = 0.f;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) {
+            const int e = lane + 32 * m;
+            if (e < E && !((chosen >> m) & 1u) && (v[m] > bv || be == 0x7fffffff)) {
+                bv = v[m];
+                be = e;
+                bx = ex[m];
+            }
+        }
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(bv));
+        const int win = (int)__reduce_min_sync(
+            0xffffffffu, (be != 0x7fffffff && order_key(bv) == kmax) ? (uint32_t)be : 0xffffffffu);
+        const float wx = __shfl_sync(0xffffffffu, bx, win & 31);
+        if ((win & 31) == lane) chosen |= 1u << (win >> 5);
+        if (lane == j) {
+            sel_e = win;
+            sel_x = wx;
+        }
+    }
+    float g;
+    if (gate_mode == MOE_GATE_RAW_PROB) {
+        g = sel_x * inv;
+    } else {
+        float gs = lane < k ? sel_x : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+        g = sel_x / gs;
+    }
+    if (lane < k) {
+        idx[tok * k + lane] = sel_e;
+        gates[tok * k + lane] = g;
+    }
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) p[m] = ex[m] * inv;
+}
+
+// Lane's logits of token tok before the bias: the sum over the S K chunks of zpart[s][tok][e]
+// (s = 0..S-1 in order), -inf for absent experts. With one chunk the loads are left in flight
+// (nothing consumes them here), so a call for the next token overlaps the current one.
+template <int MAXM>
+__device__ __forceinline__ void load_logits(const float *__restrict__ zpart, int S, int Epad,
+                                            int64_t T, int64_t tok, int E, float (&v)[MAXM]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        if (e >= E) {
+            v[m] = -INFINITY;
+        } else if (S == 1) {
+            v[m] = __ldg(zpart + tok * Epad + e);
+        } else {
+            float z = 0.f;
+            for (int s = 0; s < S; ++s) z += __ldg(zpart + ((int64_t)s * T + tok) * Epad + e);
+            v[m] = z;
+        }
+    }
+}
+
+// Warp per token over this block's tokens (the next token's logits loaded while the current one
+// is processed), then the block's sums of p per expert (per warp in token order, then over the
+// warps in order).
+template <int MAXM>
+__global__ void __launch_bounds__(SEL_WARPS * 32)
+    router_select_kernel(const float *__restrict__ zpart, int S, int Epad, int tpb,
+                         const RouterArgs a) {
+    __shared__ float wsum[SEL_WARPS][MAXM * 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E;
+    const int64_t t0 = (int64_t)blockIdx.x * tpb;
+    int64_t t_end = t0 + tpb;
+    if (t_end > a.T) t_end = a.T;
+    float bias[MAXM], acc[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        bias[m] = (a.b_r && e < E) ? __ldg(a.b_r + e) : 0.f;
+        acc[m] = 0.f;
+    }
+    int64_t tok = t0 + warp;
+    float v[MAXM];
+    if (tok < t_end) load_logits<MAXM>(zpart, S, Epad, a.T, tok, E, v);
+    while (tok < t_end) {
+        const int64_t nxt = tok + SEL_WARPS;
+        float vn[MAXM];
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) vn[m] = -INFINITY;
+        if (nxt < t_end) load_logits<MAXM>(zpart, S, Epad, a.T, nxt, E, vn);
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) v[m] += bias[m];  // -inf stays -inf for absent experts
+        float p[MAXM];
+        select_token<MAXM>(v, E, a.k, a.gate_mode, tok, a.idx, a.gates, p);
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) {
+            if (lane + 32 * m < E) acc[m] += p[m];
+            v[m] = vn[m];
+        }
+        tok = nxt;
+    }
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) wsum[warp][lane + 32 * m] = acc[m];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < SEL_WARPS; ++w) s += wsum[w][e];
+        a.psum[(int64_t)blockIdx.x * E + e] = s;
+    }
+}
+
 enum RouterPath { PATH_SPLITD, PATH_SMALL, PATH_TC, PATH_TILE };
 
 RouterPath router_path(const moe_config_t &c) {
@@ -476,7 +637,10 @@ int64_t router_partial_rows(const moe_config_t &c) {
             const int tpb = small_tokens_per_block(c.T);
             return (c.T + tpb - 1) / tpb;
         }
-        case PATH_TC: return (c.T + ROUTER_TC_TOKENS - 1) / ROUTER_TC_TOKENS;
+        case PATH_TC: {
+            const int tpb = select_tokens_per_block(c.T);
+            return (c.T + tpb - 1) / tpb;
+        }
         default: {
             const int bt = geometry(c.E).BT;
             return (c.T + bt - 1) / bt;
@@ -488,7 +652,7 @@ size_t router_scratch_bytes(const moe_config_t &c) {
     return router_path(c) == PATH_TC ? router_tc_scratch_bytes(c) : 0;
 }
 
-int router_launches(const moe_config_t &c) { return router_path(c) == PATH_TC ? 2 : 1; }
+int router_launches(const moe_config_t &c) { return router_path(c) == PATH_TC ? 3 : 1; }
 
 cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
                                const float *b_r, int32_t *topk_idx, float *gates,
@@ -497,8 +661,22 @@ cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float
     if (c.T == 0) return cudaSuccess;
     RouterArgs a{h, W_r, b_r, topk_idx, gates, psum_part, c.T, c.d, c.E, c.k, c.gate, 0};
     const RouterPath path = router_path(c);
-    if (path == PATH_TC)
-        return launch_router_tc(c, h, W_r, b_r, topk_idx, gates, psum_part, scratch, dev_status, s);
+    if (path == PATH_TC) {
+        cudaError_t err = launch_router_tc(c, h, W_r, scratch, dev_status, s);
+        if (err != cudaSuccess) return err;
+        const float *zpart = router_tc_logits(scratch, c);
+        const int S = router_tc_splits(c), Epad = router_tc_epad(c);
+        const int tpb = select_tokens_per_block(c.T);
+        const unsigned blocks = (unsigned)((c.T + tpb - 1) / tpb);
+        constexpr unsigned thr = SEL_WARPS * 32;
+        switch ((c.E + 31) / 32) {
+            case 1: router_select_kernel<1><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
+            case 2: router_select_kernel<2><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
+            case 3: router_select_kernel<3><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
+            default: router_select_kernel<4><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
+        }
+        return cudaGetLastError();
+    }
     const bool bf16 = c.dtype == MOE_BF16;
     if (path == PATH_SPLITD) {
         switch (small_emax(c.E)) {

@@ -97,11 +97,11 @@ def test_fuse_gather_flag():
     # router, dispatch, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine, aux
     ("micro", {}, 7),
     ("decode", {}, 7),
-    ("mixtral", {}, 8),                           # tensor-core router: W_r split + router
-    ("mixtral", {"fuse_gather": True}, 7),        # no permute
-    ("switch", {}, 7),                            # top-1: GEMM2 scatters into y, no combine
-    ("switch", {"capacity_factor": 1.0}, 8),      # drops possible: combine runs
-    ("switch", {"fuse_gather": True}, 6),
+    ("mixtral", {}, 9),                           # tensor-core router: split, logits, select
+    ("mixtral", {"fuse_gather": True}, 8),        # no permute
+    ("switch", {}, 8),                            # top-1: GEMM2 scatters into y, no combine
+    ("switch", {"capacity_factor": 1.0}, 9),      # drops possible: combine runs
+    ("switch", {"fuse_gather": True}, 7),
     ("micro", {"T": 0}, 0),
 ])
 def test_forward_launch_count(name, kw, expect):

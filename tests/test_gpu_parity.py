@@ -34,6 +34,10 @@ SMALL = [
     wl.small("tc_router_E100_raw_prob", T=300, d=128, f=128, E=100, k=1, act=G,
              gate=wl.GATE_RAW_PROB),
     wl.small("small_router_E20_f32", T=77, d=320, f=64, E=20, k=5, dtype="f32"),
+    # tensor-core logits: E = 32 (two accumulator chains), E = 8 with d split over two K chunks;
+    # token counts not a multiple of the 128-token tile
+    wl.small("tc_router_E32_chains", T=2000, d=256, f=128, E=32, k=2, router_bias_var=1.0),
+    wl.small("tc_router_E8_ksplit", T=1500, d=512, f=128, E=8, k=2),
     wl.small("smem_router_f32_many_tokens", T=1500, d=320, f=64, E=8, k=2, dtype="f32"),
     # capacity factor (drops): single-chunk and multi-chunk dispatch, f32 and bf16, everything
     # dropped (C = 0)
@@ -47,6 +51,15 @@ SMALL = [
     # paired-CTA GEMM (experts of >= 4 M tiles): odd tile counts, ragged N tail, skew
     wl.small("paired_gelu_bias", T=2500, d=256, f=320, E=3, k=2, act=G, has_bias=True),
     wl.small("paired_swiglu_skewed", T=3000, d=128, f=256, E=4, k=2, router_bias_var=3.0),
+    # paired kernel on an expert's odd last M tile (the second CTA's rows all masked): E = 1,
+    # k = 1 and E = 2, k = 2 fix the rows per expert at T, so the last tile holds 40, 100 or 128
+    # rows; SwiGLU with a ragged last N tile, GELU with biases, the top-1 scatter, and the
+    # fused gather
+    wl.small("pair_half_tail40_swiglu", T=552, d=256, f=320, E=1, k=1),
+    wl.small("pair_half_tail100_gelu", T=868, d=192, f=256, E=1, k=1, act=G, has_bias=True,
+             gate=wl.GATE_RAW_PROB),
+    wl.small("pair_half_tail128_k2", T=640, d=128, f=384, E=2, k=2),
+    wl.small("pair_half_gather", T=552, d=128, f=256, E=2, k=2, fuse_gather=True),
     # moe_forward with GEMM1 gathering its rows of h (single-CTA and paired kernels, ragged row
     # counts that leave part of a 4-row gather past an expert's end), with and without top-1 scatter
     wl.small("gather_ragged_k3", T=301, d=192, f=320, E=5, k=3, fuse_gather=True),
