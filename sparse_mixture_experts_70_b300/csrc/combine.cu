@@ -46,37 +46,59 @@ template <> struct Vec8<float> {
     }
 };
 
-// y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :]: one thread per (token,
-// 8-element vector), consecutive threads along the row; f32 FMA in j order, one rounding.
+constexpr int CB_THREADS = 256;
+constexpr int CB_SLOTS = 1024;  // slot entries a block stages in shared memory
+
+// y[t, :] = sum_{j<k} gates[t, j] * y_perm[slot_of[t k + j], :]. A block takes tpb consecutive
+// tokens: their slot indices and gates go to shared memory first (checked once), then one thread
+// per (token, 8-element vector) sums its rows with f32 FMA in j order and one rounding, the slots
+// in groups of 4 whose row loads are issued together.
 template <typename VT>
-__global__ void __launch_bounds__(256) combine_kernel(const void *__restrict__ y_perm,
-                                                      const int32_t *__restrict__ slot_of,
-                                                      const float *__restrict__ gates,
-                                                      void *__restrict__ y, int64_t T, int64_t P,
-                                                      int d, int k, uint32_t *dev_status) {
+__global__ void __launch_bounds__(CB_THREADS) combine_kernel(const void *__restrict__ y_perm,
+                                                             const int32_t *__restrict__ slot_of,
+                                                             const float *__restrict__ gates,
+                                                             void *__restrict__ y, int64_t T,
+                                                             int64_t P, int d, int k, int tpb,
+                                                             uint32_t *dev_status) {
+    __shared__ int32_t s_row[CB_SLOTS];
+    __shared__ float s_g[CB_SLOTS];
     const int v8 = d / 8;
-    const int64_t units = T * v8;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
-         u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = u / v8;
-        const int i = (int)(u - t * v8);
+    const int64_t t0 = (int64_t)blockIdx.x * tpb;
+    const int nt = (int)(T - t0 < tpb ? T - t0 : tpb);
+    const int ns = nt * k;
+    for (int q = threadIdx.x; q < ns; q += CB_THREADS) {
+        int32_t r = __ldg(slot_of + t0 * k + q);
+        if (r != -1 && (r < 0 || r >= P)) {  // -1: dropped by the capacity
+            report(dev_status, DEV_ERR_INDEX);
+            r = -1;
+        }
+        s_row[q] = r;
+        s_g[q] = __ldg(gates + t0 * k + q);
+    }
+    __syncthreads();
+    const int units = nt * v8;
+    for (int u = threadIdx.x; u < units; u += CB_THREADS) {
+        const int tl = u / v8, i = u - tl * v8;
+        const int32_t *rows = s_row + tl * k;
+        const float *gs = s_g + tl * k;
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int32_t row = __ldg(slot_of + t * k + j);
-            const float g = __ldg(gates + t * k + j);
-            if (row == -1) continue;  // dropped by the capacity: contributes nothing
-            if (row < 0 || row >= P) {
-                report(dev_status, DEV_ERR_INDEX);
-                continue;
-            }
-            Vec8<VT> v;
-            v.load(y_perm, (int64_t)row * v8 + i);
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            Vec8<VT> v[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, v.get(q), acc[q]);
+            for (int jj = 0; jj < 4; ++jj)
+                if (j0 + jj < k && rows[j0 + jj] >= 0)
+                    v[jj].load(y_perm, (int64_t)rows[j0 + jj] * v8 + i);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                if (j0 + jj < k && rows[j0 + jj] >= 0) {
+                    const float g = gs[j0 + jj];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, v[jj].get(q), acc[q]);
+                }
         }
-        Vec8<VT>::store(y, u, acc);
+        Vec8<VT>::store(y, (t0 + tl) * v8 + i, acc);
     }
 }
 
@@ -116,16 +138,20 @@ __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ c
 cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
                            const float *gates, void *y, uint32_t *dev_status, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
-    int64_t blocks = (c.T * (c.d / 8) + 255) / 256;
-    const int64_t cap = (int64_t)num_sms() * 8;
-    if (blocks > cap) blocks = cap;
+    // about 8 (token, vector) units per thread, within the staged slot budget, and at least
+    // about two blocks per SM when there are enough tokens
+    int64_t tpb = 8 * CB_THREADS / (c.d / 8);
+    if (tpb > c.T / (2 * num_sms())) tpb = c.T / (2 * num_sms());
+    if (tpb < 1) tpb = 1;
+    if (tpb * c.k > CB_SLOTS) tpb = CB_SLOTS / c.k;
+    const int64_t blocks = (c.T + tpb - 1) / tpb;
     const int64_t P = c.T * c.k;
     if (c.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
-            y_perm, slot_of, gates, y, c.T, P, c.d, c.k, dev_status);
+        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, CB_THREADS, 0, s>>>(
+            y_perm, slot_of, gates, y, c.T, P, c.d, c.k, (int)tpb, dev_status);
     else
-        combine_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(y_perm, slot_of, gates, y, c.T, P,
-                                                               c.d, c.k, dev_status);
+        combine_kernel<float><<<(unsigned)blocks, CB_THREADS, 0, s>>>(
+            y_perm, slot_of, gates, y, c.T, P, c.d, c.k, (int)tpb, dev_status);
     return cudaGetLastError();
 }
 

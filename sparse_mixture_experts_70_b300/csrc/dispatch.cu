@@ -233,44 +233,45 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
     }
 }
 
-// x_perm[r, :] = h[sorted_token[r], :] -- one thread per (row, 16-byte vector), consecutive
-// threads along the row, four vectors per thread in flight.
+// x_perm[slot_of[t k + j], :] = h[t, :] for every kept slot (slot_of >= 0; -1 marks a slot the
+// capacity dropped): one thread per (token, 16-byte vector), two units in flight per thread. Each
+// row of h is read once and stored to its token's k places, which is x_perm[r] =
+// h[sorted_token[r]] for every kept row r.
 __global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ h,
-                                                      const int32_t *__restrict__ sorted_token,
-                                                      uint4 *__restrict__ x_perm,
-                                                      const int32_t *__restrict__ rows_kept,
-                                                      int64_t P, int64_t T, int vecs,
+                                                      const int32_t *__restrict__ slot_of,
+                                                      uint4 *__restrict__ x_perm, int64_t P,
+                                                      int64_t T, int k, int vecs,
                                                       uint32_t *dev_status) {
-    int64_t rows = __ldg(rows_kept);
-    if (rows < 0 || rows > P) {
-        report(dev_status, DEV_ERR_INDEX);
-        rows = 0;
-    }
-    const int64_t units = rows * vecs;
+    const int64_t units = T * vecs;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u0 < units;
-         u0 += 4 * stride) {
-        uint4 v[4];
-        int64_t dst[4];
+         u0 += 2 * stride) {
+        uint4 v[2];
+        int64_t t[2];
+        int iv[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const int64_t u = u0 + q * stride;
-            dst[q] = -1;
+            t[q] = -1;
             if (u < units) {
-                const int64_t r = u / vecs;
-                const int i = (int)(u - r * vecs);
-                const int t = __ldg(sorted_token + r);
-                if (t < 0 || t >= T) {
-                    report(dev_status, DEV_ERR_INDEX);
-                } else {
-                    v[q] = __ldg(h + (int64_t)t * vecs + i);
-                    dst[q] = u;
-                }
+                t[q] = u / vecs;
+                iv[q] = (int)(u - t[q] * vecs);
+                v[q] = __ldg(h + u);
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (dst[q] >= 0) x_perm[dst[q]] = v[q];
+        for (int q = 0; q < 2; ++q) {
+            if (t[q] < 0) continue;
+            for (int j = 0; j < k; ++j) {
+                const int32_t r = __ldg(slot_of + t[q] * k + j);
+                if (r == -1) continue;
+                if (r < 0 || r >= P) {
+                    report(dev_status, DEV_ERR_INDEX);
+                    continue;
+                }
+                x_perm[(int64_t)r * vecs + iv[q]] = v[q];
+            }
+        }
     }
 }
 
@@ -385,19 +386,18 @@ cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_id
     return launch_dispatch(c, topk_idx, b, s);
 }
 
-cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
-                           const int32_t *offsets, void *x_perm, uint32_t *dev_status,
-                           cudaStream_t s) {
+cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *slot_of,
+                           void *x_perm, uint32_t *dev_status, cudaStream_t s) {
     const int64_t P = c.T * c.k;
     if (P == 0) return cudaSuccess;
     const int es = c.dtype == MOE_BF16 ? 2 : 4;
     const int vecs = c.d * es / 16;
-    int64_t blocks = (P * vecs + 1023) / 1024;
+    int64_t blocks = (c.T * vecs + 511) / 512;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    permute_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(h), sorted_token,
-                                                    static_cast<uint4 *>(x_perm), offsets + c.E, P,
-                                                    c.T, vecs, dev_status);
+    permute_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(h), slot_of,
+                                                    static_cast<uint4 *>(x_perm), P, c.T, c.k,
+                                                    vecs, dev_status);
     return cudaGetLastError();
 }
 

@@ -115,10 +115,9 @@ constexpr int64_t STATIC_LOOKBACK_CELLS = 65536;
 cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_idx,
                                    int32_t *counts, int32_t *offsets, int32_t *sorted_token,
                                    int32_t *slot_of, uint32_t *status, cudaStream_t s);
-// Rows copied: offsets[E] (read on the device; fewer than T k when a capacity drops slots).
-cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *sorted_token,
-                           const int32_t *offsets, void *x_perm, uint32_t *dev_status,
-                           cudaStream_t s);
+// x_perm[slot_of[s]] = h[s / k] for every kept slot s (slot_of = -1: dropped by a capacity).
+cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *slot_of,
+                           void *x_perm, uint32_t *dev_status, cudaStream_t s);
 cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
                            const float *gates, void *y, uint32_t *dev_status, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,

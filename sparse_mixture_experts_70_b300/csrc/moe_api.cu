@@ -173,7 +173,7 @@ moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx
                    reinterpret_cast<uint32_t *>(w + L.status)};
     st = from_cuda(launch_dispatch(*cfg, topk_idx, b, s));
     if (st != MOE_OK || !x_perm || cfg->T == 0) return st;
-    return from_cuda(launch_permute(*cfg, h, sorted_token, offsets, x_perm, b.dev_status, s));
+    return from_cuda(launch_permute(*cfg, h, slot_of, x_perm, b.dev_status, s));
 }
 
 moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *topk_idx,
@@ -194,7 +194,7 @@ moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *t
     st = from_cuda(launch_dispatch_static(*cfg, topk_idx, counts, offsets, sorted_token, slot_of,
                                           status, s));
     if (st != MOE_OK || !x_perm || cfg->T == 0) return st;
-    return from_cuda(launch_permute(*cfg, h, sorted_token, offsets, x_perm, status, s));
+    return from_cuda(launch_permute(*cfg, h, slot_of, x_perm, status, s));
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets,
@@ -301,7 +301,7 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     fb.sorted_token = sorted_token;
     if (plan.gather) {
         fb.gather_h = h;
-    } else if ((e = launch_permute(c, h, sorted_token, offsets, x_perm, dev_status, s)) !=
+    } else if ((e = launch_permute(c, h, slot_of, x_perm, dev_status, s)) !=
                cudaSuccess) {
         return MOE_ERR_CUDA;
     }
