@@ -19,6 +19,8 @@ The JSON line also carries:
                measured peaks, else its algorithmic bytes against the measured HBM bandwidth;
   cpu_baseline the double-precision oracle on this machine's host cores, on a bounded token
                sample of the same workload (rank 0, N = 1 only);
+  graph        the same step recorded once in a CUDA graph (Layer.capture) and replayed K times:
+               the launch-bound shapes' time without host launch cost;
   clocks       nvidia-smi samples taken during the timed region.
 --impl reference times the oracle itself (the method's plain statement) as the reference arm.
 """
@@ -263,7 +265,25 @@ def main() -> None:
         raise SystemExit("device status after e2e region")
     pipe.close()
 
-    ms, e_ms, ffn_ms = D.max_over_ranks([ms, e_ms, ffn_ms], device="cuda")
+    # the same step recorded once in a CUDA graph and replayed (host launch cost removed)
+    graph = layer.capture(dev["h"])
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    g_start = torch.cuda.Event(enable_timing=True)
+    g_stop = torch.cuda.Event(enable_timing=True)
+    D.barrier()
+    g_start.record()
+    for _ in range(args.steps):
+        graph.replay()
+    g_stop.record()
+    torch.cuda.synchronize()
+    g_ms = g_start.elapsed_time(g_stop) / args.steps
+    if B.moe_device_status(layer.ws) != B.MOE_OK:
+        raise SystemExit("device status after graph region")
+    del graph
+
+    ms, e_ms, ffn_ms, g_ms = D.max_over_ranks([ms, e_ms, ffn_ms, g_ms], device="cuda")
     if rank != 0:
         D.shutdown()
         return
@@ -314,6 +334,8 @@ def main() -> None:
                 "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
                 "d2h_bytes_per_step": T * d * layer.y.element_size() + 4},
         "gpu_launches": launches_per_step * args.steps,
+        "graph": {"value": D.job_tokens_per_s(T, world, g_ms), "unit": "tokens/s",
+                  "ms_per_step": g_ms},
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

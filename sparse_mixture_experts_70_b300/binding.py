@@ -289,6 +289,20 @@ class Layer:
             moe_forward_events(*args, ffn_events[0], ffn_events[1], stream)
         return self.y
 
+    def capture(self, h: torch.Tensor) -> "torch.cuda.CUDAGraph":
+        """Record one moe_forward on the device tensor h into a CUDA graph. ``replay()`` reruns
+        the layer on whatever h then holds (same buffer), writing self.y / aux / topk / counts.
+        A forward on a side stream first settles the library's one-time host queries."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.forward(h)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.forward(h)
+        return graph
+
 
 class Pipeline:
     """moe_pipeline_*: batches of h in host memory through the layer, each batch's copy-in and
