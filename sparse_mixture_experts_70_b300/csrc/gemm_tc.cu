@@ -243,9 +243,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int nk = a.K / BK;
     const unsigned long long lim = a.spin_limit_ns;
 
-    if (warp == 0) {
-        // The whole warp runs the producer loop: lane 0 waits for free slots and issues the B
-        // (and tiled A) copies; with a fused gather every lane copies 4 of the tile's 128 A rows.
+    if (warp == 0 && a.a_rows == nullptr) {
+        // Producer: lane 0 waits for free slots and issues the A and B copies.
+        if (lane == 0) {
+            int stage = 0, eh = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, last_phase = 0;  // per-stage bits
+            bool ok = !a.withhold_loads;
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                // B rows of this N tile: SwiGLU stacks 128 rows of W1 over 128 rows of W3
+                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                     : ti.e * a.N + ti.n * BN;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full + 8 * stage;
+                    const uint32_t sb = sB + stage * B_STAGE;
+                    mbar_expect_tx(fb, A_STAGE + B_STAGE);
+                    tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
+                    if (a.epi == EPI_SWIGLU) {
+                        tma_load_2d(sb, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
+                    } else {
+                        tma_load_2d(sb, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kb * BK, brow + BN / 2);
+                    }
+                    issued |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy into this CTA's ring must have landed before it may exit.
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    mbar_wait(bar_full + 8 * s, (last_phase >> s) & 1u, nullptr, a.dev_status, lim);
+        }
+    } else if (warp == 0) {
+        // Producer with a fused gather: the whole warp runs the loop; lane 0 waits for free
+        // slots and issues the B copies, and every lane copies 4 of the tile's 128 A rows.
         const bool gather = a.a_rows != nullptr;
         int stage = 0, eh = 0;
         uint32_t phase = 0;
@@ -465,8 +506,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int nk = a.K / BK;
     const unsigned long long lim = a.spin_limit_ns;
 
-    if (warp == 0) {
-        // The whole warp runs the producer loop (see the single-CTA kernel).
+    if (warp == 0 && a.a_rows == nullptr) {
+        // Producer: lane 0 waits for free slots and issues this CTA's A and B copies, which
+        // complete on the leader's barrier.
+        if (lane == 0) {
+            int stage = 0, eh = 0;
+            uint32_t phase = 0;
+            bool ok = !a.withhold_loads;
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                // this CTA's half of the B tile: SwiGLU W1 (CTA 0) / W3 (CTA 1) rows, else rows
+                // 128 r.. of the 256-row W tile
+                const CUtensorMap *bm = (a.epi == EPI_SWIGLU && rank == 1) ? &tmB3 : &tmB;
+                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                     : ti.e * a.N + ti.n * BN + rank * (BN / 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);  // leader's barrier
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_HALF + B_HALF));
+                    tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
+                    tma_load_2d_pair(sB + stage * B_HALF, bm, fb, kb * BK, brow);
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // A slot is released only after the leader's MMAs consumed it, hence after every copy
+            // into it (this CTA's included) landed: wait for all slots once more before exiting.
+            if (ok) {
+                for (int i = 0; i < STAGES2; ++i) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim))
+                        break;
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 0) {
+        // Producer with a fused gather: the whole warp runs the loop (see the single-CTA
+        // kernel).
         const bool gather = a.a_rows != nullptr;
         int stage = 0, eh = 0;
         uint32_t phase = 0;
