@@ -60,6 +60,12 @@ SMALL = [
              gate=wl.GATE_RAW_PROB),
     wl.small("pair_half_tail128_k2", T=640, d=128, f=384, E=2, k=2),
     wl.small("pair_half_gather", T=552, d=128, f=256, E=2, k=2, fuse_gather=True),
+    # paired GEMM with more units than clusters and a partial last wave (308 / 88 units of
+    # 256 x 256 for the SwiGLU layer, 200 / 80 for the top-1 GELU layer with biases and the fused
+    # scatter) and long K loops (d = 1024, f = 1792 / 2560)
+    wl.small("split_tail_swiglu_k2", T=2600, d=1024, f=1792, E=2, k=2),
+    wl.small("split_tail_gelu_top1", T=5120, d=1024, f=2560, E=1, k=1, act=G, has_bias=True,
+             gate=wl.GATE_RAW_PROB),
     # moe_forward with GEMM1 gathering its rows of h (single-CTA and paired kernels, ragged row
     # counts that leave part of a 4-row gather past an expert's end), with and without top-1 scatter
     wl.small("gather_ragged_k3", T=301, d=192, f=320, E=5, k=3, fuse_gather=True),
