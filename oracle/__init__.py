@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_dispatch_capacity.argtypes = [I64, I32, I32, P, I64, P, P, P, P]
         L.oracle_aux_loss.argtypes = [I64, I32, I32, P, P]
         L.oracle_aux_loss.restype = D
+        L.oracle_selection_keys.argtypes = [I64, I32, P, P, P]
+        L.oracle_update_sel_bias.argtypes = [I64, I32, I32, P, D, P, P]
+        L.oracle_zloss.argtypes = [I64, I32, P]
+        L.oracle_zloss.restype = D
         L.oracle_param_count.argtypes = [I32, I64, I64, I32, I32, I32, I64, I64, I32, P, P]
         L.oracle_gelu_tanh.argtypes = [D]
         L.oracle_gelu_tanh.restype = D
@@ -248,6 +252,33 @@ def aux_loss(counts: np.ndarray, p: np.ndarray, k: int) -> float:
     return float(lib().oracle_aux_loss(T, E, k, _ptr(counts), _ptr(p)))
 
 
+def selection_keys(p: np.ndarray, b) -> np.ndarray:
+    """Keys p + b of the selection-only routing bias (its top-k is the biased choice)."""
+    p = _np(p, np.float64)
+    T, E = p.shape
+    b = _np(np.asarray(b, dtype=np.float64).reshape(E), np.float64)
+    key = np.empty((T, E), np.float64)
+    lib().oracle_selection_keys(T, E, _ptr(p), _ptr(b), _ptr(key))
+    return key
+
+
+def update_sel_bias(counts: np.ndarray, T: int, k: int, gamma: float, b) -> np.ndarray:
+    """One step of the routing-bias update: +gamma below the mean load, -gamma above."""
+    counts = _np(counts, np.int32)
+    E = counts.shape[0]
+    b = _np(np.asarray(b, dtype=np.float64).reshape(E), np.float64)
+    out = np.empty(E, np.float64)
+    lib().oracle_update_sel_bias(T, E, k, _ptr(counts), float(gamma), _ptr(b), _ptr(out))
+    return out
+
+
+def zloss(z: np.ndarray) -> float:
+    """Router z-loss (1/T) sum_t (log sum_e exp z[t, e])^2."""
+    z = _np(z, np.float64)
+    T, E = z.shape
+    return float(lib().oracle_zloss(T, E, _ptr(z)))
+
+
 def param_count(n_layers, d, f, E, k, mats, shared_per_layer, shared_global, with_router=True):
     tot = ctypes.c_int64()
     act = ctypes.c_int64()
@@ -279,7 +310,11 @@ def route(w, inputs) -> dict:
     """Router, top-k, gates, dispatch and auxiliary value over all T tokens of workload w
     (with the workload's capacity limit when it has one)."""
     z, p = router(inputs["h"], inputs["W_r"], inputs.get("b_r"))
-    idx, bnd, ins = topk(z, w.k)
+    sel_bias = inputs.get("sel_bias")
+    if sel_bias is not None:  # selection-only routing bias: choose by p + b, gate by p
+        idx, bnd, ins = topk(selection_keys(p, sel_bias), w.k)
+    else:
+        idx, bnd, ins = topk(z, w.k)
     g = gates(z, p, idx, gate_code(w))
     factor = getattr(w, "capacity_factor", 0.0)
     if factor > 0:
@@ -290,7 +325,7 @@ def route(w, inputs) -> dict:
         counts, offsets, sorted_token, slot_of = dispatch(idx, w.E)
     aux = aux_loss(counts, p, w.k)
     return dict(z=z, p=p, idx=idx, boundary=bnd, inset=ins, g=g, counts=counts, offsets=offsets,
-                sorted_token=sorted_token, slot_of=slot_of, aux=aux, capacity=C)
+                sorted_token=sorted_token, slot_of=slot_of, aux=aux, zloss=zloss(z), capacity=C)
 
 
 def reference(w, inputs, tokens=None) -> dict:

@@ -21,7 +21,13 @@
  *   [LENSA-5] same page, Step 5 of 6 "Capacity & Dropped Tokens" (dropless grouping, MegaBlocks).
  *   [LENSA-6] same page, Step 6 of 6 "MoE in Practice" (Mixtral expert = 3 x 4096 x 14336).
  *   [JAGGI]   arjunjaggi.com "Mixture of Experts in LLMs: How Sparse Models Scale", sections
- *             "The Router" (Switch k = 1) and "Switch Transformers" (router kept in float32).
+ *             "The Router" (Switch k = 1) and "Switch Transformers" (router kept in float32); its
+ *             training section names the router z-loss of ST-MoE (Zoph et al., arXiv:2202.08906)
+ *             as a penalty on large router logits.
+ *   [LENSA-4] also: DeepSeek-V3 replaces the auxiliary loss by a per-expert routing bias that is
+ *             nudged up or down. The pages give neither formula; both are taken from the cited
+ *             papers (ST-MoE, router z-loss; DeepSeek-V3 Technical Report, auxiliary-loss-free
+ *             load balancing), as read below.
  *
  * Readings where the pages leave a step open (each is also listed with the design notes):
  *   - f_i = count_i / (T k), so that sum_i f_i = 1 and the auxiliary term is exactly 1 under
@@ -36,6 +42,13 @@
  *   - Capacity ([LENSA-5]): C = floor(factor T k / E); an expert keeps the first C of its slots
  *     in that order; a dropped slot contributes nothing and the kept gates are not renormalised;
  *     the auxiliary value uses the routed (pre-drop) counts.
+ *   - Router z-loss (ST-MoE): (1/T) sum_t (log sum_e exp z[t,e])^2 over the router logits z
+ *     (router bias included); its weight is the caller's.
+ *   - Selection-only routing bias (DeepSeek-V3): the k experts are chosen by the keys
+ *     p[t,e] + b[e] (p the full softmax of this router, the affinity its gates use), descending,
+ *     ties to the lower index; the gates, p and the auxiliary value stay those of the unbiased
+ *     router. After a step, b[e] moves by +gamma when expert e received fewer routing slots than
+ *     the mean T k / E, by -gamma when more, and not at all when equal.
  *
  * Precision: inputs are read exactly as stored (f32, or bf16 widened bit-exactly) and every sum,
  * product and transcendental is taken in double, in index order, with no intermediate rounding.
@@ -143,6 +156,43 @@ void oracle_gates(int64_t T, int32_t E, int32_t k, int32_t mode, const double *z
             for (int32_t j = 0; j < k; ++j) g[t * k + j] = exp(z[t * E + it[j]] - zmax) / s;
         }
     }
+}
+
+/* [LENSA-4] (DeepSeek-V3's routing bias, reading above): the selection keys p[t,e] + b[e]; the
+ * top-k of these keys (oracle_topk) is the biased choice. */
+void oracle_selection_keys(int64_t T, int32_t E, const double *p, const double *b, double *key)
+{
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t e = 0; e < E; ++e) key[t * E + e] = p[t * E + e] + b[e];
+}
+
+/* [LENSA-4] (reading above): b_out[e] = b_in[e] + gamma * sign(T k / E - counts[e]). */
+void oracle_update_sel_bias(int64_t T, int32_t E, int32_t k, const int32_t *counts, double gamma,
+                            const double *b_in, double *b_out)
+{
+    const double mean = (double)T * (double)k / (double)E;
+    for (int32_t e = 0; e < E; ++e) {
+        const double c = (double)counts[e];
+        b_out[e] = b_in[e] + (c < mean ? gamma : (c > mean ? -gamma : 0.0));
+    }
+}
+
+/* [JAGGI] (ST-MoE's router z-loss, reading above): (1/T) sum_t (log sum_e exp z[t,e])^2, the
+ * log-sum-exp taken as zmax + log sum_e exp(z - zmax). 0 for T = 0. */
+double oracle_zloss(int64_t T, int32_t E, const double *z)
+{
+    double acc = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        const double *zt = z + t * E;
+        double zmax = zt[0];
+        for (int32_t e = 1; e < E; ++e)
+            if (zt[e] > zmax) zmax = zt[e];
+        double s = 0.0;
+        for (int32_t e = 0; e < E; ++e) s += exp(zt[e] - zmax);
+        const double lse = zmax + log(s);
+        acc += lse * lse;
+    }
+    return T > 0 ? acc / (double)T : 0.0;
 }
 
 /* [LENSA-4] histogram of routing slots per expert, [LENSA-5] dropless grouping: a stable counting

@@ -507,3 +507,88 @@ def test_dropped_slots_contribute_nothing():
             assert (ref["y"][t] == 0).all()
     # the auxiliary value uses the routed (pre-drop) counts
     assert ref["counts"].sum() == w.P
+
+
+# ---------------------------------------------------------------------------------------------
+# router z-loss (ST-MoE, named by arjunjaggi.com) and the selection-only routing bias
+# (DeepSeek-V3, named by lensaml.com Step 4); the formulas are the cited papers'
+
+def test_zloss_closed_forms():
+    E = 8
+    # all logits equal to c: log-sum-exp = c + ln E
+    for c in (0.0, 1.5, -3.0):
+        z = np.full((5, E), c)
+        assert oracle.zloss(z) == pytest.approx((c + np.log(E)) ** 2, rel=1e-15)
+    # one expert: log-sum-exp is the logit itself
+    z1 = np.array([[0.5], [-2.0], [3.0]])
+    assert oracle.zloss(z1) == pytest.approx(np.mean(z1[:, 0] ** 2), rel=1e-15)
+    # one dominant logit: log-sum-exp -> that logit (the others add exp(-60) terms)
+    z = np.zeros((1, 4))
+    z[0, 2] = 60.0
+    assert oracle.zloss(z) == pytest.approx(60.0 ** 2, rel=1e-15)
+    assert oracle.zloss(np.zeros((0, 4))) == 0.0
+
+
+def test_zloss_matches_scipy_logsumexp():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(31)
+    z = rng.standard_normal((200, 13)) * 4.0
+    assert oracle.zloss(z) == pytest.approx(np.mean(logsumexp(z, axis=1) ** 2), rel=1e-13)
+
+
+def test_biased_selection_brute_force_and_unbiased_gates():
+    """The chosen set is the unique S with min over S of p + b > max outside S (random keys have
+    no ties); the gates are the unbiased ones: RENORM = p_j / sum_S p, RAW_PROB = p_j."""
+    rng = np.random.default_rng(33)
+    for E, k in [(4, 1), (5, 2), (6, 3), (6, 5)]:
+        z = rng.standard_normal((40, E))
+        p = np.exp(z - z.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        b = rng.standard_normal(E) * 0.3
+        key = oracle.selection_keys(p, b)
+        np.testing.assert_array_equal(key, p + b)
+        idx, _, _ = oracle.topk(key, k)
+        for t in range(40):
+            best = [S for S in itertools.combinations(range(E), k)
+                    if min(key[t, list(S)]) > max([key[t, e] for e in range(E) if e not in S],
+                                                  default=-np.inf)]
+            assert len(best) == 1 and set(idx[t]) == set(best[0])
+            assert list(idx[t]) == sorted(idx[t], key=lambda e: -key[t, e])
+        g = oracle.gates(z, p, idx, oracle.RENORM)
+        ps = np.take_along_axis(p, idx, 1)
+        np.testing.assert_allclose(g, ps / ps.sum(1, keepdims=True), rtol=1e-13)
+        np.testing.assert_allclose(oracle.gates(z, p, idx, oracle.RAW_PROB), ps, rtol=0, atol=0)
+
+
+def test_biased_selection_special_cases():
+    rng = np.random.default_rng(34)
+    z = rng.standard_normal((64, 6))
+    p = np.exp(z) / np.exp(z).sum(1, keepdims=True)
+    # no bias: the same choice as by the logits (softmax is monotone)
+    np.testing.assert_array_equal(oracle.topk(oracle.selection_keys(p, np.zeros(6)), 2)[0],
+                                  oracle.topk(z, 2)[0])
+    # a bias above 1 puts its expert first for every token; one below -1 keeps it out
+    b = np.zeros(6)
+    b[4], b[1] = 2.0, -2.0
+    idx = oracle.topk(oracle.selection_keys(p, b), 3)[0]
+    assert (idx[:, 0] == 4).all() and not (idx == 1).any()
+
+
+def test_sel_bias_update_rule():
+    counts = np.array([5, 2, 3, 6], np.int32)          # T k = 16, mean load 4
+    out = oracle.update_sel_bias(counts, T=8, k=2, gamma=0.125, b=[0.0, 1.0, -1.0, 0.5])
+    np.testing.assert_array_equal(out, [-0.125, 1.125, -0.875, 0.375])
+    even = oracle.update_sel_bias(np.array([4, 4, 4, 4], np.int32), T=8, k=2, gamma=0.3, b=[0.1] * 4)
+    np.testing.assert_array_equal(even, [0.1] * 4)
+
+
+def test_route_with_sel_bias_keeps_unbiased_p_and_aux():
+    w = wl.small(T=120, d=32, f=32, E=6, k=2, act=wl.ACT_GELU_TANH, dtype="f32")
+    inp = wl.generate(w)
+    plain = oracle.route(w, inp)
+    b = np.array([0.3, 0, 0, 0, -0.3, 0.1])
+    biased = oracle.route(w, dict(inp, sel_bias=torch.tensor(b, dtype=torch.float32)))
+    np.testing.assert_array_equal(plain["p"], biased["p"])
+    assert plain["zloss"] == biased["zloss"]
+    assert (biased["counts"][0] > plain["counts"][0]) and (biased["counts"][4] < plain["counts"][4])
+    assert biased["aux"] == pytest.approx(oracle.aux_loss(biased["counts"], biased["p"], w.k))
