@@ -187,7 +187,8 @@ def main() -> None:
     w = wl.WORKLOADS[args.workload]
     if args.override:
         kv = dict(item.split("=") for item in args.override.split(","))
-        w = w.with_(name=w.name + "_override", **{k_: int(v) for k_, v in kv.items()})
+        w = w.with_(name=w.name + "_override",
+                    **{k_: (float(v) if "." in v or "e" in v else int(v)) for k_, v in kv.items()})
     if args.warmup < 3:
         args.warmup = 3
 

@@ -93,7 +93,7 @@ moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
 /* Zero the workspace header (status word and dispatch flags) on `stream`. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
-/* Number of floats of the router's per-block probability sums, psum_part [rows, E]. */
+/* Rows of the router's per-block partial sums psum_part [rows, E + 1]. */
 moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows);
 
 /* Steps 1-2. Router, softmax and top-k (lensaml.com "Mixture of Experts", Step 2 "The Router"
@@ -101,16 +101,26 @@ moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows);
  * the router is kept in f32).
  *   h        [T, d] dtype           input activations
  *   W_r      [d, E] float           router weight;  b_r [E] float or NULL
- *   topk_idx [T, k] int32  (out)    chosen experts, logits descending, ties to the lower index
+ *   sel_bias [E] float or NULL      selection-only routing bias b (lensaml.com Step 4 names
+ *            DeepSeek-V3's per-expert routing bias that replaces the auxiliary loss; the rule is
+ *            the DeepSeek-V3 Technical Report's auxiliary-loss-free balancing): the k experts are
+ *            chosen by p + b instead of the logits; the gates, p (hence psum_part and the
+ *            auxiliary value) stay those of the unbiased router. See moe_update_sel_bias.
+ *   topk_idx [T, k] int32  (out)    chosen experts, keys descending (the logits, or p + b),
+ *                                   ties to the lower index
  *   gates    [T, k] float  (out)    gate of each chosen expert (RENORM or RAW_PROB)
- *   psum_part [moe_router_partials rows, E] float (out) per-block sums of p over tokens, in a
- *            fixed order (input of moe_aux_loss).
- *   ws       workspace (moe_workspace_size bytes): for bf16 h and 32 < E <= 128 the router runs
- *            on the tensor cores with W_r split exactly into three bf16 pieces stored in ws.
- * Logits are accumulated in f32 from the stored h (every product exact); exp is CUDA's expf. */
+ *   psum_part [moe_router_partials rows, E + 1] float (out) per-block sums in a fixed order:
+ *            columns 0..E-1 the sums of p over the block's tokens (input of the auxiliary value),
+ *            column E the sum of (log sum_e exp z[t, e])^2 (input of the router z-loss).
+ *   ws       workspace (moe_workspace_size bytes): for bf16 h and E <= 128 with more tokens than
+ *            the few-token path takes, the logits run on the tensor cores with W_r split exactly
+ *            into three bf16 pieces stored in ws, and their partial sums are staged in ws.
+ * Logits are accumulated in f32 from the stored h (every product exact); exp and log are CUDA's
+ * expf and logf. */
 moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float *W_r,
-                             const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
-                             void *ws, size_t ws_bytes, void *stream);
+                             const float *b_r, const float *sel_bias, int32_t *topk_idx,
+                             float *gates, float *psum_part, void *ws, size_t ws_bytes,
+                             void *stream);
 
 /* Step 3. Dispatch (lensaml.com "Mixture of Experts", Step 4 "Load Balancing": the histogram of
  * routing slots per expert; Step 5 "Capacity & Dropped Tokens": dropless grouping of any number
@@ -177,31 +187,43 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int3
 
 /* Step 5b. Auxiliary load-balancing value (lensaml.com "Mixture of Experts", Step 4):
  *   aux = E . sum_e f_e P_e,  f_e = counts[e] / (T k),  P_e = (1/T) sum_t p[t, e]
- * (the weight alpha is the caller's). Reduced in a fixed order. aux_out: one float (device).
- * T = 0 gives 0. */
+ * (the weight alpha is the caller's), and the router z-loss (arjunjaggi.com "Mixture of Experts
+ * in LLMs" names ST-MoE's z-loss, a penalty on large router logits; the formula is ST-MoE's,
+ * Zoph et al. 2022):
+ *   zloss = (1/T) sum_t (log sum_e exp z[t, e])^2     (z the router logits, b_r included)
+ * Both reduced in a fixed order. aux_out: one float (device); zloss_out: one float or NULL.
+ * T = 0 gives 0 for both. */
 moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const float *psum_part,
-                          float *aux_out, void *stream);
+                          float *aux_out, float *zloss_out, void *stream);
 
-/* Steps 1-5 in one call. y [T, d] dtype (out); aux_out one float (out); topk_idx_out [T, k] and
+/* One step of the selection-only routing bias (DeepSeek-V3's rule, as for sel_bias above):
+ * sel_bias[e] += gamma when expert e received fewer routing slots than the mean T k / E,
+ * -= gamma when more, unchanged when equal (compared exactly in integers). counts [E] int32 and
+ * sel_bias [E] float are device pointers; gamma must be finite. */
+moe_status_t moe_update_sel_bias(const moe_config_t *cfg, const int32_t *counts, float *sel_bias,
+                                 float gamma, void *stream);
+
+/* Steps 1-5 in one call. sel_bias [E] float or NULL as for moe_router_topk. y [T, d] dtype
+ * (out); aux_out one float (out); zloss_out one float (out) or NULL; topk_idx_out [T, k] and
  * counts_out [E] are optional copies of the routing (NULL to skip). Everything else lives in ws.
  * Same results as the step calls in sequence, bit for bit, except for a dropless (capacity_factor
  * 0) top-1 bf16 layer: there the second expert GEMM writes y[t] = g * expert(h[t]) itself, with
  * one bf16 rounding instead of two (no y_perm, no combine kernel). */
 moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
-                         const float *b_r, const void *W1, const float *b1, const void *W3,
-                         const void *W2, const float *b2, void *y, float *aux_out,
-                         int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
-                         void *stream);
+                         const float *b_r, const float *sel_bias, const void *W1,
+                         const float *b1, const void *W3, const void *W2, const float *b2,
+                         void *y, float *aux_out, float *zloss_out, int32_t *topk_idx_out,
+                         int32_t *counts_out, void *ws, size_t ws_bytes, void *stream);
 
 /* moe_forward that also records two caller-created CUDA events (cudaEvent_t, passed as void*) on
  * `stream`: ffn_begin right before the expert-FFN launches and ffn_end right after them, so that
  * a caller can time the dominant step live inside a longer run. Same results as moe_forward. */
 moe_status_t moe_forward_events(const moe_config_t *cfg, const void *h, const float *W_r,
-                                const float *b_r, const void *W1, const float *b1,
-                                const void *W3, const void *W2, const float *b2, void *y,
-                                float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
-                                void *ws, size_t ws_bytes, void *stream, void *ffn_begin,
-                                void *ffn_end);
+                                const float *b_r, const float *sel_bias, const void *W1,
+                                const float *b1, const void *W3, const void *W2,
+                                const float *b2, void *y, float *aux_out, float *zloss_out,
+                                int32_t *topk_idx_out, int32_t *counts_out, void *ws,
+                                size_t ws_bytes, void *stream, void *ffn_begin, void *ffn_end);
 
 /* Number of kernels one moe_forward call with `cfg` launches (device memsets not counted; 0 for
  * T = 0). Host-only: reads no device state. MOE_ERR_INVALID_ARG for an invalid cfg or a NULL

@@ -42,8 +42,9 @@ typedef struct moe_pipeline moe_pipeline_t;
  * (checked before any CUDA call), MOE_ERR_CUDA when an allocation or stream creation fails
  * (nothing is leaked). */
 moe_status_t moe_pipeline_create(const moe_config_t *cfg, const float *W_r, const float *b_r,
-                                 const void *W1, const float *b1, const void *W3, const void *W2,
-                                 const float *b2, void *stream, moe_pipeline_t **out);
+                                 const float *sel_bias, const void *W1, const float *b1,
+                                 const void *W3, const void *W2, const float *b2, void *stream,
+                                 moe_pipeline_t **out);
 
 /* Enqueue one batch and return without waiting:
  *   h_host   [T, d] dtype, host memory (read by the copy-in)

@@ -56,19 +56,20 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
             "moe_workspace_init": [_P, ctypes.c_size_t, _P],
             "moe_router_partials": [_CFG, ctypes.POINTER(ctypes.c_int64)],
-            "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+            "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_build_dispatch": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_build_dispatch_static": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
             "moe_expert_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_combine": [_CFG, _P, _P, _P, _P, _P],
-            "moe_aux_loss": [_CFG, _P, _P, _P, _P],
-            "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+            "moe_aux_loss": [_CFG, _P, _P, _P, _P, _P],
+            "moe_update_sel_bias": [_CFG, _P, _P, ctypes.c_float, _P],
+            "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                             ctypes.c_size_t, _P],
-            "moe_forward_events": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                   ctypes.c_size_t, _P, _P, _P],
+            "moe_forward_events": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, ctypes.c_size_t, _P, _P, _P],
             "moe_device_status": [_P, _P],
             "moe_forward_launch_count": [_CFG, ctypes.POINTER(ctypes.c_int32)],
-            "moe_pipeline_create": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P,
+            "moe_pipeline_create": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     ctypes.POINTER(ctypes.c_void_p)],
             "moe_pipeline_submit": [_P, _P, _P, _P],
             "moe_pipeline_join": [_P, _P],
@@ -172,9 +173,11 @@ def workspace(cfg: moe_config_t, device="cuda") -> torch.Tensor:
     return torch.zeros(max(moe_workspace_size(cfg), 1024), dtype=torch.uint8, device=device)
 
 
-def moe_router_topk(cfg, h, W_r, b_r, topk_idx, gates, psum_part, ws, stream=None) -> None:
-    _check(lib().moe_router_topk(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(topk_idx),
-                                 _ptr(gates), _ptr(psum_part), _ptr(ws),
+def moe_router_topk(cfg, h, W_r, b_r, topk_idx, gates, psum_part, ws, stream=None,
+                    sel_bias=None) -> None:
+    """psum_part: [moe_router_partials(cfg), E + 1] float; sel_bias: [E] float or None."""
+    _check(lib().moe_router_topk(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(sel_bias),
+                                 _ptr(topk_idx), _ptr(gates), _ptr(psum_part), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)),
            "moe_router_topk")
 
@@ -207,17 +210,24 @@ def moe_combine(cfg, y_perm, slot_of, gates, y, stream=None) -> None:
                              _stream(stream)), "moe_combine")
 
 
-def moe_aux_loss(cfg, counts, psum_part, aux_out, stream=None) -> None:
+def moe_aux_loss(cfg, counts, psum_part, aux_out, stream=None, zloss_out=None) -> None:
     _check(lib().moe_aux_loss(ctypes.byref(cfg), _ptr(counts), _ptr(psum_part), _ptr(aux_out),
-                              _stream(stream)), "moe_aux_loss")
+                              _ptr(zloss_out), _stream(stream)), "moe_aux_loss")
+
+
+def moe_update_sel_bias(cfg, counts, sel_bias, gamma: float, stream=None) -> None:
+    """One step of the selection-only routing bias: +gamma below the mean load, -gamma above."""
+    _check(lib().moe_update_sel_bias(ctypes.byref(cfg), _ptr(counts), _ptr(sel_bias),
+                                     float(gamma), _stream(stream)), "moe_update_sel_bias")
 
 
 def moe_forward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out, counts_out, ws,
-                stream=None) -> None:
-    _check(lib().moe_forward(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(W1), _ptr(b1),
-                             _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y), _ptr(aux_out),
-                             _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
-                             ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+                stream=None, sel_bias=None, zloss_out=None) -> None:
+    _check(lib().moe_forward(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(sel_bias),
+                             _ptr(W1), _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y),
+                             _ptr(aux_out), _ptr(zloss_out), _ptr(topk_idx_out),
+                             _ptr(counts_out), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream)), "moe_forward")
 
 
 def moe_debug_dispatch_timeout(cfg, topk_idx, counts, offsets, sorted_token, slot_of, ws,
@@ -241,15 +251,17 @@ def moe_debug_expert_ffn_timeout(cfg, x_perm, offsets, W1, b1, W3, W2, b2, y_per
 
 
 def moe_forward_events(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out,
-                       counts_out, ws, ffn_begin, ffn_end, stream=None) -> None:
+                       counts_out, ws, ffn_begin, ffn_end, stream=None, sel_bias=None,
+                       zloss_out=None) -> None:
     """moe_forward recording torch.cuda.Event ffn_begin / ffn_end around the expert FFN."""
     for ev in (ffn_begin, ffn_end):
         if not ev.cuda_event:  # torch creates the CUDA event on its first record
             ev.record(stream if isinstance(stream, torch.cuda.Stream)
                       else torch.cuda.current_stream())
-    _check(lib().moe_forward_events(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(W1),
-                                    _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2), _ptr(y),
-                                    _ptr(aux_out), _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
+    _check(lib().moe_forward_events(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r),
+                                    _ptr(sel_bias), _ptr(W1), _ptr(b1), _ptr(W3), _ptr(W2),
+                                    _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(zloss_out),
+                                    _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream),
                                     ffn_begin.cuda_event, ffn_end.cuda_event),
            "moe_forward_events")
@@ -264,7 +276,9 @@ def moe_device_status(ws, stream=None) -> int:
 # convenience: the whole layer on tensors already on the device
 
 class Layer:
-    """Holds device copies of a layer's weights and a workspace; ``forward(h)`` calls moe_forward."""
+    """Holds device copies of a layer's weights (and an optional "sel_bias" [E] float, the
+    selection-only routing bias) and a workspace; ``forward(h)`` calls moe_forward, writing y,
+    aux, zloss, topk_idx and counts."""
 
     def __init__(self, cfg: moe_config_t, weights: dict, device="cuda"):
         self.cfg = cfg
@@ -275,6 +289,7 @@ class Layer:
         dt = torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
         self.y = torch.empty((cfg.T, cfg.d), dtype=dt, device=dev)
         self.aux = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.zloss = torch.zeros(1, dtype=torch.float32, device=dev)
         self.topk_idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
         self.counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
 
@@ -283,10 +298,11 @@ class Layer:
         w = self.w
         args = (self.cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"), w["W2"],
                 w.get("b2"), self.y, self.aux, self.topk_idx, self.counts, self.ws)
+        extra = dict(sel_bias=w.get("sel_bias"), zloss_out=self.zloss)
         if ffn_events is None:
-            moe_forward(*args, stream)
+            moe_forward(*args, stream, **extra)
         else:
-            moe_forward_events(*args, ffn_events[0], ffn_events[1], stream)
+            moe_forward_events(*args, ffn_events[0], ffn_events[1], stream, **extra)
         return self.y
 
     def capture(self, h: torch.Tensor) -> "torch.cuda.CUDAGraph":
@@ -318,7 +334,8 @@ class Pipeline:
         w = self.w
         handle = ctypes.c_void_p()
         _check(lib().moe_pipeline_create(ctypes.byref(cfg), _ptr(w["W_r"]), _ptr(w.get("b_r")),
-                                         _ptr(w["W1"]), _ptr(w.get("b1")), _ptr(w.get("W3")),
+                                         _ptr(w.get("sel_bias")), _ptr(w["W1"]),
+                                         _ptr(w.get("b1")), _ptr(w.get("W3")),
                                          _ptr(w["W2"]), _ptr(w.get("b2")), _stream(self.stream),
                                          ctypes.byref(handle)), "moe_pipeline_create")
         self._handle = handle

@@ -102,35 +102,54 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const void *__restr
     }
 }
 
-// aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T), reduced in a fixed order:
-// thread (g, e) of the block sums rows g, g + G, g + 2G, ... (G = 1024 / E groups), then thread e
-// adds the G group sums in g order, then thread 0 adds the E terms in e order.
+// aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T) and the router z-loss
+// (sum_b psum_part[b, E]) / T, reduced in a fixed order: thread (g, c) of the block sums rows
+// g, g + G, g + 2G, ... of column c (G = 1024 / (E + 1) groups), then thread c adds the G group
+// sums in g order, then thread 0 adds the E terms in e order.
 __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ counts,
                                                    const float *__restrict__ psum, int64_t rows,
-                                                   int E, int64_t T, int k, float *aux_out) {
+                                                   int E, int64_t T, int k, float *aux_out,
+                                                   float *zloss_out) {
     __shared__ float part[1024];
-    __shared__ float term[256];
-    const int G = 1024 / E;
-    const int g = threadIdx.x / E, e = threadIdx.x % E;
+    __shared__ float term[257];
+    const int C = E + 1;
+    const int G = 1024 / C;
+    const int g = threadIdx.x / C, col = threadIdx.x % C;
     if (g < G) {
         float s = 0.f;
-        for (int64_t b = g; b < rows; b += G) s += __ldg(psum + b * E + e);
-        part[g * E + e] = s;
+        for (int64_t b = g; b < rows; b += G) s += __ldg(psum + b * C + col);
+        part[g * C + col] = s;
     }
     __syncthreads();
-    if (threadIdx.x < E) {
+    if (threadIdx.x < C) {
         float s = 0.f;
-        for (int q = 0; q < G; ++q) s += part[q * E + threadIdx.x];
-        const float Pe = s / (float)T;
-        const float fe = (float)counts[threadIdx.x] / ((float)T * (float)k);
-        term[threadIdx.x] = fe * Pe;
+        for (int q = 0; q < G; ++q) s += part[q * C + threadIdx.x];
+        if ((int)threadIdx.x < E) {
+            const float Pe = s / (float)T;
+            const float fe = (float)counts[threadIdx.x] / ((float)T * (float)k);
+            term[threadIdx.x] = fe * Pe;
+        } else {
+            term[E] = s;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         float acc = 0.f;
         for (int q = 0; q < E; ++q) acc += term[q];
         *aux_out = T > 0 ? (float)E * acc : 0.f;
+        if (zloss_out) *zloss_out = T > 0 ? term[E] / (float)T : 0.f;
     }
+}
+
+// One step of the selection-only routing bias: b[e] += gamma when expert e received fewer routing
+// slots than the mean T k / E, -= gamma when more (compared exactly: counts[e] E against T k).
+__global__ void update_sel_bias_kernel(const int32_t *__restrict__ counts, float *b, int E,
+                                       int64_t slots, float gamma) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const int64_t ce = (int64_t)counts[e] * E;
+    if (ce < slots) b[e] += gamma;
+    else if (ce > slots) b[e] -= gamma;
 }
 
 }  // namespace
@@ -156,10 +175,21 @@ cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int3
 }
 
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
-                       float *aux_out, cudaStream_t s) {
-    if (c.T == 0) return cudaMemsetAsync(aux_out, 0, sizeof(float), s);
+                       float *aux_out, float *zloss_out, cudaStream_t s) {
+    if (c.T == 0) {
+        cudaError_t err = cudaMemsetAsync(aux_out, 0, sizeof(float), s);
+        if (err == cudaSuccess && zloss_out) err = cudaMemsetAsync(zloss_out, 0, sizeof(float), s);
+        return err;
+    }
     aux_kernel<<<1, 1024, 0, s>>>(counts, psum_part, router_partial_rows(c), c.E, c.T, c.k,
-                                 aux_out);
+                                 aux_out, zloss_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_update_sel_bias(const moe_config_t &c, const int32_t *counts, float *sel_bias,
+                                   float gamma, cudaStream_t s) {
+    update_sel_bias_kernel<<<(c.E + 255) / 256, 256, 0, s>>>(counts, sel_bias, c.E,
+                                                             c.T * (int64_t)c.k, gamma);
     return cudaGetLastError();
 }
 

@@ -66,7 +66,8 @@ inline int64_t dispatch_chunks(const moe_config_t &c) {
     return (P + DISPATCH_THREADS - 1) / DISPATCH_THREADS;
 }
 
-// Rows of psum_part the router writes (one per router block; depends only on the shape).
+// Rows of psum_part [rows, E + 1] the router writes (one per router block; depends only on the
+// shape).
 int64_t router_partial_rows(const moe_config_t &c);
 // Workspace bytes the router needs (tensor-core path: the split router weights and the partial
 // logits).
@@ -93,9 +94,9 @@ int dispatch_blocks_per_sm();
 // ------------------------------------------------------------------------------------------
 // launchers (each returns the launch's cudaError_t)
 cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
-                               const float *b_r, int32_t *topk_idx, float *gates,
-                               float *psum_part, void *scratch, uint32_t *dev_status,
-                               cudaStream_t s);
+                               const float *b_r, const float *sel_bias, int32_t *topk_idx,
+                               float *gates, float *psum_part, void *scratch,
+                               uint32_t *dev_status, cudaStream_t s);
 // W_r split and the partial logits on the tensor cores (the selection follows in router.cu).
 cudaError_t launch_router_tc(const moe_config_t &c, const void *h, const float *W_r,
                              void *scratch, uint32_t *dev_status, cudaStream_t s);
@@ -120,8 +121,11 @@ cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *
                            void *x_perm, uint32_t *dev_status, cudaStream_t s);
 cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int32_t *slot_of,
                            const float *gates, void *y, uint32_t *dev_status, cudaStream_t s);
+// aux_out: E sum f P; zloss_out (may be nullptr): the router z-loss.
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
-                       float *aux_out, cudaStream_t s);
+                       float *aux_out, float *zloss_out, cudaStream_t s);
+cudaError_t launch_update_sel_bias(const moe_config_t &c, const int32_t *counts, float *sel_bias,
+                                   float gamma, cudaStream_t s);
 
 struct FfnBufs {
     const void *x_perm;

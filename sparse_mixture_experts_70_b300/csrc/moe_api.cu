@@ -64,7 +64,7 @@ WsLayout ws_layout(const moe_config_t &c) {
     L.disp_flags_bytes = 256 + nch * E * 8;
     off = align_up(off + L.disp_flags_bytes);
     L.disp_excl = off;                    off = align_up(off + nch * E * 4);
-    L.psum = off;                         off = align_up(off + (size_t)router_partial_rows(c) * E * 4);
+    L.psum = off;                         off = align_up(off + (size_t)router_partial_rows(c) * (E + 1) * 4);
     L.router = off;                       off = align_up(off + router_scratch_bytes(c));
     L.topk_idx = off;                     off = align_up(off + P * 4);
     L.gates = off;                        off = align_up(off + P * 4);
@@ -135,19 +135,21 @@ moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows) {
 }
 
 moe_status_t moe_router_topk(const moe_config_t *cfg, const void *h, const float *W_r,
-                             const float *b_r, int32_t *topk_idx, float *gates, float *psum_part,
-                             void *ws, size_t ws_bytes, void *stream) {
+                             const float *b_r, const float *sel_bias, int32_t *topk_idx,
+                             float *gates, float *psum_part, void *ws, size_t ws_bytes,
+                             void *stream) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(*cfg);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     if (cfg->T == 0) return MOE_OK;
-    if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) || !aligned4(topk_idx) ||
-        !aligned4(gates) || !aligned4(psum_part))
+    if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) ||
+        (sel_bias && !aligned4(sel_bias)) || !aligned4(topk_idx) || !aligned4(gates) ||
+        !aligned4(psum_part))
         return MOE_ERR_INVALID_ARG;
     char *w = static_cast<char *>(ws);
-    return from_cuda(launch_router_topk(*cfg, h, W_r, b_r, topk_idx, gates, psum_part,
+    return from_cuda(launch_router_topk(*cfg, h, W_r, b_r, sel_bias, topk_idx, gates, psum_part,
                                         w + L.router, reinterpret_cast<uint32_t *>(w + L.status),
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -231,12 +233,22 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int3
 }
 
 moe_status_t moe_aux_loss(const moe_config_t *cfg, const int32_t *counts, const float *psum_part,
-                          float *aux_out, void *stream) {
+                          float *aux_out, float *zloss_out, void *stream) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
-    if (!aligned4(aux_out)) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(aux_out) || (zloss_out && !aligned4(zloss_out))) return MOE_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!aligned4(counts) || !aligned4(psum_part))) return MOE_ERR_INVALID_ARG;
-    return from_cuda(launch_aux(*cfg, counts, psum_part, aux_out, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_aux(*cfg, counts, psum_part, aux_out, zloss_out,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_update_sel_bias(const moe_config_t *cfg, const int32_t *counts, float *sel_bias,
+                                 float gamma, void *stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if (!aligned4(counts) || !aligned4(sel_bias) || !isfinite(gamma)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_update_sel_bias(*cfg, counts, sel_bias, gamma,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 // The fused variants moe_forward takes on the tensor-core path: with fuse_gather GEMM1 gathers
@@ -252,18 +264,21 @@ static ForwardPlan plan_of(const moe_config_t &c) {
 }
 
 static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const float *W_r,
-                                 const float *b_r, const void *W1, const float *b1,
-                                 const void *W3, const void *W2, const float *b2, void *y,
-                                 float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
-                                 void *ws, size_t ws_bytes, void *stream, cudaEvent_t ev_ffn0,
+                                 const float *b_r, const float *sel_bias, const void *W1,
+                                 const float *b1, const void *W3, const void *W2,
+                                 const float *b2, void *y, float *aux_out, float *zloss_out,
+                                 int32_t *topk_idx_out, int32_t *counts_out, void *ws,
+                                 size_t ws_bytes, void *stream, cudaEvent_t ev_ffn0,
                                  cudaEvent_t ev_ffn1) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     const moe_config_t &c = *cfg;
-    if (!aligned16(ws) || !aligned4(aux_out)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || !aligned4(aux_out) || (zloss_out && !aligned4(zloss_out)))
+        return MOE_ERR_INVALID_ARG;
     if (c.T > 0) {
-        if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) || !aligned16(W1) ||
-            !aligned16(W2) || !aligned16(y))
+        if (!aligned16(h) || !aligned4(W_r) || (b_r && !aligned4(b_r)) ||
+            (sel_bias && !aligned4(sel_bias)) || !aligned16(W1) || !aligned16(W2) ||
+            !aligned16(y))
             return MOE_ERR_INVALID_ARG;
         if (c.act == MOE_ACT_SWIGLU && !aligned16(W3)) return MOE_ERR_INVALID_ARG;
         if (c.has_bias && (!aligned4(b1) || !aligned4(b2))) return MOE_ERR_INVALID_ARG;
@@ -288,9 +303,11 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     if (c.T == 0) {
         cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s);
         if (e == cudaSuccess) e = cudaMemsetAsync(aux_out, 0, sizeof(float), s);
+        if (e == cudaSuccess && zloss_out) e = cudaMemsetAsync(zloss_out, 0, sizeof(float), s);
         return from_cuda(e);
     }
-    cudaError_t e = launch_router_topk(c, h, W_r, b_r, topk, gates, psum, w + L.router, dev_status, s);
+    cudaError_t e = launch_router_topk(c, h, W_r, b_r, sel_bias, topk, gates, psum, w + L.router,
+                                       dev_status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
@@ -315,7 +332,8 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     if (ev_ffn1 && cudaEventRecord(ev_ffn1, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!scatter && (e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if ((e = launch_aux(c, counts, psum, aux_out, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 
@@ -385,24 +403,24 @@ moe_status_t moe_forward_launch_count(const moe_config_t *cfg, int32_t *kernels)
 }
 
 moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
-                         const float *b_r, const void *W1, const float *b1, const void *W3,
-                         const void *W2, const float *b2, void *y, float *aux_out,
-                         int32_t *topk_idx_out, int32_t *counts_out, void *ws, size_t ws_bytes,
-                         void *stream) {
-    return forward_impl(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out,
-                        counts_out, ws, ws_bytes, stream, nullptr, nullptr);
+                         const float *b_r, const float *sel_bias, const void *W1,
+                         const float *b1, const void *W3, const void *W2, const float *b2,
+                         void *y, float *aux_out, float *zloss_out, int32_t *topk_idx_out,
+                         int32_t *counts_out, void *ws, size_t ws_bytes, void *stream) {
+    return forward_impl(cfg, h, W_r, b_r, sel_bias, W1, b1, W3, W2, b2, y, aux_out, zloss_out,
+                        topk_idx_out, counts_out, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
 moe_status_t moe_forward_events(const moe_config_t *cfg, const void *h, const float *W_r,
-                                const float *b_r, const void *W1, const float *b1,
-                                const void *W3, const void *W2, const float *b2, void *y,
-                                float *aux_out, int32_t *topk_idx_out, int32_t *counts_out,
-                                void *ws, size_t ws_bytes, void *stream, void *ffn_begin,
-                                void *ffn_end) {
+                                const float *b_r, const float *sel_bias, const void *W1,
+                                const float *b1, const void *W3, const void *W2,
+                                const float *b2, void *y, float *aux_out, float *zloss_out,
+                                int32_t *topk_idx_out, int32_t *counts_out, void *ws,
+                                size_t ws_bytes, void *stream, void *ffn_begin, void *ffn_end) {
     if (!ffn_begin || !ffn_end) return MOE_ERR_INVALID_ARG;
-    return forward_impl(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out,
-                        counts_out, ws, ws_bytes, stream, static_cast<cudaEvent_t>(ffn_begin),
-                        static_cast<cudaEvent_t>(ffn_end));
+    return forward_impl(cfg, h, W_r, b_r, sel_bias, W1, b1, W3, W2, b2, y, aux_out, zloss_out,
+                        topk_idx_out, counts_out, ws, ws_bytes, stream,
+                        static_cast<cudaEvent_t>(ffn_begin), static_cast<cudaEvent_t>(ffn_end));
 }
 
 moe_status_t moe_device_status(void *ws, void *stream) {

@@ -18,7 +18,7 @@
 
 struct moe_pipeline {
     moe_config_t cfg;
-    const float *W_r, *b_r, *b1, *b2;
+    const float *W_r, *b_r, *sel_bias, *b1, *b2;
     const void *W1, *W3, *W2;
     cudaStream_t compute;   // the caller's stream
     cudaStream_t in, out;   // owned
@@ -60,14 +60,16 @@ void release(moe_pipeline *p) {
 extern "C" {
 
 moe_status_t moe_pipeline_create(const moe_config_t *cfg, const float *W_r, const float *b_r,
-                                 const void *W1, const float *b1, const void *W3, const void *W2,
-                                 const float *b2, void *stream, moe_pipeline_t **out) {
+                                 const float *sel_bias, const void *W1, const float *b1,
+                                 const void *W3, const void *W2, const float *b2, void *stream,
+                                 moe_pipeline_t **out) {
     if (!out) return MOE_ERR_INVALID_ARG;
     *out = nullptr;
     size_t ws_bytes = 0;
     const moe_status_t st = moe_workspace_size(cfg, &ws_bytes);
     if (st != MOE_OK) return st;
-    if (!aligned4(W_r) || (b_r && !aligned4(b_r)) || !aligned16(W1) || !aligned16(W2))
+    if (!aligned4(W_r) || (b_r && !aligned4(b_r)) || (sel_bias && !aligned4(sel_bias)) ||
+        !aligned16(W1) || !aligned16(W2))
         return MOE_ERR_INVALID_ARG;
     if (cfg->act == MOE_ACT_SWIGLU && !aligned16(W3)) return MOE_ERR_INVALID_ARG;
     if (cfg->has_bias && (!aligned4(b1) || !aligned4(b2))) return MOE_ERR_INVALID_ARG;
@@ -77,6 +79,7 @@ moe_status_t moe_pipeline_create(const moe_config_t *cfg, const float *W_r, cons
     p->cfg = *cfg;
     p->W_r = W_r;
     p->b_r = b_r;
+    p->sel_bias = sel_bias;
     p->W1 = W1;
     p->b1 = b1;
     p->W3 = W3;
@@ -128,9 +131,9 @@ moe_status_t moe_pipeline_submit(moe_pipeline_t *p, const void *h_host, void *y_
         return MOE_ERR_CUDA;
     if (reuse && cudaStreamWaitEvent(p->compute, p->y_copied[s], 0) != cudaSuccess)
         return MOE_ERR_CUDA;
-    const moe_status_t st = moe_forward(&p->cfg, p->h[s], p->W_r, p->b_r, p->W1, p->b1, p->W3,
-                                        p->W2, p->b2, p->y[s], p->aux[s], nullptr, nullptr, p->ws,
-                                        p->ws_bytes, p->compute);
+    const moe_status_t st = moe_forward(&p->cfg, p->h[s], p->W_r, p->b_r, p->sel_bias, p->W1,
+                                        p->b1, p->W3, p->W2, p->b2, p->y[s], p->aux[s], nullptr,
+                                        nullptr, nullptr, p->ws, p->ws_bytes, p->compute);
     if (st != MOE_OK) return st;
     if (cudaEventRecord(p->fwd_done[s], p->compute) != cudaSuccess ||
         cudaStreamWaitEvent(p->out, p->fwd_done[s], 0) != cudaSuccess)

@@ -21,8 +21,10 @@
 //   router_tile_kernel   everything else: a block owns BT tokens x all E experts and runs a
 //                        register-blocked f32 FMA contraction staged through shared memory.
 // All four end with the same per-token step: max, sum of exponentials and k rounds of arg-max
-// (larger logit first, lower index on equal logits), and per-block sums of p in token order
-// (one row of psum_part per block), the input of the auxiliary value.
+// (larger logit first, lower index on equal logits; with a selection-only routing bias b, larger
+// p + b first), and per-block sums in a fixed order: one row of psum_part [rows, E + 1] per block
+// holding the sums of p per expert (input of the auxiliary value) and the sum of the squared
+// log-sum-exp of the logits (input of the router z-loss).
 #include "internal.cuh"
 
 namespace moe {
@@ -40,65 +42,90 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 struct RouterArgs {
     const void *h;
     const float *W_r, *b_r;
+    const float *sel_bias;  // selection-only routing bias [E] or nullptr
     int32_t *idx;
     float *gates, *psum;
     int64_t T;
     int d, E, k, gate_mode, tokens_per_block;
 };
 
-// Per-token step shared by the CUDA-core kernels. Lane l holds the logits of experts
-// l + 32 m (m < MAXM, -inf where absent). Writes the k chosen experts and their gates and returns
-// zmax and the softmax denominator in every lane.
+// A float's bits as an unsigned key with the same order (-inf lowest; no NaN here).
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Per-token step of every router path (warp per token). Lane l holds the logits v[m] of experts
+// l + 32 m (-inf where absent) and, when `biased`, their selection biases sb[m]. Every
+// exponential ex = exp(z - zmax) is taken once and serves the softmax sum, the gates and p. The
+// k experts are chosen by the largest keys -- the logits, or p + b with a selection bias -- in
+// k rounds of arg-max on the redux unit over order-preserving integer keys (exact: the largest
+// key, then the lowest index among equal ones); lane j keeps the j-th. Gates: RENORM = the
+// softmax over the chosen logits (ex_j / sum of the chosen ex), RAW_PROB = p_j. Writes idx and
+// gates, returns p[m] = ex / sum and the log-sum-exp of the logits.
 template <int MAXM>
-__device__ __forceinline__ void route_token(const float (&v)[MAXM], int E, int k, int gate_mode,
-                                            int64_t tok, int32_t *idx, float *gates, float &zmax,
-                                            float &ssum) {
+__device__ __forceinline__ void route_token(const float (&v)[MAXM], const float (&sb)[MAXM],
+                                            bool biased, int E, int k, int gate_mode,
+                                            int64_t tok, int32_t *idx, float *gates,
+                                            float (&p)[MAXM], float &lse) {
     const int lane = threadIdx.x & 31;
-    zmax = -INFINITY;
+    float lmax = -INFINITY;
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m) zmax = fmaxf(zmax, v[m]);
+    for (int m = 0; m < MAXM; ++m) lmax = fmaxf(lmax, v[m]);
+    const float zmax = key_float(__reduce_max_sync(0xffffffffu, order_key(lmax)));
+    float ex[MAXM], ssum = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-    ssum = 0.f;
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m)
-        if (lane + 32 * m < E) ssum += expf(v[m] - zmax);
+    for (int m = 0; m < MAXM; ++m) {
+        ex[m] = lane + 32 * m < E ? expf(v[m] - zmax) : 0.f;
+        ssum += ex[m];
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-
-    // k rounds of arg-max; lane j keeps the j-th winner.
+    const float inv = 1.f / ssum;
+    lse = zmax + logf(ssum);
+    float key[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        p[m] = ex[m] * inv;
+        key[m] = biased ? p[m] + sb[m] : v[m];
+    }
     uint32_t chosen = 0;
     int sel_e = -1;
-    float sel_v = 0.f;
+    float sel_x = 0.f;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
+        // this lane's best remaining candidate (its lowest index among equal keys)
+        float bv = -INFINITY, bx = 0.f;
         int be = 0x7fffffff;
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             const int e = lane + 32 * m;
-            if (e < E && !((chosen >> m) & 1u) && (v[m] > bv || (v[m] == bv && e < be))) {
-                bv = v[m];
+            if (e < E && !((chosen >> m) & 1u) && (key[m] > bv || be == 0x7fffffff)) {
+                bv = key[m];
                 be = e;
+                bx = ex[m];
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(bv));
+        const int win = (int)__reduce_min_sync(
+            0xffffffffu, (be != 0x7fffffff && order_key(bv) == kmax) ? (uint32_t)be : 0xffffffffu);
+        const float wx = __shfl_sync(0xffffffffu, bx, win & 31);
+        if ((win & 31) == lane) chosen |= 1u << (win >> 5);
+        if (lane == j) {
+            sel_e = win;
+            sel_x = wx;
         }
-        if ((be & 31) == lane) chosen |= 1u << (be >> 5);
-        if (lane == j) { sel_e = be; sel_v = bv; }
     }
     float g;
     if (gate_mode == MOE_GATE_RAW_PROB) {
-        g = expf(sel_v - zmax) / ssum;
+        g = sel_x * inv;
     } else {
-        const float ex = lane < k ? expf(sel_v - zmax) : 0.f;
-        float gs = ex;
+        float gs = lane < k ? sel_x : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-        g = ex / gs;
+        g = sel_x / gs;
     }
     if (lane < k) {
         idx[tok * k + lane] = sel_e;
@@ -175,7 +202,9 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
     const int64_t t_end = min(a.T, t_begin + (int64_t)a.tokens_per_block);
     const int my_e = lane & (EMAX - 1);
     const float bias = (a.b_r && my_e < E) ? a.b_r[my_e] : 0.f;
-    float psum_lane = 0.f;
+    float sbv[1];
+    sbv[0] = (a.sel_bias && my_e < E) ? a.sel_bias[my_e] : 0.f;
+    float psum_lane = 0.f, lse2 = 0.f;
     // Each warp takes two tokens at a time: every W_r read from shared memory feeds both.
     for (int64_t t = t_begin + 2 * warp; t < t_end; t += 2 * SMALL_WARPS) {
         const bool two = t + 1 < t_end;
@@ -241,18 +270,27 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
             }
             float v[1];
             v[0] = (lane < EMAX && my_e < E) ? av[0] + bias : -INFINITY;
-            float zmax, ssum;
-            route_token<1>(v, E, a.k, a.gate_mode, t + tt, a.idx, a.gates, zmax, ssum);
-            if (lane < E) psum_lane += expf(v[0] - zmax) / ssum;
+            float p[1], lse;
+            route_token<1>(v, sbv, a.sel_bias != nullptr, E, a.k, a.gate_mode, t + tt, a.idx,
+                           a.gates, p, lse);
+            if (lane < E) psum_lane += p[0];
+            lse2 += lse * lse;
         }
     }
     red[warp][lane] = psum_lane;
+    __shared__ float red_lse[SMALL_WARPS];
+    if (lane == 0) red_lse[warp] = lse2;
     __syncthreads();
     if (tid < E) {
         float s = 0.f;
 #pragma unroll
         for (int w = 0; w < SMALL_WARPS; ++w) s += red[w][tid];
-        a.psum[(int64_t)blockIdx.x * E + tid] = s;
+        a.psum[(int64_t)blockIdx.x * (E + 1) + tid] = s;
+    } else if (tid == E) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < SMALL_WARPS; ++w) s += red_lse[w];
+        a.psum[(int64_t)blockIdx.x * (E + 1) + E] = s;
     }
 }
 
@@ -319,11 +357,14 @@ __global__ void __launch_bounds__(RT_THREADS) router_splitd_kernel(RouterArgs a)
 #pragma unroll
             for (int w = 0; w < SMALL_WARPS; ++w) z += part[w][lane];
         }
-        float v[1];
+        float v[1], sbv[1];
         v[0] = (lane < EMAX && lane < E) ? z + (a.b_r ? a.b_r[lane] : 0.f) : -INFINITY;
-        float zmax, ssum;
-        route_token<1>(v, E, a.k, a.gate_mode, t, a.idx, a.gates, zmax, ssum);
-        if (lane < E) a.psum[t * E + lane] = expf(v[0] - zmax) / ssum;
+        sbv[0] = (a.sel_bias && lane < E) ? a.sel_bias[lane] : 0.f;
+        float p[1], lse;
+        route_token<1>(v, sbv, a.sel_bias != nullptr, E, a.k, a.gate_mode, t, a.idx, a.gates, p,
+                       lse);
+        if (lane < E) a.psum[t * (E + 1) + lane] = p[0];
+        if (lane == 0) a.psum[t * (E + 1) + E] = lse * lse;
     }
 }
 
@@ -358,6 +399,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
     float *hs = sm;                       // [BT][DK + 1]
     float *wsm = sm + BT * (DK + 1);      // [DK][E]
     float *zs = sm;                       // [BT][E], reuses the staging area after phase 1
+    float *lse_s = zs + BT * E;           // [BT] squared log-sum-exp per token
 
     const bool active = tid < TR * TC;
     const int r = tid / TC, c = tid % TC;
@@ -407,11 +449,18 @@ __global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
     const int warp = tid >> 5, lane = tid & 31;
     constexpr int NW = RT_THREADS / 32;
     constexpr int MAXM = 8;  // E <= 256 -> at most 8 logits per lane
+    float sbv[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        sbv[m] = (a.sel_bias && e < E) ? a.sel_bias[e] : 0.f;
+    }
     for (int row = warp; row < BT; row += NW) {
         const int64_t tok = t0 + row;
         float *zr = zs + row * E;
         if (tok >= a.T) {
             for (int e = lane; e < E; e += 32) zr[e] = 0.f;
+            if (lane == 0) lse_s[row] = 0.f;
             continue;
         }
         float v[MAXM];
@@ -420,20 +469,25 @@ __global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
             const int e = lane + 32 * m;
             v[m] = e < E ? zr[e] : -INFINITY;
         }
-        float zmax, ssum;
-        route_token<MAXM>(v, E, a.k, a.gate_mode, tok, a.idx, a.gates, zmax, ssum);
+        float p[MAXM], lse;
+        route_token<MAXM>(v, sbv, a.sel_bias != nullptr, E, a.k, a.gate_mode, tok, a.idx,
+                          a.gates, p, lse);
         __syncwarp();
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             const int e = lane + 32 * m;
-            if (e < E) zr[e] = expf(v[m] - zmax) / ssum;
+            if (e < E) zr[e] = p[m];
         }
+        if (lane == 0) lse_s[row] = lse * lse;
     }
     __syncthreads();
-    if (tid < E) {
+    for (int e = tid; e <= E; e += RT_THREADS) {
         float s = 0.f;
-        for (int row = 0; row < BT; ++row) s += zs[row * E + tid];
-        a.psum[(int64_t)blockIdx.x * E + tid] = s;
+        if (e < E)
+            for (int row = 0; row < BT; ++row) s += zs[row * E + e];
+        else
+            for (int row = 0; row < BT; ++row) s += lse_s[row];
+        a.psum[(int64_t)blockIdx.x * (E + 1) + e] = s;
     }
 }
 
@@ -458,81 +512,6 @@ int select_tokens_per_block(int64_t T) {
     int64_t tpb = (T + 295) / 296;
     tpb = (tpb + SEL_WARPS - 1) / SEL_WARPS * SEL_WARPS;
     return (int)(tpb < SEL_WARPS ? SEL_WARPS : tpb);
-}
-
-// A float's bits as an unsigned key with the same order (-inf lowest; no NaN here).
-__device__ __forceinline__ uint32_t order_key(float x) {
-    const uint32_t u = __float_as_uint(x);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_float(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// The per-token step for the selection kernel: as route_token, but every exponential
-// ex = exp(z - zmax) is taken once and serves the softmax sum, the gates and p (returned in
-// p[m] = ex / sum, for the per-expert sums), and the warp-wide maxima use the redux unit on the
-// order-preserving keys (exact: the largest logit, then the lowest index among equal ones).
-template <int MAXM>
-__device__ __forceinline__ void select_token(const float (&v)[MAXM], int E, int k, int gate_mode,
-                                             int64_t tok, int32_t *idx, float *gates,
-                                             float (&p)[MAXM]) {
-    const int lane = threadIdx.x & 31;
-    float lmax = -INFINITY;
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) lmax = fmaxf(lmax, v[m]);
-    const float zmax = key_float(__reduce_max_sync(0xffffffffu, order_key(lmax)));
-    float ex[MAXM], ssum = 0.f;
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-        ex[m] = lane + 32 * m < E ? expf(v[m] - zmax) : 0.f;
-        ssum += ex[m];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-    const float inv = 1.f / ssum;
-    // k rounds of arg-max (larger logit first, lower index on ties); lane j keeps the j-th.
-    uint32_t chosen = 0;
-    int sel_e = -1;
-    float sel_x = 0.f;
-    for (int j = 0; j < k; ++j) {
-        // this lane's best remaining candidate (its lowest index among equal logits)
-        float bv = -INFINITY, bx = 0.f;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            const int e = lane + 32 * m;
-            if (e < E && !((chosen >> m) & 1u) && (v[m] > bv || be == 0x7fffffff)) {
-                bv = v[m];
-                be = e;
-                bx = ex[m];
-            }
-        }
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(bv));
-        const int win = (int)__reduce_min_sync(
-            0xffffffffu, (be != 0x7fffffff && order_key(bv) == kmax) ? (uint32_t)be : 0xffffffffu);
-        const float wx = __shfl_sync(0xffffffffu, bx, win & 31);
-        if ((win & 31) == lane) chosen |= 1u << (win >> 5);
-        if (lane == j) {
-            sel_e = win;
-            sel_x = wx;
-        }
-    }
-    float g;
-    if (gate_mode == MOE_GATE_RAW_PROB) {
-        g = sel_x * inv;
-    } else {
-        float gs = lane < k ? sel_x : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-        g = sel_x / gs;
-    }
-    if (lane < k) {
-        idx[tok * k + lane] = sel_e;
-        gates[tok * k + lane] = g;
-    }
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) p[m] = ex[m] * inv;
 }
 
 // Lane's logits of token tok before the bias: the sum over the S K chunks of zpart[s][tok][e]
@@ -565,16 +544,18 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
     router_select_kernel(const float *__restrict__ zpart, int S, int Epad, int tpb,
                          const RouterArgs a) {
     __shared__ float wsum[SEL_WARPS][MAXM * 32];
+    __shared__ float wlse[SEL_WARPS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E;
     const int64_t t0 = (int64_t)blockIdx.x * tpb;
     int64_t t_end = t0 + tpb;
     if (t_end > a.T) t_end = a.T;
-    float bias[MAXM], acc[MAXM];
+    float bias[MAXM], sbv[MAXM], acc[MAXM], lse2 = 0.f;
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
         const int e = lane + 32 * m;
         bias[m] = (a.b_r && e < E) ? __ldg(a.b_r + e) : 0.f;
+        sbv[m] = (a.sel_bias && e < E) ? __ldg(a.sel_bias + e) : 0.f;
         acc[m] = 0.f;
     }
     int64_t tok = t0 + warp;
@@ -588,8 +569,10 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
         if (nxt < t_end) load_logits<MAXM>(zpart, S, Epad, a.T, nxt, E, vn);
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) v[m] += bias[m];  // -inf stays -inf for absent experts
-        float p[MAXM];
-        select_token<MAXM>(v, E, a.k, a.gate_mode, tok, a.idx, a.gates, p);
+        float p[MAXM], lse;
+        route_token<MAXM>(v, sbv, a.sel_bias != nullptr, E, a.k, a.gate_mode, tok, a.idx,
+                          a.gates, p, lse);
+        lse2 += lse * lse;
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             if (lane + 32 * m < E) acc[m] += p[m];
@@ -599,11 +582,12 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
     }
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) wsum[warp][lane + 32 * m] = acc[m];
+    if (lane == 0) wlse[warp] = lse2;
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
         float s = 0.f;
-        for (int w = 0; w < SEL_WARPS; ++w) s += wsum[w][e];
-        a.psum[(int64_t)blockIdx.x * E + e] = s;
+        for (int w = 0; w < SEL_WARPS; ++w) s += e < E ? wsum[w][e] : wlse[w];
+        a.psum[(int64_t)blockIdx.x * (E + 1) + e] = s;
     }
 }
 
@@ -655,11 +639,11 @@ size_t router_scratch_bytes(const moe_config_t &c) {
 int router_launches(const moe_config_t &c) { return router_path(c) == PATH_TC ? 3 : 1; }
 
 cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float *W_r,
-                               const float *b_r, int32_t *topk_idx, float *gates,
-                               float *psum_part, void *scratch, uint32_t *dev_status,
-                               cudaStream_t s) {
+                               const float *b_r, const float *sel_bias, int32_t *topk_idx,
+                               float *gates, float *psum_part, void *scratch,
+                               uint32_t *dev_status, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
-    RouterArgs a{h, W_r, b_r, topk_idx, gates, psum_part, c.T, c.d, c.E, c.k, c.gate, 0};
+    RouterArgs a{h, W_r, b_r, sel_bias, topk_idx, gates, psum_part, c.T, c.d, c.E, c.k, c.gate, 0};
     const RouterPath path = router_path(c);
     if (path == PATH_TC) {
         cudaError_t err = launch_router_tc(c, h, W_r, scratch, dev_status, s);
@@ -711,7 +695,7 @@ cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float
     const Geo g = geometry(c.E);
     const int64_t blocks = (c.T + g.BT - 1) / g.BT;
     const size_t stage = sizeof(float) * ((size_t)g.BT * (DK + 1) + (size_t)DK * c.E);
-    const size_t logits = sizeof(float) * (size_t)g.BT * c.E;
+    const size_t logits = sizeof(float) * (size_t)g.BT * (c.E + 1);
     const size_t smem = stage > logits ? stage : logits;
     const bool wide = g.RE == 4;
     if (bf16)

@@ -7,7 +7,8 @@ layer on its own batch. Two things need the other ranks:
   * the auxiliary value of a global batch split over ranks by tokens. With f_e = counts_e/(T k)
     and P_e = (1/T) sum_t p[t,e] over the WHOLE batch (lensaml.com "Mixture of Experts", Step 4),
     each rank contributes its routed counts and its per-expert sums of p; one all-reduce of
-    2E + 1 numbers gives the global value (``global_aux``).
+    2E + 1 numbers gives the global value (``global_aux``). The router z-loss of the whole batch
+    likewise needs each rank's sum of squared log-sum-exp and its token count (``global_zloss``).
 Everything here works with any backend (NCCL on GPUs, gloo on CPU for the tests).
 """
 from __future__ import annotations
@@ -78,6 +79,19 @@ def global_aux(counts: torch.Tensor, psum: torch.Tensor, tokens: int, k: int) ->
     f = buf[:E] / (T * k)
     P = buf[E:2 * E] / T
     return float(E * (f * P).sum().item())
+
+
+def global_zloss(lse2_sum: float, tokens: int) -> float:
+    """Router z-loss of the batch formed by all ranks' tokens: (sum of (log sum_e exp z)^2 over
+    every rank's tokens) / (all tokens). lse2_sum is this rank's sum (column E of psum_part,
+    summed over rows); one all-reduce of 2 numbers, in float64."""
+    buf = torch.tensor([float(lse2_sum), float(tokens)], dtype=torch.float64)
+    if active():
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        buf = buf.to(dev)
+        dist.all_reduce(buf, op=dist.ReduceOp.SUM)
+        buf = buf.cpu()
+    return float(buf[0] / buf[1]) if buf[1] > 0 else 0.0
 
 
 def shutdown() -> None:

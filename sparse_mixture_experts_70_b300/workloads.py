@@ -49,6 +49,7 @@ class Workload:
     seed: int
     capacity_factor: float = 0.0  # > 0: each expert keeps at most floor(factor T k / E) slots
     fuse_gather: bool = False     # the layer call reads expert rows of h without a permuted copy
+    sel_bias_std: float = 0.0     # > 0: a selection-only routing bias b ~ N(0, std^2) per expert
 
     @property
     def P(self) -> int:
@@ -133,6 +134,9 @@ def generate(w: Workload, pin_memory: bool = False) -> dict[str, torch.Tensor | 
     out["W1"], out["W3"], out["W2"] = W1, W3, W2
     out["b1"] = torch.zeros((w.E, w.f), dtype=torch.float32) if w.has_bias else None
     out["b2"] = torch.zeros((w.E, w.d), dtype=torch.float32) if w.has_bias else None
+    # drawn last, so that every other input is the same with or without it
+    out["sel_bias"] = (_randn(g, (w.E,), w.sel_bias_std, torch.float32)
+                       if w.sel_bias_std > 0 else None)
     if pin_memory:
         out["h"] = out["h"].pin_memory()
     return out
@@ -153,11 +157,13 @@ def generate_router_inputs(w: Workload) -> dict[str, torch.Tensor | None]:
 def small(name: str = "small", *, T: int, d: int, f: int, E: int, k: int, act: str = ACT_SWIGLU,
           gate: str = GATE_RENORM, dtype: str = "bf16", has_bias: bool = False,
           router_bias_var: float | None = None, seed: int = 11,
-          capacity_factor: float = 0.0, fuse_gather: bool = False) -> Workload:
+          capacity_factor: float = 0.0, fuse_gather: bool = False,
+          sel_bias_std: float = 0.0) -> Workload:
     """A custom-shaped workload for parity cases (ragged tails, several tiles, edge cases)."""
     return Workload(name, T=T, d=d, f=f, E=E, k=k, act=act, gate=gate, dtype=dtype,
                     has_bias=has_bias, router_bias_var=router_bias_var, seed=seed,
-                    capacity_factor=capacity_factor, fuse_gather=fuse_gather)
+                    capacity_factor=capacity_factor, fuse_gather=fuse_gather,
+                    sel_bias_std=sel_bias_std)
 
 
 def random_biases(w: Workload, inputs: dict, seed: int) -> dict:

@@ -25,10 +25,12 @@ def main() -> None:
     idx, _, _ = oracle.topk(z, w.k)
     counts, *_ = oracle.dispatch(idx, w.E)
     aux = D.global_aux(torch.from_numpy(counts), torch.from_numpy(p.sum(0)), hi - lo, w.k)
+    zl = D.global_zloss(oracle.zloss(z) * (hi - lo), hi - lo)
     slowest = D.max_over_ranks([float(rank + 1), 10.0 - rank])
     value = D.job_tokens_per_s(hi - lo, world, slowest[0])
     D.barrier()
-    print(json.dumps({"rank": rank, "aux": aux, "slowest": slowest, "value": value}), flush=True)
+    print(json.dumps({"rank": rank, "aux": aux, "zloss": zl, "slowest": slowest, "value": value}),
+          flush=True)
     D.shutdown()
 
 

@@ -30,7 +30,7 @@ def run_steps(w, inputs: dict, dev: dict | None = None) -> dict:
     rows = B.moe_router_partials(cfg)
     idx = torch.full((max(T, 1), k), -7, dtype=torch.int32, device="cuda")
     gates = torch.empty((max(T, 1), k), dtype=torch.float32, device="cuda")
-    psum = torch.empty((max(rows, 1), E), dtype=torch.float32, device="cuda")
+    psum = torch.empty((max(rows, 1), E + 1), dtype=torch.float32, device="cuda")
     counts = torch.full((E,), -7, dtype=torch.int32, device="cuda")
     offsets = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
     sorted_token = torch.full((max(P, 1),), -7, dtype=torch.int32, device="cuda")
@@ -39,17 +39,19 @@ def run_steps(w, inputs: dict, dev: dict | None = None) -> dict:
     y_perm = torch.empty((max(P, 1), d), dtype=dt, device="cuda")
     y = torch.empty((max(T, 1), d), dtype=dt, device="cuda")
     aux = torch.full((1,), -7.0, dtype=torch.float32, device="cuda")
-    B.moe_router_topk(cfg, dev["h"], dev["W_r"], dev["b_r"], idx, gates, psum, ws)
+    B.moe_router_topk(cfg, dev["h"], dev["W_r"], dev["b_r"], idx, gates, psum, ws,
+                      sel_bias=dev.get("sel_bias"))
     B.moe_build_dispatch(cfg, idx, dev["h"], counts, offsets, sorted_token, slot_of, x_perm, ws)
     B.moe_expert_ffn(cfg, x_perm, offsets, dev["W1"], dev["b1"], dev["W3"], dev["W2"], dev["b2"],
                      y_perm, ws)
     B.moe_combine(cfg, y_perm, slot_of, gates, y)
-    B.moe_aux_loss(cfg, counts, psum, aux)
+    zloss = torch.full((1,), -7.0, dtype=torch.float32, device="cuda")
+    B.moe_aux_loss(cfg, counts, psum, aux, zloss_out=zloss)
     status = B.moe_device_status(ws)
     torch.cuda.synchronize()
     out = dict(idx=idx[:T], gates=gates[:T], counts=counts, offsets=offsets,
                sorted_token=sorted_token[:P], slot_of=slot_of[:P], x_perm=x_perm[:P],
-               y_perm=y_perm[:P], y=y[:T], aux=aux, status=status)
+               y_perm=y_perm[:P], y=y[:T], aux=aux, zloss=zloss, status=status)
     return {k_: (v.cpu() if isinstance(v, torch.Tensor) else v) for k_, v in out.items()}
 
 
@@ -59,8 +61,8 @@ def run_forward(w, dev: dict, layer: B.Layer | None = None) -> dict:
     layer.forward(dev["h"])
     status = B.moe_device_status(layer.ws)
     torch.cuda.synchronize()
-    return dict(y=layer.y.cpu(), aux=layer.aux.cpu(), idx=layer.topk_idx.cpu(),
-                counts=layer.counts.cpu(), status=status)
+    return dict(y=layer.y.cpu(), aux=layer.aux.cpu(), zloss=layer.zloss.cpu(),
+                idx=layer.topk_idx.cpu(), counts=layer.counts.cpu(), status=status)
 
 
 def routing_agreement(ref: dict, idx_gpu: np.ndarray) -> np.ndarray:

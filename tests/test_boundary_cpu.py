@@ -71,7 +71,7 @@ def test_invalid_configs_are_rejected(kw, expect):
     st, _ = _ws_size(cfg)
     assert st == expect
     L = B.lib()
-    assert L.moe_forward(ctypes.byref(cfg), *([None] * 13), 0, None) == expect
+    assert L.moe_forward(ctypes.byref(cfg), *([None] * 15), 0, None) == expect
 
 
 def test_fuse_gather_flag():
@@ -90,7 +90,7 @@ def test_fuse_gather_flag():
     bad = B.config(T=64, d=128, f=256, E=8, k=2)
     bad.fuse_gather = 2
     assert _ws_size(bad)[0] == B.MOE_ERR_INVALID_ARG
-    assert B.lib().moe_forward(ctypes.byref(bad), *([None] * 13), 0, None) == B.MOE_ERR_INVALID_ARG
+    assert B.lib().moe_forward(ctypes.byref(bad), *([None] * 15), 0, None) == B.MOE_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("name,kw,expect", [
@@ -113,17 +113,19 @@ def test_pipeline_arguments_are_checked_before_any_cuda_call():
     L = B.lib()
     out = ctypes.c_void_p(123)
     bad = B.config(T=64, d=100, f=256, E=8, k=2)
-    assert L.moe_pipeline_create(ctypes.byref(bad), *([None] * 8), ctypes.byref(out)) == \
+    assert L.moe_pipeline_create(ctypes.byref(bad), *([None] * 9), ctypes.byref(out)) == \
         B.MOE_ERR_INVALID_ARG
     assert out.value is None  # *out cleared
     good = B.config(T=64, d=128, f=256, E=8, k=2)
     # NULL weights, misaligned weights, NULL out
-    assert L.moe_pipeline_create(ctypes.byref(good), *([None] * 8), ctypes.byref(out)) == \
+    assert L.moe_pipeline_create(ctypes.byref(good), *([None] * 9), ctypes.byref(out)) == \
         B.MOE_ERR_INVALID_ARG
-    assert L.moe_pipeline_create(ctypes.byref(good), 4, None, 18, None, 32, 64, None, None,
+    assert L.moe_pipeline_create(ctypes.byref(good), 4, None, None, 18, None, 32, 64, None, None,
                                  ctypes.byref(out)) == B.MOE_ERR_INVALID_ARG
-    assert L.moe_pipeline_create(ctypes.byref(good), 16, None, 32, None, 48, 64, None, None,
-                                 None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pipeline_create(ctypes.byref(good), 16, None, 18, 32, None, 48, 64, None, None,
+                                 ctypes.byref(out)) == B.MOE_ERR_INVALID_ARG  # misaligned sel_bias
+    assert L.moe_pipeline_create(ctypes.byref(good), 16, None, None, 32, None, 48, 64, None,
+                                 None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_pipeline_submit(None, 16, 16, 16) == B.MOE_ERR_INVALID_ARG
     assert L.moe_pipeline_join(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_pipeline_device_status(None) == B.MOE_ERR_INVALID_ARG
@@ -136,26 +138,34 @@ def test_null_and_misaligned_pointers_are_rejected_on_the_host():
     st, n = _ws_size(cfg)
     assert st == 0
     fake = 1 << 40          # never dereferenced: the checks run before any launch
-    # missing h
-    assert L.moe_forward(ctypes.byref(cfg), None, fake, None, fake, None, fake, fake, None, fake,
-                         fake, None, None, fake, n, None) == B.MOE_ERR_INVALID_ARG
-    # misaligned W1
-    assert L.moe_forward(ctypes.byref(cfg), fake, fake, None, fake + 2, None, fake, fake, None,
-                         fake, fake, None, None, fake, n, None) == B.MOE_ERR_INVALID_ARG
-    # workspace too small
-    assert L.moe_forward(ctypes.byref(cfg), fake, fake, None, fake, None, fake, fake, None, fake,
-                         fake, None, None, fake, n - 1, None) == B.MOE_ERR_WORKSPACE
+    # moe_forward(cfg, h, W_r, b_r, sel_bias, W1, b1, W3, W2, b2, y, aux, zloss, topk, counts,
+    #             ws, ws_bytes, stream)
+    def fwd(h=fake, sel=None, W1=fake, zl=None, ws_bytes=n):
+        return L.moe_forward(ctypes.byref(cfg), h, fake, None, sel, W1, None, fake, fake, None,
+                             fake, fake, zl, None, None, fake, ws_bytes, None)
+    assert fwd(h=None) == B.MOE_ERR_INVALID_ARG             # missing h
+    assert fwd(W1=fake + 2) == B.MOE_ERR_INVALID_ARG        # misaligned W1
+    assert fwd(sel=fake + 2) == B.MOE_ERR_INVALID_ARG       # misaligned selection bias
+    assert fwd(zl=fake + 2) == B.MOE_ERR_INVALID_ARG        # misaligned z-loss output
+    assert fwd(ws_bytes=n - 1) == B.MOE_ERR_WORKSPACE       # workspace too small
     assert L.moe_expert_ffn(ctypes.byref(cfg), fake, fake, fake, None, fake, fake, None, fake,
                             fake, n - 1, None) == B.MOE_ERR_WORKSPACE
     assert L.moe_build_dispatch(ctypes.byref(cfg), fake, None, None, fake, fake, fake, None,
                                 fake, n, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(cfg), fake, fake, fake, fake + 8, None) == \
         B.MOE_ERR_INVALID_ARG
-    assert L.moe_router_topk(ctypes.byref(cfg), fake, None, None, fake, fake, fake, fake, n,
+    assert L.moe_router_topk(ctypes.byref(cfg), fake, None, None, None, fake, fake, fake, fake, n,
                              None) == B.MOE_ERR_INVALID_ARG
-    assert L.moe_router_topk(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake, n - 1,
-                             None) == B.MOE_ERR_WORKSPACE
-    assert L.moe_aux_loss(ctypes.byref(cfg), fake, fake, None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_topk(ctypes.byref(cfg), fake, fake, None, fake + 1, fake, fake, fake, fake,
+                             n, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_topk(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake, fake,
+                             n - 1, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_aux_loss(ctypes.byref(cfg), fake, fake, None, None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_aux_loss(ctypes.byref(cfg), fake, fake, fake, fake + 2, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert L.moe_update_sel_bias(ctypes.byref(cfg), fake, None, 0.1, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_update_sel_bias(ctypes.byref(cfg), fake, fake, float("inf"), None) == \
+        B.MOE_ERR_INVALID_ARG
     assert L.moe_device_status(None, None) == B.MOE_ERR_INVALID_ARG
 
 

@@ -43,6 +43,7 @@ def test_two_gloo_ranks_reduce_aux_and_timing():
     ref = oracle.route(w, wl.generate_router_inputs(w))
     for o in outs:
         assert o["aux"] == pytest.approx(ref["aux"], rel=1e-12)
+        assert o["zloss"] == pytest.approx(ref["zloss"], rel=1e-12)
         assert o["slowest"] == [2.0, 10.0]
         assert o["value"] == pytest.approx(48 * 2 / 2e-3)
     # a rank alone sees only its own half: its aux differs from the batch's

@@ -51,6 +51,15 @@ SMALL = [
     # paired-CTA GEMM (experts of >= 4 M tiles): odd tile counts, ragged N tail, skew
     wl.small("paired_gelu_bias", T=2500, d=256, f=320, E=3, k=2, act=G, has_bias=True),
     wl.small("paired_swiglu_skewed", T=3000, d=128, f=256, E=4, k=2, router_bias_var=3.0),
+    # selection-only routing bias (experts chosen by p + b, gates from p) on every router path:
+    # few-token split-d (bf16), shared-memory W_r (f32), tiled (f32, E > 32), tensor cores
+    wl.small("sel_bias_splitd", T=300, d=256, f=128, E=16, k=2, sel_bias_std=0.05),
+    wl.small("sel_bias_small_f32", T=1500, d=128, f=64, E=8, k=2, dtype="f32", sel_bias_std=0.1),
+    wl.small("sel_bias_tile_f32", T=200, d=128, f=64, E=40, k=3, dtype="f32", sel_bias_std=0.02),
+    wl.small("sel_bias_tc", T=2000, d=256, f=128, E=64, k=4, router_bias_var=1.0,
+             sel_bias_std=0.01),
+    wl.small("sel_bias_tc_top1_raw", T=1800, d=128, f=128, E=100, k=1, act=G,
+             gate=wl.GATE_RAW_PROB, sel_bias_std=0.01),
     # paired kernel on an expert's odd last M tile (the second CTA's rows all masked): E = 1,
     # k = 1 and E = 2, k = 2 fix the rows per expert at T, so the last tile holds 40, 100 or 128
     # rows; SwiGLU with a ragged last N tile, GELU with biases, the top-1 scatter, and the
@@ -106,6 +115,7 @@ def _check_steps(w, inputs, ref, got):
     # the permute is a copy: bit-exact
     assert torch.equal(got["x_perm"][:kept], inputs["h"][torch.from_numpy(st[:kept]).long()])
     assert got["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
+    assert got["zloss"].item() == pytest.approx(ref["zloss"], rel=AUX_REL)
     return diff
 
 
@@ -150,6 +160,7 @@ def test_small_cases_step_by_step(w):
         assert torch.equal(fw["y"], got["y"])
     assert torch.equal(fw["idx"], got["idx"]) and torch.equal(fw["counts"], got["counts"])
     assert fw["aux"].item() == got["aux"].item()
+    assert fw["zloss"].item() == got["zloss"].item()
 
 
 def _token_sample(w):
@@ -177,6 +188,7 @@ def test_full_size_workloads(name):
     if len(diff) == 0:
         np.testing.assert_array_equal(fw["counts"].numpy(), ref["counts"])
     assert fw["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
+    assert fw["zloss"].item() == pytest.approx(ref["zloss"], rel=AUX_REL)
     stats = check_layer_output(w, ref, fw["y"], skip_tokens=diff)
     print(f"{name}: near-tie tokens {len(diff)}, {stats}")
     got = run_steps(w, inputs, dev)
@@ -229,3 +241,18 @@ def test_outputs_stay_inside_their_buffers_and_runs_are_deterministic():
     assert (ybuf[:guard] == 7.0).all() and (ybuf[guard + w.T:] == 7.0).all()
     assert (ibuf[:guard] == -5).all() and (ibuf[guard + w.T * w.k:] == -5).all()
     assert (cbuf[:guard] == -5).all() and (cbuf[guard + w.E:] == -5).all()
+
+
+def test_sel_bias_update_step():
+    """moe_update_sel_bias moves each bias by +gamma below the mean load and -gamma above it
+    (the oracle's rule, in f32), on the counts of a routed batch."""
+    w = wl.small("update", T=700, d=128, f=64, E=10, k=3, router_bias_var=2.0, sel_bias_std=0.05)
+    inputs = _inputs(w)
+    dev = to_dev(inputs)
+    got = run_steps(w, inputs, dev)
+    counts = got["counts"].numpy()
+    b = dev["sel_bias"].clone()
+    B.moe_update_sel_bias(B.config_for(w), got["counts"].cuda(), b, 0.0078125)
+    expect = oracle.update_sel_bias(counts, w.T, w.k, 0.0078125, inputs["sel_bias"].numpy())
+    np.testing.assert_array_equal(b.cpu().numpy(), expect.astype(np.float32))
+    assert (counts * w.E != w.P).any()

@@ -22,7 +22,7 @@ def _routing(w, dev, cfg, ws):
     rows = B.moe_router_partials(cfg)
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
     gates = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
-    psum = torch.empty((rows, w.E), dtype=torch.float32, device="cuda")
+    psum = torch.empty((rows, w.E + 1), dtype=torch.float32, device="cuda")
     B.moe_router_topk(cfg, dev["h"], dev["W_r"], dev["b_r"], idx, gates, psum, ws)
     return idx
 

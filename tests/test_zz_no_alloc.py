@@ -22,7 +22,7 @@ def _dispatch_both(w):
     rows = B.moe_router_partials(cfg)
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    psum = torch.empty((rows, E), dtype=torch.float32, device="cuda")
+    psum = torch.empty((rows, E + 1), dtype=torch.float32, device="cuda")
     B.moe_router_topk(cfg, h, W_r, b_r, idx, gates, psum, B.workspace(cfg))
     outs = []
     for use_static in (False, True):
