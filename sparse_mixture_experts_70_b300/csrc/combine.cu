@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const void *__restr
                                                              uint32_t *dev_status) {
     __shared__ int32_t s_row[CB_SLOTS];
     __shared__ float s_g[CB_SLOTS];
+    pdl_wait();
     const int v8 = d / 8;
     const int64_t t0 = (int64_t)blockIdx.x * tpb;
     const int nt = (int)(T - t0 < tpb ? T - t0 : tpb);
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const void *__restr
         }
         Vec8<VT>::store(y, (t0 + tl) * v8 + i, acc);
     }
+    pdl_trigger();
 }
 
 // aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T) and the router z-loss
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ c
                                                    float *zloss_out) {
     __shared__ float part[1024];
     __shared__ float term[257];
+    pdl_wait();
     const int C = E + 1;
     const int G = 1024 / C;
     const int g = threadIdx.x / C, col = threadIdx.x % C;
@@ -139,17 +142,21 @@ __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ c
         *aux_out = T > 0 ? (float)E * acc : 0.f;
         if (zloss_out) *zloss_out = T > 0 ? term[E] / (float)T : 0.f;
     }
+    pdl_trigger();
 }
 
 // One step of the selection-only routing bias: b[e] += gamma when expert e received fewer routing
 // slots than the mean T k / E, -= gamma when more (compared exactly: counts[e] E against T k).
 __global__ void update_sel_bias_kernel(const int32_t *__restrict__ counts, float *b, int E,
                                        int64_t slots, float gamma) {
+    pdl_wait();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    const int64_t ce = (int64_t)counts[e] * E;
-    if (ce < slots) b[e] += gamma;
-    else if (ce > slots) b[e] -= gamma;
+    if (e < E) {
+        const int64_t ce = (int64_t)counts[e] * E;
+        if (ce < slots) b[e] += gamma;
+        else if (ce > slots) b[e] -= gamma;
+    }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -165,13 +172,12 @@ cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int3
     if (tpb * c.k > CB_SLOTS) tpb = CB_SLOTS / c.k;
     const int64_t blocks = (c.T + tpb - 1) / tpb;
     const int64_t P = c.T * c.k;
+    const dim3 grid((unsigned)blocks), block(CB_THREADS);
     if (c.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, CB_THREADS, 0, s>>>(
-            y_perm, slot_of, gates, y, c.T, P, c.d, c.k, (int)tpb, dev_status);
-    else
-        combine_kernel<float><<<(unsigned)blocks, CB_THREADS, 0, s>>>(
-            y_perm, slot_of, gates, y, c.T, P, c.d, c.k, (int)tpb, dev_status);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, s, 1, y_perm, slot_of,
+                          gates, y, c.T, P, c.d, c.k, (int)tpb, dev_status);
+    return launch_pdl(combine_kernel<float>, grid, block, 0, s, 1, y_perm, slot_of, gates, y, c.T,
+                      P, c.d, c.k, (int)tpb, dev_status);
 }
 
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
@@ -181,16 +187,14 @@ cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float
         if (err == cudaSuccess && zloss_out) err = cudaMemsetAsync(zloss_out, 0, sizeof(float), s);
         return err;
     }
-    aux_kernel<<<1, 1024, 0, s>>>(counts, psum_part, router_partial_rows(c), c.E, c.T, c.k,
-                                 aux_out, zloss_out);
-    return cudaGetLastError();
+    return launch_pdl(aux_kernel, dim3(1), dim3(1024), 0, s, 1, counts, psum_part,
+                      router_partial_rows(c), c.E, c.T, c.k, aux_out, zloss_out);
 }
 
 cudaError_t launch_update_sel_bias(const moe_config_t &c, const int32_t *counts, float *sel_bias,
                                    float gamma, cudaStream_t s) {
-    update_sel_bias_kernel<<<(c.E + 255) / 256, 256, 0, s>>>(counts, sel_bias, c.E,
-                                                             c.T * (int64_t)c.k, gamma);
-    return cudaGetLastError();
+    return launch_pdl(update_sel_bias_kernel, dim3((c.E + 255) / 256), dim3(256), 0, s, 1, counts,
+                      sel_bias, c.E, c.T * (int64_t)c.k, gamma);
 }
 
 }  // namespace moe

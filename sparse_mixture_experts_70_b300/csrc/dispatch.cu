@@ -98,6 +98,7 @@ __device__ __forceinline__ int chunk_ranks(const DispatchArgs &a, int c, int32_t
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(DispatchArgs a) {
     __shared__ int32_t cnt[32 * 256];
     __shared__ int32_t s_off[257];
+    pdl_wait();
     const int tid = threadIdx.x, E = a.E;
     int lrank, agg;
     const int e = chunk_ranks(a, 0, cnt, &lrank, &agg);
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(Di
             a.slot_of[tid] = pos;
         }
     }
+    pdl_trigger();
 }
 
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchArgs a) {
@@ -231,6 +233,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
             }
         }
     }
+    pdl_trigger();  // (this kernel is launched cooperatively, without a dependent wait of its own)
 }
 
 // x_perm[slot_of[t k + j], :] = h[t, :] for every kept slot (slot_of >= 0; -1 marks a slot the
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ 
                                                       uint4 *__restrict__ x_perm, int64_t P,
                                                       int64_t T, int k, int vecs,
                                                       uint32_t *dev_status) {
+    pdl_wait();
     const int64_t units = T * vecs;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u0 < units;
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ 
             }
         }
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -317,8 +322,7 @@ cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, cons
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold = hook.withhold;
     if (a.nchunks == 1 && !hook.withhold) {
-        dispatch_single_kernel<<<1, DISPATCH_THREADS, 0, s>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(dispatch_single_kernel, dim3(1), dim3(DISPATCH_THREADS), 0, s, 1, a);
     }
     cudaError_t err = cudaMemsetAsync(b.flags, 0, b.flags_bytes, s);
     if (err != cudaSuccess) return err;
@@ -395,10 +399,9 @@ cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *
     int64_t blocks = (c.T * vecs + 511) / 512;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    permute_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4 *>(h), slot_of,
-                                                    static_cast<uint4 *>(x_perm), P, c.T, c.k,
-                                                    vecs, dev_status);
-    return cudaGetLastError();
+    return launch_pdl(permute_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+                      static_cast<const uint4 *>(h), slot_of, static_cast<uint4 *>(x_perm), P, c.T,
+                      c.k, vecs, dev_status);
 }
 
 }  // namespace moe

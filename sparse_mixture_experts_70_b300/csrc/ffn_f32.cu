@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(F32Args a) {
     __shared__ float B3s[EPI == EPI_SWIGLU ? FK : 1][FB + 4];
     __shared__ int32_t s_e, s_row0, s_rows;
     const int tid = threadIdx.x;
+    pdl_wait();
     if (tid == 0) {
         int cum = 0, e_found = -1, m = 0;
         for (int e = 0; e < a.E; ++e) {
@@ -128,14 +129,14 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(F32Args a) {
             orow[n] = v;
         }
     }
+    pdl_trigger();
 }
 
 template <int EPI>
 cudaError_t launch_f32(const F32Args &a, int64_t P, cudaStream_t s) {
     const int64_t mtiles = (P + FB - 1) / FB + a.E;
     dim3 grid((unsigned)mtiles, (unsigned)(a.N / FB));
-    ffn_f32_kernel<EPI><<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(ffn_f32_kernel<EPI>, grid, dim3(256), 0, s, 1, a);
 }
 
 }  // namespace

@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int32_t *s_off = s_cum + 260;                             // [E+1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();  // offsets and A come from earlier kernels on the stream
     const int E = a.E;
     constexpr bool PAIR = false;
     const int rank = 0;
@@ -399,6 +400,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -455,6 +457,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int32_t *s_off = s_cum + 260;                             // [E+1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();  // offsets and A come from earlier kernels on the stream
     const int E = a.E;
     const int rank = (int)cluster_ctarank();
     const bool leader = rank == 0;
@@ -659,6 +662,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // no copy, commit or remote arrive targets either CTA any more
@@ -739,28 +743,17 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     const bool pair = clusters > 0 && P >= (int64_t)PAIR_MIN_TILES * BM * E;
     if (pair) {
         const int64_t units = ((P + 2 * BM - 1) / (2 * BM) + E) * (int64_t)a.n_tiles;
-        int64_t ncl = clusters < units ? clusters : units;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * ncl));
-        cfg.blockDim = dim3(TC_THREADS);
-        cfg.dynamicSmemBytes = TC_SMEM_PAIR;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, mA, mB, mB3, a);
+        const int64_t ncl = clusters < units ? clusters : units;
+        return launch_pdl(grouped_gemm_pair_kernel, dim3((unsigned)(2 * ncl)), dim3(TC_THREADS),
+                          TC_SMEM_PAIR, s, 2, mA, mB, mB3, a);
     }
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
     if (grid > upper) grid = upper;
     cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel, TC_SMEM);
     if (err != cudaSuccess) return err;
-    grouped_gemm_tc_kernel<<<(unsigned)grid, TC_THREADS, TC_SMEM, s>>>(mA, mB, mB3, a);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_tc_kernel, dim3((unsigned)grid), dim3(TC_THREADS), TC_SMEM, s,
+                      1, mA, mB, mB3, a);
 }
 
 }  // namespace

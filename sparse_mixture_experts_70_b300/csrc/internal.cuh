@@ -30,6 +30,16 @@ __device__ __forceinline__ void report(uint32_t *dev_status, uint32_t bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched with it allowed
+// (launch_pdl), so it may be scheduled while the previous kernel on the stream finishes; it calls
+// pdl_wait() before it touches memory that earlier stream work writes (the wait returns once that
+// work has completed and its writes are visible), and pdl_trigger() after its own work, so that
+// the next kernel's launch overlaps this one's tail. Both are no-ops without a dependent launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Test hook: a shorter spin limit and one withheld signal, so that a bounded wait runs out
 // (the kernel then records DEV_ERR_TIMEOUT and returns). Normal calls use the defaults.
 struct FaultHook {
@@ -86,6 +96,32 @@ float *router_tc_logits(void *scratch, const moe_config_t &c);
 WsLayout ws_layout(const moe_config_t &c);
 
 int num_sms();
+
+// <<<grid, block, smem, s>>> with programmatic dependent launch allowed (and a cluster of
+// cluster_x CTAs along x when > 1).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (cluster_x > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device, size).
 cudaError_t set_max_dynamic_smem(const void *kernel, size_t bytes);
 // Resident blocks per SM of the dispatch kernel on the current device (queried once).

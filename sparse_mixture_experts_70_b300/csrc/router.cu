@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
     constexpr int V = EMAX / 4;
     const int E = a.E, d = a.d, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *wf = reinterpret_cast<float *>(w4);
+    pdl_wait();
     if (E == EMAX) {
         // one float4 of W_r (4 experts of one input row) lands in one float4 slot; 8 in flight
         const int n4 = d * EMAX / 4;
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_small_kernel(RouterArgs a) 
         for (int w = 0; w < SMALL_WARPS; ++w) s += red_lse[w];
         a.psum[(int64_t)blockIdx.x * (E + 1) + E] = s;
     }
+    pdl_trigger();
 }
 
 // Few tokens: one token per block, the 8 warps take the 256-wide slices of d in turn and read
@@ -303,6 +305,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_splitd_kernel(RouterArgs a)
     __shared__ float part[SMALL_WARPS][EMAX];
     const int E = a.E, d = a.d, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
+    pdl_wait();
     const Tin *hrow = reinterpret_cast<const Tin *>(a.h) + t * d;
     const int nj = (d + 255) / 256;
     const bool vec = (E & 3) == 0;
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_splitd_kernel(RouterArgs a)
         if (lane < E) a.psum[t * (E + 1) + lane] = p[0];
         if (lane == 0) a.psum[t * (E + 1) + E] = lse * lse;
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -388,6 +392,7 @@ __host__ __device__ inline Geo geometry(int E) {
 template <int RT, int RE, typename Tin>
 __global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
     extern __shared__ float sm[];
+    pdl_wait();
     const int E = a.E, d = a.d;
     const int TC = E / RE;
     const int TR = RT_THREADS / TC;
@@ -489,6 +494,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_tile_kernel(RouterArgs a) {
             for (int row = 0; row < BT; ++row) s += lse_s[row];
         a.psum[(int64_t)blockIdx.x * (E + 1) + e] = s;
     }
+    pdl_trigger();
 }
 
 template <typename K>
@@ -497,8 +503,7 @@ cudaError_t launch_k(K kern, const RouterArgs &a, int64_t blocks, size_t smem, c
         cudaError_t err = set_max_dynamic_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
     }
-    kern<<<(unsigned)blocks, RT_THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(RT_THREADS), smem, s, 1, a);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -545,6 +550,7 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
                          const RouterArgs a) {
     __shared__ float wsum[SEL_WARPS][MAXM * 32];
     __shared__ float wlse[SEL_WARPS];
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E;
     const int64_t t0 = (int64_t)blockIdx.x * tpb;
@@ -589,6 +595,7 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
         for (int w = 0; w < SEL_WARPS; ++w) s += e < E ? wsum[w][e] : wlse[w];
         a.psum[(int64_t)blockIdx.x * (E + 1) + e] = s;
     }
+    pdl_trigger();
 }
 
 enum RouterPath { PATH_SPLITD, PATH_SMALL, PATH_TC, PATH_TILE };
@@ -652,14 +659,13 @@ cudaError_t launch_router_topk(const moe_config_t &c, const void *h, const float
         const int S = router_tc_splits(c), Epad = router_tc_epad(c);
         const int tpb = select_tokens_per_block(c.T);
         const unsigned blocks = (unsigned)((c.T + tpb - 1) / tpb);
-        constexpr unsigned thr = SEL_WARPS * 32;
+        const dim3 grid(blocks), thr(SEL_WARPS * 32);
         switch ((c.E + 31) / 32) {
-            case 1: router_select_kernel<1><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
-            case 2: router_select_kernel<2><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
-            case 3: router_select_kernel<3><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
-            default: router_select_kernel<4><<<blocks, thr, 0, s>>>(zpart, S, Epad, tpb, a); break;
+            case 1: return launch_pdl(router_select_kernel<1>, grid, thr, 0, s, 1, zpart, S, Epad, tpb, a);
+            case 2: return launch_pdl(router_select_kernel<2>, grid, thr, 0, s, 1, zpart, S, Epad, tpb, a);
+            case 3: return launch_pdl(router_select_kernel<3>, grid, thr, 0, s, 1, zpart, S, Epad, tpb, a);
+            default: return launch_pdl(router_select_kernel<4>, grid, thr, 0, s, 1, zpart, S, Epad, tpb, a);
         }
-        return cudaGetLastError();
     }
     const bool bf16 = c.dtype == MOE_BF16;
     if (path == PATH_SPLITD) {

@@ -62,6 +62,7 @@ struct LogitsArgs {
 __global__ void router_split_kernel(const float *__restrict__ W_r, __nv_bfloat16 *__restrict__ out,
                                     int d, int E, int Epad) {
     __shared__ float tile[32][33];
+    pdl_wait();
     const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x, ty = threadIdx.y;
     for (int r = ty; r < 32; r += 8) {
@@ -84,6 +85,7 @@ __global__ void router_split_kernel(const float *__restrict__ W_r, __nv_bfloat16
             out[2 * plane + (int64_t)e * d + i] = lo;
         }
     }
+    pdl_trigger();
 }
 
 __global__ void __launch_bounds__(L_THREADS, 1)
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(L_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctl + 256);
     volatile int *s_abort = reinterpret_cast<volatile int *>(ctl + 260);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();  // h, the W_r pieces and the previous use of zpart come from earlier stream work
     const int nk = a.d / RK;
     const int kps = nk / S;  // K stages per chunk (S divides nk)
     const int ntiles = (int)((a.T + RB - 1) / RB);
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(L_THREADS, 1)
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -301,8 +305,8 @@ cudaError_t launch_router_tc(const moe_config_t &c, const void *h, const float *
     const int Epad = plan.Epad;
     auto *pieces = static_cast<__nv_bfloat16 *>(scratch);
     dim3 sg((c.d + 31) / 32, (Epad + 31) / 32);
-    router_split_kernel<<<sg, dim3(32, 8), 0, s>>>(W_r, pieces, c.d, c.E, Epad);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err =
+        launch_pdl(router_split_kernel, sg, dim3(32, 8), 0, s, 1, W_r, pieces, c.d, c.E, Epad);
     if (err != cudaSuccess) return err;
     CUtensorMap mh, mw;
     if (!make_map(&mh, h, c.T, c.d, RB)) return cudaErrorInvalidValue;
@@ -326,8 +330,8 @@ cudaError_t launch_router_tc(const moe_config_t &c, const void *h, const float *
     const int64_t blocks = items < num_sms() ? items : num_sms();
     err = set_max_dynamic_smem((const void *)router_logits_kernel, smem);
     if (err != cudaSuccess) return err;
-    router_logits_kernel<<<(unsigned)blocks, L_THREADS, smem, s>>>(mh, mw, a);
-    return cudaGetLastError();
+    return launch_pdl(router_logits_kernel, dim3((unsigned)blocks), dim3(L_THREADS), smem, s, 1,
+                      mh, mw, a);
 }
 
 }  // namespace moe
