@@ -60,6 +60,11 @@ SMALL = [
              sel_bias_std=0.01),
     wl.small("sel_bias_tc_top1_raw", T=1800, d=128, f=128, E=100, k=1, act=G,
              gate=wl.GATE_RAW_PROB, sel_bias_std=0.01),
+    # the largest k (32) on the tensor-core and tiled router paths; E = 256 with a selection bias
+    # on the bf16 tiled router
+    wl.small("k32_tc", T=400, d=128, f=64, E=64, k=32, router_bias_var=1.0),
+    wl.small("k32_tile_f32", T=150, d=64, f=64, E=48, k=32, dtype="f32"),
+    wl.small("e256_sel_bias_tile", T=600, d=128, f=64, E=256, k=8, sel_bias_std=0.002),
     # paired kernel on an expert's odd last M tile (the second CTA's rows all masked): E = 1,
     # k = 1 and E = 2, k = 2 fix the rows per expert at T, so the last tile holds 40, 100 or 128
     # rows; SwiGLU with a ragged last N tile, GELU with biases, the top-1 scatter, and the
