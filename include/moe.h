@@ -17,7 +17,9 @@
  *     whose scratch is a static device array inside the library, and the pipeline objects of
  *     moe_pipeline.h, which own their device buffers and streams.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call is
- *     asynchronous on that stream; results are valid once the stream reaches the call.
+ *     asynchronous on that stream; results are valid once the stream reaches the call. A
+ *     workspace serves one call at a time: calls that may overlap (on different streams) need
+ *     different workspaces.
  *   - All tensors are dense row-major. "dtype" below is cfg->dtype: MOE_F32 (float) or MOE_BF16
  *     (bfloat16, raw 16-bit storage). Router weights, router bias, expert biases and gates are
  *     always float. Integer tensors are int32.
