@@ -50,6 +50,7 @@ METRIC = "MoE layer tokens/s at 1 B300; % of bf16 TC peak (GEMM) or HBM BW (deco
 # proportion: weights once, activations once). Average of GEMM1 (2.19 GB) and GEMM2 (1.34 GB).
 MEASURED_TRAFFIC = {"mixtral": 1.76e9}
 GEMM_KERNEL = "grouped_gemm_pair_kernel / grouped_gemm_tc_kernel"
+F32_KERNEL = "ffn_f32_kernel (CUDA-core FFMA)"
 
 
 def _peaks() -> dict:
@@ -297,7 +298,24 @@ def main() -> None:
     intensity = flops / nbytes
     ridge = peaks["bf16_sustained"] * 1e12 / (peaks["hbm"] * 1e9)
     traffic = MEASURED_TRAFFIC.get(w.name if not args.override else "")
-    if intensity >= ridge:
+    if w.dtype == "f32":
+        # f32 experts run as FFMA chains on the CUDA cores: the compute roof is the FP32 ALU rate,
+        # SMs x 128 FP32 lanes x 2 flop x the maximum SM clock (derived, not measured)
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        mhz = clocks.get("sm_max_mhz") or 2032.0
+        alu = sms * 128 * 2 * mhz * 1e6 / 1e12
+        if intensity >= alu * 1e12 / (peaks["hbm"] * 1e9):
+            roofline = {"bound": "alu", "kernel": F32_KERNEL, "achieved": tflops, "peak": alu,
+                        "unit": "TFLOP/s", "frac": tflops / alu,
+                        "peak_kind": f"FP32 FFMA, {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz "
+                                     "(derived)", "traffic": traffic,
+                        "flop_per_byte": intensity, "hbm_gbs": gbs}
+        else:
+            roofline = {"bound": "hbm", "kernel": F32_KERNEL, "achieved": gbs,
+                        "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                        "peak_kind": f"HBM copy ({peaks['source']})", "traffic": traffic,
+                        "flop_per_byte": intensity, "alu_tflops": tflops}
+    elif intensity >= ridge:
         roofline = {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops,
                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                     "frac": tflops / peaks["bf16_sustained"],

@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const void *__restr
 
 // aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T) and the router z-loss
 // (sum_b psum_part[b, E]) / T, reduced in a fixed order: thread (g, c) of the block sums rows
-// g, g + G, g + 2G, ... of column c (G = 1024 / (E + 1) groups), then thread c adds the G group
-// sums in g order, then thread 0 adds the E terms in e order.
+// g, g + G, g + 2G, ... of column c (G = 1024 / (E + 1) groups) into eight running sums (row
+// g + iG goes to sum i mod 8) added pairwise at the end, then thread c adds the G group sums in
+// g order, then thread 0 adds the E terms in e order.
 __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ counts,
                                                    const float *__restrict__ psum, int64_t rows,
                                                    int E, int64_t T, int k, float *aux_out,
@@ -119,9 +120,19 @@ __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ c
     const int G = 1024 / C;
     const int g = threadIdx.x / C, col = threadIdx.x % C;
     if (g < G) {
-        float s = 0.f;
-        for (int64_t b = g; b < rows; b += G) s += __ldg(psum + b * C + col);
-        part[g * C + col] = s;
+        // eight rows in flight per thread (eight partial sums, added in a fixed order)
+        float s8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s8[u] = 0.f;
+        int64_t b = g;
+        for (; b + 7 * (int64_t)G < rows; b += 8 * (int64_t)G) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s8[u] += __ldg(psum + (b + u * (int64_t)G) * C + col);
+        }
+#pragma unroll
+        for (int u = 0; u < 7; ++u)
+            if (b + u * (int64_t)G < rows) s8[u] += __ldg(psum + (b + u * (int64_t)G) * C + col);
+        part[g * C + col] = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
     }
     __syncthreads();
     if (threadIdx.x < C) {

@@ -5,16 +5,23 @@
 // Step 1 and Step 6: a full expert is three d x f matrices):
 //   GELU form   : H = GELU_tanh(X W1_e^T + b1_e),   Y = H W2_e^T + b2_e
 //   SwiGLU form : H = SiLU(X W1_e^T) * (X W3_e^T),  Y = H W2_e^T
-// Two launches of one tiled kernel (64 x 64 output tile, K-step 16, 4 x 4 outputs per thread).
-// A block finds its (expert, row tile) from a tile table it builds from offsets, so the grid is
-// sized on the host without knowing the per-expert counts.
+// Two launches of one tiled FFMA kernel. A block computes a TBM x TBN output tile of one expert
+// (thread tile TM x TN, 256 threads); it finds its (expert, row tile) from the offsets, staged in
+// shared memory, so the grid is sized on the host without knowing the per-expert counts.
+// The K loop streams 32-wide slices of the A rows and of the weight rows into shared memory with
+// cp.async, several slices in flight, so the loads of later slices overlap the FMAs of the
+// current one; within a slice the next k group's operands are read while the current one's FMAs
+// run. Small layers (few output tiles) take 32 x 32 tiles, so that more SMs get work. Every output
+// is one f32 FMA chain in ascending k, the same for both tile shapes.
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int FB = 64;   // tile rows and columns
-constexpr int FK = 16;   // K-step
+constexpr int FK = 32;          // K slice
+constexpr int FLD = FK + 4;     // shared row stride in floats: 16-byte aligned rows, and eight
+                                // consecutive rows start in eight different 16-byte bank groups
+constexpr int FTHREADS = 256;
 
 enum { EPI_STORE = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
 
@@ -29,28 +36,54 @@ struct F32Args {
     int64_t P;
 };
 
+template <int TBM, int TBN, int NS, int EPI>
+struct FTile {
+    static constexpr int NB = EPI == EPI_SWIGLU ? 2 : 1;          // weight matrices per tile
+    static constexpr int STAGE_FLOATS = (TBM + NB * TBN) * FLD;
+    static constexpr size_t SMEM = (size_t)NS * STAGE_FLOATS * sizeof(float);  // NS slices
+};
+
 __device__ __forceinline__ float gelu_tanh(float x) {
     return 0.5f * x * (1.f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));
 }
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
-template <int EPI>
-__global__ void __launch_bounds__(256) ffn_f32_kernel(F32Args a) {
-    __shared__ float As[FK][FB + 4];
-    __shared__ float Bs[FK][FB + 4];
-    __shared__ float B3s[EPI == EPI_SWIGLU ? FK : 1][FB + 4];
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int TBM, int TBN, int TM, int TN, int NS, int EPI>
+__global__ void __launch_bounds__(FTHREADS) ffn_f32_kernel(F32Args a) {
+    static_assert((TBM / TM) * (TBN / TN) == FTHREADS, "one thread per TM x TN outputs");
+    using Tl = FTile<TBM, TBN, NS, EPI>;
+    constexpr int RSTEP = TBM / TM, CSTEP = TBN / TN;  // a thread's rows / columns are strided
+    constexpr int CHUNKS = FK / 4;                      // 16-byte pieces per row slice
+    extern __shared__ __align__(16) float fsm[];
+    __shared__ int32_t s_off[257];
     __shared__ int32_t s_e, s_row0, s_rows;
     const int tid = threadIdx.x;
     pdl_wait();
+    for (int i = tid; i <= a.E; i += FTHREADS) s_off[i] = a.offsets[i];
+    __syncthreads();
     if (tid == 0) {
         int cum = 0, e_found = -1, m = 0;
         for (int e = 0; e < a.E; ++e) {
-            const int lo = a.offsets[e], hi = a.offsets[e + 1];
+            const int lo = s_off[e], hi = s_off[e + 1];
             if (hi < lo || lo < 0 || hi > a.P) {
                 report(a.dev_status, DEV_ERR_INDEX);
                 break;
             }
-            const int mt = (hi - lo + FB - 1) / FB;
+            const int mt = (hi - lo + TBM - 1) / TBM;
             if ((int)blockIdx.x < cum + mt) {
                 e_found = e;
                 m = blockIdx.x - cum;
@@ -60,65 +93,105 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(F32Args a) {
         }
         s_e = e_found;
         if (e_found >= 0) {
-            s_row0 = a.offsets[e_found] + m * FB;
-            s_rows = min(FB, a.offsets[e_found + 1] - s_row0);
+            s_row0 = s_off[e_found] + m * TBM;
+            s_rows = min(TBM, s_off[e_found + 1] - s_row0);
         }
     }
     __syncthreads();
     const int e = s_e;
     if (e < 0) return;
     const int row0 = s_row0, rows = s_rows;
-    const int n0 = blockIdx.y * FB;
-    const int ty = tid / 16, tx = tid % 16;
+    const int n0 = blockIdx.y * TBN;
+    const int ty = tid / CSTEP, tx = tid % CSTEP;
     const float *Be = a.B + (int64_t)e * a.N * a.K;
     const float *B3e = EPI == EPI_SWIGLU ? a.B3 + (int64_t)e * a.N * a.K : nullptr;
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(fsm));
 
-    float acc[4][4], acc3[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = acc3[i][j] = 0.f;
-
-    const int lr = tid / 4, lk = (tid % 4) * 4;  // loader: row (or column) and K offset
-    for (int k0 = 0; k0 < a.K; k0 += FK) {
-        float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lr < rows) av = *reinterpret_cast<const float4 *>(a.A + (int64_t)(row0 + lr) * a.K + k0 + lk);
-        const float4 bv = *reinterpret_cast<const float4 *>(Be + (int64_t)(n0 + lr) * a.K + k0 + lk);
-        As[lk + 0][lr] = av.x; As[lk + 1][lr] = av.y; As[lk + 2][lr] = av.z; As[lk + 3][lr] = av.w;
-        Bs[lk + 0][lr] = bv.x; Bs[lk + 1][lr] = bv.y; Bs[lk + 2][lr] = bv.z; Bs[lk + 3][lr] = bv.w;
-        if (EPI == EPI_SWIGLU) {
-            const float4 cv = *reinterpret_cast<const float4 *>(B3e + (int64_t)(n0 + lr) * a.K + k0 + lk);
-            B3s[lk + 0][lr] = cv.x; B3s[lk + 1][lr] = cv.y; B3s[lk + 2][lr] = cv.z; B3s[lk + 3][lr] = cv.w;
+    // One K slice into stage `st`: TBM A rows (zeros past the tile's last row), then TBN rows of
+    // each weight matrix.
+    auto load_slice = [&](int st, int k0) {
+        const uint32_t sA = sbase + st * Tl::STAGE_FLOATS * 4;
+        for (int c = tid; c < TBM * CHUNKS; c += FTHREADS) {
+            const int r = c / CHUNKS, q = c % CHUNKS;
+            const bool ok = r < rows;
+            const float *src = a.A + (int64_t)(row0 + (ok ? r : 0)) * a.K + k0 + 4 * q;
+            cp_async16(sA + (r * FLD + 4 * q) * 4, src, ok ? 16 : 0);
         }
-        __syncthreads();
+        const uint32_t sB = sA + TBM * FLD * 4;
+        for (int c = tid; c < Tl::NB * TBN * CHUNKS; c += FTHREADS) {
+            const int r = c / CHUNKS, q = c % CHUNKS;
+            const float *W = (EPI == EPI_SWIGLU && r >= TBN) ? B3e + (int64_t)(n0 + r - TBN) * a.K
+                                                              : Be + (int64_t)(n0 + r) * a.K;
+            cp_async16(sB + (r * FLD + 4 * q) * 4, W + k0 + 4 * q, 16);
+        }
+    };
+
+    float acc[TM][TN], acc3[TM][TN];
 #pragma unroll
-        for (int kk = 0; kk < FK; ++kk) {
-            float x[4], w[4], w3[4];
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = As[kk][ty + 16 * i];
+        for (int j = 0; j < TN; ++j) acc[i][j] = acc3[i][j] = 0.f;
+
+    const int nk = a.K / FK;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                w[j] = Bs[kk][tx + 16 * j];
-                if (EPI == EPI_SWIGLU) w3[j] = B3s[kk][tx + 16 * j];
+    for (int s = 0; s < NS - 1; ++s) {
+        if (s < nk) load_slice(s, s * FK);
+        cp_async_commit();
+    }
+    for (int kb = 0; kb < nk; ++kb) {
+        cp_async_wait<NS - 2>();       // this thread's copies of slice kb have landed
+        __syncthreads();               // everyone's have, and slice kb-1 is no longer read
+        const int nxt = kb + NS - 1;
+        if (nxt < nk) load_slice(nxt % NS, nxt * FK);
+        cp_async_commit();
+        const float *As = fsm + (kb % NS) * Tl::STAGE_FLOATS;
+        const float *Bs = As + TBM * FLD;
+        const float *B3s = Bs + TBN * FLD;
+        // operands of the next 4-wide k group are read from shared memory while the FMAs of the
+        // current group run (two register sets, alternating)
+        float4 x[2][TM], w[2][TN], w3[2][TN];
+        auto fetch = [&](int b, int kk) {
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+                x[b][i] = *reinterpret_cast<const float4 *>(As + (ty + RSTEP * i) * FLD + kk);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                w[b][j] = *reinterpret_cast<const float4 *>(Bs + (tx + CSTEP * j) * FLD + kk);
+                if (EPI == EPI_SWIGLU)
+                    w3[b][j] = *reinterpret_cast<const float4 *>(B3s + (tx + CSTEP * j) * FLD + kk);
             }
+        };
+        fetch(0, 0);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+        for (int g = 0; g < FK / 4; ++g) {
+            const int b = g & 1;
+            if (g + 1 < FK / 4) fetch(b ^ 1, 4 * (g + 1));
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    acc[i][j] = fmaf(x[i], w[j], acc[i][j]);
-                    if (EPI == EPI_SWIGLU) acc3[i][j] = fmaf(x[i], w3[j], acc3[i][j]);
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) {
+                    acc[i][j] = fmaf(x[b][i].x, w[b][j].x, acc[i][j]);
+                    acc[i][j] = fmaf(x[b][i].y, w[b][j].y, acc[i][j]);
+                    acc[i][j] = fmaf(x[b][i].z, w[b][j].z, acc[i][j]);
+                    acc[i][j] = fmaf(x[b][i].w, w[b][j].w, acc[i][j]);
+                    if (EPI == EPI_SWIGLU) {
+                        acc3[i][j] = fmaf(x[b][i].x, w3[b][j].x, acc3[i][j]);
+                        acc3[i][j] = fmaf(x[b][i].y, w3[b][j].y, acc3[i][j]);
+                        acc3[i][j] = fmaf(x[b][i].z, w3[b][j].z, acc3[i][j]);
+                        acc3[i][j] = fmaf(x[b][i].w, w3[b][j].w, acc3[i][j]);
+                    }
                 }
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = ty + 16 * i;
+    for (int i = 0; i < TM; ++i) {
+        const int r = ty + RSTEP * i;
         if (r >= rows) continue;
         float *orow = a.out + (int64_t)(row0 + r) * a.N;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx + 16 * j;
+        for (int j = 0; j < TN; ++j) {
+            const int n = n0 + tx + CSTEP * j;
             float v = acc[i][j];
             if (EPI == EPI_SWIGLU) {
                 v = silu(v) * acc3[i][j];
@@ -132,11 +205,27 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(F32Args a) {
     pdl_trigger();
 }
 
+template <int TBM, int TBN, int TM, int TN, int NS, int EPI>
+cudaError_t launch_tiles(const F32Args &a, int64_t P, cudaStream_t s) {
+    constexpr size_t smem = FTile<TBM, TBN, NS, EPI>::SMEM;
+    const void *k = (const void *)ffn_f32_kernel<TBM, TBN, TM, TN, NS, EPI>;
+    cudaError_t err = set_max_dynamic_smem(k, smem);
+    if (err != cudaSuccess) return err;
+    // at most one partial row tile per expert beyond P / TBM full ones
+    const int64_t mtiles = (P + TBM - 1) / TBM + a.E;
+    dim3 grid((unsigned)mtiles, (unsigned)(a.N / TBN));
+    return launch_pdl(ffn_f32_kernel<TBM, TBN, TM, TN, NS, EPI>, grid, dim3(FTHREADS), smem, s, 1,
+                      a);
+}
+
 template <int EPI>
 cudaError_t launch_f32(const F32Args &a, int64_t P, cudaStream_t s) {
-    const int64_t mtiles = (P + FB - 1) / FB + a.E;
-    dim3 grid((unsigned)mtiles, (unsigned)(a.N / FB));
-    return launch_pdl(ffn_f32_kernel<EPI>, grid, dim3(256), 0, s, 1, a);
+    // 64 x 64 tiles (4 x 4 per thread, 3 slices in flight) when they give every SM two blocks,
+    // else 32 x 32 tiles (2 x 2 per thread, 4 slices in flight: less work per slice to hide the
+    // load latency behind)
+    const int64_t big = ((P + 63) / 64 + a.E) * (int64_t)(a.N / 64);
+    if (big >= 2 * (int64_t)num_sms()) return launch_tiles<64, 64, 4, 4, 3, EPI>(a, P, s);
+    return launch_tiles<32, 32, 2, 2, 4, EPI>(a, P, s);
 }
 
 }  // namespace

@@ -23,6 +23,13 @@ SMALL = [
     wl.small("ragged_gelu_bias_f32", T=133, d=128, f=192, E=5, k=2, act=G, dtype="f32",
              has_bias=True),
     wl.small("f32_swiglu", T=200, d=128, f=256, E=8, k=2, dtype="f32"),
+    # f32 FFN with its 64 x 64 tiles (at least two blocks per SM): GEMM1 only (GELU with biases,
+    # SwiGLU), and both GEMMs with skewed loads
+    wl.small("f32_big_tiles_gelu_bias", T=2048, d=128, f=512, E=4, k=2, act=G, dtype="f32",
+             has_bias=True),
+    wl.small("f32_big_tiles_swiglu", T=1100, d=256, f=512, E=6, k=2, dtype="f32"),
+    wl.small("f32_big_tiles_both", T=4000, d=256, f=256, E=4, k=2, dtype="f32",
+             router_bias_var=2.0),
     wl.small("gelu_bias_raw_prob", T=517, d=256, f=512, E=16, k=1, act=G,
              gate=wl.GATE_RAW_PROB, has_bias=True),
     wl.small("skewed_idle", T=1000, d=128, f=256, E=32, k=4, router_bias_var=8.0),
