@@ -213,6 +213,34 @@ def test_full_size_workloads(name):
         assert (got["counts"] > 0).all()
 
 
+LARGE = [
+    # 2M slots: 1954 dispatch chunks, so the look-back runs over many rounds of co-resident blocks
+    wl.small("many_slots", T=1_000_000, d=64, f=64, E=8, k=2, router_bias_var=1.0),
+    # the largest E and k together over 640K slots (tiled router, k = 32 combine)
+    wl.small("e256_k32_many", T=20_000, d=128, f=64, E=256, k=32),
+    # long K: d = 8192 (GEMM1 with 128 K stages, few-token split-d router)
+    wl.small("wide_d", T=300, d=8192, f=256, E=4, k=2),
+]
+
+
+@pytest.mark.parametrize("w", LARGE, ids=lambda w: w.name)
+def test_large_cases(w):
+    """Shapes at the edges of what the library takes, through moe_forward: routing, counts and
+    aux over every token, the layer output on a deterministic token sample."""
+    inputs = _inputs(w)
+    tokens = oracle.sample_tokens(w.T, stride=max(1, w.T // 4096))
+    ref = oracle.reference(w, inputs, tokens=tokens)
+    dev = to_dev(inputs)
+    fw = run_forward(w, dev)
+    assert fw["status"] == B.MOE_OK
+    diff = routing_agreement(ref, fw["idx"].numpy())
+    if len(diff) == 0:
+        np.testing.assert_array_equal(fw["counts"].numpy(), ref["counts"])
+    assert fw["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
+    stats = check_layer_output(w, ref, fw["y"], skip_tokens=diff)
+    print(f"{w.name}: near-tie tokens {len(diff)}, {stats}")
+
+
 def test_empty_batch():
     w = wl.small("empty", T=0, d=64, f=64, E=4, k=2)
     cfg = B.config_for(w)
