@@ -14,10 +14,11 @@
 //   2. Decoupled look-back over chunks (Merrill & Garland, single-pass prefix scan): thread e
 //      publishes (AGGREGATE, count) for its expert, then walks back over earlier chunks adding
 //      aggregates until it meets an INCLUSIVE prefix, and publishes (INCLUSIVE, prefix). Each
-//      flag/value pair is one 64-bit release store, read with acquire loads.
-//   3. The last chunk knows the totals: it writes counts and offsets (exclusive scan over
-//      experts) and raises a done flag; every block waits for it and scatters sorted_token and
-//      slot_of.
+//      flag/value pair is one 64-bit release store; readers load eight earlier words per round
+//      trip (relaxed loads: the word itself is all they need).
+//   3. The last chunk knows the totals: it writes counts and offsets (an exclusive scan over
+//      experts by warp scans) and raises a done flag; every block waits for it and scatters
+//      sorted_token and slot_of.
 // The launch is cooperative, so all blocks are co-resident and every wait can be satisfied;
 // each wait is still bounded by %globaltimer and reports DEV_ERR_TIMEOUT instead of hanging.
 #include "internal.cuh"
@@ -25,6 +26,7 @@
 namespace moe {
 namespace {
 
+constexpr int LB_WINDOW = 8;  // look-back words read per round trip
 constexpr uint64_t FLAG_AGG = 1ull << 32;
 constexpr uint64_t FLAG_INC = 2ull << 32;
 
@@ -44,9 +46,11 @@ struct DispatchArgs {
 __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+// A look-back word carries its flag and its count in one 64-bit store, so a reader needs only
+// that word: relaxed loads (at gpu scope, from L2) may be issued several at a time.
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
     unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
@@ -93,29 +97,53 @@ __device__ __forceinline__ int chunk_ranks(const DispatchArgs &a, int c, int32_t
     return e;
 }
 
+// counts[e] = tot[e], offsets = exclusive scan over e of the kept rows min(tot[e], cap), and
+// s_off[e] = offsets[e], for e < E <= 256, by the block's first 8 warps (warp scans, then a scan
+// of the 8 warp totals); the whole block calls it. offsets[E] is the number of kept rows.
+__device__ __forceinline__ void publish_offsets(const DispatchArgs &a, const int32_t *tot,
+                                                int32_t *s_off, int32_t *s_wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = a.E;
+    int kept = 0, incl = 0;
+    if (tid < 256) {
+        if (tid < E) {
+            const int c = tot[tid];
+            kept = (a.cap >= 0 && c > a.cap) ? (int)a.cap : c;
+        }
+        incl = kept;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_wsum[w] = incl;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        int base = 0;
+        for (int q = 0; q < w; ++q) base += s_wsum[q];
+        const int excl = base + incl - kept;
+        if (tid < E) {
+            a.counts[tid] = tot[tid];
+            a.offsets[tid] = excl;
+            s_off[tid] = excl;
+        }
+        if (tid == E - 1) a.offsets[E] = excl + kept;
+    }
+    __syncthreads();
+}
+
 // All slots fit in one chunk: histogram, scan over experts and scatter in one block, with no
 // look-back, flags or workspace.
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(DispatchArgs a) {
     __shared__ int32_t cnt[32 * 256];
-    __shared__ int32_t s_off[257];
+    __shared__ int32_t s_tot[256], s_off[257], s_wsum[8];
     pdl_wait();
     const int tid = threadIdx.x, E = a.E;
     int lrank, agg;
     const int e = chunk_ranks(a, 0, cnt, &lrank, &agg);
-    if (tid < E) s_off[tid] = agg;
+    if (tid < E) s_tot[tid] = agg;
     __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int q = 0; q < E; ++q) {
-            const int c = s_off[q];
-            a.counts[q] = c;
-            a.offsets[q] = run;
-            s_off[q] = run;
-            run += (a.cap >= 0 && c > a.cap) ? (int)a.cap : c;
-        }
-        a.offsets[E] = run;
-    }
-    __syncthreads();
+    publish_offsets(a, s_tot, s_off, s_wsum);
     if (e >= 0) {
         if (a.cap >= 0 && lrank >= a.cap) {
             a.slot_of[tid] = -1;  // over capacity: dropped
@@ -130,7 +158,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(Di
 
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchArgs a) {
     __shared__ int32_t cnt[32 * 256];
-    __shared__ int32_t s_tot[257];
+    __shared__ int32_t s_tot[257], s_pub[257], s_wsum[8];
     __shared__ int s_abort;
     const int tid = threadIdx.x, E = a.E;
     if (tid == 0) s_abort = 0;
@@ -153,24 +181,39 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
                 unsigned long long t_start = 0;
                 int q = c - 1;
                 uint32_t spins = 0;
+                // walk back LB_WINDOW chunks per round trip: read their words together, then
+                // add them in order up to the first INCLUSIVE one; an unpublished word ends the
+                // round and is read again
                 while (q >= 0) {
-                    const unsigned long long v = ld_acquire(a.words + (size_t)q * E + tid);
-                    const unsigned long long flag = v & 0xffffffff00000000ull;
-                    if (flag == 0) {
-                        if ((++spins & 255u) == 0) {
-                            const unsigned long long now = globaltimer_ns();
-                            if (t_start == 0) t_start = now;
-                            else if (now - t_start > a.spin_limit_ns) {
-                                report(a.dev_status, DEV_ERR_TIMEOUT);
-                                s_abort = 1;
-                                break;
-                            }
+                    unsigned long long v[LB_WINDOW];
+#pragma unroll
+                    for (int i = 0; i < LB_WINDOW; ++i)
+                        v[i] = q - i >= 0 ? ld_relaxed(a.words + (size_t)(q - i) * E + tid) : 0ull;
+                    int used = 0;
+                    bool inclusive = false;
+#pragma unroll
+                    for (int i = 0; i < LB_WINDOW; ++i) {
+                        if (q - i < 0) break;
+                        const unsigned long long flag = v[i] & 0xffffffff00000000ull;
+                        if (flag == 0) break;
+                        excl += (int)(uint32_t)v[i];
+                        ++used;
+                        if (flag == FLAG_INC) {
+                            inclusive = true;
+                            break;
                         }
-                        continue;
                     }
-                    excl += (int)(uint32_t)v;
-                    if (flag == FLAG_INC) break;
-                    --q;
+                    if (inclusive) break;
+                    q -= used;
+                    if (used == 0 && (++spins & 255u) == 0) {
+                        const unsigned long long now = globaltimer_ns();
+                        if (t_start == 0) t_start = now;
+                        else if (now - t_start > a.spin_limit_ns) {
+                            report(a.dev_status, DEV_ERR_TIMEOUT);
+                            s_abort = 1;
+                            break;
+                        }
+                    }
                 }
                 st_release(mine, FLAG_INC | (uint32_t)(excl + agg));
             }
@@ -179,14 +222,8 @@ __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_kernel(DispatchA
         }
         if (c == a.nchunks - 1) {
             __syncthreads();
+            publish_offsets(a, s_tot, s_pub, s_wsum);
             if (tid == 0) {
-                int run = 0;
-                for (int e = 0; e < E; ++e) {
-                    a.counts[e] = s_tot[e];
-                    a.offsets[e] = run;
-                    run += (a.cap >= 0 && s_tot[e] > a.cap) ? (int)a.cap : s_tot[e];
-                }
-                a.offsets[E] = run;
                 __threadfence();
                 st_release_u32(a.done, 1u);
             }
