@@ -10,11 +10,17 @@
 // Both are "A times B-transposed" with A and B K-contiguous, which is exactly the K-major operand
 // form of tcgen05.mma.
 //
-// Kernel design (one persistent CTA per SM, 192 threads, static round-robin tile schedule):
+// Two kernels share this design. grouped_gemm_tc_kernel: one persistent CTA per SM, 320 threads,
+// static round-robin tile schedule over 128 x 256 output tiles. grouped_gemm_pair_kernel (experts
+// of at least four M tiles on average): 2-CTA clusters computing 256 x 256 tiles with
+// tcgen05.mma.cta_group::2, each CTA holding half of A and half of B, a 6-stage ring. In both:
 //   warp 0      TMA producer: 2-D tiled bulk copies (128-byte swizzle) of a 128 x 64 A tile and
-//               a 256 x 64 B tile (SwiGLU: 128 rows of W1 stacked on 128 rows of W3) into a
-//               4-stage shared-memory ring, signalling mbarriers with transaction counts.
-//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M = 128, N = 256,
+//               a 256 x 64 B tile (SwiGLU: 128 rows of W1 stacked on 128 rows of W3; a pair CTA
+//               copies its halves) into the shared-memory ring, signalling mbarriers with
+//               transaction counts (the opt-in fused gather reads A rows of h with
+//               tile::gather4 instead).
+//   warp 1      MMA issuer (one thread; in a pair, the leader CTA's, with cta_group::2 and
+//               M = 256): tcgen05.mma.cta_group::1.kind::f16, M = 128, N = 256,
 //               K = 16, f32 accumulation in tensor memory; tcgen05.commit releases a ring stage
 //               when its MMAs have read it, and hands a finished accumulator to the epilogue.
 //               Warp 1 also owns the 512-column TMEM allocation (two 128 x 256 f32 accumulators,
@@ -27,6 +33,7 @@
 // few weight tiles (read once from HBM, then from L2) and one expert's activations.
 // Rows of an expert's last M tile that belong to the next expert (or lie past the end, which TMA
 // fills with zeros) are computed and masked at the store.
+// A dropless top-1 GEMM2 may scatter g * row straight into y[token] (fused combine).
 // Every mbarrier wait is bounded by %globaltimer: on expiry the CTA records DEV_ERR_TIMEOUT,
 // stops issuing, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include "tc_ptx.cuh"
