@@ -148,7 +148,10 @@ def run_reference(args, w) -> None:
     if rank != 0:
         return
     import oracle
-    cb = _cpu_baseline(w, budget_s=max(2.0, 60.0 / max(args.steps + args.warmup, 1)))
+    # each step a bounded token sample sized so that all warm-up and timed steps together take
+    # about two minutes (a run of the sample takes between half and all of its budget)
+    per_step = 120.0 / max(args.steps + args.warmup, 1)
+    cb = _cpu_baseline(w, budget_s=max(0.02, per_step))
     n_tok = int(cb["sample"].split()[1])
     sub = w.with_(T=n_tok)
     inputs = wl.generate(w)
