@@ -145,8 +145,41 @@ def _check_expert_rows(w, inputs, got, rows):
         assert rel_l2(yg, yr) <= 1e-2
 
 
+def _random_case(seed: int):
+    """A seeded random layer shape and variant within the library's limits, small enough for the
+    oracle to check every output."""
+    rng = np.random.default_rng(1000 + seed)
+    dtype = "f32" if rng.random() < 0.3 else "bf16"
+    act = G if rng.random() < 0.5 else S
+    E = int(rng.integers(1, 41))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    return wl.small(
+        f"random_{seed}", T=int(rng.integers(1, 900)), d=64 * int(rng.integers(1, 6)),
+        f=64 * int(rng.integers(1, 9)), E=E, k=k, act=act,
+        gate=wl.GATE_RAW_PROB if rng.random() < 0.3 else wl.GATE_RENORM, dtype=dtype,
+        has_bias=bool(act == G and rng.random() < 0.5),
+        router_bias_var=float(rng.choice([1.0, 4.0])) if rng.random() < 0.4 else None,
+        seed=int(rng.integers(1, 10_000)),
+        capacity_factor=float(rng.choice([0.5, 1.0, 1.25])) if rng.random() < 0.3 else 0.0,
+        sel_bias_std=0.01 if rng.random() < 0.2 else 0.0)
+
+
+RANDOM = [_random_case(i) for i in range(32)]
+
+
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_small_cases_step_by_step(w):
+    _check_case(w)
+
+
+@pytest.mark.parametrize("w", RANDOM, ids=lambda w: w.name)
+def test_random_shapes_step_by_step(w):
+    """32 seeded random shapes and variants (dtype, activation, gate mode, biases, router bias,
+    capacity, selection bias; T < 900, E <= 40, k <= 8)."""
+    _check_case(w)
+
+
+def _check_case(w):
     inputs = _inputs(w)
     ref = oracle.reference(w, inputs)
     dev = to_dev(inputs)
