@@ -58,6 +58,18 @@ def test_expert_ranges_cover_every_expert_once():
             assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 1
 
 
+def test_send_splits_and_single_rank_exchange():
+    """Rows sent per owner are the sums of the owner's block of counts; with one process the
+    count exchange returns this rank's block unchanged."""
+    import torch
+    counts = torch.tensor([5, 0, 3, 7, 1], dtype=torch.int32)
+    assert ep.send_splits(counts, 2) == [8, 8]        # experts 0-2 | 3-4
+    assert ep.send_splits(counts, 3) == [5, 10, 1]    # 0-1 | 2-3 | 4
+    assert ep.send_splits(counts, 1) == [16]
+    got = ep.exchange_counts(counts, 1)
+    assert got.shape == (1, 5) and got.tolist() == [[5, 0, 3, 7, 1]]
+
+
 @pytest.mark.parametrize("case", list(CASES))
 def test_two_ranks_match_the_layer_on_their_tokens(case):
     w, _ = CASES[case]
