@@ -312,6 +312,11 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
     if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    // the auxiliary value and z-loss need only the counts and the router's partial sums: reduce
+    // them now, while both are still in L2, not after the expert GEMMs have streamed the weights
+    // through it
+    if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
     const ForwardPlan plan = plan_of(c);
     const bool scatter = plan.scatter;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
@@ -331,8 +336,6 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (ev_ffn1 && cudaEventRecord(ev_ffn1, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!scatter && (e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
@@ -397,7 +400,7 @@ moe_status_t moe_forward_launch_count(const moe_config_t *cfg, int32_t *kernels)
         return MOE_OK;
     }
     const ForwardPlan plan = plan_of(*cfg);
-    // router (+ split), dispatch, permute, two FFN launches, combine, aux
+    // router (+ split), dispatch, aux, permute, two FFN launches, combine
     *kernels = router_launches(*cfg) + 1 + (plan.gather ? 0 : 1) + 2 + (plan.scatter ? 0 : 1) + 1;
     return MOE_OK;
 }

@@ -94,7 +94,7 @@ def test_fuse_gather_flag():
 
 
 @pytest.mark.parametrize("name,kw,expect", [
-    # router, dispatch, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine, aux
+    # router, dispatch, aux, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine
     ("micro", {}, 7),
     ("decode", {}, 7),
     ("mixtral", {}, 9),                           # tensor-core router: split, logits, select
