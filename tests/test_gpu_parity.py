@@ -274,6 +274,30 @@ def test_large_cases(w):
     print(f"{w.name}: near-tie tokens {len(diff)}, {stats}")
 
 
+@pytest.mark.parametrize("k,dtype", [(1, "bf16"), (2, "bf16"), (2, "f32")])
+def test_every_token_to_one_expert(k, dtype):
+    """A router bias of 50 on expert 5 sends every token's first choice there: one expert holds
+    T rows (many GEMM tiles, every dispatch chunk a single expert), the others share the rest."""
+    w = wl.small(f"one_hot_k{k}_{dtype}", T=3000, d=128, f=192, E=8, k=k, dtype=dtype,
+                 act=G if k == 1 else S, gate=wl.GATE_RAW_PROB if k == 1 else wl.GATE_RENORM,
+                 seed=77)
+    inputs = _inputs(w)
+    b = torch.zeros(w.E)
+    b[5] = 50.0
+    inputs["b_r"] = b
+    ref = oracle.reference(w, inputs)
+    assert ref["counts"][5] == w.T
+    dev = to_dev(inputs)
+    got = run_steps(w, inputs, dev)
+    _check_steps(w, inputs, ref, got)
+    assert int(got["counts"][5]) == w.T
+    check_layer_output(w, ref, got["y"])
+    fw = run_forward(w, dev)
+    assert fw["status"] == B.MOE_OK
+    check_layer_output(w, ref, fw["y"])
+    assert fw["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
+
+
 def test_empty_batch():
     w = wl.small("empty", T=0, d=64, f=64, E=4, k=2)
     cfg = B.config_for(w)
