@@ -1,6 +1,6 @@
-"""Benchmark of the MoE layer forward on B300: tokens/s and the grouped expert GEMM's roofline.
+"""Benchmark of the MoE layer forward on B300: tokens/s and each expert FFN's roofline fraction.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|mixtral|...] [--impl ours|reference]
 
 One step = one moe_forward call: the whole layer (router + top-k, dispatch + permute, grouped
 expert FFN, combine, auxiliary value) over one batch of the workload's seeded synthetic inputs,
@@ -8,17 +8,25 @@ with weights and inputs resident in HBM. Each rank (one process per GPU, launche
 an independent replica of the layer on its own batch: there is no exchange on this path, so the
 scaling is weak and `value` is the tokens of all ranks over the slowest rank's time.
 
-The JSON line also carries:
+By default (`--workload all`) the run times all five workloads one after another, each for K
+steps after W warm-up steps, and prints ONE line: the Mixtral-shape layer is the headline (its
+keys at the top level) and every workload's own measurements sit under `workloads`.
+
+Each measurement carries:
   e2e          the same metric through the C-ABI pipeline (moe_pipeline_submit) with host
                buffers: every step copies its pinned h in and its y (plus aux) out inside the
                timed region, the copies of neighbouring steps overlapping the layer computation;
-  roofline     the dominant kernel (the grouped expert GEMM, launched twice per step: GEMM1 and
+  roofline     the dominant kernel (the grouped expert FFN, launched twice per step: GEMM1 and
                GEMM2) over its CUDA-event duration, recorded by moe_forward_events on the
-               launching stream inside the timed region: algorithmic flops against the measured
-               bf16 tensor peak when the FFN's flops per HBM byte exceed the ridge point of the
-               measured peaks, else its algorithmic bytes against the measured HBM bandwidth;
-  cpu_baseline the double-precision oracle on this machine's host cores, on a bounded token
-               sample of the same workload (rank 0, N = 1 only);
+               launching stream inside the timed region: algorithmic flops against the bf16
+               tensor peak when the FFN's flops per HBM byte exceed the ridge point, else its
+               algorithmic bytes against the measured HBM copy bandwidth (f32 layers: flops
+               against the FP32 FFMA rate measured in the same run). The tensor peak is the burst
+               figure unless the timed region ran for a second or more under the power cap
+               (then the sustained figure); `frac_alt` gives the fraction against the other one;
+  cpu_baseline the double-precision oracle on this machine's host cores (rank 0, N = 1 only):
+               routing over all T tokens plus the expert MLPs and combine of a token sample,
+               extrapolated to T tokens;
   graph        the same step recorded once in a CUDA graph (Layer.capture) and replayed K times:
                the launch-bound shapes' time without host launch cost;
   clocks       nvidia-smi samples taken during the timed region.
@@ -44,13 +52,22 @@ sys.path.insert(0, ROOT)
 from sparse_mixture_experts_70_b300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE layer tokens/s at 1 B300; % of bf16 TC peak (GEMM) or HBM BW (decode)"
-# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu capture summarised in
-# profiles/grouped_gemm_pair_T2048_E2_k1.md (a reduced case: 2 of 8 experts, 2048 of 8192 rows),
-# scaled to the full Mixtral-shape launch by the experts and rows processed (traffic grows in
-# proportion: weights once, activations once). Average of GEMM1 (2.19 GB) and GEMM2 (1.34 GB).
-MEASURED_TRAFFIC = {"mixtral": 1.76e9}
+HEADLINE = "mixtral"
+ORDER = ["mixtral", "many_small", "switch", "decode", "micro"]
+# DRAM bytes (read + write) per launch of the dominant kernel, averaged over its two launches
+# (GEMM1, GEMM2), from ncu captures of the current kernels. `scale` says how the figure relates
+# to the full workload: "full" = captured at the full shape; otherwise captured on a reduced case
+# and scaled by the experts and rows processed (the traffic grows in proportion: weights once,
+# activations once).
+MEASURED_TRAFFIC = {
+    "mixtral": {"bytes": 1.76e9, "scale": "scaled from a reduced ncu capture (T=2048, E=2, k=1: "
+                                          "2 of 8 experts, 2048 of 8192 rows)"},
+}
 GEMM_KERNEL = "grouped_gemm_pair_kernel / grouped_gemm_tc_kernel"
 F32_KERNEL = "ffn_f32_kernel (CUDA-core FFMA)"
+# A timed region at least this long and capped by power is "sustained"; anything shorter, or
+# without sw_power_cap in its clock samples, runs at the burst rate.
+SUSTAINED_REGION_S = 1.0
 
 
 def _peaks() -> dict:
@@ -61,6 +78,53 @@ def _peaks() -> dict:
         return dict(bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
                     hbm=p["hbm_gbs"], source="measured")
     return dict(bf16=1800.0, bf16_sustained=1400.0, hbm=6400.0, source="fallback")
+
+
+def roofline(w, ffn_ms: float, peaks: dict, region_s: float, reasons, alu: dict | None = None,
+             traffic: dict | None = None) -> dict:
+    """The expert FFN's roofline entry.
+
+    w: the workload (its algorithmic flops and bytes); ffn_ms: the FFN's live duration per step
+    (both launches); peaks: tensor (burst, sustained) and HBM peaks; region_s / reasons: length
+    of the timed region and the clock-event reasons seen in it; alu: {"tflops": measured FP32
+    FFMA rate, "how": ...} for f32 layers; traffic: {"bytes": DRAM bytes per launch, "scale": how
+    it was taken} or None.
+    """
+    flops, nbytes = w.expert_flops(), w.ffn_bytes()
+    launches = 2
+    tflops = flops / (ffn_ms * 1e-3) / 1e12
+    gbs = nbytes / (ffn_ms * 1e-3) / 1e9
+    intensity = flops / nbytes
+    sustained = region_s >= SUSTAINED_REGION_S and "sw_power_cap" in set(reasons or ())
+    tc_peak, tc_alt = ((peaks["bf16_sustained"], peaks["bf16"]) if sustained
+                       else (peaks["bf16"], peaks["bf16_sustained"]))
+    tc_kind = "bf16 sustained" if sustained else "bf16 burst"
+    alt_kind = "bf16 burst" if sustained else "bf16 sustained"
+    common = {"flop_per_byte": intensity, "launches_per_step": launches,
+              "algorithmic_flops_per_launch": flops / launches,
+              "algorithmic_bytes_per_launch": nbytes / launches,
+              "traffic": traffic["bytes"] if traffic else None,
+              "traffic_source": traffic["scale"] if traffic else None,
+              "region_s": region_s}
+    if w.dtype == "f32":
+        rate = alu["tflops"]
+        if intensity >= rate * 1e12 / (peaks["hbm"] * 1e9):
+            return {"bound": "alu", "kernel": F32_KERNEL, "achieved": tflops, "peak": rate,
+                    "unit": "TFLOP/s", "frac": tflops / rate, "peak_kind": alu["how"],
+                    "hbm_gbs": gbs, **common}
+        return {"bound": "hbm", "kernel": F32_KERNEL, "achieved": gbs, "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                "peak_kind": f"HBM copy ({peaks['source']})", "alu_tflops": tflops, **common}
+    ridge = tc_peak * 1e12 / (peaks["hbm"] * 1e9)
+    if intensity >= ridge:
+        return {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops, "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": tflops / tc_peak,
+                "peak_kind": f"{tc_kind} ({peaks['source']})", "frac_alt": tflops / tc_alt,
+                "frac_alt_kind": alt_kind, "hbm_gbs": gbs, **common}
+    return {"bound": "hbm", "kernel": GEMM_KERNEL, "achieved": gbs, "peak": peaks["hbm"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm"],
+            "peak_kind": f"HBM copy ({peaks['source']})", "tensor_tflops": tflops,
+            "tensor_frac": tflops / tc_peak, "tensor_peak_kind": tc_kind, **common}
 
 
 class Clocks:
@@ -115,66 +179,242 @@ class Clocks:
                 "power_w_max": max(power) if power else None}
 
 
-def _cpu_baseline(w, budget_s: float = 12.0) -> dict:
-    """The oracle (double, OpenMP over rows) on a bounded prefix of the workload's tokens."""
-    import oracle
-    threads = oracle.max_threads()
-    inputs = wl.generate(w)
+class OracleRun:
+    """The oracle (double, OpenMP over rows) on the host cores for one workload: routing (router,
+    top-k, gates, dispatch, aux) over all T tokens, then the expert MLPs and combine over the first
+    n tokens; a run's tokens/s is T / (routing time + the n tokens' time scaled to T tokens)."""
 
-    def run(n):
-        sub = w.with_(T=n)
-        part = dict(inputs)
-        part["h"] = inputs["h"][:n].contiguous()
+    def __init__(self, w, inputs: dict):
+        import oracle
+        self.oracle = oracle
+        self.w, self.inputs = w, inputs
+        self.threads = oracle.max_threads()
+
+    def run(self, n: int) -> dict:
+        oracle, w, inputs = self.oracle, self.w, self.inputs
         t0 = time.perf_counter()
-        oracle.reference(sub, part)
-        return time.perf_counter() - t0
+        r = oracle.route(w, inputs)
+        t_route = time.perf_counter() - t0
+        keep = None if r["capacity"] < 0 else (r["slot_of"] >= 0).reshape(w.T, w.k)
+        toks = torch.arange(n, dtype=torch.int64).numpy()
+        t1 = time.perf_counter()
+        oracle.forward_rows(toks, inputs["h"], r["idx"], r["g"], inputs["W1"], inputs.get("W3"),
+                            inputs["W2"], inputs.get("b1"), inputs.get("b2"), oracle.act_code(w),
+                            keep=keep)
+        t_rows = time.perf_counter() - t1
+        total = t_route + t_rows * w.T / n
+        return {"value": w.T / total, "unit": "tokens/s", "cores": self.threads, "kind": "oracle",
+                "sample": f"{w.name}: routing (router, top-k, gates, dispatch, aux) over all {w.T} "
+                          f"tokens in {t_route:.2f} s, expert MLPs + combine over the first {n} "
+                          f"tokens in {t_rows:.2f} s, scaled to {w.T} tokens: {total:.1f} s of "
+                          f"double-precision work on {self.threads} threads",
+                "seconds": t_route + t_rows}
 
-    n = 1
-    t = run(n)
-    while t < budget_s / 8 and n < w.T:
-        n = min(w.T, n * 4)
-        t = run(n)
-    if t < budget_s / 2 and n < w.T:
-        n = min(w.T, max(n + 1, int(n * (budget_s / 2) / max(t, 1e-3))))
-        t = run(n)
-    return {"value": n / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {w.T} tokens of the {w.name} workload, full layer "
-                      f"(router, top-k, gates, dispatch, expert MLPs, combine, aux) in double, "
-                      f"{t:.1f} s"}
+    def calibrate(self, budget_s: float) -> int:
+        """The token count n whose run takes about budget_s (between a half and all of it)."""
+        n = 1
+        t = self.run(n)["seconds"]
+        while t < budget_s / 8 and n < self.w.T:
+            n = min(self.w.T, n * 4)
+            t = self.run(n)["seconds"]
+        if t < budget_s / 2 and n < self.w.T:
+            n = min(self.w.T, max(n + 1, int(n * (budget_s * 0.75) / max(t, 1e-3))))
+        return n
 
 
-def run_reference(args, w) -> None:
+def _cpu_baseline(w, inputs: dict, budget_s: float = 12.0) -> dict:
+    """The oracle on a bounded sample of workload w (see OracleRun), about budget_s seconds."""
+    o = OracleRun(w, inputs)
+    out = o.run(o.calibrate(budget_s / 2))
+    out.pop("seconds")
+    return out
+
+
+def run_reference(args, todo) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import oracle
-    # each step a bounded token sample sized so that all warm-up and timed steps together take
-    # about two minutes (a run of the sample takes between half and all of its budget)
-    per_step = 120.0 / max(args.steps + args.warmup, 1)
-    cb = _cpu_baseline(w, budget_s=max(0.02, per_step))
-    n_tok = int(cb["sample"].split()[1])
-    sub = w.with_(T=n_tok)
+    w = todo[0] if len(todo) == 1 else wl.WORKLOADS[HEADLINE]
     inputs = wl.generate(w)
-    part = dict(inputs)
-    part["h"] = inputs["h"][:n_tok].contiguous()
+    # every step: routing over all T tokens plus the expert MLPs of a token sample, sized once so
+    # that all warm-up and timed steps together take about two minutes
+    o = OracleRun(w, inputs)
+    n = o.calibrate(max(0.02, 120.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
-        oracle.reference(sub, part)
+        o.run(n)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.reference(sub, part)
+    vals = [o.run(n) for _ in range(args.steps)]
     dt = time.perf_counter() - t0
-    value = n_tok * args.steps / dt
+    value = len(vals) / sum(1.0 / v["value"] for v in vals)   # T tokens per step, harmonic mean
+    cb = dict(vals[-1])
+    cb.pop("seconds")
     cb["value"] = value
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": 1e3 * w.T / value, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, N(0,1/fan_in))",
-            "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "k": w.k,
-                       "act": w.act, "gate": w.gate, "sample_tokens": n_tok},
-            "cpu_baseline": cb,
+            "config": _config(w, args.gpus), "wall_s": dt, "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _config(w, world: int) -> dict:
+    return {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "k": w.k, "act": w.act,
+            "gate": w.gate, "per_rank_tokens": w.T, "parallelism": f"replicas x{world}",
+            "l2": "working set smaller than L2: each step timed alone, L2 flushed in between "
+                  "(256 MB written outside the step's events)" if _l2_resident(w) else
+                  f"inputs larger than L2 ({w.weight_bytes() / 1e9:.3f} GB of expert weights read "
+                  "every step), steps back to back"}
+
+
+def _l2_resident(w) -> bool:
+    """Whether the layer's weights and activations fit in the 126 MB L2 (then steps are timed
+    one at a time with L2 flushed in between)."""
+    es = 4 if w.dtype == "f32" else 2
+    return w.weight_bytes() + w.T * w.d * es * 2 + w.P * (2 * w.d + w.f) * es < 126e6
+
+
+def _ffma_rate(local: int) -> dict:
+    """The FP32 FFMA rate of this GPU, measured by libmoe's probe kernel (CUDA events)."""
+    from sparse_mixture_experts_70_b300 import binding as B
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    out = torch.zeros(1, dtype=torch.float32, device="cuda")
+    blocks, threads, iters = sms * 4, 512, 4096
+    flops = B.moe_fp32_ffma_probe(blocks, threads, iters, out)   # warm-up, and the flop count
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = math.inf
+    for _ in range(5):
+        e0.record()
+        B.moe_fp32_ffma_probe(blocks, threads, iters, out)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    rate = flops / (best * 1e-3) / 1e12
+    return {"tflops": rate, "how": f"FP32 FFMA, measured: moe_fp32_ffma_probe ({blocks} blocks x "
+                                   f"{threads} threads, 8 chains x {iters * 16} FMAs), best of 5"}
+
+
+def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.0) -> dict:
+    """One workload: K timed moe_forward calls (+ live FFN events), the host-buffer pipeline,
+    the CUDA-graph replay; returns its measurement entry (rank 0 reads it)."""
+    cfg = B.config_for(w)
+    inputs = wl.generate(w)
+    dev = {k: (v.cuda().contiguous() if v is not None else None) for k, v in inputs.items()}
+    T, d = w.T, w.d
+    stream = torch.cuda.current_stream()
+    layer = B.Layer(cfg, dev)          # weights resident, workspace and outputs preallocated
+    h = dev["h"]
+
+    for _ in range(args.warmup):
+        layer.forward(h, stream)
+    torch.cuda.synchronize()
+    st = B.moe_device_status(layer.ws)
+    if st != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after warm-up: {B.status_string(st)}")
+
+    # A layer whose working set fits in L2 (the micro shape) is timed step by step with L2
+    # flushed in between (a 256 MB buffer written outside the step's events); the larger layers
+    # stream more than L2 holds every step and run back to back.
+    flush = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if _l2_resident(w)
+             else None)
+
+    def timed(step, n, stream_):
+        """ms per step of n calls of step(i) on stream_ (mean; events on stream_)."""
+        if flush is None:
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream_)
+            for i in range(n):
+                step(i)
+            t1.record(stream_)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / n
+        total = 0.0
+        for i in range(n):
+            flush.zero_()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream_)
+            step(i)
+            t1.record(stream_)
+            torch.cuda.synchronize()
+            total += t0.elapsed_time(t1)
+        return total / n
+
+    # Timed region: K calls of moe_forward (the call a user makes); each also records two events
+    # on its stream around the expert-FFN launches, the dominant kernel's live duration.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        D.barrier()
+        torch.cuda.synchronize()
+        ms = timed(lambda i: layer.forward(h, stream, ffn_events=evs[i]), args.steps, stream)
+        D.barrier()
+    clocks = clk.summary()
+    ffn_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
+    st = B.moe_device_status(layer.ws)
+    if st != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after timed region: {B.status_string(st)}")
+
+    # end to end through the C-ABI pipeline with host buffers (pinned): every step copies its h in
+    # and its y + aux out; the copies of neighbouring steps overlap the layer computation
+    h_host = inputs["h"].pin_memory()
+    y_host = torch.empty((T, d), dtype=w.torch_dtype).pin_memory()
+    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    pipe = B.Pipeline(cfg, layer.w, stream=stream)
+    for _ in range(args.warmup):
+        pipe.submit(h_host, y_host, aux_host)
+    if pipe.device_status() != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after e2e warm-up")
+
+    def e2e_step(i):
+        pipe.submit(h_host, y_host, aux_host)
+        if flush is not None or i == args.steps - 1:
+            pipe.join(stream)
+
+    D.barrier()
+    e_ms = timed(e2e_step, args.steps, stream)
+    if pipe.device_status() != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after e2e region")
+    pipe.close()
+
+    # the same step recorded once in a CUDA graph and replayed (host launch cost removed)
+    graph = layer.capture(dev["h"])
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    D.barrier()
+    g_ms = timed(lambda i: graph.replay(), args.steps, torch.cuda.current_stream())
+    if B.moe_device_status(layer.ws) != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after graph region")
+    del graph, flush
+
+    ms, e_ms, ffn_ms, g_ms = D.max_over_ranks([ms, e_ms, ffn_ms, g_ms], device="cuda")
+    launches_per_step = B.moe_forward_launch_count(cfg)
+    region_s = ms * args.steps * 1e-3
+    traffic = None if args.override else MEASURED_TRAFFIC.get(w.name)
+    entry = {
+        "value": D.job_tokens_per_s(T, world, ms),
+        "unit": "tokens/s",
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "dtype": w.dtype,
+        "config": _config(w, world),
+        "breakdown_ms": {"expert_ffn": ffn_ms, "router_dispatch_combine_aux": ms - ffn_ms},
+        "roofline": roofline(w, ffn_ms, peaks, region_s, clocks.get("reasons"), alu, traffic),
+        "e2e": {"value": D.job_tokens_per_s(T, world, e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
+                "d2h_bytes_per_step": T * d * layer.y.element_size() + 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "graph": {"value": D.job_tokens_per_s(T, world, g_ms), "unit": "tokens/s",
+                  "ms_per_step": g_ms},
+        "clocks": clocks,
+    }
+    del layer, dev
+    torch.cuda.empty_cache()
+    if world == 1 and cpu_budget_s > 0:
+        entry["cpu_baseline"] = _cpu_baseline(w, inputs, budget_s=cpu_budget_s)
+    return entry
 
 
 def main() -> None:
@@ -182,22 +422,24 @@ def main() -> None:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="mixtral", choices=list(wl.WORKLOADS))
+    ap.add_argument("--workload", default="all", choices=["all"] + list(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--override", default="",
                     help="reshape the workload for profiling, e.g. T=2048,E=2,k=1 (not a bench line)")
     args = ap.parse_args()
-    w = wl.WORKLOADS[args.workload]
+    names = ORDER if args.workload == "all" else [args.workload]
+    todo = [wl.WORKLOADS[n] for n in names]
     if args.override:
         kv = dict(item.split("=") for item in args.override.split(","))
-        w = w.with_(name=w.name + "_override",
-                    **{k_: (float(v) if "." in v or "e" in v else int(v)) for k_, v in kv.items()})
+        todo = [w.with_(name=w.name + "_override",
+                        **{k_: (float(v) if "." in v or "e" in v else int(v))
+                           for k_, v in kv.items()}) for w in todo]
     if args.warmup < 3:
         args.warmup = 3
 
     if args.impl == "reference":
-        run_reference(args, w)
+        run_reference(args, todo)
         return
 
     from sparse_mixture_experts_70_b300 import binding as B
@@ -209,159 +451,47 @@ def main() -> None:
         D.init("nccl", torch.device("cuda", local))
 
     peaks = _peaks()
-    cfg = B.config_for(w)
-    inputs = wl.generate(w)
-    dev = {k: (v.cuda().contiguous() if v is not None else None) for k, v in inputs.items()}
-    T, k, E, d = w.T, w.k, w.E, w.d
-    stream = torch.cuda.current_stream()
-    layer = B.Layer(cfg, dev)          # weights resident, workspace and outputs preallocated
-    h = dev["h"]
-
-    for _ in range(args.warmup):
-        layer.forward(h, stream)
-    torch.cuda.synchronize()
-    st = B.moe_device_status(layer.ws)
-    if st != B.MOE_OK:
-        raise SystemExit(f"device status after warm-up: {B.status_string(st)}")
-
-    # Timed region: K calls of moe_forward (the call a user makes); each also records two events
-    # on its stream around the expert-FFN launches, the dominant kernel's live duration.
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
-        D.barrier()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(args.steps):
-            layer.forward(h, stream, ffn_events=evs[i])
-        stop.record(stream)
-        torch.cuda.synchronize()
-        D.barrier()
-    clocks = clk.summary()
-    ms = start.elapsed_time(stop) / args.steps
-    ffn_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
-    st = B.moe_device_status(layer.ws)
-    if st != B.MOE_OK:
-        raise SystemExit(f"device status after timed region: {B.status_string(st)}")
-
-    # end to end through the C-ABI pipeline with host buffers (pinned): every step copies its h in
-    # and its y + aux out; the copies of neighbouring steps overlap the layer computation
-    h_host = inputs["h"].pin_memory()
-    y_host = torch.empty((T, d), dtype=w.torch_dtype).pin_memory()
-    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    pipe = B.Pipeline(cfg, layer.w, stream=stream)
-    for _ in range(args.warmup):
-        pipe.submit(h_host, y_host, aux_host)
-    if pipe.device_status() != B.MOE_OK:
-        raise SystemExit("device status after e2e warm-up")
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_stop = torch.cuda.Event(enable_timing=True)
-    D.barrier()
-    e_start.record(stream)
-    for _ in range(args.steps):
-        pipe.submit(h_host, y_host, aux_host)
-    pipe.join(stream)
-    e_stop.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e_start.elapsed_time(e_stop) / args.steps
-    if pipe.device_status() != B.MOE_OK:
-        raise SystemExit("device status after e2e region")
-    pipe.close()
-
-    # the same step recorded once in a CUDA graph and replayed (host launch cost removed)
-    graph = layer.capture(dev["h"])
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    g_start = torch.cuda.Event(enable_timing=True)
-    g_stop = torch.cuda.Event(enable_timing=True)
-    D.barrier()
-    g_start.record()
-    for _ in range(args.steps):
-        graph.replay()
-    g_stop.record()
-    torch.cuda.synchronize()
-    g_ms = g_start.elapsed_time(g_stop) / args.steps
-    if B.moe_device_status(layer.ws) != B.MOE_OK:
-        raise SystemExit("device status after graph region")
-    del graph
-
-    ms, e_ms, ffn_ms, g_ms = D.max_over_ranks([ms, e_ms, ffn_ms, g_ms], device="cuda")
+    alu = _ffma_rate(local) if any(w.dtype == "f32" for w in todo) else None
+    entries = {}
+    for w in todo:
+        headline = w.name.split("_override")[0] == HEADLINE or len(todo) == 1
+        budget = 0.0 if args.no_cpu_baseline else (12.0 if headline else 3.0)
+        entries[w.name] = bench_workload(w, args, peaks, D, B, local, world, alu, budget)
     if rank != 0:
         D.shutdown()
         return
 
-    # The expert FFN's roofline: tensor-bound when its arithmetic intensity (flops per HBM byte
-    # it must move) is above the ridge point of the measured peaks, else HBM-bound (decode).
-    flops, nbytes = w.expert_flops(), w.ffn_bytes()
-    tflops = flops / (ffn_ms * 1e-3) / 1e12
-    gbs = nbytes / (ffn_ms * 1e-3) / 1e9
-    intensity = flops / nbytes
-    ridge = peaks["bf16_sustained"] * 1e12 / (peaks["hbm"] * 1e9)
-    traffic = MEASURED_TRAFFIC.get(w.name if not args.override else "")
-    if w.dtype == "f32":
-        # f32 experts run as FFMA chains on the CUDA cores: the compute roof is the FP32 ALU rate,
-        # SMs x 128 FP32 lanes x 2 flop x the maximum SM clock (derived, not measured)
-        sms = torch.cuda.get_device_properties(local).multi_processor_count
-        mhz = clocks.get("sm_max_mhz") or 2032.0
-        alu = sms * 128 * 2 * mhz * 1e6 / 1e12
-        if intensity >= alu * 1e12 / (peaks["hbm"] * 1e9):
-            roofline = {"bound": "alu", "kernel": F32_KERNEL, "achieved": tflops, "peak": alu,
-                        "unit": "TFLOP/s", "frac": tflops / alu,
-                        "peak_kind": f"FP32 FFMA, {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz "
-                                     "(derived)", "traffic": traffic,
-                        "flop_per_byte": intensity, "hbm_gbs": gbs}
-        else:
-            roofline = {"bound": "hbm", "kernel": F32_KERNEL, "achieved": gbs,
-                        "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                        "peak_kind": f"HBM copy ({peaks['source']})", "traffic": traffic,
-                        "flop_per_byte": intensity, "alu_tflops": tflops}
-    elif intensity >= ridge:
-        roofline = {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": tflops,
-                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": tflops / peaks["bf16_sustained"],
-                    "peak_kind": f"bf16 sustained ({peaks['source']})",
-                    "frac_of_burst": tflops / peaks["bf16"], "traffic": traffic,
-                    "flop_per_byte": intensity, "hbm_gbs": gbs}
-    else:
-        roofline = {"bound": "hbm", "kernel": GEMM_KERNEL, "achieved": gbs, "peak": peaks["hbm"],
-                    "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                    "peak_kind": f"HBM copy ({peaks['source']})", "traffic": traffic,
-                    "flop_per_byte": intensity, "tensor_tflops": tflops}
-    # the library's own count of the kernels one moe_forward launches for this config
-    launches_per_step = B.moe_forward_launch_count(cfg)
+    head_name = next((n for n in entries if n.split("_override")[0] == HEADLINE),
+                     next(iter(entries)))
+    head = entries[head_name]
     line = {
         "metric": METRIC,
-        "value": D.job_tokens_per_s(T, world, ms),
+        "value": head["value"],
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms,
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
+        "dtype": head["dtype"],
         "data": "synthetic (seeded; h ~ N(0,1), weights ~ N(0, 1/fan_in))",
-        "config": {"workload": w.name, "T": T, "d": d, "f": w.f, "E": E, "k": k,
-                   "act": w.act, "gate": w.gate, "per_rank_tokens": T,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({w.weight_bytes() / 1e9:.2f} GB of expert "
-                         "weights read every step)"},
-        "breakdown_ms": {"expert_ffn": ffn_ms, "router_dispatch_combine_aux": ms - ffn_ms},
-        "roofline": roofline,
-        "e2e": {"value": D.job_tokens_per_s(T, world, e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
-                "d2h_bytes_per_step": T * d * layer.y.element_size() + 4},
-        "gpu_launches": launches_per_step * args.steps,
-        "graph": {"value": D.job_tokens_per_s(T, world, g_ms), "unit": "tokens/s",
-                  "ms_per_step": g_ms},
-        "clocks": clocks,
+        "config": head["config"],
+        "breakdown_ms": head["breakdown_ms"],
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "gpu_launches_all_workloads": sum(e["gpu_launches"] for e in entries.values()),
+        "graph": head["graph"],
+        "clocks": head["clocks"],
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(w)
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if alu is not None:
+        line["fp32_ffma_tflops"] = alu
+    if len(entries) > 1:
+        line["workloads"] = entries
     print(json.dumps(line), flush=True)
     D.shutdown()
 

@@ -158,7 +158,10 @@ moe_status_t moe_build_dispatch(const moe_config_t *cfg, const int32_t *topk_idx
  *           into it (1 = a spin-wait ran out of time, 2 = an index out of range). With NULL they
  *           are not reported.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) and
- * caches it; make that first call before any stream capture. No call allocates or frees memory.
+ * caches it per device and context (a later call looks it up again only if the device's context
+ * changed, e.g. after cudaDeviceReset); the cache is guarded by a mutex, so host threads may make
+ * their first calls concurrently. Make the first call on a device before any stream capture. No
+ * call allocates or frees memory.
  * All calls share the one array: each call clears the parts that must start at zero, and calls
  * whose kernels overlap on the GPU (different streams without ordering) race on it. */
 moe_status_t moe_build_dispatch_static(const moe_config_t *cfg, const int32_t *topk_idx,

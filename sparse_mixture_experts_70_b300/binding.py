@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             "moe_pipeline_join": [_P, _P],
             "moe_pipeline_device_status": [_P],
             "moe_pipeline_destroy": [_P],
+            "moe_fp32_ffma_probe": [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                    ctypes.POINTER(ctypes.c_double)],
             "moe_debug_dispatch_timeout": [_CFG, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                            ctypes.c_uint64, _P],
             "moe_debug_expert_ffn_timeout": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -228,6 +230,14 @@ def moe_forward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out, 
                              _ptr(aux_out), _ptr(zloss_out), _ptr(topk_idx_out),
                              _ptr(counts_out), _ptr(ws), ws.numel() * ws.element_size(),
                              _stream(stream)), "moe_forward")
+
+
+def moe_fp32_ffma_probe(blocks: int, threads: int, iters: int, out, stream=None) -> float:
+    """Launch the FP32 FFMA probe (include/moe_probe.h) on `stream`; returns its flop count."""
+    flops = ctypes.c_double()
+    _check(lib().moe_fp32_ffma_probe(int(blocks), int(threads), int(iters), _ptr(out),
+                                     _stream(stream), ctypes.byref(flops)), "moe_fp32_ffma_probe")
+    return flops.value
 
 
 def moe_debug_dispatch_timeout(cfg, topk_idx, counts, offsets, sorted_token, slot_of, ws,

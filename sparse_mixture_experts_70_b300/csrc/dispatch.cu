@@ -21,6 +21,11 @@
 //      sorted_token and slot_of.
 // The launch is cooperative, so all blocks are co-resident and every wait can be satisfied;
 // each wait is still bounded by %globaltimer and reports DEV_ERR_TIMEOUT instead of hanging.
+#include <cuda.h>
+
+#include <atomic>
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace moe {
@@ -320,17 +325,18 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ 
 }  // namespace
 
 int dispatch_blocks_per_sm() {
-    static int cache[64] = {0};
+    // per-device cache; several host threads may fill it at once (they store the same value)
+    static std::atomic<int> cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int per_sm = 0;
+    int per_sm = cache[dev].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel,
                                                           DISPATCH_THREADS, 0) != cudaSuccess)
             return 0;
-        cache[dev] = per_sm;
+        cache[dev].store(per_sm, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return per_sm;
 }
 
 cudaError_t launch_dispatch(const moe_config_t &c, const int32_t *topk_idx, const DispatchBufs &b,
@@ -389,21 +395,54 @@ constexpr size_t STATIC_SCRATCH_BYTES =
     STATIC_HDR + (size_t)STATIC_LOOKBACK_CELLS * 8 + (size_t)STATIC_LOOKBACK_CELLS * 4;
 static __device__ __align__(256) unsigned char g_dispatch_scratch[STATIC_SCRATCH_BYTES];
 
-// Device address of g_dispatch_scratch on the current device, looked up once per device (host
-// code only sees a stand-in symbol; it must not hand that to a kernel).
+// Device address of g_dispatch_scratch in the current device's context. Host code only sees a
+// stand-in symbol, which must never reach a kernel. The address is looked up once per (device,
+// context) -- the first call on a device, and again after cudaDeviceReset gave the device a new
+// primary context (the module, and with it the array, is then loaded anew) -- under a mutex, so
+// concurrent first calls from several host threads are safe.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+static CtxGetCurrentFn ctx_get_current_fn() {
+    static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(p);
+        return nullptr;
+    }();
+    return fn;
+}
+
 static cudaError_t static_scratch(unsigned char **out) {
-    static unsigned char *cache[64] = {nullptr};
+    struct Entry {
+        CUcontext ctx;
+        unsigned char *ptr;
+    };
+    static Entry cache[64] = {};
+    static std::mutex mu;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!cache[dev]) {
+    const CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
+    if (!ctx) {  // no context on this thread yet: cudaSetDevice binds the primary context
+        err = cudaSetDevice(dev);
+        if (err != cudaSuccess) return err;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorInitializationError;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].ctx != ctx || !cache[dev].ptr) {
         void *p = nullptr;
         err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
         if (err != cudaSuccess) return err;
-        cache[dev] = static_cast<unsigned char *>(p);
+        cache[dev].ctx = ctx;
+        cache[dev].ptr = static_cast<unsigned char *>(p);
     }
-    *out = cache[dev];
+    *out = cache[dev].ptr;
     return cudaSuccess;
 }
 

@@ -36,6 +36,8 @@
 // A dropless top-1 GEMM2 may scatter g * row straight into y[token] (fused combine).
 // Every mbarrier wait is bounded by %globaltimer: on expiry the CTA records DEV_ERR_TIMEOUT,
 // stops issuing, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include <atomic>
+
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -684,11 +686,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // Resident 2-CTA clusters of the pair kernel on this device (0: cannot launch it).
 int pair_clusters() {
-    static int cache[64];
-    static bool done[64];
+    // per-device cache (done: queried); several host threads may fill it at once
+    static std::atomic<int> cache[64] = {};
+    static std::atomic<bool> done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!done[dev]) {
+    if (!done[dev].load(std::memory_order_acquire)) {
         int n = 0;
         if (set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel, TC_SMEM_PAIR) ==
             cudaSuccess) {
@@ -707,10 +710,10 @@ int pair_clusters() {
                 n = 0;
         }
         cudaGetLastError();
-        cache[dev] = n;
-        done[dev] = true;
+        cache[dev].store(n, std::memory_order_relaxed);
+        done[dev].store(true, std::memory_order_release);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 // A_rows / A_src_rows: fused gather of A (see TcArgs); out_token / out_gate: fused scatter.

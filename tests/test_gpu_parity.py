@@ -211,17 +211,31 @@ def _check_case(w):
 def _token_sample(w):
     if w.T <= 256:
         return np.arange(w.T)
-    n = {"mixtral": 24, "many_small": 128, "switch": 256}.get(w.name, 128)
+    n = {"mixtral": 256, "many_small": 256, "switch": 512}.get(w.name, 128)
     edge = max(n // 4, 4)
     mid = np.linspace(edge, w.T - edge - 1, n - 2 * edge).astype(np.int64)
     return np.unique(np.concatenate([np.arange(edge), mid, np.arange(w.T - edge, w.T)]))
 
 
+def _tile_rows(offsets: np.ndarray, bm: int = 128) -> np.ndarray:
+    """Rows of y_perm that touch every 128-row M tile of every expert: its first and last valid
+    row and one row in each 32-row quarter (the four TMEM lane quarters of a tile's
+    accumulator), so every tile's masked store and every epilogue warp's rows are compared."""
+    rows = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for r0 in range(lo, hi, bm):
+            last = min(r0 + bm, hi) - 1
+            rows += [r0, last] + [r0 + 32 * q + 17 for q in range(4) if r0 + 32 * q + 17 <= last]
+    return np.unique(np.array(rows, dtype=np.int64))
+
+
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
 def test_full_size_workloads(name):
     """The five workloads at full size, through moe_forward (the call the benchmark times) and
-    through the five step calls: routing, counts and permutation over all tokens, the layer
-    output on a deterministic token sample (every token for micro and decode)."""
+    through the five step calls: routing, counts and permutation over all tokens; the expert MLP
+    output on rows of every M tile of every expert; the layer output on a deterministic token
+    sample (every token for micro and decode)."""
     w = wl.WORKLOADS[name]
     inputs = _inputs(w)
     tokens = _token_sample(w)
@@ -229,21 +243,28 @@ def test_full_size_workloads(name):
     dev = to_dev(inputs)
     fw = run_forward(w, dev)
     assert fw["status"] == B.MOE_OK
-    diff = routing_agreement(ref, fw["idx"].numpy())
+    idx_fw = fw["idx"].numpy()
+    diff = routing_agreement(ref, idx_fw)
+    # the fused call's counts are those of its own routing, whether or not there are near ties
+    np.testing.assert_array_equal(fw["counts"].numpy(), np.bincount(idx_fw.ravel(), minlength=w.E))
     if len(diff) == 0:
         np.testing.assert_array_equal(fw["counts"].numpy(), ref["counts"])
     assert fw["aux"].item() == pytest.approx(ref["aux"], rel=AUX_REL)
     assert fw["zloss"].item() == pytest.approx(ref["zloss"], rel=AUX_REL)
     stats = check_layer_output(w, ref, fw["y"], skip_tokens=diff)
-    print(f"{name}: near-tie tokens {len(diff)}, {stats}")
     got = run_steps(w, inputs, dev)
     _check_steps(w, inputs, ref, got)
+    assert torch.equal(got["idx"], fw["idx"]) and torch.equal(got["counts"], fw["counts"])
+    rows = _tile_rows(got["offsets"].numpy())
+    _check_expert_rows(w, inputs, got, rows)
     if _fused_scatter(w):
         check_layer_output(w, ref, got["y"], skip_tokens=diff)
     else:
         assert torch.equal(got["y"], fw["y"])
     if name == "decode":
         assert (got["counts"] > 0).all()
+    print(f"{name}: near-tie tokens {len(diff)}, layer output {stats} on {len(tokens)} tokens, "
+          f"expert rows checked {len(rows)} of {int(got['offsets'][-1])}")
 
 
 LARGE = [

@@ -12,7 +12,7 @@ from sparse_mixture_experts_70_b300 import binding as B
 from sparse_mixture_experts_70_b300 import workloads as wl
 
 
-def _dispatch_both(w):
+def _dispatch_both(w, with_status=True):
     cfg = B.config_for(w)
     inp = wl.generate_router_inputs(w)
     h = inp["h"].cuda()
@@ -32,10 +32,10 @@ def _dispatch_both(w):
         so = torch.full((P,), -3, dtype=torch.int32, device="cuda")
         xp = torch.zeros((P, d), dtype=w.torch_dtype, device="cuda")
         if use_static:
-            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            status = torch.zeros(1, dtype=torch.int32, device="cuda") if with_status else None
             B.moe_build_dispatch_static(cfg, idx, h, counts, offsets, st, so, xp, status)
             torch.cuda.synchronize()
-            assert status.item() == 0
+            assert status is None or status.item() == 0
         else:
             ws = B.workspace(cfg)
             B.moe_build_dispatch(cfg, idx, h, counts, offsets, st, so, xp, ws)
@@ -55,6 +55,19 @@ def test_static_scratch_dispatch_equals_workspace_dispatch_on_consecutive_calls(
         counts = ref[0].numpy()
         assert counts.sum() == w.P
         np.testing.assert_array_equal(counts, np.bincount(idx.numpy().ravel(), minlength=w.E))
+
+
+@pytest.mark.gpu
+def test_static_scratch_dispatch_without_a_status_word():
+    """status = NULL: device-side failures are then not reported (they land in the array's
+    header); the results are the same. Single-chunk (one block, no look-back) and multi-chunk
+    shapes, one after the other."""
+    for w in (wl.small("static_nostatus_a", T=300, d=64, f=64, E=12, k=3, seed=41),
+              wl.small("static_nostatus_b", T=6000, d=64, f=64, E=24, k=2,
+                       router_bias_var=1.0, seed=42)):
+        idx, (ref, got) = _dispatch_both(w, with_status=False)
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
 
 
 @pytest.mark.gpu
