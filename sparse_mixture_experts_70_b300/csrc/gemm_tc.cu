@@ -51,7 +51,15 @@ constexpr int B_STAGE = BN * BK * 2;  // 32 KiB
 constexpr int TC_THREADS = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CTL_BYTES = 4096;
-constexpr size_t TC_SMEM = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + CTL_BYTES;
+// Output staging of the TMA-store epilogue: one 32-row x 32-column bf16 box (2 KiB) per epilogue
+// warp, after the control block.
+#ifndef MOE_GEMM_TMA_STORE
+#define MOE_GEMM_TMA_STORE 1
+#endif
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_BOX = 32 * 64;
+constexpr size_t TC_SMEM =
+    1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + CTL_BYTES + (size_t)EPI_WARPS * EPI_BOX;
 
 enum { EPI_STORE = 0, EPI_GELU = 1, EPI_SWIGLU = 2 };
 
@@ -64,6 +72,8 @@ struct TcArgs {
     int E, K, N, n_tiles, epi;
     unsigned long long spin_limit_ns;  // bound of every mbarrier wait
     int withhold_loads;                // test hook: the producer issues no loads
+    int tma_out;  // 1: 32-row groups that lie wholly inside a tile's valid rows leave through
+                  // shared-memory staging and TMA stores (the other rows: per-thread stores)
     // fused gather (GEMM1): A row r is row a_rows[r] of a [a_src_rows, K] tensor, read with
     // 4-row TMA gathers, instead of row r of a permuted copy
     const int32_t *a_rows;
@@ -114,13 +124,45 @@ __device__ __forceinline__ Tile decode_tile(int t, int &eh, const int32_t *s_cum
     return ti;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// One 32 x 32 output box through this warp's staging buffer `stg`: wait until the previous TMA
+// store has read the buffer, write this lane's row (32 bf16 in pk) with the 64-byte swizzle,
+// make the writes visible to the async proxy, and let lane 0 issue the store at (col, row0).
+__device__ __forceinline__ void stage_and_store(const CUtensorMap *tmO, uint32_t stg,
+                                                const uint32_t (&pk)[16], int col, int row0,
+                                                int lane) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+    const uint32_t rowaddr = stg + (uint32_t)lane * 64u;
+    const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(rowaddr + (((uint32_t)j ^ sw) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                     pk[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmO, stg, col, row0);
+        bulk_commit();
+    }
+}
+
 // Convert this thread's accumulator row (TMEM lane q*32+lane of accumulator `acc_col`) of tile
 // ti into bf16 outputs: half the tile's columns per thread (`half`), bias / GELU / SwiGLU in f32.
-// Every tcgen05.ld here is executed by the whole warp; only the stores depend on the row.
+// Every tcgen05.ld here is executed by the whole warp; only the stores depend on the row. A warp
+// whose 32 rows are all valid stores through its staging buffer `stg` with TMA (when a.tma_out).
 __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, uint32_t tmem_base,
-                                              uint32_t acc_col, int q, int lane, int half) {
+                                              uint32_t acc_col, int q, int lane, int half,
+                                              const CUtensorMap *tmO, uint32_t stg) {
     const int r = q * 32 + lane;
     const bool valid = r < ti.rows;
+    const bool boxed = a.tma_out && q * 32 + 32 <= ti.rows;  // warp-uniform
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
     __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
     float gscale = 1.f;
@@ -135,7 +177,14 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
             float x1[32], x3[32];
             tmem_ld32x2(trow + c, trow + BN / 2 + c, x1, x3);
             const int col = ti.n * (BN / 2) + c;
-            if (valid && col < a.N) {
+            if (boxed && col < a.N) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16(silu_fast(x1[2 * i]) * x3[2 * i],
+                                      silu_fast(x1[2 * i + 1]) * x3[2 * i + 1]);
+                stage_and_store(tmO, stg, pk, col, ti.row0 + q * 32, lane);
+            } else if (valid && col < a.N) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -167,7 +216,12 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= gscale;
             }
-            if (valid) {
+            if (boxed) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                stage_and_store(tmO, stg, pk, col, ti.row0 + q * 32, lane);
+            } else if (valid) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -184,7 +238,8 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
-                           const __grid_constant__ CUtensorMap tmB3, const TcArgs a) {
+                           const __grid_constant__ CUtensorMap tmB3,
+                           const __grid_constant__ CUtensorMap tmO, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -391,6 +446,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else {
         const int q = warp & 3;           // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;  // which half of the tile's columns it converts
+        const uint32_t stg = smem_u32(ctl + CTL_BYTES) + (uint32_t)(warp - 2) * EPI_BOX;
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < total; t += ustep) {
@@ -401,12 +457,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half);
+            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half, &tmO, stg);
             tc_fence_before();
             mbar_arrive(bar_tempty + 8 * acc);
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
+        if (lane == 0) bulk_wait_all();  // this warp's TMA stores have completed
+        __syncwarp();
     }
 
     pdl_trigger();
@@ -443,12 +501,14 @@ constexpr int STAGES2 = 6;
 #endif
 constexpr int A_HALF = BM * BK * 2;          // 16 KiB: this CTA's A rows
 constexpr int B_HALF = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the B tile
-constexpr size_t TC_SMEM_PAIR = 1024 + (size_t)STAGES2 * (A_HALF + B_HALF) + CTL_BYTES;
+constexpr size_t TC_SMEM_PAIR =
+    1024 + (size_t)STAGES2 * (A_HALF + B_HALF) + CTL_BYTES + (size_t)EPI_WARPS * EPI_BOX;
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmB3, const TcArgs a) {
+                             const __grid_constant__ CUtensorMap tmB3,
+                             const __grid_constant__ CUtensorMap tmO, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -652,6 +712,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else {
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
+        const uint32_t stg = smem_u32(ctl + CTL_BYTES) + (uint32_t)(warp - 2) * EPI_BOX;
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < total; t += ustep) {
@@ -662,13 +723,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half);
+            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half, &tmO, stg);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
+        if (lane == 0) bulk_wait_all();  // this warp's TMA stores have completed
+        __syncwarp();
     }
 
     pdl_trigger();
@@ -723,9 +786,12 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
                         const int32_t *A_rows = nullptr, int64_t A_src_rows = 0,
                         const int32_t *out_token = nullptr, const float *out_gate = nullptr) {
     // every B box is 128 rows: one half of the 256-row B tile; a gathered A reads one-row boxes
-    CUtensorMap mA, mB, mB3;
+    CUtensorMap mA, mB, mB3, mO;
     if (A_rows ? !make_map(&mA, A, A_src_rows, K, 1) : !make_map(&mA, A, P, K, BM))
         return cudaErrorInvalidValue;
+    // the output of the TMA-store epilogue: [P, N] rows in sorted order (the scattering top-1
+    // GEMM2 writes token rows with per-thread stores instead and never reads this map)
+    if (!make_store_map(&mO, out, out_token ? 1 : P, N)) return cudaErrorInvalidValue;
     if (!make_map(&mB, B, (int64_t)E * N, K, BN / 2)) return cudaErrorInvalidValue;
     if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, BN / 2))
         return cudaErrorInvalidValue;
@@ -743,6 +809,7 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.epi = epi;
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold_loads = hook.withhold;
+    a.tma_out = (MOE_GEMM_TMA_STORE && out_token == nullptr) ? 1 : 0;
     a.a_rows = A_rows;
     a.a_src_rows = A_src_rows;
     a.out_token = out_token;
@@ -755,7 +822,7 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
         const int64_t units = ((P + 2 * BM - 1) / (2 * BM) + E) * (int64_t)a.n_tiles;
         const int64_t ncl = clusters < units ? clusters : units;
         return launch_pdl(grouped_gemm_pair_kernel, dim3((unsigned)(2 * ncl)), dim3(TC_THREADS),
-                          TC_SMEM_PAIR, s, 2, mA, mB, mB3, a);
+                          TC_SMEM_PAIR, s, 2, mA, mB, mB3, mO, a);
     }
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
@@ -763,7 +830,7 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel, TC_SMEM);
     if (err != cudaSuccess) return err;
     return launch_pdl(grouped_gemm_tc_kernel, dim3((unsigned)grid), dim3(TC_THREADS), TC_SMEM, s,
-                      1, mA, mB, mB3, a);
+                      1, mA, mB, mB3, mO, a);
 }
 
 }  // namespace
