@@ -25,7 +25,8 @@ Only the exchange lives here; every compute step goes through a backend object:
   combine(y_perm [T k, d], slot_of, gates) -> y [T, d]
 LibmoeBackend runs them on the GPU through the C ABI (the regroup of step 3 with
 moe_build_dispatch and moe_combine). The split sizes of an all_to_all must be known on the host,
-so each forward copies the E counts to the host once.
+so each forward copies the E counts to the host once. With NCCL the rows move between devices
+directly; with gloo (a host transport) they are staged through host copies.
 """
 from __future__ import annotations
 
@@ -73,12 +74,18 @@ def exchange_counts(counts: torch.Tensor, world: int) -> torch.Tensor:
 
 def _all_to_all_rows(x: torch.Tensor, out: torch.Tensor, send: list[int],
                      recv: list[int]) -> torch.Tensor:
-    """Rows of x go to the ranks in `send` split order; `out` receives `recv` rows per rank."""
-    if D.active():
+    """Rows of x go to the ranks in `send` split order; `out` receives `recv` rows per rank.
+    NCCL moves device rows directly; gloo (host transport) moves host copies of them."""
+    if not D.active():
+        out.copy_(x)
+    elif x.is_cuda and dist.get_backend() != "nccl":
+        staged = torch.empty(out.shape, dtype=out.dtype)
+        dist.all_to_all_single(staged, x.contiguous().cpu(), output_split_sizes=recv,
+                               input_split_sizes=send)
+        out.copy_(staged)
+    else:
         dist.all_to_all_single(out, x.contiguous(), output_split_sizes=recv,
                                input_split_sizes=send)
-    else:
-        out.copy_(x)
     return out
 
 
