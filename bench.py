@@ -262,8 +262,9 @@ def run_reference(args, todo) -> None:
 def _config(w, world: int) -> dict:
     return {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "k": w.k, "act": w.act,
             "gate": w.gate, "per_rank_tokens": w.T, "parallelism": f"replicas x{world}",
-            "l2": "working set smaller than L2: each step timed alone, L2 flushed in between "
-                  "(256 MB written outside the step's events)" if _l2_resident(w) else
+            "l2": "working set smaller than L2: each step bracketed by its own events, L2 "
+                  "flushed between steps (256 MB written outside the events)" if _l2_resident(w)
+                  else
                   f"inputs larger than L2 ({w.weight_bytes() / 1e9:.3f} GB of expert weights read "
                   "every step), steps back to back"}
 
@@ -314,36 +315,45 @@ def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.
         raise SystemExit(f"{w.name}: device status after warm-up: {B.status_string(st)}")
 
     # A layer whose working set fits in L2 (the micro shape) is timed step by step with L2
-    # flushed in between (a 256 MB buffer written outside the step's events); the larger layers
-    # stream more than L2 holds every step and run back to back.
+    # flushed in between (a 256 MB buffer written between the step's events, queued on the same
+    # stream); the larger layers stream more than L2 holds every step and run back to back.
     flush = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if _l2_resident(w)
              else None)
 
+    def new_events(n):
+        """n pairs of timing events, created (first record) outside any timed region."""
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n)]
+        for e0, e1 in pairs:
+            e0.record(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return pairs
+
     def timed(step, n, stream_):
-        """ms per step of n calls of step(i) on stream_ (mean; events on stream_)."""
+        """ms per step of n calls of step(i) on stream_ (mean; events on stream_). With L2
+        flushes, every step is bracketed by its own events and the flush kernel runs between
+        steps, outside them; the host queues all n steps before waiting once."""
         if flush is None:
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            (t0, t1), = new_events(1)
             t0.record(stream_)
             for i in range(n):
                 step(i)
             t1.record(stream_)
             torch.cuda.synchronize()
             return t0.elapsed_time(t1) / n
-        total = 0.0
+        pairs = new_events(n)
         for i in range(n):
             flush.zero_()
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(stream_)
+            pairs[i][0].record(stream_)
             step(i)
-            t1.record(stream_)
-            torch.cuda.synchronize()
-            total += t0.elapsed_time(t1)
-        return total / n
+            pairs[i][1].record(stream_)
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in pairs) / n
 
     # Timed region: K calls of moe_forward (the call a user makes); each also records two events
     # on its stream around the expert-FFN launches, the dominant kernel's live duration.
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    evs = new_events(args.steps)
     with Clocks(local) as clk:
         D.barrier()
         torch.cuda.synchronize()

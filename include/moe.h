@@ -92,7 +92,9 @@ typedef struct {
  * Returns MOE_ERR_INVALID_ARG for an invalid cfg. */
 moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
-/* Zero the workspace header (status word and dispatch flags) on `stream`. */
+/* Zero the workspace header -- its first 2048 bytes: the device status word and the counters of
+ * the combine that moe_forward fuses into the expert launch of small f32 layers -- on `stream`.
+ * MOE_ERR_INVALID_ARG if ws is not 16-byte aligned or ws_bytes < 2048. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Rows of the router's per-block partial sums psum_part [rows, E + 1]. */
@@ -213,7 +215,11 @@ moe_status_t moe_update_sel_bias(const moe_config_t *cfg, const int32_t *counts,
  * counts_out [E] are optional copies of the routing (NULL to skip). Everything else lives in ws.
  * Same results as the step calls in sequence, bit for bit, except for a dropless (capacity_factor
  * 0) top-1 bf16 layer: there the second expert GEMM writes y[t] = g * expert(h[t]) itself, with
- * one bf16 rounding instead of two (no y_perm, no combine kernel). */
+ * one bf16 rounding instead of two (no y_perm, no combine kernel). Fewer kernels than the step
+ * calls where the shape allows: a layer whose T k slots fit one dispatch chunk (<= 1024) reduces
+ * the auxiliary value in the dispatch's kernel; f32 layers read their expert rows of h directly
+ * (no permuted copy), and small f32 layers (T k d <= 262144, d <= 8192) form y in the second
+ * expert launch (no combine kernel). moe_forward_launch_count tells how many kernels run. */
 moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_r,
                          const float *b_r, const float *sel_bias, const void *W1,
                          const float *b1, const void *W3, const void *W2, const float *b2,

@@ -31,7 +31,7 @@ def _nvcc() -> str:
 def _deps_mtime() -> float:
     files = [os.path.join(INCLUDE, "moe.h"), os.path.join(INCLUDE, "moe_pipeline.h"),
              os.path.join(INCLUDE, "moe_probe.h"),
-             os.path.join(CSRC, "internal.cuh"),
+             os.path.join(CSRC, "internal.cuh"), os.path.join(CSRC, "layer_dev.cuh"),
              os.path.join(CSRC, "tc_ptx.cuh")]
     return max(os.path.getmtime(f) for f in files)
 

@@ -5,9 +5,12 @@
 // N . sum_i f_i P_i, with f_i the fraction of routing slots sent to expert i and P_i its mean
 // router probability, equal to 1 under uniform routing.
 #include "internal.cuh"
+#include "layer_dev.cuh"
 
 namespace moe {
 namespace {
+
+using namespace dev;
 
 template <typename T> struct Vec8;
 template <> struct Vec8<__nv_bfloat16> {
@@ -104,25 +107,6 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(const void *__restr
     pdl_trigger();
 }
 
-// Sum over the 32 lanes of a warp by an xor butterfly: a fixed order, the same result in every
-// lane.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// aux = E * sum_e (counts[e] / (T k)) * (sum_b psum_part[b, e] / T) and the router z-loss
-// (sum_b psum_part[b, E]) / T, reduced in a fixed order:
-//   1. thread (g, c) sums rows g, g + G, g + 2G, ... of column c (G = 1024 / (E + 1) groups)
-//      into AUX_ILP running sums (row g + iG goes to sum i mod AUX_ILP, that many loads in
-//      flight), added pairwise at the end;
-//   2. warp w takes columns w, w + 32, ...: lane l adds group sums l, l + 32, ..., then the warp
-//      adds its lanes by a butterfly;
-//   3. warp 0 forms the E terms f_e P_e (lane l: experts l, l + 32, ...) and adds them likewise.
-// Every step is a tree or a short chain, so the kernel is a few memory latencies long.
-constexpr int AUX_ILP = 16;  // a power of two
-
 __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ counts,
                                                    const float *__restrict__ psum, int64_t rows,
                                                    int E, int64_t T, int k, float *aux_out,
@@ -131,47 +115,7 @@ __global__ void __launch_bounds__(1024) aux_kernel(const int32_t *__restrict__ c
     __shared__ float colsum[257];
     __shared__ int32_t s_counts[256];
     pdl_wait();
-    const int C = E + 1;
-    const int G = 1024 / C;
-    const int g = threadIdx.x / C, col = threadIdx.x % C;
-    if ((int)threadIdx.x < E) s_counts[threadIdx.x] = counts[threadIdx.x];
-    if (g < G) {
-        float r[AUX_ILP];
-#pragma unroll
-        for (int u = 0; u < AUX_ILP; ++u) r[u] = 0.f;
-        int64_t b = g;
-        for (; b + (AUX_ILP - 1) * (int64_t)G < rows; b += AUX_ILP * (int64_t)G) {
-#pragma unroll
-            for (int u = 0; u < AUX_ILP; ++u) r[u] += __ldg(psum + (b + u * (int64_t)G) * C + col);
-        }
-#pragma unroll
-        for (int u = 0; u < AUX_ILP - 1; ++u)
-            if (b + u * (int64_t)G < rows) r[u] += __ldg(psum + (b + u * (int64_t)G) * C + col);
-#pragma unroll
-        for (int w = AUX_ILP / 2; w > 0; w >>= 1)  // pairwise: r[u] += r[u + w]
-#pragma unroll
-            for (int u = 0; u < w; ++u) r[u] += r[u + w];
-        part[g * C + col] = r[0];
-    }
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int c = warp; c < C; c += 32) {
-        float v = 0.f;
-        for (int q = lane; q < G; q += 32) v += part[q * C + c];
-        v = warp_sum(v);
-        if (lane == 0) colsum[c] = v;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const float fT = (float)T, fTk = (float)T * (float)k;
-        float v = 0.f;
-        for (int e = lane; e < E; e += 32) v += ((float)s_counts[e] / fTk) * (colsum[e] / fT);
-        v = warp_sum(v);
-        if (lane == 0) {
-            *aux_out = T > 0 ? (float)E * v : 0.f;
-            if (zloss_out) *zloss_out = T > 0 ? colsum[E] / fT : 0.f;
-        }
-    }
+    aux_block(counts, psum, rows, E, T, k, aux_out, zloss_out, part, colsum, s_counts);
     pdl_trigger();
 }
 

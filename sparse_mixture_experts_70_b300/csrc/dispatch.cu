@@ -27,137 +27,36 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "layer_dev.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int LB_WINDOW = 8;  // look-back words read per round trip
-constexpr uint64_t FLAG_AGG = 1ull << 32;
-constexpr uint64_t FLAG_INC = 2ull << 32;
+using namespace dev;
 
-struct DispatchArgs {
-    const int32_t *idx;
-    int32_t *counts, *offsets, *sorted_token, *slot_of, *excl;
-    unsigned long long *words;  // [nchunks][E] look-back words
-    uint32_t *done;
-    uint32_t *dev_status;
-    int64_t P;
-    int k, E, nchunks;
-    int64_t cap;  // per-expert capacity, -1 when dropless
-    unsigned long long spin_limit_ns;
-    int withhold;  // test hook: chunk 0 never publishes its look-back word
-};
-
-__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-// A look-back word carries its flag and its count in one 64-bit store, so a reader needs only
-// that word: relaxed loads (at gpu scope, from L2) may be issued several at a time.
-__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Chunk histogram: returns this thread's expert (-1 for no slot) and its rank inside the chunk;
-// thread e < E receives the chunk's count of expert e in *agg.
-__device__ __forceinline__ int chunk_ranks(const DispatchArgs &a, int c, int32_t *cnt, int *lrank,
-                                           int *agg) {
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = a.E;
-    const int64_t s = (int64_t)c * DISPATCH_THREADS + tid;
-    int e = -1;
-    if (s < a.P) {
-        e = a.idx[s];
-        if (e < 0 || e >= E) {
-            report(a.dev_status, DEV_ERR_INDEX);
-            e = -1;
-        }
-    }
-    for (int q = tid; q < 32 * E; q += DISPATCH_THREADS) cnt[q] = 0;
-    __syncthreads();
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank == 0) cnt[w * E + e] = __popc(peers);
-    __syncthreads();
-    int run = 0;
-    if (tid < E) {
-        for (int ww = 0; ww < 32; ++ww) {
-            const int v = cnt[ww * E + tid];
-            cnt[ww * E + tid] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    *lrank = e >= 0 ? cnt[w * E + e] + rank : 0;
-    *agg = run;
-    __syncthreads();
-    return e;
-}
-
-// counts[e] = tot[e], offsets = exclusive scan over e of the kept rows min(tot[e], cap), and
-// s_off[e] = offsets[e], for e < E <= 256, by the block's first 8 warps (warp scans, then a scan
-// of the 8 warp totals); the whole block calls it. offsets[E] is the number of kept rows.
-__device__ __forceinline__ void publish_offsets(const DispatchArgs &a, const int32_t *tot,
-                                                int32_t *s_off, int32_t *s_wsum) {
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = a.E;
-    int kept = 0, incl = 0;
-    if (tid < 256) {
-        if (tid < E) {
-            const int c = tot[tid];
-            kept = (a.cap >= 0 && c > a.cap) ? (int)a.cap : c;
-        }
-        incl = kept;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) s_wsum[w] = incl;
-    }
-    __syncthreads();
-    if (tid < 256) {
-        int base = 0;
-        for (int q = 0; q < w; ++q) base += s_wsum[q];
-        const int excl = base + incl - kept;
-        if (tid < E) {
-            a.counts[tid] = tot[tid];
-            a.offsets[tid] = excl;
-            s_off[tid] = excl;
-        }
-        if (tid == E - 1) a.offsets[E] = excl + kept;
-    }
-    __syncthreads();
-}
-
-// All slots fit in one chunk: histogram, scan over experts and scatter in one block, with no
-// look-back, flags or workspace.
 __global__ void __launch_bounds__(DISPATCH_THREADS, 1) dispatch_single_kernel(DispatchArgs a) {
     __shared__ int32_t cnt[32 * 256];
     __shared__ int32_t s_tot[256], s_off[257], s_wsum[8];
     pdl_wait();
-    const int tid = threadIdx.x, E = a.E;
-    int lrank, agg;
-    const int e = chunk_ranks(a, 0, cnt, &lrank, &agg);
-    if (tid < E) s_tot[tid] = agg;
-    __syncthreads();
-    publish_offsets(a, s_tot, s_off, s_wsum);
-    if (e >= 0) {
-        if (a.cap >= 0 && lrank >= a.cap) {
-            a.slot_of[tid] = -1;  // over capacity: dropped
-        } else {
-            const int pos = s_off[e] + lrank;
-            a.sorted_token[pos] = tid / a.k;
-            a.slot_of[tid] = pos;
-        }
-    }
+    dispatch_single_block(a, cnt, s_tot, s_off, s_wsum);
+    pdl_trigger();
+}
+
+// A single-chunk layer's dispatch and its auxiliary value and z-loss in one block: the counts the
+// dispatch publishes and the router's partial sums are reduced right after, in the same fixed
+// order as aux_kernel (both call aux_block).
+__global__ void __launch_bounds__(DISPATCH_THREADS, 1)
+    dispatch_aux_kernel(DispatchArgs a, const float *psum, int64_t rows, int64_t T,
+                        float *aux_out, float *zloss_out) {
+    __shared__ int32_t cnt[32 * 256];
+    __shared__ int32_t s_tot[256], s_off[257], s_wsum[8];
+    __shared__ float part[1024];
+    __shared__ float colsum[257];
+    __shared__ int32_t s_counts[256];
+    pdl_wait();
+    dispatch_single_block(a, cnt, s_tot, s_off, s_wsum);
+    __syncthreads();  // the counts written by the dispatch are visible to the whole block
+    aux_block(a.counts, psum, rows, a.E, T, a.k, aux_out, zloss_out, part, colsum, s_counts);
     pdl_trigger();
 }
 
@@ -464,6 +363,27 @@ cudaError_t launch_dispatch_static(const moe_config_t &c, const int32_t *topk_id
     // Without a caller status word, device-side failures land in the (cleared) header.
     b.dev_status = status ? status : reinterpret_cast<uint32_t *>(scratch + 64);
     return launch_dispatch(c, topk_idx, b, s);
+}
+
+cudaError_t launch_dispatch_aux(const moe_config_t &c, const int32_t *topk_idx,
+                                const DispatchBufs &b, const float *psum_part, float *aux_out,
+                                float *zloss_out, cudaStream_t s) {
+    if (c.T == 0 || dispatch_chunks(c) != 1) return cudaErrorInvalidValue;
+    DispatchArgs a = {};
+    a.idx = topk_idx;
+    a.counts = b.counts;
+    a.offsets = b.offsets;
+    a.sorted_token = b.sorted_token;
+    a.slot_of = b.slot_of;
+    a.dev_status = b.dev_status;
+    a.P = c.T * c.k;
+    a.k = c.k;
+    a.E = c.E;
+    a.nchunks = 1;
+    a.cap = capacity_of(c);
+    a.spin_limit_ns = SPIN_LIMIT_NS;
+    return launch_pdl(dispatch_aux_kernel, dim3(1), dim3(DISPATCH_THREADS), 0, s, 1, a, psum_part,
+                      router_partial_rows(c), c.T, aux_out, zloss_out);
 }
 
 cudaError_t launch_permute(const moe_config_t &c, const void *h, const int32_t *slot_of,

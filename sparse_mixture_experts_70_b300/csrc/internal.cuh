@@ -52,8 +52,14 @@ struct FaultHook {
 constexpr int DISPATCH_THREADS = 1024;  // slots per dispatch chunk
 constexpr int GEMM_BM = 128;            // rows per tensor-core tile
 
+// The workspace header: the status word at offset 0 and, from WS_ARRIVE_OFFSET, the arrival
+// counters of the fused f32 combine (one per output column tile). moe_workspace_init zeroes it.
+constexpr size_t WS_HEADER_BYTES = 2048;
+constexpr size_t WS_ARRIVE_OFFSET = 1024;
+constexpr int F32_COMBINE_TILES = (int)((WS_HEADER_BYTES - WS_ARRIVE_OFFSET) / 4);
+
 struct WsLayout {
-    size_t status;        // u32 device status word
+    size_t status;        // header: u32 device status word, combine arrival counters
     size_t disp_flags;    // u32 done flag + pad, then nchunks*E u64 look-back words
     size_t disp_flags_bytes;
     size_t disp_excl;     // nchunks*E int32 (per-chunk exclusive counts)
@@ -160,6 +166,11 @@ cudaError_t launch_combine(const moe_config_t &c, const void *y_perm, const int3
 // aux_out: E sum f P; zloss_out (may be nullptr): the router z-loss.
 cudaError_t launch_aux(const moe_config_t &c, const int32_t *counts, const float *psum_part,
                        float *aux_out, float *zloss_out, cudaStream_t s);
+// Dispatch and auxiliary value of a layer whose slots fit one dispatch chunk (T k <= 1024), in
+// one single-block kernel: the results of launch_dispatch followed by launch_aux.
+cudaError_t launch_dispatch_aux(const moe_config_t &c, const int32_t *topk_idx,
+                                const DispatchBufs &b, const float *psum_part, float *aux_out,
+                                float *zloss_out, cudaStream_t s);
 cudaError_t launch_update_sel_bias(const moe_config_t &c, const int32_t *counts, float *sel_bias,
                                    float gamma, cudaStream_t s);
 
@@ -176,7 +187,17 @@ struct FfnBufs {
     const int32_t *sorted_token = nullptr;
     void *scatter_y = nullptr;               // top-1: GEMM2 writes y[token] = g * expert(h)
     const float *gates = nullptr;
+    // f32, ffn_f32_combine_ok: the second launch also forms y = sum_j g_j y_perm[slot_of] in the
+    // last block of every column tile (arrive: zeroed counters in the workspace header, one per
+    // column tile, left zero again)
+    void *combine_y = nullptr;
+    const int32_t *slot_of = nullptr;
+    uint32_t *arrive = nullptr;
 };
+// The f32 combine fused into the second expert launch: at most this many slot elements (T k d),
+// which the last block of each column tile reads and combines.
+constexpr int64_t F32_COMBINE_MAX = 256 * 1024;
+bool ffn_f32_combine_ok(const moe_config_t &c);
 cudaError_t launch_ffn_f32(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,
                           const FaultHook &hook = FaultHook());

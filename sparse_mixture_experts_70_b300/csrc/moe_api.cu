@@ -64,7 +64,7 @@ WsLayout ws_layout(const moe_config_t &c) {
     const size_t E = (size_t)c.E;
     const size_t nch = (size_t)dispatch_chunks(c);
     size_t off = 0;
-    L.status = off;                       off = align_up(off + 256);
+    L.status = off;                       off = align_up(off + WS_HEADER_BYTES);
     L.disp_flags = off;
     L.disp_flags_bytes = 256 + nch * E * 8;
     off = align_up(off + L.disp_flags_bytes);
@@ -127,8 +127,9 @@ moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes) {
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
-    if (!aligned16(ws) || ws_bytes < 1024) return MOE_ERR_INVALID_ARG;
-    return from_cuda(cudaMemsetAsync(ws, 0, 1024, static_cast<cudaStream_t>(stream)));
+    if (!aligned16(ws) || ws_bytes < WS_HEADER_BYTES) return MOE_ERR_INVALID_ARG;
+    return from_cuda(
+        cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_router_partials(const moe_config_t *cfg, int64_t *rows) {
@@ -256,16 +257,21 @@ moe_status_t moe_update_sel_bias(const moe_config_t *cfg, const int32_t *counts,
                                             static_cast<cudaStream_t>(stream)));
 }
 
-// The fused variants moe_forward takes on the tensor-core path: with fuse_gather GEMM1 gathers
-// its rows of h itself (no permuted copy); a dropless top-1 layer's GEMM2 scatters g * output
-// straight into y (no combine).
+// The fused variants moe_forward takes. The first expert launch gathers its rows of h itself (no
+// permuted copy): always for f32 (a 16-byte cp.async per piece, from any row), with fuse_gather
+// on the tensor-core path. A dropless top-1 bf16 layer's second GEMM scatters g * output straight
+// into y (no combine kernel). A layer whose slots fit one dispatch chunk reduces its auxiliary
+// value in the dispatch's block (dispatch_aux). A small f32 layer's second expert launch also
+// forms y (f32_combine). Every variant gives the step calls' bits except the top-1 scatter (one
+// bf16 rounding fewer).
 struct ForwardPlan {
-    bool gather, scatter;
+    bool gather, scatter, dispatch_aux, f32_combine;
 };
 
 static ForwardPlan plan_of(const moe_config_t &c) {
     const bool tc = c.dtype == MOE_BF16;
-    return {tc && c.fuse_gather != 0, tc && c.k == 1 && capacity_of(c) < 0};
+    return {!tc || c.fuse_gather != 0, tc && c.k == 1 && capacity_of(c) < 0,
+            c.T > 0 && dispatch_chunks(c) == 1, !tc && ffn_f32_combine_ok(c)};
 }
 
 static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const float *W_r,
@@ -311,36 +317,45 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
         if (e == cudaSuccess && zloss_out) e = cudaMemsetAsync(zloss_out, 0, sizeof(float), s);
         return from_cuda(e);
     }
+    const ForwardPlan plan = plan_of(c);
+    const bool scatter = plan.scatter;
+    DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
+                    reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
     cudaError_t e = launch_router_topk(c, h, W_r, b_r, sel_bias, topk, gates, psum, w + L.router,
                                        dev_status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
-                    reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
-    if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
     // the auxiliary value and z-loss need only the counts and the router's partial sums: reduce
-    // them now, while both are still in L2, not after the expert GEMMs have streamed the weights
-    // through it
-    if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
+    // them right after the dispatch, while both are still in L2, not after the expert GEMMs have
+    // streamed the weights through it (for a single-chunk layer, in the dispatch's own block)
+    if (plan.dispatch_aux) {
+        if ((e = launch_dispatch_aux(c, topk, db, psum, aux_out, zloss_out, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else {
+        if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
+        if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    if (!plan.gather && (e = launch_permute(c, h, slot_of, x_perm, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
-    const ForwardPlan plan = plan_of(c);
-    const bool scatter = plan.scatter;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
     fb.sorted_token = sorted_token;
-    if (plan.gather) {
-        fb.gather_h = h;
-    } else if ((e = launch_permute(c, h, slot_of, x_perm, dev_status, s)) !=
-               cudaSuccess) {
-        return MOE_ERR_CUDA;
-    }
+    if (plan.gather) fb.gather_h = h;
     if (scatter) {
         fb.scatter_y = y;
         fb.gates = gates;
+    }
+    if (plan.f32_combine) {
+        fb.combine_y = y;
+        fb.slot_of = slot_of;
+        fb.gates = gates;
+        fb.arrive = reinterpret_cast<uint32_t *>(w + L.status + WS_ARRIVE_OFFSET);
     }
     if (ev_ffn0 && cudaEventRecord(ev_ffn0, s) != cudaSuccess) return MOE_ERR_CUDA;
     e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (ev_ffn1 && cudaEventRecord(ev_ffn1, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (!scatter && (e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
+    if (!scatter && !plan.f32_combine &&
+        (e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
@@ -405,8 +420,10 @@ moe_status_t moe_forward_launch_count(const moe_config_t *cfg, int32_t *kernels)
         return MOE_OK;
     }
     const ForwardPlan plan = plan_of(*cfg);
-    // router (+ split), dispatch, aux, permute, two FFN launches, combine
-    *kernels = router_launches(*cfg) + 1 + (plan.gather ? 0 : 1) + 2 + (plan.scatter ? 0 : 1) + 1;
+    // router (+ split), dispatch and aux (one kernel for a single chunk), permute, two FFN
+    // launches, combine
+    *kernels = router_launches(*cfg) + (plan.dispatch_aux ? 1 : 2) + (plan.gather ? 0 : 1) + 2 +
+               ((plan.scatter || plan.f32_combine) ? 0 : 1);
     return MOE_OK;
 }
 

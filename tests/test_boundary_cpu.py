@@ -95,8 +95,11 @@ def test_fuse_gather_flag():
 
 @pytest.mark.parametrize("name,kw,expect", [
     # router, dispatch, aux, permute, GEMM1, GEMM2 (or the two f32 FFN launches), combine
-    ("micro", {}, 7),
-    ("decode", {}, 7),
+    ("micro", {}, 4),                             # dispatch + aux in one kernel; f32: GEMM1
+                                                  # gathers from h, GEMM2 forms y
+    ("micro", {"dtype": "bf16"}, 6),              # dispatch + aux in one kernel
+    ("micro", {"T": 2000}, 6),                    # two chunks; too many slots for the f32 combine
+    ("decode", {}, 6),                            # dispatch + aux in one kernel
     ("mixtral", {}, 9),                           # tensor-core router: split, logits, select
     ("mixtral", {"fuse_gather": True}, 8),        # no permute
     ("switch", {}, 8),                            # top-1: GEMM2 scatters into y, no combine

@@ -1,7 +1,10 @@
 """The kernel count moe_forward_launch_count reports against the kernels the CUDA profiler sees
-in one moe_forward call, on configurations that take each launch plan: f32 (two FFN kernels),
-the tensor-core router (W_r split first), top-1 with the GEMM2 scatter (no combine), a capacity
-factor (combine kept), the fused gather (no permute)."""
+in one moe_forward call, on configurations that take each launch plan: a small f32 layer
+(dispatch and aux in one kernel, the first FFN kernel gathering from h, the second forming y), a
+small bf16 layer (dispatch and aux in one kernel, permute, tensor-core GEMMs, combine), an f32
+layer with more slots than one dispatch chunk and than the fused combine takes, the tensor-core
+router (W_r split first), top-1 with the GEMM2 scatter (no combine), a capacity factor (combine
+kept), the fused gather (no permute)."""
 import json
 import os
 import tempfile
@@ -20,6 +23,9 @@ OURS = ("router", "dispatch", "permute", "gemm", "ffn", "combine", "aux")
 
 CASES = [
     wl.small("f32_gelu", T=200, d=128, f=256, E=8, k=2, act=wl.ACT_GELU_TANH, dtype="f32"),
+    wl.small("bf16_single_chunk", T=100, d=128, f=256, E=8, k=2),
+    wl.small("f32_many_slots", T=1200, d=128, f=256, E=8, k=2, act=wl.ACT_GELU_TANH,
+             dtype="f32"),
     wl.small("tc_router_k2", T=3000, d=256, f=256, E=8, k=2),
     wl.small("top1_scatter", T=3000, d=128, f=256, E=16, k=1, act=wl.ACT_GELU_TANH,
              gate=wl.GATE_RAW_PROB),
