@@ -60,8 +60,12 @@ ORDER = ["mixtral", "many_small", "switch", "decode", "micro"]
 # and scaled by the experts and rows processed (the traffic grows in proportion: weights once,
 # activations once).
 MEASURED_TRAFFIC = {
-    "mixtral": {"bytes": 1.76e9, "scale": "scaled from a reduced ncu capture (T=2048, E=2, k=1: "
-                                          "2 of 8 experts, 2048 of 8192 rows)"},
+    "mixtral": {"bytes": 1.76e9, "scale": "ncu capture of a reduced case (T=2048, E=2, k=1: 2 of "
+                                          "8 experts, 2048 of 8192 rows), scaled x4"},
+    "switch": {"bytes": 1.39e9, "scale": "ncu capture of a reduced case (T=16384, E=64: half the "
+                                         "experts and rows), scaled x2"},
+    "decode": {"bytes": 1.42e9, "scale": "ncu capture of a reduced case (T=16, E=4: half the "
+                                         "experts and rows), scaled x2"},
 }
 GEMM_KERNEL = "grouped_gemm_pair_kernel / grouped_gemm_tc_kernel"
 F32_KERNEL = "ffn_f32_kernel (CUDA-core FFMA)"

@@ -8,6 +8,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.cuh"
 #include "moe_debug.h"
 
@@ -268,6 +270,15 @@ struct ForwardPlan {
     bool gather, scatter, dispatch_aux, f32_combine;
 };
 
+// NVTX range over the launches of one step of the layer (host side: it marks where the step's
+// kernels are issued; profilers can filter kernels by it). Costs nothing without a tool attached.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 static ForwardPlan plan_of(const moe_config_t &c) {
     const bool tc = c.dtype == MOE_BF16;
     return {!tc || c.fuse_gather != 0, tc && c.k == 1 && capacity_of(c) < 0,
@@ -321,22 +332,31 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     const bool scatter = plan.scatter;
     DispatchBufs db{counts, offsets, sorted_token, slot_of, w + L.disp_flags, L.disp_flags_bytes,
                     reinterpret_cast<int32_t *>(w + L.disp_excl), dev_status};
-    cudaError_t e = launch_router_topk(c, h, W_r, b_r, sel_bias, topk, gates, psum, w + L.router,
-                                       dev_status, s);
+    NvtxRange layer_range("moe_forward");
+    cudaError_t e;
+    {
+        NvtxRange r("moe router + top-k");
+        e = launch_router_topk(c, h, W_r, b_r, sel_bias, topk, gates, psum, w + L.router,
+                               dev_status, s);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     // the auxiliary value and z-loss need only the counts and the router's partial sums: reduce
     // them right after the dispatch, while both are still in L2, not after the expert GEMMs have
     // streamed the weights through it (for a single-chunk layer, in the dispatch's own block)
-    if (plan.dispatch_aux) {
-        if ((e = launch_dispatch_aux(c, topk, db, psum, aux_out, zloss_out, s)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    } else {
-        if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
-        if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
+    {
+        NvtxRange r("moe dispatch + aux + permute");
+        if (plan.dispatch_aux) {
+            if ((e = launch_dispatch_aux(c, topk, db, psum, aux_out, zloss_out, s)) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        } else {
+            if ((e = launch_dispatch(c, topk, db, s)) != cudaSuccess) return MOE_ERR_CUDA;
+            if ((e = launch_aux(c, counts, psum, aux_out, zloss_out, s)) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        if (!plan.gather &&
+            (e = launch_permute(c, h, slot_of, x_perm, dev_status, s)) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    if (!plan.gather && (e = launch_permute(c, h, slot_of, x_perm, dev_status, s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
     FfnBufs fb{x_perm, offsets, W1, W3, W2, b1, b2, w + L.H, y_perm, dev_status};
     fb.sorted_token = sorted_token;
     if (plan.gather) fb.gather_h = h;
@@ -351,12 +371,17 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
         fb.arrive = reinterpret_cast<uint32_t *>(w + L.status + WS_ARRIVE_OFFSET);
     }
     if (ev_ffn0 && cudaEventRecord(ev_ffn0, s) != cudaSuccess) return MOE_ERR_CUDA;
-    e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);
+    {
+        NvtxRange r("moe expert ffn");
+        e = c.dtype == MOE_BF16 ? launch_ffn_tc(c, fb, s) : launch_ffn_f32(c, fb, s);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (ev_ffn1 && cudaEventRecord(ev_ffn1, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (!scatter && !plan.f32_combine &&
-        (e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (!scatter && !plan.f32_combine) {
+        NvtxRange r("moe combine");
+        if ((e = launch_combine(c, y_perm, slot_of, gates, y, dev_status, s)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     return MOE_OK;
 }
 
