@@ -56,10 +56,6 @@ constexpr int CTL_BYTES = 4096;
 #ifndef MOE_GEMM_TMA_STORE
 #define MOE_GEMM_TMA_STORE 1
 #endif
-// Split a half-full last wave of the single-CTA kernel into 128-column halves (0: never).
-#ifndef MOE_GEMM_HALF_TAIL
-#define MOE_GEMM_HALF_TAIL 1
-#endif
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_BOX = 32 * 64;
 constexpr size_t TC_SMEM =
@@ -78,8 +74,6 @@ struct TcArgs {
     int withhold_loads;                // test hook: the producer issues no loads
     int tma_out;  // 1: 32-row groups that lie wholly inside a tile's valid rows leave through
                   // shared-memory staging and TMA stores (the other rows: per-thread stores)
-    int half_tail;  // single-CTA kernel, GELU / plain epilogue: a last wave that is at most half
-                    // full runs as twice as many 128 x 128 halves
     // fused gather (GEMM1): A row r is row a_rows[r] of a [a_src_rows, K] tensor, read with
     // 4-row TMA gathers, instead of row r of a permuted copy
     const int32_t *a_rows;
@@ -109,7 +103,6 @@ __device__ __forceinline__ int4 gather_rows(const TcArgs &a, int row0, int rows,
 
 struct Tile {
     int e, n, row0, rows;  // rows <= 0: nothing to compute (the idle half of a CTA pair)
-    int half = -1;         // single-CTA split tail: -1 the whole 256-column tile, 0 / 1 a half
 };
 // Unit t of the schedule. s_cum[e] is the first unit of expert e (E+1 entries); within an
 // expert, units run N-major, M-minor. A unit is one 128-row M tile, or -- for a CTA pair -- two
@@ -128,18 +121,6 @@ __device__ __forceinline__ Tile decode_tile(int t, int &eh, const int32_t *s_cum
     ti.n = n;
     ti.row0 = s_off[e] + m * BM;
     ti.rows = min(BM, s_off[e + 1] - ti.row0);
-    return ti;
-}
-
-// Work item `it` of the single-CTA kernel. Items before `tail0` are the units themselves; from
-// `tail0` on (the last, at most half-full wave, when the kernel splits it) every unit counts
-// twice, as its two 128-column halves, so that the last wave takes half as long.
-__device__ __forceinline__ Tile item_tile(int it, int tail0, int &eh, const int32_t *s_cum,
-                                          const int32_t *s_off, int n_tiles) {
-    if (it < tail0) return decode_tile<false>(it, eh, s_cum, s_off, n_tiles, 0);
-    const int u = it - tail0;
-    Tile ti = decode_tile<false>(tail0 + u / 2, eh, s_cum, s_off, n_tiles, 0);
-    ti.half = u & 1;
     return ti;
 }
 
@@ -216,12 +197,9 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
             }
         }
     } else {
-        // a split-tail item holds 128 accumulator columns (its half of the 256-column tile)
-        const int width = ti.half >= 0 ? BN / 2 : BN;
-        const int col_base = ti.n * BN + (ti.half > 0 ? BN / 2 : 0);
 #pragma unroll 1
-        for (int c = half * (width / 2); c < (half + 1) * (width / 2); c += 32) {
-            const int col = col_base + c;
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+            const int col = ti.n * BN + c;
             if (col >= a.N) break;  // warp-uniform
             float v[32];
             tmem_ld32(trow + c, v);
@@ -282,6 +260,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();  // offsets and A come from earlier kernels on the stream
     const int E = a.E;
+    constexpr bool PAIR = false;
+    const int rank = 0;
     const int unit0 = (int)blockIdx.x;
     const int ustep = (int)gridDim.x;
 
@@ -325,11 +305,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = s_cum[E];
-    // the last wave of units, when at most half full, runs as twice as many 128-column halves
-    const int wave = (int)gridDim.x;
-    int tail0 = a.half_tail ? total / wave * wave : total;
-    if (2 * (total - tail0) > wave) tail0 = total;
-    const int items = total + (total - tail0);
     const int nk = a.K / BK;
     const unsigned long long lim = a.spin_limit_ns;
 
@@ -340,14 +315,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bits
             bool ok = !a.withhold_loads;
-            for (int t = unit0; t < items && ok; t += ustep) {
-                const Tile ti = item_tile(t, tail0, eh, s_cum, s_off, a.n_tiles);
-                // B rows of this N tile: SwiGLU stacks 128 rows of W1 over 128 rows of W3; a
-                // split-tail item reads only its 128-row half
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                // B rows of this N tile: SwiGLU stacks 128 rows of W1 over 128 rows of W3
                 const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
-                                                     : ti.e * a.N + ti.n * BN +
-                                                           (ti.half > 0 ? BN / 2 : 0);
-                const uint32_t bytes = A_STAGE + (ti.half >= 0 ? B_STAGE / 2 : B_STAGE);
+                                                     : ti.e * a.N + ti.n * BN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
                         ok = false;
@@ -355,15 +327,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     const uint32_t fb = bar_full + 8 * stage;
                     const uint32_t sb = sB + stage * B_STAGE;
-                    mbar_expect_tx(fb, bytes);
+                    mbar_expect_tx(fb, A_STAGE + B_STAGE);
                     tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
                     if (a.epi == EPI_SWIGLU) {
                         tma_load_2d(sb, &tmB, fb, kb * BK, brow);
                         tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
                     } else {
                         tma_load_2d(sb, &tmB, fb, kb * BK, brow);
-                        if (ti.half < 0)
-                            tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kb * BK, brow + BN / 2);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kb * BK, brow + BN / 2);
                     }
                     issued |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -386,8 +357,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t phase = 0;
         uint32_t issued = 0, last_phase = 0;  // per-stage bits
         bool ok = !a.withhold_loads;
-        for (int t = unit0; t < items && ok; t += ustep) {
-            const Tile ti = item_tile(t, tail0, eh, s_cum, s_off, a.n_tiles);
+        for (int t = unit0; t < total && ok; t += ustep) {
+            const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
             const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
                                                  : ti.e * a.N + ti.n * BN;
             const int4 gr = gather ? gather_rows(a, ti.row0, ti.rows, lane) : make_int4(0, 0, 0, 0);
@@ -437,10 +408,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int stage = 0, acc = 0, eh = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            for (int t = unit0; t < items && ok; t += ustep) {
-                const Tile ti = item_tile(t, tail0, eh, s_cum, s_off, a.n_tiles);
+            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            for (int t = unit0; t < total && ok; t += ustep) {
+                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
                 const bool idle = ti.rows <= 0;
-                const uint32_t idesc = ti.half >= 0 ? idesc_bf16(BM, BN / 2) : idesc_bf16(BM, BN);
                 if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
@@ -478,8 +449,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t stg = smem_u32(ctl + CTL_BYTES) + (uint32_t)(warp - 2) * EPI_BOX;
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
-        for (int t = unit0; t < items; t += ustep) {
-            const Tile ti = item_tile(t, tail0, eh, s_cum, s_off, a.n_tiles);
+        for (int t = unit0; t < total; t += ustep) {
+            const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -839,7 +810,6 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold_loads = hook.withhold;
     a.tma_out = (MOE_GEMM_TMA_STORE && out_token == nullptr) ? 1 : 0;
-    a.half_tail = (MOE_GEMM_HALF_TAIL && epi != EPI_SWIGLU && A_rows == nullptr) ? 1 : 0;
     a.a_rows = A_rows;
     a.a_src_rows = A_src_rows;
     a.out_token = out_token;

@@ -87,6 +87,9 @@ SMALL = [
     wl.small("split_tail_swiglu_k2", T=2600, d=1024, f=1792, E=2, k=2),
     wl.small("split_tail_gelu_top1", T=5120, d=1024, f=2560, E=1, k=1, act=G, has_bias=True,
              gate=wl.GATE_RAW_PROB),
+    # a paired GELU GEMM1 with biases whose 80 units leave a last wave of 6 on 74 clusters
+    wl.small("pair_partial_wave_gelu", T=5120, d=256, f=1024, E=1, k=1, act=G, has_bias=True,
+             gate=wl.GATE_RAW_PROB, seed=19),
     # moe_forward with GEMM1 gathering its rows of h (single-CTA and paired kernels, ragged row
     # counts that leave part of a 4-row gather past an expert's end), with and without top-1 scatter
     wl.small("gather_ragged_k3", T=301, d=192, f=320, E=5, k=3, fuse_gather=True),
