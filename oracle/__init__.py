@@ -1,4 +1,5 @@
-"""Double-precision CPU oracle of the top-k MoE FFN layer forward -- TEST INFRASTRUCTURE ONLY.
+"""Double-precision CPU oracle of the top-k MoE FFN layer (forward and backward) -- TEST
+INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import this
 package. The CUDA library and its Python binding never import, link or call it; the two share no
@@ -65,6 +66,12 @@ def lib() -> ctypes.CDLL:
         L.oracle_gelu_tanh.restype = D
         L.oracle_silu.argtypes = [D]
         L.oracle_silu.restype = D
+        L.oracle_gelu_tanh_grad.argtypes = [D]
+        L.oracle_gelu_tanh_grad.restype = D
+        L.oracle_silu_grad.argtypes = [D]
+        L.oracle_silu_grad.restype = D
+        L.oracle_backward.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, I32, P, P, P, P, P,
+                                      I32, P, P, P, P, P, I32, D, D, P, P, P, P, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -113,6 +120,8 @@ def _ptr(x) -> int | None:
 def _f32(x):
     if x is None:
         return None
+    if isinstance(x, np.ndarray):
+        x = torch.from_numpy(np.ascontiguousarray(x))
     return x.detach().cpu().to(torch.float32).contiguous()
 
 
@@ -293,6 +302,45 @@ def gelu_tanh(x: float) -> float:
 
 def silu(x: float) -> float:
     return float(lib().oracle_silu(float(x)))
+
+
+def gelu_tanh_grad(x: float) -> float:
+    return float(lib().oracle_gelu_tanh_grad(float(x)))
+
+
+def silu_grad(x: float) -> float:
+    return float(lib().oracle_silu_grad(float(x)))
+
+
+def backward(h, W_r, b_r, W1, W3, W2, b1, b2, idx, dy, act: int, gate_mode: int, keep=None,
+             aux_weight: float = 0.0, zloss_weight: float = 0.0) -> dict:
+    """Gradients of sum(dy * y) + aux_weight * aux + zloss_weight * zloss for the routing idx
+    (held fixed), all in double: dh, dW_r, db_r, dW1, dW3, dW2, db1, db2 (None where the layer
+    has no such parameter) and dg, dL/dg of every slot [T, k]."""
+    hs, hdt = _stored(h)
+    T, d = hs.shape
+    Wr = _f32(W_r)
+    E = Wr.shape[1]
+    br = _f32(b_r)
+    idx = _np(idx, np.int32)
+    k = idx.shape[1]
+    w1, w3, w2, wdt = _weights(W1, W3, W2)
+    f = w1.shape[1]
+    b1c, b2c = _f32(b1), _f32(b2)
+    dys, dydt = _stored(dy)
+    kp = None if keep is None else _np(keep, np.uint8)
+    out = dict(dh=np.empty((T, d)), dW_r=np.empty((d, E)), db_r=np.empty(E) if br is not None
+               else None, dW1=np.empty((E, f, d)), dW3=np.empty((E, f, d)) if act == SWIGLU
+               else None, dW2=np.empty((E, d, f)), db1=np.empty((E, f)) if b1c is not None
+               else None, db2=np.empty((E, d)) if b2c is not None else None,
+               dg=np.empty((T, k)))
+    lib().oracle_backward(T, d, f, E, k, act, gate_mode, _ptr(hs), hdt, _ptr(Wr), _ptr(br),
+                          _ptr(w1), _ptr(w3), _ptr(w2), wdt, _ptr(b1c), _ptr(b2c), _ptr(idx),
+                          _ptr(kp), _ptr(dys), dydt, float(aux_weight), float(zloss_weight),
+                          _ptr(out["dh"]), _ptr(out["dW_r"]), _ptr(out["db_r"]), _ptr(out["dW1"]),
+                          _ptr(out["dW3"]), _ptr(out["dW2"]), _ptr(out["db1"]), _ptr(out["db2"]),
+                          _ptr(out["dg"]))
+    return out
 
 
 # ----------------------------------------------------------------------------------------------

@@ -396,3 +396,214 @@ void oracle_param_count(int32_t n_layers, int64_t d, int64_t f, int32_t E, int32
     *total = (int64_t)n_layers * (shared_per_layer + router + (int64_t)E * expert) + shared_global;
     *active = (int64_t)n_layers * (shared_per_layer + router + (int64_t)k * expert) + shared_global;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Backward pass. [CURIO] opening text and [LENSA-3]: selecting the top-k experts is not
+ * differentiable, so the gradient reaches the router only through the weights of the chosen
+ * experts (for Switch top-1, through p_i); [LENSA-4]: of the auxiliary term only P_i is
+ * differentiable; [JAGGI] "How Routing Works": the router trains by ordinary backpropagation.
+ * Reading: idx, the routed counts (hence f_i) and the capacity drops are constants of the step;
+ * everything else is differentiated exactly by the chain rule, in double.
+ *
+ * The loss whose gradient is returned is
+ *     L = sum_{t,o} dy[t,o] y[t,o] + aux_weight * (E sum_e f_e P_e) + zloss_weight * zloss,
+ * so dy is the upstream gradient of y. */
+
+/* d/dx of the tanh-form GELU: with u = c (x + 0.044715 x^3), c = sqrt(2/pi),
+ * 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) c (1 + 3 * 0.044715 x^2). */
+static double gelu_tanh_grad(double x)
+{
+    const double c = sqrt(2.0 / M_PI);
+    const double th = tanh(c * (x + 0.044715 * x * x * x));
+    return 0.5 * (1.0 + th) + 0.5 * x * (1.0 - th * th) * c * (1.0 + 3.0 * 0.044715 * x * x);
+}
+
+/* d/dx of SiLU: s (1 + x (1 - s)) with s = 1 / (1 + e^-x). */
+static double silu_grad(double x)
+{
+    const double s = 1.0 / (1.0 + exp(-x));
+    return s * (1.0 + x * (1.0 - s));
+}
+
+double oracle_gelu_tanh_grad(double x) { return gelu_tanh_grad(x); }
+double oracle_silu_grad(double x) { return silu_grad(x); }
+
+/* Gradient of L with respect to the router logits of one token, given dg[j] = dL/dg_j of its k
+ * gates (0 for a dropped slot):
+ *   RENORM  : g = softmax over the chosen logits, so dz[e_j] = g_j (dg_j - sum_l g_l dg_l) and
+ *             dz = 0 off the chosen set;
+ *   RAW_PROB: g_j = p[e_j], so dz[i] = sum_j dg_j p[e_j] (delta(i, e_j) - p[i]);
+ *   plus the auxiliary term: dL/dp[t,e] = aux_weight E f_e / T =: c_e, through the softmax
+ *   dz[i] += p[i] (c_i - sum_e c_e p[e]);
+ *   plus the z-loss: d/dz[i] of zloss_weight (1/T) lse^2 is zloss_weight (2/T) lse p[i]. */
+static void router_logit_grad(int64_t T, int32_t E, int32_t k, int32_t gate_mode,
+                              const double *zt, const double *pt, const int32_t *it,
+                              const double *gt, const double *dg, const double *fe,
+                              double aux_weight, double zloss_weight, double *dz)
+{
+    for (int32_t e = 0; e < E; ++e) dz[e] = 0.0;
+    if (gate_mode == OR_RAW_PROB) {
+        double s = 0.0;
+        for (int32_t j = 0; j < k; ++j) s += dg[j] * pt[it[j]];
+        for (int32_t e = 0; e < E; ++e) dz[e] = -pt[e] * s;
+        for (int32_t j = 0; j < k; ++j) dz[it[j]] += dg[j] * pt[it[j]];
+    } else {
+        double s = 0.0;
+        for (int32_t j = 0; j < k; ++j) s += gt[j] * dg[j];
+        for (int32_t j = 0; j < k; ++j) dz[it[j]] += gt[j] * (dg[j] - s);
+    }
+    if (aux_weight != 0.0) {
+        double s = 0.0;
+        for (int32_t e = 0; e < E; ++e) s += aux_weight * (double)E * fe[e] / (double)T * pt[e];
+        for (int32_t e = 0; e < E; ++e)
+            dz[e] += pt[e] * (aux_weight * (double)E * fe[e] / (double)T - s);
+    }
+    if (zloss_weight != 0.0) {
+        double zmax = zt[0];
+        for (int32_t e = 1; e < E; ++e)
+            if (zt[e] > zmax) zmax = zt[e];
+        double s = 0.0;
+        for (int32_t e = 0; e < E; ++e) s += exp(zt[e] - zmax);
+        const double lse = zmax + log(s);
+        for (int32_t e = 0; e < E; ++e) dz[e] += zloss_weight * 2.0 / (double)T * lse * pt[e];
+    }
+}
+
+/* The whole backward of the layer for the routing idx [T, k] (keep [T, k] may be NULL: every
+ * slot is processed). Outputs, all overwritten (NULL where the layer has no such parameter):
+ *   dh [T, d], dW_r [d, E], db_r [E], dW1 and dW3 [E, f, d], dW2 [E, d, f], db1 [E, f],
+ *   db2 [E, d]; dg_out [T, k] (may be NULL): dL/dg of every slot.
+ * Expert e's weight gradients are sums over its slots in token order; dh[t] adds the k slots'
+ * input gradients in slot order and then the router's h-gradient. */
+void oracle_backward(int64_t T, int32_t d, int32_t f, int32_t E, int32_t k, int32_t act,
+                     int32_t gate_mode, const void *h, int32_t h_dtype, const float *W_r,
+                     const float *b_r, const void *W1, const void *W3, const void *W2,
+                     int32_t w_dtype, const float *b1, const float *b2, const int32_t *idx,
+                     const unsigned char *keep, const void *dy, int32_t dy_dtype,
+                     double aux_weight, double zloss_weight, double *dh, double *dW_r,
+                     double *db_r, double *dW1, double *dW3, double *dW2, double *db1,
+                     double *db2, double *dg_out)
+{
+    const int64_t P = T * k;
+    double *z = (double *)malloc(sizeof(double) * (size_t)(T * E + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(T * E + 1));
+    double *g = (double *)malloc(sizeof(double) * (size_t)(P + 1));
+    double *dg = (double *)calloc((size_t)(P + 1), sizeof(double));
+    double *dxs = (double *)calloc((size_t)(P * d + 1), sizeof(double));
+    double *fe = (double *)calloc((size_t)(E > 0 ? E : 1), sizeof(double));
+    oracle_router(T, d, E, h, h_dtype, W_r, b_r, z, p);
+    oracle_gates(T, E, k, gate_mode, z, p, idx, g);
+    for (int64_t s = 0; s < P; ++s) fe[idx[s]] += 1.0;
+    for (int32_t e = 0; e < E; ++e) fe[e] /= (double)T * (double)k;
+
+    const int64_t wsz = (int64_t)E * f * d;
+    for (int64_t i = 0; i < wsz; ++i) {
+        dW1[i] = 0.0;
+        dW2[i] = 0.0;
+        if (dW3) dW3[i] = 0.0;
+    }
+    if (db1) for (int64_t i = 0; i < (int64_t)E * f; ++i) db1[i] = 0.0;
+    if (db2) for (int64_t i = 0; i < (int64_t)E * d; ++i) db2[i] = 0.0;
+
+    /* experts: each one owns its weight gradients; slots of expert e in token order */
+#pragma omp parallel
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dyt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *a1 = (double *)malloc(sizeof(double) * (size_t)f);
+        double *a3 = (double *)malloc(sizeof(double) * (size_t)f);
+        double *hid = (double *)malloc(sizeof(double) * (size_t)f);
+        double *dhid = (double *)malloc(sizeof(double) * (size_t)f);
+        double *da1 = (double *)malloc(sizeof(double) * (size_t)f);
+        double *da3 = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t e = 0; e < E; ++e) {
+            const int64_t base1 = (int64_t)e * f * d, base2 = (int64_t)e * d * f;
+            for (int64_t s = 0; s < P; ++s) {
+                if (idx[s] != e || (keep && !keep[s])) continue;
+                const int64_t t = s / k;
+                for (int32_t i = 0; i < d; ++i) {
+                    x[i] = widen(h, h_dtype, t * d + i);
+                    dyt[i] = widen(dy, dy_dtype, t * d + i);
+                }
+                /* forward of this slot: pre-activations, hidden row and output */
+                for (int32_t n = 0; n < f; ++n) {
+                    double u = 0.0, v = 0.0;
+                    for (int32_t i = 0; i < d; ++i) {
+                        u += widen(W1, w_dtype, base1 + (int64_t)n * d + i) * x[i];
+                        if (act == OR_SWIGLU) v += widen(W3, w_dtype, base1 + (int64_t)n * d + i) * x[i];
+                    }
+                    if (act != OR_SWIGLU && b1) u += (double)b1[(int64_t)e * f + n];
+                    a1[n] = u;
+                    a3[n] = v;
+                    hid[n] = act == OR_SWIGLU ? silu(u) * v : gelu_tanh(u);
+                }
+                /* dL/dg of this slot: dy[t] . (W2_e hid + b2_e) */
+                double dgs = 0.0;
+                for (int32_t o = 0; o < d; ++o) {
+                    double yo = 0.0;
+                    for (int32_t n = 0; n < f; ++n) yo += widen(W2, w_dtype, base2 + (int64_t)o * f + n) * hid[n];
+                    if (act != OR_SWIGLU && b2) yo += (double)b2[(int64_t)e * d + o];
+                    dgs += dyt[o] * yo;
+                }
+                dg[s] = dgs;
+                /* the slot's output enters y scaled by its gate */
+                const double gs = g[s];
+                for (int32_t n = 0; n < f; ++n) dhid[n] = 0.0;
+                for (int32_t o = 0; o < d; ++o) {
+                    const double dyo = gs * dyt[o];
+                    for (int32_t n = 0; n < f; ++n) {
+                        dW2[base2 + (int64_t)o * f + n] += dyo * hid[n];
+                        dhid[n] += widen(W2, w_dtype, base2 + (int64_t)o * f + n) * dyo;
+                    }
+                    if (act != OR_SWIGLU && db2) db2[(int64_t)e * d + o] += dyo;
+                }
+                for (int32_t n = 0; n < f; ++n) {
+                    if (act == OR_SWIGLU) {
+                        da1[n] = dhid[n] * a3[n] * silu_grad(a1[n]);
+                        da3[n] = dhid[n] * silu(a1[n]);
+                    } else {
+                        da1[n] = dhid[n] * gelu_tanh_grad(a1[n]);
+                        da3[n] = 0.0;
+                    }
+                }
+                double *dx = dxs + s * d;
+                for (int32_t n = 0; n < f; ++n) {
+                    for (int32_t i = 0; i < d; ++i) {
+                        dW1[base1 + (int64_t)n * d + i] += da1[n] * x[i];
+                        dx[i] += widen(W1, w_dtype, base1 + (int64_t)n * d + i) * da1[n];
+                        if (act == OR_SWIGLU) {
+                            dW3[base1 + (int64_t)n * d + i] += da3[n] * x[i];
+                            dx[i] += widen(W3, w_dtype, base1 + (int64_t)n * d + i) * da3[n];
+                        }
+                    }
+                    if (act != OR_SWIGLU && db1) db1[(int64_t)e * f + n] += da1[n];
+                }
+            }
+        }
+        free(x); free(dyt); free(a1); free(a3); free(hid); free(dhid); free(da1); free(da3);
+    }
+
+    /* router: dz per token, then dh, dW_r and db_r */
+    double *dz = (double *)malloc(sizeof(double) * (size_t)(T * E + 1));
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        router_logit_grad(T, E, k, gate_mode, z + t * E, p + t * E, idx + t * k, g + t * k,
+                          dg + t * k, fe, aux_weight, zloss_weight, dz + t * E);
+        for (int32_t i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int32_t j = 0; j < k; ++j) acc += dxs[(t * k + j) * d + i];
+            for (int32_t e = 0; e < E; ++e) acc += (double)W_r[(int64_t)i * E + e] * dz[t * E + e];
+            dh[t * d + i] = acc;
+        }
+    }
+    for (int64_t i = 0; i < (int64_t)d * E; ++i) dW_r[i] = 0.0;
+    if (db_r) for (int32_t e = 0; e < E; ++e) db_r[e] = 0.0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t e = 0; e < E; ++e) {
+            for (int32_t i = 0; i < d; ++i) dW_r[(int64_t)i * E + e] += widen(h, h_dtype, t * d + i) * dz[t * E + e];
+            if (db_r) db_r[e] += dz[t * E + e];
+        }
+    if (dg_out) for (int64_t s = 0; s < P; ++s) dg_out[s] = dg[s];
+    free(z); free(p); free(g); free(dg); free(dxs); free(fe); free(dz);
+}
