@@ -81,6 +81,11 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_uint64, _P],
             "moe_debug_expert_ffn_timeout": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                              ctypes.c_size_t, ctypes.c_uint64, _P],
+            "moe_backward_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
+            "moe_backward_launch_count": [_CFG, ctypes.POINTER(ctypes.c_int32)],
+            "moe_backward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
+                             ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                             _P, ctypes.c_size_t, _P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -277,6 +282,32 @@ def moe_forward_events(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_id
            "moe_forward_events")
 
 
+def moe_backward_workspace_size(cfg: moe_config_t) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_backward_launch_count(cfg: moe_config_t) -> int:
+    n = ctypes.c_int32()
+    _check(lib().moe_backward_launch_count(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_backward_launch_count")
+    return n.value
+
+
+def moe_backward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, topk_idx, counts, dy, aux_weight,
+                 zloss_weight, dh, dW_r, db_r, dW1, db1, dW3, dW2, db2, ws, bws,
+                 stream=None) -> None:
+    _check(lib().moe_backward(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(W1),
+                              _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2), _ptr(topk_idx),
+                              _ptr(counts), _ptr(dy), float(aux_weight), float(zloss_weight),
+                              _ptr(dh), _ptr(dW_r), _ptr(db_r), _ptr(dW1), _ptr(db1), _ptr(dW3),
+                              _ptr(dW2), _ptr(db2), _ptr(ws), ws.numel() * ws.element_size(),
+                              _ptr(bws), bws.numel() * bws.element_size(), _stream(stream)),
+           "moe_backward")
+
+
 def moe_device_status(ws, stream=None) -> int:
     """Synchronise, read and clear the device status word; returns the status code."""
     return int(lib().moe_device_status(_ptr(ws), _stream(stream)))
@@ -314,6 +345,38 @@ class Layer:
         else:
             moe_forward_events(*args, ffn_events[0], ffn_events[1], stream, **extra)
         return self.y
+
+    def backward(self, h: torch.Tensor, dy: torch.Tensor, aux_weight: float = 0.0,
+                 zloss_weight: float = 0.0, stream=None) -> dict:
+        """moe_backward after forward(h): the gradients of sum(dy * y) + aux_weight * aux +
+        zloss_weight * zloss (bf16 layers). Returns device tensors dh, dW_r, db_r, dW1, dW3,
+        dW2, db1, db2 (None where the layer has no such parameter), owned by the Layer and
+        overwritten by the next call."""
+        cfg, w = self.cfg, self.w
+        dev = h.device
+        if getattr(self, "bws", None) is None:
+            self.bws = torch.empty(max(moe_backward_workspace_size(cfg), 16), dtype=torch.uint8,
+                                   device=dev)
+        if getattr(self, "grads", None) is None:
+            E, d, f = cfg.E, cfg.d, cfg.f
+            bf = torch.bfloat16
+            sw = cfg.act == MOE_ACT_SWIGLU
+            self.grads = dict(
+                dh=torch.empty((cfg.T, d), dtype=bf, device=dev),
+                dW_r=torch.empty((d, E), dtype=torch.float32, device=dev),
+                db_r=torch.empty(E, dtype=torch.float32, device=dev)
+                if w.get("b_r") is not None else None,
+                dW1=torch.empty((E, f, d), dtype=bf, device=dev),
+                dW3=torch.empty((E, f, d), dtype=bf, device=dev) if sw else None,
+                dW2=torch.empty((E, d, f), dtype=bf, device=dev),
+                db1=torch.empty((E, f), dtype=torch.float32, device=dev) if cfg.has_bias else None,
+                db2=torch.empty((E, d), dtype=torch.float32, device=dev) if cfg.has_bias else None)
+        g = self.grads
+        moe_backward(cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"), w["W2"],
+                     w.get("b2"), self.topk_idx, self.counts, dy, aux_weight, zloss_weight,
+                     g["dh"], g["dW_r"], g["db_r"], g["dW1"], g["db1"], g["dW3"], g["dW2"],
+                     g["db2"], self.ws, self.bws, stream)
+        return g
 
     def capture(self, h: torch.Tensor) -> "torch.cuda.CUDAGraph":
         """Record one moe_forward on the device tensor h into a CUDA graph. ``replay()`` reruns

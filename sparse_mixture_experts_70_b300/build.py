@@ -17,7 +17,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
 
 SOURCES = ["moe_api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "combine.cu", "ffn_f32.cu", "gemm_tc.cu",
-           "pipeline.cu", "probe.cu"]
+           "pipeline.cu", "probe.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I" + INCLUDE, "-I" + CSRC]
@@ -30,7 +30,7 @@ def _nvcc() -> str:
 
 def _deps_mtime() -> float:
     files = [os.path.join(INCLUDE, "moe.h"), os.path.join(INCLUDE, "moe_pipeline.h"),
-             os.path.join(INCLUDE, "moe_probe.h"),
+             os.path.join(INCLUDE, "moe_probe.h"), os.path.join(INCLUDE, "moe_backward.h"),
              os.path.join(CSRC, "internal.cuh"), os.path.join(CSRC, "layer_dev.cuh"),
              os.path.join(CSRC, "tc_ptx.cuh")]
     return max(os.path.getmtime(f) for f in files)

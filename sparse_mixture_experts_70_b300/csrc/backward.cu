@@ -1,0 +1,963 @@
+// backward.cu -- the backward pass of the MoE layer (bf16 layers, tensor-core GEMMs).
+//
+// The pages: selecting the top-k experts is not differentiable, so the gradient reaches the
+// router only through the weights of the chosen experts -- for Switch top-1 through the router
+// probability p_i (llm.curionode.com "Mixture of Experts.", opening text; lensaml.com "Mixture of
+// Experts", Step 3 "Top-k Routing"); of the auxiliary term only P_i is differentiable (Step 4
+// "Load Balancing"); the router trains by ordinary backpropagation (arjunjaggi.com "Mixture of
+// Experts in LLMs", "How Routing Works"). So idx, the routed counts and the capacity drops of the
+// forward are constants here, and the loss differentiated is
+//     L = sum dy * y + aux_weight * (E sum_e f_e P_e) + zloss_weight * zloss.
+//
+// With X the permuted rows of h, a slot r of expert e with gate g_r, and dYu[r] = dy[token(r)]:
+//   A1 = X W1_e^T (+ b1), A3 = X W3_e^T           recomputed (two row-grouped GEMMs)
+//   dHu = dYu W2_e                                 row-grouped GEMM, dy rows gathered by TMA
+//   SwiGLU: Hact = SiLU(A1) A3, dA1 = g dHu A3 SiLU'(A1), dA3 = g dHu SiLU(A1)
+//   GELU  : Hact = GELU(A1),    dA1 = g dHu GELU'(A1)
+//   dg_r = dHu . Hact (+ dy . b2_e)                gradient of the slot's gate
+//   dX = dA1 W1_e + dA3 W3_e                        one row-grouped GEMM over K = [dA1 | dA3]
+//   dW2_e = (g dYu)^T Hact, dW1_e = dA1^T X, dW3_e = dA3^T X   K-grouped GEMMs over the slots
+//   db2_e = sum_r g_r dYu[r], db1_e = sum_r dA1[r]
+//   router: dz from dg through the gate softmax (RENORM) or p (RAW_PROB), plus the auxiliary
+//           term and the z-loss; dh = sum_j dX[slot] + dz W_r^T, dW_r = h^T dz, db_r = sum dz.
+// The weight-gradient GEMMs contract over slots, so their operands are stored transposed with
+// every expert's slots padded to a multiple of 64 columns (zeros in the pad): segment e of the
+// padded slot axis is [kseg[e], kseg[e+1]), kseg[e+1] - kseg[e] = roundup64(count_e).
+#include "internal.cuh"
+#include "moe_backward.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BT = 64;  // tile edge of the transposing kernels
+
+__device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+        v[2 * i] = __low2float(p);
+        v[2 * i + 1] = __high2float(p);
+    }
+}
+
+// The expert whose padded segment holds padded column c (kseg in shared memory, E+1 entries).
+__device__ __forceinline__ int segment_of(const int32_t *kseg, int E, int c) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (kseg[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------------------------
+// prep: gate of every sorted row (gate_r[slot_of[s]] = gates[s] for kept slots) and the padded
+// segment offsets kseg (block 0).
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, const float *gates,
+                                                       const int32_t *offsets, int64_t P, int E,
+                                                       float *gate_r, int32_t *kseg,
+                                                       uint32_t *dev_status) {
+    pdl_wait();
+    const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int rows = offsets[E];
+    if (s < P) {
+        const int r = slot_of[s];
+        if (r >= rows || (int64_t)r >= P) report(dev_status, DEV_ERR_INDEX);
+        else if (r >= 0) gate_r[r] = gates[s];
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        int acc = 0;
+        kseg[0] = 0;
+        for (int e = 0; e < E; ++e) {
+            const int cnt = offsets[e + 1] - offsets[e];
+            acc += (cnt + BT - 1) / BT * BT;
+            kseg[e + 1] = acc;
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// dst[b][c][coff + r] = src[b][r][c] for src [B][R][C], dst rows of ldd elements (bf16). R and C
+// are multiples of 64; one 64 x 64 tile per block through shared memory.
+__global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16 *src, int R, int C,
+                                                        __nv_bfloat16 *dst, int ldd, int coff) {
+    __shared__ __nv_bfloat16 tile[BT][BT + 8];
+    pdl_wait();
+    const int c0 = blockIdx.x * BT, r0 = blockIdx.y * BT;
+    const int64_t b = blockIdx.z;
+    const __nv_bfloat16 *s = src + b * (int64_t)R * C;
+    __nv_bfloat16 *d = dst + b * (int64_t)C * ldd;
+    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+        const int r = i >> 3, ch = i & 7;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(s + (int64_t)(r0 + r) * C + c0) + ch);
+        *reinterpret_cast<uint4 *>(&tile[r][ch * 8]) = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+        const int c = i >> 3, ch = i & 7;
+        __align__(16) __nv_bfloat16 out[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) out[j] = tile[ch * 8 + j][c];
+        *reinterpret_cast<uint4 *>(d + (int64_t)(c0 + c) * ldd + coff + r0 + ch * 8) =
+            *reinterpret_cast<const uint4 *>(out);
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Gather-transpose into the padded slot layout: dst[i][c] = scale_r src[sorted_token[r]][i] for
+// padded column c of segment e holding sorted row r = offsets[e] + c - kseg[e], zero in the pad.
+// blockIdx.z selects one of two jobs (X: h, no scale; dYs: dy scaled by the row's gate, with the
+// column-tile sums of the scaled values in part [kw/64][d] when part is given, for db2).
+struct GatherT {
+    const __nv_bfloat16 *src;
+    const float *scale;  // gate_r or null
+    __nv_bfloat16 *dst;  // [d, kw]
+    float *part;         // [kw/64, d] or null
+};
+__global__ void __launch_bounds__(256) gather_transpose_kernel(GatherT j0, GatherT j1,
+                                                               const int32_t *sorted_token,
+                                                               const int32_t *offsets,
+                                                               const int32_t *kseg_g, int E,
+                                                               int64_t T, int64_t P, int d,
+                                                               int64_t kw, uint32_t *dev_status) {
+    __shared__ float tile[BT][BT + 1];  // [slot j][feature i]
+    __shared__ int32_t kseg[257];
+    __shared__ int32_t tok[BT];
+    __shared__ float scl[BT];
+    pdl_wait();
+    const GatherT J = blockIdx.z == 0 ? j0 : j1;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) kseg[e] = kseg_g[e];
+    __syncthreads();
+    const int c0 = blockIdx.x * BT;
+    if (J.src == nullptr || c0 >= kseg[E]) {
+        pdl_trigger();
+        return;
+    }
+    const int e = segment_of(kseg, E, c0);
+    const int cnt = offsets[e + 1] - offsets[e];
+    const int local0 = c0 - kseg[e];
+    const int i0 = blockIdx.y * BT;
+    if (threadIdx.x < BT) {
+        const int l = local0 + threadIdx.x;
+        int t = -1;
+        float sc = 0.f;
+        const int r = offsets[e] + l;
+        if (l < cnt && (r < 0 || (int64_t)r >= P)) report(dev_status, DEV_ERR_INDEX);
+        if (l < cnt && r >= 0 && (int64_t)r < P) {
+            t = sorted_token[r];
+            if (t < 0 || t >= T) {
+                report(dev_status, DEV_ERR_INDEX);
+                t = -1;
+            } else {
+                sc = J.scale ? J.scale[r] : 1.f;
+            }
+        }
+        tok[threadIdx.x] = t;
+        scl[threadIdx.x] = sc;
+    }
+    __syncthreads();
+    // rows of src (one 64-feature chunk each), 8 features per thread-step
+    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+        const int jr = i >> 3, ch = i & 7;
+        float v[8];
+        if (tok[jr] >= 0) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
+                                      J.src + (int64_t)tok[jr] * d + i0) + ch);
+            unpack8(u, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] *= scl[jr];
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tile[jr][ch * 8 + q] = v[q];
+    }
+    __syncthreads();
+    // transposed rows: feature i, 64 padded columns; column-tile sums for the bias gradient
+    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+        const int fi = i >> 3, ch = i & 7;
+        float v[8];
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v[q] = tile[ch * 8 + q][fi];
+            sum += v[q];
+        }
+        const uint4 u = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
+                                   pack2(v[6], v[7]));
+        *reinterpret_cast<uint4 *>(J.dst + (int64_t)(i0 + fi) * kw + c0 + ch * 8) = u;
+        if (J.part) {
+            // the 8 threads of feature fi are 8 consecutive lanes: sum them in a fixed order
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if (ch == 0) J.part[(int64_t)blockIdx.x * d + i0 + fi] = sum;
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Activation backward on one 64-slot x 64-feature tile: padded columns [c0, c0 + 64) of one
+// expert (blockIdx.x), features [n0, n0 + 64) (blockIdx.y). Reads A1 (and A3), dHu and the row
+// gates; writes dA [rows, K'] row-major (dA1 in columns [0, f), dA3 in [f, 2f) for SwiGLU), the
+// transposed dA1T, dA3T and HT = Hact^T [f, kw] (zeros in the pad), dg_part[n-tile][r] = the
+// tile's part of dHu . Hact, and (when db1_part is given) the tile's column sums of dA1.
+struct ActBwd {
+    const __nv_bfloat16 *A1, *A3, *dHu;
+    const float *gate_r;
+    const int32_t *offsets, *kseg;
+    __nv_bfloat16 *dA, *dA1T, *dA3T, *HT;
+    float *dg_part;   // [f/64, P]
+    float *db1_part;  // [kw/64, f] or null
+    int64_t P, kw;
+    int E, f, swiglu;
+};
+
+__device__ __forceinline__ float gelu_tanh_acc(float x, float &slope) {
+    const float c = 0.7978845608028654f;
+    const float th = tanhf(c * (x + 0.044715f * x * x * x));
+    slope = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * c * (1.f + 3.f * 0.044715f * x * x);
+    return 0.5f * x * (1.f + th);
+}
+
+__global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *dev_status) {
+    __shared__ float s1[BT][BT + 1];            // dA1 (f32, for the bias sums)
+    __shared__ __nv_bfloat16 s3[BT][BT + 2];    // dA3
+    __shared__ __nv_bfloat16 sh[BT][BT + 2];    // Hact
+    __shared__ int32_t kseg[257];
+    pdl_wait();
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) kseg[e] = a.kseg[e];
+    __syncthreads();
+    const int c0 = blockIdx.x * BT;
+    if (c0 >= kseg[a.E]) {
+        pdl_trigger();
+        return;
+    }
+    const int e = segment_of(kseg, a.E, c0);
+    const int rbase = a.offsets[e] + (c0 - kseg[e]);  // sorted row of column c0
+    const int rend = a.offsets[e + 1];
+    if (rend > a.P || rbase < 0) {
+        report(dev_status, DEV_ERR_INDEX);
+        pdl_trigger();
+        return;
+    }
+    const int n0 = blockIdx.y * BT;
+    const int K2 = a.swiglu ? 2 * a.f : a.f;
+    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+        const int jr = i >> 3, ch = i & 7;
+        const int r = rbase + jr;
+        const bool valid = r < rend;
+        float d1[8], d3[8], hv[8];
+        float dg = 0.f;
+        if (valid) {
+            const int64_t off = (int64_t)r * a.f + n0 + ch * 8;
+            float x1[8], x3[8], du[8];
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.A1 + off)), x1);
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.dHu + off)), du);
+            if (a.swiglu) unpack8(__ldg(reinterpret_cast<const uint4 *>(a.A3 + off)), x3);
+            const float g = a.gate_r[r];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (a.swiglu) {
+                    const float sg = 1.f / (1.f + expf(-x1[q]));
+                    const float si = x1[q] * sg;
+                    hv[q] = si * x3[q];
+                    d1[q] = g * du[q] * x3[q] * sg * (1.f + x1[q] * (1.f - sg));
+                    d3[q] = g * du[q] * si;
+                } else {
+                    float slope;
+                    hv[q] = gelu_tanh_acc(x1[q], slope);
+                    d1[q] = g * du[q] * slope;
+                    d3[q] = 0.f;
+                }
+                dg += du[q] * hv[q];
+            }
+            __nv_bfloat16 *row = a.dA + (int64_t)r * K2 + n0 + ch * 8;
+            *reinterpret_cast<uint4 *>(row) =
+                make_uint4(pack2(d1[0], d1[1]), pack2(d1[2], d1[3]), pack2(d1[4], d1[5]),
+                           pack2(d1[6], d1[7]));
+            if (a.swiglu)
+                *reinterpret_cast<uint4 *>(row + a.f) =
+                    make_uint4(pack2(d3[0], d3[1]), pack2(d3[2], d3[3]), pack2(d3[4], d3[5]),
+                               pack2(d3[6], d3[7]));
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d1[q] = d3[q] = hv[q] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s1[jr][ch * 8 + q] = d1[q];
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) {
+            *reinterpret_cast<uint32_t *>(&s3[jr][ch * 8 + q]) = pack2(d3[q], d3[q + 1]);
+            *reinterpret_cast<uint32_t *>(&sh[jr][ch * 8 + q]) = pack2(hv[q], hv[q + 1]);
+        }
+        // the row's 8 feature groups are 8 consecutive lanes: sum them in a fixed order
+        dg += __shfl_xor_sync(0xffffffffu, dg, 1);
+        dg += __shfl_xor_sync(0xffffffffu, dg, 2);
+        dg += __shfl_xor_sync(0xffffffffu, dg, 4);
+        if (valid && ch == 0) a.dg_part[(int64_t)blockIdx.y * a.P + r] = dg;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+        const int fi = i >> 3, ch = i & 7;
+        float v1[8];
+        float sum = 0.f;
+        __align__(16) __nv_bfloat16 o3[8], oh[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v1[q] = s1[ch * 8 + q][fi];
+            sum += v1[q];
+            o3[q] = s3[ch * 8 + q][fi];
+            oh[q] = sh[ch * 8 + q][fi];
+        }
+        const int64_t off = (int64_t)(n0 + fi) * a.kw + c0 + ch * 8;
+        *reinterpret_cast<uint4 *>(a.dA1T + off) =
+            make_uint4(pack2(v1[0], v1[1]), pack2(v1[2], v1[3]), pack2(v1[4], v1[5]),
+                       pack2(v1[6], v1[7]));
+        if (a.swiglu) *reinterpret_cast<uint4 *>(a.dA3T + off) = *reinterpret_cast<const uint4 *>(o3);
+        *reinterpret_cast<uint4 *>(a.HT + off) = *reinterpret_cast<const uint4 *>(oh);
+        if (a.db1_part) {
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if (ch == 0) a.db1_part[(int64_t)blockIdx.x * a.f + n0 + fi] = sum;
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Router backward, one warp per token: the logits z (from the tensor-core partial logits
+// part[S][T][ldp], or a direct dot product over d), p, lse, the gate gradients dg_j of the k slots
+// (the tiles' parts summed, plus dy . b2_e when b2 is given), then dz = dL/dz into dz [T, E].
+constexpr int RB_MAXEW = 8;  // experts per lane: E <= 256
+struct RouterBwd {
+    const __nv_bfloat16 *h, *dy;
+    const float *W_r, *b_r, *b2;
+    const float *part;  // tensor-core partial logits or null
+    int S, ldp;
+    const int32_t *topk_idx, *slot_of, *counts;
+    const float *gates, *dg_part;
+    int n_part;         // f / 64 partial rows of dg
+    int64_t T, P;
+    int d, E, k, raw_prob;
+    float aux_weight, zloss_weight;
+    float *dz;
+};
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint32_t *dev_status) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= a.T) {
+        pdl_trigger();
+        return;
+    }
+    const int E = a.E;
+    float z[RB_MAXEW], p[RB_MAXEW], dz[RB_MAXEW];
+#pragma unroll
+    for (int i = 0; i < RB_MAXEW; ++i) z[i] = 0.f;
+    if (a.part) {
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E)
+                for (int s = 0; s < a.S; ++s) z[i] += a.part[((int64_t)s * a.T + t) * a.ldp + e];
+        }
+    } else {
+        const __nv_bfloat16 *ht = a.h + t * a.d;
+        for (int i0 = 0; i0 < a.d; ++i0) {
+            const float hv = bf(ht[i0]);
+            const float *wr = a.W_r + (int64_t)i0 * E;
+#pragma unroll
+            for (int i = 0; i < RB_MAXEW; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) z[i] = fmaf(hv, __ldg(wr + e), z[i]);
+            }
+        }
+    }
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < RB_MAXEW; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            if (a.b_r) z[i] += a.b_r[e];
+            zmax = fmaxf(zmax, z[i]);
+        }
+    }
+    zmax = warp_max_f(zmax);
+    float se = 0.f;
+#pragma unroll
+    for (int i = 0; i < RB_MAXEW; ++i) {
+        const int e = lane + 32 * i;
+        p[i] = e < E ? expf(z[i] - zmax) : 0.f;
+        se += p[i];
+    }
+    se = warp_sum_f(se);
+    const float lse = zmax + logf(se);
+#pragma unroll
+    for (int i = 0; i < RB_MAXEW; ++i) {
+        p[i] /= se;
+        dz[i] = 0.f;
+    }
+    // gate gradients: the warp sums slot j's partial rows (and its bias term) in a fixed order
+    float dg_mine = 0.f;  // lane j < k keeps dg_j
+    int e_mine = 0;
+    float g_mine = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        const int64_t sidx = t * a.k + j;
+        const int r = a.slot_of[sidx];
+        const int ej = a.topk_idx[sidx];
+        if (ej < 0 || ej >= E || r >= a.P) report(dev_status, DEV_ERR_INDEX);
+        float v = 0.f;
+        if (r >= 0 && r < a.P && ej >= 0 && ej < E) {
+            for (int q = lane; q < a.n_part; q += 32) v += a.dg_part[(int64_t)q * a.P + r];
+            if (a.b2) {
+                const __nv_bfloat16 *dyt = a.dy + t * a.d;
+                const float *b2e = a.b2 + (int64_t)ej * a.d;
+                for (int o = lane; o < a.d; o += 32) v = fmaf(bf(dyt[o]), b2e[o], v);
+            }
+        }
+        v = warp_sum_f(v);
+        if (lane == j) {
+            dg_mine = v;
+            e_mine = ej < 0 || ej >= E ? 0 : ej;
+            g_mine = a.gates[sidx];
+        }
+    }
+    // the probability p[e_j] of every slot's expert, gathered from its owner lane
+    float pj = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, e_mine, j);
+        float pe = 0.f;
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i)
+            if (ej == lane + 32 * i) pe = p[i];
+        pe = warp_sum_f(pe);
+        if (lane == j) pj = pe;
+    }
+    const bool has = lane < a.k;
+    float add_j;  // dz contribution of slot j at its own expert
+    if (a.raw_prob) {
+        const float S = warp_sum_f(has ? dg_mine * pj : 0.f);
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i) dz[i] = -p[i] * S;
+        add_j = dg_mine * pj;
+    } else {
+        const float S = warp_sum_f(has ? g_mine * dg_mine : 0.f);
+        add_j = g_mine * (dg_mine - S);
+    }
+    for (int j = 0; j < a.k; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, e_mine, j);
+        const float v = __shfl_sync(0xffffffffu, add_j, j);
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i)
+            if (ej == lane + 32 * i) dz[i] += v;
+    }
+    if (a.aux_weight != 0.f) {
+        // dL/dp[t, e] = aux_weight E f_e / T with f_e = counts[e] / (T k)
+        const float scale = a.aux_weight * (float)E / ((float)a.T * (float)a.T * (float)a.k);
+        float c[RB_MAXEW];
+        float sdot = 0.f;
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i) {
+            const int e = lane + 32 * i;
+            c[i] = e < E ? scale * (float)a.counts[e] : 0.f;
+            sdot += c[i] * p[i];
+        }
+        sdot = warp_sum_f(sdot);
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i) dz[i] += p[i] * (c[i] - sdot);
+    }
+    if (a.zloss_weight != 0.f) {
+        const float zs = a.zloss_weight * 2.f / (float)a.T * lse;
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i) dz[i] += zs * p[i];
+    }
+#pragma unroll
+    for (int i = 0; i < RB_MAXEW; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) a.dz[t * E + e] = dz[i];
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// dh[t, i] = sum_j dX[slot_of[t, j], i] + sum_e dz[t, e] W_r[i, e]: 32 tokens x 64 features per
+// block, 8 features per thread; W_r's 64 rows and the tokens' dz in shared memory.
+__global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const int32_t *slot_of,
+                                                 const float *dz, const float *W_r, int64_t T,
+                                                 int d, int E, int k, int64_t rows,
+                                                 __nv_bfloat16 *dh, uint32_t *dev_status) {
+    extern __shared__ float dsm[];
+    float *sW = dsm;               // [E][64]
+    float *sz = dsm + E * BT;      // [32][E]
+    pdl_wait();
+    const int i0 = blockIdx.x * BT;
+    const int64_t t0 = (int64_t)blockIdx.y * 32;
+    for (int x = threadIdx.x; x < E * BT; x += blockDim.x) {
+        const int ii = x / E, e = x - ii * E;  // coalesced over W_r's row i0 + ii
+        sW[e * BT + ii] = W_r[(int64_t)(i0 + ii) * E + e];
+    }
+    for (int x = threadIdx.x; x < 32 * E; x += blockDim.x) {
+        const int tl = x / E;
+        sz[x] = t0 + tl < T ? dz[(t0 + tl) * E + (x - tl * E)] : 0.f;
+    }
+    __syncthreads();
+    const int tl = threadIdx.x >> 3, ch = threadIdx.x & 7;
+    const int64_t t = t0 + tl;
+    if (t < T) {
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int r = slot_of[t * k + j];
+            if (r >= rows) report(dev_status, DEV_ERR_INDEX);
+            if (r < 0 || r >= rows) continue;
+            float v[8];
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(dX + (int64_t)r * d + i0) + ch), v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] += v[q];
+        }
+        const float *zt = sz + tl * E;
+        for (int e = 0; e < E; ++e) {
+            const float ze = zt[e];
+            const float4 w0 = *reinterpret_cast<const float4 *>(sW + e * BT + ch * 8);
+            const float4 w1 = *reinterpret_cast<const float4 *>(sW + e * BT + ch * 8 + 4);
+            acc[0] = fmaf(ze, w0.x, acc[0]);
+            acc[1] = fmaf(ze, w0.y, acc[1]);
+            acc[2] = fmaf(ze, w0.z, acc[2]);
+            acc[3] = fmaf(ze, w0.w, acc[3]);
+            acc[4] = fmaf(ze, w1.x, acc[4]);
+            acc[5] = fmaf(ze, w1.y, acc[5]);
+            acc[6] = fmaf(ze, w1.z, acc[6]);
+            acc[7] = fmaf(ze, w1.w, acc[7]);
+        }
+        *reinterpret_cast<uint4 *>(dh + t * d + i0 + ch * 8) =
+            make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
+                       pack2(acc[6], acc[7]));
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// dW_r partial sums: block (x, y) adds h[t, i] dz[t, e] over tokens [y ts, (y + 1) ts) for 64
+// features i into part[y][i][e]; the blocks of x = 0 also sum dz into partb[y][e] (db_r).
+// Thread: feature i0 + tid % 64, experts [g EQ, g EQ + EQ) with g = tid / 64.
+template <int EQ>
+__global__ void __launch_bounds__(256) dwr_part_kernel(const __nv_bfloat16 *h, const float *dz,
+                                                       int64_t T, int d, int E, int64_t ts,
+                                                       float *part, float *partb) {
+    extern __shared__ float dsm[];
+    float *sh = dsm;             // [32][64]
+    float *sz = dsm + 32 * BT;   // [32][E]
+    pdl_wait();
+    const int i0 = blockIdx.x * BT;
+    const int ci = threadIdx.x & 63, g = threadIdx.x >> 6;
+    const int eb = g * EQ;
+    const int64_t ta = (int64_t)blockIdx.y * ts;
+    const int64_t tb = ta + ts < T ? ta + ts : T;
+    const bool bias = blockIdx.x == 0 && partb != nullptr;
+    float acc[EQ], accb[EQ];
+#pragma unroll
+    for (int q = 0; q < EQ; ++q) acc[q] = accb[q] = 0.f;
+    for (int64_t t0 = ta; t0 < tb; t0 += 32) {
+        __syncthreads();
+        {
+            const int tl = threadIdx.x >> 3, ch = threadIdx.x & 7;
+            float v[8];
+            if (t0 + tl < tb) {
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(h + (t0 + tl) * d + i0) + ch), v);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sh[tl * BT + ch * 8 + q] = v[q];
+        }
+        for (int x = threadIdx.x; x < 32 * E; x += blockDim.x) {
+            const int tl = x / E;
+            sz[x] = t0 + tl < tb ? dz[(t0 + tl) * E + (x - tl * E)] : 0.f;
+        }
+        __syncthreads();
+        for (int tl = 0; tl < 32; ++tl) {
+            const float hv = sh[tl * BT + ci];
+            const float *zt = sz + tl * E + eb;
+#pragma unroll
+            for (int q = 0; q < EQ; ++q)
+                if (eb + q < E) acc[q] = fmaf(hv, zt[q], acc[q]);
+            if (bias) {
+#pragma unroll
+                for (int q = 0; q < EQ; ++q)
+                    if (eb + q < E) accb[q] += zt[q];
+            }
+        }
+    }
+    float *out = part + (int64_t)blockIdx.y * d * E + (int64_t)(i0 + ci) * E;
+#pragma unroll
+    for (int q = 0; q < EQ; ++q)
+        if (eb + q < E) out[eb + q] = acc[q];
+    if (bias && ci == 0) {
+#pragma unroll
+        for (int q = 0; q < EQ; ++q)
+            if (eb + q < E) partb[(int64_t)blockIdx.y * E + eb + q] = accb[q];
+    }
+    pdl_trigger();
+}
+
+// out[x] = sum_{s < nsplit} part[s][x] for x < n (in split order); outb likewise over E.
+__global__ void __launch_bounds__(256) split_sum_kernel(const float *part, int nsplit, int64_t n,
+                                                        float *out, const float *partb, int E,
+                                                        float *outb) {
+    pdl_wait();
+    const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x < n) {
+        float v = 0.f;
+        for (int s = 0; s < nsplit; ++s) v += part[(int64_t)s * n + x];
+        out[x] = v;
+    }
+    if (outb && x < E) {
+        float v = 0.f;
+        for (int s = 0; s < nsplit; ++s) v += partb[(int64_t)s * E + x];
+        outb[x] = v;
+    }
+    pdl_trigger();
+}
+
+// Bias gradients from the per-column-tile sums: out[e][n] = sum over the 64-column tiles of
+// segment e of part[tile][n] (zero for an expert without slots).
+__global__ void __launch_bounds__(256) seg_sum_kernel(const float *part, int width,
+                                                      const int32_t *kseg, int E, float *out) {
+    pdl_wait();
+    const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x < (int64_t)E * width) {
+        const int e = (int)(x / width), n = (int)(x - (int64_t)e * width);
+        float v = 0.f;
+        for (int c = kseg[e] / BT; c < kseg[e + 1] / BT; ++c) v += part[(int64_t)c * width + n];
+        out[x] = v;
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+
+size_t al(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+struct BwdLayout {
+    size_t gate_r, kseg, W2T, WT, A1, A3, dHu, dA, dA1T, dA3T, HT, dX, XT, dYsT, dg_part,
+        db1_part, db2_part, dz, dwr_part, dwr_partb, total;
+    int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
+    int K2, n_part, nsplit;
+    int64_t ts;  // tokens per dW_r split
+};
+
+BwdLayout bwd_layout(const moe_config_t &c) {
+    BwdLayout L = {};
+    const int64_t P = c.T * c.k;
+    const bool sw = c.act == MOE_ACT_SWIGLU;
+    L.kw = (P + BT - 1) / BT * BT + (int64_t)BT * c.E;
+    L.K2 = sw ? 2 * c.f : c.f;
+    L.n_part = c.f / BT;
+    const int tiles_x = c.d / BT;
+    int64_t ns = (2 * 148 + tiles_x - 1) / tiles_x;
+    const int64_t tmax = (c.T + 31) / 32;
+    if (ns > tmax) ns = tmax;
+    if (ns < 1) ns = 1;
+    L.ts = ((c.T + ns - 1) / ns + 31) / 32 * 32;
+    if (L.ts < 32) L.ts = 32;
+    L.nsplit = (int)((c.T + L.ts - 1) / L.ts);
+    if (L.nsplit < 1) L.nsplit = 1;
+    const size_t E = (size_t)c.E, d = (size_t)c.d, f = (size_t)c.f, kw = (size_t)L.kw;
+    const size_t nt = kw / BT;
+    size_t off = 0;
+    L.gate_r = off;     off = al(off + (size_t)P * 4);
+    L.kseg = off;       off = al(off + (E + 1) * 4);
+    L.W2T = off;        off = al(off + E * f * d * 2);
+    L.WT = off;         off = al(off + E * d * (size_t)L.K2 * 2);
+    L.A1 = off;         off = al(off + (size_t)P * f * 2);
+    L.A3 = off;         off = al(off + (sw ? (size_t)P * f * 2 : 0));
+    L.dHu = off;        off = al(off + (size_t)P * f * 2);
+    L.dA = off;         off = al(off + (size_t)P * (size_t)L.K2 * 2);
+    L.dA1T = off;       off = al(off + f * kw * 2);
+    L.dA3T = off;       off = al(off + (sw ? f * kw * 2 : 0));
+    L.HT = off;         off = al(off + f * kw * 2);
+    L.dX = off;         off = al(off + (size_t)P * d * 2);
+    L.XT = off;         off = al(off + d * kw * 2);
+    L.dYsT = off;       off = al(off + d * kw * 2);
+    L.dg_part = off;    off = al(off + (size_t)L.n_part * (size_t)P * 4);
+    L.db1_part = off;   off = al(off + (c.has_bias ? nt * f * 4 : 0));
+    L.db2_part = off;   off = al(off + (c.has_bias ? nt * d * 4 : 0));
+    L.dz = off;         off = al(off + (size_t)c.T * E * 4);
+    L.dwr_part = off;   off = al(off + (size_t)L.nsplit * d * E * 4);
+    L.dwr_partb = off;  off = al(off + (size_t)L.nsplit * E * 4);
+    L.total = off;
+    return L;
+}
+
+template <int EQ>
+cudaError_t launch_dwr(const moe_config_t &c, const BwdLayout &L, const void *h, const float *dz,
+                       float *part, float *partb, cudaStream_t s) {
+    const size_t smem = (size_t)(32 * BT + 32 * c.E) * 4;
+    cudaError_t err = set_max_dynamic_smem((const void *)dwr_part_kernel<EQ>, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(dwr_part_kernel<EQ>, dim3(c.d / BT, L.nsplit), dim3(256), smem, s, 1,
+                      static_cast<const __nv_bfloat16 *>(h), dz, c.T, c.d, c.E, L.ts, part, partb);
+}
+
+bool al16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
+bool al4(const void *p) { return p && ((uintptr_t)p & 3u) == 0; }
+
+}  // namespace
+
+int backward_launches(const moe_config_t &c) {
+    if (c.T == 0) return 0;
+    const bool sw = c.act == MOE_ACT_SWIGLU;
+    const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
+    return 1 /*prep*/ + (sw ? 3 : 2) /*weight transposes*/ + (sw ? 2 : 1) /*A1, A3*/ +
+           1 /*dHu*/ + 1 /*act*/ + 1 /*dX*/ + 1 /*gather-transpose*/ + (sw ? 3 : 2) /*dW*/ +
+           router + 1 /*router bwd*/ + 1 /*dh*/ + 2 /*dW_r*/ + (c.has_bias ? 2 : 0);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes) {
+    const moe_status_t st = validate_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    *bytes = bwd_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t *kernels) {
+    const moe_status_t st = validate_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!kernels) return MOE_ERR_INVALID_ARG;
+    if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    *kernels = backward_launches(*cfg);
+    return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W_r,
+                          const float *b_r, const void *W1, const float *b1, const void *W3,
+                          const void *W2, const float *b2, const int32_t *topk_idx,
+                          const int32_t *counts, const void *dy, float aux_weight,
+                          float zloss_weight, void *dh, float *dW_r, float *db_r, void *dW1,
+                          float *db1, void *dW3, void *dW2, float *db2, void *ws, size_t ws_bytes,
+                          void *bws, size_t bws_bytes, void *stream) {
+    moe_status_t st = validate_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config_t &c = *cfg;
+    if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    const bool sw = c.act == MOE_ACT_SWIGLU;
+    if (!isfinite(aux_weight) || !isfinite(zloss_weight)) return MOE_ERR_INVALID_ARG;
+    if (!al16(ws) || !al16(bws) || !al4(dW_r) || !al16(dW1) || !al16(dW2) ||
+        (sw && !al16(dW3)) || ((b_r != nullptr) != (db_r != nullptr)) || (db_r && !al4(db_r)) ||
+        (c.has_bias && (!al4(db1) || !al4(db2) || !al4(b1) || !al4(b2))))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    const BwdLayout B = bwd_layout(c);
+    if (ws_bytes < L.total || bws_bytes < B.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t E = c.E, d = c.d, f = c.f;
+    if (c.T == 0) {
+        // no tokens: every gradient is zero
+        cudaError_t e = cudaMemsetAsync(dW_r, 0, (size_t)d * E * 4, s);
+        if (e == cudaSuccess && db_r) e = cudaMemsetAsync(db_r, 0, (size_t)E * 4, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW1, 0, (size_t)(E * f * d) * 2, s);
+        if (e == cudaSuccess && sw) e = cudaMemsetAsync(dW3, 0, (size_t)(E * f * d) * 2, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, (size_t)(E * f * d) * 2, s);
+        if (e == cudaSuccess && c.has_bias) e = cudaMemsetAsync(db1, 0, (size_t)(E * f) * 4, s);
+        if (e == cudaSuccess && c.has_bias) e = cudaMemsetAsync(db2, 0, (size_t)(E * d) * 4, s);
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    if (!al16(h) || !al4(W_r) || (b_r && !al4(b_r)) || !al16(W1) || !al16(W2) ||
+        (sw && !al16(W3)) || !al16(dy) || !al16(dh) || (topk_idx && !al4(topk_idx)) ||
+        (counts && !al4(counts)))
+        return MOE_ERR_INVALID_ARG;
+    char *w = static_cast<char *>(ws);
+    char *b = static_cast<char *>(bws);
+    uint32_t *dev_status = reinterpret_cast<uint32_t *>(w + L.status);
+    const int32_t *idx = topk_idx ? topk_idx : reinterpret_cast<const int32_t *>(w + L.topk_idx);
+    const int32_t *cnt = counts ? counts : reinterpret_cast<const int32_t *>(w + L.counts);
+    const float *gates = reinterpret_cast<const float *>(w + L.gates);
+    const int32_t *offsets = reinterpret_cast<const int32_t *>(w + L.offsets);
+    const int32_t *sorted_token = reinterpret_cast<const int32_t *>(w + L.sorted_token);
+    const int32_t *slot_of = reinterpret_cast<const int32_t *>(w + L.slot_of);
+    const bool have_xperm = !c.fuse_gather;
+    const int64_t P = c.T * c.k;
+    auto bf = [&](size_t o) { return reinterpret_cast<__nv_bfloat16 *>(b + o); };
+    auto fl = [&](size_t o) { return reinterpret_cast<float *>(b + o); };
+    float *gate_r = fl(B.gate_r);
+    int32_t *kseg = reinterpret_cast<int32_t *>(b + B.kseg);
+    const auto *Wb1 = static_cast<const __nv_bfloat16 *>(W1);
+    const auto *Wb3 = static_cast<const __nv_bfloat16 *>(W3);
+    const auto *Wb2 = static_cast<const __nv_bfloat16 *>(W2);
+    cudaError_t e;
+#define MOE_TRY(x)                                   \
+    do {                                             \
+        if ((e = (x)) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+    // 1. sorted-row gates and the padded segment offsets
+    MOE_TRY(launch_pdl(bwd_prep_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0, s, 1,
+                       slot_of, gates, offsets, P, c.E, gate_r, kseg, dev_status));
+    // 2. transposed weights: W2T [E, f, d]; WT [E, d, K2] = [W1^T | W3^T]
+    MOE_TRY(launch_pdl(transpose_kernel, dim3(c.f / BT, c.d / BT, c.E), dim3(256), 0, s, 1, Wb2,
+                       c.d, c.f, bf(B.W2T), c.d, 0));
+    MOE_TRY(launch_pdl(transpose_kernel, dim3(c.d / BT, c.f / BT, c.E), dim3(256), 0, s, 1, Wb1,
+                       c.f, c.d, bf(B.WT), B.K2, 0));
+    if (sw)
+        MOE_TRY(launch_pdl(transpose_kernel, dim3(c.d / BT, c.f / BT, c.E), dim3(256), 0, s, 1,
+                           Wb3, c.f, c.d, bf(B.WT), B.K2, c.f));
+    // 3. recomputed pre-activations A1 = X W1^T (+ b1), A3 = X W3^T
+    const void *xa = have_xperm ? static_cast<const void *>(w + L.x_perm) : h;
+    const int32_t *xrows = have_xperm ? nullptr : sorted_token;
+    MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W1, P, c.E, c.d, c.f, offsets,
+                             c.has_bias ? b1 : nullptr, bf(B.A1), dev_status, s));
+    if (sw)
+        MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W3, P, c.E, c.d, c.f, offsets, nullptr,
+                                 bf(B.A3), dev_status, s));
+    // 4. dHu = dy[token] W2_e (rows of dy gathered through sorted_token)
+    MOE_TRY(launch_gemm_rows(dy, sorted_token, c.T, bf(B.W2T), P, c.E, c.d, c.f, offsets,
+                             nullptr, bf(B.dHu), dev_status, s));
+    // 5. activation backward: dA, dA1T, dA3T, HT, dg parts, db1 parts
+    ActBwd ab;
+    ab.A1 = bf(B.A1);
+    ab.A3 = sw ? bf(B.A3) : nullptr;
+    ab.dHu = bf(B.dHu);
+    ab.gate_r = gate_r;
+    ab.offsets = offsets;
+    ab.kseg = kseg;
+    ab.dA = bf(B.dA);
+    ab.dA1T = bf(B.dA1T);
+    ab.dA3T = sw ? bf(B.dA3T) : nullptr;
+    ab.HT = bf(B.HT);
+    ab.dg_part = fl(B.dg_part);
+    ab.db1_part = c.has_bias ? fl(B.db1_part) : nullptr;
+    ab.P = P;
+    ab.kw = B.kw;
+    ab.E = c.E;
+    ab.f = c.f;
+    ab.swiglu = sw ? 1 : 0;
+    MOE_TRY(launch_pdl(act_bwd_kernel, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256), 0, s, 1,
+                       ab, dev_status));
+    // 6. dX = dA [W1 | W3] (one GEMM over K2)
+    MOE_TRY(launch_gemm_rows(bf(B.dA), nullptr, 0, bf(B.WT), P, c.E, B.K2, c.d, offsets, nullptr,
+                             bf(B.dX), dev_status, s));
+    // 7. XT and dYsT = (g dy[token])^T in the padded slot layout (+ db2 parts)
+    GatherT gx{static_cast<const __nv_bfloat16 *>(h), nullptr, bf(B.XT), nullptr};
+    GatherT gy{static_cast<const __nv_bfloat16 *>(dy), gate_r, bf(B.dYsT),
+               c.has_bias ? fl(B.db2_part) : nullptr};
+    MOE_TRY(launch_pdl(gather_transpose_kernel, dim3((unsigned)(B.kw / BT), c.d / BT, 2),
+                       dim3(256), 0, s, 1, gx, gy, sorted_token, offsets,
+                       static_cast<const int32_t *>(kseg), c.E, c.T, P, c.d, B.kw, dev_status));
+    // 8. weight gradients over each expert's slots
+    MOE_TRY(launch_gemm_kgroup(bf(B.dYsT), bf(B.HT), kseg, c.E, c.d, c.f, B.kw, dW2, dev_status,
+                               s));
+    MOE_TRY(launch_gemm_kgroup(bf(B.dA1T), bf(B.XT), kseg, c.E, c.f, c.d, B.kw, dW1, dev_status,
+                               s));
+    if (sw)
+        MOE_TRY(launch_gemm_kgroup(bf(B.dA3T), bf(B.XT), kseg, c.E, c.f, c.d, B.kw, dW3,
+                                   dev_status, s));
+    // 9. router: logits (tensor-core partials when the forward used them), dz
+    RouterBwd rb;
+    rb.h = static_cast<const __nv_bfloat16 *>(h);
+    rb.dy = static_cast<const __nv_bfloat16 *>(dy);
+    rb.W_r = W_r;
+    rb.b_r = b_r;
+    rb.b2 = c.has_bias ? b2 : nullptr;
+    rb.part = nullptr;
+    rb.S = 0;
+    rb.ldp = 0;
+    if (router_launches(c) == 3) {
+        void *scratch = w + L.router;
+        MOE_TRY(launch_router_tc(c, h, W_r, scratch, dev_status, s));
+        rb.part = router_tc_logits(scratch, c);
+        rb.S = router_tc_splits(c);
+        rb.ldp = router_tc_epad(c);
+    }
+    rb.topk_idx = idx;
+    rb.slot_of = slot_of;
+    rb.counts = cnt;
+    rb.gates = gates;
+    rb.dg_part = fl(B.dg_part);
+    rb.n_part = B.n_part;
+    rb.T = c.T;
+    rb.P = P;
+    rb.d = c.d;
+    rb.E = c.E;
+    rb.k = c.k;
+    rb.raw_prob = c.gate == MOE_GATE_RAW_PROB ? 1 : 0;
+    rb.aux_weight = aux_weight;
+    rb.zloss_weight = zloss_weight;
+    rb.dz = fl(B.dz);
+    MOE_TRY(launch_pdl(router_bwd_kernel, dim3((unsigned)((c.T + 7) / 8)), dim3(256), 0, s, 1, rb,
+                       dev_status));
+    // 10. dh = sum_j dX[slot] + dz W_r^T
+    {
+        const size_t smem = (size_t)(BT * c.E + 32 * c.E) * 4;
+        MOE_TRY(set_max_dynamic_smem((const void *)dh_kernel, smem));
+        MOE_TRY(launch_pdl(dh_kernel, dim3(c.d / BT, (unsigned)((c.T + 31) / 32)), dim3(256), smem,
+                           s, 1, static_cast<const __nv_bfloat16 *>(bf(B.dX)), slot_of,
+                           static_cast<const float *>(fl(B.dz)), W_r, c.T, c.d, c.E, c.k, P,
+                           static_cast<__nv_bfloat16 *>(dh), dev_status));
+    }
+    // 11. dW_r = h^T dz, db_r = sum dz (split over tokens, then summed in split order)
+    {
+        const int eq = (c.E + 3) / 4;
+        float *part = fl(B.dwr_part), *partb = b_r ? fl(B.dwr_partb) : nullptr;
+        const float *dz = fl(B.dz);
+        if (eq <= 2) MOE_TRY(launch_dwr<2>(c, B, h, dz, part, partb, s));
+        else if (eq <= 8) MOE_TRY(launch_dwr<8>(c, B, h, dz, part, partb, s));
+        else if (eq <= 16) MOE_TRY(launch_dwr<16>(c, B, h, dz, part, partb, s));
+        else if (eq <= 32) MOE_TRY(launch_dwr<32>(c, B, h, dz, part, partb, s));
+        else MOE_TRY(launch_dwr<64>(c, B, h, dz, part, partb, s));
+        const int64_t n = d * E;
+        MOE_TRY(launch_pdl(split_sum_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
+                           static_cast<const float *>(part), B.nsplit, n, dW_r,
+                           static_cast<const float *>(partb), c.E, db_r));
+    }
+    // 12. bias gradients
+    if (c.has_bias) {
+        MOE_TRY(launch_pdl(seg_sum_kernel, dim3((unsigned)((E * f + 255) / 256)), dim3(256), 0, s,
+                           1, static_cast<const float *>(fl(B.db1_part)), c.f,
+                           static_cast<const int32_t *>(kseg), c.E, db1));
+        MOE_TRY(launch_pdl(seg_sum_kernel, dim3((unsigned)((E * d + 255) / 256)), dim3(256), 0, s,
+                           1, static_cast<const float *>(fl(B.db2_part)), c.d,
+                           static_cast<const int32_t *>(kseg), c.E, db2));
+    }
+#undef MOE_TRY
+    return MOE_OK;
+}
+
+}  // extern "C"

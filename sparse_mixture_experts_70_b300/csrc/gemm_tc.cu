@@ -82,6 +82,11 @@ struct TcArgs {
     // out_token[r], scaled by out_gate[out_token[r]]
     const int32_t *out_token;
     const float *out_gate;
+    // K-grouped mode (the weight gradients of the backward): unit (e, n, m) is the 128 x 256
+    // tile (m, n) of expert e's [M, N] output, rows e M + m 128 of out [E M, N]; it sums A and B
+    // columns [offsets[e], offsets[e+1]) -- multiples of 64, zero-padded -- of A [M, K] and
+    // B [N, K] (K: the padded width). m_tiles = ceil(M / 128).
+    int M, m_tiles;
 };
 
 // The 4 source rows this lane gathers for tile ti (rows 4 lane .. 4 lane + 3 of the tile);
@@ -104,6 +109,19 @@ __device__ __forceinline__ int4 gather_rows(const TcArgs &a, int row0, int rows,
 struct Tile {
     int e, n, row0, rows;  // rows <= 0: nothing to compute (the idle half of a CTA pair)
 };
+// Unit t of the K-grouped schedule: expert-major, then N tile, then M tile; row0 is the output
+// row (e M + m 128), rows the valid rows of the tile.
+__device__ __forceinline__ Tile decode_tile_kg(int t, const TcArgs &a) {
+    const int per = a.m_tiles * a.n_tiles;
+    Tile ti;
+    ti.e = t / per;
+    const int local = t - ti.e * per;
+    ti.n = local / a.m_tiles;
+    const int m = local - ti.n * a.m_tiles;
+    ti.row0 = ti.e * a.M + m * BM;
+    ti.rows = min(BM, a.M - m * BM);
+    return ti;
+}
 // Unit t of the schedule. s_cum[e] is the first unit of expert e (E+1 entries); within an
 // expert, units run N-major, M-minor. A unit is one 128-row M tile, or -- for a CTA pair -- two
 // adjacent M tiles, of which CTA `rank` takes the first or the second. eh only moves forward.
@@ -157,9 +175,12 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap *tmO, uint32_t
 // ti into bf16 outputs: half the tile's columns per thread (`half`), bias / GELU / SwiGLU in f32.
 // Every tcgen05.ld here is executed by the whole warp; only the stores depend on the row. A warp
 // whose 32 rows are all valid stores through its staging buffer `stg` with TMA (when a.tma_out).
+// zero: the tile summed nothing (an expert with no slots in K-grouped mode) and stores zeros
+// without reading the accumulator.
 __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, uint32_t tmem_base,
                                               uint32_t acc_col, int q, int lane, int half,
-                                              const CUtensorMap *tmO, uint32_t stg) {
+                                              const CUtensorMap *tmO, uint32_t stg,
+                                              bool zero = false) {
     const int r = q * 32 + lane;
     const bool valid = r < ti.rows;
     const bool boxed = a.tma_out && q * 32 + 32 <= ti.rows;  // warp-uniform
@@ -202,7 +223,12 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
             const int col = ti.n * BN + c;
             if (col >= a.N) break;  // warp-uniform
             float v[32];
-            tmem_ld32(trow + c, v);
+            if (zero) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            } else {
+                tmem_ld32(trow + c, v);
+            }
             if (a.bias) {
                 const float *bp = a.bias + (int64_t)ti.e * a.N + col;
 #pragma unroll
@@ -234,7 +260,8 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
     }
 }
 
-// One CTA per SM; see the file comment.
+// One CTA per SM; see the file comment. KG: the K-grouped schedule (TcArgs).
+template <bool KG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -283,21 +310,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tmem_relinquish();
     }
     if (warp == 2 && lane == 0) {
-        int cum = 0;
-        bool bad = false;
-        for (int e = 0; e < E; ++e) {
-            const int lo = a.offsets[e], hi = a.offsets[e + 1];
-            if (lo < 0 || hi < lo || (int64_t)hi > a.P) bad = true;
-            s_off[e] = lo;
-            s_cum[e] = cum;
-            const int mt = (hi - lo + BM - 1) / BM;
-            if (!bad) cum += mt * a.n_tiles;
-        }
-        s_off[E] = a.offsets[E];
-        s_cum[E] = cum;
-        if (bad) {
-            report(a.dev_status, DEV_ERR_INDEX);
-            for (int e = 0; e <= E; ++e) s_cum[e] = 0;
+        if (KG) {
+            // K segments: multiples of BK, ascending, within the operands' width
+            bool bad = a.offsets[0] != 0;
+            for (int e = 0; e <= E; ++e) {
+                const int v = a.offsets[e];
+                if (v < 0 || v % BK != 0 || (int64_t)v > (int64_t)a.K ||
+                    (e > 0 && v < s_off[e - 1]))
+                    bad = true;
+                s_off[e] = v;
+            }
+            s_cum[E] = bad ? 0 : E * a.m_tiles * a.n_tiles;
+            if (bad) report(a.dev_status, DEV_ERR_INDEX);
+        } else {
+            int cum = 0;
+            bool bad = false;
+            for (int e = 0; e < E; ++e) {
+                const int lo = a.offsets[e], hi = a.offsets[e + 1];
+                if (lo < 0 || hi < lo || (int64_t)hi > a.P) bad = true;
+                s_off[e] = lo;
+                s_cum[e] = cum;
+                const int mt = (hi - lo + BM - 1) / BM;
+                if (!bad) cum += mt * a.n_tiles;
+            }
+            s_off[E] = a.offsets[E];
+            s_cum[E] = cum;
+            if (bad) {
+                report(a.dev_status, DEV_ERR_INDEX);
+                for (int e = 0; e <= E; ++e) s_cum[e] = 0;
+            }
         }
     }
     tc_fence_before();
@@ -316,11 +357,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t issued = 0, last_phase = 0;  // per-stage bits
             bool ok = !a.withhold_loads;
             for (int t = unit0; t < total && ok; t += ustep) {
-                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                const Tile ti = KG ? decode_tile_kg(t, a)
+                                   : decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
                 // B rows of this N tile: SwiGLU stacks 128 rows of W1 over 128 rows of W3
-                const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
-                                                     : ti.e * a.N + ti.n * BN;
-                for (int kb = 0; kb < nk; ++kb) {
+                const int brow = KG ? ti.n * BN
+                                    : (a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
+                                                           : ti.e * a.N + ti.n * BN);
+                const int arow = KG ? ti.row0 - ti.e * a.M : ti.row0;
+                const int kx0 = KG ? s_off[ti.e] : 0;
+                const int nkt = KG ? (s_off[ti.e + 1] - s_off[ti.e]) / BK : nk;
+                for (int kb = 0; kb < nkt; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
@@ -328,13 +374,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t fb = bar_full + 8 * stage;
                     const uint32_t sb = sB + stage * B_STAGE;
                     mbar_expect_tx(fb, A_STAGE + B_STAGE);
-                    tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kb * BK, ti.row0);
+                    const int kx = kx0 + kb * BK;
+                    tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kx, arow);
                     if (a.epi == EPI_SWIGLU) {
-                        tma_load_2d(sb, &tmB, fb, kb * BK, brow);
-                        tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kb * BK, brow);
+                        tma_load_2d(sb, &tmB, fb, kx, brow);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kx, brow);
                     } else {
-                        tma_load_2d(sb, &tmB, fb, kb * BK, brow);
-                        tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kb * BK, brow + BN / 2);
+                        tma_load_2d(sb, &tmB, fb, kx, brow);
+                        tma_load_2d(sb + B_STAGE / 2, &tmB, fb, kx, brow + BN / 2);
                     }
                     issued |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -410,12 +457,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             constexpr uint32_t idesc = idesc_bf16(BM, BN);
             for (int t = unit0; t < total && ok; t += ustep) {
-                const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                const Tile ti = KG ? decode_tile_kg(t, a)
+                                   : decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
                 const bool idle = ti.rows <= 0;
+                const int nkt = KG ? (s_off[ti.e + 1] - s_off[ti.e]) / BK : nk;
                 if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = 0; kb < nkt; ++kb) {
                     if (!mbar_wait(bar_full + 8 * stage, phase, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
@@ -450,14 +499,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < total; t += ustep) {
-            const Tile ti = decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
+            const Tile ti = KG ? decode_tile_kg(t, a)
+                               : decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half, &tmO, stg);
+            const bool zero = KG && s_off[ti.e + 1] == s_off[ti.e];
+            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half, &tmO, stg, zero);
             tc_fence_before();
             mbar_arrive(bar_tempty + 8 * acc);
             acc ^= 1;
@@ -814,6 +865,8 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.a_src_rows = A_src_rows;
     a.out_token = out_token;
     a.out_gate = out_gate;
+    a.M = 0;
+    a.m_tiles = 0;
     // The CTA-pair kernel when experts average at least four M tiles (on an expert's odd last
     // tile the second CTA computes masked rows, a small loss there).
     const int clusters = pair_clusters();
@@ -827,13 +880,69 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
     if (grid > upper) grid = upper;
-    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel, TC_SMEM);
+    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<false>, TC_SMEM);
     if (err != cudaSuccess) return err;
-    return launch_pdl(grouped_gemm_tc_kernel, dim3((unsigned)grid), dim3(TC_THREADS), TC_SMEM, s,
-                      1, mA, mB, mB3, mO, a);
+    return launch_pdl(grouped_gemm_tc_kernel<false>, dim3((unsigned)grid), dim3(TC_THREADS),
+                      TC_SMEM, s, 1, mA, mB, mB3, mO, a);
+}
+
+// K-grouped GEMM: out[e M + m, n] = sum over k in [kseg[e], kseg[e+1]) of A[m, k] B[n, k] for
+// every expert e (zeros where the segment is empty). A [M, kwidth], B [N, kwidth], out [E M, N],
+// all bf16 row-major; kseg [E+1] device int32, multiples of 64, pad columns zero.
+cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, int E, int M, int N,
+                           int64_t kwidth, void *out, uint32_t *dev_status, cudaStream_t s) {
+    if (E <= 0 || M <= 0 || N <= 0 || kwidth <= 0 || kwidth % BK != 0 || kwidth >= (1ll << 31))
+        return cudaErrorInvalidValue;
+    CUtensorMap mA, mB, mO;
+    if (!make_map(&mA, A, M, kwidth, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mB, B, N, kwidth, BN / 2)) return cudaErrorInvalidValue;
+    if (!make_store_map(&mO, out, (int64_t)E * M, N)) return cudaErrorInvalidValue;
+    TcArgs a = {};
+    a.offsets = kseg;
+    a.bias = nullptr;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.dev_status = dev_status;
+    a.P = (int64_t)E * M;
+    a.E = E;
+    a.K = (int)kwidth;
+    a.N = N;
+    a.n_tiles = (N + BN - 1) / BN;
+    a.epi = EPI_STORE;
+    a.spin_limit_ns = SPIN_LIMIT_NS;
+    a.withhold_loads = 0;
+    a.tma_out = MOE_GEMM_TMA_STORE;
+    a.a_rows = nullptr;
+    a.a_src_rows = 0;
+    a.out_token = nullptr;
+    a.out_gate = nullptr;
+    a.M = M;
+    a.m_tiles = (M + BM - 1) / BM;
+    const int64_t units = (int64_t)E * a.m_tiles * a.n_tiles;
+    if (units >= (1ll << 31)) return cudaErrorInvalidValue;
+    int64_t grid = num_sms();
+    if (grid > units) grid = units;
+    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true>, TC_SMEM);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(grouped_gemm_tc_kernel<true>, dim3((unsigned)grid), dim3(TC_THREADS),
+                      TC_SMEM, s, 1, mA, mB, mB, mO, a);
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_rows(const void *A, const int32_t *A_rows, int64_t A_src_rows,
+                             const void *B, int64_t P, int E, int K, int N,
+                             const int32_t *offsets, const float *bias, void *out,
+                             uint32_t *dev_status, cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    return launch_gemm(A, B, nullptr, P, E, K, N, EPI_STORE, offsets, bias, out, dev_status,
+                       FaultHook(), s, A_rows, A_rows ? A_src_rows : 0);
+}
+
+cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,
+                               int N, int64_t kwidth, void *out, uint32_t *dev_status,
+                               cudaStream_t s) {
+    return launch_gemm_kg(A, B, kseg, E, M, N, kwidth, out, dev_status, s);
+}
 
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,
                           const FaultHook &hook) {

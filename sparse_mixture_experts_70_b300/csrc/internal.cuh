@@ -100,6 +100,10 @@ int router_tc_epad(const moe_config_t &c);
 float *router_tc_logits(void *scratch, const moe_config_t &c);
 
 WsLayout ws_layout(const moe_config_t &c);
+// The argument checks every entry point applies to a configuration (MOE_OK when valid).
+moe_status_t validate_config(const moe_config_t *c);
+// Kernels one moe_backward call launches for c (bf16).
+int backward_launches(const moe_config_t &c);
 
 int num_sms();
 
@@ -201,5 +205,19 @@ bool ffn_f32_combine_ok(const moe_config_t &c);
 cudaError_t launch_ffn_f32(const moe_config_t &c, const FfnBufs &b, cudaStream_t s);
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,
                           const FaultHook &hook = FaultHook());
+
+// Row-grouped tensor-core GEMM with a plain store: out[r, n] = A_r . B[e N + n] (+ bias[e, n])
+// for r in expert e's rows [offsets[e], offsets[e+1]); A row r is row A_rows[r] of a
+// [A_src_rows, K] tensor when A_rows is given (TMA gathers), else row r of A [P, K]. bf16.
+cudaError_t launch_gemm_rows(const void *A, const int32_t *A_rows, int64_t A_src_rows,
+                             const void *B, int64_t P, int E, int K, int N,
+                             const int32_t *offsets, const float *bias, void *out,
+                             uint32_t *dev_status, cudaStream_t s);
+// K-grouped tensor-core GEMM (weight gradients): out[e M + m, n] = sum_{k in [kseg[e],
+// kseg[e+1])} A[m, k] B[n, k]; A [M, kwidth], B [N, kwidth] bf16 with zero pad columns; kseg
+// device int32 [E+1], multiples of 64. Empty segments give zero tiles.
+cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,
+                               int N, int64_t kwidth, void *out, uint32_t *dev_status,
+                               cudaStream_t s);
 
 }  // namespace moe

@@ -111,6 +111,12 @@ moe_status_t check_cfg(const moe_config_t *c) {
     return MOE_OK;
 }
 
+}  // namespace
+
+moe_status_t moe::validate_config(const moe_config_t *c) { return check_cfg(c); }
+
+namespace {
+
 bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
 bool aligned4(const void *p) { return p && ((uintptr_t)p & 3u) == 0; }
 

@@ -1,0 +1,126 @@
+"""Parity of moe_backward (through the C ABI) with the oracle's double-precision backward, on the
+GPU's own routing (the expert choice is held fixed in the backward, so the oracle differentiates
+at the GPU's idx). Cases span several row tiles with ragged tails, N and M tiles that are not
+multiples of the tile, capacity drops, a router bias and a selection-only bias, top-1 Switch
+gates with biases, the fused gather (no permuted copy), the tensor-core router, and an expert
+that receives no slot. Every gradient is compared by relative L2 norm against the bf16 bound;
+the auxiliary and z-loss terms are checked on their own with dy = 0."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mixture_experts_70_b300 import binding as B
+from sparse_mixture_experts_70_b300 import workloads as wl
+
+from parity import BF16_REL_L2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dh", "dW_r", "db_r", "dW1", "dW3", "dW2", "db1", "db2")
+
+
+def _case(w, bias_seed=None, zero_expert=False):
+    inputs = wl.generate(w)
+    if bias_seed is not None:
+        inputs = wl.random_biases(w, inputs, bias_seed)
+    if zero_expert:
+        # expert 0 is never chosen: a large negative router bias on its logit
+        b_r = inputs["b_r"].clone() if inputs.get("b_r") is not None else torch.zeros(w.E)
+        b_r[0] = -60.0
+        inputs["b_r"] = b_r
+    return inputs
+
+
+def _dy(w, seed):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randn((w.T, w.d), generator=g).to(torch.bfloat16)
+
+
+def _run(w, inputs, dy, aux_weight, zloss_weight):
+    dev = to_dev(inputs)
+    cfg = B.config_for(w)
+    layer = B.Layer(cfg, dev)
+    layer.forward(dev["h"])
+    # poison the backward workspace: every pad and partial must be written before it is read
+    layer.bws = torch.full((max(B.moe_backward_workspace_size(cfg), 16),), 255, dtype=torch.uint8,
+                           device="cuda")
+    g = layer.backward(dev["h"], dy.cuda(), aux_weight, zloss_weight)
+    torch.cuda.synchronize()
+    assert B.moe_device_status(layer.ws) == B.MOE_OK
+    idx = layer.topk_idx.cpu().numpy()
+    return {k: (v.float().cpu().numpy() if v is not None else None) for k, v in g.items()}, idx
+
+
+def _oracle(w, inputs, idx, dy, aux_weight, zloss_weight):
+    keep = None
+    if w.capacity_factor > 0:
+        C = oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
+        _, _, _, slot_of = oracle.dispatch_capacity(idx, w.E, C)
+        keep = (slot_of >= 0).reshape(w.T, w.k)
+    return oracle.backward(inputs["h"], inputs["W_r"], inputs.get("b_r"), inputs["W1"],
+                           inputs.get("W3"), inputs["W2"], inputs.get("b1"), inputs.get("b2"),
+                           idx, dy, oracle.act_code(w), oracle.gate_code(w), keep=keep,
+                           aux_weight=aux_weight, zloss_weight=zloss_weight)
+
+
+def _rel_l2(a, b):
+    den = float(np.linalg.norm(b))
+    return float(np.linalg.norm(a - b)) / max(den, 1e-30)
+
+
+def _compare(got, ref, bound=BF16_REL_L2, names=GRADS):
+    for name in names:
+        if ref[name] is None:
+            assert got[name] is None, name
+            continue
+        assert got[name].shape == ref[name].shape, name
+        assert np.isfinite(got[name]).all(), name
+        err = _rel_l2(got[name], ref[name])
+        assert err <= bound, (name, err)
+
+
+CASES = [
+    (wl.small("bwd_swiglu_renorm", T=600, d=256, f=384, E=4, k=2, seed=21), {}, 0.0, 0.0),
+    (wl.small("bwd_gelu_bias_raw_top1", T=700, d=192, f=256, E=5, k=1, act=wl.ACT_GELU_TANH,
+              gate=wl.GATE_RAW_PROB, has_bias=True, router_bias_var=1.0, seed=22),
+     dict(bias_seed=5), 0.3, 0.05),
+    (wl.small("bwd_capacity", T=512, d=128, f=256, E=8, k=2, capacity_factor=1.0, seed=23), {},
+     0.2, 0.0),
+    (wl.small("bwd_selbias_top4", T=400, d=128, f=192, E=16, k=4, sel_bias_std=0.5,
+              router_bias_var=0.5, seed=24), {}, 0.1, 0.1),
+    (wl.small("bwd_gather", T=500, d=128, f=256, E=6, k=2, fuse_gather=True, seed=25), {}, 0.0,
+     0.0),
+    (wl.small("bwd_tc_router", T=3000, d=256, f=256, E=8, k=2, seed=26), {}, 0.05, 0.02),
+    (wl.small("bwd_zero_expert", T=300, d=128, f=128, E=6, k=2, seed=27), dict(zero_expert=True),
+     0.0, 0.0),
+]
+
+
+@pytest.mark.parametrize("w,opts,aux_w,z_w", CASES, ids=lambda c: getattr(c, "name", ""))
+def test_backward_matches_oracle(w, opts, aux_w, z_w):
+    inputs = _case(w, **opts)
+    dy = _dy(w, w.seed + 100)
+    got, idx = _run(w, inputs, dy, aux_w, z_w)
+    ref = _oracle(w, inputs, idx, dy, aux_w, z_w)
+    _compare(got, ref)
+    if opts.get("zero_expert"):
+        assert not (idx == 0).any()
+        for name in ("dW1", "dW3", "dW2"):
+            if got[name] is not None:
+                assert (got[name][0] == 0).all(), name
+
+
+@pytest.mark.parametrize("aux_w,z_w", [(1.0, 0.0), (0.0, 1.0)])
+def test_auxiliary_and_zloss_gradients_alone(aux_w, z_w):
+    """dy = 0: only the auxiliary term (through P_i) or only the z-loss reaches the router, and
+    the expert weights get no gradient."""
+    w = wl.small("bwd_aux_only", T=640, d=128, f=128, E=8, k=2, router_bias_var=0.5, seed=28)
+    inputs = _case(w)
+    dy = torch.zeros((w.T, w.d), dtype=torch.bfloat16)
+    got, idx = _run(w, inputs, dy, aux_w, z_w)
+    ref = _oracle(w, inputs, idx, dy, aux_w, z_w)
+    _compare(got, ref, names=("dh", "dW_r", "db_r"))
+    for name in ("dW1", "dW3", "dW2"):
+        assert (got[name] == 0).all(), name
