@@ -88,29 +88,49 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, c
 }
 
 // ---------------------------------------------------------------------------------------------
-// dst[b][c][coff + r] = src[b][r][c] for src [B][R][C], dst rows of ldd elements (bf16). R and C
-// are multiples of 64; one 64 x 64 tile per block through shared memory.
+// dst[b][c][coff + r] = src[b][r][c] for src [B][R][C] and dst rows of ldd elements (bf16; R a
+// multiple of 32, C of 64). One warp per 32 x 64 patch, each lane an 8 x 8 block transposed in
+// registers: rows (2p, 2p+1) of a column pair interleave with one byte permute per word, after
+// which output row c's words are input words picked by index. Loads: 8 lanes read 128
+// contiguous bytes of a row; stores: 4 lanes write 64 contiguous bytes of an output row.
 __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16 *src, int R, int C,
-                                                        __nv_bfloat16 *dst, int ldd, int coff) {
-    __shared__ __nv_bfloat16 tile[BT][BT + 8];
+                                                        __nv_bfloat16 *dst, int ldd, int coff,
+                                                        int64_t patches) {
     pdl_wait();
-    const int c0 = blockIdx.x * BT, r0 = blockIdx.y * BT;
-    const int64_t b = blockIdx.z;
-    const __nv_bfloat16 *s = src + b * (int64_t)R * C;
-    __nv_bfloat16 *d = dst + b * (int64_t)C * ldd;
-    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
-        const int r = i >> 3, ch = i & 7;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(s + (int64_t)(r0 + r) * C + c0) + ch);
-        *reinterpret_cast<uint4 *>(&tile[r][ch * 8]) = v;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
-        const int c = i >> 3, ch = i & 7;
-        __align__(16) __nv_bfloat16 out[8];
+    const int lane = threadIdx.x & 31;
+    const int64_t p = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (p < patches) {
+        const int pc = C / 64;
+        const int64_t per_b = (int64_t)(R / 32) * pc;
+        const int64_t b = p / per_b;
+        const int q = (int)(p - b * per_b);
+        const int r0 = (q / pc) * 32 + 8 * (lane >> 3);
+        const int c0 = (q % pc) * 64 + 8 * (lane & 7);
+        const __nv_bfloat16 *s = src + b * (int64_t)R * C + (int64_t)r0 * C + c0;
+        uint32_t w[8][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) out[j] = tile[ch * 8 + j][c];
-        *reinterpret_cast<uint4 *>(d + (int64_t)(c0 + c) * ldd + coff + r0 + ch * 8) =
-            *reinterpret_cast<const uint4 *>(out);
+        for (int r = 0; r < 8; ++r) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(s + (int64_t)r * C));
+            w[r][0] = v.x;
+            w[r][1] = v.y;
+            w[r][2] = v.z;
+            w[r][3] = v.w;
+        }
+        __nv_bfloat16 *d = dst + b * (int64_t)C * ldd + (int64_t)c0 * ldd + coff + r0;
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) {
+            // output rows 2 cq (low halves) and 2 cq + 1 (high halves): word p = rows 2p, 2p + 1
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int pr = 0; pr < 4; ++pr) {
+                lo[pr] = __byte_perm(w[2 * pr][cq], w[2 * pr + 1][cq], 0x5410);
+                hi[pr] = __byte_perm(w[2 * pr][cq], w[2 * pr + 1][cq], 0x7632);
+            }
+            *reinterpret_cast<uint4 *>(d + (int64_t)(2 * cq) * ldd) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(d + (int64_t)(2 * cq + 1) * ldd) =
+                make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
     }
     pdl_trigger();
 }
@@ -390,14 +410,27 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint
                 for (int s = 0; s < a.S; ++s) z[i] += a.part[((int64_t)s * a.T + t) * a.ldp + e];
         }
     } else {
+        // lanes split d; 8 experts at a time, each partial dot summed over the warp and kept by
+        // the expert's owner lane
         const __nv_bfloat16 *ht = a.h + t * a.d;
-        for (int i0 = 0; i0 < a.d; ++i0) {
-            const float hv = bf(ht[i0]);
-            const float *wr = a.W_r + (int64_t)i0 * E;
+        for (int e0 = 0; e0 < E; e0 += 8) {
+            float pz[8];
 #pragma unroll
-            for (int i = 0; i < RB_MAXEW; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E) z[i] = fmaf(hv, __ldg(wr + e), z[i]);
+            for (int q = 0; q < 8; ++q) pz[q] = 0.f;
+            for (int i0 = lane; i0 < a.d; i0 += 32) {
+                const float hv = bf(ht[i0]);
+                const float *wr = a.W_r + (int64_t)i0 * E + e0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (e0 + q < E) pz[q] = fmaf(hv, __ldg(wr + q), pz[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float v = warp_sum_f(pz[q]);
+                const int e = e0 + q;
+#pragma unroll
+                for (int i = 0; i < RB_MAXEW; ++i)
+                    if (e < E && e == lane + 32 * i) z[i] = v;
             }
         }
     }
@@ -508,84 +541,97 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint
 }
 
 // ---------------------------------------------------------------------------------------------
-// dh[t, i] = sum_j dX[slot_of[t, j], i] + sum_e dz[t, e] W_r[i, e]: 32 tokens x 64 features per
-// block, 8 features per thread; W_r's 64 rows and the tokens' dz in shared memory.
+// dh[t, i] = sum_j dX[slot_of[t, j], i] + sum_e dz[t, e] W_r[i, e]: 64 tokens x 64 features per
+// block; thread (ig = tid % 16, tg = tid / 16) owns tokens 4 tg .. 4 tg + 3 and features
+// 4 ig .. 4 ig + 3 (16 accumulators, two 16-byte shared loads per 16 FMAs). Experts go through
+// shared memory 64 at a time: W_r's 64 rows as sw[e][i] and dz as sz[e][t].
+constexpr int DH_T = 64, DH_ECH = 64, DH_LD = 68;
 __global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const int32_t *slot_of,
                                                  const float *dz, const float *W_r, int64_t T,
                                                  int d, int E, int k, int64_t rows,
                                                  __nv_bfloat16 *dh, uint32_t *dev_status) {
-    extern __shared__ float dsm[];
-    float *sW = dsm;               // [E][64]
-    float *sz = dsm + E * BT;      // [32][E]
+    __shared__ __align__(16) float sw[DH_ECH][BT];
+    __shared__ __align__(16) float sz[DH_ECH][DH_LD];
     pdl_wait();
     const int i0 = blockIdx.x * BT;
-    const int64_t t0 = (int64_t)blockIdx.y * 32;
-    for (int x = threadIdx.x; x < E * BT; x += blockDim.x) {
-        const int ii = x / E, e = x - ii * E;  // coalesced over W_r's row i0 + ii
-        sW[e * BT + ii] = W_r[(int64_t)(i0 + ii) * E + e];
-    }
-    for (int x = threadIdx.x; x < 32 * E; x += blockDim.x) {
-        const int tl = x / E;
-        sz[x] = t0 + tl < T ? dz[(t0 + tl) * E + (x - tl * E)] : 0.f;
-    }
-    __syncthreads();
-    const int tl = threadIdx.x >> 3, ch = threadIdx.x & 7;
-    const int64_t t = t0 + tl;
-    if (t < T) {
-        float acc[8];
+    const int64_t t0 = (int64_t)blockIdx.y * DH_T;
+    const int ig = threadIdx.x & 15, tg = threadIdx.x >> 4;
+    float acc[4][4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    for (int e0 = 0; e0 < E; e0 += DH_ECH) {
+        const int ne = E - e0 < DH_ECH ? E - e0 : DH_ECH;
+        __syncthreads();
+        for (int x = threadIdx.x; x < DH_ECH * BT; x += blockDim.x) {
+            const int ii = x / DH_ECH, e = x - ii * DH_ECH;  // along a row of W_r
+            sw[e][ii] = e < ne ? W_r[(int64_t)(i0 + ii) * E + e0 + e] : 0.f;
+        }
+        for (int x = threadIdx.x; x < DH_ECH * DH_T; x += blockDim.x) {
+            const int tt = x / DH_ECH, e = x - tt * DH_ECH;  // along a row of dz
+            sz[e][tt] = (e < ne && t0 + tt < T) ? dz[(t0 + tt) * E + e0 + e] : 0.f;
+        }
+        __syncthreads();
+        for (int e = 0; e < ne; ++e) {
+            const float4 w4 = *reinterpret_cast<const float4 *>(&sw[e][ig * 4]);
+            const float4 z4 = *reinterpret_cast<const float4 *>(&sz[e][tg * 4]);
+            const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+            const float zv[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(zv[a], wv[b], acc[a][b]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int64_t t = t0 + tg * 4 + a;
+        if (t >= T) break;
         for (int j = 0; j < k; ++j) {
             const int r = slot_of[t * k + j];
             if (r >= rows) report(dev_status, DEV_ERR_INDEX);
             if (r < 0 || r >= rows) continue;
-            float v[8];
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(dX + (int64_t)r * d + i0) + ch), v);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] += v[q];
+            const uint2 u =
+                __ldg(reinterpret_cast<const uint2 *>(dX + (int64_t)r * d + i0 + ig * 4));
+            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+            acc[a][0] += __low2float(p0);
+            acc[a][1] += __high2float(p0);
+            acc[a][2] += __low2float(p1);
+            acc[a][3] += __high2float(p1);
         }
-        const float *zt = sz + tl * E;
-        for (int e = 0; e < E; ++e) {
-            const float ze = zt[e];
-            const float4 w0 = *reinterpret_cast<const float4 *>(sW + e * BT + ch * 8);
-            const float4 w1 = *reinterpret_cast<const float4 *>(sW + e * BT + ch * 8 + 4);
-            acc[0] = fmaf(ze, w0.x, acc[0]);
-            acc[1] = fmaf(ze, w0.y, acc[1]);
-            acc[2] = fmaf(ze, w0.z, acc[2]);
-            acc[3] = fmaf(ze, w0.w, acc[3]);
-            acc[4] = fmaf(ze, w1.x, acc[4]);
-            acc[5] = fmaf(ze, w1.y, acc[5]);
-            acc[6] = fmaf(ze, w1.z, acc[6]);
-            acc[7] = fmaf(ze, w1.w, acc[7]);
-        }
-        *reinterpret_cast<uint4 *>(dh + t * d + i0 + ch * 8) =
-            make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
-                       pack2(acc[6], acc[7]));
+        *reinterpret_cast<uint2 *>(dh + t * d + i0 + ig * 4) =
+            make_uint2(pack2(acc[a][0], acc[a][1]), pack2(acc[a][2], acc[a][3]));
     }
     pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------------------
-// dW_r partial sums: block (x, y) adds h[t, i] dz[t, e] over tokens [y ts, (y + 1) ts) for 64
-// features i into part[y][i][e]; the blocks of x = 0 also sum dz into partb[y][e] (db_r).
-// Thread: feature i0 + tid % 64, experts [g EQ, g EQ + EQ) with g = tid / 64.
-template <int EQ>
+// dW_r partial sums: block (x, y, z) adds h[t, i] dz[t, e] over the tokens [y ts, (y + 1) ts)
+// for features [64 x, 64 x + 64) and experts [z 16 EPT, (z + 1) 16 EPT) into part[y][i][e];
+// thread (ig = tid % 16, eg = tid / 16) owns 4 features x EPT experts. The blocks of x = 0 also
+// sum dz over their tokens into partb[y][e] (db_r).
+template <int EPT>
 __global__ void __launch_bounds__(256) dwr_part_kernel(const __nv_bfloat16 *h, const float *dz,
                                                        int64_t T, int d, int E, int64_t ts,
                                                        float *part, float *partb) {
-    extern __shared__ float dsm[];
-    float *sh = dsm;             // [32][64]
-    float *sz = dsm + 32 * BT;   // [32][E]
+    constexpr int ETILE = 16 * EPT;
+    __shared__ __align__(16) float sh[32][BT];
+    __shared__ __align__(16) float sz[32][ETILE];
     pdl_wait();
     const int i0 = blockIdx.x * BT;
-    const int ci = threadIdx.x & 63, g = threadIdx.x >> 6;
-    const int eb = g * EQ;
+    const int e0 = blockIdx.z * ETILE;
+    const int ig = threadIdx.x & 15, eg = threadIdx.x >> 4;
     const int64_t ta = (int64_t)blockIdx.y * ts;
     const int64_t tb = ta + ts < T ? ta + ts : T;
-    const bool bias = blockIdx.x == 0 && partb != nullptr;
-    float acc[EQ], accb[EQ];
+    const bool bias = blockIdx.x == 0 && partb != nullptr && (int)threadIdx.x < ETILE;
+    float acc[4][EPT];
 #pragma unroll
-    for (int q = 0; q < EQ; ++q) acc[q] = accb[q] = 0.f;
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < EPT; ++b) acc[a][b] = 0.f;
+    float accb = 0.f;
     for (int64_t t0 = ta; t0 < tb; t0 += 32) {
         __syncthreads();
         {
@@ -598,35 +644,49 @@ __global__ void __launch_bounds__(256) dwr_part_kernel(const __nv_bfloat16 *h, c
                 for (int q = 0; q < 8; ++q) v[q] = 0.f;
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sh[tl * BT + ch * 8 + q] = v[q];
+            for (int q = 0; q < 8; ++q) sh[tl][ch * 8 + q] = v[q];
         }
-        for (int x = threadIdx.x; x < 32 * E; x += blockDim.x) {
-            const int tl = x / E;
-            sz[x] = t0 + tl < tb ? dz[(t0 + tl) * E + (x - tl * E)] : 0.f;
+        for (int x = threadIdx.x; x < 32 * ETILE; x += blockDim.x) {
+            const int tl = x / ETILE, e = x - tl * ETILE;
+            sz[tl][e] = (t0 + tl < tb && e0 + e < E) ? dz[(t0 + tl) * E + e0 + e] : 0.f;
         }
         __syncthreads();
+#pragma unroll 4
         for (int tl = 0; tl < 32; ++tl) {
-            const float hv = sh[tl * BT + ci];
-            const float *zt = sz + tl * E + eb;
+            const float4 h4 = *reinterpret_cast<const float4 *>(&sh[tl][ig * 4]);
+            const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
+            float zv[EPT];
+            if constexpr (EPT % 4 == 0) {
 #pragma unroll
-            for (int q = 0; q < EQ; ++q)
-                if (eb + q < E) acc[q] = fmaf(hv, zt[q], acc[q]);
-            if (bias) {
+                for (int b = 0; b < EPT; b += 4) {
+                    const float4 z4 = *reinterpret_cast<const float4 *>(&sz[tl][eg * EPT + b]);
+                    zv[b] = z4.x;
+                    zv[b + 1] = z4.y;
+                    zv[b + 2] = z4.z;
+                    zv[b + 3] = z4.w;
+                }
+            } else {
 #pragma unroll
-                for (int q = 0; q < EQ; ++q)
-                    if (eb + q < E) accb[q] += zt[q];
+                for (int b = 0; b < EPT; ++b) zv[b] = sz[tl][eg * EPT + b];
             }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < EPT; ++b) acc[a][b] = fmaf(hv[a], zv[b], acc[a][b]);
         }
+        if (bias)
+            for (int tl = 0; tl < 32; ++tl) accb += sz[tl][threadIdx.x];
     }
-    float *out = part + (int64_t)blockIdx.y * d * E + (int64_t)(i0 + ci) * E;
+    float *out = part + (int64_t)blockIdx.y * d * E;
 #pragma unroll
-    for (int q = 0; q < EQ; ++q)
-        if (eb + q < E) out[eb + q] = acc[q];
-    if (bias && ci == 0) {
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int q = 0; q < EQ; ++q)
-            if (eb + q < E) partb[(int64_t)blockIdx.y * E + eb + q] = accb[q];
-    }
+        for (int b = 0; b < EPT; ++b) {
+            const int e = e0 + eg * EPT + b;
+            if (e < E) out[(int64_t)(i0 + ig * 4 + a) * E + e] = acc[a][b];
+        }
+    if (bias && e0 + (int)threadIdx.x < E)
+        partb[(int64_t)blockIdx.y * E + e0 + threadIdx.x] = accb;
     pdl_trigger();
 }
 
@@ -669,8 +729,12 @@ __global__ void __launch_bounds__(256) seg_sum_kernel(const float *part, int wid
 
 size_t al(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
+// dW_r kernel shape: experts per thread and expert tiles of 16 EPT
+int dwr_ept(int E) { return E <= 16 ? 1 : E <= 32 ? 2 : E <= 64 ? 4 : 8; }
+int dwr_etiles(int E) { return (E + 16 * dwr_ept(E) - 1) / (16 * dwr_ept(E)); }
+
 struct BwdLayout {
-    size_t gate_r, kseg, W2T, WT, A1, A3, dHu, dA, dA1T, dA3T, HT, dX, XT, dYsT, dg_part,
+    size_t gate_r, kseg, W2T, WT, A1, A3, dHu, dYu, dA, dA1T, dA3T, HT, dX, XT, dYsT, dg_part,
         db1_part, db2_part, dz, dwr_part, dwr_partb, total;
     int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
     int K2, n_part, nsplit;
@@ -684,7 +748,7 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     L.kw = (P + BT - 1) / BT * BT + (int64_t)BT * c.E;
     L.K2 = sw ? 2 * c.f : c.f;
     L.n_part = c.f / BT;
-    const int tiles_x = c.d / BT;
+    const int tiles_x = c.d / BT * dwr_etiles(c.E);
     int64_t ns = (2 * 148 + tiles_x - 1) / tiles_x;
     const int64_t tmax = (c.T + 31) / 32;
     if (ns > tmax) ns = tmax;
@@ -703,6 +767,7 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     L.A1 = off;         off = al(off + (size_t)P * f * 2);
     L.A3 = off;         off = al(off + (sw ? (size_t)P * f * 2 : 0));
     L.dHu = off;        off = al(off + (size_t)P * f * 2);
+    L.dYu = off;        off = al(off + (size_t)P * d * 2);
     L.dA = off;         off = al(off + (size_t)P * (size_t)L.K2 * 2);
     L.dA1T = off;       off = al(off + f * kw * 2);
     L.dA3T = off;       off = al(off + (sw ? f * kw * 2 : 0));
@@ -720,14 +785,12 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     return L;
 }
 
-template <int EQ>
+template <int EPT>
 cudaError_t launch_dwr(const moe_config_t &c, const BwdLayout &L, const void *h, const float *dz,
                        float *part, float *partb, cudaStream_t s) {
-    const size_t smem = (size_t)(32 * BT + 32 * c.E) * 4;
-    cudaError_t err = set_max_dynamic_smem((const void *)dwr_part_kernel<EQ>, smem);
-    if (err != cudaSuccess) return err;
-    return launch_pdl(dwr_part_kernel<EQ>, dim3(c.d / BT, L.nsplit), dim3(256), smem, s, 1,
-                      static_cast<const __nv_bfloat16 *>(h), dz, c.T, c.d, c.E, L.ts, part, partb);
+    return launch_pdl(dwr_part_kernel<EPT>, dim3(c.d / BT, L.nsplit, dwr_etiles(c.E)), dim3(256),
+                      0, s, 1, static_cast<const __nv_bfloat16 *>(h), dz, c.T, c.d, c.E, L.ts,
+                      part, partb);
 }
 
 bool al16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
@@ -740,7 +803,7 @@ int backward_launches(const moe_config_t &c) {
     const bool sw = c.act == MOE_ACT_SWIGLU;
     const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
     return 1 /*prep*/ + (sw ? 3 : 2) /*weight transposes*/ + (sw ? 2 : 1) /*A1, A3*/ +
-           1 /*dHu*/ + 1 /*act*/ + 1 /*dX*/ + 1 /*gather-transpose*/ + (sw ? 3 : 2) /*dW*/ +
+           2 /*dy permute, dHu*/ + 1 /*act*/ + 1 /*dX*/ + 1 /*gather-transpose*/ + (sw ? 3 : 2) /*dW*/ +
            router + 1 /*router bwd*/ + 1 /*dh*/ + 2 /*dW_r*/ + (c.has_bias ? 2 : 0);
 }
 
@@ -832,13 +895,15 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     MOE_TRY(launch_pdl(bwd_prep_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0, s, 1,
                        slot_of, gates, offsets, P, c.E, gate_r, kseg, dev_status));
     // 2. transposed weights: W2T [E, f, d]; WT [E, d, K2] = [W1^T | W3^T]
-    MOE_TRY(launch_pdl(transpose_kernel, dim3(c.f / BT, c.d / BT, c.E), dim3(256), 0, s, 1, Wb2,
-                       c.d, c.f, bf(B.W2T), c.d, 0));
-    MOE_TRY(launch_pdl(transpose_kernel, dim3(c.d / BT, c.f / BT, c.E), dim3(256), 0, s, 1, Wb1,
-                       c.f, c.d, bf(B.WT), B.K2, 0));
+    const int64_t patches = E * (d / 32) * (f / 64);  // 32 x 64 patches of one weight tensor
+    const dim3 tgrid((unsigned)((patches + 7) / 8));
+    MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb2, c.d, c.f, bf(B.W2T), c.d,
+                       0, patches));
+    MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb1, c.f, c.d, bf(B.WT), B.K2,
+                       0, patches));
     if (sw)
-        MOE_TRY(launch_pdl(transpose_kernel, dim3(c.d / BT, c.f / BT, c.E), dim3(256), 0, s, 1,
-                           Wb3, c.f, c.d, bf(B.WT), B.K2, c.f));
+        MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb3, c.f, c.d, bf(B.WT),
+                           B.K2, c.f, patches));
     // 3. recomputed pre-activations A1 = X W1^T (+ b1), A3 = X W3^T
     const void *xa = have_xperm ? static_cast<const void *>(w + L.x_perm) : h;
     const int32_t *xrows = have_xperm ? nullptr : sorted_token;
@@ -847,8 +912,10 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     if (sw)
         MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W3, P, c.E, c.d, c.f, offsets, nullptr,
                                  bf(B.A3), dev_status, s));
-    // 4. dHu = dy[token] W2_e (rows of dy gathered through sorted_token)
-    MOE_TRY(launch_gemm_rows(dy, sorted_token, c.T, bf(B.W2T), P, c.E, c.d, c.f, offsets,
+    // 4. dHu = dYu W2_e with dYu[r] = dy[sorted_token[r]] (the rows of dy permuted once, as the
+    // forward permutes h: a TMA gather would repeat for every column tile)
+    MOE_TRY(launch_permute(c, dy, slot_of, bf(B.dYu), dev_status, s));
+    MOE_TRY(launch_gemm_rows(bf(B.dYu), nullptr, 0, bf(B.W2T), P, c.E, c.d, c.f, offsets,
                              nullptr, bf(B.dHu), dev_status, s));
     // 5. activation backward: dA, dA1T, dA3T, HT, dg parts, db1 parts
     ActBwd ab;
@@ -925,23 +992,21 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
                        dev_status));
     // 10. dh = sum_j dX[slot] + dz W_r^T
     {
-        const size_t smem = (size_t)(BT * c.E + 32 * c.E) * 4;
-        MOE_TRY(set_max_dynamic_smem((const void *)dh_kernel, smem));
-        MOE_TRY(launch_pdl(dh_kernel, dim3(c.d / BT, (unsigned)((c.T + 31) / 32)), dim3(256), smem,
-                           s, 1, static_cast<const __nv_bfloat16 *>(bf(B.dX)), slot_of,
+        MOE_TRY(launch_pdl(dh_kernel, dim3(c.d / BT, (unsigned)((c.T + DH_T - 1) / DH_T)),
+                           dim3(256), 0, s, 1, static_cast<const __nv_bfloat16 *>(bf(B.dX)), slot_of,
                            static_cast<const float *>(fl(B.dz)), W_r, c.T, c.d, c.E, c.k, P,
                            static_cast<__nv_bfloat16 *>(dh), dev_status));
     }
     // 11. dW_r = h^T dz, db_r = sum dz (split over tokens, then summed in split order)
     {
-        const int eq = (c.E + 3) / 4;
         float *part = fl(B.dwr_part), *partb = b_r ? fl(B.dwr_partb) : nullptr;
         const float *dz = fl(B.dz);
-        if (eq <= 2) MOE_TRY(launch_dwr<2>(c, B, h, dz, part, partb, s));
-        else if (eq <= 8) MOE_TRY(launch_dwr<8>(c, B, h, dz, part, partb, s));
-        else if (eq <= 16) MOE_TRY(launch_dwr<16>(c, B, h, dz, part, partb, s));
-        else if (eq <= 32) MOE_TRY(launch_dwr<32>(c, B, h, dz, part, partb, s));
-        else MOE_TRY(launch_dwr<64>(c, B, h, dz, part, partb, s));
+        switch (dwr_ept(c.E)) {
+            case 1: MOE_TRY(launch_dwr<1>(c, B, h, dz, part, partb, s)); break;
+            case 2: MOE_TRY(launch_dwr<2>(c, B, h, dz, part, partb, s)); break;
+            case 4: MOE_TRY(launch_dwr<4>(c, B, h, dz, part, partb, s)); break;
+            default: MOE_TRY(launch_dwr<8>(c, B, h, dz, part, partb, s)); break;
+        }
         const int64_t n = d * E;
         MOE_TRY(launch_pdl(split_sum_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
                            static_cast<const float *>(part), B.nsplit, n, dW_r,
