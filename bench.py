@@ -29,7 +29,12 @@ Each measurement carries:
                extrapolated to T tokens;
   graph        the same step recorded once in a CUDA graph (Layer.capture) and replayed K times:
                the launch-bound shapes' time without host launch cost;
-  clocks       nvidia-smi samples taken during the timed region.
+  clocks       nvidia-smi samples taken during the timed region;
+  backward     (bf16 workloads) K moe_backward calls after moe_forward_train (which keeps the
+               first GEMM's pre-activations), for an upstream gradient dy ~ N(0, 1) with
+               auxiliary and z-loss weights: ms per step, tokens/s and the roofline of the whole
+               backward (algorithmic work: the data and weight gradients of the expert GEMMs,
+               twice the forward's flops); train_step times K forward_train + backward pairs.
 --impl reference times the oracle itself (the method's plain statement) as the reference arm.
 """
 from __future__ import annotations
@@ -84,6 +89,40 @@ def _peaks() -> dict:
     return dict(bf16=1800.0, bf16_sustained=1400.0, hbm=6400.0, source="fallback")
 
 
+def _tc_peak(peaks: dict, region_s: float, reasons) -> tuple:
+    """(peak, other peak, kind, other kind): the sustained tensor peak for a region of a second
+    or more under the power cap, else the burst peak."""
+    sustained = region_s >= SUSTAINED_REGION_S and "sw_power_cap" in set(reasons or ())
+    if sustained:
+        return peaks["bf16_sustained"], peaks["bf16"], "bf16 sustained", "bf16 burst"
+    return peaks["bf16"], peaks["bf16_sustained"], "bf16 burst", "bf16 sustained"
+
+
+# weights of the auxiliary value and of the z-loss in the loss the backward differentiates
+BWD_AUX_WEIGHT, BWD_ZLOSS_WEIGHT = 0.01, 0.001
+
+
+def backward_roofline(w, bwd_ms: float, peaks: dict, region_s: float, reasons) -> dict:
+    """The backward's roofline entry. Algorithmic flops: the expert GEMMs' data gradients (dX,
+    dHact) and weight gradients, twice the forward's; algorithmic bytes: every expert's weights
+    read and its weight gradients written once, plus h, dy and dh. The bound is the tensor peak
+    when flops per byte exceed the ridge point, else the HBM copy bandwidth."""
+    flops = 2 * w.expert_flops()
+    nbytes = 2 * w.weight_bytes() + 3 * w.T * w.d * 2
+    sec = bwd_ms * 1e-3
+    tflops, gbs = flops / sec / 1e12, nbytes / sec / 1e9
+    tc_peak, tc_alt, kind, alt_kind = _tc_peak(peaks, region_s, reasons)
+    common = {"algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+              "flop_per_byte": flops / nbytes, "region_s": region_s}
+    if flops / nbytes >= tc_peak * 1e12 / (peaks["hbm"] * 1e9):
+        return {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": tflops / tc_peak, "peak_kind": f"{kind} ({peaks['source']})",
+                "frac_alt": tflops / tc_alt, "frac_alt_kind": alt_kind, "hbm_gbs": gbs, **common}
+    return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm"], "peak_kind": f"HBM copy ({peaks['source']})",
+            "tensor_tflops": tflops, **common}
+
+
 def roofline(w, ffn_ms: float, peaks: dict, region_s: float, reasons, alu: dict | None = None,
              traffic: dict | None = None) -> dict:
     """The expert FFN's roofline entry.
@@ -99,11 +138,7 @@ def roofline(w, ffn_ms: float, peaks: dict, region_s: float, reasons, alu: dict 
     tflops = flops / (ffn_ms * 1e-3) / 1e12
     gbs = nbytes / (ffn_ms * 1e-3) / 1e9
     intensity = flops / nbytes
-    sustained = region_s >= SUSTAINED_REGION_S and "sw_power_cap" in set(reasons or ())
-    tc_peak, tc_alt = ((peaks["bf16_sustained"], peaks["bf16"]) if sustained
-                       else (peaks["bf16"], peaks["bf16_sustained"]))
-    tc_kind = "bf16 sustained" if sustained else "bf16 burst"
-    alt_kind = "bf16 burst" if sustained else "bf16 sustained"
+    tc_peak, tc_alt, tc_kind, alt_kind = _tc_peak(peaks, region_s, reasons)
     common = {"flop_per_byte": intensity, "launches_per_step": launches,
               "algorithmic_flops_per_launch": flops / launches,
               "algorithmic_bytes_per_launch": nbytes / launches,
@@ -400,7 +435,10 @@ def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.
     g_ms = timed(lambda i: graph.replay(), args.steps, torch.cuda.current_stream())
     if B.moe_device_status(layer.ws) != B.MOE_OK:
         raise SystemExit(f"{w.name}: device status after graph region")
-    del graph, flush
+    del graph
+    bwd = (bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed)
+           if w.dtype == "bf16" and not args.no_backward else None)
+    del flush
 
     ms, e_ms, ffn_ms, g_ms = D.max_over_ranks([ms, e_ms, ffn_ms, g_ms], device="cuda")
     launches_per_step = B.moe_forward_launch_count(cfg)
@@ -424,11 +462,64 @@ def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.
                   "ms_per_step": g_ms},
         "clocks": clocks,
     }
+    if bwd is not None:
+        entry["backward"] = bwd
     del layer, dev
     torch.cuda.empty_cache()
     if world == 1 and cpu_budget_s > 0:
         entry["cpu_baseline"] = _cpu_baseline(w, inputs, budget_s=cpu_budget_s)
     return entry
+
+
+def bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed) -> dict:
+    """The backward of workload w for a seeded dy ~ N(0, 1): K moe_backward calls after one
+    moe_forward_train of h (the routing they differentiate at and the saved pre-activations),
+    then K training steps (moe_forward_train + moe_backward); returns the measurement entry."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed + 1000)
+    dy = torch.randn((w.T, w.d), generator=g, device="cuda").to(torch.bfloat16)
+    layer.forward_train(h, stream)
+    bwd = lambda i: layer.backward(h, dy, BWD_AUX_WEIGHT, BWD_ZLOSS_WEIGHT, stream)  # noqa: E731
+
+    def train(i):
+        layer.forward_train(h, stream)
+        bwd(i)
+
+    for i in range(args.warmup):
+        bwd(i)
+    torch.cuda.synchronize()
+    if B.moe_device_status(layer.ws) != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after backward warm-up")
+    with Clocks(local) as clk:
+        D.barrier()
+        torch.cuda.synchronize()
+        ms = timed(bwd, args.steps, stream)
+        D.barrier()
+    clocks = clk.summary()
+    for i in range(args.warmup):
+        train(i)
+    torch.cuda.synchronize()
+    D.barrier()
+    t_ms = timed(train, args.steps, stream)
+    if B.moe_device_status(layer.ws) != B.MOE_OK:
+        raise SystemExit(f"{w.name}: device status after the backward regions")
+    ms, t_ms = D.max_over_ranks([ms, t_ms], device="cuda")
+    world = D.env()[1]
+    launches = B.moe_backward_launch_count(layer.cfg, True)
+    fwd_launches = B.moe_forward_launch_count(layer.cfg)
+    del layer.bws, layer.grads
+    layer.bws = layer.grads = None
+    return {"value": D.job_tokens_per_s(w.T, world, ms), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": args.steps, "pre_activations": "saved by the forward",
+            "aux_weight": BWD_AUX_WEIGHT, "zloss_weight": BWD_ZLOSS_WEIGHT,
+            "roofline": backward_roofline(w, ms, peaks, ms * args.steps * 1e-3,
+                                          clocks.get("reasons")),
+            "gpu_launches": launches * args.steps, "launches_per_step": launches,
+            "train_step": {"value": D.job_tokens_per_s(w.T, world, t_ms), "unit": "tokens/s",
+                           "ms_per_step": t_ms,
+                           "what": "moe_forward_train + moe_backward, one call each",
+                           "gpu_launches": (launches + fwd_launches) * args.steps},
+            "clocks": clocks}
 
 
 def main() -> None:
@@ -439,6 +530,7 @@ def main() -> None:
     ap.add_argument("--workload", default="all", choices=["all"] + list(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     ap.add_argument("--override", default="",
                     help="reshape the workload for profiling, e.g. T=2048,E=2,k=1 (not a bench line)")
     args = ap.parse_args()
@@ -502,6 +594,8 @@ def main() -> None:
     }
     if "cpu_baseline" in head:
         line["cpu_baseline"] = head["cpu_baseline"]
+    if "backward" in head:
+        line["backward"] = head["backward"]
     if alu is not None:
         line["fp32_ffma_tflops"] = alu
     if len(entries) > 1:

@@ -38,9 +38,23 @@ extern "C" {
  * partial sums. MOE_ERR_UNSUPPORTED for f32, MOE_ERR_INVALID_ARG for an invalid cfg. */
 moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
-/* Number of kernels one moe_backward call with cfg launches (0 for T = 0; device memsets not
- * counted). Host-only. */
-moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t *kernels);
+/* Number of kernels one moe_backward call with cfg and saved_preact launches (0 for T = 0;
+ * device memsets not counted). Host-only. */
+moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t saved_preact,
+                                       int32_t *kernels);
+
+/* moe_forward (include/moe.h; same arguments, results and errors) for a training step: the first
+ * expert GEMM also stores its pre-activations -- x . W1_e (+ b1_e), and x . W3_e for SwiGLU,
+ * [T k, f] bf16 each, the values its epilogue activates -- into the backward workspace bws
+ * (moe_backward_workspace_size bytes, 16-byte aligned), so that moe_backward with
+ * saved_preact = 1 need not recompute them. bf16 only (MOE_ERR_UNSUPPORTED for f32);
+ * MOE_ERR_WORKSPACE if bws is too small or misaligned, MOE_ERR_INVALID_ARG if it is NULL. */
+moe_status_t moe_forward_train(const moe_config_t *cfg, const void *h, const float *W_r,
+                               const float *b_r, const float *sel_bias, const void *W1,
+                               const float *b1, const void *W3, const void *W2, const float *b2,
+                               void *y, float *aux_out, float *zloss_out, int32_t *topk_idx_out,
+                               int32_t *counts_out, void *ws, size_t ws_bytes, void *bws,
+                               size_t bws_bytes, void *stream);
 
 /* Gradients of the layer for the upstream gradient dy, after a moe_forward call with the same
  * cfg, inputs and workspace `ws` (the backward reads the routing the forward left there:
@@ -52,6 +66,9 @@ moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t *kernels
  *   counts   [E] int32 or NULL        likewise for counts_out
  *   dy       [T, d] bf16              upstream gradient of y
  *   aux_weight, zloss_weight          the weights of the auxiliary value and of the z-loss in L
+ *   saved_preact                      1: the forward was moe_forward_train with this bws, whose
+ *                                     pre-activations are used; 0: they are recomputed (two
+ *                                     grouped GEMMs for SwiGLU, one for GELU)
  * Outputs (device, caller-owned, fully overwritten):
  *   dh   [T, d] bf16
  *   dW_r [d, E] f32;  db_r [E] f32 (given exactly when b_r is given)
@@ -59,9 +76,9 @@ moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t *kernels
  *   db1  [E, f] f32, db2 [E, d] f32 (when cfg->has_bias, else ignored)
  * An expert that received no slot gets zero weight gradients. Alignment: h, dy, dh and the
  * weight tensors 16 bytes, the f32 tensors 4 bytes, ws and bws 16 bytes.
- * Errors: MOE_ERR_INVALID_ARG (pointers, alignment, non-finite weights, b_r given without db_r or
- * the reverse), MOE_ERR_UNSUPPORTED (f32), MOE_ERR_WORKSPACE (ws or bws too small), MOE_ERR_CUDA
- * (a launch failed); out-of-range indices in the forward's routing set MOE_ERR_DEVICE_INDEX in
+ * Errors: MOE_ERR_INVALID_ARG (pointers, alignment, a non-finite aux_weight or zloss_weight, b_r
+ * given without db_r or the reverse, saved_preact not 0 or 1), MOE_ERR_UNSUPPORTED (f32),
+ * MOE_ERR_WORKSPACE (ws or bws too small), MOE_ERR_CUDA (a launch failed); out-of-range indices in the forward's routing set MOE_ERR_DEVICE_INDEX in
  * the device status word (moe_device_status). Asynchronous on `stream`; allocates nothing. */
 moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W_r,
                           const float *b_r, const void *W1, const float *b1, const void *W3,
@@ -69,7 +86,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
                           const int32_t *counts, const void *dy, float aux_weight,
                           float zloss_weight, void *dh, float *dW_r, float *db_r, void *dW1,
                           float *db1, void *dW3, void *dW2, float *db2, void *ws, size_t ws_bytes,
-                          void *bws, size_t bws_bytes, void *stream);
+                          void *bws, size_t bws_bytes, int32_t saved_preact, void *stream);
 
 #ifdef __cplusplus
 }

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_gelu_tanh_grad.restype = D
         L.oracle_silu_grad.argtypes = [D]
         L.oracle_silu_grad.restype = D
+        L.oracle_backward_sampled.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, I32, P, P, P,
+                                              P, P, I32, P, P, P, P, P, I32, D, D, I64, P, P,
+                                              I64, P, P, P, P, P]
         L.oracle_backward.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, I32, P, P, P, P, P,
                                       I32, P, P, P, P, P, I32, D, D, P, P, P, P, P, P, P, P, P]
         _lib = L
@@ -340,6 +343,38 @@ def backward(h, W_r, b_r, W1, W3, W2, b1, b2, idx, dy, act: int, gate_mode: int,
                           _ptr(out["dh"]), _ptr(out["dW_r"]), _ptr(out["db_r"]), _ptr(out["dW1"]),
                           _ptr(out["dW3"]), _ptr(out["dW2"]), _ptr(out["db1"]), _ptr(out["db2"]),
                           _ptr(out["dg"]))
+    return out
+
+
+def backward_sampled(h, W_r, b_r, W1, W3, W2, b1, b2, idx, dy, act: int, gate_mode: int,
+                     tokens, cols, keep=None, aux_weight: float = 0.0,
+                     zloss_weight: float = 0.0) -> dict:
+    """Selected entries of backward() at any size: dh rows of `tokens`, and for each (e, n) in
+    `cols` row n of dW1_e (and dW3_e) and column n of dW2_e, each as a length-d vector."""
+    hs, hdt = _stored(h)
+    T, d = hs.shape
+    Wr = _f32(W_r)
+    E = Wr.shape[1]
+    br = _f32(b_r)
+    idx = _np(idx, np.int32)
+    k = idx.shape[1]
+    w1, w3, w2, wdt = _weights(W1, W3, W2)
+    f = w1.shape[1]
+    b1c, b2c = _f32(b1), _f32(b2)
+    dys, dydt = _stored(dy)
+    kp = None if keep is None else _np(keep, np.uint8)
+    tokens = _np(tokens, np.int64)
+    cols = np.asarray(cols, dtype=np.int32).reshape(-1, 2)
+    ce, cn = _np(cols[:, 0], np.int32), _np(cols[:, 1], np.int32)
+    out = dict(dh=np.empty((len(tokens), d)), dW1=np.empty((len(cols), d)),
+               dW3=np.empty((len(cols), d)) if act == SWIGLU else None,
+               dW2=np.empty((len(cols), d)))
+    lib().oracle_backward_sampled(T, d, f, E, k, act, gate_mode, _ptr(hs), hdt, _ptr(Wr), _ptr(br),
+                                  _ptr(w1), _ptr(w3), _ptr(w2), wdt, _ptr(b1c), _ptr(b2c),
+                                  _ptr(idx), _ptr(kp), _ptr(dys), dydt, float(aux_weight),
+                                  float(zloss_weight), len(tokens), _ptr(tokens), _ptr(out["dh"]),
+                                  len(cols), _ptr(ce), _ptr(cn), _ptr(out["dW1"]),
+                                  _ptr(out["dW3"]), _ptr(out["dW2"]))
     return out
 
 

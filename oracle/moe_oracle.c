@@ -607,3 +607,151 @@ void oracle_backward(int64_t T, int32_t d, int32_t f, int32_t E, int32_t k, int3
     if (dg_out) for (int64_t s = 0; s < P; ++s) dg_out[s] = dg[s];
     free(z); free(p); free(g); free(dg); free(dxs); free(fe); free(dz);
 }
+
+/* Selected entries of the same backward, at any size: each depends on a bounded set of slots.
+ *   dh rows of the listed tokens (their k slots' input gradients, then the router's term);
+ *   for each listed (expert e, hidden unit n): row n of dW1_e and of dW3_e (SwiGLU) and column n
+ *   of dW2_e, sums over e's kept slots in token order.
+ * z and p come from the router over all T tokens (the gates of every slot of a listed expert are
+ * needed); counts are the routed counts of idx. Outputs: dh_rows [n_tok, d], dW1_rows and
+ * dW3_rows [n_cols, d] (dW3_rows may be NULL), dW2_cols [n_cols, d] (dW2_e[o, n] at [c, o]). */
+void oracle_backward_sampled(int64_t T, int32_t d, int32_t f, int32_t E, int32_t k, int32_t act,
+                             int32_t gate_mode, const void *h, int32_t h_dtype, const float *W_r,
+                             const float *b_r, const void *W1, const void *W3, const void *W2,
+                             int32_t w_dtype, const float *b1, const float *b2,
+                             const int32_t *idx, const unsigned char *keep, const void *dy,
+                             int32_t dy_dtype, double aux_weight, double zloss_weight,
+                             int64_t n_tok, const int64_t *tokens, double *dh_rows,
+                             int64_t n_cols, const int32_t *col_e, const int32_t *col_n,
+                             double *dW1_rows, double *dW3_rows, double *dW2_cols)
+{
+    const int64_t P = T * k;
+    double *z = (double *)malloc(sizeof(double) * (size_t)(T * E + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(T * E + 1));
+    double *g = (double *)malloc(sizeof(double) * (size_t)(P + 1));
+    double *fe = (double *)calloc((size_t)(E > 0 ? E : 1), sizeof(double));
+    oracle_router(T, d, E, h, h_dtype, W_r, b_r, z, p);
+    oracle_gates(T, E, k, gate_mode, z, p, idx, g);
+    for (int64_t s = 0; s < P; ++s) fe[idx[s]] += 1.0;
+    for (int32_t e = 0; e < E; ++e) fe[e] /= (double)T * (double)k;
+
+    /* dh rows: each token's slots, forward and backward in full, then the router term */
+#pragma omp parallel
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dyt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *a1 = (double *)malloc(sizeof(double) * (size_t)f);
+        double *a3 = (double *)malloc(sizeof(double) * (size_t)f);
+        double *hid = (double *)malloc(sizeof(double) * (size_t)f);
+        double *dhid = (double *)malloc(sizeof(double) * (size_t)f);
+        double *dg = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+        double *dz = (double *)malloc(sizeof(double) * (size_t)E);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t q = 0; q < n_tok; ++q) {
+            const int64_t t = tokens[q];
+            double *out = dh_rows + q * d;
+            for (int32_t i = 0; i < d; ++i) {
+                x[i] = widen(h, h_dtype, t * d + i);
+                dyt[i] = widen(dy, dy_dtype, t * d + i);
+                out[i] = 0.0;
+            }
+            for (int32_t j = 0; j < k; ++j) {
+                const int64_t s = t * k + j;
+                dg[j] = 0.0;
+                if (keep && !keep[s]) continue;
+                const int32_t e = idx[s];
+                const int64_t base1 = (int64_t)e * f * d, base2 = (int64_t)e * d * f;
+                for (int32_t n = 0; n < f; ++n) {
+                    double u = 0.0, v = 0.0;
+                    for (int32_t i = 0; i < d; ++i) {
+                        u += widen(W1, w_dtype, base1 + (int64_t)n * d + i) * x[i];
+                        if (act == OR_SWIGLU) v += widen(W3, w_dtype, base1 + (int64_t)n * d + i) * x[i];
+                    }
+                    if (act != OR_SWIGLU && b1) u += (double)b1[(int64_t)e * f + n];
+                    a1[n] = u;
+                    a3[n] = v;
+                    hid[n] = act == OR_SWIGLU ? silu(u) * v : gelu_tanh(u);
+                    dhid[n] = 0.0;
+                }
+                double dgs = 0.0;
+                for (int32_t o = 0; o < d; ++o) {
+                    double yo = 0.0;
+                    for (int32_t n = 0; n < f; ++n) {
+                        const double w2 = widen(W2, w_dtype, base2 + (int64_t)o * f + n);
+                        yo += w2 * hid[n];
+                        dhid[n] += w2 * g[s] * dyt[o];
+                    }
+                    if (act != OR_SWIGLU && b2) yo += (double)b2[(int64_t)e * d + o];
+                    dgs += dyt[o] * yo;
+                }
+                dg[j] = dgs;
+                for (int32_t n = 0; n < f; ++n) {
+                    double d1, d3 = 0.0;
+                    if (act == OR_SWIGLU) {
+                        d1 = dhid[n] * a3[n] * silu_grad(a1[n]);
+                        d3 = dhid[n] * silu(a1[n]);
+                    } else {
+                        d1 = dhid[n] * gelu_tanh_grad(a1[n]);
+                    }
+                    for (int32_t i = 0; i < d; ++i) {
+                        out[i] += widen(W1, w_dtype, base1 + (int64_t)n * d + i) * d1;
+                        if (act == OR_SWIGLU) out[i] += widen(W3, w_dtype, base1 + (int64_t)n * d + i) * d3;
+                    }
+                }
+            }
+            router_logit_grad(T, E, k, gate_mode, z + t * E, p + t * E, idx + t * k, g + t * k,
+                              dg, fe, aux_weight, zloss_weight, dz);
+            for (int32_t i = 0; i < d; ++i)
+                for (int32_t e = 0; e < E; ++e) out[i] += (double)W_r[(int64_t)i * E + e] * dz[e];
+        }
+        free(x); free(dyt); free(a1); free(a3); free(hid); free(dhid); free(dg); free(dz);
+    }
+
+    /* weight-gradient rows and columns of the listed (e, n) */
+#pragma omp parallel
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t c = 0; c < n_cols; ++c) {
+            const int32_t e = col_e[c], n = col_n[c];
+            const int64_t base1 = (int64_t)e * f * d, base2 = (int64_t)e * d * f;
+            double *r1 = dW1_rows + c * d, *r2 = dW2_cols + c * d;
+            double *r3 = dW3_rows ? dW3_rows + c * d : NULL;
+            for (int32_t i = 0; i < d; ++i) {
+                r1[i] = 0.0;
+                r2[i] = 0.0;
+                if (r3) r3[i] = 0.0;
+            }
+            for (int64_t s = 0; s < P; ++s) {
+                if (idx[s] != e || (keep && !keep[s])) continue;
+                const int64_t t = s / k;
+                double u = 0.0, v = 0.0, dh_n = 0.0;
+                for (int32_t i = 0; i < d; ++i) {
+                    x[i] = widen(h, h_dtype, t * d + i);
+                    u += widen(W1, w_dtype, base1 + (int64_t)n * d + i) * x[i];
+                    if (act == OR_SWIGLU) v += widen(W3, w_dtype, base1 + (int64_t)n * d + i) * x[i];
+                }
+                if (act != OR_SWIGLU && b1) u += (double)b1[(int64_t)e * f + n];
+                const double hid = act == OR_SWIGLU ? silu(u) * v : gelu_tanh(u);
+                for (int32_t o = 0; o < d; ++o) {
+                    const double dyo = g[s] * widen(dy, dy_dtype, t * d + o);
+                    r2[o] += dyo * hid;
+                    dh_n += widen(W2, w_dtype, base2 + (int64_t)o * f + n) * dyo;
+                }
+                double d1, d3 = 0.0;
+                if (act == OR_SWIGLU) {
+                    d1 = dh_n * v * silu_grad(u);
+                    d3 = dh_n * silu(u);
+                } else {
+                    d1 = dh_n * gelu_tanh_grad(u);
+                }
+                for (int32_t i = 0; i < d; ++i) {
+                    r1[i] += d1 * x[i];
+                    if (r3) r3[i] += d3 * x[i];
+                }
+            }
+        }
+        free(x);
+    }
+    free(z); free(p); free(g); free(fe);
+}

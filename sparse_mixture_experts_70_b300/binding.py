@@ -82,10 +82,12 @@ def lib() -> ctypes.CDLL:
             "moe_debug_expert_ffn_timeout": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                              ctypes.c_size_t, ctypes.c_uint64, _P],
             "moe_backward_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
-            "moe_backward_launch_count": [_CFG, ctypes.POINTER(ctypes.c_int32)],
+            "moe_backward_launch_count": [_CFG, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
             "moe_backward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
                              ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
-                             _P, ctypes.c_size_t, _P],
+                             _P, ctypes.c_size_t, ctypes.c_int32, _P],
+            "moe_forward_train": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                  ctypes.c_size_t, _P, ctypes.c_size_t, _P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -289,22 +291,34 @@ def moe_backward_workspace_size(cfg: moe_config_t) -> int:
     return n.value
 
 
-def moe_backward_launch_count(cfg: moe_config_t) -> int:
+def moe_backward_launch_count(cfg: moe_config_t, saved_preact: bool = False) -> int:
     n = ctypes.c_int32()
-    _check(lib().moe_backward_launch_count(ctypes.byref(cfg), ctypes.byref(n)),
-           "moe_backward_launch_count")
+    _check(lib().moe_backward_launch_count(ctypes.byref(cfg), 1 if saved_preact else 0,
+                                           ctypes.byref(n)), "moe_backward_launch_count")
     return n.value
+
+
+def moe_forward_train(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, y, aux_out, topk_idx_out, counts_out,
+                      ws, bws, stream=None, sel_bias=None, zloss_out=None) -> None:
+    _check(lib().moe_forward_train(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r),
+                                   _ptr(sel_bias), _ptr(W1), _ptr(b1), _ptr(W3), _ptr(W2),
+                                   _ptr(b2), _ptr(y), _ptr(aux_out), _ptr(zloss_out),
+                                   _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _ptr(bws),
+                                   bws.numel() * bws.element_size(), _stream(stream)),
+           "moe_forward_train")
 
 
 def moe_backward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, topk_idx, counts, dy, aux_weight,
                  zloss_weight, dh, dW_r, db_r, dW1, db1, dW3, dW2, db2, ws, bws,
-                 stream=None) -> None:
+                 stream=None, saved_preact: bool = False) -> None:
     _check(lib().moe_backward(ctypes.byref(cfg), _ptr(h), _ptr(W_r), _ptr(b_r), _ptr(W1),
                               _ptr(b1), _ptr(W3), _ptr(W2), _ptr(b2), _ptr(topk_idx),
                               _ptr(counts), _ptr(dy), float(aux_weight), float(zloss_weight),
                               _ptr(dh), _ptr(dW_r), _ptr(db_r), _ptr(dW1), _ptr(db1), _ptr(dW3),
                               _ptr(dW2), _ptr(db2), _ptr(ws), ws.numel() * ws.element_size(),
-                              _ptr(bws), bws.numel() * bws.element_size(), _stream(stream)),
+                              _ptr(bws), bws.numel() * bws.element_size(),
+                              1 if saved_preact else 0, _stream(stream)),
            "moe_backward")
 
 
@@ -340,23 +354,40 @@ class Layer:
         args = (self.cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"), w["W2"],
                 w.get("b2"), self.y, self.aux, self.topk_idx, self.counts, self.ws)
         extra = dict(sel_bias=w.get("sel_bias"), zloss_out=self.zloss)
+        self.saved_preact = False
         if ffn_events is None:
             moe_forward(*args, stream, **extra)
         else:
             moe_forward_events(*args, ffn_events[0], ffn_events[1], stream, **extra)
         return self.y
 
+    def _bws(self, device) -> torch.Tensor:
+        if getattr(self, "bws", None) is None:
+            self.bws = torch.empty(max(moe_backward_workspace_size(self.cfg), 16),
+                                   dtype=torch.uint8, device=device)
+        return self.bws
+
+    def forward_train(self, h: torch.Tensor, stream=None) -> torch.Tensor:
+        """moe_forward_train on h: forward() that also keeps GEMM1's pre-activations in the
+        backward workspace, so that the next backward() does not recompute them (bf16)."""
+        w = self.w
+        moe_forward_train(self.cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"),
+                          w["W2"], w.get("b2"), self.y, self.aux, self.topk_idx, self.counts,
+                          self.ws, self._bws(h.device), stream, sel_bias=w.get("sel_bias"),
+                          zloss_out=self.zloss)
+        self.saved_preact = True
+        return self.y
+
     def backward(self, h: torch.Tensor, dy: torch.Tensor, aux_weight: float = 0.0,
                  zloss_weight: float = 0.0, stream=None) -> dict:
-        """moe_backward after forward(h): the gradients of sum(dy * y) + aux_weight * aux +
+        """moe_backward after forward(h) or forward_train(h) (whose saved pre-activations it
+        then uses): the gradients of sum(dy * y) + aux_weight * aux +
         zloss_weight * zloss (bf16 layers). Returns device tensors dh, dW_r, db_r, dW1, dW3,
         dW2, db1, db2 (None where the layer has no such parameter), owned by the Layer and
         overwritten by the next call."""
         cfg, w = self.cfg, self.w
         dev = h.device
-        if getattr(self, "bws", None) is None:
-            self.bws = torch.empty(max(moe_backward_workspace_size(cfg), 16), dtype=torch.uint8,
-                                   device=dev)
+        self._bws(dev)
         if getattr(self, "grads", None) is None:
             E, d, f = cfg.E, cfg.d, cfg.f
             bf = torch.bfloat16
@@ -375,7 +406,8 @@ class Layer:
         moe_backward(cfg, h, w["W_r"], w.get("b_r"), w["W1"], w.get("b1"), w.get("W3"), w["W2"],
                      w.get("b2"), self.topk_idx, self.counts, dy, aux_weight, zloss_weight,
                      g["dh"], g["dW_r"], g["db_r"], g["dW1"], g["db1"], g["dW3"], g["dW2"],
-                     g["db2"], self.ws, self.bws, stream)
+                     g["db2"], self.ws, self.bws, stream,
+                     saved_preact=getattr(self, "saved_preact", False))
         return g
 
     def capture(self, h: torch.Tensor) -> "torch.cuda.CUDAGraph":

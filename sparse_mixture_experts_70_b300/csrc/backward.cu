@@ -798,11 +798,18 @@ bool al4(const void *p) { return p && ((uintptr_t)p & 3u) == 0; }
 
 }  // namespace
 
-int backward_launches(const moe_config_t &c) {
+size_t backward_ws_bytes(const moe_config_t &c) { return bwd_layout(c).total; }
+
+size_t backward_pre_offset(const moe_config_t &c, int which) {
+    const BwdLayout L = bwd_layout(c);
+    return which == 0 ? L.A1 : L.A3;
+}
+
+int backward_launches(const moe_config_t &c, bool saved) {
     if (c.T == 0) return 0;
     const bool sw = c.act == MOE_ACT_SWIGLU;
     const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
-    return 1 /*prep*/ + (sw ? 3 : 2) /*weight transposes*/ + (sw ? 2 : 1) /*A1, A3*/ +
+    return 1 /*prep*/ + (sw ? 3 : 2) /*weight transposes*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
            2 /*dy permute, dHu*/ + 1 /*act*/ + 1 /*dX*/ + 1 /*gather-transpose*/ + (sw ? 3 : 2) /*dW*/ +
            router + 1 /*router bwd*/ + 1 /*dh*/ + 2 /*dW_r*/ + (c.has_bias ? 2 : 0);
 }
@@ -822,12 +829,13 @@ moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes)
     return MOE_OK;
 }
 
-moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t *kernels) {
+moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t saved_preact,
+                                       int32_t *kernels) {
     const moe_status_t st = validate_config(cfg);
     if (st != MOE_OK) return st;
-    if (!kernels) return MOE_ERR_INVALID_ARG;
+    if (!kernels || (saved_preact != 0 && saved_preact != 1)) return MOE_ERR_INVALID_ARG;
     if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-    *kernels = backward_launches(*cfg);
+    *kernels = backward_launches(*cfg, saved_preact != 0);
     return MOE_OK;
 }
 
@@ -837,13 +845,14 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
                           const int32_t *counts, const void *dy, float aux_weight,
                           float zloss_weight, void *dh, float *dW_r, float *db_r, void *dW1,
                           float *db1, void *dW3, void *dW2, float *db2, void *ws, size_t ws_bytes,
-                          void *bws, size_t bws_bytes, void *stream) {
+                          void *bws, size_t bws_bytes, int32_t saved_preact, void *stream) {
     moe_status_t st = validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config_t &c = *cfg;
     if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     const bool sw = c.act == MOE_ACT_SWIGLU;
     if (!isfinite(aux_weight) || !isfinite(zloss_weight)) return MOE_ERR_INVALID_ARG;
+    if (saved_preact != 0 && saved_preact != 1) return MOE_ERR_INVALID_ARG;
     if (!al16(ws) || !al16(bws) || !al4(dW_r) || !al16(dW1) || !al16(dW2) ||
         (sw && !al16(dW3)) || ((b_r != nullptr) != (db_r != nullptr)) || (db_r && !al4(db_r)) ||
         (c.has_bias && (!al4(db1) || !al4(db2) || !al4(b1) || !al4(b2))))
@@ -904,14 +913,17 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     if (sw)
         MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb3, c.f, c.d, bf(B.WT),
                            B.K2, c.f, patches));
-    // 3. recomputed pre-activations A1 = X W1^T (+ b1), A3 = X W3^T
-    const void *xa = have_xperm ? static_cast<const void *>(w + L.x_perm) : h;
-    const int32_t *xrows = have_xperm ? nullptr : sorted_token;
-    MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W1, P, c.E, c.d, c.f, offsets,
-                             c.has_bias ? b1 : nullptr, bf(B.A1), dev_status, s));
-    if (sw)
-        MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W3, P, c.E, c.d, c.f, offsets, nullptr,
-                                 bf(B.A3), dev_status, s));
+    // 3. pre-activations A1 = X W1^T (+ b1), A3 = X W3^T: left in bws by moe_forward_train, or
+    // recomputed here
+    if (!saved_preact) {
+        const void *xa = have_xperm ? static_cast<const void *>(w + L.x_perm) : h;
+        const int32_t *xrows = have_xperm ? nullptr : sorted_token;
+        MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W1, P, c.E, c.d, c.f, offsets,
+                                 c.has_bias ? b1 : nullptr, bf(B.A1), dev_status, s));
+        if (sw)
+            MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W3, P, c.E, c.d, c.f, offsets, nullptr,
+                                     bf(B.A3), dev_status, s));
+    }
     // 4. dHu = dYu W2_e with dYu[r] = dy[sorted_token[r]] (the rows of dy permuted once, as the
     // forward permutes h: a TMA gather would repeat for every column tile)
     MOE_TRY(launch_permute(c, dy, slot_of, bf(B.dYu), dev_status, s));

@@ -87,6 +87,9 @@ struct TcArgs {
     // columns [offsets[e], offsets[e+1]) -- multiples of 64, zero-padded -- of A [M, K] and
     // B [N, K] (K: the padded width). m_tiles = ceil(M / 128).
     int M, m_tiles;
+    // training forward (GEMM1): the pre-activations also go to pre1 (x . W1_e + b1) and, for
+    // SwiGLU, pre3 (x . W3_e), [P, N] bf16 each (null: not saved)
+    __nv_bfloat16 *pre1, *pre3;
 };
 
 // The 4 source rows this lane gathers for tile ti (rows 4 lane .. 4 lane + 3 of the tile);
@@ -140,6 +143,16 @@ __device__ __forceinline__ Tile decode_tile(int t, int &eh, const int32_t *s_cum
     ti.row0 = s_off[e] + m * BM;
     ti.rows = min(BM, s_off[e + 1] - ti.row0);
     return ti;
+}
+
+// 32 f32 values as bf16 at dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const float (&v)[32]) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        d[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                          pack_bf16(v[8 * i + 6], v[8 * i + 7]));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -198,6 +211,11 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
             float x1[32], x3[32];
             tmem_ld32x2(trow + c, trow + BN / 2 + c, x1, x3);
             const int col = ti.n * (BN / 2) + c;
+            if (a.pre1 && valid && col < a.N) {
+                const int64_t off = (int64_t)(ti.row0 + r) * a.N + col;
+                store_row32(a.pre1 + off, x1);
+                store_row32(a.pre3 + off, x3);
+            }
             if (boxed && col < a.N) {
                 uint32_t pk[16];
 #pragma unroll
@@ -234,6 +252,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] += __ldg(bp + i);
             }
+            if (a.pre1 && valid) store_row32(a.pre1 + (int64_t)(ti.row0 + r) * a.N + col, v);
             if (a.epi == EPI_GELU) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_fast(v[i]);
@@ -835,7 +854,8 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
                         int N, int epi, const int32_t *offsets, const float *bias, void *out,
                         uint32_t *dev_status, const FaultHook &hook, cudaStream_t s,
                         const int32_t *A_rows = nullptr, int64_t A_src_rows = 0,
-                        const int32_t *out_token = nullptr, const float *out_gate = nullptr) {
+                        const int32_t *out_token = nullptr, const float *out_gate = nullptr,
+                        void *pre1 = nullptr, void *pre3 = nullptr) {
     // every B box is 128 rows: one half of the 256-row B tile; a gathered A reads one-row boxes
     CUtensorMap mA, mB, mB3, mO;
     if (A_rows ? !make_map(&mA, A, A_src_rows, K, 1) : !make_map(&mA, A, P, K, BM))
@@ -867,6 +887,8 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.out_gate = out_gate;
     a.M = 0;
     a.m_tiles = 0;
+    a.pre1 = static_cast<__nv_bfloat16 *>(pre1);
+    a.pre3 = static_cast<__nv_bfloat16 *>(pre3);
     // The CTA-pair kernel when experts average at least four M tiles (on an expert's odd last
     // tile the second CTA computes masked rows, a small loss there).
     const int clusters = pair_clusters();
@@ -917,6 +939,7 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     a.out_gate = nullptr;
     a.M = M;
     a.m_tiles = (M + BM - 1) / BM;
+    a.pre1 = a.pre3 = nullptr;
     const int64_t units = (int64_t)E * a.m_tiles * a.n_tiles;
     if (units >= (1ll << 31)) return cudaErrorInvalidValue;
     int64_t grid = num_sms();
@@ -956,7 +979,8 @@ cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t 
     cudaError_t err = launch_gemm(gather ? b.gather_h : b.x_perm, b.W1, b.W3, P, c.E, c.d, c.f,
                                   swiglu ? EPI_SWIGLU : EPI_GELU, b.offsets,
                                   c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, hook, s,
-                                  gather ? b.sorted_token : nullptr, c.T);
+                                  gather ? b.sorted_token : nullptr, c.T, nullptr, nullptr,
+                                  b.pre1, swiglu ? b.pre3 : nullptr);
     if (err != cudaSuccess) return err;
     return launch_gemm(b.H, b.W2, nullptr, P, c.E, c.f, c.d, EPI_STORE, b.offsets,
                        c.has_bias ? b.b2 : nullptr, scatter ? b.scatter_y : b.y_perm,

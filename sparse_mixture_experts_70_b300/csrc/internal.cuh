@@ -102,8 +102,13 @@ float *router_tc_logits(void *scratch, const moe_config_t &c);
 WsLayout ws_layout(const moe_config_t &c);
 // The argument checks every entry point applies to a configuration (MOE_OK when valid).
 moe_status_t validate_config(const moe_config_t *c);
-// Kernels one moe_backward call launches for c (bf16).
-int backward_launches(const moe_config_t &c);
+// Kernels one moe_backward call launches for c (bf16); saved: the pre-activations come from
+// moe_forward_train (no recompute).
+int backward_launches(const moe_config_t &c, bool saved);
+// Backward workspace: its size, and where moe_forward_train stores the pre-activations A1, A3
+// ([P, f] bf16 each; A3 for SwiGLU only).
+size_t backward_ws_bytes(const moe_config_t &c);
+size_t backward_pre_offset(const moe_config_t &c, int which);
 
 int num_sms();
 
@@ -197,6 +202,9 @@ struct FfnBufs {
     void *combine_y = nullptr;
     const int32_t *slot_of = nullptr;
     uint32_t *arrive = nullptr;
+    // training forward (tensor-core path): GEMM1 also stores its pre-activations, [P, f] bf16
+    // each (pre3: SwiGLU only)
+    void *pre1 = nullptr, *pre3 = nullptr;
 };
 // The f32 combine fused into the second expert launch: at most this many slot elements (T k d),
 // which the last block of each column tile reads and combines.

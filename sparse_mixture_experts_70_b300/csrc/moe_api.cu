@@ -297,7 +297,8 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
                                  const float *b2, void *y, float *aux_out, float *zloss_out,
                                  int32_t *topk_idx_out, int32_t *counts_out, void *ws,
                                  size_t ws_bytes, void *stream, cudaEvent_t ev_ffn0,
-                                 cudaEvent_t ev_ffn1) {
+                                 cudaEvent_t ev_ffn1, void *bws = nullptr,
+                                 size_t bws_bytes = 0) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     const moe_config_t &c = *cfg;
@@ -315,6 +316,8 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     }
     const WsLayout L = ws_layout(c);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (bws && (c.dtype != MOE_BF16)) return MOE_ERR_UNSUPPORTED;
+    if (bws && (!aligned16(bws) || bws_bytes < backward_ws_bytes(c))) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *w = static_cast<char *>(ws);
     uint32_t *dev_status = reinterpret_cast<uint32_t *>(w + L.status);
@@ -369,6 +372,10 @@ static moe_status_t forward_impl(const moe_config_t *cfg, const void *h, const f
     if (scatter) {
         fb.scatter_y = y;
         fb.gates = gates;
+    }
+    if (bws) {
+        fb.pre1 = static_cast<char *>(bws) + backward_pre_offset(c, 0);
+        fb.pre3 = static_cast<char *>(bws) + backward_pre_offset(c, 1);
     }
     if (plan.f32_combine) {
         fb.combine_y = y;
@@ -465,6 +472,18 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *h, const float *W_
                          int32_t *counts_out, void *ws, size_t ws_bytes, void *stream) {
     return forward_impl(cfg, h, W_r, b_r, sel_bias, W1, b1, W3, W2, b2, y, aux_out, zloss_out,
                         topk_idx_out, counts_out, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status_t moe_forward_train(const moe_config_t *cfg, const void *h, const float *W_r,
+                               const float *b_r, const float *sel_bias, const void *W1,
+                               const float *b1, const void *W3, const void *W2, const float *b2,
+                               void *y, float *aux_out, float *zloss_out, int32_t *topk_idx_out,
+                               int32_t *counts_out, void *ws, size_t ws_bytes, void *bws,
+                               size_t bws_bytes, void *stream) {
+    if (!bws) return MOE_ERR_INVALID_ARG;
+    return forward_impl(cfg, h, W_r, b_r, sel_bias, W1, b1, W3, W2, b2, y, aux_out, zloss_out,
+                        topk_idx_out, counts_out, ws, ws_bytes, stream, nullptr, nullptr, bws,
+                        bws_bytes);
 }
 
 moe_status_t moe_forward_events(const moe_config_t *cfg, const void *h, const float *W_r,

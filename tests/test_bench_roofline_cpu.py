@@ -78,3 +78,21 @@ def test_traffic_is_labelled_with_its_source():
     assert "scaled" in r["traffic_source"]
     r = bench.roofline(w, 2.0, PEAKS, region_s=0.1, reasons=[], traffic=None)
     assert r["traffic"] is None and r["traffic_source"] is None
+
+
+def test_backward_roofline_counts_twice_the_forward_flops():
+    """The backward's algorithmic flops are the data and weight gradients of the expert GEMMs
+    (twice the forward's); the Mixtral shape is tensor-bound, the decode shape HBM-bound (its
+    weights read and its weight gradients written once)."""
+    w = wl.WORKLOADS["mixtral"]
+    ms = 2 * w.expert_flops() / 1000e12 * 1e3  # a backward at 1000 TF/s
+    r = bench.backward_roofline(w, ms, PEAKS, region_s=0.5, reasons=[])
+    assert r["bound"] == "tensor" and r["peak"] == PEAKS["bf16"]
+    assert r["achieved"] == pytest.approx(1000.0, rel=1e-9)
+    assert r["algorithmic_flops"] == 2 * w.expert_flops()
+    d = wl.WORKLOADS["decode"]
+    nbytes = 2 * d.weight_bytes() + 3 * d.T * d.d * 2
+    r = bench.backward_roofline(d, nbytes / 5000e9 * 1e3, PEAKS, region_s=0.5, reasons=[])
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(5000.0, rel=1e-9)
+    assert r["frac"] == pytest.approx(5000.0 / PEAKS["hbm"], rel=1e-9)

@@ -176,3 +176,56 @@ def test_router_partial_rows():
     for name, w in wl.WORKLOADS.items():
         rows = B.moe_router_partials(B.config_for(w))
         assert 1 <= rows <= w.T
+
+
+@pytest.mark.parametrize("name,saved,expect", [("mixtral", 0, 20), ("mixtral", 1, 18),
+                                               ("switch", 0, 17), ("switch", 1, 16),
+                                               ("decode", 0, 18), ("many_small", 1, 18)])
+def test_backward_launch_count(name, saved, expect):
+    cfg = B.config_for(wl.WORKLOADS[name])
+    assert B.moe_backward_launch_count(cfg, bool(saved)) == expect
+
+
+def test_backward_arguments_are_checked_before_any_cuda_call():
+    L = B.lib()
+    fake = 1 << 40          # never dereferenced: the checks run before any launch
+    f32 = B.config_for(wl.WORKLOADS["micro"])
+    n = ctypes.c_size_t()
+    assert L.moe_backward_workspace_size(ctypes.byref(f32), ctypes.byref(n)) == \
+        B.MOE_ERR_UNSUPPORTED
+    k = ctypes.c_int32()
+    assert L.moe_backward_launch_count(ctypes.byref(f32), 0, ctypes.byref(k)) == \
+        B.MOE_ERR_UNSUPPORTED
+    cfg = B.config(T=64, d=128, f=256, E=8, k=2)
+    assert L.moe_backward_launch_count(ctypes.byref(cfg), 2, ctypes.byref(k)) == \
+        B.MOE_ERR_INVALID_ARG
+    nws, nbws = B.moe_workspace_size(cfg), B.moe_backward_workspace_size(cfg)
+
+    # moe_backward(cfg, h, W_r, b_r, W1, b1, W3, W2, b2, topk, counts, dy, aux_w, z_w, dh, dW_r,
+    #              db_r, dW1, db1, dW3, dW2, db2, ws, ws_bytes, bws, bws_bytes, saved, stream)
+    def bwd(c=cfg, b_r=None, db_r=None, aux=0.0, ws=fake, bws=fake, bws_bytes=nbws, saved=0,
+            dW1=fake):
+        return L.moe_backward(ctypes.byref(c), fake, fake, b_r, dW1, None, fake, fake, None,
+                              None, None, fake, aux, 0.0, fake, fake, db_r, fake, None, fake,
+                              fake, None, ws, nws, bws, bws_bytes, saved, None)
+    assert bwd(c=f32) == B.MOE_ERR_UNSUPPORTED
+    assert bwd(saved=2) == B.MOE_ERR_INVALID_ARG
+    assert bwd(aux=float("nan")) == B.MOE_ERR_INVALID_ARG
+    assert bwd(ws=None) == B.MOE_ERR_INVALID_ARG
+    assert bwd(bws=fake + 8) == B.MOE_ERR_INVALID_ARG
+    assert bwd(dW1=fake + 2) == B.MOE_ERR_INVALID_ARG
+    assert bwd(b_r=fake) == B.MOE_ERR_INVALID_ARG          # b_r without db_r
+    assert bwd(db_r=fake) == B.MOE_ERR_INVALID_ARG         # db_r without b_r
+    assert bwd(bws_bytes=nbws - 1) == B.MOE_ERR_WORKSPACE
+
+    # moe_forward_train(..., ws, ws_bytes, bws, bws_bytes, stream)
+    def fwd_train(c=cfg, bws=fake, bws_bytes=nbws):
+        return L.moe_forward_train(ctypes.byref(c), fake, fake, None, None, fake, None, fake,
+                                   fake, None, fake, fake, None, None, None, fake, nws, bws,
+                                   bws_bytes, None)
+    assert fwd_train(bws=None) == B.MOE_ERR_INVALID_ARG
+    assert fwd_train(bws_bytes=nbws - 1) == B.MOE_ERR_WORKSPACE
+    nf = B.moe_workspace_size(f32)
+    assert L.moe_forward_train(ctypes.byref(f32), fake, fake, None, None, fake, fake, None, fake,
+                               fake, fake, fake, None, None, None, fake, nf, fake, 1 << 30,
+                               None) == B.MOE_ERR_UNSUPPORTED

@@ -38,14 +38,17 @@ def _dy(w, seed):
     return torch.randn((w.T, w.d), generator=g).to(torch.bfloat16)
 
 
-def _run(w, inputs, dy, aux_weight, zloss_weight):
+def _run(w, inputs, dy, aux_weight, zloss_weight, train=False):
     dev = to_dev(inputs)
     cfg = B.config_for(w)
     layer = B.Layer(cfg, dev)
-    layer.forward(dev["h"])
     # poison the backward workspace: every pad and partial must be written before it is read
     layer.bws = torch.full((max(B.moe_backward_workspace_size(cfg), 16),), 255, dtype=torch.uint8,
                            device="cuda")
+    if train:
+        layer.forward_train(dev["h"])  # keeps the pre-activations in bws
+    else:
+        layer.forward(dev["h"])
     g = layer.backward(dev["h"], dy.cuda(), aux_weight, zloss_weight)
     torch.cuda.synchronize()
     assert B.moe_device_status(layer.ws) == B.MOE_OK
@@ -124,3 +127,27 @@ def test_auxiliary_and_zloss_gradients_alone(aux_w, z_w):
     _compare(got, ref, names=("dh", "dW_r", "db_r"))
     for name in ("dW1", "dW3", "dW2"):
         assert (got[name] == 0).all(), name
+
+
+@pytest.mark.parametrize("w,opts,aux_w,z_w", [CASES[0], CASES[1], CASES[2], CASES[4]],
+                         ids=lambda c: getattr(c, "name", ""))
+def test_training_forward_saves_what_the_backward_recomputes(w, opts, aux_w, z_w):
+    """moe_forward_train + moe_backward(saved_preact = 1) against the oracle, and against the
+    recomputing backward; the training forward's y equals moe_forward's bit for bit."""
+    inputs = _case(w, **opts)
+    dy = _dy(w, w.seed + 200)
+    got, idx = _run(w, inputs, dy, aux_w, z_w, train=True)
+    rec, idx2 = _run(w, inputs, dy, aux_w, z_w, train=False)
+    assert np.array_equal(idx, idx2)
+    _compare(got, _oracle(w, inputs, idx, dy, aux_w, z_w))
+    for name in GRADS:
+        if rec[name] is not None:
+            assert _rel_l2(got[name], rec[name]) <= 1e-3, name
+    dev = to_dev(inputs)
+    cfg = B.config_for(w)
+    a, b = B.Layer(cfg, dev), B.Layer(cfg, dev)
+    ya = a.forward(dev["h"]).clone()
+    yb = b.forward_train(dev["h"]).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yb)
+    assert torch.equal(a.aux, b.aux) and torch.equal(a.topk_idx, b.topk_idx)

@@ -185,3 +185,30 @@ def test_backward_is_linear_in_dy_without_aux_terms():
                         idx, -2.0 * dy, oracle.GELU_TANH, oracle.RENORM)
     for key in ("dh", "dW_r", "db_r", "dW1", "dW2", "db1", "db2", "dg"):
         np.testing.assert_allclose(b[key], -2.0 * a[key], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("act,gate,k,capacity", [(oracle.SWIGLU, oracle.RENORM, 2, 0.0),
+                                                (oracle.GELU_TANH, oracle.RAW_PROB, 1, 0.0),
+                                                (oracle.SWIGLU, oracle.RENORM, 2, 0.75)])
+def test_sampled_backward_equals_the_full_backward(act, gate, k, capacity):
+    """The sampled form (used at sizes where the full backward is out of reach) gives the same
+    entries as the full backward, which the finite differences above pin."""
+    T, d, f, E = 9, 8, 12, 4
+    p, dy, _ = _layer(9, T, d, f, E, k, act, gate, act == oracle.GELU_TANH, True)
+    _, _, idx, _ = _route(p, k, None)
+    keep = None
+    if capacity > 0:
+        _, _, _, slot_of = oracle.dispatch_capacity(idx, E, oracle.capacity(capacity, T, k, E))
+        keep = (slot_of >= 0).reshape(T, k)
+    args = (p["h"], p["W_r"], p["b_r"], p["W1"], p["W3"], p["W2"], p["b1"], p["b2"], idx, dy,
+            act, gate)
+    full = oracle.backward(*args, keep=keep, aux_weight=0.3, zloss_weight=0.2)
+    toks = np.array([0, 4, T - 1])
+    cols = [(e, n) for e in range(E) for n in (0, f - 1)]
+    sm = oracle.backward_sampled(*args, toks, cols, keep=keep, aux_weight=0.3, zloss_weight=0.2)
+    np.testing.assert_allclose(sm["dh"], full["dh"][toks], rtol=1e-12, atol=1e-13)
+    for c, (e, n) in enumerate(cols):
+        np.testing.assert_allclose(sm["dW1"][c], full["dW1"][e, n], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(sm["dW2"][c], full["dW2"][e, :, n], rtol=1e-12, atol=1e-13)
+        if act == oracle.SWIGLU:
+            np.testing.assert_allclose(sm["dW3"][c], full["dW3"][e, n], rtol=1e-12, atol=1e-13)
