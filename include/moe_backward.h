@@ -33,9 +33,8 @@
 extern "C" {
 #endif
 
-/* Bytes of backward workspace `bws` for cfg (bf16 only): the transposed weights, the recomputed
- * pre-activations, the intermediate gradients in row and transposed layouts and the router's
- * partial sums. MOE_ERR_UNSUPPORTED for f32, MOE_ERR_INVALID_ARG for an invalid cfg. */
+/* Bytes of backward workspace `bws` for cfg (bf16 only): the pre-activations, the intermediate
+ * gradients in row and transposed layouts and the router's partial sums. MOE_ERR_UNSUPPORTED for f32, MOE_ERR_INVALID_ARG for an invalid cfg. */
 moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes);
 
 /* Number of kernels one moe_backward call with cfg and saved_preact launches (0 for T = 0;

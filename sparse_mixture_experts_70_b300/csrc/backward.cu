@@ -16,6 +16,7 @@
 //   GELU  : Hact = GELU(A1),    dA1 = g dHu GELU'(A1)
 //   dg_r = dHu . Hact (+ dy . b2_e)                gradient of the slot's gate
 //   dX = dA1 W1_e + dA3 W3_e                        one row-grouped GEMM over K = [dA1 | dA3]
+// The data-gradient GEMMs read W2, W1 and W3 in their stored layouts as MN-major operands.
 //   dW2_e = (g dYu)^T Hact, dW1_e = dA1^T X, dW3_e = dA3^T X   K-grouped GEMMs over the slots
 //   db2_e = sum_r g_r dYu[r], db1_e = sum_r dA1[r]
 //   router: dz from dg through the gate softmax (RENORM) or p (RAW_PROB), plus the auxiliary
@@ -23,6 +24,8 @@
 // The weight-gradient GEMMs contract over slots, so their operands are stored transposed with
 // every expert's slots padded to a multiple of 64 columns (zeros in the pad): segment e of the
 // padded slot axis is [kseg[e], kseg[e+1]), kseg[e+1] - kseg[e] = roundup64(count_e).
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.cuh"
 #include "moe_backward.h"
 #include "tc_ptx.cuh"
@@ -82,54 +85,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, c
             const int cnt = offsets[e + 1] - offsets[e];
             acc += (cnt + BT - 1) / BT * BT;
             kseg[e + 1] = acc;
-        }
-    }
-    pdl_trigger();
-}
-
-// ---------------------------------------------------------------------------------------------
-// dst[b][c][coff + r] = src[b][r][c] for src [B][R][C] and dst rows of ldd elements (bf16; R a
-// multiple of 32, C of 64). One warp per 32 x 64 patch, each lane an 8 x 8 block transposed in
-// registers: rows (2p, 2p+1) of a column pair interleave with one byte permute per word, after
-// which output row c's words are input words picked by index. Loads: 8 lanes read 128
-// contiguous bytes of a row; stores: 4 lanes write 64 contiguous bytes of an output row.
-__global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16 *src, int R, int C,
-                                                        __nv_bfloat16 *dst, int ldd, int coff,
-                                                        int64_t patches) {
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t p = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (p < patches) {
-        const int pc = C / 64;
-        const int64_t per_b = (int64_t)(R / 32) * pc;
-        const int64_t b = p / per_b;
-        const int q = (int)(p - b * per_b);
-        const int r0 = (q / pc) * 32 + 8 * (lane >> 3);
-        const int c0 = (q % pc) * 64 + 8 * (lane & 7);
-        const __nv_bfloat16 *s = src + b * (int64_t)R * C + (int64_t)r0 * C + c0;
-        uint32_t w[8][4];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(s + (int64_t)r * C));
-            w[r][0] = v.x;
-            w[r][1] = v.y;
-            w[r][2] = v.z;
-            w[r][3] = v.w;
-        }
-        __nv_bfloat16 *d = dst + b * (int64_t)C * ldd + (int64_t)c0 * ldd + coff + r0;
-#pragma unroll
-        for (int cq = 0; cq < 4; ++cq) {
-            // output rows 2 cq (low halves) and 2 cq + 1 (high halves): word p = rows 2p, 2p + 1
-            uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int pr = 0; pr < 4; ++pr) {
-                lo[pr] = __byte_perm(w[2 * pr][cq], w[2 * pr + 1][cq], 0x5410);
-                hi[pr] = __byte_perm(w[2 * pr][cq], w[2 * pr + 1][cq], 0x7632);
-            }
-            *reinterpret_cast<uint4 *>(d + (int64_t)(2 * cq) * ldd) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<uint4 *>(d + (int64_t)(2 * cq + 1) * ldd) =
-                make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
     }
     pdl_trigger();
@@ -734,7 +689,7 @@ int dwr_ept(int E) { return E <= 16 ? 1 : E <= 32 ? 2 : E <= 64 ? 4 : 8; }
 int dwr_etiles(int E) { return (E + 16 * dwr_ept(E) - 1) / (16 * dwr_ept(E)); }
 
 struct BwdLayout {
-    size_t gate_r, kseg, W2T, WT, A1, A3, dHu, dYu, dA, dA1T, dA3T, HT, dX, XT, dYsT, dg_part,
+    size_t gate_r, kseg, A1, A3, dHu, dYu, dA, dA1T, dA3T, HT, dX, XT, dYsT, dg_part,
         db1_part, db2_part, dz, dwr_part, dwr_partb, total;
     int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
     int K2, n_part, nsplit;
@@ -762,8 +717,6 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     size_t off = 0;
     L.gate_r = off;     off = al(off + (size_t)P * 4);
     L.kseg = off;       off = al(off + (E + 1) * 4);
-    L.W2T = off;        off = al(off + E * f * d * 2);
-    L.WT = off;         off = al(off + E * d * (size_t)L.K2 * 2);
     L.A1 = off;         off = al(off + (size_t)P * f * 2);
     L.A3 = off;         off = al(off + (sw ? (size_t)P * f * 2 : 0));
     L.dHu = off;        off = al(off + (size_t)P * f * 2);
@@ -809,7 +762,7 @@ int backward_launches(const moe_config_t &c, bool saved) {
     if (c.T == 0) return 0;
     const bool sw = c.act == MOE_ACT_SWIGLU;
     const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
-    return 1 /*prep*/ + (sw ? 3 : 2) /*weight transposes*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
+    return 1 /*prep*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
            2 /*dy permute, dHu*/ + 1 /*act*/ + 1 /*dX*/ + 1 /*gather-transpose*/ + (sw ? 3 : 2) /*dW*/ +
            router + 1 /*router bwd*/ + 1 /*dh*/ + 2 /*dW_r*/ + (c.has_bias ? 2 : 0);
 }
@@ -892,9 +845,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     auto fl = [&](size_t o) { return reinterpret_cast<float *>(b + o); };
     float *gate_r = fl(B.gate_r);
     int32_t *kseg = reinterpret_cast<int32_t *>(b + B.kseg);
-    const auto *Wb1 = static_cast<const __nv_bfloat16 *>(W1);
-    const auto *Wb3 = static_cast<const __nv_bfloat16 *>(W3);
-    const auto *Wb2 = static_cast<const __nv_bfloat16 *>(W2);
+    // profilers can select the backward's kernels by this range (no cost without a tool)
+    struct Range {
+        Range() { nvtxRangePushA("moe_backward"); }
+        ~Range() { nvtxRangePop(); }
+    } range;
     cudaError_t e;
 #define MOE_TRY(x)                                   \
     do {                                             \
@@ -903,16 +858,6 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     // 1. sorted-row gates and the padded segment offsets
     MOE_TRY(launch_pdl(bwd_prep_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0, s, 1,
                        slot_of, gates, offsets, P, c.E, gate_r, kseg, dev_status));
-    // 2. transposed weights: W2T [E, f, d]; WT [E, d, K2] = [W1^T | W3^T]
-    const int64_t patches = E * (d / 32) * (f / 64);  // 32 x 64 patches of one weight tensor
-    const dim3 tgrid((unsigned)((patches + 7) / 8));
-    MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb2, c.d, c.f, bf(B.W2T), c.d,
-                       0, patches));
-    MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb1, c.f, c.d, bf(B.WT), B.K2,
-                       0, patches));
-    if (sw)
-        MOE_TRY(launch_pdl(transpose_kernel, tgrid, dim3(256), 0, s, 1, Wb3, c.f, c.d, bf(B.WT),
-                           B.K2, c.f, patches));
     // 3. pre-activations A1 = X W1^T (+ b1), A3 = X W3^T: left in bws by moe_forward_train, or
     // recomputed here
     if (!saved_preact) {
@@ -927,8 +872,9 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     // 4. dHu = dYu W2_e with dYu[r] = dy[sorted_token[r]] (the rows of dy permuted once, as the
     // forward permutes h: a TMA gather would repeat for every column tile)
     MOE_TRY(launch_permute(c, dy, slot_of, bf(B.dYu), dev_status, s));
-    MOE_TRY(launch_gemm_rows(bf(B.dYu), nullptr, 0, bf(B.W2T), P, c.E, c.d, c.f, offsets,
-                             nullptr, bf(B.dHu), dev_status, s));
+    // (W2_e read MN-major: rows o of W2 [E d, f] are the K index)
+    MOE_TRY(launch_gemm_rows_bmn(bf(B.dYu), W2, nullptr, c.d, 0, P, c.E, c.d, c.f, offsets,
+                                 bf(B.dHu), dev_status, s));
     // 5. activation backward: dA, dA1T, dA3T, HT, dg parts, db1 parts
     ActBwd ab;
     ab.A1 = bf(B.A1);
@@ -950,9 +896,9 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     ab.swiglu = sw ? 1 : 0;
     MOE_TRY(launch_pdl(act_bwd_kernel, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256), 0, s, 1,
                        ab, dev_status));
-    // 6. dX = dA [W1 | W3] (one GEMM over K2)
-    MOE_TRY(launch_gemm_rows(bf(B.dA), nullptr, 0, bf(B.WT), P, c.E, B.K2, c.d, offsets, nullptr,
-                             bf(B.dX), dev_status, s));
+    // 6. dX = dA1 W1_e + dA3 W3_e: one GEMM over K2 = [dA1 | dA3], B = W1 then W3 read MN-major
+    MOE_TRY(launch_gemm_rows_bmn(bf(B.dA), W1, sw ? W3 : nullptr, c.f, sw ? c.f / BT : 0, P, c.E,
+                                 B.K2, c.d, offsets, bf(B.dX), dev_status, s));
     // 7. XT and dYsT = (g dy[token])^T in the padded slot layout (+ db2 parts)
     GatherT gx{static_cast<const __nv_bfloat16 *>(h), nullptr, bf(B.XT), nullptr};
     GatherT gy{static_cast<const __nv_bfloat16 *>(dy), gate_r, bf(B.dYsT),

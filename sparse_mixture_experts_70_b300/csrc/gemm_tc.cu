@@ -90,6 +90,11 @@ struct TcArgs {
     // training forward (GEMM1): the pre-activations also go to pre1 (x . W1_e + b1) and, for
     // SwiGLU, pre3 (x . W3_e), [P, N] bf16 each (null: not saved)
     __nv_bfloat16 *pre1, *pre3;
+    // MN-major B (kernels instantiated with MN): B is read from a [rows, N] tensor whose rows are
+    // the K index, as 64 x 64 boxes; expert e's k-block kb is rows e b_krows + 64 kb of tmB, or,
+    // from k-block b_ksplit on (when > 0), rows e b_krows + 64 (kb - b_ksplit) of tmB3 (B is the
+    // two tensors stacked along K). In K-grouped mode, rows kseg[e] + 64 kb.
+    int b_mn, b_ksplit, b_krows;
 };
 
 // The 4 source rows this lane gathers for tile ti (rows 4 lane .. 4 lane + 3 of the tile);
@@ -279,8 +284,9 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
     }
 }
 
-// One CTA per SM; see the file comment. KG: the K-grouped schedule (TcArgs).
-template <bool KG>
+// One CTA per SM; see the file comment. KG: the K-grouped schedule; MN: MN-major B allowed
+// (TcArgs).
+template <bool KG, bool MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -395,7 +401,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     mbar_expect_tx(fb, A_STAGE + B_STAGE);
                     const int kx = kx0 + kb * BK;
                     tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kx, arow);
-                    if (a.epi == EPI_SWIGLU) {
+                    if (MN && a.b_mn) {
+                        // four 64 x 64 boxes along N, rows = this k-block of the expert's B
+                        const bool second = a.b_ksplit > 0 && kb >= a.b_ksplit;
+                        const int krow = KG ? kx
+                                            : ti.e * a.b_krows + (second ? kb - a.b_ksplit : kb) * BK;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(sb + q * (B_STAGE / 4), second ? &tmB3 : &tmB, fb,
+                                        ti.n * BN + q * 64, krow);
+                    } else if (a.epi == EPI_SWIGLU) {
                         tma_load_2d(sb, &tmB, fb, kx, brow);
                         tma_load_2d(sb + B_STAGE / 2, &tmB3, fb, kx, brow);
                     } else {
@@ -474,7 +489,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int stage = 0, acc = 0, eh = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            const bool bmn = MN && a.b_mn;
+            const uint32_t idesc = idesc_bf16(BM, BN) | (bmn ? IDESC_B_MN : 0u);
             for (int t = unit0; t < total && ok; t += ustep) {
                 const Tile ti = KG ? decode_tile_kg(t, a)
                                    : decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
@@ -491,10 +507,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tc_fence_after();
                     if (!idle) {
                         const uint64_t ad = sdesc_k_sw128(sA + stage * A_STAGE);
-                        const uint64_t bd = sdesc_k_sw128(sB + stage * B_STAGE);
+                        const uint64_t bd = bmn ? sdesc_mn_sw128(sB + stage * B_STAGE, B_STAGE / 4)
+                                                : sdesc_k_sw128(sB + stage * B_STAGE);
+                        const uint64_t bstep = bmn ? 2048 >> 4 : 2;  // one K = 16 step
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            umma_bf16(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            umma_bf16(dt, ad + 2 * kk, bd + bstep * kk, idesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit(bar_empty + 8 * stage);
                     if (++stage == STAGES) {
@@ -574,6 +593,7 @@ constexpr int B_HALF = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the B
 constexpr size_t TC_SMEM_PAIR =
     1024 + (size_t)STAGES2 * (A_HALF + B_HALF) + CTL_BYTES + (size_t)EPI_WARPS * EPI_BOX;
 
+template <bool MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
@@ -670,7 +690,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);  // leader's barrier
                     if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_HALF + B_HALF));
                     tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
-                    tma_load_2d_pair(sB + stage * B_HALF, bm, fb, kb * BK, brow);
+                    if (MN && a.b_mn) {
+                        // this CTA's 128 columns of B: two 64 x 64 boxes
+                        const bool second = a.b_ksplit > 0 && kb >= a.b_ksplit;
+                        const int krow = ti.e * a.b_krows + (second ? kb - a.b_ksplit : kb) * BK;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d_pair(sB + stage * B_HALF + q * (B_HALF / 2),
+                                             second ? &tmB3 : &tmB, fb,
+                                             ti.n * BN + rank * (BN / 2) + q * 64, krow);
+                    } else {
+                        tma_load_2d_pair(sB + stage * B_HALF, bm, fb, kb * BK, brow);
+                    }
                     if (++stage == STAGES2) {
                         stage = 0;
                         phase ^= 1u;
@@ -749,7 +780,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
+            const bool bmn = MN && a.b_mn;
+            const uint32_t idesc = idesc_bf16(2 * BM, BN) | (bmn ? IDESC_B_MN : 0u);
             for (int t = unit0; t < total && ok; t += ustep) {
                 if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
                 tc_fence_after();
@@ -761,10 +793,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint64_t ad = sdesc_k_sw128(sA + stage * A_HALF);
-                    const uint64_t bd = sdesc_k_sw128(sB + stage * B_HALF);
+                    const uint64_t bd = bmn ? sdesc_mn_sw128(sB + stage * B_HALF, B_HALF / 2)
+                                            : sdesc_k_sw128(sB + stage * B_HALF);
+                    const uint64_t bstep = bmn ? 2048 >> 4 : 2;  // one K = 16 step
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_pair(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16_pair(dt, ad + 2 * kk, bd + bstep * kk, idesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair_multicast(bar_empty + 8 * stage, BOTH);
                     if (++stage == STAGES2) {
                         stage = 0;
@@ -826,7 +861,7 @@ int pair_clusters() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (!done[dev].load(std::memory_order_acquire)) {
         int n = 0;
-        if (set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel, TC_SMEM_PAIR) ==
+        if (set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel<false>, TC_SMEM_PAIR) ==
             cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * 74);
@@ -839,7 +874,7 @@ int pair_clusters() {
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel, &cfg) != cudaSuccess)
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<false>, &cfg) != cudaSuccess)
                 n = 0;
         }
         cudaGetLastError();
@@ -855,7 +890,8 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
                         uint32_t *dev_status, const FaultHook &hook, cudaStream_t s,
                         const int32_t *A_rows = nullptr, int64_t A_src_rows = 0,
                         const int32_t *out_token = nullptr, const float *out_gate = nullptr,
-                        void *pre1 = nullptr, void *pre3 = nullptr) {
+                        void *pre1 = nullptr, void *pre3 = nullptr, int b_mn = 0,
+                        int b_ksplit = 0, int b_krows = 0) {
     // every B box is 128 rows: one half of the 256-row B tile; a gathered A reads one-row boxes
     CUtensorMap mA, mB, mB3, mO;
     if (A_rows ? !make_map(&mA, A, A_src_rows, K, 1) : !make_map(&mA, A, P, K, BM))
@@ -863,9 +899,18 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     // the output of the TMA-store epilogue: [P, N] rows in sorted order (the scattering top-1
     // GEMM2 writes token rows with per-thread stores instead and never reads this map)
     if (!make_store_map(&mO, out, out_token ? 1 : P, N)) return cudaErrorInvalidValue;
-    if (!make_map(&mB, B, (int64_t)E * N, K, BN / 2)) return cudaErrorInvalidValue;
-    if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, BN / 2))
-        return cudaErrorInvalidValue;
+    if (b_mn) {
+        // B as [E b_krows, N] row-major (rows = K index), read in 64 x 64 boxes; B3 likewise
+        if (A_rows || epi != EPI_STORE || b_krows <= 0 || b_krows % BK != 0)
+            return cudaErrorInvalidValue;
+        if (!make_map(&mB, B, (int64_t)E * b_krows, N, 64)) return cudaErrorInvalidValue;
+        if (!make_map(&mB3, b_ksplit > 0 ? B3 : B, (int64_t)E * b_krows, N, 64))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_map(&mB, B, (int64_t)E * N, K, BN / 2)) return cudaErrorInvalidValue;
+        if (!make_map(&mB3, epi == EPI_SWIGLU ? B3 : B, (int64_t)E * N, K, BN / 2))
+            return cudaErrorInvalidValue;
+    }
     TcArgs a;
     a.offsets = offsets;
     a.bias = bias;
@@ -889,6 +934,9 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.m_tiles = 0;
     a.pre1 = static_cast<__nv_bfloat16 *>(pre1);
     a.pre3 = static_cast<__nv_bfloat16 *>(pre3);
+    a.b_mn = b_mn;
+    a.b_ksplit = b_ksplit;
+    a.b_krows = b_krows;
     // The CTA-pair kernel when experts average at least four M tiles (on an expert's odd last
     // tile the second CTA computes masked rows, a small loss there).
     const int clusters = pair_clusters();
@@ -896,15 +944,29 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     if (pair) {
         const int64_t units = ((P + 2 * BM - 1) / (2 * BM) + E) * (int64_t)a.n_tiles;
         const int64_t ncl = clusters < units ? clusters : units;
-        return launch_pdl(grouped_gemm_pair_kernel, dim3((unsigned)(2 * ncl)), dim3(TC_THREADS),
-                          TC_SMEM_PAIR, s, 2, mA, mB, mB3, mO, a);
+        if (b_mn) {
+            cudaError_t err =
+                set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel<true>, TC_SMEM_PAIR);
+            if (err != cudaSuccess) return err;
+            return launch_pdl(grouped_gemm_pair_kernel<true>, dim3((unsigned)(2 * ncl)),
+                              dim3(TC_THREADS), TC_SMEM_PAIR, s, 2, mA, mB, mB3, mO, a);
+        }
+        return launch_pdl(grouped_gemm_pair_kernel<false>, dim3((unsigned)(2 * ncl)),
+                          dim3(TC_THREADS), TC_SMEM_PAIR, s, 2, mA, mB, mB3, mO, a);
     }
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
     int64_t grid = num_sms();
     if (grid > upper) grid = upper;
-    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<false>, TC_SMEM);
+    if (b_mn) {
+        cudaError_t err =
+            set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<false, true>, TC_SMEM);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(grouped_gemm_tc_kernel<false, true>, dim3((unsigned)grid),
+                          dim3(TC_THREADS), TC_SMEM, s, 1, mA, mB, mB3, mO, a);
+    }
+    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<false, false>, TC_SMEM);
     if (err != cudaSuccess) return err;
-    return launch_pdl(grouped_gemm_tc_kernel<false>, dim3((unsigned)grid), dim3(TC_THREADS),
+    return launch_pdl(grouped_gemm_tc_kernel<false, false>, dim3((unsigned)grid), dim3(TC_THREADS),
                       TC_SMEM, s, 1, mA, mB, mB3, mO, a);
 }
 
@@ -940,13 +1002,14 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     a.M = M;
     a.m_tiles = (M + BM - 1) / BM;
     a.pre1 = a.pre3 = nullptr;
+    a.b_mn = a.b_ksplit = a.b_krows = 0;
     const int64_t units = (int64_t)E * a.m_tiles * a.n_tiles;
     if (units >= (1ll << 31)) return cudaErrorInvalidValue;
     int64_t grid = num_sms();
     if (grid > units) grid = units;
-    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true>, TC_SMEM);
+    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, false>, TC_SMEM);
     if (err != cudaSuccess) return err;
-    return launch_pdl(grouped_gemm_tc_kernel<true>, dim3((unsigned)grid), dim3(TC_THREADS),
+    return launch_pdl(grouped_gemm_tc_kernel<true, false>, dim3((unsigned)grid), dim3(TC_THREADS),
                       TC_SMEM, s, 1, mA, mB, mB, mO, a);
 }
 
@@ -959,6 +1022,18 @@ cudaError_t launch_gemm_rows(const void *A, const int32_t *A_rows, int64_t A_src
     if (P == 0) return cudaSuccess;
     return launch_gemm(A, B, nullptr, P, E, K, N, EPI_STORE, offsets, bias, out, dev_status,
                        FaultHook(), s, A_rows, A_rows ? A_src_rows : 0);
+}
+
+cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, int b_krows,
+                                 int b_ksplit, int64_t P, int E, int K, int N,
+                                 const int32_t *offsets, void *out, uint32_t *dev_status,
+                                 cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    if (K != (b_ksplit > 0 ? 2 * b_krows : b_krows) || (b_ksplit > 0 && b_ksplit * BK != b_krows))
+        return cudaErrorInvalidValue;
+    return launch_gemm(A, B, B3, P, E, K, N, EPI_STORE, offsets, nullptr, out, dev_status,
+                       FaultHook(), s, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 1, b_ksplit,
+                       b_krows);
 }
 
 cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,

@@ -221,6 +221,14 @@ cudaError_t launch_gemm_rows(const void *A, const int32_t *A_rows, int64_t A_src
                              const void *B, int64_t P, int E, int K, int N,
                              const int32_t *offsets, const float *bias, void *out,
                              uint32_t *dev_status, cudaStream_t s);
+// The same with B read MN-major from its natural layout: expert e's B is rows
+// [e b_krows, (e + 1) b_krows) of a [E b_krows, N] tensor (rows = the K index); with
+// b_ksplit = b_krows / 64 > 0, B is that tensor stacked along K on B3's rows (K = 2 b_krows),
+// else K = b_krows. No bias, no gather.
+cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, int b_krows,
+                                 int b_ksplit, int64_t P, int E, int K, int N,
+                                 const int32_t *offsets, void *out, uint32_t *dev_status,
+                                 cudaStream_t s);
 // K-grouped tensor-core GEMM (weight gradients): out[e M + m, n] = sum_{k in [kseg[e],
 // kseg[e+1])} A[m, k] B[n, k]; A [M, kwidth], B [N, kwidth] bf16 with zero pad columns; kseg
 // device int32 [E+1], multiples of 64. Empty segments give zero tiles.

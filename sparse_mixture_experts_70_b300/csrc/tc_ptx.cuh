@@ -247,6 +247,20 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     d |= (uint64_t)2 << 61;
     return d;
 }
+// Shared-memory descriptor of an MN-major operand stored as TMA boxes of 64 K rows x 64 MN
+// elements (128 bytes, 128-byte swizzle; 8 KiB per box): the canonical MN-major SW128 layout
+// with its 64-element MN blocks `lbo` bytes apart (leading byte offset) and its 8-row K groups
+// 1024 bytes apart (stride byte offset). One K = 16 step of an MMA is 16 rows: +2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction-descriptor bits that mark A (bit 15) or B (bit 16) as MN-major.
+constexpr uint32_t IDESC_A_MN = 1u << 15, IDESC_B_MN = 1u << 16;
 // Instruction descriptor of kind::f16: f32 accumulator (bits 4-5 = 1), A and B bf16 (bits 7-9,
 // 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {

@@ -98,6 +98,8 @@ CASES = [
     (wl.small("bwd_tc_router", T=3000, d=256, f=256, E=8, k=2, seed=26), {}, 0.05, 0.02),
     (wl.small("bwd_zero_expert", T=300, d=128, f=128, E=6, k=2, seed=27), dict(zero_expert=True),
      0.0, 0.0),
+    # experts of at least four row tiles: the data-gradient GEMMs take the CTA-pair kernel
+    (wl.small("bwd_pair", T=1100, d=128, f=320, E=2, k=2, seed=29), {}, 0.0, 0.0),
 ]
 
 
