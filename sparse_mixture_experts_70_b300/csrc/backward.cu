@@ -10,20 +10,23 @@
 //     L = sum dy * y + aux_weight * (E sum_e f_e P_e) + zloss_weight * zloss.
 //
 // With X the permuted rows of h, a slot r of expert e with gate g_r, and dYu[r] = dy[token(r)]:
-//   A1 = X W1_e^T (+ b1), A3 = X W3_e^T           recomputed (two row-grouped GEMMs)
-//   dHu = dYu W2_e                                 row-grouped GEMM, dy rows gathered by TMA
+//   A1 = X W1_e^T (+ b1), A3 = X W3_e^T     saved by the training forward, or recomputed (two
+//                                           row-grouped GEMMs)
+//   dHu = dYu W2_e                           row-grouped GEMM
 //   SwiGLU: Hact = SiLU(A1) A3, dA1 = g dHu A3 SiLU'(A1), dA3 = g dHu SiLU(A1)
 //   GELU  : Hact = GELU(A1),    dA1 = g dHu GELU'(A1)
-//   dg_r = dHu . Hact (+ dy . b2_e)                gradient of the slot's gate
-//   dX = dA1 W1_e + dA3 W3_e                        one row-grouped GEMM over K = [dA1 | dA3]
-// The data-gradient GEMMs read W2, W1 and W3 in their stored layouts as MN-major operands.
-//   dW2_e = (g dYu)^T Hact, dW1_e = dA1^T X, dW3_e = dA3^T X   K-grouped GEMMs over the slots
+//   dg_r = dHu . Hact (+ dy . b2_e)          gradient of the slot's gate
+//   dX = dA1 W1_e + dA3 W3_e                  one row-grouped GEMM over K = [dA1 | dA3]
+//   dW2_e = dYu^T (g Hact), dW1_e = dA1^T X, dW3_e = dA3^T X   K-grouped GEMMs over the slots
 //   db2_e = sum_r g_r dYu[r], db1_e = sum_r dA1[r]
 //   router: dz from dg through the gate softmax (RENORM) or p (RAW_PROB), plus the auxiliary
 //           term and the z-loss; dh = sum_j dX[slot] + dz W_r^T, dW_r = h^T dz, db_r = sum dz.
-// The weight-gradient GEMMs contract over slots, so their operands are stored transposed with
-// every expert's slots padded to a multiple of 64 columns (zeros in the pad): segment e of the
-// padded slot axis is [kseg[e], kseg[e+1]), kseg[e+1] - kseg[e] = roundup64(count_e).
+// Layout: the per-slot tensors of the backward (rows of h and dy, dHu, dA, g Hact, dX) live in a
+// padded row layout, expert e's slots at rows [kseg[e], kseg[e+1]) with kseg[e+1] - kseg[e] =
+// roundup64(count_e) and zero pad rows. Every GEMM reads its operands in their stored layouts:
+// the data-gradient GEMMs take W2, W1 and W3 as MN-major B operands, and the weight-gradient
+// GEMMs, which contract over each expert's slots (the rows), take both operands MN-major in
+// 64-row K blocks that never straddle two experts.
 #include <nvtx3/nvToolsExt.h>
 
 #include "internal.cuh"
@@ -91,44 +94,39 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, c
 }
 
 // ---------------------------------------------------------------------------------------------
-// Gather-transpose into the padded slot layout: dst[i][c] = scale_r src[sorted_token[r]][i] for
-// padded column c of segment e holding sorted row r = offsets[e] + c - kseg[e], zero in the pad.
-// blockIdx.z selects one of two jobs (X: h, no scale; dYs: dy scaled by the row's gate, with the
-// column-tile sums of the scaled values in part [kw/64][d] when part is given, for db2).
-struct GatherT {
-    const __nv_bfloat16 *src;
-    const float *scale;  // gate_r or null
-    __nv_bfloat16 *dst;  // [d, kw]
-    float *part;         // [kw/64, d] or null
-};
-__global__ void __launch_bounds__(256) gather_transpose_kernel(GatherT j0, GatherT j1,
-                                                               const int32_t *sorted_token,
-                                                               const int32_t *offsets,
-                                                               const int32_t *kseg_g, int E,
-                                                               int64_t T, int64_t P, int d,
-                                                               int64_t kw, uint32_t *dev_status) {
-    __shared__ float tile[BT][BT + 1];  // [slot j][feature i]
+// Padded-row gathers: for padded row c = kseg[e] + l of expert e, when l < count_e (sorted row
+// r = offsets[e] + l, token t = sorted_token[r]): Xp[c] = h[t] and dYp[c] = dy[t]; pad rows are
+// zero. When db2_part is given, db2_part[tile][o] is the tile's sum of gate_r[r] dy[t, o].
+// Block (x, y): the 64 rows of tile x, columns [2048 y, 2048 y + 2048), 8 per thread.
+constexpr int GP_COLS = 2048;
+__global__ void __launch_bounds__(256) gather_pad_kernel(const __nv_bfloat16 *h,
+                                                         const __nv_bfloat16 *dy,
+                                                         const int32_t *sorted_token,
+                                                         const int32_t *offsets,
+                                                         const int32_t *kseg_g,
+                                                         const float *gate_r, int E, int64_t T,
+                                                         int64_t P, int d, __nv_bfloat16 *Xp,
+                                                         __nv_bfloat16 *dYp, float *db2_part,
+                                                         uint32_t *dev_status) {
     __shared__ int32_t kseg[257];
     __shared__ int32_t tok[BT];
     __shared__ float scl[BT];
     pdl_wait();
-    const GatherT J = blockIdx.z == 0 ? j0 : j1;
     for (int e = threadIdx.x; e <= E; e += blockDim.x) kseg[e] = kseg_g[e];
     __syncthreads();
     const int c0 = blockIdx.x * BT;
-    if (J.src == nullptr || c0 >= kseg[E]) {
+    if (c0 >= kseg[E]) {
         pdl_trigger();
         return;
     }
     const int e = segment_of(kseg, E, c0);
     const int cnt = offsets[e + 1] - offsets[e];
     const int local0 = c0 - kseg[e];
-    const int i0 = blockIdx.y * BT;
     if (threadIdx.x < BT) {
         const int l = local0 + threadIdx.x;
+        const int r = offsets[e] + l;
         int t = -1;
         float sc = 0.f;
-        const int r = offsets[e] + l;
         if (l < cnt && (r < 0 || (int64_t)r >= P)) report(dev_status, DEV_ERR_INDEX);
         if (l < cnt && r >= 0 && (int64_t)r < P) {
             t = sorted_token[r];
@@ -136,69 +134,59 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(GatherT j0, Gathe
                 report(dev_status, DEV_ERR_INDEX);
                 t = -1;
             } else {
-                sc = J.scale ? J.scale[r] : 1.f;
+                sc = gate_r[r];
             }
         }
         tok[threadIdx.x] = t;
         scl[threadIdx.x] = sc;
     }
     __syncthreads();
-    // rows of src (one 64-feature chunk each), 8 features per thread-step
-    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
-        const int jr = i >> 3, ch = i & 7;
-        float v[8];
-        if (tok[jr] >= 0) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
-                                      J.src + (int64_t)tok[jr] * d + i0) + ch);
-            unpack8(u, v);
+    const int col = blockIdx.y * GP_COLS + threadIdx.x * 8;
+    if (col < d) {
+        float acc[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] *= scl[jr];
-        } else {
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll 4
+        for (int jr = 0; jr < BT; ++jr) {
+            const int t = tok[jr];
+            uint4 hv = make_uint4(0, 0, 0, 0), dv = make_uint4(0, 0, 0, 0);
+            if (t >= 0) {
+                hv = __ldg(reinterpret_cast<const uint4 *>(h + (int64_t)t * d + col));
+                dv = __ldg(reinterpret_cast<const uint4 *>(dy + (int64_t)t * d + col));
+            }
+            const int64_t o = (int64_t)(c0 + jr) * d + col;
+            *reinterpret_cast<uint4 *>(Xp + o) = hv;
+            *reinterpret_cast<uint4 *>(dYp + o) = dv;
+            if (db2_part) {
+                float v[8];
+                unpack8(dv, v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = 0.f;
+                for (int q = 0; q < 8; ++q) acc[q] = fmaf(scl[jr], v[q], acc[q]);
+            }
         }
+        if (db2_part) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) tile[jr][ch * 8 + q] = v[q];
-    }
-    __syncthreads();
-    // transposed rows: feature i, 64 padded columns; column-tile sums for the bias gradient
-    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
-        const int fi = i >> 3, ch = i & 7;
-        float v[8];
-        float sum = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            v[q] = tile[ch * 8 + q][fi];
-            sum += v[q];
-        }
-        const uint4 u = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
-                                   pack2(v[6], v[7]));
-        *reinterpret_cast<uint4 *>(J.dst + (int64_t)(i0 + fi) * kw + c0 + ch * 8) = u;
-        if (J.part) {
-            // the 8 threads of feature fi are 8 consecutive lanes: sum them in a fixed order
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (ch == 0) J.part[(int64_t)blockIdx.x * d + i0 + fi] = sum;
+            for (int q = 0; q < 8; ++q) db2_part[(int64_t)blockIdx.x * d + col + q] = acc[q];
         }
     }
     pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------------------
-// Activation backward on one 64-slot x 64-feature tile: padded columns [c0, c0 + 64) of one
-// expert (blockIdx.x), features [n0, n0 + 64) (blockIdx.y). Reads A1 (and A3), dHu and the row
-// gates; writes dA [rows, K'] row-major (dA1 in columns [0, f), dA3 in [f, 2f) for SwiGLU), the
-// transposed dA1T, dA3T and HT = Hact^T [f, kw] (zeros in the pad), dg_part[n-tile][r] = the
-// tile's part of dHu . Hact, and (when db1_part is given) the tile's column sums of dA1.
+// Activation backward on one 64-row x 64-feature tile: padded rows [c0, c0 + 64) of one expert
+// (blockIdx.x), features [n0, n0 + 64) (blockIdx.y). Reads the pre-activations A1 (and A3) of
+// sorted row r = offsets[e] + l, dHu of padded row c = kseg[e] + l, and the row's gate g; writes
+// padded rows of dA [kw, K2] (dA1 in columns [0, f), dA3 in [f, 2f) for SwiGLU) and of
+// Hs = g Hact [kw, f] (pad rows zero), dg_part[n-tile][r] = the tile's part of dHu . Hact, and
+// (when db1_part is given) the tile's column sums of dA1.
 struct ActBwd {
     const __nv_bfloat16 *A1, *A3, *dHu;
     const float *gate_r;
     const int32_t *offsets, *kseg;
-    __nv_bfloat16 *dA, *dA1T, *dA3T, *HT;
+    __nv_bfloat16 *dA, *Hs;
     float *dg_part;   // [f/64, P]
     float *db1_part;  // [kw/64, f] or null
-    int64_t P, kw;
+    int64_t P;
     int E, f, swiglu;
 };
 
@@ -210,9 +198,7 @@ __device__ __forceinline__ float gelu_tanh_acc(float x, float &slope) {
 }
 
 __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *dev_status) {
-    __shared__ float s1[BT][BT + 1];            // dA1 (f32, for the bias sums)
-    __shared__ __nv_bfloat16 s3[BT][BT + 2];    // dA3
-    __shared__ __nv_bfloat16 sh[BT][BT + 2];    // Hact
+    __shared__ float s1[BT][BT + 1];  // dA1 (f32) for the bias sums
     __shared__ int32_t kseg[257];
     pdl_wait();
     for (int e = threadIdx.x; e <= a.E; e += blockDim.x) kseg[e] = a.kseg[e];
@@ -223,7 +209,7 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
         return;
     }
     const int e = segment_of(kseg, a.E, c0);
-    const int rbase = a.offsets[e] + (c0 - kseg[e]);  // sorted row of column c0
+    const int rbase = a.offsets[e] + (c0 - kseg[e]);  // sorted row of padded row c0
     const int rend = a.offsets[e + 1];
     if (rend > a.P || rbase < 0) {
         report(dev_status, DEV_ERR_INDEX);
@@ -236,49 +222,52 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
         const int jr = i >> 3, ch = i & 7;
         const int r = rbase + jr;
         const bool valid = r < rend;
-        float d1[8], d3[8], hv[8];
+        float d1[8], d3[8], hs[8];
         float dg = 0.f;
         if (valid) {
             const int64_t off = (int64_t)r * a.f + n0 + ch * 8;
             float x1[8], x3[8], du[8];
             unpack8(__ldg(reinterpret_cast<const uint4 *>(a.A1 + off)), x1);
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.dHu + off)), du);
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(
+                        a.dHu + (int64_t)(c0 + jr) * a.f + n0 + ch * 8)), du);
             if (a.swiglu) unpack8(__ldg(reinterpret_cast<const uint4 *>(a.A3 + off)), x3);
             const float g = a.gate_r[r];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
+                float hv;
                 if (a.swiglu) {
                     const float sg = 1.f / (1.f + expf(-x1[q]));
                     const float si = x1[q] * sg;
-                    hv[q] = si * x3[q];
+                    hv = si * x3[q];
                     d1[q] = g * du[q] * x3[q] * sg * (1.f + x1[q] * (1.f - sg));
                     d3[q] = g * du[q] * si;
                 } else {
                     float slope;
-                    hv[q] = gelu_tanh_acc(x1[q], slope);
+                    hv = gelu_tanh_acc(x1[q], slope);
                     d1[q] = g * du[q] * slope;
                     d3[q] = 0.f;
                 }
-                dg += du[q] * hv[q];
+                hs[q] = g * hv;
+                dg += du[q] * hv;
             }
-            __nv_bfloat16 *row = a.dA + (int64_t)r * K2 + n0 + ch * 8;
-            *reinterpret_cast<uint4 *>(row) =
-                make_uint4(pack2(d1[0], d1[1]), pack2(d1[2], d1[3]), pack2(d1[4], d1[5]),
-                           pack2(d1[6], d1[7]));
-            if (a.swiglu)
-                *reinterpret_cast<uint4 *>(row + a.f) =
-                    make_uint4(pack2(d3[0], d3[1]), pack2(d3[2], d3[3]), pack2(d3[4], d3[5]),
-                               pack2(d3[6], d3[7]));
         } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) d1[q] = d3[q] = hv[q] = 0.f;
+            for (int q = 0; q < 8; ++q) d1[q] = d3[q] = hs[q] = 0.f;
         }
+        __nv_bfloat16 *row = a.dA + (int64_t)(c0 + jr) * K2 + n0 + ch * 8;
+        *reinterpret_cast<uint4 *>(row) =
+            make_uint4(pack2(d1[0], d1[1]), pack2(d1[2], d1[3]), pack2(d1[4], d1[5]),
+                       pack2(d1[6], d1[7]));
+        if (a.swiglu)
+            *reinterpret_cast<uint4 *>(row + a.f) =
+                make_uint4(pack2(d3[0], d3[1]), pack2(d3[2], d3[3]), pack2(d3[4], d3[5]),
+                           pack2(d3[6], d3[7]));
+        *reinterpret_cast<uint4 *>(a.Hs + (int64_t)(c0 + jr) * a.f + n0 + ch * 8) =
+            make_uint4(pack2(hs[0], hs[1]), pack2(hs[2], hs[3]), pack2(hs[4], hs[5]),
+                       pack2(hs[6], hs[7]));
+        if (a.db1_part) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) s1[jr][ch * 8 + q] = d1[q];
-#pragma unroll
-        for (int q = 0; q < 8; q += 2) {
-            *reinterpret_cast<uint32_t *>(&s3[jr][ch * 8 + q]) = pack2(d3[q], d3[q + 1]);
-            *reinterpret_cast<uint32_t *>(&sh[jr][ch * 8 + q]) = pack2(hv[q], hv[q + 1]);
+            for (int q = 0; q < 8; ++q) s1[jr][ch * 8 + q] = d1[q];
         }
         // the row's 8 feature groups are 8 consecutive lanes: sum them in a fixed order
         dg += __shfl_xor_sync(0xffffffffu, dg, 1);
@@ -286,30 +275,12 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
         dg += __shfl_xor_sync(0xffffffffu, dg, 4);
         if (valid && ch == 0) a.dg_part[(int64_t)blockIdx.y * a.P + r] = dg;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
-        const int fi = i >> 3, ch = i & 7;
-        float v1[8];
-        float sum = 0.f;
-        __align__(16) __nv_bfloat16 o3[8], oh[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            v1[q] = s1[ch * 8 + q][fi];
-            sum += v1[q];
-            o3[q] = s3[ch * 8 + q][fi];
-            oh[q] = sh[ch * 8 + q][fi];
-        }
-        const int64_t off = (int64_t)(n0 + fi) * a.kw + c0 + ch * 8;
-        *reinterpret_cast<uint4 *>(a.dA1T + off) =
-            make_uint4(pack2(v1[0], v1[1]), pack2(v1[2], v1[3]), pack2(v1[4], v1[5]),
-                       pack2(v1[6], v1[7]));
-        if (a.swiglu) *reinterpret_cast<uint4 *>(a.dA3T + off) = *reinterpret_cast<const uint4 *>(o3);
-        *reinterpret_cast<uint4 *>(a.HT + off) = *reinterpret_cast<const uint4 *>(oh);
-        if (a.db1_part) {
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (ch == 0) a.db1_part[(int64_t)blockIdx.x * a.f + n0 + fi] = sum;
+    if (a.db1_part) {
+        __syncthreads();
+        if (threadIdx.x < BT) {
+            float sum = 0.f;
+            for (int jr = 0; jr < BT; ++jr) sum += s1[jr][threadIdx.x];
+            a.db1_part[(int64_t)blockIdx.x * a.f + n0 + threadIdx.x] = sum;
         }
     }
     pdl_trigger();
@@ -496,18 +467,25 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint
 }
 
 // ---------------------------------------------------------------------------------------------
-// dh[t, i] = sum_j dX[slot_of[t, j], i] + sum_e dz[t, e] W_r[i, e]: 64 tokens x 64 features per
-// block; thread (ig = tid % 16, tg = tid / 16) owns tokens 4 tg .. 4 tg + 3 and features
+// dh[t, i] = sum_j dX[c(t, j), i] + sum_e dz[t, e] W_r[i, e], where c(t, j) is the padded row of
+// slot (t, j): kseg[e] + slot_of[t k + j] - offsets[e] with e = idx[t k + j] (dropped slots
+// contribute nothing). 64 tokens x 64 features per block; thread (ig = tid % 16, tg = tid / 16) owns tokens 4 tg .. 4 tg + 3 and features
 // 4 ig .. 4 ig + 3 (16 accumulators, two 16-byte shared loads per 16 FMAs). Experts go through
 // shared memory 64 at a time: W_r's 64 rows as sw[e][i] and dz as sz[e][t].
 constexpr int DH_T = 64, DH_ECH = 64, DH_LD = 68;
 __global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const int32_t *slot_of,
-                                                 const float *dz, const float *W_r, int64_t T,
-                                                 int d, int E, int k, int64_t rows,
+                                                 const int32_t *idx, const int32_t *offsets_g,
+                                                 const int32_t *kseg_g, const float *dz,
+                                                 const float *W_r, int64_t T, int d, int E, int k,
                                                  __nv_bfloat16 *dh, uint32_t *dev_status) {
     __shared__ __align__(16) float sw[DH_ECH][BT];
     __shared__ __align__(16) float sz[DH_ECH][DH_LD];
+    __shared__ int32_t kseg[257], offs[257];
     pdl_wait();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        kseg[e] = kseg_g[e];
+        offs[e] = offsets_g[e];
+    }
     const int i0 = blockIdx.x * BT;
     const int64_t t0 = (int64_t)blockIdx.y * DH_T;
     const int ig = threadIdx.x & 15, tg = threadIdx.x >> 4;
@@ -545,10 +523,15 @@ __global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const 
         if (t >= T) break;
         for (int j = 0; j < k; ++j) {
             const int r = slot_of[t * k + j];
-            if (r >= rows) report(dev_status, DEV_ERR_INDEX);
-            if (r < 0 || r >= rows) continue;
+            if (r < 0) continue;  // dropped by the capacity
+            const int e = idx[t * k + j];
+            const int c = (e >= 0 && e < E) ? kseg[e] + (r - offs[e]) : -1;
+            if (e < 0 || e >= E || r < offs[e] || c >= kseg[e + 1]) {
+                report(dev_status, DEV_ERR_INDEX);
+                continue;
+            }
             const uint2 u =
-                __ldg(reinterpret_cast<const uint2 *>(dX + (int64_t)r * d + i0 + ig * 4));
+                __ldg(reinterpret_cast<const uint2 *>(dX + (int64_t)c * d + i0 + ig * 4));
             const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
             const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
             acc[a][0] += __low2float(p0);
@@ -689,7 +672,7 @@ int dwr_ept(int E) { return E <= 16 ? 1 : E <= 32 ? 2 : E <= 64 ? 4 : 8; }
 int dwr_etiles(int E) { return (E + 16 * dwr_ept(E) - 1) / (16 * dwr_ept(E)); }
 
 struct BwdLayout {
-    size_t gate_r, kseg, A1, A3, dHu, dYu, dA, dA1T, dA3T, HT, dX, XT, dYsT, dg_part,
+    size_t gate_r, kseg, A1, A3, Xp, dYp, dHu, dA, Hs, dX, dg_part,
         db1_part, db2_part, dz, dwr_part, dwr_partb, total;
     int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
     int K2, n_part, nsplit;
@@ -719,15 +702,13 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     L.kseg = off;       off = al(off + (E + 1) * 4);
     L.A1 = off;         off = al(off + (size_t)P * f * 2);
     L.A3 = off;         off = al(off + (sw ? (size_t)P * f * 2 : 0));
-    L.dHu = off;        off = al(off + (size_t)P * f * 2);
-    L.dYu = off;        off = al(off + (size_t)P * d * 2);
-    L.dA = off;         off = al(off + (size_t)P * (size_t)L.K2 * 2);
-    L.dA1T = off;       off = al(off + f * kw * 2);
-    L.dA3T = off;       off = al(off + (sw ? f * kw * 2 : 0));
-    L.HT = off;         off = al(off + f * kw * 2);
-    L.dX = off;         off = al(off + (size_t)P * d * 2);
-    L.XT = off;         off = al(off + d * kw * 2);
-    L.dYsT = off;       off = al(off + d * kw * 2);
+    // padded row layout [kw, .]: expert e's slots at rows [kseg[e], kseg[e+1]), pad rows zero
+    L.Xp = off;         off = al(off + kw * d * 2);
+    L.dYp = off;        off = al(off + kw * d * 2);
+    L.dHu = off;        off = al(off + kw * f * 2);
+    L.dA = off;         off = al(off + kw * (size_t)L.K2 * 2);
+    L.Hs = off;         off = al(off + kw * f * 2);
+    L.dX = off;         off = al(off + kw * d * 2);
     L.dg_part = off;    off = al(off + (size_t)L.n_part * (size_t)P * 4);
     L.db1_part = off;   off = al(off + (c.has_bias ? nt * f * 4 : 0));
     L.db2_part = off;   off = al(off + (c.has_bias ? nt * d * 4 : 0));
@@ -763,7 +744,7 @@ int backward_launches(const moe_config_t &c, bool saved) {
     const bool sw = c.act == MOE_ACT_SWIGLU;
     const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
     return 1 /*prep*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
-           2 /*dy permute, dHu*/ + 1 /*act*/ + 1 /*dX*/ + 1 /*gather-transpose*/ + (sw ? 3 : 2) /*dW*/ +
+           2 /*padded gathers, dHu*/ + 1 /*act*/ + 1 /*dX*/ + (sw ? 3 : 2) /*dW*/ +
            router + 1 /*router bwd*/ + 1 /*dh*/ + 2 /*dW_r*/ + (c.has_bias ? 2 : 0);
 }
 
@@ -850,10 +831,9 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         Range() { nvtxRangePushA("moe_backward"); }
         ~Range() { nvtxRangePop(); }
     } range;
-    cudaError_t e;
-#define MOE_TRY(x)                                   \
-    do {                                             \
-        if ((e = (x)) != cudaSuccess) return MOE_ERR_CUDA; \
+#define MOE_TRY(x)                                     \
+    do {                                               \
+        if ((x) != cudaSuccess) return MOE_ERR_CUDA;   \
     } while (0)
     // 1. sorted-row gates and the padded segment offsets
     MOE_TRY(launch_pdl(bwd_prep_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0, s, 1,
@@ -869,51 +849,48 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
             MOE_TRY(launch_gemm_rows(xa, xrows, c.T, W3, P, c.E, c.d, c.f, offsets, nullptr,
                                      bf(B.A3), dev_status, s));
     }
-    // 4. dHu = dYu W2_e with dYu[r] = dy[sorted_token[r]] (the rows of dy permuted once, as the
-    // forward permutes h: a TMA gather would repeat for every column tile)
-    MOE_TRY(launch_permute(c, dy, slot_of, bf(B.dYu), dev_status, s));
-    // (W2_e read MN-major: rows o of W2 [E d, f] are the K index)
-    MOE_TRY(launch_gemm_rows_bmn(bf(B.dYu), W2, nullptr, c.d, 0, P, c.E, c.d, c.f, offsets,
+    // 4. padded rows of h and dy (+ db2 parts), then dHu = dYp W2_e over each expert's padded
+    // rows (W2_e read MN-major: rows o of W2 [E d, f] are the K index)
+    const int32_t *ksegc = kseg;
+    MOE_TRY(launch_pdl(gather_pad_kernel,
+                       dim3((unsigned)(B.kw / BT), (unsigned)((c.d + GP_COLS - 1) / GP_COLS)),
+                       dim3(256), 0, s, 1, static_cast<const __nv_bfloat16 *>(h),
+                       static_cast<const __nv_bfloat16 *>(dy), sorted_token, offsets, ksegc,
+                       static_cast<const float *>(gate_r), c.E, c.T, P, c.d, bf(B.Xp), bf(B.dYp),
+                       c.has_bias ? fl(B.db2_part) : nullptr, dev_status));
+    MOE_TRY(launch_gemm_rows_bmn(bf(B.dYp), W2, nullptr, c.d, 0, B.kw, c.E, c.d, c.f, ksegc,
                                  bf(B.dHu), dev_status, s));
-    // 5. activation backward: dA, dA1T, dA3T, HT, dg parts, db1 parts
+    // 5. activation backward: dA, Hs = g Hact (padded rows), dg parts, db1 parts
     ActBwd ab;
     ab.A1 = bf(B.A1);
     ab.A3 = sw ? bf(B.A3) : nullptr;
     ab.dHu = bf(B.dHu);
     ab.gate_r = gate_r;
     ab.offsets = offsets;
-    ab.kseg = kseg;
+    ab.kseg = ksegc;
     ab.dA = bf(B.dA);
-    ab.dA1T = bf(B.dA1T);
-    ab.dA3T = sw ? bf(B.dA3T) : nullptr;
-    ab.HT = bf(B.HT);
+    ab.Hs = bf(B.Hs);
     ab.dg_part = fl(B.dg_part);
     ab.db1_part = c.has_bias ? fl(B.db1_part) : nullptr;
     ab.P = P;
-    ab.kw = B.kw;
     ab.E = c.E;
     ab.f = c.f;
     ab.swiglu = sw ? 1 : 0;
     MOE_TRY(launch_pdl(act_bwd_kernel, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256), 0, s, 1,
                        ab, dev_status));
-    // 6. dX = dA1 W1_e + dA3 W3_e: one GEMM over K2 = [dA1 | dA3], B = W1 then W3 read MN-major
-    MOE_TRY(launch_gemm_rows_bmn(bf(B.dA), W1, sw ? W3 : nullptr, c.f, sw ? c.f / BT : 0, P, c.E,
-                                 B.K2, c.d, offsets, bf(B.dX), dev_status, s));
-    // 7. XT and dYsT = (g dy[token])^T in the padded slot layout (+ db2 parts)
-    GatherT gx{static_cast<const __nv_bfloat16 *>(h), nullptr, bf(B.XT), nullptr};
-    GatherT gy{static_cast<const __nv_bfloat16 *>(dy), gate_r, bf(B.dYsT),
-               c.has_bias ? fl(B.db2_part) : nullptr};
-    MOE_TRY(launch_pdl(gather_transpose_kernel, dim3((unsigned)(B.kw / BT), c.d / BT, 2),
-                       dim3(256), 0, s, 1, gx, gy, sorted_token, offsets,
-                       static_cast<const int32_t *>(kseg), c.E, c.T, P, c.d, B.kw, dev_status));
-    // 8. weight gradients over each expert's slots
-    MOE_TRY(launch_gemm_kgroup(bf(B.dYsT), bf(B.HT), kseg, c.E, c.d, c.f, B.kw, dW2, dev_status,
-                               s));
-    MOE_TRY(launch_gemm_kgroup(bf(B.dA1T), bf(B.XT), kseg, c.E, c.f, c.d, B.kw, dW1, dev_status,
-                               s));
+    // 6. dX = dA1 W1_e + dA3 W3_e over the padded rows: one GEMM over K2 = [dA1 | dA3], B = W1
+    // then W3 read MN-major
+    MOE_TRY(launch_gemm_rows_bmn(bf(B.dA), W1, sw ? W3 : nullptr, c.f, sw ? c.f / BT : 0, B.kw,
+                                 c.E, B.K2, c.d, ksegc, bf(B.dX), dev_status, s));
+    // 7. weight gradients over each expert's padded rows, every operand MN-major:
+    //    dW2_e = dYp^T Hs, dW1_e = dA1^T Xp, dW3_e = dA3^T Xp
+    MOE_TRY(launch_gemm_kgroup_mn(bf(B.dYp), c.d, bf(B.Hs), c.f, ksegc, c.E, c.d, c.f, B.kw, dW2,
+                                  dev_status, s));
+    MOE_TRY(launch_gemm_kgroup_mn(bf(B.dA), B.K2, bf(B.Xp), c.d, ksegc, c.E, c.f, c.d, B.kw, dW1,
+                                  dev_status, s));
     if (sw)
-        MOE_TRY(launch_gemm_kgroup(bf(B.dA3T), bf(B.XT), kseg, c.E, c.f, c.d, B.kw, dW3,
-                                   dev_status, s));
+        MOE_TRY(launch_gemm_kgroup_mn(bf(B.dA) + c.f, B.K2, bf(B.Xp), c.d, ksegc, c.E, c.f, c.d,
+                                      B.kw, dW3, dev_status, s));
     // 9. router: logits (tensor-core partials when the forward used them), dz
     RouterBwd rb;
     rb.h = static_cast<const __nv_bfloat16 *>(h);
@@ -948,13 +925,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     rb.dz = fl(B.dz);
     MOE_TRY(launch_pdl(router_bwd_kernel, dim3((unsigned)((c.T + 7) / 8)), dim3(256), 0, s, 1, rb,
                        dev_status));
-    // 10. dh = sum_j dX[slot] + dz W_r^T
-    {
-        MOE_TRY(launch_pdl(dh_kernel, dim3(c.d / BT, (unsigned)((c.T + DH_T - 1) / DH_T)),
-                           dim3(256), 0, s, 1, static_cast<const __nv_bfloat16 *>(bf(B.dX)), slot_of,
-                           static_cast<const float *>(fl(B.dz)), W_r, c.T, c.d, c.E, c.k, P,
-                           static_cast<__nv_bfloat16 *>(dh), dev_status));
-    }
+    // 10. dh = sum_j dX[padded row of slot j] + dz W_r^T
+    MOE_TRY(launch_pdl(dh_kernel, dim3(c.d / BT, (unsigned)((c.T + DH_T - 1) / DH_T)), dim3(256),
+                       0, s, 1, static_cast<const __nv_bfloat16 *>(bf(B.dX)), slot_of, idx,
+                       offsets, ksegc, static_cast<const float *>(fl(B.dz)), W_r, c.T, c.d, c.E,
+                       c.k, static_cast<__nv_bfloat16 *>(dh), dev_status));
     // 11. dW_r = h^T dz, db_r = sum dz (split over tokens, then summed in split order)
     {
         float *part = fl(B.dwr_part), *partb = b_r ? fl(B.dwr_partb) : nullptr;

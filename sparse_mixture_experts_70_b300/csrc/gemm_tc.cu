@@ -95,6 +95,9 @@ struct TcArgs {
     // from k-block b_ksplit on (when > 0), rows e b_krows + 64 (kb - b_ksplit) of tmB3 (B is the
     // two tensors stacked along K). In K-grouped mode, rows kseg[e] + 64 kb.
     int b_mn, b_ksplit, b_krows;
+    // MN-major A (K-grouped mode with MN): A is [K rows, M] (rows = the K index), read as two
+    // 64 x 64 boxes at columns m 128 and m 128 + 64, rows kseg[e] + 64 kb
+    int a_mn;
 };
 
 // The 4 source rows this lane gathers for tile ti (rows 4 lane .. 4 lane + 3 of the tile);
@@ -400,7 +403,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t sb = sB + stage * B_STAGE;
                     mbar_expect_tx(fb, A_STAGE + B_STAGE);
                     const int kx = kx0 + kb * BK;
-                    tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kx, arow);
+                    if (MN && a.a_mn) {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d(sA + stage * A_STAGE + q * (A_STAGE / 2), &tmA, fb,
+                                        arow + q * 64, kx);
+                    } else {
+                        tma_load_2d(sA + stage * A_STAGE, &tmA, fb, kx, arow);
+                    }
                     if (MN && a.b_mn) {
                         // four 64 x 64 boxes along N, rows = this k-block of the expert's B
                         const bool second = a.b_ksplit > 0 && kb >= a.b_ksplit;
@@ -489,8 +499,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int stage = 0, acc = 0, eh = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            const bool bmn = MN && a.b_mn;
-            const uint32_t idesc = idesc_bf16(BM, BN) | (bmn ? IDESC_B_MN : 0u);
+            const bool bmn = MN && a.b_mn, amn = MN && a.a_mn;
+            const uint32_t idesc =
+                idesc_bf16(BM, BN) | (bmn ? IDESC_B_MN : 0u) | (amn ? IDESC_A_MN : 0u);
             for (int t = unit0; t < total && ok; t += ustep) {
                 const Tile ti = KG ? decode_tile_kg(t, a)
                                    : decode_tile<PAIR>(t, eh, s_cum, s_off, a.n_tiles, rank);
@@ -506,13 +517,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     tc_fence_after();
                     if (!idle) {
-                        const uint64_t ad = sdesc_k_sw128(sA + stage * A_STAGE);
+                        const uint64_t ad = amn ? sdesc_mn_sw128(sA + stage * A_STAGE, A_STAGE / 2)
+                                                : sdesc_k_sw128(sA + stage * A_STAGE);
                         const uint64_t bd = bmn ? sdesc_mn_sw128(sB + stage * B_STAGE, B_STAGE / 4)
                                                 : sdesc_k_sw128(sB + stage * B_STAGE);
-                        const uint64_t bstep = bmn ? 2048 >> 4 : 2;  // one K = 16 step
+                        // one K = 16 step: 32 bytes along a K-major row, 16 rows of an MN-major box
+                        const uint64_t astep = amn ? 2048 >> 4 : 2, bstep = bmn ? 2048 >> 4 : 2;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            umma_bf16(dt, ad + 2 * kk, bd + bstep * kk, idesc,
+                            umma_bf16(dt, ad + astep * kk, bd + bstep * kk, idesc,
                                       (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit(bar_empty + 8 * stage);
@@ -937,6 +950,7 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.b_mn = b_mn;
     a.b_ksplit = b_ksplit;
     a.b_krows = b_krows;
+    a.a_mn = 0;
     // The CTA-pair kernel when experts average at least four M tiles (on an expert's odd last
     // tile the second CTA computes masked rows, a small loss there).
     const int clusters = pair_clusters();
@@ -970,16 +984,24 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
                       TC_SMEM, s, 1, mA, mB, mB3, mO, a);
 }
 
-// K-grouped GEMM: out[e M + m, n] = sum over k in [kseg[e], kseg[e+1]) of A[m, k] B[n, k] for
-// every expert e (zeros where the segment is empty). A [M, kwidth], B [N, kwidth], out [E M, N],
-// all bf16 row-major; kseg [E+1] device int32, multiples of 64, pad columns zero.
+// K-grouped GEMM: out[e M + m, n] = sum over k in [kseg[e], kseg[e+1]) of A(m, k) B(n, k) for
+// every expert e (zeros where the segment is empty); kseg [E+1] device int32, multiples of 64.
+// mn = 0: A [M, kwidth] and B [N, kwidth] K-major (zero pad columns); mn = 1: A [kwidth, M] and
+// B [kwidth, N] MN-major with row strides lda and ldb (zero pad rows). out [E M, N]; all bf16.
 cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, int E, int M, int N,
-                           int64_t kwidth, void *out, uint32_t *dev_status, cudaStream_t s) {
+                           int64_t kwidth, void *out, uint32_t *dev_status, cudaStream_t s,
+                           int mn, int64_t lda, int64_t ldb) {
     if (E <= 0 || M <= 0 || N <= 0 || kwidth <= 0 || kwidth % BK != 0 || kwidth >= (1ll << 31))
         return cudaErrorInvalidValue;
     CUtensorMap mA, mB, mO;
-    if (!make_map(&mA, A, M, kwidth, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mB, B, N, kwidth, BN / 2)) return cudaErrorInvalidValue;
+    if (mn) {
+        if (M % 64 != 0 || N % 64 != 0 || lda < M || ldb < N) return cudaErrorInvalidValue;
+        if (!make_map_ld(&mA, A, kwidth, M, lda, 64)) return cudaErrorInvalidValue;
+        if (!make_map_ld(&mB, B, kwidth, N, ldb, 64)) return cudaErrorInvalidValue;
+    } else {
+        if (!make_map(&mA, A, M, kwidth, BM)) return cudaErrorInvalidValue;
+        if (!make_map(&mB, B, N, kwidth, BN / 2)) return cudaErrorInvalidValue;
+    }
     if (!make_store_map(&mO, out, (int64_t)E * M, N)) return cudaErrorInvalidValue;
     TcArgs a = {};
     a.offsets = kseg;
@@ -1002,12 +1024,21 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     a.M = M;
     a.m_tiles = (M + BM - 1) / BM;
     a.pre1 = a.pre3 = nullptr;
-    a.b_mn = a.b_ksplit = a.b_krows = 0;
+    a.b_mn = a.a_mn = mn;
+    a.b_ksplit = a.b_krows = 0;
     const int64_t units = (int64_t)E * a.m_tiles * a.n_tiles;
     if (units >= (1ll << 31)) return cudaErrorInvalidValue;
     int64_t grid = num_sms();
     if (grid > units) grid = units;
-    cudaError_t err = set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, false>, TC_SMEM);
+    if (mn) {
+        cudaError_t err =
+            set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, true>, TC_SMEM);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(grouped_gemm_tc_kernel<true, true>, dim3((unsigned)grid),
+                          dim3(TC_THREADS), TC_SMEM, s, 1, mA, mB, mB, mO, a);
+    }
+    cudaError_t err =
+        set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, false>, TC_SMEM);
     if (err != cudaSuccess) return err;
     return launch_pdl(grouped_gemm_tc_kernel<true, false>, dim3((unsigned)grid), dim3(TC_THREADS),
                       TC_SMEM, s, 1, mA, mB, mB, mO, a);
@@ -1039,7 +1070,13 @@ cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, i
 cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,
                                int N, int64_t kwidth, void *out, uint32_t *dev_status,
                                cudaStream_t s) {
-    return launch_gemm_kg(A, B, kseg, E, M, N, kwidth, out, dev_status, s);
+    return launch_gemm_kg(A, B, kseg, E, M, N, kwidth, out, dev_status, s, 0, 0, 0);
+}
+
+cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,
+                                  const int32_t *kseg, int E, int M, int N, int64_t rows,
+                                  void *out, uint32_t *dev_status, cudaStream_t s) {
+    return launch_gemm_kg(A, B, kseg, E, M, N, rows, out, dev_status, s, 1, lda, ldb);
 }
 
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,

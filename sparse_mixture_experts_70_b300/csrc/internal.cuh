@@ -235,5 +235,11 @@ cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, i
 cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,
                                int N, int64_t kwidth, void *out, uint32_t *dev_status,
                                cudaStream_t s);
+// The same over MN-major operands in the padded row layout: A [rows, M] with row stride lda and
+// B [rows, N] with row stride ldb (bf16; the K index is the row, expert e's rows
+// [kseg[e], kseg[e+1]) with zero pad rows).
+cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,
+                                  const int32_t *kseg, int E, int M, int N, int64_t rows,
+                                  void *out, uint32_t *dev_status, cudaStream_t s);
 
 }  // namespace moe

@@ -359,16 +359,22 @@ inline EncodeTiledFn encode_fn() {
 
 // 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of box_rows x 64 with the
 // 128-byte swizzle; out-of-range rows read as zeros.
-inline bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
+inline bool make_map_ld(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld,
+                        int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};  // 64 bf16 = one 128-byte swizzle row
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A [rows, cols] bf16 row-major tensor (row stride = cols) in boxes of 64 columns x box_rows.
+inline bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
+    return make_map_ld(m, ptr, rows, cols, cols, box_rows);
 }
 
 // 2-D bf16 tensor [rows, cols] written by TMA stores of 32 x 32 boxes staged in shared memory as
