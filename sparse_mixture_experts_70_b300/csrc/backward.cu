@@ -67,11 +67,12 @@ __device__ __forceinline__ int segment_of(const int32_t *kseg, int E, int c) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// prep: gate of every sorted row (gate_r[slot_of[s]] = gates[s] for kept slots) and the padded
-// segment offsets kseg (block 0).
+// prep: gate of every sorted row (gate_r[slot_of[s]] = gates[s] for kept slots), and in block 0
+// the padded segment offsets kseg and the router GEMMs' one-group segments seg.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, const float *gates,
                                                        const int32_t *offsets, int64_t P, int E,
-                                                       float *gate_r, int32_t *kseg,
+                                                       int64_t T, int nsplit, float *gate_r,
+                                                       int32_t *kseg, int32_t *seg,
                                                        uint32_t *dev_status) {
     pdl_wait();
     const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -82,6 +83,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, c
         else if (r >= 0) gate_r[r] = gates[s];
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
+        // segments of the router GEMMs: rows [0, T) as one group for dz W_r^T, and the K range
+        // [0, roundup64(T)) of h^T dz cut into nsplit groups of whole 64-row blocks
+        seg[0] = 0;
+        seg[1] = (int32_t)T;
+        const int64_t blocks = (T + BT - 1) / BT;
+        for (int g = 0; g <= nsplit; ++g) seg[2 + g] = (int32_t)(blocks * g / nsplit * BT);
         int acc = 0;
         kseg[0] = 0;
         for (int e = 0; e < E; ++e) {
@@ -289,7 +296,10 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
 // ---------------------------------------------------------------------------------------------
 // Router backward, one warp per token: the logits z (from the tensor-core partial logits
 // part[S][T][ldp], or a direct dot product over d), p, lse, the gate gradients dg_j of the k slots
-// (the tiles' parts summed, plus dy . b2_e when b2 is given), then dz = dL/dz into dz [T, E].
+// (the tiles' parts summed, plus dy . b2_e when b2 is given), then dz = dL/dz. dz leaves as bf16
+// pieces for the two router GEMMs: Zp[t] = [hi(dz) | lo(dz) | hi(dz) | 0 ...] (Kp columns), with
+// hi = bf16(dz) and lo = bf16(dz - hi), so that dz W_r^T ~ hi Whi + lo Whi + hi Wlo and
+// h^T dz ~ h^T hi + h^T lo hold to about 2^-16; the per-block sums of dz (db_r) go to dbr_part.
 constexpr int RB_MAXEW = 8;  // experts per lane: E <= 256
 struct RouterBwd {
     const __nv_bfloat16 *h, *dy;
@@ -302,7 +312,9 @@ struct RouterBwd {
     int64_t T, P;
     int d, E, k, raw_prob;
     float aux_weight, zloss_weight;
-    float *dz;
+    __nv_bfloat16 *Zp;  // [T, Kp]
+    int Kp;
+    float *dbr_part;    // [gridDim.x, E]
 };
 
 __device__ __forceinline__ float warp_sum_f(float v) {
@@ -316,16 +328,11 @@ __device__ __forceinline__ float warp_max_f(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint32_t *dev_status) {
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= a.T) {
-        pdl_trigger();
-        return;
-    }
+// dz of token t into this lane's experts lane + 32 i.
+__device__ __forceinline__ void router_token_grad(const RouterBwd &a, int64_t t, int lane,
+                                                  float (&dz)[RB_MAXEW], uint32_t *dev_status) {
     const int E = a.E;
-    float z[RB_MAXEW], p[RB_MAXEW], dz[RB_MAXEW];
+    float z[RB_MAXEW], p[RB_MAXEW];
 #pragma unroll
     for (int i = 0; i < RB_MAXEW; ++i) z[i] = 0.f;
     if (a.part) {
@@ -458,69 +465,98 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint
 #pragma unroll
         for (int i = 0; i < RB_MAXEW; ++i) dz[i] += zs * p[i];
     }
+}
+
+// Warps stride over the tokens; each block sums dz over its tokens (per warp in token order,
+// then over the warps in order) into dbr_part[blockIdx.x].
+__global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint32_t *dev_status) {
+    __shared__ float wsum[8][256];
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int E = a.E;
+    float acc[RB_MAXEW];
+#pragma unroll
+    for (int i = 0; i < RB_MAXEW; ++i) acc[i] = 0.f;
+    for (int64_t t = (int64_t)blockIdx.x * 8 + warp; t < a.T; t += (int64_t)gridDim.x * 8) {
+        float dz[RB_MAXEW];
+        router_token_grad(a, t, lane, dz, dev_status);
+        __nv_bfloat16 *zp = a.Zp + t * a.Kp;
+#pragma unroll
+        for (int i = 0; i < RB_MAXEW; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(dz[i]);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(dz[i] - __bfloat162float(hi));
+                zp[e] = hi;
+                zp[E + e] = lo;
+                zp[2 * E + e] = hi;
+                acc[i] += dz[i];
+            }
+        }
+        for (int c = 3 * E + lane; c < a.Kp; c += 32) zp[c] = __float2bfloat16_rn(0.f);
+    }
 #pragma unroll
     for (int i = 0; i < RB_MAXEW; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) a.dz[t * E + e] = dz[i];
+        if (e < E) wsum[warp][e] = acc[i];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float v = 0.f;
+        for (int w = 0; w < 8; ++w) v += wsum[w][e];
+        a.dbr_part[(int64_t)blockIdx.x * E + e] = v;
+    }
+    pdl_trigger();
+}
+
+// Wp[i] = [hi(W_r[i, :]) | hi(W_r[i, :]) | lo(W_r[i, :]) | 0 ...] (Kp columns): the router weight
+// as bf16 pieces matching Zp, for dz W_r^T on the tensor cores.
+__global__ void __launch_bounds__(256) wr_pieces_kernel(const float *W_r, int d, int E, int Kp,
+                                                        __nv_bfloat16 *Wp) {
+    pdl_wait();
+    const int64_t n = (int64_t)d * Kp;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = x / Kp;
+        const int c = (int)(x - i * Kp);
+        float v = 0.f;
+        if (c < 3 * E) {
+            const int e = c % E;
+            const float w = W_r[i * E + e];
+            const float hi = __bfloat162float(__float2bfloat16_rn(w));
+            v = c < 2 * E ? hi : w - hi;
+        }
+        Wp[x] = __float2bfloat16_rn(v);
     }
     pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------------------
-// dh[t, i] = sum_j dX[c(t, j), i] + sum_e dz[t, e] W_r[i, e], where c(t, j) is the padded row of
-// slot (t, j): kseg[e] + slot_of[t k + j] - offsets[e] with e = idx[t k + j] (dropped slots
-// contribute nothing). 64 tokens x 64 features per block; thread (ig = tid % 16, tg = tid / 16) owns tokens 4 tg .. 4 tg + 3 and features
-// 4 ig .. 4 ig + 3 (16 accumulators, two 16-byte shared loads per 16 FMAs). Experts go through
-// shared memory 64 at a time: W_r's 64 rows as sw[e][i] and dz as sz[e][t].
-constexpr int DH_T = 64, DH_ECH = 64, DH_LD = 68;
-__global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const int32_t *slot_of,
-                                                 const int32_t *idx, const int32_t *offsets_g,
-                                                 const int32_t *kseg_g, const float *dz,
-                                                 const float *W_r, int64_t T, int d, int E, int k,
+// dh[t, i] = dhr[t, i] + sum_j dX[c(t, j), i]: the router's term dz W_r^T (f32, from the tensor
+// cores) plus the k slots' input gradients, where c(t, j) = kseg[e] + slot_of[t k + j] -
+// offsets[e] with e = idx[t k + j] is the slot's padded row (dropped slots contribute nothing).
+// One thread per 8 features of a token.
+__global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const float *dhr,
+                                                 const int32_t *slot_of, const int32_t *idx,
+                                                 const int32_t *offsets_g, const int32_t *kseg_g,
+                                                 int64_t T, int d, int E, int k,
                                                  __nv_bfloat16 *dh, uint32_t *dev_status) {
-    __shared__ __align__(16) float sw[DH_ECH][BT];
-    __shared__ __align__(16) float sz[DH_ECH][DH_LD];
     __shared__ int32_t kseg[257], offs[257];
     pdl_wait();
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
         kseg[e] = kseg_g[e];
         offs[e] = offsets_g[e];
     }
-    const int i0 = blockIdx.x * BT;
-    const int64_t t0 = (int64_t)blockIdx.y * DH_T;
-    const int ig = threadIdx.x & 15, tg = threadIdx.x >> 4;
-    float acc[4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-    for (int e0 = 0; e0 < E; e0 += DH_ECH) {
-        const int ne = E - e0 < DH_ECH ? E - e0 : DH_ECH;
-        __syncthreads();
-        for (int x = threadIdx.x; x < DH_ECH * BT; x += blockDim.x) {
-            const int ii = x / DH_ECH, e = x - ii * DH_ECH;  // along a row of W_r
-            sw[e][ii] = e < ne ? W_r[(int64_t)(i0 + ii) * E + e0 + e] : 0.f;
-        }
-        for (int x = threadIdx.x; x < DH_ECH * DH_T; x += blockDim.x) {
-            const int tt = x / DH_ECH, e = x - tt * DH_ECH;  // along a row of dz
-            sz[e][tt] = (e < ne && t0 + tt < T) ? dz[(t0 + tt) * E + e0 + e] : 0.f;
-        }
-        __syncthreads();
-        for (int e = 0; e < ne; ++e) {
-            const float4 w4 = *reinterpret_cast<const float4 *>(&sw[e][ig * 4]);
-            const float4 z4 = *reinterpret_cast<const float4 *>(&sz[e][tg * 4]);
-            const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-            const float zv[4] = {z4.x, z4.y, z4.z, z4.w};
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(zv[a], wv[b], acc[a][b]);
-        }
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int64_t t = t0 + tg * 4 + a;
-        if (t >= T) break;
+    __syncthreads();
+    const int vecs = d / 8;
+    const int64_t n = T * vecs;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = x / vecs;
+        const int i0 = (int)(x - t * vecs) * 8;
+        const float4 r0 = *reinterpret_cast<const float4 *>(dhr + t * d + i0);
+        const float4 r1 = *reinterpret_cast<const float4 *>(dhr + t * d + i0 + 4);
+        float acc[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         for (int j = 0; j < k; ++j) {
             const int r = slot_of[t * k + j];
             if (r < 0) continue;  // dropped by the capacity
@@ -530,119 +566,48 @@ __global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const 
                 report(dev_status, DEV_ERR_INDEX);
                 continue;
             }
-            const uint2 u =
-                __ldg(reinterpret_cast<const uint2 *>(dX + (int64_t)c * d + i0 + ig * 4));
-            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-            acc[a][0] += __low2float(p0);
-            acc[a][1] += __high2float(p0);
-            acc[a][2] += __low2float(p1);
-            acc[a][3] += __high2float(p1);
-        }
-        *reinterpret_cast<uint2 *>(dh + t * d + i0 + ig * 4) =
-            make_uint2(pack2(acc[a][0], acc[a][1]), pack2(acc[a][2], acc[a][3]));
-    }
-    pdl_trigger();
-}
-
-// ---------------------------------------------------------------------------------------------
-// dW_r partial sums: block (x, y, z) adds h[t, i] dz[t, e] over the tokens [y ts, (y + 1) ts)
-// for features [64 x, 64 x + 64) and experts [z 16 EPT, (z + 1) 16 EPT) into part[y][i][e];
-// thread (ig = tid % 16, eg = tid / 16) owns 4 features x EPT experts. The blocks of x = 0 also
-// sum dz over their tokens into partb[y][e] (db_r).
-template <int EPT>
-__global__ void __launch_bounds__(256) dwr_part_kernel(const __nv_bfloat16 *h, const float *dz,
-                                                       int64_t T, int d, int E, int64_t ts,
-                                                       float *part, float *partb) {
-    constexpr int ETILE = 16 * EPT;
-    __shared__ __align__(16) float sh[32][BT];
-    __shared__ __align__(16) float sz[32][ETILE];
-    pdl_wait();
-    const int i0 = blockIdx.x * BT;
-    const int e0 = blockIdx.z * ETILE;
-    const int ig = threadIdx.x & 15, eg = threadIdx.x >> 4;
-    const int64_t ta = (int64_t)blockIdx.y * ts;
-    const int64_t tb = ta + ts < T ? ta + ts : T;
-    const bool bias = blockIdx.x == 0 && partb != nullptr && (int)threadIdx.x < ETILE;
-    float acc[4][EPT];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < EPT; ++b) acc[a][b] = 0.f;
-    float accb = 0.f;
-    for (int64_t t0 = ta; t0 < tb; t0 += 32) {
-        __syncthreads();
-        {
-            const int tl = threadIdx.x >> 3, ch = threadIdx.x & 7;
             float v[8];
-            if (t0 + tl < tb) {
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(h + (t0 + tl) * d + i0) + ch), v);
-            } else {
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(dX + (int64_t)c * d + i0)), v);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = 0.f;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sh[tl][ch * 8 + q] = v[q];
+            for (int q = 0; q < 8; ++q) acc[q] += v[q];
         }
-        for (int x = threadIdx.x; x < 32 * ETILE; x += blockDim.x) {
-            const int tl = x / ETILE, e = x - tl * ETILE;
-            sz[tl][e] = (t0 + tl < tb && e0 + e < E) ? dz[(t0 + tl) * E + e0 + e] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int tl = 0; tl < 32; ++tl) {
-            const float4 h4 = *reinterpret_cast<const float4 *>(&sh[tl][ig * 4]);
-            const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
-            float zv[EPT];
-            if constexpr (EPT % 4 == 0) {
-#pragma unroll
-                for (int b = 0; b < EPT; b += 4) {
-                    const float4 z4 = *reinterpret_cast<const float4 *>(&sz[tl][eg * EPT + b]);
-                    zv[b] = z4.x;
-                    zv[b + 1] = z4.y;
-                    zv[b + 2] = z4.z;
-                    zv[b + 3] = z4.w;
-                }
-            } else {
-#pragma unroll
-                for (int b = 0; b < EPT; ++b) zv[b] = sz[tl][eg * EPT + b];
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < EPT; ++b) acc[a][b] = fmaf(hv[a], zv[b], acc[a][b]);
-        }
-        if (bias)
-            for (int tl = 0; tl < 32; ++tl) accb += sz[tl][threadIdx.x];
+        *reinterpret_cast<uint4 *>(dh + t * d + i0) =
+            make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
+                       pack2(acc[6], acc[7]));
     }
-    float *out = part + (int64_t)blockIdx.y * d * E;
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < EPT; ++b) {
-            const int e = e0 + eg * EPT + b;
-            if (e < E) out[(int64_t)(i0 + ig * 4 + a) * E + e] = acc[a][b];
-        }
-    if (bias && e0 + (int)threadIdx.x < E)
-        partb[(int64_t)blockIdx.y * E + e0 + threadIdx.x] = accb;
     pdl_trigger();
 }
 
-// out[x] = sum_{s < nsplit} part[s][x] for x < n (in split order); outb likewise over E.
-__global__ void __launch_bounds__(256) split_sum_kernel(const float *part, int nsplit, int64_t n,
-                                                        float *out, const float *partb, int E,
-                                                        float *outb) {
+// dW_r[i, e] = sum over the K groups g of o[g][i, e] + o[g][i, E + e], from the GEMM
+// h^T [hi | lo] split into nsplit groups of rows (o [nsplit, d, ldo] f32, summed in group order);
+// db_r[e] = the sum of the router blocks' dz sums (when db_r is given): warp e of the blocks past
+// the dW_r threads strides over the blocks' sums and adds its lanes in a fixed order.
+__global__ void __launch_bounds__(256) router_final_kernel(const float *o, int ldo, int d, int E,
+                                                           int nsplit, const float *dbr_part,
+                                                           int nblk, float *dW_r, float *db_r) {
     pdl_wait();
+    const int64_t n = (int64_t)d * E;
     const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (x < n) {
+        const int64_t i = x / E;
+        const int e = (int)(x - i * E);
         float v = 0.f;
-        for (int s = 0; s < nsplit; ++s) v += part[(int64_t)s * n + x];
-        out[x] = v;
+        for (int g = 0; g < nsplit; ++g) {
+            const float *og = o + ((int64_t)g * d + i) * ldo;
+            v += og[e] + og[E + e];
+        }
+        dW_r[x] = v;
     }
-    if (outb && x < E) {
-        float v = 0.f;
-        for (int s = 0; s < nsplit; ++s) v += partb[(int64_t)s * E + x];
-        outb[x] = v;
+    const int64_t nb = (n + blockDim.x - 1) / blockDim.x;  // blocks of the dW_r part
+    if (db_r && blockIdx.x >= nb) {
+        const int64_t e = (int64_t)(blockIdx.x - nb) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        const int lane = threadIdx.x & 31;
+        if (e < E) {
+            float v = 0.f;
+            for (int b = lane; b < nblk; b += 32) v += dbr_part[(int64_t)b * E + e];
+            v = warp_sum_f(v);
+            if (lane == 0) db_r[e] = v;
+        }
     }
     pdl_trigger();
 }
@@ -667,16 +632,23 @@ __global__ void __launch_bounds__(256) seg_sum_kernel(const float *part, int wid
 
 size_t al(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
-// dW_r kernel shape: experts per thread and expert tiles of 16 EPT
-int dwr_ept(int E) { return E <= 16 ? 1 : E <= 32 ? 2 : E <= 64 ? 4 : 8; }
-int dwr_etiles(int E) { return (E + 16 * dwr_ept(E) - 1) / (16 * dwr_ept(E)); }
+
+
+// Blocks of the router backward (their dz sums make db_r).
+constexpr int RB_BLOCKS_MAX = 512;
+int router_bwd_blocks(int64_t T) {
+    const int64_t b = (T + 7) / 8;
+    return (int)(b < RB_BLOCKS_MAX ? (b > 0 ? b : 1) : RB_BLOCKS_MAX);
+}
 
 struct BwdLayout {
-    size_t gate_r, kseg, A1, A3, Xp, dYp, dHu, dA, Hs, dX, dg_part,
-        db1_part, db2_part, dz, dwr_part, dwr_partb, total;
+    size_t gate_r, kseg, seg, A1, A3, Xp, dYp, dHu, dA, Hs, dX, dg_part, db1_part, db2_part, Zp,
+        Wp, dhr, dwr_out, dbr_part, total;
     int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
-    int K2, n_part, nsplit;
-    int64_t ts;  // tokens per dW_r split
+    int K2, n_part;
+    int Kp;      // columns of the bf16 pieces of dz and W_r: roundup64(3 E)
+    int Nr;      // columns of h^T [hi | lo]: roundup64(2 E)
+    int nsplit;  // K groups of h^T [hi | lo]
 };
 
 BwdLayout bwd_layout(const moe_config_t &c) {
@@ -686,20 +658,25 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     L.kw = (P + BT - 1) / BT * BT + (int64_t)BT * c.E;
     L.K2 = sw ? 2 * c.f : c.f;
     L.n_part = c.f / BT;
-    const int tiles_x = c.d / BT * dwr_etiles(c.E);
-    int64_t ns = (2 * 148 + tiles_x - 1) / tiles_x;
-    const int64_t tmax = (c.T + 31) / 32;
-    if (ns > tmax) ns = tmax;
-    if (ns < 1) ns = 1;
-    L.ts = ((c.T + ns - 1) / ns + 31) / 32 * 32;
-    if (L.ts < 32) L.ts = 32;
-    L.nsplit = (int)((c.T + L.ts - 1) / L.ts);
-    if (L.nsplit < 1) L.nsplit = 1;
+    L.Kp = (3 * c.E + BT - 1) / BT * BT;
+    L.Nr = (2 * c.E + BT - 1) / BT * BT;
+    {
+        // enough K groups that the d/128 x Nr/256 output tiles of h^T [hi | lo] fill the SMs,
+        // each group at least 512 rows
+        const int64_t tiles = (int64_t)((c.d + 127) / 128) * ((L.Nr + 255) / 256);
+        int64_t g = (148 + tiles - 1) / tiles;
+        const int64_t gmax = (c.T + 511) / 512;
+        if (g > gmax) g = gmax;
+        if (g < 1) g = 1;
+        if (g > 64) g = 64;
+        L.nsplit = (int)g;
+    }
     const size_t E = (size_t)c.E, d = (size_t)c.d, f = (size_t)c.f, kw = (size_t)L.kw;
     const size_t nt = kw / BT;
     size_t off = 0;
     L.gate_r = off;     off = al(off + (size_t)P * 4);
     L.kseg = off;       off = al(off + (E + 1) * 4);
+    L.seg = off;        off = al(off + (size_t)(3 + L.nsplit) * 4);
     L.A1 = off;         off = al(off + (size_t)P * f * 2);
     L.A3 = off;         off = al(off + (sw ? (size_t)P * f * 2 : 0));
     // padded row layout [kw, .]: expert e's slots at rows [kseg[e], kseg[e+1]), pad rows zero
@@ -712,19 +689,13 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     L.dg_part = off;    off = al(off + (size_t)L.n_part * (size_t)P * 4);
     L.db1_part = off;   off = al(off + (c.has_bias ? nt * f * 4 : 0));
     L.db2_part = off;   off = al(off + (c.has_bias ? nt * d * 4 : 0));
-    L.dz = off;         off = al(off + (size_t)c.T * E * 4);
-    L.dwr_part = off;   off = al(off + (size_t)L.nsplit * d * E * 4);
-    L.dwr_partb = off;  off = al(off + (size_t)L.nsplit * E * 4);
+    L.Zp = off;         off = al(off + (size_t)c.T * L.Kp * 2);
+    L.Wp = off;         off = al(off + d * L.Kp * 2);
+    L.dhr = off;        off = al(off + (size_t)c.T * d * 4);
+    L.dwr_out = off;    off = al(off + (size_t)L.nsplit * d * L.Nr * 4);
+    L.dbr_part = off;   off = al(off + (size_t)router_bwd_blocks(c.T) * E * 4);
     L.total = off;
     return L;
-}
-
-template <int EPT>
-cudaError_t launch_dwr(const moe_config_t &c, const BwdLayout &L, const void *h, const float *dz,
-                       float *part, float *partb, cudaStream_t s) {
-    return launch_pdl(dwr_part_kernel<EPT>, dim3(c.d / BT, L.nsplit, dwr_etiles(c.E)), dim3(256),
-                      0, s, 1, static_cast<const __nv_bfloat16 *>(h), dz, c.T, c.d, c.E, L.ts,
-                      part, partb);
 }
 
 bool al16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
@@ -743,9 +714,10 @@ int backward_launches(const moe_config_t &c, bool saved) {
     if (c.T == 0) return 0;
     const bool sw = c.act == MOE_ACT_SWIGLU;
     const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
-    return 1 /*prep*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
+    return 2 /*prep, W_r pieces*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
            2 /*padded gathers, dHu*/ + 1 /*act*/ + 1 /*dX*/ + (sw ? 3 : 2) /*dW*/ +
-           router + 1 /*router bwd*/ + 1 /*dh*/ + 2 /*dW_r*/ + (c.has_bias ? 2 : 0);
+           router + 1 /*router bwd*/ + 2 /*dz W_r^T, dh*/ + 2 /*h^T dz, dW_r and db_r*/ +
+           (c.has_bias ? 2 : 0);
 }
 
 }  // namespace moe
@@ -836,8 +808,18 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         if ((x) != cudaSuccess) return MOE_ERR_CUDA;   \
     } while (0)
     // 1. sorted-row gates and the padded segment offsets
+    int32_t *seg = reinterpret_cast<int32_t *>(b + B.seg);
     MOE_TRY(launch_pdl(bwd_prep_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0, s, 1,
-                       slot_of, gates, offsets, P, c.E, gate_r, kseg, dev_status));
+                       slot_of, gates, offsets, P, c.E, c.T, B.nsplit, gate_r, kseg, seg,
+                       dev_status));
+    // 2. the router weight as bf16 pieces (for dz W_r^T on the tensor cores)
+    {
+        const int64_t n = d * B.Kp;
+        int64_t blocks = (n + 255) / 256;
+        if (blocks > 4 * (int64_t)num_sms()) blocks = 4 * (int64_t)num_sms();
+        MOE_TRY(launch_pdl(wr_pieces_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, W_r, c.d,
+                           c.E, B.Kp, bf(B.Wp)));
+    }
     // 3. pre-activations A1 = X W1^T (+ b1), A3 = X W3^T: left in bws by moe_forward_train, or
     // recomputed here
     if (!saved_preact) {
@@ -922,28 +904,35 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     rb.raw_prob = c.gate == MOE_GATE_RAW_PROB ? 1 : 0;
     rb.aux_weight = aux_weight;
     rb.zloss_weight = zloss_weight;
-    rb.dz = fl(B.dz);
-    MOE_TRY(launch_pdl(router_bwd_kernel, dim3((unsigned)((c.T + 7) / 8)), dim3(256), 0, s, 1, rb,
+    rb.Zp = bf(B.Zp);
+    rb.Kp = B.Kp;
+    rb.dbr_part = fl(B.dbr_part);
+    const int rblocks = router_bwd_blocks(c.T);
+    MOE_TRY(launch_pdl(router_bwd_kernel, dim3((unsigned)rblocks), dim3(256), 0, s, 1, rb,
                        dev_status));
-    // 10. dh = sum_j dX[padded row of slot j] + dz W_r^T
-    MOE_TRY(launch_pdl(dh_kernel, dim3(c.d / BT, (unsigned)((c.T + DH_T - 1) / DH_T)), dim3(256),
-                       0, s, 1, static_cast<const __nv_bfloat16 *>(bf(B.dX)), slot_of, idx,
-                       offsets, ksegc, static_cast<const float *>(fl(B.dz)), W_r, c.T, c.d, c.E,
-                       c.k, static_cast<__nv_bfloat16 *>(dh), dev_status));
-    // 11. dW_r = h^T dz, db_r = sum dz (split over tokens, then summed in split order)
+    // 10. the router's h-gradient dz W_r^T = Zp Wp^T (f32, one group of T rows), then
+    // dh = that + sum_j dX[padded row of slot j]
+    MOE_TRY(launch_gemm_rows_f32(bf(B.Zp), bf(B.Wp), c.T, 1, B.Kp, c.d, seg, fl(B.dhr),
+                                 dev_status, s));
     {
-        float *part = fl(B.dwr_part), *partb = b_r ? fl(B.dwr_partb) : nullptr;
-        const float *dz = fl(B.dz);
-        switch (dwr_ept(c.E)) {
-            case 1: MOE_TRY(launch_dwr<1>(c, B, h, dz, part, partb, s)); break;
-            case 2: MOE_TRY(launch_dwr<2>(c, B, h, dz, part, partb, s)); break;
-            case 4: MOE_TRY(launch_dwr<4>(c, B, h, dz, part, partb, s)); break;
-            default: MOE_TRY(launch_dwr<8>(c, B, h, dz, part, partb, s)); break;
-        }
-        const int64_t n = d * E;
-        MOE_TRY(launch_pdl(split_sum_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
-                           static_cast<const float *>(part), B.nsplit, n, dW_r,
-                           static_cast<const float *>(partb), c.E, db_r));
+        const int64_t n = c.T * (d / 8);
+        int64_t blocks = (n + 255) / 256;
+        if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
+        MOE_TRY(launch_pdl(dh_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+                           static_cast<const __nv_bfloat16 *>(bf(B.dX)),
+                           static_cast<const float *>(fl(B.dhr)), slot_of, idx, offsets, ksegc,
+                           c.T, c.d, c.E, c.k, static_cast<__nv_bfloat16 *>(dh), dev_status));
+    }
+    // 11. dW_r = h^T dz as h^T [hi | lo] on the tensor cores (MN-major operands, one group of
+    // K = T rows, rows past T read as zeros), then the two halves added and db_r reduced
+    MOE_TRY(launch_gemm_kgroup_mn(h, c.d, bf(B.Zp), B.Kp, seg + 2, B.nsplit, c.d, B.Nr,
+                                  (c.T + BT - 1) / BT * BT, nullptr, dev_status, s, c.T,
+                                  fl(B.dwr_out)));
+    {
+        const int64_t nb = (d * E + 255) / 256, eb = b_r ? (E + 7) / 8 : 0;
+        MOE_TRY(launch_pdl(router_final_kernel, dim3((unsigned)(nb + eb)), dim3(256), 0, s, 1,
+                           static_cast<const float *>(fl(B.dwr_out)), B.Nr, c.d, c.E, B.nsplit,
+                           static_cast<const float *>(fl(B.dbr_part)), rblocks, dW_r, db_r));
     }
     // 12. bias gradients
     if (c.has_bias) {

@@ -98,6 +98,8 @@ struct TcArgs {
     // MN-major A (K-grouped mode with MN): A is [K rows, M] (rows = the K index), read as two
     // 64 x 64 boxes at columns m 128 and m 128 + 64, rows kseg[e] + 64 kb
     int a_mn;
+    // f32 output (plain store, no bias or activation): out_f32 [rows, N] instead of out
+    float *out_f32;
 };
 
 // The 4 source rows this lane gathers for tile ti (rows 4 lane .. 4 lane + 3 of the tile);
@@ -122,6 +124,20 @@ struct Tile {
 };
 // Unit t of the K-grouped schedule: expert-major, then N tile, then M tile; row0 is the output
 // row (e M + m 128), rows the valid rows of the tile.
+// Unit t of the K-grouped schedule of a CTA pair: expert-major, then N tile, then pairs of M tiles,
+// of which CTA `rank` takes the first or the second (rows <= 0: past M, an idle half).
+__device__ __forceinline__ Tile decode_tile_kg_pair(int t, const TcArgs &a, int rank) {
+    const int mp_n = (a.m_tiles + 1) / 2;
+    const int per = mp_n * a.n_tiles;
+    Tile ti;
+    ti.e = t / per;
+    const int local = t - ti.e * per;
+    ti.n = local / mp_n;
+    const int m = 2 * (local - ti.n * mp_n) + rank;
+    ti.row0 = ti.e * a.M + m * BM;
+    ti.rows = min(BM, a.M - m * BM);
+    return ti;
+}
 __device__ __forceinline__ Tile decode_tile_kg(int t, const TcArgs &a) {
     const int per = a.m_tiles * a.n_tiles;
     Tile ti;
@@ -268,6 +284,16 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
             if (a.out_token) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= gscale;
+            }
+            if (a.out_f32) {
+                if (valid) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.out_f32 +
+                                                             (int64_t)(ti.row0 + r) * a.N + col);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+                continue;
             }
             if (boxed) {
                 uint32_t pk[16];
@@ -606,7 +632,8 @@ constexpr int B_HALF = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the B
 constexpr size_t TC_SMEM_PAIR =
     1024 + (size_t)STAGES2 * (A_HALF + B_HALF) + CTL_BYTES + (size_t)EPI_WARPS * EPI_BOX;
 
-template <bool MN>
+// KG: the K-grouped schedule (MN-major A and B only); MN: MN-major B allowed.
+template <bool KG, bool MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
@@ -654,7 +681,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);  // collective: the same columns in both
         tmem_relinquish_pair();
     }
-    if (warp == 2 && lane == 0) {
+    if (warp == 2 && lane == 0 && KG) {
+        // K segments: multiples of BK, ascending, within the operands' rows
+        bool bad = a.offsets[0] != 0;
+        for (int e = 0; e <= E; ++e) {
+            const int v = a.offsets[e];
+            if (v < 0 || v % BK != 0 || (int64_t)v > (int64_t)a.K || (e > 0 && v < s_off[e - 1]))
+                bad = true;
+            s_off[e] = v;
+        }
+        s_cum[E] = bad ? 0 : E * ((a.m_tiles + 1) / 2) * a.n_tiles;
+        if (bad) report(a.dev_status, DEV_ERR_INDEX);
+    } else if (warp == 2 && lane == 0) {
         int cum = 0;
         bool bad = false;
         for (int e = 0; e < E; ++e) {
@@ -689,24 +727,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t phase = 0;
             bool ok = !a.withhold_loads;
             for (int t = unit0; t < total && ok; t += ustep) {
-                const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
+                const Tile ti = KG ? decode_tile_kg_pair(t, a, rank)
+                                   : decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
                 // this CTA's half of the B tile: SwiGLU W1 (CTA 0) / W3 (CTA 1) rows, else rows
                 // 128 r.. of the 256-row W tile
                 const CUtensorMap *bm = (a.epi == EPI_SWIGLU && rank == 1) ? &tmB3 : &tmB;
                 const int brow = a.epi == EPI_SWIGLU ? ti.e * a.N + ti.n * (BN / 2)
                                                      : ti.e * a.N + ti.n * BN + rank * (BN / 2);
-                for (int kb = 0; kb < nk; ++kb) {
+                const int nkt = KG ? (s_off[ti.e + 1] - s_off[ti.e]) / BK : nk;
+                for (int kb = 0; kb < nkt; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);  // leader's barrier
                     if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_HALF + B_HALF));
-                    tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
+                    if (KG) {
+                        // this CTA's 128 columns of the MN-major A: two 64 x 64 boxes
+                        const int kx = s_off[ti.e] + kb * BK;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d_pair(sA + stage * A_HALF + q * (A_HALF / 2), &tmA, fb,
+                                             ti.row0 - ti.e * a.M + q * 64, kx);
+                    } else {
+                        tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
+                    }
                     if (MN && a.b_mn) {
                         // this CTA's 128 columns of B: two 64 x 64 boxes
                         const bool second = a.b_ksplit > 0 && kb >= a.b_ksplit;
-                        const int krow = ti.e * a.b_krows + (second ? kb - a.b_ksplit : kb) * BK;
+                        const int krow = KG ? s_off[ti.e] + kb * BK
+                                            : ti.e * a.b_krows + (second ? kb - a.b_ksplit : kb) * BK;
 #pragma unroll
                         for (int q = 0; q < 2; ++q)
                             tma_load_2d_pair(sB + stage * B_HALF + q * (B_HALF / 2),
@@ -793,25 +843,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            const bool bmn = MN && a.b_mn;
-            const uint32_t idesc = idesc_bf16(2 * BM, BN) | (bmn ? IDESC_B_MN : 0u);
+            const bool bmn = MN && a.b_mn, amn = KG;
+            const uint32_t idesc =
+                idesc_bf16(2 * BM, BN) | (bmn ? IDESC_B_MN : 0u) | (amn ? IDESC_A_MN : 0u);
             for (int t = unit0; t < total && ok; t += ustep) {
                 if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1u, s_abort, a.dev_status, lim)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < nk; ++kb) {
+                int nkt = nk;
+                if (KG) {
+                    const Tile ti = decode_tile_kg_pair(t, a, 0);
+                    nkt = (s_off[ti.e + 1] - s_off[ti.e]) / BK;
+                }
+                for (int kb = 0; kb < nkt; ++kb) {
                     if (!mbar_wait(bar_full + 8 * stage, phase, s_abort, a.dev_status, lim)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_k_sw128(sA + stage * A_HALF);
+                    const uint64_t ad = amn ? sdesc_mn_sw128(sA + stage * A_HALF, A_HALF / 2)
+                                            : sdesc_k_sw128(sA + stage * A_HALF);
                     const uint64_t bd = bmn ? sdesc_mn_sw128(sB + stage * B_HALF, B_HALF / 2)
                                             : sdesc_k_sw128(sB + stage * B_HALF);
-                    const uint64_t bstep = bmn ? 2048 >> 4 : 2;  // one K = 16 step
+                    // one K = 16 step: 32 bytes along a K-major row, 16 rows of an MN-major box
+                    const uint64_t astep = amn ? 2048 >> 4 : 2, bstep = bmn ? 2048 >> 4 : 2;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_pair(dt, ad + 2 * kk, bd + bstep * kk, idesc,
+                        umma_bf16_pair(dt, ad + astep * kk, bd + bstep * kk, idesc,
                                        (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair_multicast(bar_empty + 8 * stage, BOTH);
                     if (++stage == STAGES2) {
@@ -834,14 +892,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < total; t += ustep) {
-            const Tile ti = decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
+            const Tile ti = KG ? decode_tile_kg_pair(t, a, rank)
+                               : decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half, &tmO, stg);
+            const bool zero = KG && s_off[ti.e + 1] == s_off[ti.e];
+            epilogue_tile(a, ti, tmem_base, (uint32_t)(acc * BN), q, lane, half, &tmO, stg, zero);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
@@ -874,7 +934,7 @@ int pair_clusters() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (!done[dev].load(std::memory_order_acquire)) {
         int n = 0;
-        if (set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel<false>, TC_SMEM_PAIR) ==
+        if (set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel<false, false>, TC_SMEM_PAIR) ==
             cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * 74);
@@ -887,7 +947,7 @@ int pair_clusters() {
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<false>, &cfg) != cudaSuccess)
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<false, false>, &cfg) != cudaSuccess)
                 n = 0;
         }
         cudaGetLastError();
@@ -904,7 +964,10 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
                         const int32_t *A_rows = nullptr, int64_t A_src_rows = 0,
                         const int32_t *out_token = nullptr, const float *out_gate = nullptr,
                         void *pre1 = nullptr, void *pre3 = nullptr, int b_mn = 0,
-                        int b_ksplit = 0, int b_krows = 0) {
+                        int b_ksplit = 0, int b_krows = 0, float *out_f32 = nullptr) {
+    if (out_f32 && (epi != EPI_STORE || out_token)) return cudaErrorInvalidValue;
+    // the f32 output leaves through per-thread stores; the store map only has to encode
+    if (out_f32) out = out_f32;
     // every B box is 128 rows: one half of the 256-row B tile; a gathered A reads one-row boxes
     CUtensorMap mA, mB, mB3, mO;
     if (A_rows ? !make_map(&mA, A, A_src_rows, K, 1) : !make_map(&mA, A, P, K, BM))
@@ -938,7 +1001,8 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.epi = epi;
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold_loads = hook.withhold;
-    a.tma_out = (MOE_GEMM_TMA_STORE && out_token == nullptr) ? 1 : 0;
+    a.tma_out = (MOE_GEMM_TMA_STORE && out_token == nullptr && out_f32 == nullptr) ? 1 : 0;
+    a.out_f32 = out_f32;
     a.a_rows = A_rows;
     a.a_src_rows = A_src_rows;
     a.out_token = out_token;
@@ -959,13 +1023,13 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
         const int64_t units = ((P + 2 * BM - 1) / (2 * BM) + E) * (int64_t)a.n_tiles;
         const int64_t ncl = clusters < units ? clusters : units;
         if (b_mn) {
-            cudaError_t err =
-                set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel<true>, TC_SMEM_PAIR);
+            cudaError_t err = set_max_dynamic_smem(
+                (const void *)grouped_gemm_pair_kernel<false, true>, TC_SMEM_PAIR);
             if (err != cudaSuccess) return err;
-            return launch_pdl(grouped_gemm_pair_kernel<true>, dim3((unsigned)(2 * ncl)),
+            return launch_pdl(grouped_gemm_pair_kernel<false, true>, dim3((unsigned)(2 * ncl)),
                               dim3(TC_THREADS), TC_SMEM_PAIR, s, 2, mA, mB, mB3, mO, a);
         }
-        return launch_pdl(grouped_gemm_pair_kernel<false>, dim3((unsigned)(2 * ncl)),
+        return launch_pdl(grouped_gemm_pair_kernel<false, false>, dim3((unsigned)(2 * ncl)),
                           dim3(TC_THREADS), TC_SMEM_PAIR, s, 2, mA, mB, mB3, mO, a);
     }
     const int64_t upper = ((P + BM - 1) / BM + E) * (int64_t)a.n_tiles;
@@ -984,20 +1048,28 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
                       TC_SMEM, s, 1, mA, mB, mB3, mO, a);
 }
 
+// The K-grouped GEMM runs on CTA pairs when its groups average at least this many rows of K.
+constexpr int KG_PAIR_MIN_K = 512;
+
 // K-grouped GEMM: out[e M + m, n] = sum over k in [kseg[e], kseg[e+1]) of A(m, k) B(n, k) for
 // every expert e (zeros where the segment is empty); kseg [E+1] device int32, multiples of 64.
 // mn = 0: A [M, kwidth] and B [N, kwidth] K-major (zero pad columns); mn = 1: A [kwidth, M] and
 // B [kwidth, N] MN-major with row strides lda and ldb (zero pad rows). out [E M, N]; all bf16.
 cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, int E, int M, int N,
                            int64_t kwidth, void *out, uint32_t *dev_status, cudaStream_t s,
-                           int mn, int64_t lda, int64_t ldb) {
+                           int mn, int64_t lda, int64_t ldb, int64_t map_rows = 0,
+                           float *out_f32 = nullptr) {
     if (E <= 0 || M <= 0 || N <= 0 || kwidth <= 0 || kwidth % BK != 0 || kwidth >= (1ll << 31))
         return cudaErrorInvalidValue;
+    if (out_f32) out = out_f32;  // the store map only has to encode
     CUtensorMap mA, mB, mO;
     if (mn) {
-        if (M % 64 != 0 || N % 64 != 0 || lda < M || ldb < N) return cudaErrorInvalidValue;
-        if (!make_map_ld(&mA, A, kwidth, M, lda, 64)) return cudaErrorInvalidValue;
-        if (!make_map_ld(&mB, B, kwidth, N, ldb, 64)) return cudaErrorInvalidValue;
+        // rows of A and B past map_rows (<= kwidth) read as zeros
+        const int64_t rows = map_rows > 0 ? map_rows : kwidth;
+        if (M % 64 != 0 || N % 64 != 0 || lda < M || ldb < N || rows > kwidth)
+            return cudaErrorInvalidValue;
+        if (!make_map_ld(&mA, A, rows, M, lda, 64)) return cudaErrorInvalidValue;
+        if (!make_map_ld(&mB, B, rows, N, ldb, 64)) return cudaErrorInvalidValue;
     } else {
         if (!make_map(&mA, A, M, kwidth, BM)) return cudaErrorInvalidValue;
         if (!make_map(&mB, B, N, kwidth, BN / 2)) return cudaErrorInvalidValue;
@@ -1016,7 +1088,8 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     a.epi = EPI_STORE;
     a.spin_limit_ns = SPIN_LIMIT_NS;
     a.withhold_loads = 0;
-    a.tma_out = MOE_GEMM_TMA_STORE;
+    a.tma_out = out_f32 ? 0 : MOE_GEMM_TMA_STORE;
+    a.out_f32 = out_f32;
     a.a_rows = nullptr;
     a.a_src_rows = 0;
     a.out_token = nullptr;
@@ -1028,6 +1101,19 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     a.b_ksplit = a.b_krows = 0;
     const int64_t units = (int64_t)E * a.m_tiles * a.n_tiles;
     if (units >= (1ll << 31)) return cudaErrorInvalidValue;
+    const int clusters = pair_clusters();
+    if (mn && clusters > 0 && kwidth >= (int64_t)KG_PAIR_MIN_K * E) {
+        // 256 x 256 tiles on CTA pairs (each CTA loads half of A and half of B), when the groups
+        // average KG_PAIR_MIN_K rows of K: with shorter sums the pair's per-tile handshake costs
+        // more than its halved operand traffic saves
+        const int64_t punits = (int64_t)E * ((a.m_tiles + 1) / 2) * a.n_tiles;
+        const int64_t ncl = clusters < punits ? clusters : punits;
+        cudaError_t err =
+            set_max_dynamic_smem((const void *)grouped_gemm_pair_kernel<true, true>, TC_SMEM_PAIR);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(grouped_gemm_pair_kernel<true, true>, dim3((unsigned)(2 * ncl)),
+                          dim3(TC_THREADS), TC_SMEM_PAIR, s, 2, mA, mB, mB, mO, a);
+    }
     int64_t grid = num_sms();
     if (grid > units) grid = units;
     if (mn) {
@@ -1075,8 +1161,19 @@ cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg
 
 cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,
                                   const int32_t *kseg, int E, int M, int N, int64_t rows,
-                                  void *out, uint32_t *dev_status, cudaStream_t s) {
-    return launch_gemm_kg(A, B, kseg, E, M, N, rows, out, dev_status, s, 1, lda, ldb);
+                                  void *out, uint32_t *dev_status, cudaStream_t s,
+                                  int64_t map_rows, float *out_f32) {
+    return launch_gemm_kg(A, B, kseg, E, M, N, rows, out, dev_status, s, 1, lda, ldb, map_rows,
+                          out_f32);
+}
+
+cudaError_t launch_gemm_rows_f32(const void *A, const void *B, int64_t P, int E, int K, int N,
+                                 const int32_t *offsets, float *out, uint32_t *dev_status,
+                                 cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    return launch_gemm(A, B, nullptr, P, E, K, N, EPI_STORE, offsets, nullptr, nullptr, dev_status,
+                       FaultHook(), s, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0, 0, 0,
+                       out);
 }
 
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,

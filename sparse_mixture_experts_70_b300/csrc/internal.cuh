@@ -238,8 +238,15 @@ cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg
 // The same over MN-major operands in the padded row layout: A [rows, M] with row stride lda and
 // B [rows, N] with row stride ldb (bf16; the K index is the row, expert e's rows
 // [kseg[e], kseg[e+1]) with zero pad rows).
+// map_rows > 0: rows of A and B at or past map_rows read as zeros (K extent `rows` rounded up
+// past the data); out_f32 (may be null): f32 output [E M, N] instead of the bf16 out.
 cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,
                                   const int32_t *kseg, int E, int M, int N, int64_t rows,
-                                  void *out, uint32_t *dev_status, cudaStream_t s);
+                                  void *out, uint32_t *dev_status, cudaStream_t s,
+                                  int64_t map_rows = 0, float *out_f32 = nullptr);
+// Row-grouped GEMM with K-major A and B and an f32 output [P, N] (no bias).
+cudaError_t launch_gemm_rows_f32(const void *A, const void *B, int64_t P, int E, int K, int N,
+                                 const int32_t *offsets, float *out, uint32_t *dev_status,
+                                 cudaStream_t s);
 
 }  // namespace moe
