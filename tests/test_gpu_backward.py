@@ -153,3 +153,51 @@ def test_training_forward_saves_what_the_backward_recomputes(w, opts, aux_w, z_w
     torch.cuda.synchronize()
     assert torch.equal(ya, yb)
     assert torch.equal(a.aux, b.aux) and torch.equal(a.topk_idx, b.topk_idx)
+
+
+@pytest.mark.parametrize("w", [
+    wl.small("bwd_e256_k32", T=64, d=128, f=128, E=256, k=32, seed=31),
+    wl.small("bwd_single_expert", T=300, d=128, f=192, E=1, k=1, act=wl.ACT_GELU_TANH,
+             gate=wl.GATE_RAW_PROB, has_bias=True, seed=32),
+], ids=lambda w: w.name)
+def test_backward_at_the_limits(w):
+    """E = 256 with k = 32 (every lane of the router warp holds a slot, 8 experts per lane) and a
+    single expert (its gate is p = 1, so the router gets only the bias and aux terms)."""
+    inputs = _case(w, bias_seed=7 if w.has_bias else None)
+    dy = _dy(w, w.seed + 300)
+    got, idx = _run(w, inputs, dy, 0.1, 0.05)
+    _compare(got, _oracle(w, inputs, idx, dy, 0.1, 0.05))
+
+
+def test_backward_is_deterministic_and_empty_batch_gives_zeros():
+    w = wl.small("bwd_det", T=700, d=128, f=256, E=8, k=2, router_bias_var=0.5, seed=33)
+    inputs = _case(w)
+    dev = to_dev(inputs)
+    cfg = B.config_for(w)
+    layer = B.Layer(cfg, dev)
+    layer.forward_train(dev["h"])
+    dy = _dy(w, 5).cuda()
+    first = {k: (v.clone() if v is not None else None)
+             for k, v in layer.backward(dev["h"], dy, 0.1, 0.1).items()}
+    for _ in range(3):
+        again = layer.backward(dev["h"], dy, 0.1, 0.1)
+        for k, v in first.items():
+            if v is not None:
+                assert torch.equal(v, again[k]), k  # no atomics: the same bits every call
+    torch.cuda.synchronize()
+    assert B.moe_device_status(layer.ws) == B.MOE_OK
+
+    w0 = w.with_(T=0)
+    dev0 = dict(dev)
+    dev0["h"] = torch.empty((0, w.d), dtype=torch.bfloat16, device="cuda")
+    layer0 = B.Layer(B.config_for(w0), dev0)
+    layer0.forward(dev0["h"])
+    # poison the outputs: an empty batch must overwrite every gradient with zeros
+    layer0.grads = None
+    g0 = layer0.backward(dev0["h"], torch.empty((0, w.d), dtype=torch.bfloat16, device="cuda"))
+    for k in ("dW_r", "db_r", "dW1", "dW3", "dW2"):
+        g0[k].fill_(7.0)
+    g0 = layer0.backward(dev0["h"], torch.empty((0, w.d), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    for k in ("dW_r", "db_r", "dW1", "dW3", "dW2"):
+        assert g0[k] is not None and not g0[k].any(), k
