@@ -390,7 +390,7 @@ class Layer:
         self._bws(dev)
         if getattr(self, "grads", None) is None:
             E, d, f = cfg.E, cfg.d, cfg.f
-            bf = torch.bfloat16
+            bf = torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
             sw = cfg.act == MOE_ACT_SWIGLU
             self.grads = dict(
                 dh=torch.empty((cfg.T, d), dtype=bf, device=dev),

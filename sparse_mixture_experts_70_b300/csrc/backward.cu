@@ -39,8 +39,6 @@ namespace {
 
 constexpr int BT = 64;  // tile edge of the transposing kernels
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
@@ -55,6 +53,27 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&v)[8]) {
         v[2 * i + 1] = __high2float(p);
     }
 }
+
+// 8 consecutive elements of a bf16 or f32 row (16-byte aligned) as f32, and back.
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
+    unpack8(__ldg(reinterpret_cast<const uint4 *>(p)), v);
+}
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]),
+                                               pack2(v[4], v[5]), pack2(v[6], v[7]));
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(float v) { return v; }
 
 // The expert whose padded segment holds padded column c (kseg in shared memory, E+1 entries).
 __device__ __forceinline__ int segment_of(const int32_t *kseg, int E, int c) {
@@ -106,15 +125,14 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t *slot_of, c
 // zero. When db2_part is given, db2_part[tile][o] is the tile's sum of gate_r[r] dy[t, o].
 // Block (x, y): the 64 rows of tile x, columns [2048 y, 2048 y + 2048), 8 per thread.
 constexpr int GP_COLS = 2048;
-__global__ void __launch_bounds__(256) gather_pad_kernel(const __nv_bfloat16 *h,
-                                                         const __nv_bfloat16 *dy,
+template <typename Elt>
+__global__ void __launch_bounds__(256) gather_pad_kernel(const Elt *h, const Elt *dy,
                                                          const int32_t *sorted_token,
                                                          const int32_t *offsets,
                                                          const int32_t *kseg_g,
                                                          const float *gate_r, int E, int64_t T,
-                                                         int64_t P, int d, __nv_bfloat16 *Xp,
-                                                         __nv_bfloat16 *dYp, float *db2_part,
-                                                         uint32_t *dev_status) {
+                                                         int64_t P, int d, Elt *Xp, Elt *dYp,
+                                                         float *db2_part, uint32_t *dev_status) {
     __shared__ int32_t kseg[257];
     __shared__ int32_t tok[BT];
     __shared__ float scl[BT];
@@ -156,19 +174,20 @@ __global__ void __launch_bounds__(256) gather_pad_kernel(const __nv_bfloat16 *h,
 #pragma unroll 4
         for (int jr = 0; jr < BT; ++jr) {
             const int t = tok[jr];
-            uint4 hv = make_uint4(0, 0, 0, 0), dv = make_uint4(0, 0, 0, 0);
+            float hv[8], dv[8];
             if (t >= 0) {
-                hv = __ldg(reinterpret_cast<const uint4 *>(h + (int64_t)t * d + col));
-                dv = __ldg(reinterpret_cast<const uint4 *>(dy + (int64_t)t * d + col));
+                load8(h + (int64_t)t * d + col, hv);
+                load8(dy + (int64_t)t * d + col, dv);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) hv[q] = dv[q] = 0.f;
             }
             const int64_t o = (int64_t)(c0 + jr) * d + col;
-            *reinterpret_cast<uint4 *>(Xp + o) = hv;
-            *reinterpret_cast<uint4 *>(dYp + o) = dv;
+            store8(Xp + o, hv);
+            store8(dYp + o, dv);
             if (db2_part) {
-                float v[8];
-                unpack8(dv, v);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = fmaf(scl[jr], v[q], acc[q]);
+                for (int q = 0; q < 8; ++q) acc[q] = fmaf(scl[jr], dv[q], acc[q]);
             }
         }
         if (db2_part) {
@@ -186,11 +205,12 @@ __global__ void __launch_bounds__(256) gather_pad_kernel(const __nv_bfloat16 *h,
 // padded rows of dA [kw, K2] (dA1 in columns [0, f), dA3 in [f, 2f) for SwiGLU) and of
 // Hs = g Hact [kw, f] (pad rows zero), dg_part[n-tile][r] = the tile's part of dHu . Hact, and
 // (when db1_part is given) the tile's column sums of dA1.
+template <typename Elt>
 struct ActBwd {
-    const __nv_bfloat16 *A1, *A3, *dHu;
+    const Elt *A1, *A3, *dHu;
     const float *gate_r;
     const int32_t *offsets, *kseg;
-    __nv_bfloat16 *dA, *Hs;
+    Elt *dA, *Hs;
     float *dg_part;   // [f/64, P]
     float *db1_part;  // [kw/64, f] or null
     int64_t P;
@@ -204,7 +224,8 @@ __device__ __forceinline__ float gelu_tanh_acc(float x, float &slope) {
     return 0.5f * x * (1.f + th);
 }
 
-__global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *dev_status) {
+template <typename Elt>
+__global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd<Elt> a, uint32_t *dev_status) {
     __shared__ float s1[BT][BT + 1];  // dA1 (f32) for the bias sums
     __shared__ int32_t kseg[257];
     pdl_wait();
@@ -234,10 +255,9 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
         if (valid) {
             const int64_t off = (int64_t)r * a.f + n0 + ch * 8;
             float x1[8], x3[8], du[8];
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.A1 + off)), x1);
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(
-                        a.dHu + (int64_t)(c0 + jr) * a.f + n0 + ch * 8)), du);
-            if (a.swiglu) unpack8(__ldg(reinterpret_cast<const uint4 *>(a.A3 + off)), x3);
+            load8(a.A1 + off, x1);
+            load8(a.dHu + (int64_t)(c0 + jr) * a.f + n0 + ch * 8, du);
+            if (a.swiglu) load8(a.A3 + off, x3);
             const float g = a.gate_r[r];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -261,17 +281,10 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
 #pragma unroll
             for (int q = 0; q < 8; ++q) d1[q] = d3[q] = hs[q] = 0.f;
         }
-        __nv_bfloat16 *row = a.dA + (int64_t)(c0 + jr) * K2 + n0 + ch * 8;
-        *reinterpret_cast<uint4 *>(row) =
-            make_uint4(pack2(d1[0], d1[1]), pack2(d1[2], d1[3]), pack2(d1[4], d1[5]),
-                       pack2(d1[6], d1[7]));
-        if (a.swiglu)
-            *reinterpret_cast<uint4 *>(row + a.f) =
-                make_uint4(pack2(d3[0], d3[1]), pack2(d3[2], d3[3]), pack2(d3[4], d3[5]),
-                           pack2(d3[6], d3[7]));
-        *reinterpret_cast<uint4 *>(a.Hs + (int64_t)(c0 + jr) * a.f + n0 + ch * 8) =
-            make_uint4(pack2(hs[0], hs[1]), pack2(hs[2], hs[3]), pack2(hs[4], hs[5]),
-                       pack2(hs[6], hs[7]));
+        Elt *row = a.dA + (int64_t)(c0 + jr) * K2 + n0 + ch * 8;
+        store8(row, d1);
+        if (a.swiglu) store8(row + a.f, d3);
+        store8(a.Hs + (int64_t)(c0 + jr) * a.f + n0 + ch * 8, hs);
         if (a.db1_part) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) s1[jr][ch * 8 + q] = d1[q];
@@ -301,8 +314,9 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd a, uint32_t *
 // hi = bf16(dz) and lo = bf16(dz - hi), so that dz W_r^T ~ hi Whi + lo Whi + hi Wlo and
 // h^T dz ~ h^T hi + h^T lo hold to about 2^-16; the per-block sums of dz (db_r) go to dbr_part.
 constexpr int RB_MAXEW = 8;  // experts per lane: E <= 256
+template <typename Elt>
 struct RouterBwd {
-    const __nv_bfloat16 *h, *dy;
+    const Elt *h, *dy;
     const float *W_r, *b_r, *b2;
     const float *part;  // tensor-core partial logits or null
     int S, ldp;
@@ -312,7 +326,8 @@ struct RouterBwd {
     int64_t T, P;
     int d, E, k, raw_prob;
     float aux_weight, zloss_weight;
-    __nv_bfloat16 *Zp;  // [T, Kp]
+    __nv_bfloat16 *Zp;  // [T, Kp] bf16 pieces (bf16 layers), or
+    float *dz;          // [T, E] f32 (f32 layers)
     int Kp;
     float *dbr_part;    // [gridDim.x, E]
 };
@@ -329,7 +344,8 @@ __device__ __forceinline__ float warp_max_f(float v) {
 }
 
 // dz of token t into this lane's experts lane + 32 i.
-__device__ __forceinline__ void router_token_grad(const RouterBwd &a, int64_t t, int lane,
+template <typename Elt>
+__device__ __forceinline__ void router_token_grad(const RouterBwd<Elt> &a, int64_t t, int lane,
                                                   float (&dz)[RB_MAXEW], uint32_t *dev_status) {
     const int E = a.E;
     float z[RB_MAXEW], p[RB_MAXEW];
@@ -345,13 +361,13 @@ __device__ __forceinline__ void router_token_grad(const RouterBwd &a, int64_t t,
     } else {
         // lanes split d; 8 experts at a time, each partial dot summed over the warp and kept by
         // the expert's owner lane
-        const __nv_bfloat16 *ht = a.h + t * a.d;
+        const Elt *ht = a.h + t * a.d;
         for (int e0 = 0; e0 < E; e0 += 8) {
             float pz[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) pz[q] = 0.f;
             for (int i0 = lane; i0 < a.d; i0 += 32) {
-                const float hv = bf(ht[i0]);
+                const float hv = to_f(ht[i0]);
                 const float *wr = a.W_r + (int64_t)i0 * E + e0;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
@@ -404,9 +420,9 @@ __device__ __forceinline__ void router_token_grad(const RouterBwd &a, int64_t t,
         if (r >= 0 && r < a.P && ej >= 0 && ej < E) {
             for (int q = lane; q < a.n_part; q += 32) v += a.dg_part[(int64_t)q * a.P + r];
             if (a.b2) {
-                const __nv_bfloat16 *dyt = a.dy + t * a.d;
+                const Elt *dyt = a.dy + t * a.d;
                 const float *b2e = a.b2 + (int64_t)ej * a.d;
-                for (int o = lane; o < a.d; o += 32) v = fmaf(bf(dyt[o]), b2e[o], v);
+                for (int o = lane; o < a.d; o += 32) v = fmaf(to_f(dyt[o]), b2e[o], v);
             }
         }
         v = warp_sum_f(v);
@@ -469,7 +485,9 @@ __device__ __forceinline__ void router_token_grad(const RouterBwd &a, int64_t t,
 
 // Warps stride over the tokens; each block sums dz over its tokens (per warp in token order,
 // then over the warps in order) into dbr_part[blockIdx.x].
-__global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint32_t *dev_status) {
+template <typename Elt>
+__global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd<Elt> a,
+                                                         uint32_t *dev_status) {
     __shared__ float wsum[8][256];
     pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -480,6 +498,17 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd a, uint
     for (int64_t t = (int64_t)blockIdx.x * 8 + warp; t < a.T; t += (int64_t)gridDim.x * 8) {
         float dz[RB_MAXEW];
         router_token_grad(a, t, lane, dz, dev_status);
+        if (a.dz) {
+#pragma unroll
+            for (int i = 0; i < RB_MAXEW; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) {
+                    a.dz[t * E + e] = dz[i];
+                    acc[i] += dz[i];
+                }
+            }
+            continue;
+        }
         __nv_bfloat16 *zp = a.Zp + t * a.Kp;
 #pragma unroll
         for (int i = 0; i < RB_MAXEW; ++i) {
@@ -536,11 +565,12 @@ __global__ void __launch_bounds__(256) wr_pieces_kernel(const float *W_r, int d,
 // cores) plus the k slots' input gradients, where c(t, j) = kseg[e] + slot_of[t k + j] -
 // offsets[e] with e = idx[t k + j] is the slot's padded row (dropped slots contribute nothing).
 // One thread per 8 features of a token.
-__global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const float *dhr,
+template <typename Elt>
+__global__ void __launch_bounds__(256) dh_kernel(const Elt *dX, const float *dhr,
                                                  const int32_t *slot_of, const int32_t *idx,
                                                  const int32_t *offsets_g, const int32_t *kseg_g,
-                                                 int64_t T, int d, int E, int k,
-                                                 __nv_bfloat16 *dh, uint32_t *dev_status) {
+                                                 int64_t T, int d, int E, int k, Elt *dh,
+                                                 uint32_t *dev_status) {
     __shared__ int32_t kseg[257], offs[257];
     pdl_wait();
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
@@ -567,13 +597,11 @@ __global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const 
                 continue;
             }
             float v[8];
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(dX + (int64_t)c * d + i0)), v);
+            load8(dX + (int64_t)c * d + i0, v);
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] += v[q];
         }
-        *reinterpret_cast<uint4 *>(dh + t * d + i0) =
-            make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
-                       pack2(acc[6], acc[7]));
+        store8(dh + t * d + i0, acc);
     }
     pdl_trigger();
 }
@@ -585,10 +613,11 @@ __global__ void __launch_bounds__(256) dh_kernel(const __nv_bfloat16 *dX, const 
 __global__ void __launch_bounds__(256) router_final_kernel(const float *o, int ldo, int d, int E,
                                                            int nsplit, const float *dbr_part,
                                                            int nblk, float *dW_r, float *db_r) {
+    // o == nullptr: dW_r is already final (f32 layers), only db_r is reduced
     pdl_wait();
     const int64_t n = (int64_t)d * E;
     const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (x < n) {
+    if (o && x < n) {
         const int64_t i = x / E;
         const int e = (int)(x - i * E);
         float v = 0.f;
@@ -598,7 +627,7 @@ __global__ void __launch_bounds__(256) router_final_kernel(const float *o, int l
         }
         dW_r[x] = v;
     }
-    const int64_t nb = (n + blockDim.x - 1) / blockDim.x;  // blocks of the dW_r part
+    const int64_t nb = o ? (n + blockDim.x - 1) / blockDim.x : 0;  // blocks of the dW_r part
     if (db_r && blockIdx.x >= nb) {
         const int64_t e = (int64_t)(blockIdx.x - nb) * (blockDim.x >> 5) + (threadIdx.x >> 5);
         const int lane = threadIdx.x & 31;
@@ -607,6 +636,128 @@ __global__ void __launch_bounds__(256) router_final_kernel(const float *o, int l
             for (int b = lane; b < nblk; b += 32) v += dbr_part[(int64_t)b * E + e];
             v = warp_sum_f(v);
             if (lane == 0) db_r[e] = v;
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// f32 grouped GEMM on the CUDA cores (the backward of f32 layers): C(m, n) (+)= sum_k A(m, k)
+// B(k, n) (+ bias[g][n]), A(m, k) = A[m sam + k sak], B(k, n) = B[k sbk + n sbn], per group g:
+//   rows mode (kmode = 0): rows [seg[g], seg[g+1]) of A and C (A's row a_rows[m] when given), B
+//     offset by g sbg, K = the whole K;
+//   K mode: the K range [seg[g], seg[g+1]), C offset by g cg, rows [0, M).
+// 64 x 64 output tiles, thread (tx, ty) of 16 x 16 owning 4 x 4 outputs, K in chunks of 16
+// through shared memory (loaded along whichever operand axis is contiguous).
+struct GemmF32 {
+    const float *A, *B, *bias;
+    float *C;
+    const int32_t *seg, *a_rows;
+    int64_t sam, sak, sbk, sbn, sbg, ldc, cg, a_src_rows;
+    int G, kmode, M, N, K, beta;
+};
+
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32 a, uint32_t *dev_status) {
+    __shared__ __align__(16) float As[16][BT + 4];
+    __shared__ __align__(16) float Bs[16][BT + 4];
+    __shared__ int32_t sseg[257], cum[257];
+    pdl_wait();
+    for (int q = threadIdx.x; q <= a.G; q += blockDim.x) sseg[q] = a.seg[q];
+    __syncthreads();
+    int g, m0, mend, kbeg, kend;
+    if (!a.kmode) {
+        if (threadIdx.x == 0) {
+            int acc = 0;
+            for (int q = 0; q < a.G; ++q) {
+                cum[q] = acc;
+                const int cnt = sseg[q + 1] - sseg[q];
+                acc += cnt > 0 ? (cnt + BT - 1) / BT : 0;
+            }
+            cum[a.G] = acc;
+        }
+        __syncthreads();
+        const int y = blockIdx.y;
+        if (y >= cum[a.G]) {
+            pdl_trigger();
+            return;
+        }
+        int lo = 0, hi = a.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cum[mid] <= y) lo = mid; else hi = mid - 1;
+        }
+        g = lo;
+        m0 = sseg[g] + (y - cum[g]) * BT;
+        mend = sseg[g + 1];
+        kbeg = 0;
+        kend = a.K;
+    } else {
+        g = blockIdx.z;
+        m0 = blockIdx.y * BT;
+        mend = a.M;
+        kbeg = sseg[g];
+        kend = sseg[g + 1];
+    }
+    const int n0 = blockIdx.x * BT;
+    const float *Bg = a.B + (a.kmode ? 0 : (int64_t)g * a.sbg);
+    float *Cg = a.C + (a.kmode ? (int64_t)g * a.cg : 0);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int k0 = kbeg; k0 < kend; k0 += 16) {
+        __syncthreads();
+        for (int x = threadIdx.x; x < 16 * BT; x += blockDim.x) {
+            int kk, mm;
+            if (a.sak == 1) { kk = x & 15; mm = x >> 4; } else { mm = x & 63; kk = x >> 6; }
+            const int m = m0 + mm, k = k0 + kk;
+            float v = 0.f;
+            if (m < mend && k < kend) {
+                int64_t arow = m;
+                if (a.a_rows) {
+                    arow = a.a_rows[m];
+                    if (arow < 0 || arow >= a.a_src_rows) {
+                        report(dev_status, DEV_ERR_INDEX);
+                        arow = -1;
+                    }
+                }
+                if (arow >= 0) v = a.A[arow * a.sam + (int64_t)k * a.sak];
+            }
+            As[kk][mm] = v;
+        }
+        for (int x = threadIdx.x; x < 16 * BT; x += blockDim.x) {
+            int kk, nn;
+            if (a.sbn == 1) { nn = x & 63; kk = x >> 6; } else { kk = x & 15; nn = x >> 4; }
+            const int n = n0 + nn, k = k0 + kk;
+            Bs[kk][nn] = (n < a.N && k < kend) ? Bg[(int64_t)k * a.sbk + (int64_t)n * a.sbn] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(&As[kk][ty * 4]);
+            const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 4]);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= mend) break;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx * 4 + j;
+            if (n >= a.N) break;
+            float v = acc[i][j];
+            if (a.bias) v += a.bias[(int64_t)g * a.N + n];
+            float *cp = Cg + (int64_t)m * a.ldc + n;
+            *cp = a.beta ? *cp + v : v;
         }
     }
     pdl_trigger();
@@ -643,7 +794,7 @@ int router_bwd_blocks(int64_t T) {
 
 struct BwdLayout {
     size_t gate_r, kseg, seg, A1, A3, Xp, dYp, dHu, dA, Hs, dX, dg_part, db1_part, db2_part, Zp,
-        Wp, dhr, dwr_out, dbr_part, total;
+        Wp, dz, dhr, dwr_out, dbr_part, total;
     int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
     int K2, n_part;
     int Kp;      // columns of the bf16 pieces of dz and W_r: roundup64(3 E)
@@ -673,26 +824,29 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     }
     const size_t E = (size_t)c.E, d = (size_t)c.d, f = (size_t)c.f, kw = (size_t)L.kw;
     const size_t nt = kw / BT;
+    const bool f32 = c.dtype == MOE_F32;
+    const size_t es = f32 ? 4 : 2;  // per-slot tensors in the layer's type
     size_t off = 0;
     L.gate_r = off;     off = al(off + (size_t)P * 4);
     L.kseg = off;       off = al(off + (E + 1) * 4);
     L.seg = off;        off = al(off + (size_t)(3 + L.nsplit) * 4);
-    L.A1 = off;         off = al(off + (size_t)P * f * 2);
-    L.A3 = off;         off = al(off + (sw ? (size_t)P * f * 2 : 0));
+    L.A1 = off;         off = al(off + (size_t)P * f * es);
+    L.A3 = off;         off = al(off + (sw ? (size_t)P * f * es : 0));
     // padded row layout [kw, .]: expert e's slots at rows [kseg[e], kseg[e+1]), pad rows zero
-    L.Xp = off;         off = al(off + kw * d * 2);
-    L.dYp = off;        off = al(off + kw * d * 2);
-    L.dHu = off;        off = al(off + kw * f * 2);
-    L.dA = off;         off = al(off + kw * (size_t)L.K2 * 2);
-    L.Hs = off;         off = al(off + kw * f * 2);
-    L.dX = off;         off = al(off + kw * d * 2);
+    L.Xp = off;         off = al(off + kw * d * es);
+    L.dYp = off;        off = al(off + kw * d * es);
+    L.dHu = off;        off = al(off + kw * f * es);
+    L.dA = off;         off = al(off + kw * (size_t)L.K2 * es);
+    L.Hs = off;         off = al(off + kw * f * es);
+    L.dX = off;         off = al(off + kw * d * es);
     L.dg_part = off;    off = al(off + (size_t)L.n_part * (size_t)P * 4);
     L.db1_part = off;   off = al(off + (c.has_bias ? nt * f * 4 : 0));
     L.db2_part = off;   off = al(off + (c.has_bias ? nt * d * 4 : 0));
-    L.Zp = off;         off = al(off + (size_t)c.T * L.Kp * 2);
-    L.Wp = off;         off = al(off + d * L.Kp * 2);
+    L.Zp = off;         off = al(off + (f32 ? 0 : (size_t)c.T * L.Kp * 2));
+    L.Wp = off;         off = al(off + (f32 ? 0 : d * L.Kp * 2));
+    L.dz = off;         off = al(off + (f32 ? (size_t)c.T * E * 4 : 0));
     L.dhr = off;        off = al(off + (size_t)c.T * d * 4);
-    L.dwr_out = off;    off = al(off + (size_t)L.nsplit * d * L.Nr * 4);
+    L.dwr_out = off;    off = al(off + (f32 ? 0 : (size_t)L.nsplit * d * L.Nr * 4));
     L.dbr_part = off;   off = al(off + (size_t)router_bwd_blocks(c.T) * E * 4);
     L.total = off;
     return L;
@@ -713,6 +867,10 @@ size_t backward_pre_offset(const moe_config_t &c, int which) {
 int backward_launches(const moe_config_t &c, bool saved) {
     if (c.T == 0) return 0;
     const bool sw = c.act == MOE_ACT_SWIGLU;
+    if (c.dtype == MOE_F32)  // CUDA-core GEMMs; the pre-activations are always recomputed
+        return 1 /*prep*/ + (sw ? 2 : 1) /*A1, A3*/ + 1 /*padded gathers*/ + 1 /*dHu*/ +
+               1 /*act*/ + (sw ? 2 : 1) /*dX*/ + (sw ? 3 : 2) /*dW*/ + 1 /*router bwd*/ +
+               2 /*dz W_r^T, dh*/ + 1 /*h^T dz*/ + 1 /*db_r*/ + (c.has_bias ? 2 : 0);
     const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
     return 2 /*prep, W_r pieces*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
            2 /*padded gathers, dHu*/ + 1 /*act*/ + 1 /*dX*/ + (sw ? 3 : 2) /*dW*/ +
@@ -730,7 +888,6 @@ moe_status_t moe_backward_workspace_size(const moe_config_t *cfg, size_t *bytes)
     const moe_status_t st = validate_config(cfg);
     if (st != MOE_OK) return st;
     if (!bytes) return MOE_ERR_INVALID_ARG;
-    if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     *bytes = bwd_layout(*cfg).total;
     return MOE_OK;
 }
@@ -740,7 +897,7 @@ moe_status_t moe_backward_launch_count(const moe_config_t *cfg, int32_t saved_pr
     const moe_status_t st = validate_config(cfg);
     if (st != MOE_OK) return st;
     if (!kernels || (saved_preact != 0 && saved_preact != 1)) return MOE_ERR_INVALID_ARG;
-    if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (cfg->dtype == MOE_F32 && saved_preact) return MOE_ERR_UNSUPPORTED;
     *kernels = backward_launches(*cfg, saved_preact != 0);
     return MOE_OK;
 }
@@ -755,10 +912,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     moe_status_t st = validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config_t &c = *cfg;
-    if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     const bool sw = c.act == MOE_ACT_SWIGLU;
+    const bool f32 = c.dtype == MOE_F32;
     if (!isfinite(aux_weight) || !isfinite(zloss_weight)) return MOE_ERR_INVALID_ARG;
     if (saved_preact != 0 && saved_preact != 1) return MOE_ERR_INVALID_ARG;
+    if (f32 && saved_preact) return MOE_ERR_UNSUPPORTED;  // f32 layers recompute them
     if (!al16(ws) || !al16(bws) || !al4(dW_r) || !al16(dW1) || !al16(dW2) ||
         (sw && !al16(dW3)) || ((b_r != nullptr) != (db_r != nullptr)) || (db_r && !al4(db_r)) ||
         (c.has_bias && (!al4(db1) || !al4(db2) || !al4(b1) || !al4(b2))))
@@ -768,13 +926,14 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     if (ws_bytes < L.total || bws_bytes < B.total) return MOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t E = c.E, d = c.d, f = c.f;
+    const size_t wes = f32 ? 4 : 2;  // weight-gradient element size
     if (c.T == 0) {
         // no tokens: every gradient is zero
         cudaError_t e = cudaMemsetAsync(dW_r, 0, (size_t)d * E * 4, s);
         if (e == cudaSuccess && db_r) e = cudaMemsetAsync(db_r, 0, (size_t)E * 4, s);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dW1, 0, (size_t)(E * f * d) * 2, s);
-        if (e == cudaSuccess && sw) e = cudaMemsetAsync(dW3, 0, (size_t)(E * f * d) * 2, s);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, (size_t)(E * f * d) * 2, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW1, 0, (size_t)(E * f * d) * wes, s);
+        if (e == cudaSuccess && sw) e = cudaMemsetAsync(dW3, 0, (size_t)(E * f * d) * wes, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, (size_t)(E * f * d) * wes, s);
         if (e == cudaSuccess && c.has_bias) e = cudaMemsetAsync(db1, 0, (size_t)(E * f) * 4, s);
         if (e == cudaSuccess && c.has_bias) e = cudaMemsetAsync(db2, 0, (size_t)(E * d) * 4, s);
         return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -812,6 +971,153 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     MOE_TRY(launch_pdl(bwd_prep_kernel, dim3((unsigned)((P + 255) / 256)), dim3(256), 0, s, 1,
                        slot_of, gates, offsets, P, c.E, c.T, B.nsplit, gate_r, kseg, seg,
                        dev_status));
+    if (f32) {
+        // f32 layers: the same steps on the CUDA cores (gemm_f32_kernel), no weight pieces
+        if (B.kw / BT + c.E >= 65535 || (P + BT - 1) / BT + c.E >= 65535 ||
+            (c.T + BT - 1) / BT + 1 >= 65535)
+            return MOE_ERR_UNSUPPORTED;
+        auto F = [&](size_t o) { return reinterpret_cast<float *>(b + o); };
+        auto gemm = [&](const float *A, int64_t sam, int64_t sak, const int32_t *a_rows,
+                        int64_t a_src_rows, const float *Bm, int64_t sbk, int64_t sbn,
+                        int64_t sbg, const float *bias, float *C, int64_t ldc, int64_t cg,
+                        const int32_t *sg, int G, int kmode, int M, int N, int K,
+                        int64_t rows_bound, int beta) -> cudaError_t {
+            GemmF32 ga;
+            ga.A = A;
+            ga.B = Bm;
+            ga.bias = bias;
+            ga.C = C;
+            ga.seg = sg;
+            ga.a_rows = a_rows;
+            ga.sam = sam;
+            ga.sak = sak;
+            ga.sbk = sbk;
+            ga.sbn = sbn;
+            ga.sbg = sbg;
+            ga.ldc = ldc;
+            ga.cg = cg;
+            ga.a_src_rows = a_src_rows;
+            ga.G = G;
+            ga.kmode = kmode;
+            ga.M = M;
+            ga.N = N;
+            ga.K = K;
+            ga.beta = beta;
+            const dim3 grid((unsigned)((N + BT - 1) / BT),
+                            (unsigned)(kmode ? (M + BT - 1) / BT : (rows_bound + BT - 1) / BT + G),
+                            (unsigned)(kmode ? G : 1));
+            return launch_pdl(gemm_f32_kernel, grid, dim3(256), 0, s, 1, ga, dev_status);
+        };
+        const float *hf = static_cast<const float *>(h), *dyf = static_cast<const float *>(dy);
+        const float *W1f = static_cast<const float *>(W1), *W3f = static_cast<const float *>(W3);
+        const float *W2f = static_cast<const float *>(W2);
+        // A1 = h[token] W1_e^T (+ b1), A3 = h[token] W3_e^T over the sorted rows
+        MOE_TRY(gemm(hf, d, 1, sorted_token, c.T, W1f, 1, d, f * d, c.has_bias ? b1 : nullptr,
+                     F(B.A1), f, 0, offsets, c.E, 0, 0, c.f, c.d, P, 0));
+        if (sw)
+            MOE_TRY(gemm(hf, d, 1, sorted_token, c.T, W3f, 1, d, f * d, nullptr, F(B.A3), f, 0,
+                         offsets, c.E, 0, 0, c.f, c.d, P, 0));
+        // padded rows of h and dy (+ db2 parts)
+        MOE_TRY(launch_pdl(gather_pad_kernel<float>,
+                           dim3((unsigned)(B.kw / BT), (unsigned)((c.d + GP_COLS - 1) / GP_COLS)),
+                           dim3(256), 0, s, 1, hf, dyf, sorted_token, offsets,
+                           static_cast<const int32_t *>(kseg), static_cast<const float *>(gate_r),
+                           c.E, c.T, P, c.d, F(B.Xp), F(B.dYp),
+                           c.has_bias ? F(B.db2_part) : nullptr, dev_status));
+        // dHu = dYp W2_e (W2_e [d, f]: B(k = o, n) = W2[e][o][n]) over the padded rows
+        MOE_TRY(gemm(F(B.dYp), d, 1, nullptr, 0, W2f, f, 1, d * f, nullptr, F(B.dHu), f, 0, kseg,
+                     c.E, 0, 0, c.f, c.d, B.kw, 0));
+        ActBwd<float> ab;
+        ab.A1 = F(B.A1);
+        ab.A3 = sw ? F(B.A3) : nullptr;
+        ab.dHu = F(B.dHu);
+        ab.gate_r = gate_r;
+        ab.offsets = offsets;
+        ab.kseg = kseg;
+        ab.dA = F(B.dA);
+        ab.Hs = F(B.Hs);
+        ab.dg_part = F(B.dg_part);
+        ab.db1_part = c.has_bias ? F(B.db1_part) : nullptr;
+        ab.P = P;
+        ab.E = c.E;
+        ab.f = c.f;
+        ab.swiglu = sw ? 1 : 0;
+        MOE_TRY(launch_pdl(act_bwd_kernel<float>, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256),
+                           0, s, 1, ab, dev_status));
+        // dX = dA1 W1_e (+ dA3 W3_e) (W1_e [f, d]: B(k = j, n = i) = W1[e][j][i])
+        MOE_TRY(gemm(F(B.dA), B.K2, 1, nullptr, 0, W1f, d, 1, f * d, nullptr, F(B.dX), d, 0, kseg,
+                     c.E, 0, 0, c.d, c.f, B.kw, 0));
+        if (sw)
+            MOE_TRY(gemm(F(B.dA) + c.f, B.K2, 1, nullptr, 0, W3f, d, 1, f * d, nullptr, F(B.dX), d,
+                         0, kseg, c.E, 0, 0, c.d, c.f, B.kw, 1));
+        // weight gradients over each expert's padded rows
+        MOE_TRY(gemm(F(B.dYp), 1, d, nullptr, 0, F(B.Hs), f, 1, 0, nullptr,
+                     static_cast<float *>(dW2), f, d * f, kseg, c.E, 1, c.d, c.f, 0, 0, 0));
+        MOE_TRY(gemm(F(B.dA), 1, B.K2, nullptr, 0, F(B.Xp), d, 1, 0, nullptr,
+                     static_cast<float *>(dW1), d, f * d, kseg, c.E, 1, c.f, c.d, 0, 0, 0));
+        if (sw)
+            MOE_TRY(gemm(F(B.dA) + c.f, 1, B.K2, nullptr, 0, F(B.Xp), d, 1, 0, nullptr,
+                         static_cast<float *>(dW3), d, f * d, kseg, c.E, 1, c.f, c.d, 0, 0, 0));
+        // router: dz (f32), dz W_r^T, dh, h^T dz, db_r
+        RouterBwd<float> rb;
+        rb.h = hf;
+        rb.dy = dyf;
+        rb.W_r = W_r;
+        rb.b_r = b_r;
+        rb.b2 = c.has_bias ? b2 : nullptr;
+        rb.part = nullptr;
+        rb.S = 0;
+        rb.ldp = 0;
+        rb.topk_idx = idx;
+        rb.slot_of = slot_of;
+        rb.counts = cnt;
+        rb.gates = gates;
+        rb.dg_part = F(B.dg_part);
+        rb.n_part = B.n_part;
+        rb.T = c.T;
+        rb.P = P;
+        rb.d = c.d;
+        rb.E = c.E;
+        rb.k = c.k;
+        rb.raw_prob = c.gate == MOE_GATE_RAW_PROB ? 1 : 0;
+        rb.aux_weight = aux_weight;
+        rb.zloss_weight = zloss_weight;
+        rb.Zp = nullptr;
+        rb.dz = F(B.dz);
+        rb.Kp = 0;
+        rb.dbr_part = F(B.dbr_part);
+        const int rblocks = router_bwd_blocks(c.T);
+        MOE_TRY(launch_pdl(router_bwd_kernel<float>, dim3((unsigned)rblocks), dim3(256), 0, s, 1,
+                           rb, dev_status));
+        // dz W_r^T: B(k = e, n = i) = W_r[i][e]; one group of T rows (seg = {0, T})
+        MOE_TRY(gemm(F(B.dz), E, 1, nullptr, 0, W_r, 1, E, 0, nullptr, F(B.dhr), d, 0, seg, 1, 0,
+                     0, c.d, c.E, c.T, 0));
+        {
+            const int64_t n = c.T * (d / 8);
+            int64_t blocks = (n + 255) / 256;
+            if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
+            MOE_TRY(launch_pdl(dh_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+                               static_cast<const float *>(F(B.dX)),
+                               static_cast<const float *>(F(B.dhr)), slot_of, idx, offsets,
+                               static_cast<const int32_t *>(kseg), c.T, c.d, c.E, c.k,
+                               static_cast<float *>(dh), dev_status));
+        }
+        // h^T dz straight into dW_r (K = the T tokens, seg = {0, T})
+        MOE_TRY(gemm(hf, 1, d, nullptr, 0, F(B.dz), E, 1, 0, nullptr, dW_r, E, 0, seg, 1, 1, c.d,
+                     c.E, 0, 0, 0));
+        MOE_TRY(launch_pdl(router_final_kernel, dim3((unsigned)((E + 7) / 8)), dim3(256), 0, s, 1,
+                           static_cast<const float *>(nullptr), 0, c.d, c.E, 1,
+                           static_cast<const float *>(F(B.dbr_part)), rblocks, dW_r, db_r));
+        if (c.has_bias) {
+            MOE_TRY(launch_pdl(seg_sum_kernel, dim3((unsigned)((E * f + 255) / 256)), dim3(256), 0,
+                               s, 1, static_cast<const float *>(F(B.db1_part)), c.f,
+                               static_cast<const int32_t *>(kseg), c.E, db1));
+            MOE_TRY(launch_pdl(seg_sum_kernel, dim3((unsigned)((E * d + 255) / 256)), dim3(256), 0,
+                               s, 1, static_cast<const float *>(F(B.db2_part)), c.d,
+                               static_cast<const int32_t *>(kseg), c.E, db2));
+        }
+        return MOE_OK;
+    }
     // 2. the router weight as bf16 pieces (for dz W_r^T on the tensor cores)
     {
         const int64_t n = d * B.Kp;
@@ -834,7 +1140,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     // 4. padded rows of h and dy (+ db2 parts), then dHu = dYp W2_e over each expert's padded
     // rows (W2_e read MN-major: rows o of W2 [E d, f] are the K index)
     const int32_t *ksegc = kseg;
-    MOE_TRY(launch_pdl(gather_pad_kernel,
+    MOE_TRY(launch_pdl(gather_pad_kernel<__nv_bfloat16>,
                        dim3((unsigned)(B.kw / BT), (unsigned)((c.d + GP_COLS - 1) / GP_COLS)),
                        dim3(256), 0, s, 1, static_cast<const __nv_bfloat16 *>(h),
                        static_cast<const __nv_bfloat16 *>(dy), sorted_token, offsets, ksegc,
@@ -843,7 +1149,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     MOE_TRY(launch_gemm_rows_bmn(bf(B.dYp), W2, nullptr, c.d, 0, B.kw, c.E, c.d, c.f, ksegc,
                                  bf(B.dHu), dev_status, s));
     // 5. activation backward: dA, Hs = g Hact (padded rows), dg parts, db1 parts
-    ActBwd ab;
+    ActBwd<__nv_bfloat16> ab;
     ab.A1 = bf(B.A1);
     ab.A3 = sw ? bf(B.A3) : nullptr;
     ab.dHu = bf(B.dHu);
@@ -858,7 +1164,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     ab.E = c.E;
     ab.f = c.f;
     ab.swiglu = sw ? 1 : 0;
-    MOE_TRY(launch_pdl(act_bwd_kernel, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256), 0, s, 1,
+    MOE_TRY(launch_pdl(act_bwd_kernel<__nv_bfloat16>, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256), 0, s, 1,
                        ab, dev_status));
     // 6. dX = dA1 W1_e + dA3 W3_e over the padded rows: one GEMM over K2 = [dA1 | dA3], B = W1
     // then W3 read MN-major
@@ -874,7 +1180,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         MOE_TRY(launch_gemm_kgroup_mn(bf(B.dA) + c.f, B.K2, bf(B.Xp), c.d, ksegc, c.E, c.f, c.d,
                                       B.kw, dW3, dev_status, s));
     // 9. router: logits (tensor-core partials when the forward used them), dz
-    RouterBwd rb;
+    RouterBwd<__nv_bfloat16> rb;
     rb.h = static_cast<const __nv_bfloat16 *>(h);
     rb.dy = static_cast<const __nv_bfloat16 *>(dy);
     rb.W_r = W_r;
@@ -905,10 +1211,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     rb.aux_weight = aux_weight;
     rb.zloss_weight = zloss_weight;
     rb.Zp = bf(B.Zp);
+    rb.dz = nullptr;
     rb.Kp = B.Kp;
     rb.dbr_part = fl(B.dbr_part);
     const int rblocks = router_bwd_blocks(c.T);
-    MOE_TRY(launch_pdl(router_bwd_kernel, dim3((unsigned)rblocks), dim3(256), 0, s, 1, rb,
+    MOE_TRY(launch_pdl(router_bwd_kernel<__nv_bfloat16>, dim3((unsigned)rblocks), dim3(256), 0, s, 1, rb,
                        dev_status));
     // 10. the router's h-gradient dz W_r^T = Zp Wp^T (f32, one group of T rows), then
     // dh = that + sum_j dX[padded row of slot j]
@@ -918,7 +1225,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         const int64_t n = c.T * (d / 8);
         int64_t blocks = (n + 255) / 256;
         if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
-        MOE_TRY(launch_pdl(dh_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+        MOE_TRY(launch_pdl(dh_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, s, 1,
                            static_cast<const __nv_bfloat16 *>(bf(B.dX)),
                            static_cast<const float *>(fl(B.dhr)), slot_of, idx, offsets, ksegc,
                            c.T, c.d, c.E, c.k, static_cast<__nv_bfloat16 *>(dh), dev_status));

@@ -190,11 +190,11 @@ def test_backward_arguments_are_checked_before_any_cuda_call():
     L = B.lib()
     fake = 1 << 40          # never dereferenced: the checks run before any launch
     f32 = B.config_for(wl.WORKLOADS["micro"])
-    n = ctypes.c_size_t()
-    assert L.moe_backward_workspace_size(ctypes.byref(f32), ctypes.byref(n)) == \
-        B.MOE_ERR_UNSUPPORTED
+    assert B.moe_backward_workspace_size(f32) > 0
     k = ctypes.c_int32()
-    assert L.moe_backward_launch_count(ctypes.byref(f32), 0, ctypes.byref(k)) == \
+    assert L.moe_backward_launch_count(ctypes.byref(f32), 0, ctypes.byref(k)) == B.MOE_OK
+    assert k.value == 15  # f32: CUDA-core GEMMs, pre-activations recomputed
+    assert L.moe_backward_launch_count(ctypes.byref(f32), 1, ctypes.byref(k)) == \
         B.MOE_ERR_UNSUPPORTED
     cfg = B.config(T=64, d=128, f=256, E=8, k=2)
     assert L.moe_backward_launch_count(ctypes.byref(cfg), 2, ctypes.byref(k)) == \
@@ -208,7 +208,7 @@ def test_backward_arguments_are_checked_before_any_cuda_call():
         return L.moe_backward(ctypes.byref(c), fake, fake, b_r, dW1, None, fake, fake, None,
                               None, None, fake, aux, 0.0, fake, fake, db_r, fake, None, fake,
                               fake, None, ws, nws, bws, bws_bytes, saved, None)
-    assert bwd(c=f32) == B.MOE_ERR_UNSUPPORTED
+    assert bwd(c=f32, saved=1) == B.MOE_ERR_UNSUPPORTED  # f32 layers recompute
     assert bwd(saved=2) == B.MOE_ERR_INVALID_ARG
     assert bwd(aux=float("nan")) == B.MOE_ERR_INVALID_ARG
     assert bwd(ws=None) == B.MOE_ERR_INVALID_ARG

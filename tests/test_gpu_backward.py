@@ -201,3 +201,23 @@ def test_backward_is_deterministic_and_empty_batch_gives_zeros():
     torch.cuda.synchronize()
     for k in ("dW_r", "db_r", "dW1", "dW3", "dW2"):
         assert g0[k] is not None and not g0[k].any(), k
+
+
+F32_CASES = [
+    # the micro workload's shape: GELU with biases, f32 throughout, CUDA-core GEMMs
+    (wl.small("bwd_f32_micro", T=256, d=128, f=512, E=8, k=2, act=wl.ACT_GELU_TANH, dtype="f32",
+              has_bias=True, seed=41), dict(bias_seed=8), 0.2, 0.1),
+    (wl.small("bwd_f32_swiglu_capacity", T=300, d=192, f=320, E=6, k=2, dtype="f32",
+              capacity_factor=1.0, router_bias_var=0.5, seed=42), {}, 0.0, 0.05),
+]
+F32_REL_L2 = 2e-5  # f32 products and sums throughout (the oracle is double)
+
+
+@pytest.mark.parametrize("w,opts,aux_w,z_w", F32_CASES, ids=lambda c: getattr(c, "name", ""))
+def test_f32_backward_matches_oracle(w, opts, aux_w, z_w):
+    inputs = _case(w, **opts)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 100)
+    dy = torch.randn((w.T, w.d), generator=g)
+    got, idx = _run(w, inputs, dy, aux_w, z_w)
+    _compare(got, _oracle(w, inputs, idx, dy, aux_w, z_w), bound=F32_REL_L2)
