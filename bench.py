@@ -30,11 +30,12 @@ Each measurement carries:
   graph        the same step recorded once in a CUDA graph (Layer.capture) and replayed K times:
                the launch-bound shapes' time without host launch cost;
   clocks       nvidia-smi samples taken during the timed region;
-  backward     (bf16 workloads) K moe_backward calls after moe_forward_train (which keeps the
-               first GEMM's pre-activations), for an upstream gradient dy ~ N(0, 1) with
-               auxiliary and z-loss weights: ms per step, tokens/s and the roofline of the whole
-               backward (algorithmic work: the data and weight gradients of the expert GEMMs,
-               twice the forward's flops); train_step times K forward_train + backward pairs.
+  backward     K moe_backward calls after moe_forward_train (which keeps the first GEMM's
+               pre-activations; f32 layers: after moe_forward, recomputing them), for an upstream
+               gradient dy ~ N(0, 1) with auxiliary and z-loss weights: ms per step, tokens/s and
+               the roofline of the whole backward (algorithmic work: the data and weight
+               gradients of the expert GEMMs, twice the forward's flops); train_step times K
+               forward + backward pairs.
 --impl reference times the oracle itself (the method's plain statement) as the reference arm.
 """
 from __future__ import annotations
@@ -102,18 +103,28 @@ def _tc_peak(peaks: dict, region_s: float, reasons) -> tuple:
 BWD_AUX_WEIGHT, BWD_ZLOSS_WEIGHT = 0.01, 0.001
 
 
-def backward_roofline(w, bwd_ms: float, peaks: dict, region_s: float, reasons) -> dict:
+def backward_roofline(w, bwd_ms: float, peaks: dict, region_s: float, reasons,
+                      alu: dict | None = None) -> dict:
     """The backward's roofline entry. Algorithmic flops: the expert GEMMs' data gradients (dX,
     dHact) and weight gradients, twice the forward's; algorithmic bytes: every expert's weights
     read and its weight gradients written once, plus h, dy and dh. The bound is the tensor peak
     when flops per byte exceed the ridge point, else the HBM copy bandwidth."""
     flops = 2 * w.expert_flops()
-    nbytes = 2 * w.weight_bytes() + 3 * w.T * w.d * 2
+    es = 4 if w.dtype == "f32" else 2
+    nbytes = 2 * w.weight_bytes() + 3 * w.T * w.d * es
     sec = bwd_ms * 1e-3
     tflops, gbs = flops / sec / 1e12, nbytes / sec / 1e9
     tc_peak, tc_alt, kind, alt_kind = _tc_peak(peaks, region_s, reasons)
     common = {"algorithmic_flops": flops, "algorithmic_bytes": nbytes,
               "flop_per_byte": flops / nbytes, "region_s": region_s}
+    if w.dtype == "f32":  # CUDA-core FFMA against the measured FP32 rate
+        rate = alu["tflops"]
+        if flops / nbytes >= rate * 1e12 / (peaks["hbm"] * 1e9):
+            return {"bound": "alu", "achieved": tflops, "peak": rate, "unit": "TFLOP/s",
+                    "frac": tflops / rate, "peak_kind": alu["how"], "hbm_gbs": gbs, **common}
+        return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm"], "peak_kind": f"HBM copy ({peaks['source']})",
+                "alu_tflops": tflops, **common}
     if flops / nbytes >= tc_peak * 1e12 / (peaks["hbm"] * 1e9):
         return {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": tflops / tc_peak, "peak_kind": f"{kind} ({peaks['source']})",
@@ -436,8 +447,8 @@ def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.
     if B.moe_device_status(layer.ws) != B.MOE_OK:
         raise SystemExit(f"{w.name}: device status after graph region")
     del graph
-    bwd = (bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed)
-           if w.dtype == "bf16" and not args.no_backward else None)
+    bwd = (bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed, alu)
+           if not args.no_backward else None)
     del flush
 
     ms, e_ms, ffn_ms, g_ms = D.max_over_ranks([ms, e_ms, ffn_ms, g_ms], device="cuda")
@@ -471,18 +482,21 @@ def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.
     return entry
 
 
-def bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed) -> dict:
+def bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed, alu=None) -> dict:
     """The backward of workload w for a seeded dy ~ N(0, 1): K moe_backward calls after one
-    moe_forward_train of h (the routing they differentiate at and the saved pre-activations),
-    then K training steps (moe_forward_train + moe_backward); returns the measurement entry."""
+    moe_forward_train of h (the routing they differentiate at and the saved pre-activations;
+    f32 layers: moe_forward, the backward recomputing them), then K training steps (forward +
+    backward); returns the measurement entry."""
     g = torch.Generator(device="cuda")
     g.manual_seed(w.seed + 1000)
-    dy = torch.randn((w.T, w.d), generator=g, device="cuda").to(torch.bfloat16)
-    layer.forward_train(h, stream)
+    dy = torch.randn((w.T, w.d), generator=g, device="cuda").to(w.torch_dtype)
+    f32 = w.dtype == "f32"
+    fwd = (lambda: layer.forward(h, stream)) if f32 else (lambda: layer.forward_train(h, stream))
+    fwd()
     bwd = lambda i: layer.backward(h, dy, BWD_AUX_WEIGHT, BWD_ZLOSS_WEIGHT, stream)  # noqa: E731
 
     def train(i):
-        layer.forward_train(h, stream)
+        fwd()
         bwd(i)
 
     for i in range(args.warmup):
@@ -505,19 +519,21 @@ def bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed) -> dict
         raise SystemExit(f"{w.name}: device status after the backward regions")
     ms, t_ms = D.max_over_ranks([ms, t_ms], device="cuda")
     world = D.env()[1]
-    launches = B.moe_backward_launch_count(layer.cfg, True)
+    launches = B.moe_backward_launch_count(layer.cfg, not f32)
     fwd_launches = B.moe_forward_launch_count(layer.cfg)
     del layer.bws, layer.grads
     layer.bws = layer.grads = None
     return {"value": D.job_tokens_per_s(w.T, world, ms), "unit": "tokens/s",
-            "ms_per_step": ms, "steps": args.steps, "pre_activations": "saved by the forward",
+            "ms_per_step": ms, "steps": args.steps,
+            "pre_activations": "recomputed" if f32 else "saved by the forward",
             "aux_weight": BWD_AUX_WEIGHT, "zloss_weight": BWD_ZLOSS_WEIGHT,
             "roofline": backward_roofline(w, ms, peaks, ms * args.steps * 1e-3,
-                                          clocks.get("reasons")),
+                                          clocks.get("reasons"), alu),
             "gpu_launches": launches * args.steps, "launches_per_step": launches,
             "train_step": {"value": D.job_tokens_per_s(w.T, world, t_ms), "unit": "tokens/s",
                            "ms_per_step": t_ms,
-                           "what": "moe_forward_train + moe_backward, one call each",
+                           "what": ("moe_forward + moe_backward" if f32 else
+                                    "moe_forward_train + moe_backward") + ", one call each",
                            "gpu_launches": (launches + fwd_launches) * args.steps},
             "clocks": clocks}
 

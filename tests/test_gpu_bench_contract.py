@@ -37,3 +37,10 @@ def test_bench_line_for_the_micro_workload():
     assert e2e["d2h_bytes_per_step"] == 256 * 128 * 4 + 4
     assert d["gpu_launches"] == 4 * 4   # four kernels per micro step
     assert d["clocks"]["samples"] >= 0
+    # the backward of the same f32 layer (recomputing its pre-activations on the CUDA cores)
+    b = d["backward"]
+    assert b["pre_activations"] == "recomputed"
+    assert b["roofline"]["bound"] in ("alu", "hbm") and 0 < b["roofline"]["frac"] < 1
+    assert b["value"] == pytest.approx(256 / (b["ms_per_step"] * 1e-3), rel=1e-6)
+    assert b["launches_per_step"] == 15 and b["gpu_launches"] == 15 * 4
+    assert b["train_step"]["ms_per_step"] > 0
