@@ -307,8 +307,53 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd<Elt> a, uint3
 }
 
 // ---------------------------------------------------------------------------------------------
-// Router backward, one warp per token: the logits z (from the tensor-core partial logits
-// part[S][T][ldp], or a direct dot product over d), p, lse, the gate gradients dg_j of the k slots
+// Router logits z[t, e] = h[t] . W_r[:, e] (no bias) for layers whose forward router is not the
+// tensor-core one (few tokens, or f32): one block per token (striding over the tokens), its 8
+// warps splitting d; experts 8 at a time, each thread's 8 partial dots summed over its warp by
+// shuffles and then over the warps in order.
+template <typename Elt>
+__global__ void __launch_bounds__(256) router_logits_direct_kernel(const Elt *h, const float *W_r,
+                                                                   int64_t T, int d, int E,
+                                                                   float *z) {
+    __shared__ float wpart[8][8];
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const Elt *ht = h + t * d;
+        for (int e0 = 0; e0 < E; e0 += 8) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            for (int i = threadIdx.x; i < d; i += blockDim.x) {
+                const float hv = to_f(ht[i]);
+                const float *wr = W_r + (int64_t)i * E + e0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (e0 + q < E) acc[q] = fmaf(hv, __ldg(wr + q), acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float v = acc[q];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) wpart[warp][q] = v;
+            }
+            __syncthreads();
+            if (threadIdx.x < 8 && e0 + (int)threadIdx.x < E) {
+                float v = 0.f;
+                for (int w = 0; w < 8; ++w) v += wpart[w][threadIdx.x];
+                z[t * E + e0 + threadIdx.x] = v;
+            }
+            __syncthreads();
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Router backward, one warp per token: the logits z (summed over the partial logits
+// part[S][T][ldp]: the tensor-core router's K chunks, or S = 1 from router_logits_direct_kernel),
+// p, lse, the gate gradients dg_j of the k slots
 // (the tiles' parts summed, plus dy . b2_e when b2 is given), then dz = dL/dz. dz leaves as bf16
 // pieces for the two router GEMMs: Zp[t] = [hi(dz) | lo(dz) | hi(dz) | 0 ...] (Kp columns), with
 // hi = bf16(dz) and lo = bf16(dz - hi), so that dz W_r^T ~ hi Whi + lo Whi + hi Wlo and
@@ -318,7 +363,7 @@ template <typename Elt>
 struct RouterBwd {
     const Elt *h, *dy;
     const float *W_r, *b_r, *b2;
-    const float *part;  // tensor-core partial logits or null
+    const float *part;  // partial logits [S][T][ldp]
     int S, ldp;
     const int32_t *topk_idx, *slot_of, *counts;
     const float *gates, *dg_part;
@@ -351,36 +396,12 @@ __device__ __forceinline__ void router_token_grad(const RouterBwd<Elt> &a, int64
     float z[RB_MAXEW], p[RB_MAXEW];
 #pragma unroll
     for (int i = 0; i < RB_MAXEW; ++i) z[i] = 0.f;
-    if (a.part) {
+    {
 #pragma unroll
         for (int i = 0; i < RB_MAXEW; ++i) {
             const int e = lane + 32 * i;
             if (e < E)
                 for (int s = 0; s < a.S; ++s) z[i] += a.part[((int64_t)s * a.T + t) * a.ldp + e];
-        }
-    } else {
-        // lanes split d; 8 experts at a time, each partial dot summed over the warp and kept by
-        // the expert's owner lane
-        const Elt *ht = a.h + t * a.d;
-        for (int e0 = 0; e0 < E; e0 += 8) {
-            float pz[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) pz[q] = 0.f;
-            for (int i0 = lane; i0 < a.d; i0 += 32) {
-                const float hv = to_f(ht[i0]);
-                const float *wr = a.W_r + (int64_t)i0 * E + e0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (e0 + q < E) pz[q] = fmaf(hv, __ldg(wr + q), pz[q]);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float v = warp_sum_f(pz[q]);
-                const int e = e0 + q;
-#pragma unroll
-                for (int i = 0; i < RB_MAXEW; ++i)
-                    if (e < E && e == lane + 32 * i) z[i] = v;
-            }
         }
     }
     float zmax = -INFINITY;
@@ -786,7 +807,7 @@ size_t al(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
 
 // Blocks of the router backward (their dz sums make db_r).
-constexpr int RB_BLOCKS_MAX = 512;
+constexpr int RB_BLOCKS_MAX = 4096;
 int router_bwd_blocks(int64_t T) {
     const int64_t b = (T + 7) / 8;
     return (int)(b < RB_BLOCKS_MAX ? (b > 0 ? b : 1) : RB_BLOCKS_MAX);
@@ -794,7 +815,7 @@ int router_bwd_blocks(int64_t T) {
 
 struct BwdLayout {
     size_t gate_r, kseg, seg, A1, A3, Xp, dYp, dHu, dA, Hs, dX, dg_part, db1_part, db2_part, Zp,
-        Wp, dz, dhr, dwr_out, dbr_part, total;
+        Wp, dz, zl, dhr, dwr_out, dbr_part, total;
     int64_t kw;  // padded slot width: roundup64(P) + 64 E >= sum_e roundup64(count_e)
     int K2, n_part;
     int Kp;      // columns of the bf16 pieces of dz and W_r: roundup64(3 E)
@@ -845,6 +866,8 @@ BwdLayout bwd_layout(const moe_config_t &c) {
     L.Zp = off;         off = al(off + (f32 ? 0 : (size_t)c.T * L.Kp * 2));
     L.Wp = off;         off = al(off + (f32 ? 0 : d * L.Kp * 2));
     L.dz = off;         off = al(off + (f32 ? (size_t)c.T * E * 4 : 0));
+    // logits for layers without the tensor-core router
+    L.zl = off;         off = al(off + (router_launches(c) == 3 ? 0 : (size_t)c.T * E * 4));
     L.dhr = off;        off = al(off + (size_t)c.T * d * 4);
     L.dwr_out = off;    off = al(off + (f32 ? 0 : (size_t)L.nsplit * d * L.Nr * 4));
     L.dbr_part = off;   off = al(off + (size_t)router_bwd_blocks(c.T) * E * 4);
@@ -869,9 +892,10 @@ int backward_launches(const moe_config_t &c, bool saved) {
     const bool sw = c.act == MOE_ACT_SWIGLU;
     if (c.dtype == MOE_F32)  // CUDA-core GEMMs; the pre-activations are always recomputed
         return 1 /*prep*/ + (sw ? 2 : 1) /*A1, A3*/ + 1 /*padded gathers*/ + 1 /*dHu*/ +
-               1 /*act*/ + (sw ? 2 : 1) /*dX*/ + (sw ? 3 : 2) /*dW*/ + 1 /*router bwd*/ +
+               1 /*act*/ + (sw ? 2 : 1) /*dX*/ + (sw ? 3 : 2) /*dW*/ + 2 /*logits, router bwd*/ +
                2 /*dz W_r^T, dh*/ + 1 /*h^T dz*/ + 1 /*db_r*/ + (c.has_bias ? 2 : 0);
-    const int router = router_launches(c) == 3 ? 2 : 0;  // the tensor-core logits, recomputed
+    // the logits, recomputed: the tensor-core router's two kernels, or the direct one
+    const int router = router_launches(c) == 3 ? 2 : 1;
     return 2 /*prep, W_r pieces*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
            2 /*padded gathers, dHu*/ + 1 /*act*/ + 1 /*dX*/ + (sw ? 3 : 2) /*dW*/ +
            router + 1 /*router bwd*/ + 2 /*dz W_r^T, dh*/ + 2 /*h^T dz, dW_r and db_r*/ +
@@ -1065,9 +1089,14 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         rb.W_r = W_r;
         rb.b_r = b_r;
         rb.b2 = c.has_bias ? b2 : nullptr;
-        rb.part = nullptr;
-        rb.S = 0;
-        rb.ldp = 0;
+        {
+            const int64_t blocks = c.T < 4 * (int64_t)num_sms() ? c.T : 4 * (int64_t)num_sms();
+            MOE_TRY(launch_pdl(router_logits_direct_kernel<float>, dim3((unsigned)blocks),
+                               dim3(256), 0, s, 1, hf, W_r, c.T, c.d, c.E, F(B.zl)));
+        }
+        rb.part = F(B.zl);
+        rb.S = 1;
+        rb.ldp = c.E;
         rb.topk_idx = idx;
         rb.slot_of = slot_of;
         rb.counts = cnt;
@@ -1186,15 +1215,20 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     rb.W_r = W_r;
     rb.b_r = b_r;
     rb.b2 = c.has_bias ? b2 : nullptr;
-    rb.part = nullptr;
-    rb.S = 0;
-    rb.ldp = 0;
     if (router_launches(c) == 3) {
         void *scratch = w + L.router;
         MOE_TRY(launch_router_tc(c, h, W_r, scratch, dev_status, s));
         rb.part = router_tc_logits(scratch, c);
         rb.S = router_tc_splits(c);
         rb.ldp = router_tc_epad(c);
+    } else {
+        const int64_t blocks = c.T < 4 * (int64_t)num_sms() ? c.T : 4 * (int64_t)num_sms();
+        MOE_TRY(launch_pdl(router_logits_direct_kernel<__nv_bfloat16>, dim3((unsigned)blocks),
+                           dim3(256), 0, s, 1, static_cast<const __nv_bfloat16 *>(h), W_r, c.T,
+                           c.d, c.E, fl(B.zl)));
+        rb.part = fl(B.zl);
+        rb.S = 1;
+        rb.ldp = c.E;
     }
     rb.topk_idx = idx;
     rb.slot_of = slot_of;

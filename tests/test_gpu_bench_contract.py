@@ -42,5 +42,5 @@ def test_bench_line_for_the_micro_workload():
     assert b["pre_activations"] == "recomputed"
     assert b["roofline"]["bound"] in ("alu", "hbm") and 0 < b["roofline"]["frac"] < 1
     assert b["value"] == pytest.approx(256 / (b["ms_per_step"] * 1e-3), rel=1e-6)
-    assert b["launches_per_step"] == 15 and b["gpu_launches"] == 15 * 4
+    assert b["launches_per_step"] == 16 and b["gpu_launches"] == 16 * 4
     assert b["train_step"]["ms_per_step"] > 0
