@@ -22,8 +22,9 @@ Each measurement carries:
                tensor peak when the FFN's flops per HBM byte exceed the ridge point, else its
                algorithmic bytes against the measured HBM copy bandwidth (f32 layers: flops
                against the FP32 FFMA rate measured in the same run). The tensor peak is the burst
-               figure unless the timed region ran for a second or more under the power cap
-               (then the sustained figure); `frac_alt` gives the fraction against the other one;
+               figure unless the timed region ran under the power cap for a second or more, or
+               with its median SM clock at most 0.8 of the maximum (then the sustained figure,
+               itself measured under the cap); `frac_alt` gives the fraction against the other;
   cpu_baseline the double-precision oracle on this machine's host cores (rank 0, N = 1 only):
                routing over all T tokens plus the expert MLPs and combine of a token sample,
                extrapolated to T tokens;
@@ -90,10 +91,19 @@ def _peaks() -> dict:
     return dict(bf16=1800.0, bf16_sustained=1400.0, hbm=6400.0, source="fallback")
 
 
-def _tc_peak(peaks: dict, region_s: float, reasons) -> tuple:
-    """(peak, other peak, kind, other kind): the sustained tensor peak for a region of a second
-    or more under the power cap, else the burst peak."""
-    sustained = region_s >= SUSTAINED_REGION_S and "sw_power_cap" in set(reasons or ())
+# ... or a region whose median SM clock sat at or below this fraction of the maximum under the
+# power cap (the sustained peak was measured at 1170 of 2032 MHz).
+SUSTAINED_CLOCK_FRAC = 0.8
+
+
+def _tc_peak(peaks: dict, region_s: float, reasons, clocks: dict | None = None) -> tuple:
+    """(peak, other peak, kind, other kind): the sustained tensor peak for a region that ran under
+    the power cap for a second or more, or with its median SM clock pulled down to at most
+    SUSTAINED_CLOCK_FRAC of the maximum; else the burst peak."""
+    capped = "sw_power_cap" in set(reasons or ())
+    low_clock = bool(clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz") and
+                     clocks["sm_mhz"] <= SUSTAINED_CLOCK_FRAC * clocks["sm_max_mhz"])
+    sustained = capped and (region_s >= SUSTAINED_REGION_S or low_clock)
     if sustained:
         return peaks["bf16_sustained"], peaks["bf16"], "bf16 sustained", "bf16 burst"
     return peaks["bf16"], peaks["bf16_sustained"], "bf16 burst", "bf16 sustained"
@@ -104,7 +114,7 @@ BWD_AUX_WEIGHT, BWD_ZLOSS_WEIGHT = 0.01, 0.001
 
 
 def backward_roofline(w, bwd_ms: float, peaks: dict, region_s: float, reasons,
-                      alu: dict | None = None) -> dict:
+                      alu: dict | None = None, clocks: dict | None = None) -> dict:
     """The backward's roofline entry. Algorithmic flops: the expert GEMMs' data gradients (dX,
     dHact) and weight gradients, twice the forward's; algorithmic bytes: every expert's weights
     read and its weight gradients written once, plus h, dy and dh. The bound is the tensor peak
@@ -114,7 +124,7 @@ def backward_roofline(w, bwd_ms: float, peaks: dict, region_s: float, reasons,
     nbytes = 2 * w.weight_bytes() + 3 * w.T * w.d * es
     sec = bwd_ms * 1e-3
     tflops, gbs = flops / sec / 1e12, nbytes / sec / 1e9
-    tc_peak, tc_alt, kind, alt_kind = _tc_peak(peaks, region_s, reasons)
+    tc_peak, tc_alt, kind, alt_kind = _tc_peak(peaks, region_s, reasons, clocks)
     common = {"algorithmic_flops": flops, "algorithmic_bytes": nbytes,
               "flop_per_byte": flops / nbytes, "region_s": region_s}
     if w.dtype == "f32":  # CUDA-core FFMA against the measured FP32 rate
@@ -135,7 +145,7 @@ def backward_roofline(w, bwd_ms: float, peaks: dict, region_s: float, reasons,
 
 
 def roofline(w, ffn_ms: float, peaks: dict, region_s: float, reasons, alu: dict | None = None,
-             traffic: dict | None = None) -> dict:
+             traffic: dict | None = None, clocks: dict | None = None) -> dict:
     """The expert FFN's roofline entry.
 
     w: the workload (its algorithmic flops and bytes); ffn_ms: the FFN's live duration per step
@@ -149,7 +159,7 @@ def roofline(w, ffn_ms: float, peaks: dict, region_s: float, reasons, alu: dict 
     tflops = flops / (ffn_ms * 1e-3) / 1e12
     gbs = nbytes / (ffn_ms * 1e-3) / 1e9
     intensity = flops / nbytes
-    tc_peak, tc_alt, tc_kind, alt_kind = _tc_peak(peaks, region_s, reasons)
+    tc_peak, tc_alt, tc_kind, alt_kind = _tc_peak(peaks, region_s, reasons, clocks)
     common = {"flop_per_byte": intensity, "launches_per_step": launches,
               "algorithmic_flops_per_launch": flops / launches,
               "algorithmic_bytes_per_launch": nbytes / launches,
@@ -464,7 +474,8 @@ def bench_workload(w, args, peaks, D, B, local, world, alu=None, cpu_budget_s=0.
         "dtype": w.dtype,
         "config": _config(w, world),
         "breakdown_ms": {"expert_ffn": ffn_ms, "router_dispatch_combine_aux": ms - ffn_ms},
-        "roofline": roofline(w, ffn_ms, peaks, region_s, clocks.get("reasons"), alu, traffic),
+        "roofline": roofline(w, ffn_ms, peaks, region_s, clocks.get("reasons"), alu, traffic,
+                             clocks),
         "e2e": {"value": D.job_tokens_per_s(T, world, e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * d * inputs["h"].element_size(),
                 "d2h_bytes_per_step": T * d * layer.y.element_size() + 4},
@@ -528,7 +539,7 @@ def bench_backward(w, args, layer, h, stream, peaks, D, B, local, timed, alu=Non
             "pre_activations": "recomputed" if f32 else "saved by the forward",
             "aux_weight": BWD_AUX_WEIGHT, "zloss_weight": BWD_ZLOSS_WEIGHT,
             "roofline": backward_roofline(w, ms, peaks, ms * args.steps * 1e-3,
-                                          clocks.get("reasons"), alu),
+                                          clocks.get("reasons"), alu, clocks),
             "gpu_launches": launches * args.steps, "launches_per_step": launches,
             "train_step": {"value": D.job_tokens_per_s(w.T, world, t_ms), "unit": "tokens/s",
                            "ms_per_step": t_ms,

@@ -96,3 +96,22 @@ def test_backward_roofline_counts_twice_the_forward_flops():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(5000.0, rel=1e-9)
     assert r["frac"] == pytest.approx(5000.0 / PEAKS["hbm"], rel=1e-9)
+
+
+def test_power_capped_region_with_low_clocks_uses_the_sustained_peak():
+    """A region shorter than a second but running under the power cap with its median SM clock at
+    most 0.8 of the maximum is in the regime the sustained peak was measured in; with the clock
+    near its maximum the burst peak stays."""
+    w = wl.WORKLOADS["mixtral"]
+    low = {"sm_mhz": 1218.5, "sm_max_mhz": 2032.0}
+    r = bench.roofline(w, _ffn_ms(w, 1289.0), PEAKS, region_s=0.94, reasons=["sw_power_cap"],
+                       clocks=low)
+    assert r["peak"] == PEAKS["bf16_sustained"] and "sustained" in r["peak_kind"]
+    assert r["frac_alt"] == pytest.approx(1289.0 / PEAKS["bf16"], rel=1e-6)
+    high = {"sm_mhz": 1961.0, "sm_max_mhz": 2032.0}
+    r = bench.roofline(w, _ffn_ms(w, 1289.0), PEAKS, region_s=0.94, reasons=["sw_power_cap"],
+                       clocks=high)
+    assert r["peak"] == PEAKS["bf16"]
+    # low clocks without the power cap (a lock left by someone else) are not the sustained regime
+    r = bench.roofline(w, _ffn_ms(w, 1289.0), PEAKS, region_s=0.94, reasons=[], clocks=low)
+    assert r["peak"] == PEAKS["bf16"]
