@@ -1053,27 +1053,22 @@ constexpr int KG_PAIR_MIN_K = 512;
 
 // K-grouped GEMM: out[e M + m, n] = sum over k in [kseg[e], kseg[e+1]) of A(m, k) B(n, k) for
 // every expert e (zeros where the segment is empty); kseg [E+1] device int32, multiples of 64.
-// mn = 0: A [M, kwidth] and B [N, kwidth] K-major (zero pad columns); mn = 1: A [kwidth, M] and
-// B [kwidth, N] MN-major with row strides lda and ldb (zero pad rows). out [E M, N]; all bf16.
+// A [kwidth, M] and B [kwidth, N] MN-major (the K index is the row) with row strides lda and
+// ldb, zero pad rows; rows at or past map_rows (when > 0) read as zeros. out [E M, N] bf16, or
+// out_f32 [E M, N] f32.
 cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, int E, int M, int N,
                            int64_t kwidth, void *out, uint32_t *dev_status, cudaStream_t s,
-                           int mn, int64_t lda, int64_t ldb, int64_t map_rows = 0,
+                           int64_t lda, int64_t ldb, int64_t map_rows = 0,
                            float *out_f32 = nullptr) {
     if (E <= 0 || M <= 0 || N <= 0 || kwidth <= 0 || kwidth % BK != 0 || kwidth >= (1ll << 31))
         return cudaErrorInvalidValue;
     if (out_f32) out = out_f32;  // the store map only has to encode
     CUtensorMap mA, mB, mO;
-    if (mn) {
-        // rows of A and B past map_rows (<= kwidth) read as zeros
-        const int64_t rows = map_rows > 0 ? map_rows : kwidth;
-        if (M % 64 != 0 || N % 64 != 0 || lda < M || ldb < N || rows > kwidth)
-            return cudaErrorInvalidValue;
-        if (!make_map_ld(&mA, A, rows, M, lda, 64)) return cudaErrorInvalidValue;
-        if (!make_map_ld(&mB, B, rows, N, ldb, 64)) return cudaErrorInvalidValue;
-    } else {
-        if (!make_map(&mA, A, M, kwidth, BM)) return cudaErrorInvalidValue;
-        if (!make_map(&mB, B, N, kwidth, BN / 2)) return cudaErrorInvalidValue;
-    }
+    const int64_t rows = map_rows > 0 ? map_rows : kwidth;
+    if (M % 64 != 0 || N % 64 != 0 || lda < M || ldb < N || rows > kwidth)
+        return cudaErrorInvalidValue;
+    if (!make_map_ld(&mA, A, rows, M, lda, 64)) return cudaErrorInvalidValue;
+    if (!make_map_ld(&mB, B, rows, N, ldb, 64)) return cudaErrorInvalidValue;
     if (!make_store_map(&mO, out, (int64_t)E * M, N)) return cudaErrorInvalidValue;
     TcArgs a = {};
     a.offsets = kseg;
@@ -1097,12 +1092,12 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     a.M = M;
     a.m_tiles = (M + BM - 1) / BM;
     a.pre1 = a.pre3 = nullptr;
-    a.b_mn = a.a_mn = mn;
+    a.b_mn = a.a_mn = 1;
     a.b_ksplit = a.b_krows = 0;
     const int64_t units = (int64_t)E * a.m_tiles * a.n_tiles;
     if (units >= (1ll << 31)) return cudaErrorInvalidValue;
     const int clusters = pair_clusters();
-    if (mn && clusters > 0 && kwidth >= (int64_t)KG_PAIR_MIN_K * E) {
+    if (clusters > 0 && kwidth >= (int64_t)KG_PAIR_MIN_K * E) {
         // 256 x 256 tiles on CTA pairs (each CTA loads half of A and half of B), when the groups
         // average KG_PAIR_MIN_K rows of K: with shorter sums the pair's per-tile handshake costs
         // more than its halved operand traffic saves
@@ -1116,17 +1111,10 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
     }
     int64_t grid = num_sms();
     if (grid > units) grid = units;
-    if (mn) {
-        cudaError_t err =
-            set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, true>, TC_SMEM);
-        if (err != cudaSuccess) return err;
-        return launch_pdl(grouped_gemm_tc_kernel<true, true>, dim3((unsigned)grid),
-                          dim3(TC_THREADS), TC_SMEM, s, 1, mA, mB, mB, mO, a);
-    }
     cudaError_t err =
-        set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, false>, TC_SMEM);
+        set_max_dynamic_smem((const void *)grouped_gemm_tc_kernel<true, true>, TC_SMEM);
     if (err != cudaSuccess) return err;
-    return launch_pdl(grouped_gemm_tc_kernel<true, false>, dim3((unsigned)grid), dim3(TC_THREADS),
+    return launch_pdl(grouped_gemm_tc_kernel<true, true>, dim3((unsigned)grid), dim3(TC_THREADS),
                       TC_SMEM, s, 1, mA, mB, mB, mO, a);
 }
 
@@ -1153,17 +1141,11 @@ cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, i
                        b_krows);
 }
 
-cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,
-                               int N, int64_t kwidth, void *out, uint32_t *dev_status,
-                               cudaStream_t s) {
-    return launch_gemm_kg(A, B, kseg, E, M, N, kwidth, out, dev_status, s, 0, 0, 0);
-}
-
 cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,
                                   const int32_t *kseg, int E, int M, int N, int64_t rows,
                                   void *out, uint32_t *dev_status, cudaStream_t s,
                                   int64_t map_rows, float *out_f32) {
-    return launch_gemm_kg(A, B, kseg, E, M, N, rows, out, dev_status, s, 1, lda, ldb, map_rows,
+    return launch_gemm_kg(A, B, kseg, E, M, N, rows, out, dev_status, s, lda, ldb, map_rows,
                           out_f32);
 }
 

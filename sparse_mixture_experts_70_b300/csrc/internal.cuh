@@ -229,15 +229,10 @@ cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, i
                                  int b_ksplit, int64_t P, int E, int K, int N,
                                  const int32_t *offsets, void *out, uint32_t *dev_status,
                                  cudaStream_t s);
-// K-grouped tensor-core GEMM (weight gradients): out[e M + m, n] = sum_{k in [kseg[e],
-// kseg[e+1])} A[m, k] B[n, k]; A [M, kwidth], B [N, kwidth] bf16 with zero pad columns; kseg
-// device int32 [E+1], multiples of 64. Empty segments give zero tiles.
-cudaError_t launch_gemm_kgroup(const void *A, const void *B, const int32_t *kseg, int E, int M,
-                               int N, int64_t kwidth, void *out, uint32_t *dev_status,
-                               cudaStream_t s);
-// The same over MN-major operands in the padded row layout: A [rows, M] with row stride lda and
-// B [rows, N] with row stride ldb (bf16; the K index is the row, expert e's rows
-// [kseg[e], kseg[e+1]) with zero pad rows).
+// K-grouped tensor-core GEMM (weight gradients): out[e M + m, n] = sum over the rows k in
+// [kseg[e], kseg[e+1]) of A[k, m] B[k, n], both operands MN-major in the padded row layout:
+// A [rows, M] with row stride lda and B [rows, N] with row stride ldb (bf16, zero pad rows);
+// kseg device int32 [E+1], multiples of 64. Empty segments give zero tiles.
 // map_rows > 0: rows of A and B at or past map_rows read as zeros (K extent `rows` rounded up
 // past the data); out_f32 (may be null): f32 output [E M, N] instead of the bf16 out.
 cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,

@@ -52,11 +52,14 @@ def test_backward_full_size_sampled(name):
     assert len(differ) <= max(2, w.T // 1000)
 
     rng = np.random.default_rng(w.seed)
-    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 4, replace=False)]))
+    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 10, replace=False)]))
     counts = np.bincount(idx.ravel(), minlength=w.E)
     hit = np.nonzero(counts)[0]
+    # the first and last experts with slots and a random one; two hidden units each (the first /
+    # last unit of an N tile, and a random one), so every operand's edge and interior are read
     experts = [hit[0], hit[-1], rng.choice(hit)]
-    cols = [(int(e), int(n)) for e, n in zip(experts, [0, w.f - 1, int(rng.integers(w.f))])]
+    units = [0, w.f - 1, 255 % w.f, 256 % w.f, int(rng.integers(w.f)), int(rng.integers(w.f))]
+    cols = [(int(e), int(units[2 * i + j])) for i, e in enumerate(experts) for j in range(2)]
     ref = oracle.backward_sampled(inputs["h"], inputs["W_r"], inputs.get("b_r"), inputs["W1"],
                                   inputs.get("W3"), inputs["W2"], inputs.get("b1"),
                                   inputs.get("b2"), idx, dy, oracle.act_code(w),
