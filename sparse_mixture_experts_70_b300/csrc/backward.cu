@@ -26,7 +26,9 @@
 // roundup64(count_e) and zero pad rows. Every GEMM reads its operands in their stored layouts:
 // the data-gradient GEMMs take W2, W1 and W3 as MN-major B operands, and the weight-gradient
 // GEMMs, which contract over each expert's slots (the rows), take both operands MN-major in
-// 64-row K blocks that never straddle two experts.
+// 64-row K blocks that never straddle two experts. The router's two contractions (dz W_r^T,
+// h^T dz) run on the tensor cores with dz and W_r split into hi + lo bf16 pieces. f32 layers take
+// the same steps with every product on the CUDA cores (gemm_f32_kernel).
 #include <nvtx3/nvToolsExt.h>
 
 #include "internal.cuh"
@@ -37,7 +39,7 @@ namespace moe {
 
 namespace {
 
-constexpr int BT = 64;  // tile edge of the transposing kernels
+constexpr int BT = 64;  // rows per padded segment block and tile edge of the element-wise kernels
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -221,3 +221,33 @@ def test_f32_backward_matches_oracle(w, opts, aux_w, z_w):
     dy = torch.randn((w.T, w.d), generator=g)
     got, idx = _run(w, inputs, dy, aux_w, z_w)
     _compare(got, _oracle(w, inputs, idx, dy, aux_w, z_w), bound=F32_REL_L2)
+
+
+def test_backward_reads_the_routing_from_the_workspace():
+    """moe_forward without topk_idx_out / counts_out keeps them in its workspace; moe_backward
+    with NULL for both reads them there and gives the Layer path's bits."""
+    w = wl.small("bwd_ws_routing", T=400, d=128, f=256, E=8, k=2, router_bias_var=0.5, seed=34)
+    inputs = _case(w)
+    dev = to_dev(inputs)
+    cfg = B.config_for(w)
+    dy = _dy(w, 9).cuda()
+    layer = B.Layer(cfg, dev)
+    layer.forward(dev["h"])
+    want = {k: (v.clone() if v is not None else None)
+            for k, v in layer.backward(dev["h"], dy, 0.1, 0.1).items()}
+    ws = B.workspace(cfg)
+    bws = torch.empty(B.moe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(layer.y)
+    aux = torch.zeros(1, dtype=torch.float32, device="cuda")
+    zl = torch.zeros(1, dtype=torch.float32, device="cuda")
+    B.moe_forward(cfg, dev["h"], dev["W_r"], dev.get("b_r"), dev["W1"], None, dev.get("W3"),
+                  dev["W2"], None, y, aux, None, None, ws, zloss_out=zl)
+    got = {k: (torch.empty_like(v) if v is not None else None) for k, v in want.items()}
+    B.moe_backward(cfg, dev["h"], dev["W_r"], dev.get("b_r"), dev["W1"], None, dev.get("W3"),
+                   dev["W2"], None, None, None, dy, 0.1, 0.1, got["dh"], got["dW_r"], got["db_r"],
+                   got["dW1"], None, got["dW3"], got["dW2"], None, ws, bws)
+    torch.cuda.synchronize()
+    assert B.moe_device_status(ws) == B.MOE_OK
+    for k, v in want.items():
+        if v is not None:
+            assert torch.equal(v, got[k]), k
