@@ -31,6 +31,8 @@
 // the same steps with every product on the CUDA cores (gemm_f32_kernel).
 #include <nvtx3/nvToolsExt.h>
 
+#include <type_traits>
+
 #include "internal.cuh"
 #include "moe_backward.h"
 #include "tc_ptx.cuh"
@@ -219,9 +221,13 @@ struct ActBwd {
     int E, f, swiglu;
 };
 
+// FAST: the special-function unit's tanh and exp (the forward's GELU and SiLU use the same), for
+// bf16 layers; f32 layers keep the accurate library functions.
+template <bool FAST>
 __device__ __forceinline__ float gelu_tanh_acc(float x, float &slope) {
     const float c = 0.7978845608028654f;
-    const float th = tanhf(c * (x + 0.044715f * x * x * x));
+    const float u = c * (x + 0.044715f * x * x * x);
+    const float th = FAST ? tc::tanh_approx(u) : tanhf(u);
     slope = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * c * (1.f + 3.f * 0.044715f * x * x);
     return 0.5f * x * (1.f + th);
 }
@@ -261,18 +267,20 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd<Elt> a, uint3
             load8(a.dHu + (int64_t)(c0 + jr) * a.f + n0 + ch * 8, du);
             if (a.swiglu) load8(a.A3 + off, x3);
             const float g = a.gate_r[r];
+            constexpr bool FAST = !std::is_same<Elt, float>::value;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 float hv;
                 if (a.swiglu) {
-                    const float sg = 1.f / (1.f + expf(-x1[q]));
+                    const float sg = FAST ? __fdividef(1.f, 1.f + __expf(-x1[q]))
+                                          : 1.f / (1.f + expf(-x1[q]));
                     const float si = x1[q] * sg;
                     hv = si * x3[q];
                     d1[q] = g * du[q] * x3[q] * sg * (1.f + x1[q] * (1.f - sg));
                     d3[q] = g * du[q] * si;
                 } else {
                     float slope;
-                    hv = gelu_tanh_acc(x1[q], slope);
+                    hv = gelu_tanh_acc<FAST>(x1[q], slope);
                     d1[q] = g * du[q] * slope;
                     d3[q] = 0.f;
                 }
