@@ -2,7 +2,7 @@
  * moe_oracle.c -- TEST INFRASTRUCTURE, not product code.
  *
  * A plain, slow, obviously correct CPU statement of the forward pass of one top-k routed
- * mixture-of-experts FFN layer, in double precision. Only the tests, the smoke check and the
+ * mixture-of-experts FFN layer, and of its backward pass, in double precision. Only the tests, the smoke check and the
  * benchmark's CPU-baseline leg may load it; the CUDA library never links, calls or includes it,
  * and it shares no code, header or table with the CUDA library.
  *
@@ -53,8 +53,9 @@
  * Precision: inputs are read exactly as stored (f32, or bf16 widened bit-exactly) and every sum,
  * product and transcendental is taken in double, in index order, with no intermediate rounding.
  *
- * Every function below is pinned by tests/test_oracle_pins.py against the pages' printed values,
- * closed forms, brute force or an independent library computation.
+ * Every forward function below is pinned by tests/test_oracle_pins.py against the pages' printed
+ * values, closed forms, brute force or an independent library computation; the backward by
+ * tests/test_oracle_backward_pins.py against finite differences of these forward functions.
  */
 #include <math.h>
 #include <stdint.h>
