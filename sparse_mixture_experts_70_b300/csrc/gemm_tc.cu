@@ -957,14 +957,27 @@ int pair_clusters() {
     return cache[dev].load(std::memory_order_relaxed);
 }
 
-// A_rows / A_src_rows: fused gather of A (see TcArgs); out_token / out_gate: fused scatter.
+// The optional parts of a row-grouped GEMM launch (all off by default).
+struct GemmOpts {
+    const int32_t *A_rows = nullptr;  // fused gather: A row r is row A_rows[r] of [A_src_rows, K]
+    int64_t A_src_rows = 0;
+    const int32_t *out_token = nullptr;  // fused scatter (top-1 GEMM2): row r to out[out_token[r]]
+    const float *out_gate = nullptr;     //   scaled by out_gate[out_token[r]]
+    void *pre1 = nullptr, *pre3 = nullptr;  // training forward: GEMM1's pre-activations
+    int b_mn = 0, b_ksplit = 0, b_krows = 0;  // MN-major B (see TcArgs)
+    float *out_f32 = nullptr;                 // f32 output instead of out
+};
+
 cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P, int E, int K,
                         int N, int epi, const int32_t *offsets, const float *bias, void *out,
                         uint32_t *dev_status, const FaultHook &hook, cudaStream_t s,
-                        const int32_t *A_rows = nullptr, int64_t A_src_rows = 0,
-                        const int32_t *out_token = nullptr, const float *out_gate = nullptr,
-                        void *pre1 = nullptr, void *pre3 = nullptr, int b_mn = 0,
-                        int b_ksplit = 0, int b_krows = 0, float *out_f32 = nullptr) {
+                        const GemmOpts &o = GemmOpts()) {
+    const int32_t *A_rows = o.A_rows, *out_token = o.out_token;
+    const int64_t A_src_rows = o.A_src_rows;
+    const float *out_gate = o.out_gate;
+    void *pre1 = o.pre1, *pre3 = o.pre3;
+    const int b_mn = o.b_mn, b_ksplit = o.b_ksplit, b_krows = o.b_krows;
+    float *out_f32 = o.out_f32;
     if (out_f32 && (epi != EPI_STORE || out_token)) return cudaErrorInvalidValue;
     // the f32 output leaves through per-thread stores; the store map only has to encode
     if (out_f32) out = out_f32;
@@ -1125,8 +1138,11 @@ cudaError_t launch_gemm_rows(const void *A, const int32_t *A_rows, int64_t A_src
                              const int32_t *offsets, const float *bias, void *out,
                              uint32_t *dev_status, cudaStream_t s) {
     if (P == 0) return cudaSuccess;
+    GemmOpts o;
+    o.A_rows = A_rows;
+    o.A_src_rows = A_rows ? A_src_rows : 0;
     return launch_gemm(A, B, nullptr, P, E, K, N, EPI_STORE, offsets, bias, out, dev_status,
-                       FaultHook(), s, A_rows, A_rows ? A_src_rows : 0);
+                       FaultHook(), s, o);
 }
 
 cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, int b_krows,
@@ -1136,9 +1152,12 @@ cudaError_t launch_gemm_rows_bmn(const void *A, const void *B, const void *B3, i
     if (P == 0) return cudaSuccess;
     if (K != (b_ksplit > 0 ? 2 * b_krows : b_krows) || (b_ksplit > 0 && b_ksplit * BK != b_krows))
         return cudaErrorInvalidValue;
+    GemmOpts o;
+    o.b_mn = 1;
+    o.b_ksplit = b_ksplit;
+    o.b_krows = b_krows;
     return launch_gemm(A, B, B3, P, E, K, N, EPI_STORE, offsets, nullptr, out, dev_status,
-                       FaultHook(), s, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 1, b_ksplit,
-                       b_krows);
+                       FaultHook(), s, o);
 }
 
 cudaError_t launch_gemm_kgroup_mn(const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -1153,9 +1172,10 @@ cudaError_t launch_gemm_rows_f32(const void *A, const void *B, int64_t P, int E,
                                  const int32_t *offsets, float *out, uint32_t *dev_status,
                                  cudaStream_t s) {
     if (P == 0) return cudaSuccess;
+    GemmOpts o;
+    o.out_f32 = out;
     return launch_gemm(A, B, nullptr, P, E, K, N, EPI_STORE, offsets, nullptr, nullptr, dev_status,
-                       FaultHook(), s, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0, 0, 0,
-                       out);
+                       FaultHook(), s, o);
 }
 
 cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t s,
@@ -1167,16 +1187,21 @@ cudaError_t launch_ffn_tc(const moe_config_t &c, const FfnBufs &b, cudaStream_t 
     const bool scatter = b.scatter_y != nullptr;
     if ((gather || scatter) && (b.sorted_token == nullptr || (scatter && b.gates == nullptr)))
         return cudaErrorInvalidValue;
+    GemmOpts o1;
+    o1.A_rows = gather ? b.sorted_token : nullptr;
+    o1.A_src_rows = gather ? c.T : 0;
+    o1.pre1 = b.pre1;
+    o1.pre3 = swiglu ? b.pre3 : nullptr;
     cudaError_t err = launch_gemm(gather ? b.gather_h : b.x_perm, b.W1, b.W3, P, c.E, c.d, c.f,
                                   swiglu ? EPI_SWIGLU : EPI_GELU, b.offsets,
-                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, hook, s,
-                                  gather ? b.sorted_token : nullptr, c.T, nullptr, nullptr,
-                                  b.pre1, swiglu ? b.pre3 : nullptr);
+                                  c.has_bias ? b.b1 : nullptr, b.H, b.dev_status, hook, s, o1);
     if (err != cudaSuccess) return err;
+    GemmOpts o2;
+    o2.out_token = scatter ? b.sorted_token : nullptr;
+    o2.out_gate = scatter ? b.gates : nullptr;
     return launch_gemm(b.H, b.W2, nullptr, P, c.E, c.f, c.d, EPI_STORE, b.offsets,
                        c.has_bias ? b.b2 : nullptr, scatter ? b.scatter_y : b.y_perm,
-                       b.dev_status, hook, s, nullptr, 0, scatter ? b.sorted_token : nullptr,
-                       scatter ? b.gates : nullptr);
+                       b.dev_status, hook, s, o2);
 }
 
 }  // namespace moe
