@@ -79,7 +79,7 @@ __device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f(float v) { return v; }
 
-// The expert whose padded segment holds padded column c (kseg in shared memory, E+1 entries).
+// The expert whose padded segment holds padded row c (kseg in shared memory, E+1 entries).
 __device__ __forceinline__ int segment_of(const int32_t *kseg, int E, int c) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -794,8 +794,8 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmF32 a, uint32_t
     pdl_trigger();
 }
 
-// Bias gradients from the per-column-tile sums: out[e][n] = sum over the 64-column tiles of
-// segment e of part[tile][n] (zero for an expert without slots).
+// Bias gradients from the per-tile sums: out[e][n] = sum over the 64-row tiles of expert e's
+// padded segment of part[tile][n], in tile order (zero for an expert without slots).
 __global__ void __launch_bounds__(256) seg_sum_kernel(const float *part, int width,
                                                       const int32_t *kseg, int E, float *out) {
     pdl_wait();
