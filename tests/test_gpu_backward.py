@@ -251,3 +251,38 @@ def test_backward_reads_the_routing_from_the_workspace():
     for k, v in want.items():
         if v is not None:
             assert torch.equal(v, got[k]), k
+
+
+def test_training_step_replays_from_a_cuda_graph():
+    """forward_train + backward recorded once in a CUDA graph (no host synchronisation inside)
+    and replayed: the same bits as the eager calls."""
+    w = wl.small("bwd_graph", T=900, d=256, f=256, E=8, k=2, seed=35)
+    inputs = _case(w)
+    dev = to_dev(inputs)
+    layer = B.Layer(B.config_for(w), dev)
+    dy = _dy(w, 11).cuda()
+    h = dev["h"]
+    layer.forward_train(h)
+    eager = {k: (v.clone() if v is not None else None)
+             for k, v in layer.backward(h, dy, 0.05, 0.02).items()}
+    y_eager = layer.y.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # settles the library's one-time host queries
+        layer.forward_train(h)
+        layer.backward(h, dy, 0.05, 0.02)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward_train(h)
+        layer.backward(h, dy, 0.05, 0.02)
+    for k, v in layer.grads.items():
+        if v is not None:
+            v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert B.moe_device_status(layer.ws) == B.MOE_OK
+    assert torch.equal(layer.y, y_eager)
+    for k, v in eager.items():
+        if v is not None:
+            assert torch.equal(layer.grads[k], v), k
