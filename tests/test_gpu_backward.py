@@ -100,6 +100,10 @@ CASES = [
      0.0, 0.0),
     # experts of at least four row tiles: the data-gradient GEMMs take the CTA-pair kernel
     (wl.small("bwd_pair", T=1100, d=128, f=320, E=2, k=2, seed=29), {}, 0.0, 0.0),
+    # experts of one to six row tiles (skewed routing) on the single-CTA kernels, forward and
+    # data-gradient GEMMs (W2 and W1 / W3 read MN-major)
+    (wl.small("bwd_multi_tile", T=1000, d=256, f=384, E=6, k=2, router_bias_var=1.0,
+              seed=30), {}, 0.05, 0.01),
 ]
 
 

@@ -97,6 +97,14 @@ SMALL = [
              fuse_gather=True),
     wl.small("gather_top1_scatter", T=999, d=128, f=256, E=6, k=1, act=G, gate=wl.GATE_RAW_PROB,
              has_bias=True, router_bias_var=1.0, fuse_gather=True),
+    # experts averaging two to three M tiles on the single-CTA kernel, with skewed routing (one
+    # expert of 27 rows next to experts of three or four tiles): the top-1 GELU layer with
+    # biases and the fused scatter over a ragged last N tile (f = 640), and SwiGLU with ragged
+    # K and N (d = 320)
+    wl.small("multi_tile_gelu_bias_top1", T=900, d=256, f=640, E=4, k=1, act=G,
+             has_bias=True, gate=wl.GATE_RAW_PROB, router_bias_var=2.0, seed=41),
+    wl.small("multi_tile_swiglu_k2", T=700, d=320, f=384, E=4, k=2, router_bias_var=2.0,
+             seed=42),
 ]
 
 
