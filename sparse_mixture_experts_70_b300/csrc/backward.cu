@@ -76,6 +76,30 @@ __device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
     reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
+// 8 elements in their stored form (16 bytes of bf16, 32 of f32): loaded ahead of their use, so
+// that a thread has all its loads in flight before it computes.
+template <typename Elt>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+        u = __ldg(reinterpret_cast<const uint4 *>(p));
+    }
+    __device__ __forceinline__ void get(float (&v)[8]) const { unpack8(u, v); }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float *p) {
+        a = __ldg(reinterpret_cast<const float4 *>(p));
+        b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    __device__ __forceinline__ void get(float (&v)[8]) const {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f(float v) { return v; }
 
@@ -239,7 +263,12 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd<Elt> a, uint3
     pdl_wait();
     for (int e = threadIdx.x; e <= a.E; e += blockDim.x) kseg[e] = a.kseg[e];
     __syncthreads();
-    const int c0 = blockIdx.x * BT;
+    // block b: padded rows [64 (b / (f/64)), +64), features [64 (b % (f/64)), +64) -- the
+    // feature block runs fastest, so the blocks resident at one time cover whole rows (runs of
+    // contiguous memory) rather than a 128-byte piece of every row
+    const int ncb = a.f / BT;
+    const int rb = (int)(blockIdx.x / (unsigned)ncb), cb = (int)(blockIdx.x % (unsigned)ncb);
+    const int c0 = rb * BT;
     if (c0 >= kseg[a.E]) {
         pdl_trigger();
         return;
@@ -252,21 +281,40 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd<Elt> a, uint3
         pdl_trigger();
         return;
     }
-    const int n0 = blockIdx.y * BT;
+    const int n0 = cb * BT;
     const int K2 = a.swiglu ? 2 * a.f : a.f;
-    for (int i = threadIdx.x; i < BT * (BT / 8); i += blockDim.x) {
+    // every thread first issues the loads of its IT vectors of 8, then computes them
+    constexpr int IT = BT * (BT / 8) / 256;
+    static_assert(BT * (BT / 8) % 256 == 0, "the block's vectors of 8 split evenly");
+    Raw8<Elt> ra1[IT], ra3[IT], rdu[IT];
+    float gv[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int i = (int)threadIdx.x + it * 256;
+        const int jr = i >> 3, ch = i & 7;
+        const int r = rbase + jr;
+        if (r < rend) {
+            const int64_t off = (int64_t)r * a.f + n0 + ch * 8;
+            ra1[it].load(a.A1 + off);
+            rdu[it].load(a.dHu + (int64_t)(c0 + jr) * a.f + n0 + ch * 8);
+            if (a.swiglu) ra3[it].load(a.A3 + off);
+            gv[it] = a.gate_r[r];
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int i = (int)threadIdx.x + it * 256;
         const int jr = i >> 3, ch = i & 7;
         const int r = rbase + jr;
         const bool valid = r < rend;
         float d1[8], d3[8], hs[8];
         float dg = 0.f;
         if (valid) {
-            const int64_t off = (int64_t)r * a.f + n0 + ch * 8;
             float x1[8], x3[8], du[8];
-            load8(a.A1 + off, x1);
-            load8(a.dHu + (int64_t)(c0 + jr) * a.f + n0 + ch * 8, du);
-            if (a.swiglu) load8(a.A3 + off, x3);
-            const float g = a.gate_r[r];
+            ra1[it].get(x1);
+            rdu[it].get(du);
+            if (a.swiglu) ra3[it].get(x3);
+            const float g = gv[it];
             constexpr bool FAST = !std::is_same<Elt, float>::value;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -303,14 +351,14 @@ __global__ void __launch_bounds__(256) act_bwd_kernel(const ActBwd<Elt> a, uint3
         dg += __shfl_xor_sync(0xffffffffu, dg, 1);
         dg += __shfl_xor_sync(0xffffffffu, dg, 2);
         dg += __shfl_xor_sync(0xffffffffu, dg, 4);
-        if (valid && ch == 0) a.dg_part[(int64_t)blockIdx.y * a.P + r] = dg;
+        if (valid && ch == 0) a.dg_part[(int64_t)cb * a.P + r] = dg;
     }
     if (a.db1_part) {
         __syncthreads();
         if (threadIdx.x < BT) {
             float sum = 0.f;
             for (int jr = 0; jr < BT; ++jr) sum += s1[jr][threadIdx.x];
-            a.db1_part[(int64_t)blockIdx.x * a.f + n0 + threadIdx.x] = sum;
+            a.db1_part[(int64_t)rb * a.f + n0 + threadIdx.x] = sum;
         }
     }
     pdl_trigger();
@@ -1076,8 +1124,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         ab.E = c.E;
         ab.f = c.f;
         ab.swiglu = sw ? 1 : 0;
-        MOE_TRY(launch_pdl(act_bwd_kernel<float>, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256),
-                           0, s, 1, ab, dev_status));
+        MOE_TRY(launch_pdl(act_bwd_kernel<float>, dim3((unsigned)((B.kw / BT) * (c.f / BT))),
+                           dim3(256), 0, s, 1, ab, dev_status));
         // dX = dA1 W1_e (+ dA3 W3_e) (W1_e [f, d]: B(k = j, n = i) = W1[e][j][i])
         MOE_TRY(gemm(F(B.dA), B.K2, 1, nullptr, 0, W1f, d, 1, f * d, nullptr, F(B.dX), d, 0, kseg,
                      c.E, 0, 0, c.d, c.f, B.kw, 0));
@@ -1203,8 +1251,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     ab.E = c.E;
     ab.f = c.f;
     ab.swiglu = sw ? 1 : 0;
-    MOE_TRY(launch_pdl(act_bwd_kernel<__nv_bfloat16>, dim3((unsigned)(B.kw / BT), c.f / BT), dim3(256), 0, s, 1,
-                       ab, dev_status));
+    MOE_TRY(launch_pdl(act_bwd_kernel<__nv_bfloat16>, dim3((unsigned)((B.kw / BT) * (c.f / BT))),
+                       dim3(256), 0, s, 1, ab, dev_status));
     // 6. dX = dA1 W1_e + dA3 W3_e over the padded rows: one GEMM over K2 = [dA1 | dA3], B = W1
     // then W3 read MN-major
     MOE_TRY(launch_gemm_rows_bmn(bf(B.dA), W1, sw ? W3 : nullptr, c.f, sw ? c.f / BT : 0, B.kw,
