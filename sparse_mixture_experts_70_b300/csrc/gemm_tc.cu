@@ -122,22 +122,40 @@ __device__ __forceinline__ int4 gather_rows(const TcArgs &a, int row0, int rows,
 struct Tile {
     int e, n, row0, rows;  // rows <= 0: nothing to compute (the idle half of a CTA pair)
 };
-// Unit t of the K-grouped schedule: expert-major, then N tile, then M tile; row0 is the output
-// row (e M + m 128), rows the valid rows of the tile.
-// Unit t of the K-grouped schedule of a CTA pair: expert-major, then N tile, then pairs of M tiles,
-// of which CTA `rank` takes the first or the second (rows <= 0: past M, an idle half).
-__device__ __forceinline__ Tile decode_tile_kg_pair(int t, const TcArgs &a, int rank) {
+// Unit t of the K-grouped schedule of a CTA pair: the experts in `order` (longest K segment
+// first, so that the units of long experts do not pile up in the last waves when the experts'
+// row counts are skewed), then N tile, then pairs of M tiles, of which CTA `rank` takes the first
+// or the second (rows <= 0: past M, an idle half).
+__device__ __forceinline__ Tile decode_tile_kg_pair(int t, const TcArgs &a, int rank,
+                                                    const int32_t *order) {
     const int mp_n = (a.m_tiles + 1) / 2;
     const int per = mp_n * a.n_tiles;
     Tile ti;
-    ti.e = t / per;
-    const int local = t - ti.e * per;
+    const int q = t / per;
+    ti.e = order[q];
+    const int local = t - q * per;
     ti.n = local / mp_n;
     const int m = 2 * (local - ti.n * mp_n) + rank;
     ti.row0 = ti.e * a.M + m * BM;
     ti.rows = min(BM, a.M - m * BM);
     return ti;
 }
+// The experts by K segment length (s_off [E+1]), longest first, ties by index: thread-parallel
+// ranks into order [E], the same permutation in every CTA.
+__device__ __forceinline__ void kg_order(const int32_t *s_off, int E, int32_t *order) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int len = s_off[e + 1] - s_off[e];
+        int r = 0;
+        for (int j = 0; j < E; ++j) {
+            const int lj = s_off[j + 1] - s_off[j];
+            r += (lj > len || (lj == len && j < e)) ? 1 : 0;
+        }
+        order[r] = e;
+    }
+}
+// Unit t of the K-grouped schedule of one CTA (experts of a few hundred rows, whose counts vary
+// little: expert order): expert-major, then N tile, then M tile; row0 is the output row
+// (e M + m 128), rows the valid rows of the tile.
 __device__ __forceinline__ Tile decode_tile_kg(int t, const TcArgs &a) {
     const int per = a.m_tiles * a.n_tiles;
     Tile ti;
@@ -654,6 +672,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     volatile int *s_abort = reinterpret_cast<volatile int *>(ctl + 260);
     int32_t *s_cum = reinterpret_cast<int32_t *>(ctl + 512);   // [E+1]
     int32_t *s_off = s_cum + 260;                             // [E+1]
+    int32_t *s_order = s_off + 260;                           // [E] (K-grouped)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();  // offsets and A come from earlier kernels on the stream
@@ -713,6 +732,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (KG) {
+        kg_order(s_off, E, s_order);
+        __syncthreads();
+    }
     cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy completes
     const uint32_t tmem_base = *tmem_slot;
     const int total = s_cum[E];
@@ -727,7 +750,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t phase = 0;
             bool ok = !a.withhold_loads;
             for (int t = unit0; t < total && ok; t += ustep) {
-                const Tile ti = KG ? decode_tile_kg_pair(t, a, rank)
+                const Tile ti = KG ? decode_tile_kg_pair(t, a, rank, s_order)
                                    : decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
                 // this CTA's half of the B tile: SwiGLU W1 (CTA 0) / W3 (CTA 1) rows, else rows
                 // 128 r.. of the 256-row W tile
@@ -852,7 +875,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
                 int nkt = nk;
                 if (KG) {
-                    const Tile ti = decode_tile_kg_pair(t, a, 0);
+                    const Tile ti = decode_tile_kg_pair(t, a, 0, s_order);
                     nkt = (s_off[ti.e + 1] - s_off[ti.e]) / BK;
                 }
                 for (int kb = 0; kb < nkt; ++kb) {
@@ -892,7 +915,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int acc = 0, eh = 0;
         uint32_t aphase = 0;
         for (int t = unit0; t < total; t += ustep) {
-            const Tile ti = KG ? decode_tile_kg_pair(t, a, rank)
+            const Tile ti = KG ? decode_tile_kg_pair(t, a, rank, s_order)
                                : decode_tile<true>(t, eh, s_cum, s_off, a.n_tiles, rank);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, aphase, s_abort, a.dev_status, lim);
@@ -1073,7 +1096,8 @@ cudaError_t launch_gemm_kg(const void *A, const void *B, const int32_t *kseg, in
                            int64_t kwidth, void *out, uint32_t *dev_status, cudaStream_t s,
                            int64_t lda, int64_t ldb, int64_t map_rows = 0,
                            float *out_f32 = nullptr) {
-    if (E <= 0 || M <= 0 || N <= 0 || kwidth <= 0 || kwidth % BK != 0 || kwidth >= (1ll << 31))
+    if (E <= 0 || E > 256 || M <= 0 || N <= 0 || kwidth <= 0 || kwidth % BK != 0 ||
+        kwidth >= (1ll << 31))
         return cudaErrorInvalidValue;
     if (out_f32) out = out_f32;  // the store map only has to encode
     CUtensorMap mA, mB, mO;
