@@ -666,19 +666,37 @@ __global__ void __launch_bounds__(256) dh_kernel(const Elt *dX, const float *dhr
         const float4 r0 = *reinterpret_cast<const float4 *>(dhr + t * d + i0);
         const float4 r1 = *reinterpret_cast<const float4 *>(dhr + t * d + i0 + 4);
         float acc[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        for (int j = 0; j < k; ++j) {
-            const int r = slot_of[t * k + j];
-            if (r < 0) continue;  // dropped by the capacity
-            const int e = idx[t * k + j];
-            const int c = (e >= 0 && e < E) ? kseg[e] + (r - offs[e]) : -1;
-            if (e < 0 || e >= E || r < offs[e] || c >= kseg[e + 1]) {
-                report(dev_status, DEV_ERR_INDEX);
-                continue;
-            }
-            float v[8];
-            load8(dX + (int64_t)c * d + i0, v);
+        // slots in groups of 4: the group's padded rows, then its dX loads, then the sums in
+        // slot order
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            int cr[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] += v[q];
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u;
+                cr[u] = -1;
+                if (j >= k) continue;
+                const int r = slot_of[t * k + j];
+                if (r < 0) continue;  // dropped by the capacity
+                const int e = idx[t * k + j];
+                const int c = (e >= 0 && e < E) ? kseg[e] + (r - offs[e]) : -1;
+                if (e < 0 || e >= E || r < offs[e] || c >= kseg[e + 1]) {
+                    report(dev_status, DEV_ERR_INDEX);
+                    continue;
+                }
+                cr[u] = c;
+            }
+            Raw8<Elt> raw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (cr[u] >= 0) raw[u].load(dX + (int64_t)cr[u] * d + i0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (cr[u] < 0) continue;
+                float v[8];
+                raw[u].get(v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] += v[q];
+            }
         }
         store8(dh + t * d + i0, acc);
     }
