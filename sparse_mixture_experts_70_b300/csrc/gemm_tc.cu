@@ -153,9 +153,9 @@ __device__ __forceinline__ void kg_order(const int32_t *s_off, int E, int32_t *o
         order[r] = e;
     }
 }
-// Unit t of the K-grouped schedule of one CTA (experts of a few hundred rows, whose counts vary
-// little: expert order): expert-major, then N tile, then M tile; row0 is the output row
-// (e M + m 128), rows the valid rows of the tile.
+// Unit t of the K-grouped schedule of one CTA (experts averaging under 512 rows, each unit a few
+// K blocks: the longest-first order measured slower here): expert-major, then N tile, then M
+// tile; row0 is the output row (e M + m 128), rows the valid rows of the tile.
 __device__ __forceinline__ Tile decode_tile_kg(int t, const TcArgs &a) {
     const int per = a.m_tiles * a.n_tiles;
     Tile ti;
