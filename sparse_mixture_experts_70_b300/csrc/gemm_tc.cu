@@ -73,7 +73,8 @@ struct TcArgs {
     unsigned long long spin_limit_ns;  // bound of every mbarrier wait
     int withhold_loads;                // test hook: the producer issues no loads
     int tma_out;  // 1: 32-row groups that lie wholly inside a tile's valid rows leave through
-                  // shared-memory staging and TMA stores (the other rows: per-thread stores)
+                  // shared-memory staging and TMA stores -- 4-row scatters to the rows' tokens
+                  // with out_token -- (the other rows: per-thread stores)
     // fused gather (GEMM1): A row r is row a_rows[r] of a [a_src_rows, K] tensor, read with
     // 4-row TMA gathers, instead of row r of a permuted copy
     const int32_t *a_rows;
@@ -226,10 +227,37 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap *tmO, uint32_t
     }
 }
 
+// The same for the scattering GEMM2: the warp's 32 rows go to output rows tok (one per lane, the
+// lane's token), as eight 4-row scatters of the staged box through the one-row-box map tmO.
+__device__ __forceinline__ void stage_and_scatter(const CUtensorMap *tmO, uint32_t stg,
+                                                  const uint32_t (&pk)[16], int col, int tok,
+                                                  int lane) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+    const uint32_t rowaddr = stg + (uint32_t)lane * 64u;
+    const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(rowaddr + (((uint32_t)j ^ sw) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                     pk[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r0 = __shfl_sync(0xffffffffu, tok, 4 * i);
+        const int r1 = __shfl_sync(0xffffffffu, tok, 4 * i + 1);
+        const int r2 = __shfl_sync(0xffffffffu, tok, 4 * i + 2);
+        const int r3 = __shfl_sync(0xffffffffu, tok, 4 * i + 3);
+        if (lane == 0) tma_scatter4(tmO, stg + (uint32_t)i * 256u, col, r0, r1, r2, r3);
+    }
+    if (lane == 0) bulk_commit();
+}
+
 // Convert this thread's accumulator row (TMEM lane q*32+lane of accumulator `acc_col`) of tile
 // ti into bf16 outputs: half the tile's columns per thread (`half`), bias / GELU / SwiGLU in f32.
 // Every tcgen05.ld here is executed by the whole warp; only the stores depend on the row. A warp
-// whose 32 rows are all valid stores through its staging buffer `stg` with TMA (when a.tma_out).
+// whose 32 rows are all valid stores through its staging buffer `stg` with TMA (when a.tma_out;
+// the scattering GEMM2 as eight 4-row scatters to the rows' tokens).
 // zero: the tile summed nothing (an expert with no slots in K-grouped mode) and stores zeros
 // without reading the accumulator.
 __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, uint32_t tmem_base,
@@ -237,16 +265,26 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
                                               const CUtensorMap *tmO, uint32_t stg,
                                               bool zero = false) {
     const int r = q * 32 + lane;
-    const bool valid = r < ti.rows;
-    const bool boxed = a.tma_out && q * 32 + 32 <= ti.rows;  // warp-uniform
+    bool valid = r < ti.rows;
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc_col;
     __nv_bfloat16 *orow = a.out + (int64_t)(ti.row0 + r) * a.N;
     float gscale = 1.f;
+    int tok = 0;
+    bool tok_ok = true;
     if (a.out_token && valid) {  // fused combine of a top-1 layer: y[token] = g * (H W2^T + b2)
-        const int tok = __ldg(a.out_token + ti.row0 + r);
+        tok = __ldg(a.out_token + ti.row0 + r);
+        tok_ok = tok >= 0 && (int64_t)tok < a.P;  // y has P = T rows
+        if (!tok_ok) {
+            report(a.dev_status, DEV_ERR_INDEX);
+            tok = 0;
+        }
         gscale = __ldg(a.out_gate + tok);
         orow = a.out + (int64_t)tok * a.N;
     }
+    // warp-uniform; a group with a token out of range takes the per-thread path, which skips it
+    const bool boxed = a.tma_out && q * 32 + 32 <= ti.rows &&
+                       (!a.out_token || __all_sync(0xffffffffu, tok_ok));
+    valid = valid && tok_ok;
     if (a.epi == EPI_SWIGLU) {
 #pragma unroll 1
         for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
@@ -317,7 +355,10 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs &a, const Tile &ti, u
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-                stage_and_store(tmO, stg, pk, col, ti.row0 + q * 32, lane);
+                if (a.out_token)
+                    stage_and_scatter(tmO, stg, pk, col, tok, lane);
+                else
+                    stage_and_store(tmO, stg, pk, col, ti.row0 + q * 32, lane);
             } else if (valid) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
 #pragma unroll
@@ -1002,15 +1043,16 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     const int b_mn = o.b_mn, b_ksplit = o.b_ksplit, b_krows = o.b_krows;
     float *out_f32 = o.out_f32;
     if (out_f32 && (epi != EPI_STORE || out_token)) return cudaErrorInvalidValue;
+    if (out_token && epi == EPI_SWIGLU) return cudaErrorInvalidValue;  // the scatter is GEMM2's
     // the f32 output leaves through per-thread stores; the store map only has to encode
     if (out_f32) out = out_f32;
     // every B box is 128 rows: one half of the 256-row B tile; a gathered A reads one-row boxes
     CUtensorMap mA, mB, mB3, mO;
     if (A_rows ? !make_map(&mA, A, A_src_rows, K, 1) : !make_map(&mA, A, P, K, BM))
         return cudaErrorInvalidValue;
-    // the output of the TMA-store epilogue: [P, N] rows in sorted order (the scattering top-1
-    // GEMM2 writes token rows with per-thread stores instead and never reads this map)
-    if (!make_store_map(&mO, out, out_token ? 1 : P, N)) return cudaErrorInvalidValue;
+    // the output of the TMA-store epilogue: [P, N] rows in sorted order, or for the scattering
+    // top-1 GEMM2 the token rows of y [P = T, N], written four rows at a time (one-row boxes)
+    if (!make_store_map(&mO, out, P, N, out_token ? 1 : 32)) return cudaErrorInvalidValue;
     if (b_mn) {
         // B as [E b_krows, N] row-major (rows = K index), read in 64 x 64 boxes; B3 likewise
         if (A_rows || epi != EPI_STORE || b_krows <= 0 || b_krows % BK != 0)
@@ -1037,7 +1079,7 @@ cudaError_t launch_gemm(const void *A, const void *B, const void *B3, int64_t P,
     a.epi = epi;
     a.spin_limit_ns = hook.spin_limit_ns;
     a.withhold_loads = hook.withhold;
-    a.tma_out = (MOE_GEMM_TMA_STORE && out_token == nullptr && out_f32 == nullptr) ? 1 : 0;
+    a.tma_out = (MOE_GEMM_TMA_STORE && out_f32 == nullptr) ? 1 : 0;
     a.out_f32 = out_f32;
     a.a_rows = A_rows;
     a.a_src_rows = A_src_rows;

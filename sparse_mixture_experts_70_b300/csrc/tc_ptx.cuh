@@ -129,6 +129,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  "r"(src), "r"(c0), "r"(c1)
                  : "memory");
 }
+// TMA store of four rows (r0..r3, any order) of a one-row-box tensor map, the box's columns from
+// c0, read from a 4-row tile at src (staged with the map's swizzle, like the rows of a taller box
+// at the same addresses). Bulk-group completion, as tma_store_2d.
+__device__ __forceinline__ void tma_scatter4(const CUtensorMap *map, uint32_t src, int c0, int r0,
+                                             int r1, int r2, int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile::scatter4.bulk_group"
+        " [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -380,12 +391,14 @@ inline bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols
 // 2-D bf16 tensor [rows, cols] written by TMA stores of 32 x 32 boxes staged in shared memory as
 // 32 rows of 64 bytes with the 64-byte swizzle (16-byte chunk j of row r at chunk
 // j ^ ((r >> 1) & 3)), which keeps a warp's row-per-lane staging writes free of bank conflicts.
-inline bool make_store_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols) {
+// box_rows = 1: the map of tma_scatter4 (rows written four at a time, each its own row index).
+inline bool make_store_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
+                           int box_rows = 32) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t box[2] = {32u, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
