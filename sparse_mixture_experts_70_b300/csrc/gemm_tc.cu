@@ -814,7 +814,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             tma_load_2d_pair(sA + stage * A_HALF + q * (A_HALF / 2), &tmA, fb,
                                              ti.row0 - ti.e * a.M + q * 64, kx);
                     } else {
-                        tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK, ti.row0);
+                        // an idle half (past its expert's rows) reads rows past the end of A,
+                        // which TMA fills with zeros: its masked MMA rows then multiply zeros
+                        // (less switching power under the power cap) instead of the next
+                        // expert's rows
+                        tma_load_2d_pair(sA + stage * A_HALF, &tmA, fb, kb * BK,
+                                         ti.rows > 0 ? ti.row0 : (int)a.P);
                     }
                     if (MN && a.b_mn) {
                         // this CTA's 128 columns of B: two 64 x 64 boxes
