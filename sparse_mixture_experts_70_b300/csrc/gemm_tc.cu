@@ -670,8 +670,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // memory once: CTA r holds rows 128r..128r+127 of the A tile and rows 128r..128r+127 of the
 // 256-row B tile, at the same shared-memory offsets, and receives D rows 128r..128r+127 in its
 // own tensor memory. Per SM and per 64-wide k-step that is 32 KiB of TMA writes and operand reads
-// instead of 48 KiB for the single-CTA 128 x 256 tile, whose combined shared-memory traffic caps
-// its tensor pipe near two thirds. The ring therefore holds 6 stages.
+// instead of 48 KiB for the single-CTA 128 x 256 tile, whose tensor pipe measured near two thirds
+// busy on large experts: with the same shared memory the ring holds 6 stages, so more copies are
+// in flight per SM for each flop.
 //   - Both CTAs' producers load their own halves; the copies complete on the first (leader)
 //     CTA's full barrier, which expects the bytes of both (TMA .cta_group::2 lets the barrier
 //     live in the peer CTA).
