@@ -59,9 +59,9 @@ moe_status_t moe_forward_train(const moe_config_t *cfg, const void *h, const flo
 
 /* Gradients of the layer for the upstream gradient dy, after a moe_forward call with the same
  * cfg, inputs and workspace `ws` (the backward reads the routing the forward left there:
- * gates, offsets, sorted_token, slot_of, the permuted rows unless cfg->fuse_gather, and the
- * router's scratch, which a bf16 layer's backward rewrites with the recomputed tensor-core
- * logits).
+ * gates, offsets, sorted_token, slot_of, the permuted rows unless cfg->fuse_gather, and, for a
+ * bf16 layer whose router ran on the tensor cores, the router logits in the router's scratch;
+ * ws must not be used for another forward in between).
  *   h, W_r, b_r, W1, b1, W3, W2, b2   the forward's inputs, same layouts (include/moe.h)
  *   topk_idx [T, k] int32 or NULL     the forward's topk_idx_out if it was given one, else NULL
  *                                     (the copy in ws)

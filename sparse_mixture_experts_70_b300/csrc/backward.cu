@@ -970,8 +970,9 @@ int backward_launches(const moe_config_t &c, bool saved) {
         return 1 /*prep*/ + (sw ? 2 : 1) /*A1, A3*/ + 1 /*padded gathers*/ + 1 /*dHu*/ +
                1 /*act*/ + (sw ? 2 : 1) /*dX*/ + (sw ? 3 : 2) /*dW*/ + 2 /*logits, router bwd*/ +
                2 /*dz W_r^T, dh*/ + 1 /*h^T dz*/ + 1 /*db_r*/ + (c.has_bias ? 2 : 0);
-    // the logits, recomputed: the tensor-core router's two kernels, or the direct one
-    const int router = router_launches(c) == 3 ? 2 : 1;
+    // the logits: the forward's tensor-core partials, still in the router scratch of ws, or the
+    // direct kernel
+    const int router = router_launches(c) == 3 ? 0 : 1;
     return 2 /*prep, W_r pieces*/ + (saved ? 0 : sw ? 2 : 1) /*A1, A3*/ +
            2 /*padded gathers, dHu*/ + 1 /*act*/ + 1 /*dX*/ + (sw ? 3 : 2) /*dW*/ +
            router + 1 /*router bwd*/ + 2 /*dz W_r^T, dh*/ + 2 /*h^T dz, dW_r and db_r*/ +
@@ -1284,7 +1285,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     if (sw)
         MOE_TRY(launch_gemm_kgroup_mn(bf(B.dA) + c.f, B.K2, bf(B.Xp), c.d, ksegc, c.E, c.f, c.d,
                                       B.kw, dW3, dev_status, s));
-    // 9. router: logits (tensor-core partials when the forward used them), dz
+    // 9. router: logits (the forward's tensor-core partials when its router ran on the tensor
+    // cores, else the direct kernel), dz
     RouterBwd<__nv_bfloat16> rb;
     rb.h = static_cast<const __nv_bfloat16 *>(h);
     rb.dy = static_cast<const __nv_bfloat16 *>(dy);
@@ -1292,8 +1294,9 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
     rb.b_r = b_r;
     rb.b2 = c.has_bias ? b2 : nullptr;
     if (router_launches(c) == 3) {
+        // h . W_r without the bias, [S][T][Epad] f32 partials over K chunks, as the forward's
+        // router left them (the same h and W_r, so the same values a recompute would give)
         void *scratch = w + L.router;
-        MOE_TRY(launch_router_tc(c, h, W_r, scratch, dev_status, s));
         rb.part = router_tc_logits(scratch, c);
         rb.S = router_tc_splits(c);
         rb.ldp = router_tc_epad(c);

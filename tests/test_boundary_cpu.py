@@ -178,9 +178,9 @@ def test_router_partial_rows():
         assert 1 <= rows <= w.T
 
 
-@pytest.mark.parametrize("name,saved,expect", [("mixtral", 0, 18), ("mixtral", 1, 16),
-                                               ("switch", 0, 16), ("switch", 1, 15),
-                                               ("decode", 0, 17), ("many_small", 1, 16)])
+@pytest.mark.parametrize("name,saved,expect", [("mixtral", 0, 16), ("mixtral", 1, 14),
+                                               ("switch", 0, 14), ("switch", 1, 13),
+                                               ("decode", 0, 17), ("many_small", 1, 14)])
 def test_backward_launch_count(name, saved, expect):
     cfg = B.config_for(wl.WORKLOADS[name])
     assert B.moe_backward_launch_count(cfg, bool(saved)) == expect
