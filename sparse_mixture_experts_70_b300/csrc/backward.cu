@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(256) wr_pieces_kernel(const float *W_r, int d,
 // cores) plus the k slots' input gradients, where c(t, j) = kseg[e] + slot_of[t k + j] -
 // offsets[e] with e = idx[t k + j] is the slot's padded row (dropped slots contribute nothing).
 // One thread per 8 features of a token.
-template <typename Elt>
+template <typename Elt, int G>
 __global__ void __launch_bounds__(256) dh_kernel(const Elt *dX, const float *dhr,
                                                  const int32_t *slot_of, const int32_t *idx,
                                                  const int32_t *offsets_g, const int32_t *kseg_g,
@@ -666,12 +666,12 @@ __global__ void __launch_bounds__(256) dh_kernel(const Elt *dX, const float *dhr
         const float4 r0 = *reinterpret_cast<const float4 *>(dhr + t * d + i0);
         const float4 r1 = *reinterpret_cast<const float4 *>(dhr + t * d + i0 + 4);
         float acc[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        // slots in groups of 4: the group's padded rows, then its dX loads, then the sums in
-        // slot order
-        for (int j0 = 0; j0 < k; j0 += 4) {
-            int cr[4];
+        // slots in groups of G: the group's padded rows, then its dX loads, then the sums in
+        // slot order (G = 1 for top-1 layers, where grouping only costs registers)
+        for (int j0 = 0; j0 < k; j0 += G) {
+            int cr[G];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < G; ++u) {
                 const int j = j0 + u;
                 cr[u] = -1;
                 if (j >= k) continue;
@@ -685,12 +685,12 @@ __global__ void __launch_bounds__(256) dh_kernel(const Elt *dX, const float *dhr
                 }
                 cr[u] = c;
             }
-            Raw8<Elt> raw[4];
+            Raw8<Elt> raw[G];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < G; ++u)
                 if (cr[u] >= 0) raw[u].load(dX + (int64_t)cr[u] * d + i0);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < G; ++u) {
                 if (cr[u] < 0) continue;
                 float v[8];
                 raw[u].get(v);
@@ -1202,7 +1202,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
             const int64_t n = c.T * (d / 8);
             int64_t blocks = (n + 255) / 256;
             if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
-            MOE_TRY(launch_pdl(dh_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+            const auto dhk = c.k == 1 ? dh_kernel<float, 1> : dh_kernel<float, 4>;
+            MOE_TRY(launch_pdl(dhk, dim3((unsigned)blocks), dim3(256), 0, s, 1,
                                static_cast<const float *>(F(B.dX)),
                                static_cast<const float *>(F(B.dhr)), slot_of, idx, offsets,
                                static_cast<const int32_t *>(kseg), c.T, c.d, c.E, c.k,
@@ -1338,7 +1339,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *h, const float *W
         const int64_t n = c.T * (d / 8);
         int64_t blocks = (n + 255) / 256;
         if (blocks > 8 * (int64_t)num_sms()) blocks = 8 * (int64_t)num_sms();
-        MOE_TRY(launch_pdl(dh_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+        const auto dhk = c.k == 1 ? dh_kernel<__nv_bfloat16, 1> : dh_kernel<__nv_bfloat16, 4>;
+        MOE_TRY(launch_pdl(dhk, dim3((unsigned)blocks), dim3(256), 0, s, 1,
                            static_cast<const __nv_bfloat16 *>(bf(B.dX)),
                            static_cast<const float *>(fl(B.dhr)), slot_of, idx, offsets, ksegc,
                            c.T, c.d, c.E, c.k, static_cast<__nv_bfloat16 *>(dh), dev_status));
